@@ -1,0 +1,177 @@
+"""One decode step on the CPU: token mask, sampler, accept (oracle).
+
+Mask (usetacet.com/docs/grammar, "The guarantee": the automaton masks the
+logits at every step).  Token t is allowed in state s iff walking the bytes of
+t, as model-written symbols, from s never reaches DEAD.  A state inside a
+forced region has no model-symbol transitions, so a token can end on entering
+one (the token that closes ``</calc>``) but never pass through one.  A row with
+a host-forced token gets a mask holding exactly that token (labs.miniml.ai
+"Evaluator aware decoding", "A concrete prototype on llama.cpp").
+
+Sampler ("Sampling runs after masking", usetacet.com/docs/grammar), per row,
+in float64 on the exact logit values x:
+  * no allowed token -> NO_TOKEN;
+  * temperature 0 -> argmax x over allowed tokens, ties to the lowest id;
+  * else z = x / T (T as the binary32 the kernel receives), m = max z,
+    p = exp(z - m) / sum exp(z - m) over allowed tokens;
+    top-p: sort allowed tokens by z descending, take the smallest prefix whose
+    cumulative p reaches top_p, tau = z at its end, nucleus = {z >= tau}
+    (ties at tau included); top_p >= 1 keeps every allowed token;
+    Gumbel-max: tok = argmax over the nucleus of z + g, g = -log(-log u) with
+    u from the Philox stream (oracle.philox), ties to the lowest id.
+  Reported alongside: ``gap`` (best minus second-best Gumbel score in the
+  nucleus) and ``margin`` (distance of top_p from the cumulative mass on
+  either side of the chosen threshold) -- a faithful implementation may differ
+  from this one only where one of them is below its rounding error.
+
+Accept: walk the token's bytes from the row's state (as injected symbols when
+the token was forced); flags DONE (accepting state without successors),
+FORCED_NEXT (the new state continues only with injected bytes), REJECTED
+(DEAD), NO_TOKEN (the row had no token).
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+from .dfa import DEAD, OracleDFA, walk
+from .philox import gumbel, sampler_words, uniform_from_word
+
+NO_TOKEN = 0xFFFFFFFF
+FLAG_DONE = 1
+FLAG_FORCED_NEXT = 2
+FLAG_REJECTED = 4
+FLAG_NO_TOKEN = 8
+
+
+def token_allowed(dfa: OracleDFA, state: int, tok: bytes) -> bool:
+    """The mask bit by its definition (scalar walk)."""
+    return state >= 0 and walk(dfa, state, list(tok)) != DEAD
+
+
+class VocabMatrix:
+    """Tokens as a zero-padded byte matrix, for walking all tokens at once."""
+
+    def __init__(self, tokens: list[bytes]):
+        self.tokens = tokens
+        self.V = len(tokens)
+        self.lens = np.array([len(t) for t in tokens], dtype=np.int64)
+        L = int(self.lens.max())
+        self.mat = np.zeros((self.V, L), dtype=np.int64)
+        for i, t in enumerate(tokens):
+            self.mat[i, :len(t)] = np.frombuffer(t, dtype=np.uint8)
+
+
+def token_mask(dfa: OracleDFA, vm: VocabMatrix, state: int) -> np.ndarray:
+    """Mask of every token from ``state``: the walk of ``token_allowed`` applied
+    to all tokens side by side, one byte position at a time."""
+    alive = vm.lens > 0
+    if state < 0:
+        return np.zeros(vm.V, dtype=bool)
+    st = np.full(vm.V, state, dtype=np.int64)
+    for j in range(vm.mat.shape[1]):
+        act = alive & (vm.lens > j)
+        if not act.any():
+            break
+        nxt = dfa.next[st[act], vm.mat[act, j]]
+        st[act] = np.maximum(nxt, 0)
+        alive[np.flatnonzero(act)[nxt < 0]] = False
+    return alive
+
+
+def pack_bitmask(mask: np.ndarray) -> np.ndarray:
+    """u32 words, bit (t & 31) of word (t >> 5) is token t; pad bits are zero."""
+    V = mask.shape[0]
+    W = (V + 31) // 32
+    padded = np.zeros(W * 32, dtype=np.uint64)
+    padded[:V] = mask.astype(np.uint64)
+    weights = (np.uint64(1) << np.arange(32, dtype=np.uint64))
+    return (padded.reshape(W, 32) * weights).sum(axis=1).astype(np.uint32)
+
+
+def unpack_bitmask(words: np.ndarray, V: int) -> np.ndarray:
+    w = np.asarray(words, dtype=np.uint64)
+    bits = (w[:, None] >> np.arange(32, dtype=np.uint64)) & np.uint64(1)
+    return bits.reshape(-1)[:V].astype(bool)
+
+
+def onehot_mask(V: int, tok: int) -> np.ndarray:
+    m = np.zeros(V, dtype=bool)
+    m[tok] = True
+    return m
+
+
+@dataclass
+class SampleResult:
+    tok: int
+    probs: np.ndarray     # float64 [V]
+    gap: float            # best - second best Gumbel score (inf if unique)
+    margin: float         # top-p threshold margin (inf when no truncation)
+    nucleus_size: int
+
+
+def sample_row(x: np.ndarray, allowed: np.ndarray, temp: float, top_p: float,
+               seed: int, row: int, step: int) -> SampleResult:
+    x = np.asarray(x, dtype=np.float64)
+    V = x.shape[0]
+    idx = np.flatnonzero(allowed)
+    probs = np.zeros(V, dtype=np.float64)
+    if idx.size == 0:
+        return SampleResult(NO_TOKEN, probs, np.inf, np.inf, 0)
+    xa = x[idx]
+    if temp == 0.0:
+        tok = int(idx[np.flatnonzero(xa == xa.max())[0]])
+        probs[tok] = 1.0
+        return SampleResult(tok, probs, np.inf, np.inf, 1)
+    T = float(np.float32(temp))
+    z = xa / T
+    m = z.max()
+    e = np.exp(z - m)
+    p = e / e.sum()
+    probs[idx] = p
+    if float(np.float32(top_p)) >= 1.0:
+        nuc = idx
+        zn = z
+        margin = np.inf
+    else:
+        tp = float(np.float32(top_p))
+        vals, inv = np.unique(z, return_inverse=True)          # ascending distinct z
+        mass = np.bincount(inv.reshape(-1), weights=p)[::-1]    # descending
+        cum = np.cumsum(mass)
+        hit = np.flatnonzero(cum >= tp)
+        j = int(hit[0]) if hit.size else len(cum) - 1
+        tau = vals[::-1][j]
+        keep = z >= tau
+        nuc = idx[keep]
+        zn = z[keep]
+        above = cum[j - 1] if j > 0 else 0.0
+        margin = float(min(cum[j] - tp, tp - above))
+    g = gumbel(uniform_from_word(sampler_words(nuc, row, step, seed)))
+    score = zn + g
+    best = score.max()
+    tok = int(nuc[np.flatnonzero(score == best)[0]])
+    if score.size > 1:
+        second = np.partition(score, -2)[-2]
+        gap = float(best - second)
+    else:
+        gap = np.inf
+    return SampleResult(tok, probs, gap, margin, int(nuc.size))
+
+
+def accept(dfa: OracleDFA, state: int, tok: int, tokens: list[bytes], forced: bool):
+    """Returns (next state, flags)."""
+    if tok == NO_TOKEN:
+        return state, FLAG_NO_TOKEN
+    data = tokens[tok]
+    syms = [b + 256 for b in data] if forced else list(data)
+    ns = walk(dfa, state, syms) if state >= 0 else DEAD
+    if ns < 0:
+        return DEAD, FLAG_REJECTED
+    flags = 0
+    if dfa.accept[ns] and (dfa.next[ns] < 0).all():
+        flags |= FLAG_DONE
+    if (dfa.next[ns, :256] < 0).all() and (dfa.next[ns, 256:] >= 0).any():
+        flags |= FLAG_FORCED_NEXT
+    return ns, flags
