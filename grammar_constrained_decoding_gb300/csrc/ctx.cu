@@ -1,0 +1,202 @@
+// Device context: uploads grammars and vocabulary, owns the mask cache and the
+// device status word, and launches the three step kernels on its stream.
+#include <algorithm>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "cg_internal.h"
+#include "device.cuh"
+
+namespace cgk {
+cudaError_t launch_fill_bitmask(const Tables& t, const uint32_t* states, const uint16_t* gid, const int32_t* forced,
+                                uint32_t B, uint32_t* bitmask, cudaStream_t stream);
+size_t fill_bitmask_smem(uint32_t W);
+cudaError_t launch_mask_and_sample(void* logits, int dtype, uint32_t B, uint32_t V, uint32_t W,
+                                   const uint32_t* bitmask, float temp, float top_p, uint64_t seed, uint32_t step,
+                                   uint32_t* out_tok, float* probs, int inplace, cudaStream_t stream);
+cudaError_t launch_accept(const Tables& t, const uint32_t* states, const uint16_t* gid, const uint32_t* toks,
+                          const int32_t* forced, uint32_t B, uint32_t* counts, uint32_t max_tokens,
+                          uint32_t* out_states, uint8_t* out_flags, cudaStream_t stream);
+}  // namespace cgk
+
+struct cg_ctx {
+  cudaStream_t stream = nullptr;
+  int device = 0;
+  cgk::Tables t{};
+  std::vector<void*> allocations;
+  uint64_t cache_bytes = 0;
+};
+
+namespace {
+
+template <typename T>
+cudaError_t upload(cg_ctx* c, const std::vector<T>& host, T** dev) {
+  *dev = nullptr;
+  size_t bytes = std::max<size_t>(host.size() * sizeof(T), 16);
+  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(dev), bytes);
+  if (e != cudaSuccess) return e;
+  c->allocations.push_back(*dev);
+  if (!host.empty()) e = cudaMemcpyAsync(*dev, host.data(), host.size() * sizeof(T), cudaMemcpyHostToDevice, c->stream);
+  return e;
+}
+
+void release(cg_ctx* c) {
+  for (void* p : c->allocations) cudaFree(p);
+  c->allocations.clear();
+}
+
+}  // namespace
+
+extern "C" {
+
+int cg_ctx_create(const cg_grammar* const* g, uint32_t n_g, const cg_vocab* v, void* cuda_stream, cg_ctx** out) {
+  if (!g || n_g == 0 || n_g > 65535 || !v || !out) return CG_E_ARG;
+  for (uint32_t i = 0; i < n_g; ++i) if (!g[i]) return CG_E_ARG;
+  *out = nullptr;
+  cg_ctx* c = new (std::nothrow) cg_ctx;
+  if (!c) return CG_E_NOMEM;
+  c->stream = static_cast<cudaStream_t>(cuda_stream);
+  cudaGetDevice(&c->device);
+  const uint32_t V = v->V, W = (V + 31) / 32;
+
+  std::vector<cgk::DevGrammar> gdesc(n_g);
+  std::vector<uint32_t> table;
+  std::vector<uint16_t> colmap(size_t(n_g) * 512);
+  std::vector<uint8_t> flags;
+  std::vector<uint32_t> class_of;
+  uint32_t n_classes = 0;
+  uint64_t table_off = 0;
+  uint32_t state_off = 0;
+  try {
+    for (uint32_t i = 0; i < n_g; ++i) {
+      const cg_grammar& gr = *g[i];
+      std::vector<uint32_t> cls, rep;
+      uint32_t nc = cg::mask_classes(gr, v->max_len, cls, rep);
+      gdesc[i] = {table_off, gr.dfa.n_states, gr.n_cols, state_off, 0};
+      table.insert(table.end(), gr.table.begin(), gr.table.end());
+      std::copy(gr.col_of.begin(), gr.col_of.end(), colmap.begin() + size_t(i) * 512);
+      flags.insert(flags.end(), gr.flags.begin(), gr.flags.end());
+      for (uint32_t s = 0; s < gr.dfa.n_states; ++s) class_of.push_back(cls[s] + n_classes);
+      n_classes += nc;
+      table_off += gr.table.size();
+      state_off += gr.dfa.n_states;
+    }
+  } catch (const std::bad_alloc&) {
+    delete c;
+    return CG_E_NOMEM;
+  }
+  cgk::Tables& t = c->t;
+  cudaError_t e = cudaSuccess;
+  uint32_t* d_table;
+  cgk::DevGrammar* d_gd;
+  uint16_t* d_col;
+  uint8_t* d_flags;
+  uint32_t* d_class;
+  uint32_t *d_off, *d_soff, *d_perm;
+  uint8_t *d_bytes, *d_sbytes, *d_lcp;
+  if ((e = upload(c, table, &d_table)) != cudaSuccess || (e = upload(c, gdesc, &d_gd)) != cudaSuccess ||
+      (e = upload(c, colmap, &d_col)) != cudaSuccess || (e = upload(c, flags, &d_flags)) != cudaSuccess ||
+      (e = upload(c, class_of, &d_class)) != cudaSuccess || (e = upload(c, v->off, &d_off)) != cudaSuccess ||
+      (e = upload(c, v->bytes, &d_bytes)) != cudaSuccess || (e = upload(c, v->sorted_off, &d_soff)) != cudaSuccess ||
+      (e = upload(c, v->sorted_bytes, &d_sbytes)) != cudaSuccess || (e = upload(c, v->perm, &d_perm)) != cudaSuccess ||
+      (e = upload(c, v->lcp, &d_lcp)) != cudaSuccess) {
+    release(c);
+    delete c;
+    return CG_E_CUDA;
+  }
+  uint32_t *d_cache = nullptr, *d_cstate = nullptr, *d_status = nullptr;
+  c->cache_bytes = uint64_t(n_classes) * W * 4;
+  if ((e = cudaMalloc(&d_cache, std::max<uint64_t>(c->cache_bytes, 16))) != cudaSuccess) { release(c); delete c; return CG_E_CUDA; }
+  c->allocations.push_back(d_cache);
+  if ((e = cudaMalloc(&d_cstate, size_t(n_classes) * 4 + 16)) != cudaSuccess) { release(c); delete c; return CG_E_CUDA; }
+  c->allocations.push_back(d_cstate);
+  if ((e = cudaMalloc(&d_status, 16)) != cudaSuccess) { release(c); delete c; return CG_E_CUDA; }
+  c->allocations.push_back(d_status);
+  e = cudaMemsetAsync(d_cstate, 0, size_t(n_classes) * 4 + 16, c->stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(d_status, 0, 16, c->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+  if (e == cudaSuccess && cgk::fill_bitmask_smem(W) > 48 * 1024) e = cudaErrorInvalidValue;
+  if (e != cudaSuccess) { release(c); delete c; return e == cudaErrorInvalidValue ? CG_E_LIMIT : CG_E_CUDA; }
+  t.table = d_table;
+  t.grammars = d_gd;
+  t.n_g = n_g;
+  t.colmap = d_col;
+  t.state_flags = d_flags;
+  t.class_of = d_class;
+  t.cache = d_cache;
+  t.cache_state = d_cstate;
+  t.n_classes = n_classes;
+  t.V = V;
+  t.W = W;
+  t.max_len = v->max_len;
+  t.tok_off = d_off;
+  t.tok_bytes = d_bytes;
+  t.sorted_off = d_soff;
+  t.sorted_bytes = d_sbytes;
+  t.perm = d_perm;
+  t.lcp = d_lcp;
+  t.status = d_status;
+  *out = c;
+  return CG_OK;
+}
+
+void cg_ctx_destroy(cg_ctx* c) {
+  if (!c) return;
+  cudaStreamSynchronize(c->stream);
+  release(c);
+  delete c;
+}
+
+int cg_ctx_info(const cg_ctx* c, uint32_t* n_classes, uint64_t* cache_bytes, uint32_t* V, uint32_t* W) {
+  if (!c) return CG_E_ARG;
+  if (n_classes) *n_classes = c->t.n_classes;
+  if (cache_bytes) *cache_bytes = c->cache_bytes;
+  if (V) *V = c->t.V;
+  if (W) *W = c->t.W;
+  return CG_OK;
+}
+
+int cg_ctx_status(cg_ctx* c, uint32_t* dev_code) {
+  if (!c) return CG_E_ARG;
+  uint32_t code = 0;
+  if (cudaStreamSynchronize(c->stream) != cudaSuccess) return CG_E_CUDA;
+  if (cudaMemcpy(&code, c->t.status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return CG_E_CUDA;
+  if (code && cudaMemset(c->t.status, 0, 4) != cudaSuccess) return CG_E_CUDA;
+  if (dev_code) *dev_code = code;
+  return code ? CG_E_DEVICE : CG_OK;
+}
+
+int cg_fill_bitmask(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const int32_t* d_forced, uint32_t B,
+                    uint32_t* d_bitmask) {
+  if (!c || (B && (!d_states || !d_bitmask))) return CG_E_ARG;
+  return cgk::launch_fill_bitmask(c->t, d_states, d_gid, d_forced, B, d_bitmask, c->stream) == cudaSuccess
+             ? CG_OK
+             : CG_E_CUDA;
+}
+
+int cg_mask_and_sample(cg_ctx* c, void* d_logits, int dtype, uint32_t B, uint32_t V, const uint32_t* d_bitmask,
+                       float temp, float top_p, uint64_t seed, uint32_t step, uint32_t* d_out_tok, float* d_probs,
+                       uint32_t flags) {
+  if (!c || (B && (!d_logits || !d_bitmask || !d_out_tok))) return CG_E_ARG;
+  if (dtype != CG_F32 && dtype != CG_BF16) return CG_E_ARG;
+  if (V != c->t.V || !(temp >= 0.f) || temp == INFINITY || !(top_p == top_p)) return CG_E_ARG;
+  if (flags & ~CG_SAMPLE_INPLACE) return CG_E_ARG;
+  return cgk::launch_mask_and_sample(d_logits, dtype, B, V, c->t.W, d_bitmask, temp, top_p, seed, step, d_out_tok,
+                                     d_probs, (flags & CG_SAMPLE_INPLACE) ? 1 : 0, c->stream) == cudaSuccess
+             ? CG_OK
+             : CG_E_CUDA;
+}
+
+int cg_accept(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const uint32_t* d_toks,
+              const int32_t* d_forced, uint32_t B, uint32_t* d_counts, uint32_t max_tokens, uint32_t* d_out_states,
+              uint8_t* d_out_flags) {
+  if (!c || (B && (!d_states || !d_toks || !d_out_states || !d_out_flags))) return CG_E_ARG;
+  if (d_counts && max_tokens == 0) return CG_E_ARG;
+  return cgk::launch_accept(c->t, d_states, d_gid, d_toks, d_forced, B, d_counts, max_tokens, d_out_states,
+                            d_out_flags, c->stream) == cudaSuccess
+             ? CG_OK
+             : CG_E_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,119 @@
+// Device-side views and helpers shared by the step kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/cg.h"
+
+namespace cgk {
+
+struct DevGrammar {
+  uint64_t table_off;   // first element of this grammar's [n_states x n_cols] table
+  uint32_t n_states;
+  uint32_t n_cols;
+  uint32_t state_off;   // first element of this grammar's per-state arrays
+  uint32_t pad;
+};
+
+// Everything the step kernels read, by value (a few pointers and sizes).
+struct Tables {
+  const uint32_t* table;       // next state per (state, column), CG_DEAD for none
+  const DevGrammar* grammars;
+  uint32_t n_g;
+  const uint16_t* colmap;      // [n_g][512] symbol -> column
+  const uint8_t* state_flags;  // CG_STATE_* per state (all grammars)
+  const uint32_t* class_of;    // mask class per state (all grammars, global ids)
+  uint32_t* cache;             // [n_classes][W] allowed-token bitmask per class
+  uint32_t* cache_state;       // per class: 0 empty, 1 being filled, 2 ready
+  uint32_t n_classes;
+  uint32_t V, W, max_len;
+  const uint32_t* tok_off;     // [V+1] token bytes in id order
+  const uint8_t* tok_bytes;
+  const uint32_t* sorted_off;  // [V+1] token bytes in trie (lexicographic) order
+  const uint8_t* sorted_bytes;
+  const uint32_t* perm;        // trie position -> token id
+  const uint8_t* lcp;          // common prefix with the previous trie position
+  uint32_t* status;            // first CG_DEV_* error
+};
+
+__device__ __forceinline__ void record_error(uint32_t* status, uint32_t code) {
+  atomicCAS(status, 0u, code);
+}
+
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of
+// (c0,c1,c2,c3) -> (hi(M1 c2)^c1^k0, lo(M1 c2), hi(M0 c0)^c3^k1, lo(M0 c0))
+// with the key bumped by the Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+__device__ __forceinline__ uint32_t philox_word(uint4 blk, uint32_t lane) {
+  return lane == 0 ? blk.x : lane == 1 ? blk.y : lane == 2 ? blk.z : blk.w;
+}
+
+// u = (2 * (r >> 9) + 1) * 2^-24 (exact in binary32); g = -log(-log u)
+__device__ __forceinline__ float gumbel_from_word(uint32_t r) {
+  const float u = float(2u * (r >> 9) + 1u) * 5.9604644775390625e-08f;
+  return -logf(-logf(u));
+}
+
+// Monotone 32-bit key of a float (larger float <=> larger key); -0 and +0,
+// which compare equal, share the key of +0.
+__device__ __forceinline__ uint32_t fkey(float x) {
+  uint32_t u = __float_as_uint(x);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float fkey_inv(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// (value, id) packed so that the unsigned maximum picks the larger value and,
+// among equal values, the lower id.
+__device__ __forceinline__ unsigned long long pack_best(float v, uint32_t id) {
+  return (static_cast<unsigned long long>(fkey(v)) << 32) | static_cast<unsigned long long>(~id);
+}
+__device__ __forceinline__ uint32_t best_id(unsigned long long p) { return ~static_cast<uint32_t>(p); }
+
+struct MaxOp {
+  template <typename T> __device__ __forceinline__ T operator()(T a, T b) const { return a > b ? a : b; }
+};
+struct SumOp {
+  template <typename T> __device__ __forceinline__ T operator()(T a, T b) const { return a + b; }
+};
+
+// ---- block reductions (blockDim.x a multiple of 32, <= 1024) ----------------
+template <typename T, typename Op>
+__device__ __forceinline__ T warp_reduce(T v, Op op) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// Result is returned to every thread.  `scratch` holds >= 33 elements of T;
+// `identity` is the neutral element of op.
+template <typename T, typename Op>
+__device__ T block_reduce(T v, Op op, T identity, T* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_reduce(v, op);
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    T w = lane < nw ? scratch[lane] : identity;
+    w = warp_reduce(w, op);
+    if (lane == 0) scratch[32] = w;
+  }
+  __syncthreads();
+  return scratch[32];
+}
+
+}  // namespace cgk

@@ -1,0 +1,274 @@
+/*
+ * cg.h -- C ABI of the grammar-constrained decoding library (libcg.so).
+ *
+ * The shape follows the constraint contract of usetacet.com/docs/grammar,
+ * "The guarantee is not tied to this engine": three calls over logits and
+ * u32 token ids that name no model, tokenizer, device or file --
+ *     cg_fill_bitmask    which tokens the grammar allows in each row's state,
+ *     cg_mask_and_sample mask the logits and sample after masking,
+ *     cg_accept          advance each row's automaton by its token --
+ * plus grammar compilation, vocabulary upload, the host-side evaluator of
+ * labs.miniml.ai "Evaluator aware decoding" and a host driver for forced
+ * tokens.
+ *
+ * Conventions
+ *  - Return codes: CG_OK (0) or a negative CG_E_* code; a failing call leaves
+ *    its outputs unspecified and changes no library state.  Argument errors are
+ *    detected on the host before anything is launched.
+ *  - Ownership: pointers named d_* are device pointers owned by the caller;
+ *    h_* and plain pointers are host memory owned by the caller.  Opaque
+ *    objects (cg_grammar, cg_vocab, cg_ctx, cg_driver) are owned by the
+ *    library and released by their *_destroy call.
+ *  - Asynchrony: the three step calls only enqueue kernels on the context's
+ *    CUDA stream and return; results are ready after the stream is
+ *    synchronised.  Errors that only the device can see (a state or token id
+ *    out of range, a forced token the automaton does not allow, ...) are
+ *    recorded in a device status word read by cg_ctx_status().
+ *  - States: each grammar's states are numbered 0..n_states-1 breadth-first
+ *    from the start state 0 (bytes visited in order 0..255 as written by the
+ *    model, then the same bytes as injected by the host).  CG_DEAD marks a
+ *    row whose automaton has failed.
+ *  - Bitmask layout: row-major u32 [B][W], W = ceil(V / 32); token t is bit
+ *    (t & 31) of word (t >> 5); pad bits beyond V are zero.
+ */
+#ifndef CG_H
+#define CG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes -------------------------------------------------------- */
+#define CG_OK                0
+#define CG_E_ARG            -1  /* null pointer, size out of range, mismatched sizes */
+#define CG_E_SYNTAX         -2  /* grammar source does not parse */
+#define CG_E_UNSUPPORTED    -3  /* schema feature outside the supported subset: fail closed
+                                   (dev.to "I found a runner bug...", "What exists beyond
+                                   the experiment") */
+#define CG_E_EMPTY          -4  /* the grammar accepts no string */
+#define CG_E_UNDEFINED_RULE -5  /* a GBNF rule reference has no definition */
+#define CG_E_LIMIT          -6  /* automaton, table or token length beyond a library limit */
+#define CG_E_CUDA           -7  /* a CUDA runtime call failed */
+#define CG_E_DEVICE         -8  /* cg_ctx_status: the device recorded an error */
+#define CG_E_NOMEM          -9  /* host allocation failed */
+
+/* ---- enumerations ---------------------------------------------------------- */
+#define CG_GBNF        0        /* GBNF-style rule text, start rule "root" */
+#define CG_JSON_SCHEMA 1        /* JSON-schema subset */
+
+#define CG_F32  0               /* logits as IEEE binary32 */
+#define CG_BF16 1               /* logits as bfloat16 */
+
+#define CG_DEAD     0xFFFFFFFFu /* failed automaton */
+#define CG_NO_TOKEN 0xFFFFFFFFu /* the row had no allowed token */
+
+/* per-row flags written by cg_accept */
+#define CG_FLAG_DONE        1u  /* new state accepts and has no continuation */
+#define CG_FLAG_FORCED_NEXT 2u  /* new state continues only with host-injected bytes */
+#define CG_FLAG_REJECTED    4u  /* the token was not allowed: state is CG_DEAD */
+#define CG_FLAG_NO_TOKEN    8u  /* the row had no token this step */
+#define CG_FLAG_CAPPED     16u  /* the row hit max_tokens and was reset */
+
+/* state flags exported by cg_grammar_export */
+#define CG_STATE_ACCEPT      1u
+#define CG_STATE_SINK        2u  /* accepting, no outgoing transition */
+#define CG_STATE_FORCED_ONLY 4u  /* only host-injected bytes continue */
+
+/* device status codes reported through cg_ctx_status (first one wins) */
+#define CG_DEV_OK              0
+#define CG_DEV_BAD_STATE       1  /* a state id >= n_states (and not CG_DEAD) */
+#define CG_DEV_BAD_TOKEN       2  /* a token id >= V (and not CG_NO_TOKEN) */
+#define CG_DEV_BAD_FORCED      3  /* a forced token id >= V */
+#define CG_DEV_FORCED_MISMATCH 4  /* accept: the token differs from the forced token */
+#define CG_DEV_MISSING_FORCED  5  /* fill: a forced-only state without a forced token */
+#define CG_DEV_BAD_GID         6  /* a grammar index >= n_grammars */
+#define CG_DEV_REJECTED        7  /* accept: the token walks the automaton to CG_DEAD */
+
+/* mask_and_sample flags */
+#define CG_SAMPLE_INPLACE 1u     /* also write -inf into masked logits (the "&mut [f32]" form) */
+
+typedef struct cg_grammar cg_grammar;
+typedef struct cg_vocab   cg_vocab;
+typedef struct cg_ctx     cg_ctx;
+typedef struct cg_driver  cg_driver;
+
+/* Termination bounds, usetacet.com/docs/grammar "A valid call also has to
+ * end": whitespace runs and open fields are bounded and a generation is
+ * capped at max_tokens. */
+typedef struct {
+    uint32_t ws_max;             /* longest whitespace run in one JSON slot */
+    uint32_t max_len_default;    /* maxLength of a JSON string that states none */
+    uint32_t depth_max;          /* simultaneous activations of one GBNF rule */
+    uint32_t max_items_default;  /* maxItems of a JSON array that states none */
+    uint32_t max_tokens;         /* host cap on one generation (cg_accept with counts) */
+} cg_bounds;
+
+/* ---- grammar ---------------------------------------------------------------- */
+
+/* Compile a grammar to its minimal byte-level automaton (usetacet.com/docs/grammar,
+ * "The guarantee": the automaton masks the logits at every step; nesting is
+ * bounded so the automaton is finite).
+ *  src, src_len : grammar text (GBNF rules or a JSON schema), not NUL-terminated
+ *  kind         : CG_GBNF or CG_JSON_SCHEMA
+ *  bounds       : termination bounds (not retained)
+ *  out          : receives the grammar on CG_OK
+ *  err, errlen  : optional buffer for a NUL-terminated message (may be NULL/0)
+ * Errors: CG_E_ARG, CG_E_SYNTAX, CG_E_UNSUPPORTED, CG_E_EMPTY,
+ * CG_E_UNDEFINED_RULE, CG_E_LIMIT (more than 2^24 states), CG_E_NOMEM. */
+int cg_compile(const char* src, size_t src_len, int kind, const cg_bounds* bounds,
+               cg_grammar** out, char* err, size_t errlen);
+
+void cg_grammar_destroy(cg_grammar* g);
+
+/* n_states: states of the minimal trimmed automaton; n_cols: distinct
+ * transition columns over the 512 symbols; start is always 0.  Any output
+ * pointer may be NULL. */
+int cg_grammar_info(const cg_grammar* g, uint32_t* n_states, uint32_t* n_cols, uint32_t* start);
+
+/* Export the automaton: next[s*512 + a] for symbol a (0..255 model bytes,
+ * 256..511 the same bytes injected by the host), -1 for DEAD; flags[s] is a
+ * CG_STATE_* mask.  Buffers hold n_states*512 int32 and n_states bytes. */
+int cg_grammar_export(const cg_grammar* g, int32_t* next, uint8_t* flags);
+
+/* --try-input (usetacet.com/docs/grammar, "Reading the grammar for a tool"):
+ * run a candidate string from the start state and report where it is refused.
+ *  s, n        : candidate bytes
+ *  injected    : optional per-byte marks (nonzero = byte injected by the host)
+ *  refused_at  : receives the offset of the first refused byte, or n
+ *  end_state   : receives the state after the accepted prefix (may be NULL)
+ *  accepted    : receives 1 if all n bytes are consumed and the state accepts */
+int cg_try_input(const cg_grammar* g, const uint8_t* s, size_t n, const uint8_t* injected,
+                 size_t* refused_at, uint32_t* end_state, int* accepted);
+
+/* States that are neither finished nor forced-only, increasing; a random
+ * start state is live[r mod n].  out may be NULL to query n. */
+int cg_live_states(const cg_grammar* g, uint32_t* out, uint32_t cap, uint32_t* n);
+
+/* ---- vocabulary --------------------------------------------------------------- */
+
+/* Token t is bytes[off[t] .. off[t+1]); V >= 1, every token 1..64 bytes.
+ * The library copies the data.  Errors: CG_E_ARG, CG_E_LIMIT. */
+int cg_vocab_create(const uint8_t* bytes, const uint32_t* off, uint32_t V, cg_vocab** out);
+void cg_vocab_destroy(cg_vocab* v);
+
+/* Greedy longest-match tokenisation of text (lowest id among equal strings),
+ * the forced-token encoding of labs.miniml.ai "Evaluator aware decoding", "The
+ * core idea" step 3.  Writes up to cap ids, n_out receives the count needed;
+ * CG_E_LIMIT if cap is too small, CG_E_ARG if a byte has no token. */
+int cg_tokenize_greedy(const cg_vocab* v, const uint8_t* text, size_t n, uint32_t* out,
+                       size_t cap, size_t* n_out);
+
+/* ---- device context ------------------------------------------------------------ */
+
+/* Upload n_g grammars and one vocabulary to the current CUDA device and bind
+ * the context to cuda_stream (a cudaStream_t; NULL = legacy default stream).
+ * Allocates the transition tables, the trie-ordered vocabulary and the
+ * per-mask-class cache of allowed-token bitmasks (token mask cache,
+ * labs.miniml.ai "Where XGrammar-2 could take this").  Grammars and vocab may
+ * be destroyed afterwards.  Errors: CG_E_ARG, CG_E_CUDA, CG_E_LIMIT, CG_E_NOMEM. */
+int cg_ctx_create(const cg_grammar* const* g, uint32_t n_g, const cg_vocab* v,
+                  void* cuda_stream, cg_ctx** out);
+void cg_ctx_destroy(cg_ctx* c);
+
+/* n_classes: total mask classes (states with identical masks share one);
+ * cache_bytes: device bytes of the mask cache; V, W of the vocabulary. */
+int cg_ctx_info(const cg_ctx* c, uint32_t* n_classes, uint64_t* cache_bytes, uint32_t* V, uint32_t* W);
+
+/* Synchronise the context's stream, return CG_OK or CG_E_DEVICE, and move the
+ * first recorded CG_DEV_* code into *dev_code (may be NULL), clearing it. */
+int cg_ctx_status(cg_ctx* c, uint32_t* dev_code);
+
+/* Step 1 -- which tokens may follow each row's state (usetacet.com/docs/grammar,
+ * "The guarantee"; masks come from pure automaton state ahead of the step,
+ * labs.miniml.ai "Why isn't this in production APIs yet?").
+ *  d_states  : u32 [B] automaton state of each row (CG_DEAD -> empty mask)
+ *  d_gid     : u16 [B] grammar index of each row, or NULL for grammar 0
+ *  d_forced  : i32 [B] token the host forces on the row, -1 for none, or NULL;
+ *              a forced row gets exactly that token
+ *  d_bitmask : u32 [B][W] output
+ * Token t is allowed iff walking its bytes from the state never fails.  Masks
+ * are served from the per-class cache, computed on first use. */
+int cg_fill_bitmask(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid,
+                    const int32_t* d_forced, uint32_t B, uint32_t* d_bitmask);
+
+/* Step 2 -- mask, temperature, softmax, top-p, sample ("Sampling runs after
+ * masking", usetacet.com/docs/grammar).
+ *  d_logits  : [B][V] CG_F32 or CG_BF16 (dtype), row-major, V = the vocab size
+ *  d_bitmask : u32 [B][W] from cg_fill_bitmask
+ *  temp      : 0 -> greedy argmax (ties to the lowest id); > 0 -> z = x / temp
+ *  top_p     : nucleus mass; >= 1 keeps every allowed token
+ *  seed,step : Philox4x32-10 stream; token t of row b uses word t&3 of
+ *              Philox((t>>2, b, step, 0), (seed lo, seed hi))
+ *  d_out_tok : u32 [B] sampled id, CG_NO_TOKEN for a row without allowed tokens
+ *  d_probs   : optional f32 [B][V] softmax over allowed tokens (0 elsewhere;
+ *              greedy rows get 1 at the chosen token), or NULL
+ *  flags     : CG_SAMPLE_INPLACE to also store -inf into masked logits
+ * Sampling is Gumbel-max over the nucleus: argmax z_t + g_t, g = -log(-log u). */
+int cg_mask_and_sample(cg_ctx* c, void* d_logits, int dtype, uint32_t B, uint32_t V,
+                       const uint32_t* d_bitmask, float temp, float top_p, uint64_t seed,
+                       uint32_t step, uint32_t* d_out_tok, float* d_probs, uint32_t flags);
+
+/* Step 3 -- advance each row's automaton by its token ("after injection the
+ * grammar state must be advanced", labs.miniml.ai "Evaluator aware decoding").
+ *  d_states, d_gid : as in cg_fill_bitmask (d_gid may be NULL)
+ *  d_toks          : u32 [B] tokens from cg_mask_and_sample
+ *  d_forced        : i32 [B] or NULL; a row with d_forced >= 0 must carry that
+ *                    token, and its bytes are walked as host-injected bytes
+ *  d_counts        : u32 [B] or NULL; when given, each row's token count is
+ *                    advanced and a row that finishes (CG_FLAG_DONE) or reaches
+ *                    max_tokens is reset to state 0 with count 0
+ *  max_tokens      : the cap used with d_counts (usetacet.com/docs/grammar)
+ *  d_out_states    : u32 [B] new states (may alias d_states)
+ *  d_out_flags     : u8 [B] CG_FLAG_* bits */
+int cg_accept(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const uint32_t* d_toks,
+              const int32_t* d_forced, uint32_t B, uint32_t* d_counts, uint32_t max_tokens,
+              uint32_t* d_out_states, uint8_t* d_out_flags);
+
+/* ---- evaluator-aware host side --------------------------------------------------- */
+
+#define CG_RESULT_CALC_TAG    0  /* <result>V</result> | <result_error>code</result_error> */
+#define CG_RESULT_JSON_ANSWER 1  /* , "answer": V}     | , "answer": null, "error": "code"} */
+
+/* Evaluate an arithmetic span exactly over the rationals (labs.miniml.ai
+ * "Evaluator aware decoding": "17 * 23 + 91 = 482") and format the bytes the
+ * host forces.  Grammar: expr := term (('+'|'-') term)*, term := unary
+ * (('*'|'/') unary)*, unary := '-' unary | primary, primary := NUMBER |
+ * '(' expr ')', NUMBER := [0-9]+('.'[0-9]*)? | '.'[0-9]+, spaces skipped.
+ * Failures format an error code: parse, div_zero, non_integer, overflow (more
+ * than 64 digits).  Writes up to cap bytes; out_len receives the length
+ * (CG_E_LIMIT if cap is too small).  *ok receives 1 for a numeric result. */
+int cg_eval_arith(const uint8_t* span, size_t n, int fmt, uint8_t* out, size_t cap,
+                  size_t* out_len, int* ok);
+
+/* Host driver of forced tokens for B rows (labs.miniml.ai "Evaluator aware
+ * decoding", "The core idea" steps 1-4).  Row b uses grammar rules[gid[b]]:
+ * when a step leaves the row in a forced-only state with nothing queued, the
+ * text between the last span_open and the trailing span_close is evaluated and
+ * its formatted result is tokenised into the row's queue. */
+typedef struct {
+    const uint8_t* span_open;  size_t span_open_len;
+    const uint8_t* span_close; size_t span_close_len;
+    int result_format;         /* CG_RESULT_*, or -1 for a grammar without evaluator */
+} cg_span_rule;
+
+int cg_driver_create(const cg_vocab* v, uint32_t B, const uint16_t* h_gid,
+                     const cg_span_rule* rules, uint32_t n_rules, cg_driver** out);
+void cg_driver_destroy(cg_driver* d);
+
+/* Apply one step's results on the host, in this order per row: a used forced
+ * token leaves the queue; a real token extends the row's text; a row flagged
+ * CG_FLAG_DONE or CG_FLAG_CAPPED forgets its text and queue; otherwise a row
+ * flagged CG_FLAG_FORCED_NEXT with an empty queue is evaluated.  Then writes
+ * the next step's forced token per row (-1 for none) into h_forced_next.
+ *  h_toks, h_flags, h_forced_used : this step's tokens, flags and forced ids
+ *  n_evals : optional, receives the number of evaluations this call made */
+int cg_driver_update(cg_driver* d, const uint32_t* h_toks, const uint8_t* h_flags,
+                     const int32_t* h_forced_used, int32_t* h_forced_next, uint32_t* n_evals);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CG_H */

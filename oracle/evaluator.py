@@ -17,7 +17,8 @@ division by zero as owner decisions); the reading taken here:
 
 Outcomes: an integer result -> its decimal text; otherwise an error code:
 ``parse`` (not in the language), ``div_zero``, ``non_integer`` (result is not
-an integer), ``overflow`` (more than 64 decimal digits).
+an integer), ``overflow`` (more than 64 decimal digits, or a span longer than
+4096 bytes).  The whole span is lexed before it is parsed.
 
 Forced tokenisation: greedy longest match over the vocabulary at each
 position, lowest id among equal strings (every single byte is a token in the
@@ -73,6 +74,9 @@ def _lex(span: bytes):
 
 
 def evaluate(span: bytes) -> int:
+    if len(span) > 4096:
+        # evaluators stay time bounded (same page, "Where XGrammar-2 could take this")
+        raise EvalError('overflow')
     toks = _lex(span)
     pos = 0
 

@@ -413,6 +413,13 @@ def _json_value_literal(v) -> bytes:
     raise GrammarError('unsupported', f'enum/const value of type {type(v).__name__}')
 
 
+def _count(v, what: str) -> int:
+    """A length/count keyword: a non-negative integral JSON number (<= 10**7)."""
+    if isinstance(v, bool) or not isinstance(v, (int, float)) or v != int(v) or not 0 <= v <= 10**7:
+        raise GrammarError('unsupported', f'{what} out of range')
+    return int(v)
+
+
 def schema_to_tree(text: str, ws_max: int, max_len_default: int, max_items_default: int) -> tuple:
     r"""Lower a JSON-schema subset to a tree.
 
@@ -459,6 +466,8 @@ def schema_to_tree(text: str, ws_max: int, max_len_default: int, max_items_defau
             if not vals:
                 raise GrammarError('unsupported', 'empty enum')
             ty = s.get('type')
+            if ty is not None and not isinstance(ty, str):
+                raise GrammarError('unsupported', 'enum value does not match type')
             for v in vals:
                 if isinstance(v, float):
                     raise GrammarError('unsupported', 'non-integer number in enum')
@@ -491,15 +500,18 @@ def schema_to_tree(text: str, ws_max: int, max_len_default: int, max_items_defau
             parts += [ws, lit(b'}')]
             return cat(*parts)
         if ty == 'string':
-            lo = int(s.get('minLength', 0))
+            lo = _count(s.get('minLength', 0), 'minLength')
             if 'maxLength' in s:
-                body = rep(char, lo, int(s['maxLength']))
+                hi = _count(s['maxLength'], 'maxLength')
             elif 'x-maxBytes' in s:
-                body = rep(char, lo, None)
+                hi = None
             else:
-                body = rep(char, lo, max_len_default)
+                hi = max_len_default
+            if hi is not None and hi < lo:
+                raise GrammarError('unsupported', 'maxLength < minLength')
+            body = rep(char, lo, hi)
             if 'x-maxBytes' in s:
-                body = ('and', (body, rep(sym_of(range(256)), 0, int(s['x-maxBytes']))))
+                body = ('and', (body, rep(sym_of(range(256)), 0, _count(s['x-maxBytes'], 'x-maxBytes'))))
             return cat(lit(b'"'), body, lit(b'"'))
         if ty == 'integer':
             return cat(rep(lit(b'-'), 0, 1), alt(lit(b'0'), cat(_DIGIT19, rep(_DIGIT, 0, 18))))
@@ -515,8 +527,8 @@ def schema_to_tree(text: str, ws_max: int, max_len_default: int, max_items_defau
             if 'items' not in s:
                 raise GrammarError('unsupported', 'array without items')
             item = lower(s['items'])
-            lo = int(s.get('minItems', 0))
-            hi = int(s.get('maxItems', max_items_default))
+            lo = _count(s.get('minItems', 0), 'minItems')
+            hi = _count(s.get('maxItems', max_items_default), 'maxItems')
             if hi < lo:
                 raise GrammarError('unsupported', 'maxItems < minItems')
             more = cat(ws, lit(b','), ws, item)

@@ -1,0 +1,175 @@
+"""CPU tests of libcg.so: exported symbols, the grammar compiler against the
+oracle's automata, and the host-side evaluator/tokeniser/driver against the
+oracle.  No device call is made here."""
+
+import ctypes
+import json
+import os
+import random
+import re
+
+import numpy as np
+import pytest
+
+from oracle.dfa import build_dfa
+from oracle.driver import OracleRun, Row
+from oracle.evaluator import format_result, tokenize_greedy
+from oracle.grammar import GrammarError, gbnf_to_tree, schema_to_tree
+from oracle.step import FLAG_DONE, FLAG_FORCED_NEXT
+from tests.oracle_cache import oracle_dfa, vocab
+from tests.test_oracle_grammar import _gbnf, _lang, _rand_tree
+from workloads import GRAMMARS, Bounds as WBounds
+
+gcd = pytest.importorskip("grammar_constrained_decoding_gb300")
+from grammar_constrained_decoding_gb300 import Bounds, Grammar, Vocab, Driver, eval_arith, _lib  # noqa: E402
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "cg.h")
+
+
+def _bounds(b):
+    return Bounds(b.ws_max, b.max_len_default, b.depth_max, b.max_items_default, b.max_tokens)
+
+
+def test_library_exports_every_declared_symbol():
+    text = open(HEADER).read()
+    names = set(re.findall(r"^\s*(?:int|void)\s+(cg_\w+)\s*\(", text, flags=re.M))
+    assert len(names) >= 20
+    lib = ctypes.CDLL(_lib.LIB_PATH)
+    for n in sorted(names):
+        assert hasattr(lib, n), n
+    assert names == set(_lib.SIGNATURES), names ^ set(_lib.SIGNATURES)
+
+
+@pytest.mark.parametrize("name", sorted(GRAMMARS))
+def test_compiler_matches_oracle_tables(name):
+    spec = GRAMMARS[name]
+    g = Grammar.compile(spec.source, spec.kind, _bounds(spec.bounds))
+    nxt, flags = g.export()
+    o = oracle_dfa(name)
+    assert np.array_equal(nxt, o.next)
+    assert np.array_equal((flags & _lib.CG_STATE_ACCEPT) != 0, o.accept)
+    assert np.array_equal((flags & _lib.CG_STATE_SINK) != 0, o.sink())
+    assert np.array_equal((flags & _lib.CG_STATE_FORCED_ONLY) != 0, o.forced_only())
+
+
+def test_compiler_matches_oracle_on_random_grammars():
+    rng = random.Random(99)
+    done = 0
+    while done < 150:
+        t = _rand_tree(rng, 5)
+        src = "root ::= " + _gbnf(t)
+        try:
+            o = build_dfa(gbnf_to_tree(src, 5))
+        except GrammarError:
+            with pytest.raises(_lib.CgError) as e:
+                Grammar.compile(src, "gbnf")
+            assert e.value.code == _lib.CG_E_EMPTY
+            continue
+        nxt, _ = Grammar.compile(src, "gbnf").export()
+        assert np.array_equal(nxt, o.next), src
+        done += 1
+
+
+def test_compiler_unbounded_and_recursive_rules():
+    srcs = ['root ::= ("ab" | "c")* "a" & [abc]{0,7}',
+            'root ::= e\ne ::= "x" | "(" e ")"',
+            'root ::= "a"+ "b"* & "a"{1,3} [ab]{0,2}',
+            'root ::= ( [^ ] | " "{1,3} [^ ] )* " "{0,3} & [a ]{0,9}',
+            'root ::= "q" @forced( [0-9]{1,3} ) "!"']
+    for src in srcs:
+        o = build_dfa(gbnf_to_tree(src, 4))
+        nxt, _ = Grammar.compile(src, "gbnf", Bounds(depth_max=4)).export()
+        assert np.array_equal(nxt, o.next), src
+
+
+@pytest.mark.parametrize("schema", [
+    {"type": "string", "pattern": "a+"}, {"$ref": "#/x"},
+    {"type": "object", "properties": {"a": {"type": "integer"}}},
+    {"type": "object", "properties": {"a": {"type": "integer"}}, "required": ["a"], "additionalProperties": True},
+    {"type": "integer", "minimum": 3}, {"oneOf": [{"type": "null"}]}, {"enum": [1.5]},
+    {"type": "string", "format": "date"}, {"type": "string", "minLength": 5, "maxLength": 2},
+    {"enum": ["a", 1], "type": ["string", "integer"]}, {},
+])
+def test_fail_closed_like_the_oracle(schema):
+    b = WBounds()
+    with pytest.raises(GrammarError) as oe:
+        schema_to_tree(json.dumps(schema), b.ws_max, b.max_len_default, b.max_items_default)
+    with pytest.raises(_lib.CgError) as pe:
+        Grammar.compile(json.dumps(schema), "json")
+    assert oe.value.code == "unsupported" and pe.value.code == _lib.CG_E_UNSUPPORTED
+
+
+def test_try_input_reports_refusal_offset():
+    g = Grammar.compile(GRAMMARS["calc_call"].source, "gbnf")
+    ok = b'calculate({"expression":"125*8"})'
+    assert g.try_input(ok)[0::2] == (len(ok), True)
+    ref, _, acc = g.try_input(b'calculate({"expression":"125x8"})')
+    assert (ref, acc) == (len(b'calculate({"expression":"125'), False)
+    je = Grammar.compile(GRAMMARS["json_eval"].source, "gbnf")
+    text = b'{"expression": "17 * 23 + 91", "answer": 482}'
+    inj = np.zeros(len(text), np.uint8)
+    inj[text.index(b", "):] = 1
+    assert je.try_input(text, inj)[0::2] == (len(text), True)
+    assert je.try_input(text)[0] == text.index(b", ")
+
+
+def test_live_states_match_oracle_rule():
+    from oracle.driver import live_states
+    for name in ("calc_eval", "booking_200"):
+        spec = GRAMMARS[name]
+        g = Grammar.compile(spec.source, spec.kind, _bounds(spec.bounds))
+        assert np.array_equal(g.live_states(), live_states(oracle_dfa(name)))
+
+
+def test_evaluator_matches_oracle():
+    rng = random.Random(21)
+    spans = [b"17 * 23 + 91", b"1 / 0", b"7 / 2", b"", b"(", b"1/0 x", b"(1/0", b".", b"1..2", b"--3",
+             b"9" * 33 + b" * " + b"9" * 33, b"1" * 64, b"-" + b"1" * 64, b"1" * 65, b"0.5 * 8", b"1" * 5000]
+    alphabet = b"0123456789+-*/(). "
+    spans += [bytes(rng.choice(alphabet) for _ in range(rng.randint(1, 30))) for _ in range(3000)]
+    for span in spans:
+        for fmt in ("calc_tag", "json_answer"):
+            out, _ = eval_arith(span, fmt)
+            assert out == format_result(span, fmt), span
+
+
+def test_tokenizer_matches_oracle():
+    toks = vocab("bpe", 4000)
+    v = Vocab(toks)
+    rng = random.Random(22)
+    for _ in range(300):
+        text = b"".join(rng.choice(toks) for _ in range(rng.randint(0, 12)))
+        text += bytes(rng.randrange(256) for _ in range(rng.randint(0, 4)))
+        assert v.tokenize_greedy(text) == tokenize_greedy(text, toks)
+
+
+def test_driver_matches_oracle_host_rules():
+    """The C++ driver applies the same host rules as the oracle on the same
+    stream of (token, flags): a scripted evaluator-aware generation."""
+    spec = GRAMMARS["calc_eval"]
+    toks = [bytes([b]) for b in range(256)] + [b"<result>", b"</result>", b" + ", b"17"]
+    v = Vocab(toks)
+    d = Driver(v, 1, None, [(spec.span_open, spec.span_close, _lib.CG_RESULT_CALC_TAG)])
+    run = OracleRun([oracle_dfa("calc_eval")], [spec], toks, 2048)
+    row = Row(0, 0)
+    script = list(b"The expression is <calc>") + [259, 258] + list(b"23 * 2") + list(b"</calc>")
+    fnext = np.full(1, -1, np.int32)
+    produced = []
+    for step in range(80):
+        x = np.zeros(len(toks))
+        if script and not row.queue:
+            x[script[0]] = 9.0
+        else:
+            x[ord(".")] = 9.0
+        rec = run.step_row(row, x, 0.0, 1.0, 0, step)
+        if rec["forced"] < 0 and script:
+            script.pop(0)
+        used = np.array([rec["forced"]], np.int32)
+        assert used[0] == fnext[0]
+        d.update(np.array([rec["tok"]], np.uint32), np.array([rec["flags"]], np.uint8), used, fnext)
+        assert fnext[0] == (row.queue[0] if row.queue else -1)
+        produced.append(rec["tok"])
+        if rec["flags"] & FLAG_DONE:
+            break
+    text = b"".join(toks[t] for t in produced)
+    assert text == b"The expression is <calc>17 + 23 * 2</calc><result>63</result>."
