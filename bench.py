@@ -1,0 +1,370 @@
+"""Benchmark of one constrained decode step: fill_bitmask -> mask_and_sample -> accept.
+
+Workload (default ``booking_128k``): booking-decision JSON schema automaton,
+V = 128256 synthetic tokens, B = 256 rows, bf16 logits N(0, 2) with +4 on 5% of
+tokens, temperature 0.7, top-p 0.9.  Rows start in the start state; rows that
+finish or reach 2048 tokens are reset by accept.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  ``value`` is constrained tokens/s with the step's inputs
+already resident in HBM: R pre-generated logit buffers whose total exceeds 4x
+the L2 size are used in rotation, so every step reads its logits from HBM.
+``e2e`` repeats the measurement through the same C calls with the logits copied
+from pinned host memory every step and the sampled tokens read back.
+``--impl reference`` times the CPU oracle (the plain restatement the kernels
+are checked against) on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "constrained tokens/s and µs/step (mask+apply+sample) at V=128256, B=256"
+SAMPLE_SOURCES = ["grammar_constrained_decoding_gb300/csrc/kernel_sample.cu",
+                  "grammar_constrained_decoding_gb300/csrc/device.cuh"]
+
+
+def _kernel_hash() -> str:
+    h = hashlib.sha256()
+    for p in SAMPLE_SOURCES:
+        h.update(open(os.path.join(ROOT, p), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def _traffic_record():
+    """DRAM bytes per launch of the sampling kernel from a committed ncu summary,
+    valid only while the kernel sources are unchanged."""
+    p = os.path.join(ROOT, "profiles", "sample_kernel_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("kernel_sha") != _kernel_hash():
+        return None
+    return d
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 10 ms."""
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.samples = []
+        self._stop = threading.Event()
+        self._proc = None
+        try:
+            self._proc = subprocess.Popen(["nvidia-smi", f"--id={index}", f"--query-gpu={self.QUERY}",
+                                           "--format=csv,noheader,nounits", "-lms", "10"],
+                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self._proc.stdout:
+            self.samples.append((time.time(), [v.strip() for v in line.split(",")]))
+
+    def stop(self):
+        if self._proc:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self._proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        if not inside and self.samples:
+            # timed region shorter than the sampling period: nearest samples
+            inside = [min(self.samples, key=lambda ts: abs(ts[0] - (t0 + t1) / 2))[1]]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm = sorted(float(s[1]) for s in inside if s[1].replace(".", "").isdigit())
+        mx = [float(s[2]) for s in inside if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i in range(4) if len(s) > 5 + i and s[5 + i] == "Active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_ours(args) -> dict | None:
+    import numpy as np
+    import torch
+
+    import grammar_constrained_decoding_gb300 as cg
+    from workloads import CONFIGS, GRAMMARS, make_vocab
+    from workloads.logits import make_logits_device
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+    cfg = CONFIGS[args.config]
+    B, V = cfg.B, cfg.V
+    W = (V + 31) // 32
+    spec = GRAMMARS[cfg.grammars[0]]
+    b = spec.bounds
+    grammars = [cg.Grammar.compile(GRAMMARS[n].source, GRAMMARS[n].kind,
+                                   cg.Bounds(b.ws_max, b.max_len_default, b.depth_max, b.max_items_default,
+                                             b.max_tokens)) for n in cfg.grammars]
+    toks = make_vocab(cfg.vocab_kind, V, cfg.vocab_seed)
+    stream = torch.cuda.current_stream()
+    ctx = cg.Ctx(grammars, cg.Vocab(toks), stream)
+    ctx.prefill()   # every mask class computed once, outside the timed steps
+    dtype = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    esz = 2 if cfg.dtype == "bf16" else 4
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    step_bytes = B * V * esz
+    R = max(2, -(-4 * l2 // step_bytes))
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(cfg.logit_seed + 1000 * rank)
+    bufs = [make_logits_device(B, V, 0, cfg.sigma, cfg.boost, cfg.boost_frac, cfg.dtype, "cuda", gen)
+            for _ in range(R)]
+    gid = None
+    if len(cfg.grammars) > 1:
+        gid = torch.as_tensor((np.arange(B) % len(cfg.grammars)).astype(np.int16)).cuda().view(torch.uint16)
+    states = torch.zeros(B, dtype=torch.int32, device="cuda").view(torch.uint32)
+    counts = torch.zeros(B, dtype=torch.int32, device="cuda").view(torch.uint32)
+    bm = torch.empty((B, W), dtype=torch.int32, device="cuda")
+    tok = torch.empty(B, dtype=torch.int32, device="cuda")
+    flags = torch.empty(B, dtype=torch.uint8, device="cuda")
+    seed = cfg.sample_seed
+
+    def step(i, logits, ev=None):
+        ctx.fill_bitmask(states, bm, gid=gid)
+        if ev is not None:
+            ev[0].record(stream)
+        ctx.mask_and_sample(logits, bm, cfg.temp, cfg.top_p, seed, i, tok)
+        if ev is not None:
+            ev[1].record(stream)
+        ctx.accept(states, tok.view(torch.uint32), states, flags, gid=gid, counts=counts,
+                   max_tokens=b.max_tokens)
+
+    # warm-up (fills the mask cache; excluded from timing like the pages' warm-up calls)
+    for i in range(args.warmup):
+        step(i, bufs[i % R])
+    torch.cuda.synchronize()
+    if ctx.status() != 0:
+        raise RuntimeError("device status after warm-up")
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.1)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i, bufs[(args.warmup + i) % R], evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if pg:
+        pg.barrier()
+    ms = start.elapsed_time(end)
+    k2_ms = [a.elapsed_time(z) for a, z in evs]
+    status = ctx.status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} in the timed region")
+    if pg:
+        t = torch.tensor([ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    time.sleep(0.05)
+    clocks = sampler.summary(t0, t1) if sampler else None
+    if sampler:
+        sampler.stop()
+
+    # end to end through the same calls with host buffers
+    e2e_steps = min(args.steps, args.e2e_steps)
+    nh = 2
+    host_bufs = [torch.empty((B, V), dtype=dtype, pin_memory=True) for _ in range(nh)]
+    for hb in host_bufs:
+        hb.copy_(bufs[0].cpu())
+    dev_in = torch.empty((B, V), dtype=dtype, device="cuda")
+    tok_host = torch.empty(B, dtype=torch.int32, pin_memory=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        dev_in.copy_(host_bufs[i % nh], non_blocking=True)
+        step(10**6 + i, dev_in)
+        tok_host.copy_(tok, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    if rank != 0:
+        return None
+    per_step = ms / args.steps
+    k2_avg_ms = sum(k2_ms) / len(k2_ms)
+    alg_bytes = B * (V * esz + W * 4)
+    peaks = _peaks()
+    achieved = alg_bytes / (k2_avg_ms * 1e-3) / 1e9
+    traffic = _traffic_record()
+    units = B * args.steps * world
+    info = ctx.info()
+    out = {
+        "metric": METRIC,
+        "value": round(units / (ms * 1e-3), 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(per_step, 5),
+        "us_per_step": round(per_step * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": cfg.dtype,
+        "data": "synthetic (seeded vocabulary, logits and grammar; no model)",
+        "config": {"workload": f"{cfg.name}: booking-decision JSON schema automaton "
+                               f"({grammars[0].info()['n_states']} states), V={V}, B={B}, {cfg.dtype} logits "
+                               f"N(0,{cfg.sigma}) +{cfg.boost} on {cfg.boost_frac:.0%}, T={cfg.temp}, "
+                               f"top_p={cfg.top_p}",
+                   "B": B, "V": V, "l2_policy": f"{R} rotated logit buffers, {R * step_bytes / 2**20:.0f} MiB "
+                                                 f">= 4x L2 ({l2 / 2**20:.0f} MiB): every step reads HBM",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "mask_classes": info["n_classes"]},
+        "gpu_launches": 3 * args.steps,
+        "kernel_us": {"mask_and_sample": round(k2_avg_ms * 1e3, 3),
+                      "fill_bitmask+accept": round(per_step * 1e3 - k2_avg_ms * 1e3, 3)},
+        "roofline": {"kernel": "sample_kernel (mask_and_sample)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "peak_source": f"{peaks['source']} (copy bandwidth)",
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "traffic": traffic["dram_bytes_per_launch"] if traffic else None},
+        "e2e": {"value": round(B / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": step_bytes, "d2h_bytes_per_step": B * 4, "steps": e2e_steps},
+        "clocks": clocks,
+    }
+    return out
+
+
+class OracleBench:
+    """The oracle stepping rows of the workload, each on its own trajectory from
+    the start state (the logits of a row-step are generated outside the timing)."""
+
+    def __init__(self, cfg_name: str, rows: int):
+        import numpy as np  # noqa: F401
+        from oracle.dfa import compile_grammar
+        from oracle.driver import OracleRun, Row
+        from workloads import CONFIGS, GRAMMARS, make_vocab
+        self.cfg = CONFIGS[cfg_name]
+        specs = [GRAMMARS[n] for n in self.cfg.grammars]
+        dfas = [compile_grammar(s.kind, s.source, s.bounds) for s in specs]
+        toks = make_vocab(self.cfg.vocab_kind, self.cfg.V, self.cfg.vocab_seed)
+        self.run = OracleRun(dfas, specs, toks, specs[0].bounds.max_tokens)
+        self.rows = [Row(b, b % len(specs)) for b in range(rows)]
+        self.step_of = [0] * rows
+        self.spent = 0.0
+        self.done = 0
+
+    def row_step(self, i: int) -> None:
+        import numpy as np
+        from workloads import make_logits
+        cfg = self.cfg
+        r = self.rows[i]
+        x, _ = make_logits(cfg.V, [r.b], self.step_of[i], cfg.logit_seed, cfg.sigma, cfg.boost, cfg.boost_frac,
+                           cfg.dtype)
+        t = time.perf_counter()
+        self.run.step_row(r, x[0].astype(np.float64), cfg.temp, cfg.top_p, cfg.sample_seed, self.step_of[i])
+        self.spent += time.perf_counter() - t
+        self.step_of[i] += 1
+        self.done += 1
+
+
+def cpu_baseline(cfg_name: str, budget_s: float = 15.0) -> dict:
+    ob = OracleBench(cfg_name, 4)
+    k = 0
+    while ob.spent < budget_s:
+        ob.row_step(k % 4)
+        k += 1
+    return {"value": round(ob.done / ob.spent, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{ob.done} row-steps of {cfg_name} (4 rows from the start state, round robin), "
+                      f"float64 numpy, one thread, {ob.spent:.1f} s of CPU work (logit generation excluded)"}
+
+
+def run_reference(args) -> dict | None:
+    world, rank, _ = _dist()
+    if rank != 0:
+        return None
+    ob = OracleBench(args.config, 4)
+    for i in range(args.warmup):
+        ob.row_step(i % 4)
+    ob.spent, ob.done = 0.0, 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        ob.row_step(i % 4)
+    wall = time.perf_counter() - t0
+    value = round(ob.done / ob.spent, 2)
+    cfg = ob.cfg
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ob.spent / max(1, args.steps) * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded vocabulary, logits and grammar; no model)",
+            "config": {"workload": f"{cfg.name}: V={cfg.V}, B={cfg.B}; each step is a bounded sample: "
+                                   f"one row of the batch (4 rows round robin)", "B": cfg.B, "V": cfg.V},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{ob.done} row-steps, one row per step, {wall:.1f} s wall"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="booking_128k")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        out = run_reference(args)
+    else:
+        out = run_ours(args)
+        if out is not None:
+            out["cpu_baseline"] = None if args.no_cpu_baseline else cpu_baseline(args.config)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -162,6 +162,9 @@ class Ctx:
             L.check("cg_ctx_status", rc)
         return code.value
 
+    def prefill(self) -> None:
+        L.check("cg_ctx_prefill", L.lib().cg_ctx_prefill(self._h))
+
     def fill_bitmask(self, states, bitmask, gid=None, forced=None) -> None:
         B = states.shape[0]
         L.check("cg_fill_bitmask", L.lib().cg_fill_bitmask(self._h, _ptr(states), _ptr(gid), _ptr(forced), B,

@@ -12,9 +12,11 @@ namespace cgk {
 cudaError_t launch_fill_bitmask(const Tables& t, const uint32_t* states, const uint16_t* gid, const int32_t* forced,
                                 uint32_t B, uint32_t* bitmask, cudaStream_t stream);
 size_t fill_bitmask_smem(uint32_t W);
+cudaError_t launch_prefill(const Tables& t, const uint32_t* class_rep, const uint16_t* class_gid, cudaStream_t stream);
 cudaError_t launch_mask_and_sample(void* logits, int dtype, uint32_t B, uint32_t V, uint32_t W,
                                    const uint32_t* bitmask, float temp, float top_p, uint64_t seed, uint32_t step,
-                                   uint32_t* out_tok, float* probs, int inplace, cudaStream_t stream);
+                                   uint32_t* out_tok, float* probs, int inplace, uint32_t* status,
+                                   cudaStream_t stream);
 cudaError_t launch_accept(const Tables& t, const uint32_t* states, const uint16_t* gid, const uint32_t* toks,
                           const int32_t* forced, uint32_t B, uint32_t* counts, uint32_t max_tokens,
                           uint32_t* out_states, uint8_t* out_flags, cudaStream_t stream);
@@ -26,6 +28,8 @@ struct cg_ctx {
   cgk::Tables t{};
   std::vector<void*> allocations;
   uint64_t cache_bytes = 0;
+  const uint32_t* class_rep = nullptr;   // representative state of each mask class
+  const uint16_t* class_gid = nullptr;   // grammar of each mask class
 };
 
 namespace {
@@ -64,7 +68,8 @@ int cg_ctx_create(const cg_grammar* const* g, uint32_t n_g, const cg_vocab* v, v
   std::vector<uint32_t> table;
   std::vector<uint16_t> colmap(size_t(n_g) * 512);
   std::vector<uint8_t> flags;
-  std::vector<uint32_t> class_of;
+  std::vector<uint32_t> class_of, class_rep;
+  std::vector<uint16_t> class_gid;
   uint32_t n_classes = 0;
   uint64_t table_off = 0;
   uint32_t state_off = 0;
@@ -78,6 +83,8 @@ int cg_ctx_create(const cg_grammar* const* g, uint32_t n_g, const cg_vocab* v, v
       std::copy(gr.col_of.begin(), gr.col_of.end(), colmap.begin() + size_t(i) * 512);
       flags.insert(flags.end(), gr.flags.begin(), gr.flags.end());
       for (uint32_t s = 0; s < gr.dfa.n_states; ++s) class_of.push_back(cls[s] + n_classes);
+      class_rep.insert(class_rep.end(), rep.begin(), rep.end());
+      class_gid.insert(class_gid.end(), nc, uint16_t(i));
       n_classes += nc;
       table_off += gr.table.size();
       state_off += gr.dfa.n_states;
@@ -93,14 +100,16 @@ int cg_ctx_create(const cg_grammar* const* g, uint32_t n_g, const cg_vocab* v, v
   uint16_t* d_col;
   uint8_t* d_flags;
   uint32_t* d_class;
-  uint32_t *d_off, *d_soff, *d_perm;
+  uint32_t *d_off, *d_soff, *d_perm, *d_rep;
+  uint16_t* d_cgid;
   uint8_t *d_bytes, *d_sbytes, *d_lcp;
   if ((e = upload(c, table, &d_table)) != cudaSuccess || (e = upload(c, gdesc, &d_gd)) != cudaSuccess ||
       (e = upload(c, colmap, &d_col)) != cudaSuccess || (e = upload(c, flags, &d_flags)) != cudaSuccess ||
       (e = upload(c, class_of, &d_class)) != cudaSuccess || (e = upload(c, v->off, &d_off)) != cudaSuccess ||
       (e = upload(c, v->bytes, &d_bytes)) != cudaSuccess || (e = upload(c, v->sorted_off, &d_soff)) != cudaSuccess ||
       (e = upload(c, v->sorted_bytes, &d_sbytes)) != cudaSuccess || (e = upload(c, v->perm, &d_perm)) != cudaSuccess ||
-      (e = upload(c, v->lcp, &d_lcp)) != cudaSuccess) {
+      (e = upload(c, v->lcp, &d_lcp)) != cudaSuccess || (e = upload(c, class_rep, &d_rep)) != cudaSuccess ||
+      (e = upload(c, class_gid, &d_cgid)) != cudaSuccess) {
     release(c);
     delete c;
     return CG_E_CUDA;
@@ -137,6 +146,8 @@ int cg_ctx_create(const cg_grammar* const* g, uint32_t n_g, const cg_vocab* v, v
   t.perm = d_perm;
   t.lcp = d_lcp;
   t.status = d_status;
+  c->class_rep = d_rep;
+  c->class_gid = d_cgid;
   *out = c;
   return CG_OK;
 }
@@ -167,6 +178,11 @@ int cg_ctx_status(cg_ctx* c, uint32_t* dev_code) {
   return code ? CG_E_DEVICE : CG_OK;
 }
 
+int cg_ctx_prefill(cg_ctx* c) {
+  if (!c) return CG_E_ARG;
+  return cgk::launch_prefill(c->t, c->class_rep, c->class_gid, c->stream) == cudaSuccess ? CG_OK : CG_E_CUDA;
+}
+
 int cg_fill_bitmask(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const int32_t* d_forced, uint32_t B,
                     uint32_t* d_bitmask) {
   if (!c || (B && (!d_states || !d_bitmask))) return CG_E_ARG;
@@ -183,7 +199,8 @@ int cg_mask_and_sample(cg_ctx* c, void* d_logits, int dtype, uint32_t B, uint32_
   if (V != c->t.V || !(temp >= 0.f) || temp == INFINITY || !(top_p == top_p)) return CG_E_ARG;
   if (flags & ~CG_SAMPLE_INPLACE) return CG_E_ARG;
   return cgk::launch_mask_and_sample(d_logits, dtype, B, V, c->t.W, d_bitmask, temp, top_p, seed, step, d_out_tok,
-                                     d_probs, (flags & CG_SAMPLE_INPLACE) ? 1 : 0, c->stream) == cudaSuccess
+                                     d_probs, (flags & CG_SAMPLE_INPLACE) ? 1 : 0, c->t.status, c->stream) ==
+                 cudaSuccess
              ? CG_OK
              : CG_E_CUDA;
 }

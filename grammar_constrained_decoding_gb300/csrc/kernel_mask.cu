@@ -132,6 +132,35 @@ __global__ void __launch_bounds__(kFillThreads) fill_bitmask_kernel(Tables t, co
   }
 }
 
+// One CTA per mask class: computes every class mask ahead of the decode steps.
+__global__ void __launch_bounds__(kFillThreads) prefill_kernel(Tables t, const uint32_t* __restrict__ class_rep,
+                                                                 const uint16_t* __restrict__ class_gid) {
+  extern __shared__ uint32_t smem[];
+  uint32_t* smask = smem;
+  uint16_t* scol = reinterpret_cast<uint16_t*>(smem + t.W);
+  const uint32_t cls = blockIdx.x, W = t.W;
+  if (load_acquire(t.cache_state + cls) == kStateReady) return;  // uniform: no other writer runs meanwhile
+  const uint32_t g = class_gid[cls];
+  for (uint32_t i = threadIdx.x; i < W; i += blockDim.x) smask[i] = 0u;
+  for (uint32_t i = threadIdx.x; i < 256; i += blockDim.x) scol[i] = t.colmap[size_t(g) * 512 + i];
+  __syncthreads();
+  walk_tokens(t, t.grammars[g], scol, class_rep[cls], smask);
+  __syncthreads();
+  uint32_t* cw = t.cache + size_t(cls) * W;
+  for (uint32_t i = threadIdx.x; i < W; i += blockDim.x) cw[i] = smask[i];
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) store_release(t.cache_state + cls, kStateReady);
+}
+
+cudaError_t launch_prefill(const Tables& t, const uint32_t* class_rep, const uint16_t* class_gid,
+                           cudaStream_t stream) {
+  if (t.n_classes == 0) return cudaSuccess;
+  const size_t smem = size_t(t.W) * 4 + 256 * 2;
+  prefill_kernel<<<t.n_classes, kFillThreads, smem, stream>>>(t, class_rep, class_gid);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_fill_bitmask(const Tables& t, const uint32_t* states, const uint16_t* gid, const int32_t* forced,
                                 uint32_t B, uint32_t* bitmask, cudaStream_t stream) {
   if (B == 0) return cudaSuccess;

@@ -18,6 +18,8 @@
 // the key space when the nucleus reaches below that window; a last pass draws
 // the Gumbel scores of the nucleus only.  Exponentials use exp2 with the
 // temperature folded into one scale c = log2(e) / temp.
+#include <cuda_bf16.h>
+
 #include "device.cuh"
 
 namespace cgk {
@@ -93,34 +95,24 @@ struct Gumbel {
   }
 };
 
+// The whole step for one row from the row in global memory (any dtype, any
+// V, any mode): pass A streams max / sum / greedy or full Gumbel; the top-p
+// threshold comes from the per-key window or, failing that, bisection; a last
+// pass samples the nucleus.  `smask` holds the row's bitmask; `cnt` is
+// kWindow words of shared scratch.  Returns the token; M and S through refs.
 template <bool BF16, bool VEC, int MODE>
-__global__ void __launch_bounds__(kSampleThreads) sample_kernel(void* logits, uint32_t V,
-                                                                 uint32_t W, const uint32_t* __restrict__ bitmask,
-                                                                 float temp, float top_p, uint32_t k0, uint32_t k1,
-                                                                 uint32_t step, uint32_t* __restrict__ out_tok,
-                                                                 float* __restrict__ probs, int inplace) {
-  extern __shared__ uint32_t smem[];
-  uint32_t* smask = smem;             // [W]
-  uint32_t* cnt = smem + W;           // [kWindow] (top-p, bf16)
+__device__ uint32_t general_row(char* row, uint32_t V, const uint32_t* smask, uint32_t* cnt, float temp,
+                                float top_p, uint32_t b, uint32_t k0, uint32_t k1, uint32_t step, float& M_out,
+                                double& S_out) {
   __shared__ unsigned long long red_u64[33];
   __shared__ float red_f[33];
   __shared__ double red_d[33];
   __shared__ uint32_t s_tau;
 
-  const uint32_t b = blockIdx.x;
-  const size_t esz = BF16 ? 2 : 4;
-  char* row = reinterpret_cast<char*>(logits) + size_t(b) * V * esz;
-  const uint32_t* mrow = bitmask + size_t(b) * W;
-  for (uint32_t i = threadIdx.x; i < W; i += blockDim.x) smask[i] = mrow[i];
-  __syncthreads();
-
-  // ---- pass A --------------------------------------------------------------
   const float c = (MODE == kGreedy) ? 0.f : 1.4426950408889634f / temp;
   unsigned long long best = 0ull;  // packed (value, id); 0 = none
   float m = -INFINITY;
-  float acc[kAcc];
-#pragma unroll
-  for (int j = 0; j < kAcc; ++j) acc[j] = 0.f;
+  float sum = 0.f, comp = 0.f;  // compensated (Kahan) sum of exp2((x - m) c)
   Gumbel gum{b, step, k0, k1, temp};
   auto pass_a = [&](uint32_t t, float x) {
     if (MODE == kGreedy) {
@@ -129,11 +121,14 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(void* logits, ui
     }
     if (x > m) {
       const float r = exp2f((m - x) * c);
-#pragma unroll
-      for (int j = 0; j < kAcc; ++j) acc[j] *= r;
+      sum *= r;
+      comp *= r;
       m = x;
     }
-    acc[t & (kAcc - 1)] += exp2f((x - m) * c);
+    const float y = exp2f((x - m) * c) - comp;
+    const float nt = sum + y;
+    comp = (nt - sum) - y;
+    sum = nt;
     if (MODE == kFull) best = max(best, pack_best(gum.score(t, x), t));
   };
   for_allowed<BF16, VEC>(row, V, smask, pass_a);
@@ -145,16 +140,11 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(void* logits, ui
   } else {
     M = block_reduce(m, MaxOp(), -INFINITY, red_f);
     double part = 0.0;
-    if (m > -INFINITY) {
-      const float r = exp2f((m - M) * c);
-#pragma unroll
-      for (int j = 0; j < kAcc; ++j) part += double(acc[j]) * double(r);
-    }
+    if (m > -INFINITY) part = (double(sum) - double(comp)) * double(exp2f((m - M) * c));
     S = block_reduce(part, SumOp(), 0.0, red_d);
     if (MODE == kFull) best = block_reduce(best, MaxOp(), 0ull, red_u64);
   }
 
-  // ---- top-p threshold and nucleus sample ------------------------------------
   if (MODE == kTopP && M > -INFINITY) {
     const double target = double(top_p) * S;
     uint32_t tau = kNotFound;  // bf16: 16-bit key; f32: 32-bit key
@@ -173,7 +163,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(void* logits, ui
         const uint32_t lane = threadIdx.x;
         double cum = 0.0;
         uint32_t found = kNotFound;
-        for (uint32_t base = 0; base < uint32_t(kWindow) && base <= km - lo && found == kNotFound; base += 32) {
+        for (uint32_t base = 0; base <= km - lo && found == kNotFound; base += 32) {
           const uint32_t j = base + lane;
           double mass = 0.0;
           if (j <= km - lo && cnt[j]) mass = double(cnt[j]) * double(exp2f((bf16key_to_float(km - j) - M) * c));
@@ -215,11 +205,17 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(void* logits, ui
     for_allowed<BF16, VEC>(row, V, smask, pass_c);
     best = block_reduce(best, MaxOp(), 0ull, red_u64);
   }
+  M_out = M;
+  S_out = S;
+  return best ? best_id(best) : CG_NO_TOKEN;
+}
 
-  const uint32_t tok = best ? best_id(best) : CG_NO_TOKEN;
-  if (threadIdx.x == 0) out_tok[b] = tok;
-
-  // ---- optional outputs -------------------------------------------------------
+// Optional outputs: softmax over allowed tokens (greedy: 1 at the token) and
+// -inf written into masked logits.
+template <bool BF16, int MODE>
+__device__ void write_outputs(char* row, uint32_t V, const uint32_t* smask, uint32_t tok, float M, double S,
+                              float temp, float* probs, int inplace, uint32_t b) {
+  const float c = (MODE == kGreedy) ? 0.f : 1.4426950408889634f / temp;
   if (probs) {
     float* prow = probs + size_t(b) * V;
     const float invS = (MODE == kGreedy || S <= 0.0) ? 0.f : float(1.0 / S);
@@ -238,6 +234,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(void* logits, ui
     }
   }
   if (inplace) {
+    __syncthreads();  // every read of the row is done
     for (uint32_t t = threadIdx.x; t < V; t += blockDim.x) {
       if ((smask[t >> 5] >> (t & 31)) & 1u) continue;
       if (BF16) reinterpret_cast<uint16_t*>(row)[t] = 0xFF80u;
@@ -245,6 +242,478 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(void* logits, ui
     }
   }
 }
+
+template <bool BF16, bool VEC, int MODE>
+__global__ void __launch_bounds__(kSampleThreads) sample_kernel(void* logits, uint32_t V,
+                                                                 uint32_t W, const uint32_t* __restrict__ bitmask,
+                                                                 float temp, float top_p, uint32_t k0, uint32_t k1,
+                                                                 uint32_t step, uint32_t* __restrict__ out_tok,
+                                                                 float* __restrict__ probs, int inplace) {
+  extern __shared__ uint32_t smem[];
+  uint32_t* smask = smem;             // [W]
+  uint32_t* cnt = smem + W;           // [kWindow] (top-p, bf16)
+  const uint32_t b = blockIdx.x;
+  const size_t esz = BF16 ? 2 : 4;
+  char* row = reinterpret_cast<char*>(logits) + size_t(b) * V * esz;
+  const uint32_t* mrow = bitmask + size_t(b) * W;
+  for (uint32_t i = threadIdx.x; i < W; i += blockDim.x) smask[i] = mrow[i];
+  __syncthreads();
+  float M;
+  double S;
+  const uint32_t tok = general_row<BF16, VEC, MODE>(row, V, smask, cnt, temp, top_p, b, k0, k1, step, M, S);
+  if (threadIdx.x == 0) out_tok[b] = tok;
+  write_outputs<BF16, MODE>(row, V, smask, tok, M, S, temp, probs, inplace, b);
+}
+
+// ============================================================================
+// Single-pass top-p kernel for bf16 rows (the path of the throughput metric).
+//
+// One CTA of 512 threads per row: warp 15 issues bulk asynchronous copies
+// (TMA, cp.async.bulk) of the row into a 4-slot shared-memory ring, warps
+// 0..14 consume the slots.  Slots hand over through mbarriers (full: copy
+// landed; empty: all 15 consumer warps are done), so no block barrier sits in
+// the streaming loop.  The bitmask is applied 8 logits at a time through a
+// 256-entry table of pair masks.  Each consumer thread keeps a running
+// maximum and 8 partial sums of exponentials, and for every 8-logit group one
+// bit records whether the group's maximum reached the block's running maximum
+// minus kMarginZ nats (a warp ballot per 32 groups).  The running maximum never
+// exceeds the final maximum M, so every group holding a logit within the margin
+// of M is flagged.
+//
+// After the stream, with M and S = sum exp exact, the flagged groups are read
+// again (from L2) and their allowed logits >= M - margin become the candidate
+// list, kept in the now idle ring.  The nucleus threshold is found among the
+// candidates' keys (per-key counts of the keys just below M, or bisection over
+// the list) as long as they carry at least top_p of the mass, and the Gumbel
+// scores are drawn for the nucleus entries only.  Rows whose list overflows or
+// whose nucleus reaches below the margin run general_row instead.
+// ============================================================================
+namespace fast {
+
+constexpr int kThreads = 512;
+constexpr uint32_t kConsumerWarps = 15;
+constexpr uint32_t kConsumers = kConsumerWarps * 32;            // 480
+constexpr int kStages = 4;
+constexpr uint32_t kChunkElems = kConsumers * 16;               // 7680 logits per slot
+constexpr uint32_t kChunkBytes = kChunkElems * 2;               // 15 KiB
+constexpr uint32_t kGroupsPerChunk = kChunkElems / 8;           // 960
+constexpr uint32_t kBins = 448;                                 // keys per histogram (one per thread)
+constexpr uint32_t kRing = kStages * kChunkBytes;               // 60 KiB
+constexpr uint32_t kCap = (kRing - 16 * kBins * 4) / 6;         // candidate ids (u32) + keys (u16)
+static_assert(kBins <= kThreads, "one histogram key per thread");
+constexpr float kMarginZ = 9.5f;                                // nats below the maximum kept as candidates
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// bounded wait on a phase; false when the limit ran out
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// 2^x with the multi-function unit (relative error about 2^-22; results
+// below 2^-126 flush to zero, far below any mass that matters here)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a), y = *reinterpret_cast<__nv_bfloat162*>(&b);
+  __nv_bfloat162 r = __hmax2(x, y);
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+// masked logits become -inf (bf16 0xFF80)
+__device__ __forceinline__ uint4 apply_mask(uint4 v, uint4 pm) {
+  v.x = (v.x & pm.x) | (~pm.x & 0xFF80FF80u);
+  v.y = (v.y & pm.y) | (~pm.y & 0xFF80FF80u);
+  v.z = (v.z & pm.z) | (~pm.z & 0xFF80FF80u);
+  v.w = (v.w & pm.w) | (~pm.w & 0xFF80FF80u);
+  return v;
+}
+__device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__global__ void __launch_bounds__(kThreads, 2)
+    stream_topp_kernel(void* logits, uint32_t V, uint32_t W, const uint32_t* __restrict__ bitmask, float temp,
+                       float top_p, uint32_t k0, uint32_t k1, uint32_t step, uint32_t* __restrict__ out_tok,
+                       float* __restrict__ probs, int inplace, uint32_t* status) {
+  extern __shared__ __align__(128) unsigned char dsm[];
+  unsigned char* ring = dsm;                                               // kStages slots
+  uint4* lut = reinterpret_cast<uint4*>(dsm + kRing);                      // [256]
+  uint32_t* smask = reinterpret_cast<uint32_t*>(dsm + kRing + 4096);       // [W]
+  uint32_t* gflags = smask + ((W + 3) & ~3u);                              // one bit per 8-logit group
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
+  __shared__ float red_f[33];
+  __shared__ double red_d[33];
+  __shared__ unsigned long long red_u64[33];
+  __shared__ uint32_t red_u[33];
+  __shared__ uint32_t s_maxkey, s_count, s_flag, s_tau, s_groups;
+
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, b = blockIdx.x;
+  char* row = reinterpret_cast<char*>(logits) + size_t(b) * V * 2;
+  const uint32_t nchunks = (V + kChunkElems - 1) / kChunkElems;
+  const uint32_t ngroups = V / 8;
+  const uint32_t nwords = (ngroups + 31) / 32;
+
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, kConsumerWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    s_maxkey = fkey(-INFINITY);
+    s_count = 0;
+    s_flag = 0;  // bit 0: a wait ran out
+  }
+  for (uint32_t i = tid; i < 256; i += kThreads) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      w[q] = (((i >> (2 * q)) & 1u) ? 0x0000FFFFu : 0u) | (((i >> (2 * q + 1)) & 1u) ? 0xFFFF0000u : 0u);
+    lut[i] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  const uint32_t* mrow = bitmask + size_t(b) * W;
+  for (uint32_t i = tid; i < W; i += kThreads) smask[i] = mrow[i];
+  for (uint32_t i = tid; i < nwords; i += kThreads) gflags[i] = 0u;
+  __syncthreads();
+
+  const float c = 1.4426950408889634f / temp;
+  const float margin = kMarginZ * temp;  // z = x / temp: kMarginZ nats are kMarginZ * temp logit units
+  float mt = -INFINITY;
+  float acc[kAcc];
+#pragma unroll
+  for (int j = 0; j < kAcc; ++j) acc[j] = 0.f;
+
+  if (warp == kConsumerWarps) {
+    // ---- producer: one lane keeps the ring full -------------------------------
+    if (lane == 0) {
+      for (uint32_t k = 0; k < nchunks; ++k) {
+        const uint32_t slot = k % kStages;
+        if (k >= uint32_t(kStages) && !mbar_wait(empty + slot, ((k / kStages) - 1) & 1u)) {
+          atomicOr(&s_flag, 1u);
+          break;
+        }
+        const uint32_t bytes = min(kChunkElems, V - k * kChunkElems) * 2;
+        mbar_expect_tx(full + slot, bytes);
+        bulk_g2s(ring + size_t(slot) * kChunkBytes, row + size_t(k) * kChunkBytes, bytes, full + slot);
+      }
+    }
+  } else {
+    // ---- consumers ----------------------------------------------------------------
+    // chunk 0's maximum seeds the flag threshold, so the first chunk does not
+    // flag every group
+    if (!mbar_wait(full + 0, 0)) atomicOr(&s_flag, 1u);
+    {
+      const uint4* r4 = reinterpret_cast<const uint4*>(ring);
+      float lm = -INFINITY;
+#pragma unroll
+      for (uint32_t g = 0; g < 2; ++g) {
+        const uint32_t gi = tid + kConsumers * g, t0 = gi * 8;
+        if (t0 < V) {
+          const uint4 v = apply_mask(r4[gi], lut[(smask[t0 >> 5] >> (t0 & 31)) & 0xFFu]);
+          const uint32_t mx = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
+          lm = fmaxf(lm, fmaxf(lo_f(mx), hi_f(mx)));
+        }
+      }
+      lm = warp_reduce(lm, MaxOp());
+      if (lane == 0 && lm > -INFINITY) atomicMax(&s_maxkey, fkey(lm));
+      asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");  // consumer warps only
+    }
+    float thr = fmaxf(fkey_inv(*reinterpret_cast<volatile uint32_t*>(&s_maxkey)) - margin, -3.402823466e38f);
+    for (uint32_t k = 0; k < nchunks; ++k) {
+      const uint32_t slot = k % kStages;
+      if (!mbar_wait(full + slot, (k / kStages) & 1u)) {
+        atomicOr(&s_flag, 1u);
+        break;
+      }
+      const uint4* r4 = reinterpret_cast<const uint4*>(ring + size_t(slot) * kChunkBytes);
+      const uint32_t base = k * kChunkElems;
+      float wmax = -INFINITY;
+#pragma unroll
+      for (uint32_t g = 0; g < 2; ++g) {
+        const uint32_t gi = tid + kConsumers * g, t0 = base + gi * 8;
+        bool flag = false;
+        if (t0 < V) {
+          const uint4 v = apply_mask(r4[gi], lut[(smask[t0 >> 5] >> (t0 & 31)) & 0xFFu]);
+          const uint32_t mx = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
+          const float gmax = fmaxf(lo_f(mx), hi_f(mx));
+          wmax = fmaxf(wmax, gmax);
+          if (gmax > -INFINITY) {
+            if (gmax > mt) {
+              const float r = ex2((mt - gmax) * c);
+#pragma unroll
+              for (int j = 0; j < kAcc; ++j) acc[j] *= r;
+              mt = gmax;
+            }
+            const float mc = mt * c;
+            acc[0] += ex2(fmaf(lo_f(v.x), c, -mc));
+            acc[1] += ex2(fmaf(hi_f(v.x), c, -mc));
+            acc[2] += ex2(fmaf(lo_f(v.y), c, -mc));
+            acc[3] += ex2(fmaf(hi_f(v.y), c, -mc));
+            acc[4] += ex2(fmaf(lo_f(v.z), c, -mc));
+            acc[5] += ex2(fmaf(hi_f(v.z), c, -mc));
+            acc[6] += ex2(fmaf(lo_f(v.w), c, -mc));
+            acc[7] += ex2(fmaf(hi_f(v.w), c, -mc));
+            flag = gmax >= thr;
+          }
+        }
+        // group index of this lane = k * 960 + 480 g + tid: 32 consecutive groups per warp
+        const unsigned bits = __ballot_sync(0xFFFFFFFFu, flag);
+        if (lane == 0 && bits) gflags[k * (kGroupsPerChunk / 32) + g * (kConsumers / 32) + warp] = bits;
+      }
+      const float wm = warp_reduce(wmax, MaxOp());
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(empty + slot);
+        if (wm > -INFINITY) atomicMax(&s_maxkey, fkey(wm));
+      }
+      thr = fkey_inv(*reinterpret_cast<volatile uint32_t*>(&s_maxkey)) - margin;
+    }
+  }
+  __syncthreads();
+
+  // ---- row statistics -----------------------------------------------------------
+  if ((s_flag & 1u) && tid == 0) {
+    // a wait ran out: let copies still in flight land before the shared memory
+    // is reused or released (again with a bounded wait)
+    for (uint32_t sl = 0; sl < uint32_t(kStages) && sl < nchunks; ++sl) {
+      const uint32_t issued = (nchunks - sl + kStages - 1) / kStages;
+      mbar_wait(full + sl, (issued - 1) & 1u);
+    }
+  }
+  const float M = block_reduce(mt, MaxOp(), -INFINITY, red_f);
+  double part = 0.0;
+  if (mt > -INFINITY) {
+    float a = 0.f;
+#pragma unroll
+    for (int j = 0; j < kAcc; ++j) a += acc[j];
+    part = double(a) * double(ex2((mt - M) * c));
+  }
+  const double S = block_reduce(part, SumOp(), 0.0, red_d);
+  uint32_t tok = CG_NO_TOKEN;
+  bool general = false;
+  if (s_flag & 1u) {
+    if (tid == 0) record_error(status, CG_DEV_TIMEOUT);
+  } else if (M > -INFINITY) {
+    const double target = double(top_p) * S;
+    const float thrF = M - margin;  // every allowed logit >= thrF sits in a flagged group
+    uint32_t kthr = fkey(thrF) >> 16;
+    if (bf16key_to_float(kthr) < thrF) ++kthr;
+    const uint32_t km = fkey(M) >> 16;
+    // ring reuse: per-warp key histograms, then the candidate ids and keys
+    uint32_t* wbins = reinterpret_cast<uint32_t*>(ring);                     // [16][kBins]
+    uint32_t* cid = wbins + 16 * kBins;                                      // [kCap]
+    uint16_t* ckey = reinterpret_cast<uint16_t*>(cid + kCap);                // [kCap]
+    const bool use_bins = km - kthr < kBins;
+    if (use_bins)
+      for (uint32_t i = tid; i < 16 * kBins; i += kThreads) wbins[i] = 0u;
+    if (tid == 0) s_count = 0u;
+    // ---- candidates: allowed logits >= thrF of the flagged groups ----------------
+    // flagged groups are numbered through an exclusive prefix over the flag
+    // words; in batch k, thread t takes groups k * 2048 + t + 512 r (r < 4), so
+    // every warp runs the same number of batches and reserves list space once
+    // per batch
+    uint32_t* wpre = gflags + nwords;  // [nwords] flagged groups before each word
+    {
+      // thread t owns words 3t .. 3t+2; block-wide exclusive scan of the counts
+      const uint32_t w0 = 3 * tid;
+      const uint32_t c0 = w0 < nwords ? __popc(gflags[w0]) : 0u;
+      const uint32_t c1 = w0 + 1 < nwords ? __popc(gflags[w0 + 1]) : 0u;
+      const uint32_t c2 = w0 + 2 < nwords ? __popc(gflags[w0 + 2]) : 0u;
+      const uint32_t mine = c0 + c1 + c2;
+      uint32_t incl = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= uint32_t(o)) incl += y;
+      }
+      if (lane == 31) red_u[warp] = incl;
+      __syncthreads();
+      uint32_t before = 0;
+      for (uint32_t wi = 0; wi < warp; ++wi) before += red_u[wi];
+      const uint32_t ex = before + incl - mine;
+      if (w0 < nwords) wpre[w0] = ex;
+      if (w0 + 1 < nwords) wpre[w0 + 1] = ex + c0;
+      if (w0 + 2 < nwords) wpre[w0 + 2] = ex + c0 + c1;
+      if (tid == kThreads - 1) s_groups = ex + mine;
+      __syncthreads();
+    }
+    const uint32_t G = s_groups;
+    const uint4* g4 = reinterpret_cast<const uint4*>(row);
+    uint32_t* mybins = wbins + warp * kBins;
+    for (uint32_t base = 0; base < G; base += 4 * kThreads) {
+      uint4 v[4];
+      uint32_t gidx[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const uint32_t idx = base + tid + r * kThreads;
+        gidx[r] = 0xFFFFFFFFu;
+        v[r] = make_uint4(0u, 0u, 0u, 0u);
+        if (idx < G) {
+          // last word whose prefix is <= idx
+          uint32_t lo = 0, hi = nwords - 1;
+          while (lo < hi) {
+            const uint32_t mid = (lo + hi + 1) >> 1;
+            if (wpre[mid] <= idx) lo = mid; else hi = mid - 1;
+          }
+          const uint32_t bit = __fns(gflags[lo], 0, int(idx - wpre[lo] + 1));
+          gidx[r] = lo * 32 + bit;
+          v[r] = ld_stream(g4 + gidx[r]);
+        }
+      }
+      uint32_t hits = 0;  // bit r * 8 + j: logit j of group r is a candidate
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        if (gidx[r] != 0xFFFFFFFFu) {
+          const uint32_t t0 = gidx[r] * 8;
+          v[r] = apply_mask(v[r], lut[(smask[t0 >> 5] >> (t0 & 31)) & 0xFFu]);
+          const uint32_t ww[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float f = (j & 1) ? hi_f(ww[j >> 1]) : lo_f(ww[j >> 1]);
+            hits |= (f >= thrF ? 1u : 0u) << (r * 8 + j);
+          }
+        }
+      }
+      const uint32_t nh = __popc(hits);
+      uint32_t incl = nh;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= uint32_t(o)) incl += y;
+      }
+      const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+      uint32_t wb = 0;
+      if (lane == 31 && total) wb = atomicAdd(&s_count, total);
+      uint32_t pos = __shfl_sync(0xFFFFFFFFu, wb, 31) + incl - nh;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const uint32_t ww[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if ((hits >> (r * 8 + j)) & 1u) {
+            const float f = (j & 1) ? hi_f(ww[j >> 1]) : lo_f(ww[j >> 1]);
+            const uint32_t key = fkey(f) >> 16;
+            if (pos < kCap) {
+              cid[pos] = gidx[r] * 8 + j;
+              ckey[pos] = uint16_t(key);
+            }
+            ++pos;
+            if (use_bins) atomicAdd(mybins + (km - key), 1u);
+          }
+        }
+      }
+    }
+    __syncthreads();
+    const uint32_t n_all = s_count;
+    const uint32_t n = min(n_all, kCap);
+    const double fx = 1099511627776.0;  // masses in 2^-40 units: exact sums, no rounding order
+    const unsigned long long target_q = (unsigned long long)(target * fx);
+    uint32_t tau = kNotFound;
+    if (n_all > kCap) {
+      general = true;
+    } else if (use_bins) {
+      // per-key totals, mass from the top (bin j is key km - j), block-wide
+      // prefix sum, first bin where the upper set reaches the target
+      const uint32_t L = km - kthr + 1;
+      unsigned long long q = 0;
+      if (tid < L) {
+        uint32_t cnt = 0;
+#pragma unroll
+        for (int w = 0; w < 16; ++w) cnt += wbins[w * kBins + tid];
+        if (cnt) q = (unsigned long long)(double(cnt) * double(ex2((bf16key_to_float(km - tid) - M) * c)) * fx);
+      }
+      unsigned long long incl = q;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= uint32_t(o)) incl += y;
+      }
+      if (lane == 31) red_u64[warp] = incl;
+      if (tid == 0) s_tau = kNotFound;
+      __syncthreads();
+      unsigned long long before = 0;
+      for (uint32_t wi = 0; wi < warp; ++wi) before += red_u64[wi];
+      if (tid < L && before + incl >= target_q) atomicMin(&s_tau, tid);
+      __syncthreads();
+      tau = s_tau == kNotFound ? kNotFound : km - s_tau;
+      general = tau == kNotFound;
+    } else {
+      // bisection over the list: largest key whose upper set carries >= target
+      auto mass_at = [&](uint32_t kappa) {
+        unsigned long long p = 0;
+        for (uint32_t i = tid; i < n; i += kThreads) {
+          const uint32_t key = ckey[i];
+          if (key >= kappa) p += (unsigned long long)(double(ex2((bf16key_to_float(key) - M) * c)) * fx);
+        }
+        return block_reduce(p, SumOp(), 0ull, red_u64);
+      };
+      if (mass_at(kthr) < target_q) {
+        general = true;
+      } else {
+        uint32_t lo = kthr, hi = km;
+        while (lo < hi) {
+          const uint32_t mid = lo + (hi - lo + 1) / 2;
+          if (mass_at(mid) >= target_q) lo = mid; else hi = mid - 1;
+        }
+        tau = lo;
+      }
+    }
+    if (!general) {
+      unsigned long long best = 0ull;
+      for (uint32_t i = tid; i < n; i += kThreads) {
+        const uint32_t key = ckey[i];
+        if (key < tau) continue;
+        const uint32_t id = cid[i];
+        const uint4 blk = philox4x32_10(make_uint4(id >> 2, b, step, 0u), k0, k1);
+        const float score = __fdiv_rn(bf16key_to_float(key), temp) + gumbel_from_word(philox_word(blk, id & 3u));
+        best = max(best, pack_best(score, id));
+      }
+      best = block_reduce(best, MaxOp(), 0ull, red_u64);
+      tok = best ? best_id(best) : CG_NO_TOKEN;
+    }
+  }
+  if (general) {
+    __syncthreads();
+    float M2;
+    double S2;
+    tok = general_row<true, true, kTopP>(row, V, smask, reinterpret_cast<uint32_t*>(ring), temp, top_p, b, k0, k1,
+                                         step, M2, S2);
+  }
+  if (tid == 0) out_tok[b] = tok;
+  if (probs || inplace) write_outputs<true, kTopP>(row, V, smask, tok, M, S, temp, probs, inplace, b);
+}
+
+}  // namespace fast
 
 template <bool BF16, bool VEC, int MODE>
 cudaError_t launch_variant(void* logits, uint32_t B, uint32_t V, uint32_t W, const uint32_t* bitmask,
@@ -275,12 +744,23 @@ cudaError_t launch_mode(int mode, void* logits, uint32_t B, uint32_t V, uint32_t
 
 cudaError_t launch_mask_and_sample(void* logits, int dtype, uint32_t B, uint32_t V, uint32_t W,
                                    const uint32_t* bitmask, float temp, float top_p, uint64_t seed, uint32_t step,
-                                   uint32_t* out_tok, float* probs, int inplace, cudaStream_t stream) {
+                                   uint32_t* out_tok, float* probs, int inplace, uint32_t* status,
+                                   cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
   const int mode = (temp == 0.f) ? kGreedy : (top_p >= 1.f ? kFull : kTopP);
   const bool bf16 = dtype == CG_BF16;
   const uint32_t ch = bf16 ? 8u : 4u;
   const bool vec = (V % ch == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
+  const size_t fast_smem = size_t(fast::kRing) + 4096 + ((size_t(W) + 3) & ~size_t(3)) * 4 +
+                           2 * size_t((V / 8 + 31) / 32) * 4;
+  if (bf16 && vec && mode == kTopP && fast_smem <= 110 * 1024 && (V / 8 + 31) / 32 <= 3 * 512) {
+    auto* k = fast::stream_topp_kernel;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(fast_smem));
+    if (e != cudaSuccess) return e;
+    k<<<B, fast::kThreads, fast_smem, stream>>>(logits, V, W, bitmask, temp, top_p, uint32_t(seed),
+                                                uint32_t(seed >> 32), step, out_tok, probs, inplace, status);
+    return cudaGetLastError();
+  }
   if (bf16)
     return vec ? launch_mode<true, true>(mode, logits, B, V, W, bitmask, temp, top_p, seed, step, out_tok, probs,
                                          inplace, stream)

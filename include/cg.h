@@ -86,6 +86,8 @@ extern "C" {
 #define CG_DEV_MISSING_FORCED  5  /* fill: a forced-only state without a forced token */
 #define CG_DEV_BAD_GID         6  /* a grammar index >= n_grammars */
 #define CG_DEV_REJECTED        7  /* accept: the token walks the automaton to CG_DEAD */
+#define CG_DEV_TIMEOUT         8  /* sample: a bounded wait for an asynchronous copy ran out;
+                                     the row gets CG_NO_TOKEN */
 
 /* mask_and_sample flags */
 #define CG_SAMPLE_INPLACE 1u     /* also write -inf into masked logits (the "&mut [f32]" form) */
@@ -180,6 +182,14 @@ int cg_ctx_info(const cg_ctx* c, uint32_t* n_classes, uint64_t* cache_bytes, uin
 /* Synchronise the context's stream, return CG_OK or CG_E_DEVICE, and move the
  * first recorded CG_DEV_* code into *dev_code (may be NULL), clearing it. */
 int cg_ctx_status(cg_ctx* c, uint32_t* dev_code);
+
+/* Compute the bitmask of every mask class now (one CTA per class) instead of
+ * on first use, so that later steps never walk the vocabulary.  Asynchronous
+ * on the context's stream.  The pages exclude such one-time grammar work from
+ * timing by discarding warm-up calls (seedpath.ai "Guided Decoding &
+ * Structured-Output Reliability", "What we measured": fairness controls).
+ * Errors: CG_E_ARG, CG_E_CUDA. */
+int cg_ctx_prefill(cg_ctx* c);
 
 /* Step 1 -- which tokens may follow each row's state (usetacet.com/docs/grammar,
  * "The guarantee"; masks come from pure automaton state ahead of the step,

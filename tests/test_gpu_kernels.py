@@ -51,7 +51,11 @@ def test_fill_bitmask(names, kind, V):
             expect_missing = True
     st = u32(np.where(states < 0, 0xFFFFFFFF, states).astype(np.uint32))
     W = (V + 31) // 32
-    for rep in range(2):  # first call fills the cache, second reads it
+    for rep in range(3):  # first call fills the cache, second reads it, third after prefill
+        if rep == 2:
+            ctx2 = make_ctx(names, kind, V)
+            ctx2.prefill()
+            ctx = ctx2
         bm = empty((B, W), torch.int32)
         ctx.fill_bitmask(st, bm, gid=u16(gid), forced=torch.as_tensor(forced.astype(np.int32)).cuda())
         code = ctx.status()
@@ -203,3 +207,43 @@ def test_device_status_codes():
     assert ctx.status() == 7 and host(out_f)[0] == _lib.CG_FLAG_REJECTED
     ctx.accept(u32([0]), u32([tid[b"c"]]), out_s[:1], out_f[:1])
     assert ctx.status() == 0 and host(out_f)[0] == 0
+
+
+def _topp_rows(V, B, case, rng):
+    x = rng.normal(0, 2, (B, V)).astype(np.float32)
+    masks = rng.random((B, V)) < 0.9
+    if case == "boosted":                       # the throughput workload's distribution
+        x += 4.0 * (rng.random((B, V)) < 0.05)
+    elif case == "sparse":                      # few allowed tokens, small logits: list bisection
+        masks = rng.random((B, V)) < 0.0002
+        masks[:, 7] = True
+    elif case == "flat":                        # nucleus below the candidate margin: general path
+        x = rng.uniform(-1.0, 1.0, (B, V)).astype(np.float32)
+    elif case == "ties":                        # every logit equal: candidate list overflows
+        x[:] = 0.5
+        masks[:] = True
+    import torch as _t
+    xt = _t.from_numpy(x).to(_t.bfloat16)
+    vals = xt.to(_t.float32).numpy().astype(np.float64)
+    return vals, xt.cuda(), masks
+
+
+@pytest.mark.parametrize("case,temp,top_p", [("boosted", 0.7, 0.9), ("boosted", 1.0, 0.5), ("plain", 0.7, 0.9),
+                                            ("sparse", 0.7, 0.9), ("flat", 2.0, 0.999), ("ties", 0.7, 0.9)])
+def test_single_pass_topp_branches(case, temp, top_p):
+    V, B = 128256, 12
+    ctx = make_ctx(("calc_call",), "bpe", V)
+    rng = np.random.default_rng(sum(case.encode()))
+    x, xt, masks = _topp_rows(V, B, case, rng)
+    from oracle.step import pack_bitmask
+    bm = u32(np.stack([pack_bitmask(m) for m in masks]))
+    out = empty((B,), torch.int32)
+    probs = empty((B, V), torch.float32)
+    ctx.mask_and_sample(xt, bm, temp, top_p, 99, 3, out, probs=probs)
+    assert ctx.status() == 0
+    got = host(out).view(np.uint32)
+    gp = host(probs)
+    for b in range(B):
+        res = sample_row(x[b], masks[b], temp, top_p, 99, b, 3)
+        assert same_token(int(got[b]), res), (case, b, got[b], res.tok, res.gap, res.margin, res.nucleus_size)
+        assert np.max(np.abs(gp[b] - res.probs)) <= 1e-5, (case, b)
