@@ -266,42 +266,54 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(void* logits, ui
 }
 
 // ============================================================================
-// Single-pass top-p kernel for bf16 rows (the path of the throughput metric).
+// Top-p kernel for bf16 rows (the path of the throughput metric).  Each logit
+// is read from HBM once; the few groups that can hold nucleus candidates are
+// read a second time from L2.
 //
-// One CTA of 512 threads per row: warp 15 issues bulk asynchronous copies
-// (TMA, cp.async.bulk) of the row into a 4-slot shared-memory ring, warps
-// 0..14 consume the slots.  Slots hand over through mbarriers (full: copy
-// landed; empty: all 15 consumer warps are done), so no block barrier sits in
-// the streaming loop.  The bitmask is applied 8 logits at a time through a
-// 256-entry table of pair masks.  Each consumer thread keeps a running
-// maximum and 8 partial sums of exponentials, and for every 8-logit group one
-// bit records whether the group's maximum reached the block's running maximum
-// minus kMarginZ nats (a warp ballot per 32 groups).  The running maximum never
-// exceeds the final maximum M, so every group holding a logit within the margin
-// of M is flagged.
+// One CTA of 512 threads per row.  Warp 15 fills a kStages-slot shared-memory
+// ring with bulk asynchronous copies (cp.async.bulk, completing on "full"
+// mbarriers; the copies carry an L2 evict_last hint so that the row stays in
+// L2 for the second look).  Warps 0..14 take each chunk from the ring 16 logits
+// per thread (two 8-logit groups): the bitmask is applied through a 256-entry
+// table of pair masks indexed by the group's mask byte, the group maximum is
+// taken with packed bf16 max, and exp2((x - m) c) is summed into 8 partial sums
+// against a reference m that follows the block's running maximum (published
+// per chunk with a warp max-reduction and a shared atomicMax).  A group whose
+// maximum reaches the reference minus kMarginZ nats sets its bit in a per-row
+// flag bitmap (one warp ballot per 32 groups).  The reference never exceeds the
+// final maximum M, so every allowed logit within kMarginZ nats of M lies in a
+// flagged group.
 //
-// After the stream, with M and S = sum exp exact, the flagged groups are read
-// again (from L2) and their allowed logits >= M - margin become the candidate
-// list, kept in the now idle ring.  The nucleus threshold is found among the
-// candidates' keys (per-key counts of the keys just below M, or bisection over
-// the list) as long as they carry at least top_p of the mass, and the Gumbel
-// scores are drawn for the nucleus entries only.  Rows whose list overflows or
-// whose nucleus reaches below the margin run general_row instead.
+// After the stream: M and S = sum exp2((x - M) c) come from the block; the
+// flagged groups are re-read (L2) and their allowed logits >= M - margin become
+// the candidates; the nucleus threshold is the largest key whose upper
+// set carries top_p * S (per-key counts of the candidates, or bisection), and
+// Gumbel scores are drawn for the nucleus entries only.  Rows whose nucleus
+// reaches below the margin, or whose lists overflow, run general_row instead.
 // ============================================================================
 namespace fast {
 
 constexpr int kThreads = 512;
 constexpr uint32_t kConsumerWarps = 15;
 constexpr uint32_t kConsumers = kConsumerWarps * 32;            // 480
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr uint32_t kChunkElems = kConsumers * 16;               // 7680 logits per slot
 constexpr uint32_t kChunkBytes = kChunkElems * 2;               // 15 KiB
 constexpr uint32_t kGroupsPerChunk = kChunkElems / 8;           // 960
-constexpr uint32_t kBins = 448;                                 // keys per histogram (one per thread)
-constexpr uint32_t kRing = kStages * kChunkBytes;               // 60 KiB
-constexpr uint32_t kCap = (kRing - 16 * kBins * 4) / 6;         // candidate ids (u32) + keys (u16)
-static_assert(kBins <= kThreads, "one histogram key per thread");
+constexpr uint32_t kWordsPerChunk = kGroupsPerChunk / 32;       // 30 flag words
+constexpr uint32_t kRing = kStages * kChunkBytes;               // 75 KiB
+// after the stream the ring holds the candidate list, then the key histograms
+// (later the packed nucleus entries)
+constexpr uint32_t kCap = 10000;                                // candidates (u32 id + u16 key)
+constexpr uint32_t kBins = 512;                                 // keys per histogram
+constexpr uint32_t kHists = 8;                                  // histogram copies
+constexpr uint32_t kHistOff = (kCap * 6 + 127) / 128 * 128;
+constexpr uint32_t kNucCap = kHists * kBins * 2;                // packed nucleus entries (u16)
+static_assert(kHistOff + kHists * kBins * 4 <= kRing, "histograms must fit the ring");
+constexpr int kBatch = 8;                                       // flagged groups loaded per round
 constexpr float kMarginZ = 9.5f;                                // nats below the maximum kept as candidates
+constexpr float kRefJump = 60.f;                                // logit/temp units a reference may lag
+constexpr float kNoRef = -1e30f;                                // finite reference before any allowed logit
 constexpr uint32_t kWaitLimit = 1u << 22;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -317,11 +329,16 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+      "%4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
       : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
@@ -361,28 +378,51 @@ __device__ __forceinline__ uint4 apply_mask(uint4 v, uint4 pm) {
 }
 __device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float group_max(const uint4& v) {
+  const uint32_t mx = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
+  return fmaxf(lo_f(mx), hi_f(mx));
+}
+__device__ __forceinline__ void add_exps(float* acc, const uint4& v, float c, float mc) {
+  acc[0] += ex2(fmaf(lo_f(v.x), c, -mc));
+  acc[1] += ex2(fmaf(hi_f(v.x), c, -mc));
+  acc[2] += ex2(fmaf(lo_f(v.y), c, -mc));
+  acc[3] += ex2(fmaf(hi_f(v.y), c, -mc));
+  acc[4] += ex2(fmaf(lo_f(v.z), c, -mc));
+  acc[5] += ex2(fmaf(hi_f(v.z), c, -mc));
+  acc[6] += ex2(fmaf(lo_f(v.w), c, -mc));
+  acc[7] += ex2(fmaf(hi_f(v.w), c, -mc));
+}
+
+__device__ __forceinline__ void issue_chunk(unsigned char* ring, uint64_t* full, const char* row, uint32_t V,
+                                            uint32_t k, uint64_t pol) {
+  const uint32_t slot = k % kStages;
+  const uint32_t bytes = min(kChunkElems, V - k * kChunkElems) * 2;
+  mbar_expect_tx(full + slot, bytes);
+  bulk_g2s(ring + size_t(slot) * kChunkBytes, row + size_t(k) * kChunkBytes, bytes, full + slot, pol);
+}
 
 __global__ void __launch_bounds__(kThreads, 2)
     stream_topp_kernel(void* logits, uint32_t V, uint32_t W, const uint32_t* __restrict__ bitmask, float temp,
                        float top_p, uint32_t k0, uint32_t k1, uint32_t step, uint32_t* __restrict__ out_tok,
                        float* __restrict__ probs, int inplace, uint32_t* status) {
   extern __shared__ __align__(128) unsigned char dsm[];
-  unsigned char* ring = dsm;                                               // kStages slots
-  uint4* lut = reinterpret_cast<uint4*>(dsm + kRing);                      // [256]
-  uint32_t* smask = reinterpret_cast<uint32_t*>(dsm + kRing + 4096);       // [W]
-  uint32_t* gflags = smask + ((W + 3) & ~3u);                              // one bit per 8-logit group
+  unsigned char* ring = dsm;                                                // kStages slots
+  uint4* lut = reinterpret_cast<uint4*>(dsm + kRing);                       // [256]
+  uint32_t* smask = reinterpret_cast<uint32_t*>(lut + 256);                 // [W]
+  const uint32_t nchunks = (V + kChunkElems - 1) / kChunkElems;
+  const uint32_t nfw = nchunks * kWordsPerChunk;
+  uint32_t* fbits = smask + ((W + 3) & ~3u);                                // [nfw] flag bitmap
+  // after the stream
+  uint32_t* cid = reinterpret_cast<uint32_t*>(ring);                        // [kCap]
+  uint16_t* ckey = reinterpret_cast<uint16_t*>(ring + kCap * 4);            // [kCap]
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
   __shared__ float red_f[33];
   __shared__ double red_d[33];
   __shared__ unsigned long long red_u64[33];
-  __shared__ uint32_t red_u[33];
-  __shared__ uint32_t s_maxkey, s_count, s_flag, s_tau, s_groups;
+  __shared__ uint32_t s_maxkey, s_flag, s_count, s_tau;
 
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, b = blockIdx.x;
   char* row = reinterpret_cast<char*>(logits) + size_t(b) * V * 2;
-  const uint32_t nchunks = (V + kChunkElems - 1) / kChunkElems;
-  const uint32_t ngroups = V / 8;
-  const uint32_t nwords = (ngroups + 31) / 32;
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -391,8 +431,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_maxkey = fkey(-INFINITY);
-    s_count = 0;
     s_flag = 0;  // bit 0: a wait ran out
+    s_count = 0;
   }
   for (uint32_t i = tid; i < 256; i += kThreads) {
     uint32_t w[4];
@@ -403,100 +443,93 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   const uint32_t* mrow = bitmask + size_t(b) * W;
   for (uint32_t i = tid; i < W; i += kThreads) smask[i] = mrow[i];
-  for (uint32_t i = tid; i < nwords; i += kThreads) gflags[i] = 0u;
   __syncthreads();
 
   const float c = 1.4426950408889634f / temp;
   const float margin = kMarginZ * temp;  // z = x / temp: kMarginZ nats are kMarginZ * temp logit units
-  float mt = -INFINITY;
+  const uint8_t* smask8 = reinterpret_cast<const uint8_t*>(smask);
+  float mt = kNoRef;  // this thread's reference (never above the row maximum)
   float acc[kAcc];
 #pragma unroll
   for (int j = 0; j < kAcc; ++j) acc[j] = 0.f;
 
   if (warp == kConsumerWarps) {
-    // ---- producer: one lane keeps the ring full -------------------------------
+    // ---- producer warp --------------------------------------------------------------
     if (lane == 0) {
+      const uint64_t pol = l2_evict_last_policy();
+      bool ok = true;
       for (uint32_t k = 0; k < nchunks; ++k) {
-        const uint32_t slot = k % kStages;
-        if (k >= uint32_t(kStages) && !mbar_wait(empty + slot, ((k / kStages) - 1) & 1u)) {
-          atomicOr(&s_flag, 1u);
+        if (k >= uint32_t(kStages) && !mbar_wait(empty + k % kStages, ((k / kStages) - 1) & 1u)) {
+          ok = false;
           break;
         }
-        const uint32_t bytes = min(kChunkElems, V - k * kChunkElems) * 2;
-        mbar_expect_tx(full + slot, bytes);
-        bulk_g2s(ring + size_t(slot) * kChunkBytes, row + size_t(k) * kChunkBytes, bytes, full + slot);
+        issue_chunk(ring, full, row, V, k, pol);
       }
+      if (!ok) atomicOr(&s_flag, 1u);
     }
   } else {
     // ---- consumers ----------------------------------------------------------------
-    // chunk 0's maximum seeds the flag threshold, so the first chunk does not
-    // flag every group
+    // chunk 0's maximum seeds the reference, so the first chunk does not flag
+    // every group
     if (!mbar_wait(full + 0, 0)) atomicOr(&s_flag, 1u);
     {
       const uint4* r4 = reinterpret_cast<const uint4*>(ring);
       float lm = -INFINITY;
 #pragma unroll
       for (uint32_t g = 0; g < 2; ++g) {
-        const uint32_t gi = tid + kConsumers * g, t0 = gi * 8;
-        if (t0 < V) {
-          const uint4 v = apply_mask(r4[gi], lut[(smask[t0 >> 5] >> (t0 & 31)) & 0xFFu]);
-          const uint32_t mx = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
-          lm = fmaxf(lm, fmaxf(lo_f(mx), hi_f(mx)));
-        }
+        const uint32_t gi = tid + kConsumers * g;
+        if (gi * 8 < V) lm = fmaxf(lm, group_max(apply_mask(r4[gi], lut[smask8[gi]])));
       }
-      lm = warp_reduce(lm, MaxOp());
-      if (lane == 0 && lm > -INFINITY) atomicMax(&s_maxkey, fkey(lm));
+      const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, fkey(lm));
+      if (lane == 0) atomicMax(&s_maxkey, wk);
       asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");  // consumer warps only
     }
-    float thr = fmaxf(fkey_inv(*reinterpret_cast<volatile uint32_t*>(&s_maxkey)) - margin, -3.402823466e38f);
     for (uint32_t k = 0; k < nchunks; ++k) {
       const uint32_t slot = k % kStages;
+      // reference for this chunk: the block's running maximum
+      const float mref = fkey_inv(*reinterpret_cast<volatile uint32_t*>(&s_maxkey));
+      if (mref > mt) {
+        const float r = ex2((mt - mref) * c);
+#pragma unroll
+        for (int j = 0; j < kAcc; ++j) acc[j] *= r;
+        mt = mref;
+      }
+      const float thr = mt - margin;
       if (!mbar_wait(full + slot, (k / kStages) & 1u)) {
         atomicOr(&s_flag, 1u);
         break;
       }
       const uint4* r4 = reinterpret_cast<const uint4*>(ring + size_t(slot) * kChunkBytes);
-      const uint32_t base = k * kChunkElems;
-      float wmax = -INFINITY;
+      const uint32_t gbase = k * kGroupsPerChunk;  // row group index of the chunk's group 0
+      const uint32_t gi0 = tid, gi1 = tid + kConsumers;
+      const uint32_t ngroups = min(kGroupsPerChunk, V / 8 - gbase);
+      uint4 v0 = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u), v1 = v0;
+      if (gi0 < ngroups) v0 = apply_mask(r4[gi0], lut[smask8[gbase + gi0]]);
+      if (gi1 < ngroups) v1 = apply_mask(r4[gi1], lut[smask8[gbase + gi1]]);
+      const float g0 = group_max(v0), g1 = group_max(v1);
+      const float gm = fmaxf(g0, g1);
+      if (gm > mt + kRefJump * temp) {
+        // far above the reference (or the first allowed logits): move this
+        // thread's reference before the sums can overflow
+        const float r = ex2((mt - gm) * c);
 #pragma unroll
-      for (uint32_t g = 0; g < 2; ++g) {
-        const uint32_t gi = tid + kConsumers * g, t0 = base + gi * 8;
-        bool flag = false;
-        if (t0 < V) {
-          const uint4 v = apply_mask(r4[gi], lut[(smask[t0 >> 5] >> (t0 & 31)) & 0xFFu]);
-          const uint32_t mx = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
-          const float gmax = fmaxf(lo_f(mx), hi_f(mx));
-          wmax = fmaxf(wmax, gmax);
-          if (gmax > -INFINITY) {
-            if (gmax > mt) {
-              const float r = ex2((mt - gmax) * c);
-#pragma unroll
-              for (int j = 0; j < kAcc; ++j) acc[j] *= r;
-              mt = gmax;
-            }
-            const float mc = mt * c;
-            acc[0] += ex2(fmaf(lo_f(v.x), c, -mc));
-            acc[1] += ex2(fmaf(hi_f(v.x), c, -mc));
-            acc[2] += ex2(fmaf(lo_f(v.y), c, -mc));
-            acc[3] += ex2(fmaf(hi_f(v.y), c, -mc));
-            acc[4] += ex2(fmaf(lo_f(v.z), c, -mc));
-            acc[5] += ex2(fmaf(hi_f(v.z), c, -mc));
-            acc[6] += ex2(fmaf(lo_f(v.w), c, -mc));
-            acc[7] += ex2(fmaf(hi_f(v.w), c, -mc));
-            flag = gmax >= thr;
-          }
-        }
-        // group index of this lane = k * 960 + 480 g + tid: 32 consecutive groups per warp
-        const unsigned bits = __ballot_sync(0xFFFFFFFFu, flag);
-        if (lane == 0 && bits) gflags[k * (kGroupsPerChunk / 32) + g * (kConsumers / 32) + warp] = bits;
+        for (int j = 0; j < kAcc; ++j) acc[j] *= r;
+        mt = gm;
       }
-      const float wm = warp_reduce(wmax, MaxOp());
+      const float mc = mt * c;
+      add_exps(acc, v0, c, mc);
+      add_exps(acc, v1, c, mc);
+      // chunk-local group of this lane = 480 g + tid = 32 * (15 g + warp) + lane
+      const unsigned b0 = __ballot_sync(0xFFFFFFFFu, g0 >= thr);
+      const unsigned b1 = __ballot_sync(0xFFFFFFFFu, g1 >= thr);
+      const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, fkey(gm));
       __syncwarp();
       if (lane == 0) {
+        fbits[k * kWordsPerChunk + warp] = b0;
+        fbits[k * kWordsPerChunk + kConsumerWarps + warp] = b1;
+        atomicMax(&s_maxkey, wk);
         mbar_arrive(empty + slot);
-        if (wm > -INFINITY) atomicMax(&s_maxkey, fkey(wm));
       }
-      thr = fkey_inv(*reinterpret_cast<volatile uint32_t*>(&s_maxkey)) - margin;
     }
   }
   __syncthreads();
@@ -510,125 +543,88 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_wait(full + sl, (issued - 1) & 1u);
     }
   }
-  const float M = block_reduce(mt, MaxOp(), -INFINITY, red_f);
-  double part = 0.0;
-  if (mt > -INFINITY) {
-    float a = 0.f;
+  const float M = fkey_inv(s_maxkey);  // -inf when no logit is allowed
+  // S: per-thread partial sums in float (each already a float sum), warp sums
+  // in float, the 16 warp sums in double
+  {
+    float part = 0.f;
+    if (M > -INFINITY) {
+      float a = 0.f;
 #pragma unroll
-    for (int j = 0; j < kAcc; ++j) a += acc[j];
-    part = double(a) * double(ex2((mt - M) * c));
+      for (int jj = 0; jj < kAcc; ++jj) a += acc[jj];
+      if (a > 0.f) part = a * ex2((mt - M) * c);
+    }
+    part = warp_reduce(part, SumOp());
+    if (lane == 0) red_f[warp] = part;
   }
-  const double S = block_reduce(part, SumOp(), 0.0, red_d);
+  __syncthreads();
+  double S = 0.0;
+  for (uint32_t wi = 0; wi < kThreads / 32; ++wi) S += double(red_f[wi]);
   uint32_t tok = CG_NO_TOKEN;
   bool general = false;
   if (s_flag & 1u) {
     if (tid == 0) record_error(status, CG_DEV_TIMEOUT);
-  } else if (M > -INFINITY) {
-    const double target = double(top_p) * S;
-    const float thrF = M - margin;  // every allowed logit >= thrF sits in a flagged group
-    uint32_t kthr = fkey(thrF) >> 16;
-    if (bf16key_to_float(kthr) < thrF) ++kthr;
-    const uint32_t km = fkey(M) >> 16;
-    // ring reuse: per-warp key histograms, then the candidate ids and keys
-    uint32_t* wbins = reinterpret_cast<uint32_t*>(ring);                     // [16][kBins]
-    uint32_t* cid = wbins + 16 * kBins;                                      // [kCap]
-    uint16_t* ckey = reinterpret_cast<uint16_t*>(cid + kCap);                // [kCap]
-    const bool use_bins = km - kthr < kBins;
-    if (use_bins)
-      for (uint32_t i = tid; i < 16 * kBins; i += kThreads) wbins[i] = 0u;
-    if (tid == 0) s_count = 0u;
-    // ---- candidates: allowed logits >= thrF of the flagged groups ----------------
-    // flagged groups are numbered through an exclusive prefix over the flag
-    // words; in batch k, thread t takes groups k * 2048 + t + 512 r (r < 4), so
-    // every warp runs the same number of batches and reserves list space once
-    // per batch
-    uint32_t* wpre = gflags + nwords;  // [nwords] flagged groups before each word
-    {
-      // thread t owns words 3t .. 3t+2; block-wide exclusive scan of the counts
-      const uint32_t w0 = 3 * tid;
-      const uint32_t c0 = w0 < nwords ? __popc(gflags[w0]) : 0u;
-      const uint32_t c1 = w0 + 1 < nwords ? __popc(gflags[w0 + 1]) : 0u;
-      const uint32_t c2 = w0 + 2 < nwords ? __popc(gflags[w0 + 2]) : 0u;
-      const uint32_t mine = c0 + c1 + c2;
-      uint32_t incl = mine;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= uint32_t(o)) incl += y;
-      }
-      if (lane == 31) red_u[warp] = incl;
-      __syncthreads();
-      uint32_t before = 0;
-      for (uint32_t wi = 0; wi < warp; ++wi) before += red_u[wi];
-      const uint32_t ex = before + incl - mine;
-      if (w0 < nwords) wpre[w0] = ex;
-      if (w0 + 1 < nwords) wpre[w0 + 1] = ex + c0;
-      if (w0 + 2 < nwords) wpre[w0 + 2] = ex + c0 + c1;
-      if (tid == kThreads - 1) s_groups = ex + mine;
-      __syncthreads();
-    }
-    const uint32_t G = s_groups;
+  } else if (!(M > -1e29f && M < 1e29f)) {
+    general = M > -INFINITY;  // huge or infinite logits: the plain path copes with them
+  } else {
+    // ---- candidates: allowed logits >= M - margin, read again (from L2) in the
+    // flagged groups.  Thread t takes flag words t, t + 512, ...; per round it
+    // loads up to kBatch of its flagged groups, then the warp reserves room for
+    // all their hits with one shared atomic.
+    const float thrF = M - margin;
     const uint4* g4 = reinterpret_cast<const uint4*>(row);
-    uint32_t* mybins = wbins + warp * kBins;
-    for (uint32_t base = 0; base < G; base += 4 * kThreads) {
-      uint4 v[4];
-      uint32_t gidx[4];
+    for (uint32_t w0 = 0; w0 < nfw; w0 += kThreads) {
+      const uint32_t w = w0 + tid;
+      uint32_t bits = w < nfw ? fbits[w] : 0u;
+      while (__any_sync(0xFFFFFFFFu, bits != 0u)) {
+        uint4 v[kBatch];
+        uint32_t gsel[kBatch];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const uint32_t idx = base + tid + r * kThreads;
-        gidx[r] = 0xFFFFFFFFu;
-        v[r] = make_uint4(0u, 0u, 0u, 0u);
-        if (idx < G) {
-          // last word whose prefix is <= idx
-          uint32_t lo = 0, hi = nwords - 1;
-          while (lo < hi) {
-            const uint32_t mid = (lo + hi + 1) >> 1;
-            if (wpre[mid] <= idx) lo = mid; else hi = mid - 1;
-          }
-          const uint32_t bit = __fns(gflags[lo], 0, int(idx - wpre[lo] + 1));
-          gidx[r] = lo * 32 + bit;
-          v[r] = ld_stream(g4 + gidx[r]);
-        }
-      }
-      uint32_t hits = 0;  // bit r * 8 + j: logit j of group r is a candidate
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        if (gidx[r] != 0xFFFFFFFFu) {
-          const uint32_t t0 = gidx[r] * 8;
-          v[r] = apply_mask(v[r], lut[(smask[t0 >> 5] >> (t0 & 31)) & 0xFFu]);
-          const uint32_t ww[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float f = (j & 1) ? hi_f(ww[j >> 1]) : lo_f(ww[j >> 1]);
-            hits |= (f >= thrF ? 1u : 0u) << (r * 8 + j);
+        for (int u = 0; u < kBatch; ++u) {
+          gsel[u] = kNotFound;
+          if (bits) {
+            gsel[u] = w * 32 + (__ffs(bits) - 1);
+            bits &= bits - 1;
+            v[u] = ld_stream(g4 + gsel[u]);
           }
         }
-      }
-      const uint32_t nh = __popc(hits);
-      uint32_t incl = nh;
+        uint32_t hits[kBatch];
+        uint32_t nh = 0;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= uint32_t(o)) incl += y;
-      }
-      const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-      uint32_t wb = 0;
-      if (lane == 31 && total) wb = atomicAdd(&s_count, total);
-      uint32_t pos = __shfl_sync(0xFFFFFFFFu, wb, 31) + incl - nh;
+        for (int u = 0; u < kBatch; ++u) {
+          hits[u] = 0;
+          if (gsel[u] != kNotFound) {
+            v[u] = apply_mask(v[u], lut[smask8[gsel[u]]]);
+            const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const uint32_t ww[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+            for (int q = 0; q < 4; ++q) {
+              hits[u] |= uint32_t(lo_f(wv[q]) >= thrF) << (2 * q);
+              hits[u] |= uint32_t(hi_f(wv[q]) >= thrF) << (2 * q + 1);
+            }
+            nh += __popc(hits[u]);
+          }
+        }
+        uint32_t inc = nh;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if ((hits >> (r * 8 + j)) & 1u) {
-            const float f = (j & 1) ? hi_f(ww[j >> 1]) : lo_f(ww[j >> 1]);
-            const uint32_t key = fkey(f) >> 16;
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+          if (lane >= uint32_t(o)) inc += y;
+        }
+        uint32_t wb = 0;
+        if (lane == 31 && inc) wb = atomicAdd(&s_count, inc);
+        uint32_t pos = __shfl_sync(0xFFFFFFFFu, wb, 31) + inc - nh;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          uint32_t h = hits[u];
+          while (h) {
+            const uint32_t e = __ffs(h) - 1;
+            h &= h - 1;
             if (pos < kCap) {
-              cid[pos] = gidx[r] * 8 + j;
-              ckey[pos] = uint16_t(key);
+              const uint32_t wd = e < 4 ? (e < 2 ? v[u].x : v[u].y) : (e < 6 ? v[u].z : v[u].w);
+              cid[pos] = gsel[u] * 8 + e;
+              ckey[pos] = uint16_t(fkey((e & 1u) ? hi_f(wd) : lo_f(wd)) >> 16);
             }
             ++pos;
-            if (use_bins) atomicAdd(mybins + (km - key), 1u);
           }
         }
       }
@@ -636,34 +632,45 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
     const uint32_t n_all = s_count;
     const uint32_t n = min(n_all, kCap);
+    const double target = double(top_p) * S;
+    uint32_t kthr = fkey(thrF) >> 16;  // every allowed logit with key >= kthr is a candidate
+    if (bf16key_to_float(kthr) < thrF) ++kthr;
+    const uint32_t km = fkey(M) >> 16;
     const double fx = 1099511627776.0;  // masses in 2^-40 units: exact sums, no rounding order
     const unsigned long long target_q = (unsigned long long)(target * fx);
     uint32_t tau = kNotFound;
+    uint32_t* hb = reinterpret_cast<uint32_t*>(ring + kHistOff);
     if (n_all > kCap) {
       general = true;
-    } else if (use_bins) {
-      // per-key totals, mass from the top (bin j is key km - j), block-wide
-      // prefix sum, first bin where the upper set reaches the target
+    } else if (km - kthr < kBins) {
+      // per-key counts (kHists histograms, warp w counts into histogram
+      // w % kHists), mass from the top (bin j is key km - j), block-wide prefix
+      // sum, first bin where the upper set reaches the target
+      for (uint32_t i = tid; i < kHists * kBins; i += kThreads) hb[i] = 0u;
+      __syncthreads();
+      uint32_t* mine = hb + (warp % kHists) * kBins;
+      for (uint32_t i = tid; i < n; i += kThreads) atomicAdd(mine + (km - ckey[i]), 1u);
+      __syncthreads();
       const uint32_t L = km - kthr + 1;
       unsigned long long q = 0;
       if (tid < L) {
         uint32_t cnt = 0;
 #pragma unroll
-        for (int w = 0; w < 16; ++w) cnt += wbins[w * kBins + tid];
+        for (uint32_t hw = 0; hw < kHists; ++hw) cnt += hb[hw * kBins + tid];
         if (cnt) q = (unsigned long long)(double(cnt) * double(ex2((bf16key_to_float(km - tid) - M) * c)) * fx);
       }
-      unsigned long long incl = q;
+      unsigned long long qi = q;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= uint32_t(o)) incl += y;
+        const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, qi, o);
+        if (lane >= uint32_t(o)) qi += y;
       }
-      if (lane == 31) red_u64[warp] = incl;
+      if (lane == 31) red_u64[warp] = qi;
       if (tid == 0) s_tau = kNotFound;
       __syncthreads();
       unsigned long long before = 0;
       for (uint32_t wi = 0; wi < warp; ++wi) before += red_u64[wi];
-      if (tid < L && before + incl >= target_q) atomicMin(&s_tau, tid);
+      if (tid < L && before + qi >= target_q) atomicMin(&s_tau, tid);
       __syncthreads();
       tau = s_tau == kNotFound ? kNotFound : km - s_tau;
       general = tau == kNotFound;
@@ -689,13 +696,37 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
     if (!general) {
+      // nucleus entries (candidate indices) packed densely, so that the Philox
+      // draws spread over all threads; entries past kNucCap are scored in place
+      uint16_t* nuc = reinterpret_cast<uint16_t*>(ring + kHistOff);
+      if (tid == 0) s_count = 0;
+      __syncthreads();
       unsigned long long best = 0ull;
-      for (uint32_t i = tid; i < n; i += kThreads) {
-        const uint32_t key = ckey[i];
-        if (key < tau) continue;
+      for (uint32_t i0 = 0; i0 < n; i0 += kThreads) {
+        const uint32_t i = i0 + tid;
+        const bool in = i < n && ckey[i] >= tau;
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, in);
+        uint32_t wb = 0;
+        if (lane == 0 && bal) wb = atomicAdd(&s_count, __popc(bal));
+        const uint32_t pos = __shfl_sync(0xFFFFFFFFu, wb, 0) + __popc(bal & ((1u << lane) - 1u));
+        if (in) {
+          if (pos < kNucCap) {
+            nuc[pos] = uint16_t(i);
+          } else {
+            const uint32_t id = cid[i];
+            const uint4 blk = philox4x32_10(make_uint4(id >> 2, b, step, 0u), k0, k1);
+            const float score = __fdiv_rn(bf16key_to_float(ckey[i]), temp) + gumbel_from_word(philox_word(blk, id & 3u));
+            best = max(best, pack_best(score, id));
+          }
+        }
+      }
+      __syncthreads();
+      const uint32_t nn = min(s_count, kNucCap);
+      for (uint32_t j = tid; j < nn; j += kThreads) {
+        const uint32_t i = nuc[j];
         const uint32_t id = cid[i];
         const uint4 blk = philox4x32_10(make_uint4(id >> 2, b, step, 0u), k0, k1);
-        const float score = __fdiv_rn(bf16key_to_float(key), temp) + gumbel_from_word(philox_word(blk, id & 3u));
+        const float score = __fdiv_rn(bf16key_to_float(ckey[i]), temp) + gumbel_from_word(philox_word(blk, id & 3u));
         best = max(best, pack_best(score, id));
       }
       best = block_reduce(best, MaxOp(), 0ull, red_u64);
@@ -711,6 +742,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   if (tid == 0) out_tok[b] = tok;
   if (probs || inplace) write_outputs<true, kTopP>(row, V, smask, tok, M, S, temp, probs, inplace, b);
+}
+
+size_t stream_smem(uint32_t V, uint32_t W) {
+  const uint32_t nchunks = (V + kChunkElems - 1) / kChunkElems;
+  return size_t(kRing) + 4096 + size_t((W + 3) & ~3u) * 4 + size_t(nchunks) * kWordsPerChunk * 4;
 }
 
 }  // namespace fast
@@ -751,14 +787,13 @@ cudaError_t launch_mask_and_sample(void* logits, int dtype, uint32_t B, uint32_t
   const bool bf16 = dtype == CG_BF16;
   const uint32_t ch = bf16 ? 8u : 4u;
   const bool vec = (V % ch == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
-  const size_t fast_smem = size_t(fast::kRing) + 4096 + ((size_t(W) + 3) & ~size_t(3)) * 4 +
-                           2 * size_t((V / 8 + 31) / 32) * 4;
-  if (bf16 && vec && mode == kTopP && fast_smem <= 110 * 1024 && (V / 8 + 31) / 32 <= 3 * 512) {
-    auto* k = fast::stream_topp_kernel;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(fast_smem));
+  const size_t s1 = fast::stream_smem(V, W);
+  if (bf16 && vec && mode == kTopP && s1 <= 112 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(fast::stream_topp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(s1));
     if (e != cudaSuccess) return e;
-    k<<<B, fast::kThreads, fast_smem, stream>>>(logits, V, W, bitmask, temp, top_p, uint32_t(seed),
-                                                uint32_t(seed >> 32), step, out_tok, probs, inplace, status);
+    fast::stream_topp_kernel<<<B, fast::kThreads, s1, stream>>>(logits, V, W, bitmask, temp, top_p, uint32_t(seed),
+                                                               uint32_t(seed >> 32), step, out_tok, probs, inplace,
+                                                               status);
     return cudaGetLastError();
   }
   if (bf16)
