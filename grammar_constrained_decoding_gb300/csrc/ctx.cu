@@ -15,8 +15,9 @@ size_t fill_bitmask_smem(uint32_t W);
 cudaError_t launch_prefill(const Tables& t, const uint32_t* class_rep, const uint16_t* class_gid, cudaStream_t stream);
 cudaError_t launch_mask_and_sample(void* logits, int dtype, uint32_t B, uint32_t V, uint32_t W,
                                    const uint32_t* bitmask, float temp, float top_p, uint64_t seed, uint32_t step,
-                                   uint32_t* out_tok, float* probs, int inplace, uint32_t* status,
+                                   uint32_t* out_tok, float* probs, int inplace, void* scratch, uint32_t* status,
                                    cudaStream_t stream);
+size_t sample_scratch_bytes(uint32_t B, uint32_t V);
 cudaError_t launch_accept(const Tables& t, const uint32_t* states, const uint16_t* gid, const uint32_t* toks,
                           const int32_t* forced, uint32_t B, uint32_t* counts, uint32_t max_tokens,
                           uint32_t* out_states, uint8_t* out_flags, cudaStream_t stream);
@@ -30,6 +31,8 @@ struct cg_ctx {
   uint64_t cache_bytes = 0;
   const uint32_t* class_rep = nullptr;   // representative state of each mask class
   const uint16_t* class_gid = nullptr;   // grammar of each mask class
+  void* sample_scratch = nullptr;        // candidate lists of the sampling kernel
+  size_t sample_scratch_bytes = 0;
 };
 
 namespace {
@@ -48,6 +51,9 @@ cudaError_t upload(cg_ctx* c, const std::vector<T>& host, T** dev) {
 void release(cg_ctx* c) {
   for (void* p : c->allocations) cudaFree(p);
   c->allocations.clear();
+  if (c->sample_scratch) cudaFree(c->sample_scratch);
+  c->sample_scratch = nullptr;
+  c->sample_scratch_bytes = 0;
 }
 
 }  // namespace
@@ -198,9 +204,20 @@ int cg_mask_and_sample(cg_ctx* c, void* d_logits, int dtype, uint32_t B, uint32_
   if (dtype != CG_F32 && dtype != CG_BF16) return CG_E_ARG;
   if (V != c->t.V || !(temp >= 0.f) || temp == INFINITY || !(top_p == top_p)) return CG_E_ARG;
   if (flags & ~CG_SAMPLE_INPLACE) return CG_E_ARG;
+  const size_t need = cgk::sample_scratch_bytes(B, V);
+  if (need > c->sample_scratch_bytes) {
+    // grown once per larger batch (outside any stream capture): the kernels
+    // still queued on the stream may use the old buffer
+    if (cudaStreamSynchronize(c->stream) != cudaSuccess) return CG_E_CUDA;
+    if (c->sample_scratch) cudaFree(c->sample_scratch);
+    c->sample_scratch = nullptr;
+    c->sample_scratch_bytes = 0;
+    if (cudaMalloc(&c->sample_scratch, need) != cudaSuccess) return CG_E_NOMEM;
+    c->sample_scratch_bytes = need;
+  }
   return cgk::launch_mask_and_sample(d_logits, dtype, B, V, c->t.W, d_bitmask, temp, top_p, seed, step, d_out_tok,
-                                     d_probs, (flags & CG_SAMPLE_INPLACE) ? 1 : 0, c->t.status, c->stream) ==
-                 cudaSuccess
+                                     d_probs, (flags & CG_SAMPLE_INPLACE) ? 1 : 0, c->sample_scratch, c->t.status,
+                                     c->stream) == cudaSuccess
              ? CG_OK
              : CG_E_CUDA;
 }

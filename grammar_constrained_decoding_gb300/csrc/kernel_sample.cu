@@ -266,55 +266,57 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(void* logits, ui
 }
 
 // ============================================================================
-// Top-p kernel for bf16 rows (the path of the throughput metric).  Each logit
-// is read from HBM once; the few groups that can hold nucleus candidates are
-// read a second time from L2.
+// Top-p kernel for bf16 rows (the path of the throughput metric): each logit is
+// read from HBM once.
 //
 // One CTA of 512 threads per row.  Warp 15 fills a kStages-slot shared-memory
-// ring with bulk asynchronous copies (cp.async.bulk, completing on "full"
-// mbarriers; the copies carry an L2 evict_last hint so that the row stays in
-// L2 for the second look).  Warps 0..14 take each chunk from the ring 16 logits
-// per thread (two 8-logit groups): the bitmask is applied through a 256-entry
-// table of pair masks indexed by the group's mask byte, the group maximum is
-// taken with packed bf16 max, and exp2((x - m) c) is summed into 8 partial sums
-// against a reference m that follows the block's running maximum (published
-// per chunk with a warp max-reduction and a shared atomicMax).  A group whose
-// maximum reaches the reference minus kMarginZ nats sets its bit in a per-row
-// flag bitmap (one warp ballot per 32 groups).  The reference never exceeds the
-// final maximum M, so every allowed logit within kMarginZ nats of M lies in a
-// flagged group.
+// ring with bulk asynchronous copies (cp.async.bulk completing on "full"
+// mbarriers; slots come back through "empty" mbarriers).  Warps 0..14 take each
+// chunk 16 logits per thread (two 8-logit groups): the bitmask is applied
+// through a 256-entry table of pair masks indexed by the group's mask byte, the
+// group maximum comes from packed bf16 max, and exp2((x - m) c) is summed into
+// 8 partial sums against a reference m that follows the block's running
+// maximum (published per chunk by a warp max-reduction and a shared
+// atomicMax).  A group whose maximum reaches the reference minus kMarginZ nats
+// is copied, masked, into its warp's staging area in shared memory (positions
+// from a warp ballot); whenever 32 groups are staged the warp turns them into
+// candidates -- allowed logits at or above the block's running maximum minus
+// the margin -- one group per lane, and appends them (id, 16-bit key) to the
+// row's candidate list in global memory.  The references never exceed the
+// final maximum M, so every allowed logit within kMarginZ nats of M becomes a
+// candidate.
 //
 // After the stream: M and S = sum exp2((x - M) c) come from the block; the
-// flagged groups are re-read (L2) and their allowed logits >= M - margin become
-// the candidates; the nucleus threshold is the largest key whose upper
-// set carries top_p * S (per-key counts of the candidates, or bisection), and
-// Gumbel scores are drawn for the nucleus entries only.  Rows whose nucleus
-// reaches below the margin, or whose lists overflow, run general_row instead.
+// nucleus threshold tau is the largest key whose upper set carries top_p * S
+// (per-key counts over the candidates, by keys or by coarse bins then keys);
+// the nucleus entries are packed into shared memory and Gumbel scores drawn
+// for them only.  Rows whose nucleus reaches below the margin, or whose list
+// overflows, run general_row instead.
 // ============================================================================
 namespace fast {
 
 constexpr int kThreads = 512;
 constexpr uint32_t kConsumerWarps = 15;
 constexpr uint32_t kConsumers = kConsumerWarps * 32;            // 480
-constexpr int kStages = 5;
+constexpr int kStages = 4;
 constexpr uint32_t kChunkElems = kConsumers * 16;               // 7680 logits per slot
 constexpr uint32_t kChunkBytes = kChunkElems * 2;               // 15 KiB
 constexpr uint32_t kGroupsPerChunk = kChunkElems / 8;           // 960
-constexpr uint32_t kWordsPerChunk = kGroupsPerChunk / 32;       // 30 flag words
-constexpr uint32_t kRing = kStages * kChunkBytes;               // 75 KiB
-// after the stream the ring holds the candidate list, then the key histograms
-// (later the packed nucleus entries)
-constexpr uint32_t kCap = 10000;                                // candidates (u32 id + u16 key)
-constexpr uint32_t kBins = 512;                                 // keys per histogram
-constexpr uint32_t kHists = 8;                                  // histogram copies
-constexpr uint32_t kHistOff = (kCap * 6 + 127) / 128 * 128;
-constexpr uint32_t kNucCap = kHists * kBins * 2;                // packed nucleus entries (u16)
-static_assert(kHistOff + kHists * kBins * 4 <= kRing, "histograms must fit the ring");
-constexpr int kBatch = 8;                                       // flagged groups loaded per round
-constexpr float kMarginZ = 9.5f;                                // nats below the maximum kept as candidates
+constexpr uint32_t kRing = kStages * kChunkBytes;               // 60 KiB
+constexpr uint32_t kStage = 64;                                 // staged groups per warp
+constexpr uint32_t kBins = 512;                                 // bins per histogram
+constexpr uint32_t kHists = 4;                                  // histogram copies
+static_assert(kBins == kThreads, "one histogram bin per thread in the scans");
+// after the stream the ring holds the histograms, then the packed nucleus
+constexpr uint32_t kHistBytes = kHists * kBins * 8;
+constexpr uint32_t kNucCap = (kRing - kHistBytes) / 6;          // packed nucleus entries (u32 id + u16 key)
+constexpr float kMarginZ = 9.0f;                                // nats below the maximum kept as candidates
 constexpr float kRefJump = 60.f;                                // logit/temp units a reference may lag
 constexpr float kNoRef = -1e30f;                                // finite reference before any allowed logit
 constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint32_t kSlots = 16;                                 // list entries per thread after the stream
+constexpr uint32_t kCandPerRow = kThreads * kSlots;             // candidate list entries per row (8192)
+constexpr uint32_t kBatchIds = 4;                               // nucleus id loads in flight per thread
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -329,16 +331,11 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
-__device__ __forceinline__ uint64_t l2_evict_last_policy() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol) {
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
-      "%4;" ::"r"(smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
@@ -392,37 +389,124 @@ __device__ __forceinline__ void add_exps(float* acc, const uint4& v, float c, fl
   acc[6] += ex2(fmaf(lo_f(v.w), c, -mc));
   acc[7] += ex2(fmaf(hi_f(v.w), c, -mc));
 }
+// logit e (0..7) of an 8-logit group
+__device__ __forceinline__ float group_at(const uint4& v, uint32_t e) {
+  const uint32_t wd = e < 4 ? (e < 2 ? v.x : v.y) : (e < 6 ? v.z : v.w);
+  return (e & 1u) ? hi_f(wd) : lo_f(wd);
+}
+// bf16 bits of logit e (0..7) of an 8-logit group
+__device__ __forceinline__ uint32_t group_bits(const uint4& v, uint32_t e) {
+  const uint32_t wd = e < 4 ? (e < 2 ? v.x : v.y) : (e < 6 ? v.z : v.w);
+  return (e & 1u) ? (wd >> 16) : (wd & 0xFFFFu);
+}
+// monotone 16-bit key of a bf16 (the high half of fkey of its float)
+__device__ __forceinline__ uint16_t bf16_key(uint32_t h) {
+  if (h == 0x8000u) h = 0u;
+  return uint16_t((h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u));
+}
+// mass of logit x in 2^-40 units of exp2((M - M) c) = 1: fixed point, so that
+// sums do not depend on their order
+__device__ __forceinline__ unsigned long long mass_q(float x, float M, float c) {
+  return static_cast<unsigned long long>(ex2((x - M) * c) * 1099511627776.0f);
+}
+
+// Prefix sums over bins 0..kBins-1 (bin = thread; q = this thread's bin mass),
+// starting from `base`: returns the first bin whose inclusive sum reaches
+// target (or kNotFound) and, through `above`, the sum before that bin.
+// `s_first` must hold kNotFound on entry.  Ends with the block in step.
+__device__ uint32_t scan_bins(unsigned long long q, unsigned long long target, unsigned long long base,
+                              unsigned long long* red, uint32_t* s_first, unsigned long long& above) {
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  unsigned long long qi = q;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, qi, o);
+    if (lane >= uint32_t(o)) qi += y;
+  }
+  if (lane == 31) red[warp] = qi;
+  __syncthreads();
+  unsigned long long before = base;
+  for (uint32_t wi = 0; wi < warp; ++wi) before += red[wi];
+  if (before + qi >= target) atomicMin(s_first, tid);
+  __syncthreads();
+  const uint32_t j = *s_first;
+  if (j != kNotFound && tid == j) red[32] = before + qi - q;
+  __syncthreads();
+  above = j != kNotFound ? red[32] : 0ull;
+  return j;
+}
 
 __device__ __forceinline__ void issue_chunk(unsigned char* ring, uint64_t* full, const char* row, uint32_t V,
-                                            uint32_t k, uint64_t pol) {
+                                            uint32_t k) {
   const uint32_t slot = k % kStages;
   const uint32_t bytes = min(kChunkElems, V - k * kChunkElems) * 2;
   mbar_expect_tx(full + slot, bytes);
-  bulk_g2s(ring + size_t(slot) * kChunkBytes, row + size_t(k) * kChunkBytes, bytes, full + slot, pol);
+  bulk_g2s(ring + size_t(slot) * kChunkBytes, row + size_t(k) * kChunkBytes, bytes, full + slot);
+}
+
+// One warp turns staged groups [top - n, top) into candidates: lane l takes
+// group top - n + l, keeps its allowed logits >= thr, and the warp appends them
+// to the row's list (one shared atomic per call).
+__device__ __forceinline__ void drain_stage(const uint4* stg, const uint16_t* sgid, uint32_t top, uint32_t n,
+                                            float thr, uint32_t* s_count, uint32_t* gid_out, uint16_t* gkey_out,
+                                            uint32_t gcap) {
+  const uint32_t lane = threadIdx.x & 31;
+  uint32_t hits = 0, g = 0;
+  uint4 d = make_uint4(0u, 0u, 0u, 0u);
+  if (lane < n) {
+    d = stg[top - n + lane];
+    g = sgid[top - n + lane];
+    // x >= thr for a bf16 x exactly when x >= the least bf16 not below thr
+    const __nv_bfloat162 t2 = __bfloat162bfloat162(__float2bfloat16_ru(thr));
+    const uint32_t wv[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t m = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&wv[q]), t2);
+      hits |= ((m & 1u) | ((m >> 15) & 2u)) << (2 * q);
+    }
+  }
+  const uint32_t nh = __popc(hits);
+  uint32_t inc = nh;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+    if (lane >= uint32_t(o)) inc += y;
+  }
+  uint32_t wb = 0;
+  if (lane == 31 && inc) wb = atomicAdd(s_count, inc);
+  uint32_t pos = __shfl_sync(0xFFFFFFFFu, wb, 31) + inc - nh;
+  while (hits) {
+    const uint32_t e = __ffs(hits) - 1;
+    hits &= hits - 1;
+    if (pos < gcap) {
+      gid_out[pos] = g * 8 + e;
+      gkey_out[pos] = bf16_key(group_bits(d, e));
+    }
+    ++pos;
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 2)
     stream_topp_kernel(void* logits, uint32_t V, uint32_t W, const uint32_t* __restrict__ bitmask, float temp,
                        float top_p, uint32_t k0, uint32_t k1, uint32_t step, uint32_t* __restrict__ out_tok,
-                       float* __restrict__ probs, int inplace, uint32_t* status) {
+                       float* __restrict__ probs, int inplace, uint32_t* cand_id, uint16_t* cand_key,
+                       uint32_t gcap, uint32_t* status) {
   extern __shared__ __align__(128) unsigned char dsm[];
   unsigned char* ring = dsm;                                                // kStages slots
   uint4* lut = reinterpret_cast<uint4*>(dsm + kRing);                       // [256]
-  uint32_t* smask = reinterpret_cast<uint32_t*>(lut + 256);                 // [W]
-  const uint32_t nchunks = (V + kChunkElems - 1) / kChunkElems;
-  const uint32_t nfw = nchunks * kWordsPerChunk;
-  uint32_t* fbits = smask + ((W + 3) & ~3u);                                // [nfw] flag bitmap
-  // after the stream
-  uint32_t* cid = reinterpret_cast<uint32_t*>(ring);                        // [kCap]
-  uint16_t* ckey = reinterpret_cast<uint16_t*>(ring + kCap * 4);            // [kCap]
+  uint4* stg_all = lut + 256;                                               // [kConsumerWarps][kStage]
+  uint16_t* sgid_all = reinterpret_cast<uint16_t*>(stg_all + kConsumerWarps * kStage);
+  uint32_t* smask = reinterpret_cast<uint32_t*>(sgid_all + kConsumerWarps * kStage);  // [W]
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
   __shared__ float red_f[33];
-  __shared__ double red_d[33];
   __shared__ unsigned long long red_u64[33];
   __shared__ uint32_t s_maxkey, s_flag, s_count, s_tau;
 
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, b = blockIdx.x;
   char* row = reinterpret_cast<char*>(logits) + size_t(b) * V * 2;
+  const uint32_t nchunks = (V + kChunkElems - 1) / kChunkElems;
+  uint32_t* gid_row = cand_id + size_t(b) * gcap;
+  uint16_t* gkey_row = cand_key + size_t(b) * gcap;
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -456,19 +540,22 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == kConsumerWarps) {
     // ---- producer warp --------------------------------------------------------------
     if (lane == 0) {
-      const uint64_t pol = l2_evict_last_policy();
       bool ok = true;
       for (uint32_t k = 0; k < nchunks; ++k) {
         if (k >= uint32_t(kStages) && !mbar_wait(empty + k % kStages, ((k / kStages) - 1) & 1u)) {
           ok = false;
           break;
         }
-        issue_chunk(ring, full, row, V, k, pol);
+        issue_chunk(ring, full, row, V, k);
       }
       if (!ok) atomicOr(&s_flag, 1u);
     }
   } else {
     // ---- consumers ----------------------------------------------------------------
+    uint4* stg = stg_all + warp * kStage;
+    uint16_t* sgid = sgid_all + warp * kStage;
+    uint32_t sc = 0;  // staged groups of this warp (warp-uniform)
+    const uint32_t lt = (1u << lane) - 1u;
     // chunk 0's maximum seeds the reference, so the first chunk does not flag
     // every group
     if (!mbar_wait(full + 0, 0)) atomicOr(&s_flag, 1u);
@@ -484,6 +571,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (lane == 0) atomicMax(&s_maxkey, wk);
       asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");  // consumer warps only
     }
+    bool ok = true;
     for (uint32_t k = 0; k < nchunks; ++k) {
       const uint32_t slot = k % kStages;
       // reference for this chunk: the block's running maximum
@@ -497,6 +585,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float thr = mt - margin;
       if (!mbar_wait(full + slot, (k / kStages) & 1u)) {
         atomicOr(&s_flag, 1u);
+        ok = false;
         break;
       }
       const uint4* r4 = reinterpret_cast<const uint4*>(ring + size_t(slot) * kChunkBytes);
@@ -506,8 +595,15 @@ __global__ void __launch_bounds__(kThreads, 2)
       uint4 v0 = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u), v1 = v0;
       if (gi0 < ngroups) v0 = apply_mask(r4[gi0], lut[smask8[gbase + gi0]]);
       if (gi1 < ngroups) v1 = apply_mask(r4[gi1], lut[smask8[gbase + gi1]]);
+      // the slot's data are in registers: hand the slot back
       const float g0 = group_max(v0), g1 = group_max(v1);
       const float gm = fmaxf(g0, g1);
+      const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, fkey(gm));
+      __syncwarp();
+      if (lane == 0) {
+        atomicMax(&s_maxkey, wk);
+        mbar_arrive(empty + slot);
+      }
       if (gm > mt + kRefJump * temp) {
         // far above the reference (or the first allowed logits): move this
         // thread's reference before the sums can overflow
@@ -519,17 +615,34 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float mc = mt * c;
       add_exps(acc, v0, c, mc);
       add_exps(acc, v1, c, mc);
-      // chunk-local group of this lane = 480 g + tid = 32 * (15 g + warp) + lane
-      const unsigned b0 = __ballot_sync(0xFFFFFFFFu, g0 >= thr);
-      const unsigned b1 = __ballot_sync(0xFFFFFFFFu, g1 >= thr);
-      const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, fkey(gm));
-      __syncwarp();
-      if (lane == 0) {
-        fbits[k * kWordsPerChunk + warp] = b0;
-        fbits[k * kWordsPerChunk + kConsumerWarps + warp] = b1;
-        atomicMax(&s_maxkey, wk);
-        mbar_arrive(empty + slot);
+      // stage the flagged groups (fewer than 32 are staged before each group
+      // is added, at most 63 after); turn staged groups into candidates 32 at a
+      // time
+#pragma unroll
+      for (uint32_t g = 0; g < 2; ++g) {
+        const bool f = (g ? g1 : g0) >= thr;
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, f);
+        if (bal) {
+          if (f) {
+            const uint32_t p = sc + __popc(bal & lt);
+            stg[p] = g ? v1 : v0;
+            sgid[p] = uint16_t(gbase + (g ? gi1 : gi0));
+          }
+          sc += __popc(bal);
+          if (sc >= 32) {
+            __syncwarp();
+            const float thr_now = fkey_inv(*reinterpret_cast<volatile uint32_t*>(&s_maxkey)) - margin;
+            drain_stage(stg, sgid, sc, 32, thr_now, &s_count, gid_row, gkey_row, gcap);
+            sc -= 32;
+            __syncwarp();
+          }
+        }
       }
+    }
+    if (ok && sc) {
+      __syncwarp();
+      const float thr_now = fkey_inv(*reinterpret_cast<volatile uint32_t*>(&s_maxkey)) - margin;
+      drain_stage(stg, sgid, sc, sc, thr_now, &s_count, gid_row, gkey_row, gcap);
     }
   }
   __syncthreads();
@@ -544,8 +657,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   }
   const float M = fkey_inv(s_maxkey);  // -inf when no logit is allowed
-  // S: per-thread partial sums in float (each already a float sum), warp sums
-  // in float, the 16 warp sums in double
+  // S: per-thread partial sums, warp sums and the 16 warp sums, all in float
+  // (relative error near 1e-7; double arithmetic is slow on this part)
   {
     float part = 0.f;
     if (M > -INFINITY) {
@@ -557,176 +670,157 @@ __global__ void __launch_bounds__(kThreads, 2)
     part = warp_reduce(part, SumOp());
     if (lane == 0) red_f[warp] = part;
   }
+  const bool stats_ok = !(s_flag & 1u) && M > -1e29f && M < 1e29f;
+  const float thrF = M - margin;     // every allowed logit >= thrF is a candidate
+  const uint32_t km = fkey(M) >> 16;
+  uint32_t kthr = fkey(thrF) >> 16;  // smallest key whose value is >= thrF
+  if (stats_ok && bf16key_to_float(kthr) < thrF) ++kthr;
+  // histogram bin j: keys km - j (coarse: keys (km - (j+1) 2^sh, km - j 2^sh])
+  const uint32_t span = stats_ok ? km - kthr : 0u;
+  uint32_t sh = 0;
+  while ((span >> sh) >= kBins) ++sh;
+  unsigned long long* hq = reinterpret_cast<unsigned long long*>(ring);  // [kHists][kBins]
+  uint32_t* hc = reinterpret_cast<uint32_t*>(ring);                      // [kHists][kBins] (counts)
+  __syncthreads();  // red_f complete; the ring is free
+  const uint32_t n_all = s_count;
+  if (tid == 0) s_tau = kNotFound;
+  // counts (keys) need kHists x kBins words, masses (coarse bins) twice that
+  for (uint32_t i = tid; i < kHists * kBins * (sh ? 2 : 1); i += kThreads) hc[i] = 0u;
+  float Sf = 0.f;
+#pragma unroll
+  for (uint32_t wi = 0; wi < kThreads / 32; ++wi) Sf += red_f[wi];
+  const double S = Sf;
   __syncthreads();
-  double S = 0.0;
-  for (uint32_t wi = 0; wi < kThreads / 32; ++wi) S += double(red_f[wi]);
   uint32_t tok = CG_NO_TOKEN;
   bool general = false;
   if (s_flag & 1u) {
     if (tid == 0) record_error(status, CG_DEV_TIMEOUT);
-  } else if (!(M > -1e29f && M < 1e29f)) {
+  } else if (!stats_ok) {
     general = M > -INFINITY;  // huge or infinite logits: the plain path copes with them
+  } else if (n_all > gcap) {
+    general = true;
   } else {
-    // ---- candidates: allowed logits >= M - margin, read again (from L2) in the
-    // flagged groups.  Thread t takes flag words t, t + 512, ...; per round it
-    // loads up to kBatch of its flagged groups, then the warp reserves room for
-    // all their hits with one shared atomic.
-    const float thrF = M - margin;
-    const uint4* g4 = reinterpret_cast<const uint4*>(row);
-    for (uint32_t w0 = 0; w0 < nfw; w0 += kThreads) {
-      const uint32_t w = w0 + tid;
-      uint32_t bits = w < nfw ? fbits[w] : 0u;
-      while (__any_sync(0xFFFFFFFFu, bits != 0u)) {
-        uint4 v[kBatch];
-        uint32_t gsel[kBatch];
+    const unsigned long long target_q =
+        static_cast<unsigned long long>(top_p * Sf * 1099511627776.0f);  // top_p of the mass, 2^-40 units
+    const uint32_t n = n_all;
+    const uint32_t nslots = (n + kThreads - 1) / kThreads;  // slots any thread uses
+    // the keys of this thread's list entries tid + 512 j, all loads in flight
+    // at once; keys below kthr (and empty slots) read as 0, under every
+    // threshold (ids are read later, for nucleus entries only)
+    static_assert(kCandPerRow == kThreads * kSlots, "list entries per thread");
+    uint32_t kk[kSlots / 2];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          gsel[u] = kNotFound;
-          if (bits) {
-            gsel[u] = w * 32 + (__ffs(bits) - 1);
-            bits &= bits - 1;
-            v[u] = ld_stream(g4 + gsel[u]);
-          }
-        }
-        uint32_t hits[kBatch];
-        uint32_t nh = 0;
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          hits[u] = 0;
-          if (gsel[u] != kNotFound) {
-            v[u] = apply_mask(v[u], lut[smask8[gsel[u]]]);
-            const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              hits[u] |= uint32_t(lo_f(wv[q]) >= thrF) << (2 * q);
-              hits[u] |= uint32_t(hi_f(wv[q]) >= thrF) << (2 * q + 1);
-            }
-            nh += __popc(hits[u]);
-          }
-        }
-        uint32_t inc = nh;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-          if (lane >= uint32_t(o)) inc += y;
-        }
-        uint32_t wb = 0;
-        if (lane == 31 && inc) wb = atomicAdd(&s_count, inc);
-        uint32_t pos = __shfl_sync(0xFFFFFFFFu, wb, 31) + inc - nh;
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          uint32_t h = hits[u];
-          while (h) {
-            const uint32_t e = __ffs(h) - 1;
-            h &= h - 1;
-            if (pos < kCap) {
-              const uint32_t wd = e < 4 ? (e < 2 ? v[u].x : v[u].y) : (e < 6 ? v[u].z : v[u].w);
-              cid[pos] = gsel[u] * 8 + e;
-              ckey[pos] = uint16_t(fkey((e & 1u) ? hi_f(wd) : lo_f(wd)) >> 16);
-            }
-            ++pos;
-          }
-        }
-      }
+    for (uint32_t j = 0; j < kSlots; ++j) {
+      const uint32_t i = tid + kThreads * j;
+      uint32_t key = (j < nslots && i < n) ? gkey_row[i] : 0u;
+      if (key < kthr) key = 0;
+      if (j & 1) kk[j / 2] |= key << 16; else kk[j / 2] = key;
     }
-    __syncthreads();
-    const uint32_t n_all = s_count;
-    const uint32_t n = min(n_all, kCap);
-    const double target = double(top_p) * S;
-    uint32_t kthr = fkey(thrF) >> 16;  // every allowed logit with key >= kthr is a candidate
-    if (bf16key_to_float(kthr) < thrF) ++kthr;
-    const uint32_t km = fkey(M) >> 16;
-    const double fx = 1099511627776.0;  // masses in 2^-40 units: exact sums, no rounding order
-    const unsigned long long target_q = (unsigned long long)(target * fx);
-    uint32_t tau = kNotFound;
-    uint32_t* hb = reinterpret_cast<uint32_t*>(ring + kHistOff);
-    if (n_all > kCap) {
-      general = true;
-    } else if (km - kthr < kBins) {
-      // per-key counts (kHists histograms, warp w counts into histogram
-      // w % kHists), mass from the top (bin j is key km - j), block-wide prefix
-      // sum, first bin where the upper set reaches the target
-      for (uint32_t i = tid; i < kHists * kBins; i += kThreads) hb[i] = 0u;
-      __syncthreads();
-      uint32_t* mine = hb + (warp % kHists) * kBins;
-      for (uint32_t i = tid; i < n; i += kThreads) atomicAdd(mine + (km - ckey[i]), 1u);
-      __syncthreads();
-      const uint32_t L = km - kthr + 1;
-      unsigned long long q = 0;
-      if (tid < L) {
-        uint32_t cnt = 0;
+    auto key_at = [&](uint32_t j) { return (kk[j / 2] >> ((j & 1) * 16)) & 0xFFFFu; };
+    // ---- nucleus threshold: per-key counts (or per-bin masses when the keys
+    // span more than kBins), scanned from the top
+    unsigned long long above = 0;
+    uint32_t J;
+    if (sh == 0) {
+      uint32_t* hmine = hc + (warp % kHists) * kBins;
 #pragma unroll
-        for (uint32_t hw = 0; hw < kHists; ++hw) cnt += hb[hw * kBins + tid];
-        if (cnt) q = (unsigned long long)(double(cnt) * double(ex2((bf16key_to_float(km - tid) - M) * c)) * fx);
+      for (uint32_t j = 0; j < kSlots; ++j) {
+        if (j >= nslots) break;
+        const uint32_t key = key_at(j);
+        if (key) atomicAdd(hmine + (km - key), 1u);
       }
-      unsigned long long qi = q;
+      __syncthreads();
+      uint32_t cnt = 0;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, qi, o);
-        if (lane >= uint32_t(o)) qi += y;
-      }
-      if (lane == 31) red_u64[warp] = qi;
-      if (tid == 0) s_tau = kNotFound;
-      __syncthreads();
-      unsigned long long before = 0;
-      for (uint32_t wi = 0; wi < warp; ++wi) before += red_u64[wi];
-      if (tid < L && before + qi >= target_q) atomicMin(&s_tau, tid);
-      __syncthreads();
-      tau = s_tau == kNotFound ? kNotFound : km - s_tau;
-      general = tau == kNotFound;
+      for (uint32_t h = 0; h < kHists; ++h) cnt += hc[h * kBins + tid];
+      const unsigned long long q =
+          (tid <= span && cnt) ? (unsigned long long)cnt * mass_q(bf16key_to_float(km - tid), M, c) : 0ull;
+      J = scan_bins(q, target_q, 0ull, red_u64, &s_tau, above);
+      if (J != kNotFound) J = km - J;
     } else {
-      // bisection over the list: largest key whose upper set carries >= target
-      auto mass_at = [&](uint32_t kappa) {
-        unsigned long long p = 0;
-        for (uint32_t i = tid; i < n; i += kThreads) {
-          const uint32_t key = ckey[i];
-          if (key >= kappa) p += (unsigned long long)(double(ex2((bf16key_to_float(key) - M) * c)) * fx);
+      unsigned long long* hmine = hq + (warp % kHists) * kBins;
+#pragma unroll
+      for (uint32_t j = 0; j < kSlots; ++j) {
+        if (j >= nslots) break;
+        const uint32_t key = key_at(j);
+        if (key) atomicAdd(hmine + ((km - key) >> sh), mass_q(bf16key_to_float(key), M, c));
+      }
+      __syncthreads();
+      unsigned long long q = 0;
+#pragma unroll
+      for (uint32_t h = 0; h < kHists; ++h) q += hq[h * kBins + tid];
+      const uint32_t Jc = scan_bins(q, target_q, 0ull, red_u64, &s_tau, above);
+      J = kNotFound;
+      if (Jc != kNotFound) {
+        // refine inside coarse bin Jc: keys top - i, i in [0, 2^sh)
+        for (uint32_t i = tid; i < kHists * kBins; i += kThreads) hq[i] = 0ull;
+        if (tid == 0) s_tau = kNotFound;
+        __syncthreads();
+        const uint32_t top = km - (Jc << sh);
+#pragma unroll
+        for (uint32_t j = 0; j < kSlots; ++j) {
+          if (j >= nslots) break;
+          const uint32_t key = key_at(j);
+          if (key && key <= top && top - key < (1u << sh))
+            atomicAdd(hmine + (top - key), mass_q(bf16key_to_float(key), M, c));
         }
-        return block_reduce(p, SumOp(), 0ull, red_u64);
-      };
-      if (mass_at(kthr) < target_q) {
-        general = true;
-      } else {
-        uint32_t lo = kthr, hi = km;
-        while (lo < hi) {
-          const uint32_t mid = lo + (hi - lo + 1) / 2;
-          if (mass_at(mid) >= target_q) lo = mid; else hi = mid - 1;
-        }
-        tau = lo;
+        __syncthreads();
+        unsigned long long q2 = 0;
+#pragma unroll
+        for (uint32_t h = 0; h < kHists; ++h) q2 += hq[h * kBins + tid];
+        unsigned long long above2;
+        const uint32_t j2 = scan_bins(q2, target_q, above, red_u64, &s_tau, above2);
+        if (j2 != kNotFound) J = top - j2;
       }
     }
+    const uint32_t tau = J;  // a 16-bit key
+    general = tau == kNotFound || tau < kthr;
     if (!general) {
-      // nucleus entries (candidate indices) packed densely, so that the Philox
-      // draws spread over all threads; entries past kNucCap are scored in place
-      uint16_t* nuc = reinterpret_cast<uint16_t*>(ring + kHistOff);
+      // ---- nucleus entries packed into shared memory, then Gumbel-max over them
+      uint32_t* nid = reinterpret_cast<uint32_t*>(ring + kHistBytes);
+      uint16_t* nkey = reinterpret_cast<uint16_t*>(nid + kNucCap);
       if (tid == 0) s_count = 0;
       __syncthreads();
       unsigned long long best = 0ull;
-      for (uint32_t i0 = 0; i0 < n; i0 += kThreads) {
-        const uint32_t i = i0 + tid;
-        const bool in = i < n && ckey[i] >= tau;
-        const unsigned bal = __ballot_sync(0xFFFFFFFFu, in);
-        uint32_t wb = 0;
-        if (lane == 0 && bal) wb = atomicAdd(&s_count, __popc(bal));
-        const uint32_t pos = __shfl_sync(0xFFFFFFFFu, wb, 0) + __popc(bal & ((1u << lane) - 1u));
-        if (in) {
-          if (pos < kNucCap) {
-            nuc[pos] = uint16_t(i);
-          } else {
-            const uint32_t id = cid[i];
-            const uint4 blk = philox4x32_10(make_uint4(id >> 2, b, step, 0u), k0, k1);
-            const float score = __fdiv_rn(bf16key_to_float(ckey[i]), temp) + gumbel_from_word(philox_word(blk, id & 3u));
-            best = max(best, pack_best(score, id));
+      // ids of this thread's nucleus entries, kBatchIds slots at a time with
+      // the loads in flight together
+#pragma unroll
+      for (uint32_t j0 = 0; j0 < kSlots; j0 += kBatchIds) {
+        if (j0 >= nslots) break;
+        uint32_t idb[kBatchIds];
+#pragma unroll
+        for (uint32_t u = 0; u < kBatchIds; ++u) {
+          idb[u] = 0;
+          if (key_at(j0 + u) >= tau) idb[u] = gid_row[tid + kThreads * (j0 + u)];  // tau > 0: empty slots stay out
+        }
+#pragma unroll
+        for (uint32_t u = 0; u < kBatchIds; ++u) {
+          const uint32_t key = key_at(j0 + u);
+          const bool in = key >= tau;
+          const unsigned bal = __ballot_sync(0xFFFFFFFFu, in);
+          if (!bal) continue;
+          uint32_t wb = 0;
+          if (lane == 0) wb = atomicAdd(&s_count, __popc(bal));
+          const uint32_t pos = __shfl_sync(0xFFFFFFFFu, wb, 0) + __popc(bal & ((1u << lane) - 1u));
+          if (in) {
+            const uint32_t id = idb[u];
+            if (pos < kNucCap) {
+              nid[pos] = id;
+              nkey[pos] = uint16_t(key);
+            } else {
+              const uint4 blk = philox4x32_10(make_uint4(id >> 2, b, step, 0u), k0, k1);
+              const float score = __fdiv_rn(bf16key_to_float(key), temp) + gumbel_from_word(philox_word(blk, id & 3u));
+              best = max(best, pack_best(score, id));
+            }
           }
         }
       }
       __syncthreads();
       const uint32_t nn = min(s_count, kNucCap);
       for (uint32_t j = tid; j < nn; j += kThreads) {
-        const uint32_t i = nuc[j];
-        const uint32_t id = cid[i];
+        const uint32_t id = nid[j];
         const uint4 blk = philox4x32_10(make_uint4(id >> 2, b, step, 0u), k0, k1);
-        const float score = __fdiv_rn(bf16key_to_float(ckey[i]), temp) + gumbel_from_word(philox_word(blk, id & 3u));
+        const float score = __fdiv_rn(bf16key_to_float(nkey[j]), temp) + gumbel_from_word(philox_word(blk, id & 3u));
         best = max(best, pack_best(score, id));
       }
       best = block_reduce(best, MaxOp(), 0ull, red_u64);
@@ -744,9 +838,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (probs || inplace) write_outputs<true, kTopP>(row, V, smask, tok, M, S, temp, probs, inplace, b);
 }
 
-size_t stream_smem(uint32_t V, uint32_t W) {
-  const uint32_t nchunks = (V + kChunkElems - 1) / kChunkElems;
-  return size_t(kRing) + 4096 + size_t((W + 3) & ~3u) * 4 + size_t(nchunks) * kWordsPerChunk * 4;
+size_t stream_smem(uint32_t W) {
+  return size_t(kRing) + 4096 + size_t(kConsumerWarps) * kStage * 18 + size_t((W + 3) & ~3u) * 4;
 }
 
 }  // namespace fast
@@ -778,22 +871,31 @@ cudaError_t launch_mode(int mode, void* logits, uint32_t B, uint32_t V, uint32_t
                                           inplace, stream);
 }
 
+// Device scratch the sampling kernels need for B rows of V logits: the top-p
+// path's per-row candidate lists (u32 ids, then u16 keys).
+size_t sample_scratch_bytes(uint32_t B, uint32_t V) {
+  (void)V;
+  return size_t(B) * fast::kCandPerRow * 6;
+}
+
 cudaError_t launch_mask_and_sample(void* logits, int dtype, uint32_t B, uint32_t V, uint32_t W,
                                    const uint32_t* bitmask, float temp, float top_p, uint64_t seed, uint32_t step,
-                                   uint32_t* out_tok, float* probs, int inplace, uint32_t* status,
+                                   uint32_t* out_tok, float* probs, int inplace, void* scratch, uint32_t* status,
                                    cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
   const int mode = (temp == 0.f) ? kGreedy : (top_p >= 1.f ? kFull : kTopP);
   const bool bf16 = dtype == CG_BF16;
   const uint32_t ch = bf16 ? 8u : 4u;
   const bool vec = (V % ch == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
-  const size_t s1 = fast::stream_smem(V, W);
+  const size_t s1 = fast::stream_smem(W);
   if (bf16 && vec && mode == kTopP && s1 <= 112 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(fast::stream_topp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(s1));
     if (e != cudaSuccess) return e;
+    uint32_t* cand_id = static_cast<uint32_t*>(scratch);
+    uint16_t* cand_key = reinterpret_cast<uint16_t*>(cand_id + size_t(B) * fast::kCandPerRow);
     fast::stream_topp_kernel<<<B, fast::kThreads, s1, stream>>>(logits, V, W, bitmask, temp, top_p, uint32_t(seed),
                                                                uint32_t(seed >> 32), step, out_tok, probs, inplace,
-                                                               status);
+                                                               cand_id, cand_key, fast::kCandPerRow, status);
     return cudaGetLastError();
   }
   if (bf16)

@@ -216,7 +216,11 @@ int cg_fill_bitmask(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid,
  *  d_probs   : optional f32 [B][V] softmax over allowed tokens (0 elsewhere;
  *              greedy rows get 1 at the chosen token), or NULL
  *  flags     : CG_SAMPLE_INPLACE to also store -inf into masked logits
- * Sampling is Gumbel-max over the nucleus: argmax z_t + g_t, g = -log(-log u). */
+ * Sampling is Gumbel-max over the nucleus: argmax z_t + g_t, g = -log(-log u).
+ * The context keeps a device scratch for per-row candidate lists (6 bytes x
+ * 8192 per row); the first call with a larger B than before synchronises the
+ * stream and grows it with cudaMalloc, so make that first call before any
+ * stream capture.  Returns CG_E_NOMEM when the scratch cannot be allocated. */
 int cg_mask_and_sample(cg_ctx* c, void* d_logits, int dtype, uint32_t B, uint32_t V,
                        const uint32_t* d_bitmask, float temp, float top_p, uint64_t seed,
                        uint32_t step, uint32_t* d_out_tok, float* d_probs, uint32_t flags);
