@@ -63,7 +63,7 @@ def _traffic_record():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 10 ms."""
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
     QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -74,7 +74,7 @@ class ClockSampler:
         self._proc = None
         try:
             self._proc = subprocess.Popen(["nvidia-smi", f"--id={index}", f"--query-gpu={self.QUERY}",
-                                           "--format=csv,noheader,nounits", "-lms", "10"],
+                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                           stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             return
@@ -94,7 +94,8 @@ class ClockSampler:
                 self._proc.kill()
 
     def summary(self, t0: float, t1: float) -> dict:
-        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        # a sample's line arrives up to one period after it was taken
+        inside = [s for t, s in self.samples if t0 <= t <= t1 + 0.2]
         if not inside and self.samples:
             # timed region shorter than the sampling period: nearest samples
             inside = [min(self.samples, key=lambda ts: abs(ts[0] - (t0 + t1) / 2))[1]]
@@ -139,7 +140,8 @@ def run_ours(args) -> dict | None:
                                    cg.Bounds(b.ws_max, b.max_len_default, b.depth_max, b.max_items_default,
                                              b.max_tokens)) for n in cfg.grammars]
     toks = make_vocab(cfg.vocab_kind, V, cfg.vocab_seed)
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream()      # graphs are captured on a side stream
+    torch.cuda.set_stream(stream)
     ctx = cg.Ctx(grammars, cg.Vocab(toks), stream)
     ctx.prefill()   # every mask class computed once, outside the timed steps
     dtype = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
@@ -161,52 +163,88 @@ def run_ours(args) -> dict | None:
     flags = torch.empty(B, dtype=torch.uint8, device="cuda")
     seed = cfg.sample_seed
 
-    def step(i, logits, ev=None):
+    def step(i, logits):
         ctx.fill_bitmask(states, bm, gid=gid)
-        if ev is not None:
-            ev[0].record(stream)
         ctx.mask_and_sample(logits, bm, cfg.temp, cfg.top_p, seed, i, tok)
-        if ev is not None:
-            ev[1].record(stream)
         ctx.accept(states, tok.view(torch.uint32), states, flags, gid=gid, counts=counts,
                    max_tokens=b.max_tokens)
 
-    # warm-up (fills the mask cache; excluded from timing like the pages' warm-up calls)
+    # warm-up (fills the mask cache, sizes the sampling scratch)
     for i in range(args.warmup):
         step(i, bufs[i % R])
     torch.cuda.synchronize()
     if ctx.status() != 0:
         raise RuntimeError("device status after warm-up")
 
+    # The timed steps run as CUDA graphs of G steps each (launch-bound host
+    # code out of the way); each step of a graph keeps its own step index and
+    # logits buffer.  A second set of graphs holds the same mask_and_sample
+    # launches alone, to time the sampling kernel by itself.
+    G = min(args.steps, 250)
+    plan = [G] * (args.steps // G) + ([args.steps % G] if args.steps % G else [])
+
+    def capture(first, n, only_sample):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            for i in range(first, first + n):
+                if only_sample:
+                    ctx.mask_and_sample(bufs[i % R], bm, cfg.temp, cfg.top_p, seed, i, tok)
+                else:
+                    step(i, bufs[i % R])
+        return g
+
+    graphs, first = [], args.warmup
+    for n in plan:
+        graphs.append(capture(first, n, False))
+        first += n
+    sample_graphs, first = [], args.warmup
+    for n in plan:
+        sample_graphs.append(capture(first, n, True))
+        first += n
+    # one untimed replay of each graph set (first replays upload the graphs)
+    for g in graphs + sample_graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    if ctx.status() != 0:
+        raise RuntimeError("device status after graph warm-up")
+
     sampler = ClockSampler(local) if rank == 0 else None
-    time.sleep(0.1)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    time.sleep(0.25)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
     start.record(stream)
-    for i in range(args.steps):
-        step(args.warmup + i, bufs[(args.warmup + i) % R], evs[i])
+    for g in graphs:
+        g.replay()
     end.record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
     if pg:
         pg.barrier()
     ms = start.elapsed_time(end)
-    k2_ms = [a.elapsed_time(z) for a, z in evs]
     status = ctx.status()
     if status != 0:
         raise RuntimeError(f"device status {status} in the timed region")
+    # the sampling kernel alone, same launches
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s0.record(stream)
+    for g in sample_graphs:
+        g.replay()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    k2_avg_ms = s0.elapsed_time(s1) / args.steps
     if pg:
         t = torch.tensor([ms], device="cuda")
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         ms = float(t.item())
-    time.sleep(0.05)
+    time.sleep(0.3)
     clocks = sampler.summary(t0, t1) if sampler else None
     if sampler:
         sampler.stop()
+    del graphs, sample_graphs
 
     # end to end through the same calls with host buffers
     e2e_steps = min(args.steps, args.e2e_steps)
@@ -230,7 +268,6 @@ def run_ours(args) -> dict | None:
     if rank != 0:
         return None
     per_step = ms / args.steps
-    k2_avg_ms = sum(k2_ms) / len(k2_ms)
     alg_bytes = B * (V * esz + W * 4)
     peaks = _peaks()
     achieved = alg_bytes / (k2_avg_ms * 1e-3) / 1e9
@@ -347,7 +384,7 @@ def run_reference(args) -> dict | None:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="booking_128k")

@@ -20,6 +20,10 @@
 // temperature folded into one scale c = log2(e) / temp.
 #include <cuda_bf16.h>
 
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "device.cuh"
 
 namespace cgk {
@@ -844,13 +848,29 @@ size_t stream_smem(uint32_t W) {
 
 }  // namespace fast
 
+// Raises a kernel's dynamic shared memory limit once per device (the setting
+// is per function and device; repeating it costs a driver call per launch).
+cudaError_t allow_smem(const void* kernel, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, size_t> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  size_t& have = done[{kernel, dev}];
+  if (bytes <= have) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+  if (e == cudaSuccess) have = bytes;
+  return e;
+}
+
 template <bool BF16, bool VEC, int MODE>
 cudaError_t launch_variant(void* logits, uint32_t B, uint32_t V, uint32_t W, const uint32_t* bitmask,
                            float temp, float top_p, uint64_t seed, uint32_t step, uint32_t* out_tok, float* probs,
                            int inplace, cudaStream_t stream) {
   const size_t smem = size_t(W) * 4 + ((MODE == kTopP && BF16) ? size_t(kWindow) * 4 : 0);
   auto* k = sample_kernel<BF16, VEC, MODE>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  cudaError_t e = allow_smem(reinterpret_cast<const void*>(k), smem);
   if (e != cudaSuccess) return e;
   k<<<B, kSampleThreads, smem, stream>>>(logits, V, W, bitmask, temp, top_p, uint32_t(seed), uint32_t(seed >> 32),
                                           step, out_tok, probs, inplace);
@@ -889,7 +909,7 @@ cudaError_t launch_mask_and_sample(void* logits, int dtype, uint32_t B, uint32_t
   const bool vec = (V % ch == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
   const size_t s1 = fast::stream_smem(W);
   if (bf16 && vec && mode == kTopP && s1 <= 112 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(fast::stream_topp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(s1));
+    cudaError_t e = allow_smem(reinterpret_cast<const void*>(fast::stream_topp_kernel), s1);
     if (e != cudaSuccess) return e;
     uint32_t* cand_id = static_cast<uint32_t*>(scratch);
     uint16_t* cand_key = reinterpret_cast<uint16_t*>(cand_id + size_t(B) * fast::kCandPerRow);
