@@ -279,16 +279,17 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(void* logits, ui
 // chunk 16 logits per thread (two 8-logit groups): the bitmask is applied
 // through a 256-entry table of pair masks indexed by the group's mask byte, the
 // group maximum comes from packed bf16 max, and exp2((x - m) c) is summed into
-// 8 partial sums against a reference m that follows the block's running
-// maximum (published per chunk by a warp max-reduction and a shared
-// atomicMax).  A group whose maximum reaches the reference minus kMarginZ nats
-// is copied, masked, into its warp's staging area in shared memory (positions
-// from a warp ballot); whenever 32 groups are staged the warp turns them into
+// 8 partial sums against the thread's own running maximum m (so that S does
+// not depend on warp timing).  The block's running maximum is published per
+// chunk (warp max-reduction and a shared atomicMax); a group whose maximum
+// reaches it minus kMarginZ nats is copied, masked, into its warp's staging
+// area in shared memory (positions from a warp ballot); whenever 32 groups are staged the warp turns them into
 // candidates -- allowed logits at or above the block's running maximum minus
 // the margin -- one group per lane, and appends them (id, 16-bit key) to the
-// row's candidate list in global memory.  The references never exceed the
-// final maximum M, so every allowed logit within kMarginZ nats of M becomes a
-// candidate.
+// row's candidate list in global memory.  The running maximum never exceeds
+// the final maximum M, so every allowed logit within kMarginZ nats of M
+// becomes a candidate; which others do depends on timing, but only candidates
+// at or above M - margin count afterwards.
 //
 // After the stream: M and S = sum exp2((x - M) c) come from the block; the
 // nucleus threshold tau is the largest key whose upper set carries top_p * S
@@ -315,7 +316,6 @@ static_assert(kBins == kThreads, "one histogram bin per thread in the scans");
 constexpr uint32_t kHistBytes = kHists * kBins * 8;
 constexpr uint32_t kNucCap = (kRing - kHistBytes) / 6;          // packed nucleus entries (u32 id + u16 key)
 constexpr float kMarginZ = 9.0f;                                // nats below the maximum kept as candidates
-constexpr float kRefJump = 60.f;                                // logit/temp units a reference may lag
 constexpr float kNoRef = -1e30f;                                // finite reference before any allowed logit
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kSlots = 16;                                 // list entries per thread after the stream
@@ -536,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const float c = 1.4426950408889634f / temp;
   const float margin = kMarginZ * temp;  // z = x / temp: kMarginZ nats are kMarginZ * temp logit units
   const uint8_t* smask8 = reinterpret_cast<const uint8_t*>(smask);
-  float mt = kNoRef;  // this thread's reference (never above the row maximum)
+  float mt = kNoRef;  // reference of this thread's sums: its running maximum
   float acc[kAcc];
 #pragma unroll
   for (int j = 0; j < kAcc; ++j) acc[j] = 0.f;
@@ -578,15 +578,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     bool ok = true;
     for (uint32_t k = 0; k < nchunks; ++k) {
       const uint32_t slot = k % kStages;
-      // reference for this chunk: the block's running maximum
-      const float mref = fkey_inv(*reinterpret_cast<volatile uint32_t*>(&s_maxkey));
-      if (mref > mt) {
-        const float r = ex2((mt - mref) * c);
-#pragma unroll
-        for (int j = 0; j < kAcc; ++j) acc[j] *= r;
-        mt = mref;
-      }
-      const float thr = mt - margin;
+      // flag threshold for this chunk: the block's running maximum minus the
+      // margin (never above M - margin; finite, so masked groups never flag)
+      const float thr = fmaxf(fkey_inv(*reinterpret_cast<volatile uint32_t*>(&s_maxkey)), kNoRef) - margin;
       if (!mbar_wait(full + slot, (k / kStages) & 1u)) {
         atomicOr(&s_flag, 1u);
         ok = false;
@@ -608,9 +602,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         atomicMax(&s_maxkey, wk);
         mbar_arrive(empty + slot);
       }
-      if (gm > mt + kRefJump * temp) {
-        // far above the reference (or the first allowed logits): move this
-        // thread's reference before the sums can overflow
+      if (gm > mt) {
+        // the sums' reference is this thread's own running maximum, so that
+        // they do not depend on the other warps' timing (S is reproducible)
         const float r = ex2((mt - gm) * c);
 #pragma unroll
         for (int j = 0; j < kAcc; ++j) acc[j] *= r;
@@ -635,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           sc += __popc(bal);
           if (sc >= 32) {
             __syncwarp();
-            const float thr_now = fkey_inv(*reinterpret_cast<volatile uint32_t*>(&s_maxkey)) - margin;
+            const float thr_now = fmaxf(fkey_inv(*reinterpret_cast<volatile uint32_t*>(&s_maxkey)), kNoRef) - margin;
             drain_stage(stg, sgid, sc, 32, thr_now, &s_count, gid_row, gkey_row, gcap);
             sc -= 32;
             __syncwarp();
@@ -645,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     if (ok && sc) {
       __syncwarp();
-      const float thr_now = fkey_inv(*reinterpret_cast<volatile uint32_t*>(&s_maxkey)) - margin;
+      const float thr_now = fmaxf(fkey_inv(*reinterpret_cast<volatile uint32_t*>(&s_maxkey)), kNoRef) - margin;
       drain_stage(stg, sgid, sc, sc, thr_now, &s_count, gid_row, gkey_row, gcap);
     }
   }
