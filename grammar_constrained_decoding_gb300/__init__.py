@@ -179,6 +179,17 @@ class Ctx:
             self._h, _ptr(logits), dtype, B, V, _ptr(bitmask), float(temp), float(top_p), int(seed), int(step),
             _ptr(out_tok), _ptr(probs), L.CG_SAMPLE_INPLACE if inplace else 0))
 
+    def mask_and_sample_noalloc(self, logits, bitmask, temp: float, top_p: float, seed: int, step: int, out_tok,
+                                probs=None, inplace: bool = False) -> None:
+        """mask_and_sample on the library's fixed scratch (no device allocation;
+        B <= CG_NOALLOC_MAX_ROWS; overlapping calls on one device race)."""
+        import torch
+        dtype = {torch.float32: L.CG_F32, torch.bfloat16: L.CG_BF16}[logits.dtype]
+        B, V = logits.shape
+        L.check("cg_mask_and_sample_noalloc", L.lib().cg_mask_and_sample_noalloc(
+            self._h, _ptr(logits), dtype, B, V, _ptr(bitmask), float(temp), float(top_p), int(seed), int(step),
+            _ptr(out_tok), _ptr(probs), L.CG_SAMPLE_INPLACE if inplace else 0))
+
     def accept(self, states, toks, out_states, out_flags, gid=None, forced=None, counts=None,
                max_tokens: int = 2048) -> None:
         B = states.shape[0]

@@ -18,6 +18,7 @@ CG_DEAD = CG_NO_TOKEN = 0xFFFFFFFF
 CG_FLAG_DONE, CG_FLAG_FORCED_NEXT, CG_FLAG_REJECTED, CG_FLAG_NO_TOKEN, CG_FLAG_CAPPED = 1, 2, 4, 8, 16
 CG_STATE_ACCEPT, CG_STATE_SINK, CG_STATE_FORCED_ONLY = 1, 2, 4
 CG_SAMPLE_INPLACE = 1
+CG_NOALLOC_MAX_ROWS = 64
 CG_RESULT_CALC_TAG, CG_RESULT_JSON_ANSWER = 0, 1
 
 ERROR_NAMES = {CG_E_ARG: "CG_E_ARG", CG_E_SYNTAX: "CG_E_SYNTAX", CG_E_UNSUPPORTED: "CG_E_UNSUPPORTED",
@@ -60,6 +61,9 @@ SIGNATURES = {
     "cg_mask_and_sample": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_uint32, C.c_uint32, C.c_void_p,
                                      C.c_float, C.c_float, C.c_uint64, C.c_uint32, C.c_void_p, C.c_void_p,
                                      C.c_uint32]),
+    "cg_mask_and_sample_noalloc": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_uint32, C.c_uint32, C.c_void_p,
+                                             C.c_float, C.c_float, C.c_uint64, C.c_uint32, C.c_void_p, C.c_void_p,
+                                             C.c_uint32]),
     "cg_accept": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_uint32, C.c_void_p,
                             C.c_uint32, C.c_void_p, C.c_void_p]),
     "cg_eval_arith": (C.c_int, [C.c_char_p, C.c_size_t, C.c_int, C.c_void_p, C.c_size_t, C.POINTER(C.c_size_t),

@@ -2,6 +2,7 @@
 // device status word, and launches the three step kernels on its stream.
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -56,6 +57,38 @@ void release(cg_ctx* c) {
   c->sample_scratch_bytes = 0;
 }
 
+}  // namespace
+
+// Scratch of cg_mask_and_sample_noalloc: the candidate lists of up to
+// CG_NOALLOC_MAX_ROWS rows (u32 ids, then u16 keys), fixed in the module so
+// that the call never allocates.  Its callers are the ones that must not touch
+// the allocator while decoding: cudaMalloc/cudaFree synchronise the device and
+// can fail once a server has planned all of its memory at start-up.  Shared by
+// every call on a device (calls that may overlap race on it).
+constexpr size_t kNoAllocScratchBytes = size_t(CG_NOALLOC_MAX_ROWS) * 8192 * 6;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+// device address of g_noalloc_scratch, looked up once per device
+void* noalloc_scratch(cudaError_t* err) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= 64) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
 }  // namespace
 
 extern "C" {
@@ -217,6 +250,24 @@ int cg_mask_and_sample(cg_ctx* c, void* d_logits, int dtype, uint32_t B, uint32_
   }
   return cgk::launch_mask_and_sample(d_logits, dtype, B, V, c->t.W, d_bitmask, temp, top_p, seed, step, d_out_tok,
                                      d_probs, (flags & CG_SAMPLE_INPLACE) ? 1 : 0, c->sample_scratch, c->t.status,
+                                     c->stream) == cudaSuccess
+             ? CG_OK
+             : CG_E_CUDA;
+}
+
+int cg_mask_and_sample_noalloc(cg_ctx* c, void* d_logits, int dtype, uint32_t B, uint32_t V,
+                               const uint32_t* d_bitmask, float temp, float top_p, uint64_t seed, uint32_t step,
+                               uint32_t* d_out_tok, float* d_probs, uint32_t flags) {
+  if (!c || (B && (!d_logits || !d_bitmask || !d_out_tok))) return CG_E_ARG;
+  if (dtype != CG_F32 && dtype != CG_BF16) return CG_E_ARG;
+  if (V != c->t.V || !(temp >= 0.f) || temp == INFINITY || !(top_p == top_p)) return CG_E_ARG;
+  if (flags & ~CG_SAMPLE_INPLACE) return CG_E_ARG;
+  if (B > CG_NOALLOC_MAX_ROWS || cgk::sample_scratch_bytes(B, V) > kNoAllocScratchBytes) return CG_E_LIMIT;
+  cudaError_t e = cudaSuccess;
+  void* scratch = noalloc_scratch(&e);
+  if (!scratch) return CG_E_CUDA;
+  return cgk::launch_mask_and_sample(d_logits, dtype, B, V, c->t.W, d_bitmask, temp, top_p, seed, step, d_out_tok,
+                                     d_probs, (flags & CG_SAMPLE_INPLACE) ? 1 : 0, scratch, c->t.status,
                                      c->stream) == cudaSuccess
              ? CG_OK
              : CG_E_CUDA;

@@ -225,6 +225,29 @@ int cg_mask_and_sample(cg_ctx* c, void* d_logits, int dtype, uint32_t B, uint32_
                        const uint32_t* d_bitmask, float temp, float top_p, uint64_t seed,
                        uint32_t step, uint32_t* d_out_tok, float* d_probs, uint32_t flags);
 
+/* Variant of cg_mask_and_sample that never allocates device memory.  The pages
+ * have no counterpart: it is a deployment variant of step 2, not a step of the
+ * method.  Arguments, results and error codes are those of cg_mask_and_sample,
+ * except where this block says otherwise.
+ *  - It is for callers that must not allocate device memory while decoding:
+ *    cudaMalloc/cudaFree synchronise the device and can fail once a server has
+ *    planned all of HBM (e.g. for its KV cache) at start-up.
+ *  - Scratch: a fixed array inside the library, CG_NOALLOC_MAX_ROWS x 8192 x 6
+ *    bytes (3 MiB), one per device, holding the per-row candidate lists.
+ *    B > CG_NOALLOC_MAX_ROWS returns CG_E_LIMIT without launching anything.
+ *  - Nothing in the scratch has to start at zero: the kernel writes every list
+ *    entry before it reads it.
+ *  - Every call on a device uses the same array, so calls that may overlap on
+ *    the device (other streams, other contexts, other host threads) race on it;
+ *    the caller must serialise them (one stream at a time).
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress; CG_E_CUDA if that fails); make that first call
+ *    before capturing any stream. */
+#define CG_NOALLOC_MAX_ROWS 64u
+int cg_mask_and_sample_noalloc(cg_ctx* c, void* d_logits, int dtype, uint32_t B, uint32_t V,
+                               const uint32_t* d_bitmask, float temp, float top_p, uint64_t seed,
+                               uint32_t step, uint32_t* d_out_tok, float* d_probs, uint32_t flags);
+
 /* Step 3 -- advance each row's automaton by its token ("after injection the
  * grammar state must be advanced", labs.miniml.ai "Evaluator aware decoding").
  *  d_states, d_gid : as in cg_fill_bitmask (d_gid may be NULL)
