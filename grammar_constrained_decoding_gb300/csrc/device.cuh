@@ -2,11 +2,37 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "../../include/cg.h"
 
 namespace cgk {
+
+// Programmatic dependent launch: the step's kernels (fill_bitmask ->
+// mask_and_sample -> accept -> next fill_bitmask) are launched so that each
+// may start while its predecessor finishes.  A kernel lets its dependents be
+// scheduled as soon as it starts (launch_dependents) and waits for its
+// predecessor's completion and memory (griddep_wait) before it reads anything
+// the predecessor wrote.  Both are no-ops for a normally launched kernel.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 struct DevGrammar {
   uint64_t table_off;   // first element of this grammar's [n_states x n_cols] table

@@ -10,6 +10,7 @@
 namespace cgk {
 
 constexpr int kAcceptThreads = 128;
+constexpr uint32_t kPrefetch = 16;  // token bytes whose columns are loaded up front
 
 __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(Tables t, const uint32_t* __restrict__ states,
                                                                 const uint16_t* __restrict__ gid,
@@ -17,6 +18,8 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(Tables t, const 
                                                                 const int32_t* __restrict__ forced, uint32_t B,
                                                                 uint32_t* counts, uint32_t max_tokens,
                                                                 uint32_t* out_states, uint8_t* out_flags) {
+  griddep_launch_dependents();
+  griddep_wait();  // the tokens come from the sampling kernel
   const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   const uint32_t g = gid ? gid[b] : 0u;
@@ -51,8 +54,17 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(Tables t, const 
       const uint32_t shift = f >= 0 ? 256u : 0u;
       const uint16_t* cols = t.colmap + size_t(g) * 512 + shift;
       const uint32_t* table = t.table + gd.table_off;
+      // the token's columns first (independent loads), then the chain of
+      // table lookups
+      const uint32_t i0 = t.tok_off[tok], len = t.tok_off[tok + 1] - i0;
+      uint32_t col[kPrefetch];
+#pragma unroll
+      for (uint32_t k = 0; k < kPrefetch; ++k) col[k] = k < len ? cols[t.tok_bytes[i0 + k]] : 0u;
       uint32_t st = s;
-      for (uint32_t i = t.tok_off[tok]; i < t.tok_off[tok + 1] && st != CG_DEAD; ++i)
+#pragma unroll
+      for (uint32_t k = 0; k < kPrefetch; ++k)
+        if (k < len && st != CG_DEAD) st = table[size_t(st) * gd.n_cols + col[k]];
+      for (uint32_t i = i0 + kPrefetch; i < i0 + len && st != CG_DEAD; ++i)
         st = table[size_t(st) * gd.n_cols + cols[t.tok_bytes[i]]];
       ns = st;
       if (st == CG_DEAD) {
@@ -82,9 +94,8 @@ cudaError_t launch_accept(const Tables& t, const uint32_t* states, const uint16_
                           const int32_t* forced, uint32_t B, uint32_t* counts, uint32_t max_tokens,
                           uint32_t* out_states, uint8_t* out_flags, cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
-  accept_kernel<<<(B + kAcceptThreads - 1) / kAcceptThreads, kAcceptThreads, 0, stream>>>(
-      t, states, gid, toks, forced, B, counts, max_tokens, out_states, out_flags);
-  return cudaGetLastError();
+  return launch_dependent(accept_kernel, dim3((B + kAcceptThreads - 1) / kAcceptThreads), dim3(kAcceptThreads), 0,
+                          stream, t, states, gid, toks, forced, B, counts, max_tokens, out_states, out_flags);
 }
 
 }  // namespace cgk

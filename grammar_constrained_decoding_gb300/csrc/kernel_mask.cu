@@ -70,6 +70,8 @@ __global__ void __launch_bounds__(kFillThreads) fill_bitmask_kernel(Tables t, co
   uint32_t* smask = smem;                                   // [W]
   uint16_t* scol = reinterpret_cast<uint16_t*>(smem + t.W); // [256] model-byte columns
   __shared__ uint32_t s_claim, s_ready;
+  griddep_launch_dependents();
+  griddep_wait();  // states (and forced tokens) come from the previous step
   const uint32_t b = blockIdx.x, W = t.W;
   uint32_t* out = bitmask + size_t(b) * W;
   const uint32_t g = gid ? gid[b] : 0u;
@@ -165,8 +167,8 @@ cudaError_t launch_fill_bitmask(const Tables& t, const uint32_t* states, const u
                                 uint32_t B, uint32_t* bitmask, cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
   const size_t smem = size_t(t.W) * 4 + 256 * 2;
-  fill_bitmask_kernel<<<B, kFillThreads, smem, stream>>>(t, states, gid, forced, bitmask);
-  return cudaGetLastError();
+  return launch_dependent(fill_bitmask_kernel, dim3(B), dim3(kFillThreads), smem, stream, t, states, gid, forced,
+                          bitmask);
 }
 
 size_t fill_bitmask_smem(uint32_t W) { return size_t(W) * 4 + 256 * 2; }

@@ -256,6 +256,8 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(void* logits, ui
   extern __shared__ uint32_t smem[];
   uint32_t* smask = smem;             // [W]
   uint32_t* cnt = smem + W;           // [kWindow] (top-p, bf16)
+  griddep_launch_dependents();
+  griddep_wait();  // the bitmask comes from fill_bitmask
   const uint32_t b = blockIdx.x;
   const size_t esz = BF16 ? 2 : 4;
   char* row = reinterpret_cast<char*>(logits) + size_t(b) * V * esz;
@@ -506,6 +508,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ unsigned long long red_u64[33];
   __shared__ uint32_t s_maxkey, s_flag, s_count, s_tau;
 
+  griddep_launch_dependents();
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, b = blockIdx.x;
   char* row = reinterpret_cast<char*>(logits) + size_t(b) * V * 2;
   const uint32_t nchunks = (V + kChunkElems - 1) / kChunkElems;
@@ -529,6 +532,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       w[q] = (((i >> (2 * q)) & 1u) ? 0x0000FFFFu : 0u) | (((i >> (2 * q + 1)) & 1u) ? 0xFFFF0000u : 0u);
     lut[i] = make_uint4(w[0], w[1], w[2], w[3]);
   }
+  griddep_wait();  // the bitmask comes from fill_bitmask
   const uint32_t* mrow = bitmask + size_t(b) * W;
   for (uint32_t i = tid; i < W; i += kThreads) smask[i] = mrow[i];
   __syncthreads();
@@ -866,9 +870,8 @@ cudaError_t launch_variant(void* logits, uint32_t B, uint32_t V, uint32_t W, con
   auto* k = sample_kernel<BF16, VEC, MODE>;
   cudaError_t e = allow_smem(reinterpret_cast<const void*>(k), smem);
   if (e != cudaSuccess) return e;
-  k<<<B, kSampleThreads, smem, stream>>>(logits, V, W, bitmask, temp, top_p, uint32_t(seed), uint32_t(seed >> 32),
-                                          step, out_tok, probs, inplace);
-  return cudaGetLastError();
+  return launch_dependent(k, dim3(B), dim3(kSampleThreads), smem, stream, logits, V, W, bitmask, temp, top_p,
+                          uint32_t(seed), uint32_t(seed >> 32), step, out_tok, probs, inplace);
 }
 
 template <bool BF16, bool VEC>
@@ -907,10 +910,9 @@ cudaError_t launch_mask_and_sample(void* logits, int dtype, uint32_t B, uint32_t
     if (e != cudaSuccess) return e;
     uint32_t* cand_id = static_cast<uint32_t*>(scratch);
     uint16_t* cand_key = reinterpret_cast<uint16_t*>(cand_id + size_t(B) * fast::kCandPerRow);
-    fast::stream_topp_kernel<<<B, fast::kThreads, s1, stream>>>(logits, V, W, bitmask, temp, top_p, uint32_t(seed),
-                                                               uint32_t(seed >> 32), step, out_tok, probs, inplace,
-                                                               cand_id, cand_key, fast::kCandPerRow, status);
-    return cudaGetLastError();
+    return launch_dependent(fast::stream_topp_kernel, dim3(B), dim3(fast::kThreads), s1, stream, logits, V, W,
+                            bitmask, temp, top_p, uint32_t(seed), uint32_t(seed >> 32), step, out_tok, probs, inplace,
+                            cand_id, cand_key, fast::kCandPerRow, status);
   }
   if (bf16)
     return vec ? launch_mode<true, true>(mode, logits, B, V, W, bitmask, temp, top_p, seed, step, out_tok, probs,
