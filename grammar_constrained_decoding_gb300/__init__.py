@@ -197,6 +197,19 @@ class Ctx:
                                                 _ptr(counts), max_tokens, _ptr(out_states), _ptr(out_flags)))
 
 
+    def step(self, states, logits, temp: float, top_p: float, seed: int, step: int, out_tok, out_states, out_flags,
+             gid=None, forced=None, counts=None, max_tokens: int = 2048, bitmask=None) -> None:
+        """fill_bitmask + mask_and_sample + accept in one call (one kernel on the
+        top-p bf16 path); bitmask, when given, receives the row masks."""
+        import torch
+        dtype = {torch.float32: L.CG_F32, torch.bfloat16: L.CG_BF16}[logits.dtype]
+        B, V = logits.shape
+        L.check("cg_step", L.lib().cg_step(
+            self._h, _ptr(states), _ptr(gid), _ptr(forced), B, _ptr(logits), dtype, V, float(temp), float(top_p),
+            int(seed), int(step), _ptr(counts), max_tokens, _ptr(bitmask), _ptr(out_tok), _ptr(out_states),
+            _ptr(out_flags)))
+
+
 class Driver:
     """Host driver of forced tokens (evaluator-aware grammars)."""
 

@@ -22,7 +22,7 @@ LIB = os.path.join(OUT_DIR, "libcg.so")
 
 CXX_SOURCES = ["compiler/gbnf.cpp", "compiler/schema.cpp", "compiler/automaton.cpp", "grammar.cpp", "evaluator.cpp"]
 CU_SOURCES = ["ctx.cu", "kernel_mask.cu", "kernel_sample.cu", "kernel_accept.cu"]
-HEADERS = ["compiler/ir.h", "cg_internal.h", "device.cuh"]
+HEADERS = ["compiler/ir.h", "cg_internal.h", "device.cuh", "row_ops.cuh"]
 GENCODE = "arch=compute_103a,code=sm_103a"
 
 

@@ -19,6 +19,11 @@ cudaError_t launch_mask_and_sample(void* logits, int dtype, uint32_t B, uint32_t
                                    uint32_t* out_tok, float* probs, int inplace, void* scratch, uint32_t* status,
                                    cudaStream_t stream);
 size_t sample_scratch_bytes(uint32_t B, uint32_t V);
+bool step_fusable(int dtype, uint32_t V, uint32_t W, float temp, float top_p, const void* logits);
+cudaError_t launch_step(const Tables& t, const uint32_t* states, const uint16_t* gid, const int32_t* forced,
+                        uint32_t B, void* logits, uint32_t V, float temp, float top_p, uint64_t seed, uint32_t step,
+                        uint32_t* counts, uint32_t max_tokens, uint32_t* bitmask_out, uint32_t* out_tok,
+                        uint32_t* out_states, uint8_t* out_flags, void* scratch, cudaStream_t stream);
 cudaError_t launch_accept(const Tables& t, const uint32_t* states, const uint16_t* gid, const uint32_t* toks,
                           const int32_t* forced, uint32_t B, uint32_t* counts, uint32_t max_tokens,
                           uint32_t* out_states, uint8_t* out_flags, cudaStream_t stream);
@@ -34,6 +39,8 @@ struct cg_ctx {
   const uint16_t* class_gid = nullptr;   // grammar of each mask class
   void* sample_scratch = nullptr;        // candidate lists of the sampling kernel
   size_t sample_scratch_bytes = 0;
+  uint32_t* step_bitmask = nullptr;      // bitmask of cg_step's unfused path when the caller gives none
+  size_t step_bitmask_bytes = 0;
 };
 
 namespace {
@@ -55,6 +62,22 @@ void release(cg_ctx* c) {
   if (c->sample_scratch) cudaFree(c->sample_scratch);
   c->sample_scratch = nullptr;
   c->sample_scratch_bytes = 0;
+  if (c->step_bitmask) cudaFree(c->step_bitmask);
+  c->step_bitmask = nullptr;
+  c->step_bitmask_bytes = 0;
+}
+
+// Grows a context-owned device buffer to at least `need` bytes (synchronising
+// the stream first: kernels still queued may use the old buffer).
+int grow(cg_ctx* c, void** buf, size_t* have, size_t need) {
+  if (need <= *have) return CG_OK;
+  if (cudaStreamSynchronize(c->stream) != cudaSuccess) return CG_E_CUDA;
+  if (*buf) cudaFree(*buf);
+  *buf = nullptr;
+  *have = 0;
+  if (cudaMalloc(buf, need) != cudaSuccess) return CG_E_NOMEM;
+  *have = need;
+  return CG_OK;
 }
 
 }  // namespace
@@ -237,17 +260,9 @@ int cg_mask_and_sample(cg_ctx* c, void* d_logits, int dtype, uint32_t B, uint32_
   if (dtype != CG_F32 && dtype != CG_BF16) return CG_E_ARG;
   if (V != c->t.V || !(temp >= 0.f) || temp == INFINITY || !(top_p == top_p)) return CG_E_ARG;
   if (flags & ~CG_SAMPLE_INPLACE) return CG_E_ARG;
-  const size_t need = cgk::sample_scratch_bytes(B, V);
-  if (need > c->sample_scratch_bytes) {
-    // grown once per larger batch (outside any stream capture): the kernels
-    // still queued on the stream may use the old buffer
-    if (cudaStreamSynchronize(c->stream) != cudaSuccess) return CG_E_CUDA;
-    if (c->sample_scratch) cudaFree(c->sample_scratch);
-    c->sample_scratch = nullptr;
-    c->sample_scratch_bytes = 0;
-    if (cudaMalloc(&c->sample_scratch, need) != cudaSuccess) return CG_E_NOMEM;
-    c->sample_scratch_bytes = need;
-  }
+  // grown once per larger batch (outside any stream capture)
+  const int rc = grow(c, &c->sample_scratch, &c->sample_scratch_bytes, cgk::sample_scratch_bytes(B, V));
+  if (rc != CG_OK) return rc;
   return cgk::launch_mask_and_sample(d_logits, dtype, B, V, c->t.W, d_bitmask, temp, top_p, seed, step, d_out_tok,
                                      d_probs, (flags & CG_SAMPLE_INPLACE) ? 1 : 0, c->sample_scratch, c->t.status,
                                      c->stream) == cudaSuccess
@@ -282,6 +297,37 @@ int cg_accept(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const 
                             d_out_flags, c->stream) == cudaSuccess
              ? CG_OK
              : CG_E_CUDA;
+}
+
+int cg_step(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const int32_t* d_forced, uint32_t B,
+            void* d_logits, int dtype, uint32_t V, float temp, float top_p, uint64_t seed, uint32_t step,
+            uint32_t* d_counts, uint32_t max_tokens, uint32_t* d_bitmask, uint32_t* d_out_tok,
+            uint32_t* d_out_states, uint8_t* d_out_flags) {
+  if (!c || (B && (!d_states || !d_logits || !d_out_tok || !d_out_states || !d_out_flags))) return CG_E_ARG;
+  if (dtype != CG_F32 && dtype != CG_BF16) return CG_E_ARG;
+  if (V != c->t.V || !(temp >= 0.f) || temp == INFINITY || !(top_p == top_p)) return CG_E_ARG;
+  if (d_counts && max_tokens == 0) return CG_E_ARG;
+  if (B == 0) return CG_OK;
+  int rc = grow(c, &c->sample_scratch, &c->sample_scratch_bytes, cgk::sample_scratch_bytes(B, V));
+  if (rc != CG_OK) return rc;
+  if (cgk::step_fusable(dtype, V, c->t.W, temp, top_p, d_logits))
+    return cgk::launch_step(c->t, d_states, d_gid, d_forced, B, d_logits, V, temp, top_p, seed, step, d_counts,
+                            max_tokens, d_bitmask, d_out_tok, d_out_states, d_out_flags, c->sample_scratch,
+                            c->stream) == cudaSuccess
+               ? CG_OK
+               : CG_E_CUDA;
+  // otherwise the three calls, through a context bitmask when the caller gives none
+  uint32_t* bm = d_bitmask;
+  if (!bm) {
+    rc = grow(c, reinterpret_cast<void**>(&c->step_bitmask), &c->step_bitmask_bytes, size_t(B) * c->t.W * 4);
+    if (rc != CG_OK) return rc;
+    bm = c->step_bitmask;
+  }
+  if ((rc = cg_fill_bitmask(c, d_states, d_gid, d_forced, B, bm)) != CG_OK) return rc;
+  if ((rc = cg_mask_and_sample(c, d_logits, dtype, B, V, bm, temp, top_p, seed, step, d_out_tok, nullptr, 0)) !=
+      CG_OK)
+    return rc;
+  return cg_accept(c, d_states, d_gid, d_out_tok, d_forced, B, d_counts, max_tokens, d_out_states, d_out_flags);
 }
 
 }  // extern "C"

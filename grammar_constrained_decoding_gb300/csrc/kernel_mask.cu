@@ -11,56 +11,11 @@
 // vocabulary and resumes each token's walk from the state reached after the
 // prefix it shares with the previous token, so shared prefixes are walked
 // once.  Allowed tokens set their bit (token-id order) in a shared-memory mask.
-#include "device.cuh"
+#include "row_ops.cuh"
 
 namespace cgk {
 
 constexpr int kFillThreads = 512;
-constexpr uint32_t kStateEmpty = 0, kStateBusy = 1, kStateReady = 2;
-
-__device__ __forceinline__ uint32_t load_acquire(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void store_release(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Walk all tokens from state s of grammar g; sets allowed bits in smask[W].
-__device__ void walk_tokens(const Tables& t, const DevGrammar& gd, const uint16_t* scol, uint32_t s,
-                            uint32_t* smask) {
-  const uint32_t V = t.V;
-  const uint32_t per = (V + blockDim.x - 1) / blockDim.x;
-  const uint32_t i0 = threadIdx.x * per;
-  const uint32_t i1 = min(V, i0 + per);
-  const uint32_t* table = t.table + gd.table_off;
-  const uint32_t ncols = gd.n_cols;
-  uint32_t stack[65];
-  stack[0] = s;
-  uint32_t valid = 0;  // stack[0..valid] hold the states after 0..valid bytes of the previous token
-  for (uint32_t i = i0; i < i1; ++i) {
-    const uint32_t b0 = t.sorted_off[i], len = t.sorted_off[i + 1] - b0;
-    const uint32_t l = (i == i0) ? 0u : uint32_t(t.lcp[i]);
-    bool ok = false;
-    if (l <= valid) {
-      uint32_t k = l, st = stack[l];
-      ok = true;
-      for (; k < len; ++k) {
-        const uint32_t nx = __ldg(table + size_t(st) * ncols + scol[t.sorted_bytes[b0 + k]]);
-        if (nx == CG_DEAD) { ok = false; break; }
-        st = nx;
-        stack[k + 1] = st;
-      }
-      valid = k;
-    }
-    // l > valid: the shared prefix already contains the byte that failed
-    if (ok) {
-      const uint32_t id = t.perm[i];
-      atomicOr(smask + (id >> 5), 1u << (id & 31));
-    }
-  }
-}
 
 __global__ void __launch_bounds__(kFillThreads) fill_bitmask_kernel(Tables t, const uint32_t* __restrict__ states,
                                                                       const uint16_t* __restrict__ gid,
@@ -79,17 +34,9 @@ __global__ void __launch_bounds__(kFillThreads) fill_bitmask_kernel(Tables t, co
   const uint32_t s = states[b];
 
   // rows that do not read the cache: bad grammar, forced token, dead or bad state
-  int mode = 0;  // 0 lookup, 1 zero row, 2 one-hot row
-  if (g >= t.n_g) mode = 1;
-  else if (f >= 0) mode = (uint32_t(f) < t.V) ? 2 : 1;
-  else if (s == CG_DEAD || s >= t.grammars[g].n_states) mode = 1;
-  else if (t.state_flags[t.grammars[g].state_off + s] & CG_STATE_FORCED_ONLY) mode = 1;
-  if (threadIdx.x == 0) {
-    if (g >= t.n_g) record_error(t.status, CG_DEV_BAD_GID);
-    else if (f >= 0 && uint32_t(f) >= t.V) record_error(t.status, CG_DEV_BAD_FORCED);
-    else if (f < 0 && s != CG_DEAD && s >= t.grammars[g].n_states) record_error(t.status, CG_DEV_BAD_STATE);
-    else if (mode == 1 && f < 0 && s != CG_DEAD) record_error(t.status, CG_DEV_MISSING_FORCED);
-  }
+  uint32_t err = 0;
+  const int mode = row_mask_mode(t, g, f, s, &err);  // 0 lookup, 1 zero row, 2 one-hot row
+  if (threadIdx.x == 0 && err) record_error(t.status, err);
   if (mode != 0) {
     for (uint32_t i = threadIdx.x; i < W; i += blockDim.x)
       out[i] = (mode == 2 && i == (uint32_t(f) >> 5)) ? (1u << (f & 31)) : 0u;
@@ -118,7 +65,7 @@ __global__ void __launch_bounds__(kFillThreads) fill_bitmask_kernel(Tables t, co
   for (uint32_t i = threadIdx.x; i < 256; i += blockDim.x) scol[i] = t.colmap[size_t(g) * 512 + i];
   if (threadIdx.x == 0) s_claim = atomicCAS(t.cache_state + cls, kStateEmpty, kStateBusy) == kStateEmpty;
   __syncthreads();
-  walk_tokens(t, gd, scol, s, smask);
+  walk_tokens(t, gd, scol, s, smask, threadIdx.x, blockDim.x);
   __syncthreads();
   const bool claimed = s_claim != 0u;
   uint32_t* cw = t.cache + size_t(cls) * W;
@@ -146,7 +93,7 @@ __global__ void __launch_bounds__(kFillThreads) prefill_kernel(Tables t, const u
   for (uint32_t i = threadIdx.x; i < W; i += blockDim.x) smask[i] = 0u;
   for (uint32_t i = threadIdx.x; i < 256; i += blockDim.x) scol[i] = t.colmap[size_t(g) * 512 + i];
   __syncthreads();
-  walk_tokens(t, t.grammars[g], scol, class_rep[cls], smask);
+  walk_tokens(t, t.grammars[g], scol, class_rep[cls], smask, threadIdx.x, blockDim.x);
   __syncthreads();
   uint32_t* cw = t.cache + size_t(cls) * W;
   for (uint32_t i = threadIdx.x; i < W; i += blockDim.x) cw[i] = smask[i];

@@ -24,7 +24,7 @@
 #include <mutex>
 #include <utility>
 
-#include "device.cuh"
+#include "row_ops.cuh"
 
 namespace cgk {
 
@@ -492,11 +492,95 @@ __device__ __forceinline__ void drain_stage(const uint4* stg, const uint16_t* sg
   }
 }
 
+// Inputs and outputs of the fused step (cg_step): the row's bitmask is built
+// in shared memory as cg_fill_bitmask would write it, and the sampled token is
+// accepted as cg_accept would.
+struct StepArgs {
+  Tables t;
+  const uint32_t* states;
+  const uint16_t* gid;      // may be null
+  const int32_t* forced;    // may be null
+  uint32_t* counts;         // may be null
+  uint32_t max_tokens;
+  uint32_t* out_states;
+  uint8_t* out_flags;
+  uint32_t* bitmask_out;    // may be null: the mask then never leaves the chip
+};
+
+// The row's mask in shared memory, as cg_fill_bitmask defines it (and written
+// to sa.bitmask_out when given).  All threads of the block take part; scol is
+// 512 bytes of free shared memory for the miss path.
+__device__ void step_row_mask(const StepArgs& sa, uint32_t b, uint32_t W, uint32_t* smask, uint16_t* scol,
+                              uint32_t& s_mode, uint32_t& s_cls, uint32_t& s_ready, uint32_t& s_claim,
+                              uint32_t& s_g, uint32_t& s_s, int32_t& s_f) {
+  const Tables& t = sa.t;
+  const uint32_t tid = threadIdx.x;
+  if (tid == 0) {
+    const uint32_t g = sa.gid ? sa.gid[b] : 0u;
+    const int32_t f = sa.forced ? sa.forced[b] : -1;
+    const uint32_t s = sa.states[b];
+    uint32_t err = 0;
+    const int mode = row_mask_mode(t, g, f, s, &err);
+    if (err) record_error(t.status, err);
+    uint32_t cls = 0, ready = 0;
+    if (mode == 0) {
+      cls = t.class_of[t.grammars[g].state_off + s];
+      ready = load_acquire(t.cache_state + cls) == kStateReady;
+    }
+    s_mode = uint32_t(mode);
+    s_cls = cls;
+    s_ready = ready;
+    s_g = g;
+    s_s = s;
+    s_f = f;
+  }
+  __syncthreads();
+  const uint32_t mode = s_mode;
+  if (mode == 1) {
+    for (uint32_t i = tid; i < W; i += blockDim.x) smask[i] = 0u;
+  } else if (mode == 2) {
+    const uint32_t f = uint32_t(s_f);
+    for (uint32_t i = tid; i < W; i += blockDim.x) smask[i] = (i == (f >> 5)) ? (1u << (f & 31)) : 0u;
+  } else if (s_ready) {
+    const uint32_t* crow = t.cache + size_t(s_cls) * W;
+    if ((W & 3u) == 0) {
+      const uint4* src = reinterpret_cast<const uint4*>(crow);
+      uint4* dst = reinterpret_cast<uint4*>(smask);
+      for (uint32_t i = tid; i < W / 4; i += blockDim.x) dst[i] = src[i];
+    } else {
+      for (uint32_t i = tid; i < W; i += blockDim.x) smask[i] = crow[i];
+    }
+  } else {
+    // miss: compute the class mask from the row's state, publish it if this
+    // block claims the class (as cg_fill_bitmask does)
+    const uint32_t g = s_g, cls = s_cls;
+    for (uint32_t i = tid; i < W; i += blockDim.x) smask[i] = 0u;
+    for (uint32_t i = tid; i < 256; i += blockDim.x) scol[i] = t.colmap[size_t(g) * 512 + i];
+    if (tid == 0) s_claim = atomicCAS(t.cache_state + cls, kStateEmpty, kStateBusy) == kStateEmpty;
+    __syncthreads();
+    walk_tokens(t, t.grammars[g], scol, s_s, smask, tid, blockDim.x);
+    __syncthreads();
+    if (s_claim) {
+      uint32_t* cw = t.cache + size_t(cls) * W;
+      for (uint32_t i = tid; i < W; i += blockDim.x) cw[i] = smask[i];
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) store_release(t.cache_state + cls, kStateReady);
+    }
+  }
+  if (sa.bitmask_out) {
+    __syncthreads();
+    uint32_t* out = sa.bitmask_out + size_t(b) * W;
+    for (uint32_t i = tid; i < W; i += blockDim.x) out[i] = smask[i];
+  }
+}
+
+template <bool STEP>
 __global__ void __launch_bounds__(kThreads, 2)
     stream_topp_kernel(void* logits, uint32_t V, uint32_t W, const uint32_t* __restrict__ bitmask, float temp,
                        float top_p, uint32_t k0, uint32_t k1, uint32_t step, uint32_t* __restrict__ out_tok,
                        float* __restrict__ probs, int inplace, uint32_t* cand_id, uint16_t* cand_key,
-                       uint32_t gcap, uint32_t* status) {
+                       uint32_t gcap, uint32_t* status, const StepArgs sa) {
   extern __shared__ __align__(128) unsigned char dsm[];
   unsigned char* ring = dsm;                                                // kStages slots
   uint4* lut = reinterpret_cast<uint4*>(dsm + kRing);                       // [256]
@@ -507,6 +591,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ float red_f[33];
   __shared__ unsigned long long red_u64[33];
   __shared__ uint32_t s_maxkey, s_flag, s_count, s_tau;
+  __shared__ uint32_t s_mode, s_cls, s_ready, s_claim, s_g, s_s;
+  __shared__ int32_t s_f;
 
   griddep_launch_dependents();
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, b = blockIdx.x;
@@ -532,9 +618,18 @@ __global__ void __launch_bounds__(kThreads, 2)
       w[q] = (((i >> (2 * q)) & 1u) ? 0x0000FFFFu : 0u) | (((i >> (2 * q + 1)) & 1u) ? 0xFFFF0000u : 0u);
     lut[i] = make_uint4(w[0], w[1], w[2], w[3]);
   }
-  griddep_wait();  // the bitmask comes from fill_bitmask
-  const uint32_t* mrow = bitmask + size_t(b) * W;
-  for (uint32_t i = tid; i < W; i += kThreads) smask[i] = mrow[i];
+  __syncthreads();  // barriers initialised
+  griddep_wait();   // the bitmask (or, fused, the states) come from the previous kernel
+  if (!STEP) {
+    const uint32_t* mrow = bitmask + size_t(b) * W;
+    for (uint32_t i = tid; i < W; i += kThreads) smask[i] = mrow[i];
+  } else {
+    // the logits do not depend on the mask: start the first copies now
+    if (warp == kConsumerWarps && lane == 0)
+      for (uint32_t k = 0; k < nchunks && k < uint32_t(kStages); ++k) issue_chunk(ring, full, row, V, k);
+    step_row_mask(sa, b, W, smask, reinterpret_cast<uint16_t*>(stg_all), s_mode, s_cls, s_ready, s_claim, s_g, s_s,
+                  s_f);
+  }
   __syncthreads();
 
   const float c = 1.4426950408889634f / temp;
@@ -549,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // ---- producer warp --------------------------------------------------------------
     if (lane == 0) {
       bool ok = true;
-      for (uint32_t k = 0; k < nchunks; ++k) {
+      for (uint32_t k = STEP ? min(nchunks, uint32_t(kStages)) : 0u; k < nchunks; ++k) {
         if (k >= uint32_t(kStages) && !mbar_wait(empty + k % kStages, ((k / kStages) - 1) & 1u)) {
           ok = false;
           break;
@@ -836,7 +931,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     tok = general_row<true, true, kTopP>(row, V, smask, reinterpret_cast<uint32_t*>(ring), temp, top_p, b, k0, k1,
                                          step, M2, S2);
   }
-  if (tid == 0) out_tok[b] = tok;
+  if (tid == 0) {
+    out_tok[b] = tok;
+    if (STEP) accept_row(sa.t, b, s_g, s_s, tok, s_f, sa.counts, sa.max_tokens, sa.out_states, sa.out_flags);
+  }
   if (probs || inplace) write_outputs<true, kTopP>(row, V, smask, tok, M, S, temp, probs, inplace, b);
 }
 
@@ -906,13 +1004,13 @@ cudaError_t launch_mask_and_sample(void* logits, int dtype, uint32_t B, uint32_t
   const bool vec = (V % ch == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
   const size_t s1 = fast::stream_smem(W);
   if (bf16 && vec && mode == kTopP && s1 <= 112 * 1024) {
-    cudaError_t e = allow_smem(reinterpret_cast<const void*>(fast::stream_topp_kernel), s1);
+    cudaError_t e = allow_smem(reinterpret_cast<const void*>(fast::stream_topp_kernel<false>), s1);
     if (e != cudaSuccess) return e;
     uint32_t* cand_id = static_cast<uint32_t*>(scratch);
     uint16_t* cand_key = reinterpret_cast<uint16_t*>(cand_id + size_t(B) * fast::kCandPerRow);
-    return launch_dependent(fast::stream_topp_kernel, dim3(B), dim3(fast::kThreads), s1, stream, logits, V, W,
-                            bitmask, temp, top_p, uint32_t(seed), uint32_t(seed >> 32), step, out_tok, probs, inplace,
-                            cand_id, cand_key, fast::kCandPerRow, status);
+    return launch_dependent(fast::stream_topp_kernel<false>, dim3(B), dim3(fast::kThreads), s1, stream, logits, V,
+                            W, bitmask, temp, top_p, uint32_t(seed), uint32_t(seed >> 32), step, out_tok, probs,
+                            inplace, cand_id, cand_key, fast::kCandPerRow, status, fast::StepArgs{});
   }
   if (bf16)
     return vec ? launch_mode<true, true>(mode, logits, B, V, W, bitmask, temp, top_p, seed, step, out_tok, probs,
@@ -923,6 +1021,31 @@ cudaError_t launch_mask_and_sample(void* logits, int dtype, uint32_t B, uint32_t
                                         inplace, stream)
              : launch_mode<false, false>(mode, logits, B, V, W, bitmask, temp, top_p, seed, step, out_tok, probs,
                                          inplace, stream);
+}
+
+// The fused step (fill + sample + accept) runs as one kernel when the sampling
+// takes the top-p bf16 path; returns false (nothing launched) otherwise.
+bool step_fusable(int dtype, uint32_t V, uint32_t W, float temp, float top_p, const void* logits) {
+  return dtype == CG_BF16 && temp > 0.f && top_p < 1.f && V % 8 == 0 &&
+         (reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && fast::stream_smem(W) <= 112 * 1024;
+}
+
+cudaError_t launch_step(const Tables& t, const uint32_t* states, const uint16_t* gid, const int32_t* forced,
+                        uint32_t B, void* logits, uint32_t V, float temp, float top_p, uint64_t seed, uint32_t step,
+                        uint32_t* counts, uint32_t max_tokens, uint32_t* bitmask_out, uint32_t* out_tok,
+                        uint32_t* out_states, uint8_t* out_flags, void* scratch, cudaStream_t stream) {
+  if (B == 0) return cudaSuccess;
+  const uint32_t W = t.W;
+  const size_t s1 = fast::stream_smem(W);
+  cudaError_t e = allow_smem(reinterpret_cast<const void*>(fast::stream_topp_kernel<true>), s1);
+  if (e != cudaSuccess) return e;
+  uint32_t* cand_id = static_cast<uint32_t*>(scratch);
+  uint16_t* cand_key = reinterpret_cast<uint16_t*>(cand_id + size_t(B) * fast::kCandPerRow);
+  const fast::StepArgs sa{t, states, gid, forced, counts, max_tokens, out_states, out_flags, bitmask_out};
+  return launch_dependent(fast::stream_topp_kernel<true>, dim3(B), dim3(fast::kThreads), s1, stream, logits, V, W,
+                          static_cast<const uint32_t*>(nullptr), temp, top_p, uint32_t(seed), uint32_t(seed >> 32),
+                          step, out_tok, static_cast<float*>(nullptr), 0, cand_id, cand_key, fast::kCandPerRow,
+                          t.status, sa);
 }
 
 }  // namespace cgk

@@ -1,0 +1,154 @@
+// Per-row pieces shared by the step kernels: the bitmask source of a row (as
+// cg_fill_bitmask defines it), the trie walk that computes a class mask, and
+// the automaton advance of cg_accept.  The separate kernels and the fused step
+// kernel call the same functions, so they agree bit for bit.
+#pragma once
+
+#include "device.cuh"
+
+namespace cgk {
+
+constexpr uint32_t kStateEmpty = 0, kStateBusy = 1, kStateReady = 2;
+
+__device__ __forceinline__ uint32_t load_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void store_release(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Where row's mask comes from (usetacet.com/docs/grammar, "The guarantee": the
+// mask holds exactly the tokens the grammar allows): 0 the state's mask class,
+// 1 an all-zero row (bad grammar id, bad forced id, dead or out-of-range state,
+// forced-only state without a forced token), 2 a one-hot row at the forced
+// token.  *err receives the CG_DEV_* code to record (0 for none).
+__device__ __forceinline__ int row_mask_mode(const Tables& t, uint32_t g, int32_t f, uint32_t s, uint32_t* err) {
+  int mode = 0;
+  if (g >= t.n_g) mode = 1;
+  else if (f >= 0) mode = (uint32_t(f) < t.V) ? 2 : 1;
+  else if (s == CG_DEAD || s >= t.grammars[g].n_states) mode = 1;
+  else if (t.state_flags[t.grammars[g].state_off + s] & CG_STATE_FORCED_ONLY) mode = 1;
+  uint32_t e = 0;
+  if (g >= t.n_g) e = CG_DEV_BAD_GID;
+  else if (f >= 0 && uint32_t(f) >= t.V) e = CG_DEV_BAD_FORCED;
+  else if (f < 0 && s != CG_DEAD && s >= t.grammars[g].n_states) e = CG_DEV_BAD_STATE;
+  else if (mode == 1 && f < 0 && s != CG_DEAD) e = CG_DEV_MISSING_FORCED;
+  *err = e;
+  return mode;
+}
+
+// Walk all tokens from state s of grammar g with threads tid = 0..nthreads-1;
+// sets allowed bits in smask[W] (zeroed by the caller).  Each thread takes a
+// contiguous run of the vocabulary in trie (lexicographic) order and resumes
+// each token's walk from the state reached after the prefix it shares with the
+// previous token, so shared prefixes are walked once.
+__device__ inline void walk_tokens(const Tables& t, const DevGrammar& gd, const uint16_t* scol, uint32_t s,
+                                   uint32_t* smask, uint32_t tid, uint32_t nthreads) {
+  const uint32_t V = t.V;
+  const uint32_t per = (V + nthreads - 1) / nthreads;
+  const uint32_t i0 = tid * per;
+  const uint32_t i1 = min(V, i0 + per);
+  const uint32_t* table = t.table + gd.table_off;
+  const uint32_t ncols = gd.n_cols;
+  uint32_t stack[65];
+  stack[0] = s;
+  uint32_t valid = 0;  // stack[0..valid] hold the states after 0..valid bytes of the previous token
+  for (uint32_t i = i0; i < i1; ++i) {
+    const uint32_t b0 = t.sorted_off[i], len = t.sorted_off[i + 1] - b0;
+    const uint32_t l = (i == i0) ? 0u : uint32_t(t.lcp[i]);
+    bool ok = false;
+    if (l <= valid) {
+      uint32_t k = l, st = stack[l];
+      ok = true;
+      for (; k < len; ++k) {
+        const uint32_t nx = __ldg(table + size_t(st) * ncols + scol[t.sorted_bytes[b0 + k]]);
+        if (nx == CG_DEAD) { ok = false; break; }
+        st = nx;
+        stack[k + 1] = st;
+      }
+      valid = k;
+    }
+    // l > valid: the shared prefix already contains the byte that failed
+    if (ok) {
+      const uint32_t id = t.perm[i];
+      atomicOr(smask + (id >> 5), 1u << (id & 31));
+    }
+  }
+}
+
+constexpr uint32_t kPrefetch = 16;  // token bytes whose columns are loaded up front
+
+// Advance one row by its token (labs.miniml.ai "Evaluator aware decoding":
+// after injection the grammar state must be advanced; a forced token's bytes
+// are walked as host-injected symbols).  With token counts, finished or capped
+// rows restart from state 0 (usetacet.com/docs/grammar, "A valid call also has
+// to end").  Writes out_states[b], out_flags[b] and counts[b].
+__device__ inline void accept_row(const Tables& t, uint32_t b, uint32_t g, uint32_t s, uint32_t tok, int32_t f,
+                                  uint32_t* counts, uint32_t max_tokens, uint32_t* out_states, uint8_t* out_flags) {
+  uint32_t ns = s;
+  uint8_t fl = 0;
+  if (g >= t.n_g) {
+    record_error(t.status, CG_DEV_BAD_GID);
+    ns = CG_DEAD;
+    fl = CG_FLAG_REJECTED;
+  } else if (tok == CG_NO_TOKEN) {
+    fl = CG_FLAG_NO_TOKEN;
+  } else if (tok >= t.V) {
+    record_error(t.status, CG_DEV_BAD_TOKEN);
+    ns = CG_DEAD;
+    fl = CG_FLAG_REJECTED;
+  } else if (s == CG_DEAD) {
+    fl = CG_FLAG_REJECTED;
+  } else {
+    const DevGrammar gd = t.grammars[g];
+    if (s >= gd.n_states) {
+      record_error(t.status, CG_DEV_BAD_STATE);
+      ns = CG_DEAD;
+      fl = CG_FLAG_REJECTED;
+    } else if (f >= 0 && tok != uint32_t(f)) {
+      record_error(t.status, CG_DEV_FORCED_MISMATCH);
+      ns = CG_DEAD;
+      fl = CG_FLAG_REJECTED;
+    } else {
+      const uint32_t shift = f >= 0 ? 256u : 0u;
+      const uint16_t* cols = t.colmap + size_t(g) * 512 + shift;
+      const uint32_t* table = t.table + gd.table_off;
+      // the token's columns first (independent loads), then the chain of
+      // table lookups
+      const uint32_t i0 = t.tok_off[tok], len = t.tok_off[tok + 1] - i0;
+      uint32_t col[kPrefetch];
+#pragma unroll
+      for (uint32_t k = 0; k < kPrefetch; ++k) col[k] = k < len ? cols[t.tok_bytes[i0 + k]] : 0u;
+      uint32_t st = s;
+#pragma unroll
+      for (uint32_t k = 0; k < kPrefetch; ++k)
+        if (k < len && st != CG_DEAD) st = table[size_t(st) * gd.n_cols + col[k]];
+      for (uint32_t i = i0 + kPrefetch; i < i0 + len && st != CG_DEAD; ++i)
+        st = table[size_t(st) * gd.n_cols + cols[t.tok_bytes[i]]];
+      ns = st;
+      if (st == CG_DEAD) {
+        record_error(t.status, CG_DEV_REJECTED);
+        fl = CG_FLAG_REJECTED;
+      } else {
+        const uint8_t sf = t.state_flags[gd.state_off + st];
+        if (sf & CG_STATE_SINK) fl |= CG_FLAG_DONE;
+        if (sf & CG_STATE_FORCED_ONLY) fl |= CG_FLAG_FORCED_NEXT;
+      }
+    }
+  }
+  if (counts) {
+    uint32_t n = counts[b] + (tok != CG_NO_TOKEN ? 1u : 0u);
+    if ((fl & CG_FLAG_DONE) || n >= max_tokens) {
+      if (!(fl & CG_FLAG_DONE)) fl |= CG_FLAG_CAPPED;
+      ns = 0u;
+      n = 0u;
+    }
+    counts[b] = n;
+  }
+  out_states[b] = ns;
+  out_flags[b] = fl;
+}
+
+}  // namespace cgk

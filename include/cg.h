@@ -225,6 +225,26 @@ int cg_mask_and_sample(cg_ctx* c, void* d_logits, int dtype, uint32_t B, uint32_
                        const uint32_t* d_bitmask, float temp, float top_p, uint64_t seed,
                        uint32_t step, uint32_t* d_out_tok, float* d_probs, uint32_t flags);
 
+/* One decode step in one call: cg_fill_bitmask, cg_mask_and_sample (no probs,
+ * no in-place write) and cg_accept with the same arguments, giving the same
+ * tokens, states, flags and counts bit for bit.  When the sampling takes the
+ * top-p bf16 path (dtype CG_BF16, temp > 0, top_p < 1, V a multiple of 8,
+ * 16-byte aligned logits) the three run as one kernel per row: the row's mask
+ * is built on chip from the mask-class cache, the logits are streamed once, and
+ * the token is accepted at the end of the row's block.  Otherwise the three
+ * calls run in turn.
+ *  d_bitmask : u32 [B][W] or NULL; when given it receives the masks exactly as
+ *              cg_fill_bitmask writes them.  With NULL on the unfused path the
+ *              context keeps the masks in a buffer of its own (grown like the
+ *              sampling scratch: the first call with a larger B synchronises
+ *              the stream and allocates).
+ *  d_out_states may equal d_states (each row reads its state before writing it).
+ * Errors: as the three calls. */
+int cg_step(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const int32_t* d_forced, uint32_t B,
+            void* d_logits, int dtype, uint32_t V, float temp, float top_p, uint64_t seed, uint32_t step,
+            uint32_t* d_counts, uint32_t max_tokens, uint32_t* d_bitmask, uint32_t* d_out_tok,
+            uint32_t* d_out_states, uint8_t* d_out_flags);
+
 /* Variant of cg_mask_and_sample that never allocates device memory.  The pages
  * have no counterpart: it is a deployment variant of step 2, not a step of the
  * method.  Arguments, results and error codes are those of cg_mask_and_sample,
