@@ -320,6 +320,7 @@ constexpr uint32_t kNucCap = (kRing - kHistBytes) / 6;          // packed nucleu
 constexpr float kMarginZ = 9.0f;                                // nats below the maximum kept as candidates
 constexpr float kNoRef = -1e30f;                                // finite reference before any allowed logit
 constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint32_t kMaxCols = 512;                              // symbol columns a grammar can have
 constexpr uint32_t kSlots = 16;                                 // list entries per thread after the stream
 constexpr uint32_t kCandPerRow = kThreads * kSlots;             // candidate list entries per row (8192)
 constexpr uint32_t kBatchIds = 4;                               // nucleus id loads in flight per thread
@@ -508,25 +509,46 @@ struct StepArgs {
 };
 
 // The row's mask in shared memory, as cg_fill_bitmask defines it (and written
-// to sa.bitmask_out when given).  All threads of the block take part; scol is
-// 512 bytes of free shared memory for the miss path.
+// to sa.bitmask_out when given).  All threads of the block take part.  A
+// cached class mask arrives as one bulk copy completing on *mbar_mask, issued
+// as soon as the class is known (before its ready flag is read: after
+// cg_ctx_prefill it always is); the caller waits on it with parity 0 when
+// *s_copied is set.  Also stages grammar g's column map (scols, 512 entries)
+// and the row's transition-table row (srow, n_cols entries) for the accept at
+// the end.  scol is 512 bytes of free shared memory for the miss path.
 __device__ void step_row_mask(const StepArgs& sa, uint32_t b, uint32_t W, uint32_t* smask, uint16_t* scol,
-                              uint32_t& s_mode, uint32_t& s_cls, uint32_t& s_ready, uint32_t& s_claim,
-                              uint32_t& s_g, uint32_t& s_s, int32_t& s_f) {
+                              uint16_t* scols, uint32_t* srow, uint64_t* mbar_mask, uint32_t& s_copied,
+                              uint32_t& s_srow, uint32_t& s_mode, uint32_t& s_cls, uint32_t& s_ready,
+                              uint32_t& s_claim, uint32_t& s_g, uint32_t& s_s, int32_t& s_f) {
   const Tables& t = sa.t;
   const uint32_t tid = threadIdx.x;
   if (tid == 0) {
     const uint32_t g = sa.gid ? sa.gid[b] : 0u;
     const int32_t f = sa.forced ? sa.forced[b] : -1;
     const uint32_t s = sa.states[b];
+    uint32_t copied = 0, cls = 0, ready = 0, srow_ok = 0;
+    // the class of an in-range state, fetched beside its flags so that the
+    // mask copy can start before the mode is settled
+    if (g < t.n_g && s != CG_DEAD) {
+      const DevGrammar gd = t.grammars[g];
+      if (s < gd.n_states) {
+        srow_ok = gd.n_cols <= kMaxCols;
+        if (f < 0) {
+          cls = t.class_of[gd.state_off + s];
+          if ((W & 3u) == 0) {
+            mbar_expect_tx(mbar_mask, W * 4);
+            bulk_g2s(smask, t.cache + size_t(cls) * W, W * 4, mbar_mask);
+            copied = 1;
+          }
+        }
+      }
+    }
     uint32_t err = 0;
     const int mode = row_mask_mode(t, g, f, s, &err);
     if (err) record_error(t.status, err);
-    uint32_t cls = 0, ready = 0;
-    if (mode == 0) {
-      cls = t.class_of[t.grammars[g].state_off + s];
-      ready = load_acquire(t.cache_state + cls) == kStateReady;
-    }
+    if (mode == 0) ready = load_acquire(t.cache_state + cls) == kStateReady;
+    s_copied = copied;
+    s_srow = srow_ok;
     s_mode = uint32_t(mode);
     s_cls = cls;
     s_ready = ready;
@@ -536,18 +558,27 @@ __device__ void step_row_mask(const StepArgs& sa, uint32_t b, uint32_t W, uint32
   }
   __syncthreads();
   const uint32_t mode = s_mode;
+  if (s_g < t.n_g) {
+    for (uint32_t i = tid; i < 512; i += blockDim.x) scols[i] = t.colmap[size_t(s_g) * 512 + i];
+    if (s_srow) {
+      const DevGrammar gd = t.grammars[s_g];
+      for (uint32_t i = tid; i < gd.n_cols; i += blockDim.x) srow[i] = t.table[gd.table_off + size_t(s_s) * gd.n_cols + i];
+    }
+  }
+  if (s_copied && !(mode == 0 && s_ready)) {
+    // the speculative copy is not the mask: let it land before overwriting
+    if (tid == 0) mbar_wait(mbar_mask, 0);
+    __syncthreads();
+    if (tid == 0) s_copied = 0;
+  }
   if (mode == 1) {
     for (uint32_t i = tid; i < W; i += blockDim.x) smask[i] = 0u;
   } else if (mode == 2) {
     const uint32_t f = uint32_t(s_f);
     for (uint32_t i = tid; i < W; i += blockDim.x) smask[i] = (i == (f >> 5)) ? (1u << (f & 31)) : 0u;
   } else if (s_ready) {
-    const uint32_t* crow = t.cache + size_t(s_cls) * W;
-    if ((W & 3u) == 0) {
-      const uint4* src = reinterpret_cast<const uint4*>(crow);
-      uint4* dst = reinterpret_cast<uint4*>(smask);
-      for (uint32_t i = tid; i < W / 4; i += blockDim.x) dst[i] = src[i];
-    } else {
+    if (!s_copied) {
+      const uint32_t* crow = t.cache + size_t(s_cls) * W;
       for (uint32_t i = tid; i < W; i += blockDim.x) smask[i] = crow[i];
     }
   } else {
@@ -568,11 +599,6 @@ __device__ void step_row_mask(const StepArgs& sa, uint32_t b, uint32_t W, uint32
       if (tid == 0) store_release(t.cache_state + cls, kStateReady);
     }
   }
-  if (sa.bitmask_out) {
-    __syncthreads();
-    uint32_t* out = sa.bitmask_out + size_t(b) * W;
-    for (uint32_t i = tid; i < W; i += blockDim.x) out[i] = smask[i];
-  }
 }
 
 template <bool STEP>
@@ -587,7 +613,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint4* stg_all = lut + 256;                                               // [kConsumerWarps][kStage]
   uint16_t* sgid_all = reinterpret_cast<uint16_t*>(stg_all + kConsumerWarps * kStage);
   uint32_t* smask = reinterpret_cast<uint32_t*>(sgid_all + kConsumerWarps * kStage);  // [W]
-  __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
+  uint16_t* scols = reinterpret_cast<uint16_t*>(smask + ((W + 3) & ~3u));          // [512] (fused step)
+  uint32_t* srow = reinterpret_cast<uint32_t*>(scols + 512);                        // [kMaxCols] (fused step)
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], mbar_mask;
+  __shared__ uint32_t s_copied, s_srow;
   __shared__ float red_f[33];
   __shared__ unsigned long long red_u64[33];
   __shared__ uint32_t s_maxkey, s_flag, s_count, s_tau;
@@ -606,10 +635,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(full + i, 1);
       mbar_init(empty + i, kConsumerWarps);
     }
+    mbar_init(&mbar_mask, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_maxkey = fkey(-INFINITY);
     s_flag = 0;  // bit 0: a wait ran out
     s_count = 0;
+    s_copied = 0;
+    s_srow = 0;
   }
   for (uint32_t i = tid; i < 256; i += kThreads) {
     uint32_t w[4];
@@ -627,8 +659,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     // the logits do not depend on the mask: start the first copies now
     if (warp == kConsumerWarps && lane == 0)
       for (uint32_t k = 0; k < nchunks && k < uint32_t(kStages); ++k) issue_chunk(ring, full, row, V, k);
-    step_row_mask(sa, b, W, smask, reinterpret_cast<uint16_t*>(stg_all), s_mode, s_cls, s_ready, s_claim, s_g, s_s,
-                  s_f);
+    step_row_mask(sa, b, W, smask, reinterpret_cast<uint16_t*>(stg_all), scols, srow, &mbar_mask, s_copied, s_srow,
+                  s_mode, s_cls, s_ready, s_claim, s_g, s_s, s_f);
   }
   __syncthreads();
 
@@ -659,6 +691,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint16_t* sgid = sgid_all + warp * kStage;
     uint32_t sc = 0;  // staged groups of this warp (warp-uniform)
     const uint32_t lt = (1u << lane) - 1u;
+    // the row's mask (fused step: a bulk copy from the mask cache)
+    if (STEP && s_copied && !mbar_wait(&mbar_mask, 0)) atomicOr(&s_flag, 1u);
     // chunk 0's maximum seeds the reference, so the first chunk does not flag
     // every group
     if (!mbar_wait(full + 0, 0)) atomicOr(&s_flag, 1u);
@@ -752,6 +786,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint32_t issued = (nchunks - sl + kStages - 1) / kStages;
       mbar_wait(full + sl, (issued - 1) & 1u);
     }
+    if (STEP && s_copied) mbar_wait(&mbar_mask, 0);
   }
   const float M = fkey_inv(s_maxkey);  // -inf when no logit is allowed
   // S: per-thread partial sums, warp sums and the 16 warp sums, all in float
@@ -933,13 +968,20 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   if (tid == 0) {
     out_tok[b] = tok;
-    if (STEP) accept_row(sa.t, b, s_g, s_s, tok, s_f, sa.counts, sa.max_tokens, sa.out_states, sa.out_flags);
+    if (STEP)
+      accept_row(sa.t, b, s_g, s_s, tok, s_f, sa.counts, sa.max_tokens, sa.out_states, sa.out_flags,
+                 s_g < sa.t.n_g ? scols : nullptr, s_srow ? srow : nullptr);
+  }
+  if (STEP && sa.bitmask_out) {
+    uint32_t* out = sa.bitmask_out + size_t(b) * W;
+    for (uint32_t i = tid; i < W; i += kThreads) out[i] = smask[i];
   }
   if (probs || inplace) write_outputs<true, kTopP>(row, V, smask, tok, M, S, temp, probs, inplace, b);
 }
 
 size_t stream_smem(uint32_t W) {
-  return size_t(kRing) + 4096 + size_t(kConsumerWarps) * kStage * 18 + size_t((W + 3) & ~3u) * 4;
+  return size_t(kRing) + 4096 + size_t(kConsumerWarps) * kStage * 18 + size_t((W + 3) & ~3u) * 4 + 512 * 2 +
+         size_t(kMaxCols) * 4;
 }
 
 }  // namespace fast

@@ -85,8 +85,12 @@ constexpr uint32_t kPrefetch = 16;  // token bytes whose columns are loaded up f
 // are walked as host-injected symbols).  With token counts, finished or capped
 // rows restart from state 0 (usetacet.com/docs/grammar, "A valid call also has
 // to end").  Writes out_states[b], out_flags[b] and counts[b].
+// cols_g (optional) is a copy of grammar g's 512-entry symbol -> column map
+// and srow (optional) a copy of row s of its transition table, both in shared
+// memory: they only shorten the chain of dependent loads.
 __device__ inline void accept_row(const Tables& t, uint32_t b, uint32_t g, uint32_t s, uint32_t tok, int32_t f,
-                                  uint32_t* counts, uint32_t max_tokens, uint32_t* out_states, uint8_t* out_flags) {
+                                  uint32_t* counts, uint32_t max_tokens, uint32_t* out_states, uint8_t* out_flags,
+                                  const uint16_t* cols_g = nullptr, const uint32_t* srow = nullptr) {
   uint32_t ns = s;
   uint8_t fl = 0;
   if (g >= t.n_g) {
@@ -113,7 +117,7 @@ __device__ inline void accept_row(const Tables& t, uint32_t b, uint32_t g, uint3
       fl = CG_FLAG_REJECTED;
     } else {
       const uint32_t shift = f >= 0 ? 256u : 0u;
-      const uint16_t* cols = t.colmap + size_t(g) * 512 + shift;
+      const uint16_t* cols = (cols_g ? cols_g : t.colmap + size_t(g) * 512) + shift;
       const uint32_t* table = t.table + gd.table_off;
       // the token's columns first (independent loads), then the chain of
       // table lookups
@@ -124,7 +128,7 @@ __device__ inline void accept_row(const Tables& t, uint32_t b, uint32_t g, uint3
       uint32_t st = s;
 #pragma unroll
       for (uint32_t k = 0; k < kPrefetch; ++k)
-        if (k < len && st != CG_DEAD) st = table[size_t(st) * gd.n_cols + col[k]];
+        if (k < len && st != CG_DEAD) st = (k == 0 && srow) ? srow[col[0]] : table[size_t(st) * gd.n_cols + col[k]];
       for (uint32_t i = i0 + kPrefetch; i < i0 + len && st != CG_DEAD; ++i)
         st = table[size_t(st) * gd.n_cols + cols[t.tok_bytes[i]]];
       ns = st;
