@@ -111,10 +111,8 @@ class ClockSampler:
 
 
 def _dist():
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return world, rank, local
+    from grammar_constrained_decoding_gb300.replicas import rank_info
+    return rank_info()
 
 
 def run_ours(args) -> dict | None:
@@ -125,13 +123,10 @@ def run_ours(args) -> dict | None:
     from workloads import CONFIGS, GRAMMARS, make_vocab
     from workloads.logits import make_logits_device
 
+    from grammar_constrained_decoding_gb300 import replicas
     world, rank, local = _dist()
     torch.cuda.set_device(local)
-    pg = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-        pg = dist
+    pg = replicas.init("nccl", torch.device("cuda", local))  # replicas: rows shard, nothing is exchanged
     cfg = CONFIGS[args.config]
     B, V = cfg.B, cfg.V
     W = (V + 31) // 32
@@ -151,7 +146,7 @@ def run_ours(args) -> dict | None:
     step_bytes = B * V * esz
     R = max(2, -(-4 * l2 // step_bytes))
     gen = torch.Generator(device="cuda")
-    gen.manual_seed(cfg.logit_seed + 1000 * rank)
+    gen.manual_seed(replicas.replica_seed(cfg.logit_seed, rank))
     bufs = [make_logits_device(B, V, 0, cfg.sigma, cfg.boost, cfg.boost_frac, cfg.dtype, "cuda", gen)
             for _ in range(R)]
     gid = None
@@ -244,10 +239,7 @@ def run_ours(args) -> dict | None:
     three_ms = s0.elapsed_time(s1) / args.steps
     if ctx.status() != 0:
         raise RuntimeError("device status after the three-call steps")
-    if pg:
-        t = torch.tensor([ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = replicas.max_over_ranks(ms, pg, "cuda")
     time.sleep(0.3)
     clocks = sampler.summary(t0, t1) if sampler else None
     if sampler:
@@ -281,11 +273,11 @@ def run_ours(args) -> dict | None:
     peaks = _peaks()
     achieved = alg_bytes / (k2_avg_ms * 1e-3) / 1e9
     traffic = _traffic_record()
-    units = B * args.steps * world
+    units = B * args.steps * world   # every rank decodes its own B rows
     info = ctx.info()
     out = {
         "metric": METRIC,
-        "value": round(units / (ms * 1e-3), 1),
+        "value": round(replicas.job_throughput(B * args.steps, world, ms), 1),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
