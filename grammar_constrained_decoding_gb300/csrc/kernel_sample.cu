@@ -979,6 +979,170 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (probs || inplace) write_outputs<true, kTopP>(row, V, smask, tok, M, S, temp, probs, inplace, b);
 }
 
+// ============================================================================
+// Greedy and full-softmax rows (bf16): the same bulk-copy ring, one CTA per
+// row; the consumers keep the best (value, id) of their groups.  Greedy: the
+// largest allowed logit, lowest id among equal ones.  Full: Gumbel-max over
+// every allowed logit, z_t + g_t with z = x / temp and g from the row's
+// Philox stream (two 4-word blocks per 8-logit group); fully masked groups
+// draw nothing.  With probabilities requested, the full mode also sums
+// exp2((x - m) c) for S.
+// ============================================================================
+template <int MODE, bool WANT_S>
+__global__ void __launch_bounds__(kThreads, 2)
+    stream_pick_kernel(void* logits, uint32_t V, uint32_t W, const uint32_t* __restrict__ bitmask, float temp,
+                       uint32_t k0, uint32_t k1, uint32_t step, uint32_t* __restrict__ out_tok,
+                       float* __restrict__ probs, int inplace, uint32_t* status) {
+  extern __shared__ __align__(128) unsigned char dsm[];
+  unsigned char* ring = dsm;                                  // kStages slots
+  uint4* lut = reinterpret_cast<uint4*>(dsm + kRing);         // [256]
+  uint32_t* smask = reinterpret_cast<uint32_t*>(lut + 256);   // [W]
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
+  __shared__ float red_f[33];
+  __shared__ unsigned long long red_u64[33];
+  __shared__ uint32_t s_flag;
+
+  griddep_launch_dependents();
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, b = blockIdx.x;
+  char* row = reinterpret_cast<char*>(logits) + size_t(b) * V * 2;
+  const uint32_t nchunks = (V + kChunkElems - 1) / kChunkElems;
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, kConsumerWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    s_flag = 0;
+  }
+  for (uint32_t i = tid; i < 256; i += kThreads) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      w[q] = (((i >> (2 * q)) & 1u) ? 0x0000FFFFu : 0u) | (((i >> (2 * q + 1)) & 1u) ? 0xFFFF0000u : 0u);
+    lut[i] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  __syncthreads();
+  griddep_wait();  // the bitmask comes from fill_bitmask
+  const uint32_t* mrow = bitmask + size_t(b) * W;
+  for (uint32_t i = tid; i < W; i += kThreads) smask[i] = mrow[i];
+  __syncthreads();
+
+  const float c = (MODE == kGreedy) ? 0.f : 1.4426950408889634f / temp;
+  const uint8_t* smask8 = reinterpret_cast<const uint8_t*>(smask);
+  unsigned long long best = 0ull;  // packed (value or score, id); 0 = none
+  float bestv = -INFINITY;         // greedy: this thread's best value
+  float lm = -INFINITY;            // this thread's largest allowed logit
+  float mt = kNoRef;               // reference of this thread's sums (WANT_S)
+  float acc[kAcc];
+#pragma unroll
+  for (int j = 0; j < kAcc; ++j) acc[j] = 0.f;
+
+  if (warp == kConsumerWarps) {
+    if (lane == 0) {
+      bool ok = true;
+      for (uint32_t k = 0; k < nchunks; ++k) {
+        if (k >= uint32_t(kStages) && !mbar_wait(empty + k % kStages, ((k / kStages) - 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        issue_chunk(ring, full, row, V, k);
+      }
+      if (!ok) atomicOr(&s_flag, 1u);
+    }
+  } else {
+    for (uint32_t k = 0; k < nchunks; ++k) {
+      const uint32_t slot = k % kStages;
+      if (!mbar_wait(full + slot, (k / kStages) & 1u)) {
+        atomicOr(&s_flag, 1u);
+        break;
+      }
+      const uint4* r4 = reinterpret_cast<const uint4*>(ring + size_t(slot) * kChunkBytes);
+      const uint32_t gbase = k * kGroupsPerChunk;
+      const uint32_t ngroups = min(kGroupsPerChunk, V / 8 - gbase);
+      uint4 v[2];
+      uint32_t mb[2];
+#pragma unroll
+      for (uint32_t g = 0; g < 2; ++g) {
+        const uint32_t gi = tid + kConsumers * g;
+        v[g] = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+        mb[g] = 0;
+        if (gi < ngroups) {
+          mb[g] = smask8[gbase + gi];
+          v[g] = apply_mask(r4[gi], lut[mb[g]]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + slot);  // the slot's data are in registers
+#pragma unroll
+      for (uint32_t g = 0; g < 2; ++g) {
+        const uint32_t t0 = (gbase + tid + kConsumers * g) * 8;  // id of the group's first logit
+        const float gm = group_max(v[g]);
+        lm = fmaxf(lm, gm);
+        if (MODE == kGreedy) {
+          if (gm > bestv) {  // strictly: this thread sees ids in increasing order
+            uint32_t e = 0;
+            while (e < 7 && bf16_bits_to_float(group_bits(v[g], e)) != gm) ++e;
+            best = pack_best(gm, t0 + e);
+            bestv = gm;
+          }
+        } else if (mb[g]) {
+          const uint4 p0 = philox4x32_10(make_uint4(t0 >> 2, b, step, 0u), k0, k1);
+          const uint4 p1 = philox4x32_10(make_uint4((t0 >> 2) + 1u, b, step, 0u), k0, k1);
+#pragma unroll
+          for (uint32_t e = 0; e < 8; ++e) {
+            if ((mb[g] >> e) & 1u) {
+              const float x = bf16_bits_to_float(group_bits(v[g], e));
+              const uint32_t w = philox_word(e < 4 ? p0 : p1, e & 3u);
+              best = max(best, pack_best(__fdiv_rn(x, temp) + gumbel_from_word(w), t0 + e));
+            }
+          }
+        }
+      }
+      if (WANT_S) {
+        const float gm = fmaxf(group_max(v[0]), group_max(v[1]));
+        if (gm > mt) {
+          const float r = ex2((mt - gm) * c);
+#pragma unroll
+          for (int j = 0; j < kAcc; ++j) acc[j] *= r;
+          mt = gm;
+        }
+        const float mc = mt * c;
+        add_exps(acc, v[0], c, mc);
+        add_exps(acc, v[1], c, mc);
+      }
+    }
+  }
+  __syncthreads();
+  if ((s_flag & 1u) && tid == 0) {
+    for (uint32_t sl = 0; sl < uint32_t(kStages) && sl < nchunks; ++sl) {
+      const uint32_t issued = (nchunks - sl + kStages - 1) / kStages;
+      mbar_wait(full + sl, (issued - 1) & 1u);
+    }
+  }
+  best = block_reduce(best, MaxOp(), 0ull, red_u64);
+  const float M = block_reduce(lm, MaxOp(), -INFINITY, red_f);
+  double S = 0.0;
+  if (WANT_S) {
+    float part = 0.f;
+    if (M > -INFINITY) {
+      float a = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < kAcc; ++jj) a += acc[jj];
+      if (a > 0.f) part = a * ex2((mt - M) * c);
+    }
+    S = double(block_reduce(part, SumOp(), 0.f, red_f));
+  }
+  uint32_t tok = best ? best_id(best) : CG_NO_TOKEN;
+  if (s_flag & 1u) {
+    tok = CG_NO_TOKEN;
+    if (tid == 0) record_error(status, CG_DEV_TIMEOUT);
+  }
+  if (tid == 0) out_tok[b] = tok;
+  if (probs || inplace) write_outputs<true, MODE>(row, V, smask, tok, M, S, temp, probs, inplace, b);
+}
+
+size_t pick_smem(uint32_t W) { return size_t(kRing) + 4096 + size_t((W + 3) & ~3u) * 4; }
+
 size_t stream_smem(uint32_t W) {
   return size_t(kRing) + 4096 + size_t(kConsumerWarps) * kStage * 18 + size_t((W + 3) & ~3u) * 4 + 512 * 2 +
          size_t(kMaxCols) * 4;
@@ -1053,6 +1217,15 @@ cudaError_t launch_mask_and_sample(void* logits, int dtype, uint32_t B, uint32_t
     return launch_dependent(fast::stream_topp_kernel<false>, dim3(B), dim3(fast::kThreads), s1, stream, logits, V,
                             W, bitmask, temp, top_p, uint32_t(seed), uint32_t(seed >> 32), step, out_tok, probs,
                             inplace, cand_id, cand_key, fast::kCandPerRow, status, fast::StepArgs{});
+  }
+  if (bf16 && vec && mode != kTopP && fast::pick_smem(W) <= 112 * 1024) {
+    const size_t sm = fast::pick_smem(W);
+    auto k = mode == kGreedy ? fast::stream_pick_kernel<kGreedy, false>
+                             : (probs ? fast::stream_pick_kernel<kFull, true> : fast::stream_pick_kernel<kFull, false>);
+    cudaError_t e = allow_smem(reinterpret_cast<const void*>(k), sm);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(k, dim3(B), dim3(fast::kThreads), sm, stream, logits, V, W, bitmask, temp,
+                            uint32_t(seed), uint32_t(seed >> 32), step, out_tok, probs, inplace, status);
   }
   if (bf16)
     return vec ? launch_mode<true, true>(mode, logits, B, V, W, bitmask, temp, top_p, seed, step, out_tok, probs,
