@@ -23,7 +23,8 @@ bool step_fusable(int dtype, uint32_t V, uint32_t W, float temp, float top_p, co
 cudaError_t launch_step(const Tables& t, const uint32_t* states, const uint16_t* gid, const int32_t* forced,
                         uint32_t B, void* logits, uint32_t V, float temp, float top_p, uint64_t seed, uint32_t step,
                         uint32_t* counts, uint32_t max_tokens, uint32_t* bitmask_out, uint32_t* out_tok,
-                        uint32_t* out_states, uint8_t* out_flags, void* scratch, cudaStream_t stream);
+                        uint32_t* out_states, uint8_t* out_flags, void* scratch, const DevGrammar* host_grammars,
+                        bool cache_complete, cudaStream_t stream);
 cudaError_t launch_accept(const Tables& t, const uint32_t* states, const uint16_t* gid, const uint32_t* toks,
                           const int32_t* forced, uint32_t B, uint32_t* counts, uint32_t max_tokens,
                           uint32_t* out_states, uint8_t* out_flags, cudaStream_t stream);
@@ -41,6 +42,8 @@ struct cg_ctx {
   size_t sample_scratch_bytes = 0;
   uint32_t* step_bitmask = nullptr;      // bitmask of cg_step's unfused path when the caller gives none
   size_t step_bitmask_bytes = 0;
+  std::vector<cgk::DevGrammar> grammars; // host copy of t.grammars
+  bool cache_complete = false;           // cg_ctx_prefill has filled every class mask (in stream order)
 };
 
 namespace {
@@ -210,6 +213,7 @@ int cg_ctx_create(const cg_grammar* const* g, uint32_t n_g, const cg_vocab* v, v
   t.status = d_status;
   c->class_rep = d_rep;
   c->class_gid = d_cgid;
+  c->grammars = std::move(gdesc);
   *out = c;
   return CG_OK;
 }
@@ -242,7 +246,9 @@ int cg_ctx_status(cg_ctx* c, uint32_t* dev_code) {
 
 int cg_ctx_prefill(cg_ctx* c) {
   if (!c) return CG_E_ARG;
-  return cgk::launch_prefill(c->t, c->class_rep, c->class_gid, c->stream) == cudaSuccess ? CG_OK : CG_E_CUDA;
+  if (cgk::launch_prefill(c->t, c->class_rep, c->class_gid, c->stream) != cudaSuccess) return CG_E_CUDA;
+  c->cache_complete = true;  // later kernels on the stream see every class ready
+  return CG_OK;
 }
 
 int cg_fill_bitmask(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const int32_t* d_forced, uint32_t B,
@@ -313,7 +319,7 @@ int cg_step(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const in
   if (cgk::step_fusable(dtype, V, c->t.W, temp, top_p, d_logits))
     return cgk::launch_step(c->t, d_states, d_gid, d_forced, B, d_logits, V, temp, top_p, seed, step, d_counts,
                             max_tokens, d_bitmask, d_out_tok, d_out_states, d_out_flags, c->sample_scratch,
-                            c->stream) == cudaSuccess
+                            c->grammars.data(), c->cache_complete, c->stream) == cudaSuccess
                ? CG_OK
                : CG_E_CUDA;
   // otherwise the three calls, through a context bitmask when the caller gives none

@@ -496,6 +496,8 @@ __device__ __forceinline__ void drain_stage(const uint4* stg, const uint16_t* sg
 // Inputs and outputs of the fused step (cg_step): the row's bitmask is built
 // in shared memory as cg_fill_bitmask would write it, and the sampled token is
 // accepted as cg_accept would.
+constexpr uint32_t kParamGrammars = 8;  // grammar descriptors passed by value
+
 struct StepArgs {
   Tables t;
   const uint32_t* states;
@@ -506,49 +508,61 @@ struct StepArgs {
   uint32_t* out_states;
   uint8_t* out_flags;
   uint32_t* bitmask_out;    // may be null: the mask then never leaves the chip
+  DevGrammar pg[kParamGrammars];  // copies of t.grammars[0 .. n_pg): one dependent load fewer
+  uint32_t n_pg;
+  uint32_t cache_complete;  // every class mask is in the cache (cg_ctx_prefill ran): skip the ready check
 };
 
-// The row's mask in shared memory, as cg_fill_bitmask defines it (and written
-// to sa.bitmask_out when given).  All threads of the block take part.  A
-// cached class mask arrives as one bulk copy completing on *mbar_mask, issued
-// as soon as the class is known (before its ready flag is read: after
-// cg_ctx_prefill it always is); the caller waits on it with parity 0 when
-// *s_copied is set.  Also stages grammar g's column map (scols, 512 entries)
-// and the row's transition-table row (srow, n_cols entries) for the accept at
-// the end.  scol is 512 bytes of free shared memory for the miss path.
+// Grammar g's descriptor from the kernel parameters when they hold it (an
+// unrolled select keeps the reads in the parameter space), else from memory.
+__device__ __forceinline__ DevGrammar step_grammar(const StepArgs& sa, uint32_t g) {
+  if (g >= sa.n_pg) return sa.t.grammars[g];
+  DevGrammar gd = sa.pg[0];
+#pragma unroll
+  for (uint32_t i = 1; i < kParamGrammars; ++i)
+    if (g == i) gd = sa.pg[i];
+  return gd;
+}
+
+// The row's mask in shared memory, as cg_fill_bitmask defines it.  All threads
+// of the block take part.  Thread 0 loads the row's grammar, forced token and
+// state, then the state's flags and mask class together; a cached class mask
+// arrives as one bulk copy completing on *mbar_mask (the caller waits on it,
+// parity 0, when *s_copied is set).  scol is 512 bytes of free shared memory
+// for the miss path.
 __device__ void step_row_mask(const StepArgs& sa, uint32_t b, uint32_t W, uint32_t* smask, uint16_t* scol,
-                              uint16_t* scols, uint32_t* srow, uint64_t* mbar_mask, uint32_t& s_copied,
-                              uint32_t& s_srow, uint32_t& s_mode, uint32_t& s_cls, uint32_t& s_ready,
-                              uint32_t& s_claim, uint32_t& s_g, uint32_t& s_s, int32_t& s_f) {
+                              uint64_t* mbar_mask, uint32_t& s_copied, uint32_t& s_srow, uint32_t& s_mode,
+                              uint32_t& s_cls, uint32_t& s_ready, uint32_t& s_claim, uint32_t& s_g, uint32_t& s_s,
+                              int32_t& s_f) {
   const Tables& t = sa.t;
   const uint32_t tid = threadIdx.x;
   if (tid == 0) {
     const uint32_t g = sa.gid ? sa.gid[b] : 0u;
     const int32_t f = sa.forced ? sa.forced[b] : -1;
     const uint32_t s = sa.states[b];
-    uint32_t copied = 0, cls = 0, ready = 0, srow_ok = 0;
-    // the class of an in-range state, fetched beside its flags so that the
-    // mask copy can start before the mode is settled
-    if (g < t.n_g && s != CG_DEAD) {
-      const DevGrammar gd = t.grammars[g];
-      if (s < gd.n_states) {
-        srow_ok = gd.n_cols <= kMaxCols;
-        if (f < 0) {
-          cls = t.class_of[gd.state_off + s];
-          if ((W & 3u) == 0) {
-            mbar_expect_tx(mbar_mask, W * 4);
-            bulk_g2s(smask, t.cache + size_t(cls) * W, W * 4, mbar_mask);
-            copied = 1;
-          }
-        }
-      }
+    DevGrammar gd{};
+    if (g < t.n_g) gd = step_grammar(sa, g);
+    const bool in_range = g < t.n_g && s != CG_DEAD && s < gd.n_states;
+    uint8_t sflags = 0;
+    uint32_t cls = 0;
+    if (in_range && f < 0) {
+      sflags = t.state_flags[gd.state_off + s];
+      cls = t.class_of[gd.state_off + s];
     }
     uint32_t err = 0;
-    const int mode = row_mask_mode(t, g, f, s, &err);
+    const int mode = row_mask_mode_of(t.n_g, t.V, g, f, s, gd.n_states, sflags, &err);
     if (err) record_error(t.status, err);
-    if (mode == 0) ready = load_acquire(t.cache_state + cls) == kStateReady;
+    uint32_t copied = 0, ready = 0;
+    if (mode == 0) {
+      ready = sa.cache_complete ? 1u : (load_acquire(t.cache_state + cls) == kStateReady);
+      if (ready && (W & 3u) == 0) {
+        mbar_expect_tx(mbar_mask, W * 4);
+        bulk_g2s(smask, t.cache + size_t(cls) * W, W * 4, mbar_mask);
+        copied = 1;
+      }
+    }
     s_copied = copied;
-    s_srow = srow_ok;
+    s_srow = in_range && gd.n_cols <= kMaxCols;
     s_mode = uint32_t(mode);
     s_cls = cls;
     s_ready = ready;
@@ -558,19 +572,6 @@ __device__ void step_row_mask(const StepArgs& sa, uint32_t b, uint32_t W, uint32
   }
   __syncthreads();
   const uint32_t mode = s_mode;
-  if (s_g < t.n_g) {
-    for (uint32_t i = tid; i < 512; i += blockDim.x) scols[i] = t.colmap[size_t(s_g) * 512 + i];
-    if (s_srow) {
-      const DevGrammar gd = t.grammars[s_g];
-      for (uint32_t i = tid; i < gd.n_cols; i += blockDim.x) srow[i] = t.table[gd.table_off + size_t(s_s) * gd.n_cols + i];
-    }
-  }
-  if (s_copied && !(mode == 0 && s_ready)) {
-    // the speculative copy is not the mask: let it land before overwriting
-    if (tid == 0) mbar_wait(mbar_mask, 0);
-    __syncthreads();
-    if (tid == 0) s_copied = 0;
-  }
   if (mode == 1) {
     for (uint32_t i = tid; i < W; i += blockDim.x) smask[i] = 0u;
   } else if (mode == 2) {
@@ -598,6 +599,19 @@ __device__ void step_row_mask(const StepArgs& sa, uint32_t b, uint32_t W, uint32
       __syncthreads();
       if (tid == 0) store_release(t.cache_state + cls, kStateReady);
     }
+  }
+}
+
+// The accept's tables, staged by the producer warp while the row streams:
+// grammar g's symbol -> column map and row s of its transition table.
+__device__ void stage_accept_tables(const StepArgs& sa, uint32_t g, uint32_t s, bool srow_ok, uint16_t* scols,
+                                    uint32_t* srow, uint32_t lane) {
+  const Tables& t = sa.t;
+  if (g >= t.n_g) return;
+  for (uint32_t i = lane; i < 512; i += 32) scols[i] = t.colmap[size_t(g) * 512 + i];
+  if (srow_ok) {
+    const DevGrammar gd = step_grammar(sa, g);
+    for (uint32_t i = lane; i < gd.n_cols; i += 32) srow[i] = t.table[gd.table_off + size_t(s) * gd.n_cols + i];
   }
 }
 
@@ -659,8 +673,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     // the logits do not depend on the mask: start the first copies now
     if (warp == kConsumerWarps && lane == 0)
       for (uint32_t k = 0; k < nchunks && k < uint32_t(kStages); ++k) issue_chunk(ring, full, row, V, k);
-    step_row_mask(sa, b, W, smask, reinterpret_cast<uint16_t*>(stg_all), scols, srow, &mbar_mask, s_copied, s_srow,
-                  s_mode, s_cls, s_ready, s_claim, s_g, s_s, s_f);
+    step_row_mask(sa, b, W, smask, reinterpret_cast<uint16_t*>(stg_all), &mbar_mask, s_copied, s_srow, s_mode, s_cls,
+                  s_ready, s_claim, s_g, s_s, s_f);
   }
   __syncthreads();
 
@@ -674,6 +688,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (warp == kConsumerWarps) {
     // ---- producer warp --------------------------------------------------------------
+    if (STEP) stage_accept_tables(sa, s_g, s_s, s_srow != 0u, scols, srow, lane);
     if (lane == 0) {
       bool ok = true;
       for (uint32_t k = STEP ? min(nchunks, uint32_t(kStages)) : 0u; k < nchunks; ++k) {
@@ -1248,7 +1263,8 @@ bool step_fusable(int dtype, uint32_t V, uint32_t W, float temp, float top_p, co
 cudaError_t launch_step(const Tables& t, const uint32_t* states, const uint16_t* gid, const int32_t* forced,
                         uint32_t B, void* logits, uint32_t V, float temp, float top_p, uint64_t seed, uint32_t step,
                         uint32_t* counts, uint32_t max_tokens, uint32_t* bitmask_out, uint32_t* out_tok,
-                        uint32_t* out_states, uint8_t* out_flags, void* scratch, cudaStream_t stream) {
+                        uint32_t* out_states, uint8_t* out_flags, void* scratch, const DevGrammar* host_grammars,
+                        bool cache_complete, cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
   const uint32_t W = t.W;
   const size_t s1 = fast::stream_smem(W);
@@ -1256,7 +1272,12 @@ cudaError_t launch_step(const Tables& t, const uint32_t* states, const uint16_t*
   if (e != cudaSuccess) return e;
   uint32_t* cand_id = static_cast<uint32_t*>(scratch);
   uint16_t* cand_key = reinterpret_cast<uint16_t*>(cand_id + size_t(B) * fast::kCandPerRow);
-  const fast::StepArgs sa{t, states, gid, forced, counts, max_tokens, out_states, out_flags, bitmask_out};
+  fast::StepArgs sa{t, states, gid, forced, counts, max_tokens, out_states, out_flags, bitmask_out, {}, 0u, 0u};
+  if (host_grammars && t.n_g <= fast::kParamGrammars) {
+    for (uint32_t i = 0; i < t.n_g; ++i) sa.pg[i] = host_grammars[i];
+    sa.n_pg = t.n_g;
+  }
+  sa.cache_complete = cache_complete ? 1u : 0u;
   return launch_dependent(fast::stream_topp_kernel<true>, dim3(B), dim3(fast::kThreads), s1, stream, logits, V, W,
                           static_cast<const uint32_t*>(nullptr), temp, top_p, uint32_t(seed), uint32_t(seed >> 32),
                           step, out_tok, static_cast<float*>(nullptr), 0, cand_id, cand_key, fast::kCandPerRow,

@@ -24,19 +24,30 @@ __device__ __forceinline__ void store_release(uint32_t* p, uint32_t v) {
 // 1 an all-zero row (bad grammar id, bad forced id, dead or out-of-range state,
 // forced-only state without a forced token), 2 a one-hot row at the forced
 // token.  *err receives the CG_DEV_* code to record (0 for none).
-__device__ __forceinline__ int row_mask_mode(const Tables& t, uint32_t g, int32_t f, uint32_t s, uint32_t* err) {
+// The same decision from values already loaded: n_states of grammar g (when
+// g < n_g) and the state's flags (when s < n_states).
+__device__ __forceinline__ int row_mask_mode_of(uint32_t n_g, uint32_t V, uint32_t g, int32_t f, uint32_t s,
+                                                uint32_t n_states, uint8_t sflags, uint32_t* err) {
   int mode = 0;
-  if (g >= t.n_g) mode = 1;
-  else if (f >= 0) mode = (uint32_t(f) < t.V) ? 2 : 1;
-  else if (s == CG_DEAD || s >= t.grammars[g].n_states) mode = 1;
-  else if (t.state_flags[t.grammars[g].state_off + s] & CG_STATE_FORCED_ONLY) mode = 1;
+  if (g >= n_g) mode = 1;
+  else if (f >= 0) mode = (uint32_t(f) < V) ? 2 : 1;
+  else if (s == CG_DEAD || s >= n_states) mode = 1;
+  else if (sflags & CG_STATE_FORCED_ONLY) mode = 1;
   uint32_t e = 0;
-  if (g >= t.n_g) e = CG_DEV_BAD_GID;
-  else if (f >= 0 && uint32_t(f) >= t.V) e = CG_DEV_BAD_FORCED;
-  else if (f < 0 && s != CG_DEAD && s >= t.grammars[g].n_states) e = CG_DEV_BAD_STATE;
+  if (g >= n_g) e = CG_DEV_BAD_GID;
+  else if (f >= 0 && uint32_t(f) >= V) e = CG_DEV_BAD_FORCED;
+  else if (f < 0 && s != CG_DEAD && s >= n_states) e = CG_DEV_BAD_STATE;
   else if (mode == 1 && f < 0 && s != CG_DEAD) e = CG_DEV_MISSING_FORCED;
   *err = e;
   return mode;
+}
+
+__device__ __forceinline__ int row_mask_mode(const Tables& t, uint32_t g, int32_t f, uint32_t s, uint32_t* err) {
+  const uint32_t n_states = g < t.n_g ? t.grammars[g].n_states : 0u;
+  const uint8_t sflags = (g < t.n_g && f < 0 && s != CG_DEAD && s < n_states)
+                             ? t.state_flags[t.grammars[g].state_off + s]
+                             : uint8_t(0);
+  return row_mask_mode_of(t.n_g, t.V, g, f, s, n_states, sflags, err);
 }
 
 // Walk all tokens from state s of grammar g with threads tid = 0..nthreads-1;
