@@ -386,15 +386,15 @@ __device__ __forceinline__ float group_max(const uint4& v) {
   const uint32_t mx = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
   return fmaxf(lo_f(mx), hi_f(mx));
 }
-__device__ __forceinline__ void add_exps(float* acc, const uint4& v, float c, float mc) {
-  acc[0] += ex2(fmaf(lo_f(v.x), c, -mc));
-  acc[1] += ex2(fmaf(hi_f(v.x), c, -mc));
-  acc[2] += ex2(fmaf(lo_f(v.y), c, -mc));
-  acc[3] += ex2(fmaf(hi_f(v.y), c, -mc));
-  acc[4] += ex2(fmaf(lo_f(v.z), c, -mc));
-  acc[5] += ex2(fmaf(hi_f(v.z), c, -mc));
-  acc[6] += ex2(fmaf(lo_f(v.w), c, -mc));
-  acc[7] += ex2(fmaf(hi_f(v.w), c, -mc));
+// acc[j] += exp2(x_j c - mc) for the group's logits, sums j and j + 1 paired in
+// one float2 (the packed fp32 multiply-add and add round each lane as the
+// scalar instructions do, so the sums are those of scalar code)
+__device__ __forceinline__ float2 ex2_pair(float2 z) { return make_float2(ex2(z.x), ex2(z.y)); }
+__device__ __forceinline__ void add_exps(float2* acc, const uint4& v, float2 c2, float2 nmc2) {
+  acc[0] = __fadd2_rn(acc[0], ex2_pair(__ffma2_rn(make_float2(lo_f(v.x), hi_f(v.x)), c2, nmc2)));
+  acc[1] = __fadd2_rn(acc[1], ex2_pair(__ffma2_rn(make_float2(lo_f(v.y), hi_f(v.y)), c2, nmc2)));
+  acc[2] = __fadd2_rn(acc[2], ex2_pair(__ffma2_rn(make_float2(lo_f(v.z), hi_f(v.z)), c2, nmc2)));
+  acc[3] = __fadd2_rn(acc[3], ex2_pair(__ffma2_rn(make_float2(lo_f(v.w), hi_f(v.w)), c2, nmc2)));
 }
 // logit e (0..7) of an 8-logit group
 __device__ __forceinline__ float group_at(const uint4& v, uint32_t e) {
@@ -682,9 +682,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   const float margin = kMarginZ * temp;  // z = x / temp: kMarginZ nats are kMarginZ * temp logit units
   const uint8_t* smask8 = reinterpret_cast<const uint8_t*>(smask);
   float mt = kNoRef;  // reference of this thread's sums: its running maximum
-  float acc[kAcc];
+  float2 acc[kAcc / 2];
 #pragma unroll
-  for (int j = 0; j < kAcc; ++j) acc[j] = 0.f;
+  for (int j = 0; j < kAcc / 2; ++j) acc[j] = make_float2(0.f, 0.f);
 
   if (warp == kConsumerWarps) {
     // ---- producer warp --------------------------------------------------------------
@@ -755,12 +755,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         // they do not depend on the other warps' timing (S is reproducible)
         const float r = ex2((mt - gm) * c);
 #pragma unroll
-        for (int j = 0; j < kAcc; ++j) acc[j] *= r;
+        for (int j = 0; j < kAcc / 2; ++j) acc[j] = __fmul2_rn(acc[j], make_float2(r, r));
         mt = gm;
       }
       const float mc = mt * c;
-      add_exps(acc, v0, c, mc);
-      add_exps(acc, v1, c, mc);
+      add_exps(acc, v0, make_float2(c, c), make_float2(-mc, -mc));
+      add_exps(acc, v1, make_float2(c, c), make_float2(-mc, -mc));
       // stage the flagged groups (fewer than 32 are staged before each group
       // is added, at most 63 after); turn staged groups into candidates 32 at a
       // time
@@ -811,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (M > -INFINITY) {
       float a = 0.f;
 #pragma unroll
-      for (int jj = 0; jj < kAcc; ++jj) a += acc[jj];
+      for (int jj = 0; jj < kAcc / 2; ++jj) a = (a + acc[jj].x) + acc[jj].y;
       if (a > 0.f) part = a * ex2((mt - M) * c);
     }
     part = warp_reduce(part, SumOp());
@@ -1048,9 +1048,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   float bestv = -INFINITY;         // greedy: this thread's best value
   float lm = -INFINITY;            // this thread's largest allowed logit
   float mt = kNoRef;               // reference of this thread's sums (WANT_S)
-  float acc[kAcc];
+  float2 acc[kAcc / 2];
 #pragma unroll
-  for (int j = 0; j < kAcc; ++j) acc[j] = 0.f;
+  for (int j = 0; j < kAcc / 2; ++j) acc[j] = make_float2(0.f, 0.f);
 
   if (warp == kConsumerWarps) {
     if (lane == 0) {
@@ -1118,12 +1118,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (gm > mt) {
           const float r = ex2((mt - gm) * c);
 #pragma unroll
-          for (int j = 0; j < kAcc; ++j) acc[j] *= r;
+          for (int j = 0; j < kAcc / 2; ++j) acc[j] = __fmul2_rn(acc[j], make_float2(r, r));
           mt = gm;
         }
         const float mc = mt * c;
-        add_exps(acc, v[0], c, mc);
-        add_exps(acc, v[1], c, mc);
+        add_exps(acc, v[0], make_float2(c, c), make_float2(-mc, -mc));
+        add_exps(acc, v[1], make_float2(c, c), make_float2(-mc, -mc));
       }
     }
   }
@@ -1142,7 +1142,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (M > -INFINITY) {
       float a = 0.f;
 #pragma unroll
-      for (int jj = 0; jj < kAcc; ++jj) a += acc[jj];
+      for (int jj = 0; jj < kAcc / 2; ++jj) a = (a + acc[jj].x) + acc[jj].y;
       if (a > 0.f) part = a * ex2((mt - M) * c);
     }
     S = double(block_reduce(part, SumOp(), 0.f, red_f));
