@@ -724,31 +724,46 @@ __global__ void __launch_bounds__(kThreads, 2)
       asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");  // consumer warps only
     }
     bool ok = true;
-    for (uint32_t k = 0; k < nchunks; ++k) {
-      const uint32_t slot = k % kStages;
-      // flag threshold for this chunk: the block's running maximum minus the
+    // two slots per pass: the threshold, the warp's maximum and the hand-back
+    // are paid once for four groups per thread
+    for (uint32_t k = 0; k < nchunks; k += 2) {
+      const bool two = k + 1 < nchunks;
+      // flag threshold for these chunks: the block's running maximum minus the
       // margin (never above M - margin; finite, so masked groups never flag)
       const float thr = fmaxf(fkey_inv(*reinterpret_cast<volatile uint32_t*>(&s_maxkey)), kNoRef) - margin;
-      if (!mbar_wait(full + slot, (k / kStages) & 1u)) {
+      if (!mbar_wait(full + k % kStages, (k / kStages) & 1u) ||
+          (two && !mbar_wait(full + (k + 1) % kStages, ((k + 1) / kStages) & 1u))) {
         atomicOr(&s_flag, 1u);
         ok = false;
         break;
       }
-      const uint4* r4 = reinterpret_cast<const uint4*>(ring + size_t(slot) * kChunkBytes);
-      const uint32_t gbase = k * kGroupsPerChunk;  // row group index of the chunk's group 0
-      const uint32_t gi0 = tid, gi1 = tid + kConsumers;
-      const uint32_t ngroups = min(kGroupsPerChunk, V / 8 - gbase);
-      uint4 v0 = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u), v1 = v0;
-      if (gi0 < ngroups) v0 = apply_mask(r4[gi0], lut[smask8[gbase + gi0]]);
-      if (gi1 < ngroups) v1 = apply_mask(r4[gi1], lut[smask8[gbase + gi1]]);
-      // the slot's data are in registers: hand the slot back
-      const float g0 = group_max(v0), g1 = group_max(v1);
-      const float gm = fmaxf(g0, g1);
+      uint4 v[4];
+      uint32_t gg[4];  // row group index of each of the thread's groups
+#pragma unroll
+      for (uint32_t h = 0; h < 2; ++h) {
+        const uint32_t kk = k + h;
+        const uint4* r4 = reinterpret_cast<const uint4*>(ring + size_t(kk % kStages) * kChunkBytes);
+        const uint32_t gbase = kk * kGroupsPerChunk;  // row group index of the chunk's group 0
+        const uint32_t ngroups = (h == 0 || two) ? min(kGroupsPerChunk, V / 8 - gbase) : 0u;
+#pragma unroll
+        for (uint32_t q = 0; q < 2; ++q) {
+          const uint32_t gi = tid + kConsumers * q;
+          v[2 * h + q] = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+          if (gi < ngroups) v[2 * h + q] = apply_mask(r4[gi], lut[smask8[gbase + gi]]);
+          gg[2 * h + q] = gbase + gi;
+        }
+      }
+      // the slots' data are in registers: hand the slots back
+      float gq[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) gq[q] = group_max(v[q]);
+      const float gm = fmaxf(fmaxf(gq[0], gq[1]), fmaxf(gq[2], gq[3]));
       const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, fkey(gm));
       __syncwarp();
       if (lane == 0) {
         atomicMax(&s_maxkey, wk);
-        mbar_arrive(empty + slot);
+        mbar_arrive(empty + k % kStages);
+        if (two) mbar_arrive(empty + (k + 1) % kStages);
       }
       if (gm > mt) {
         // the sums' reference is this thread's own running maximum, so that
@@ -759,20 +774,20 @@ __global__ void __launch_bounds__(kThreads, 2)
         mt = gm;
       }
       const float mc = mt * c;
-      add_exps(acc, v0, make_float2(c, c), make_float2(-mc, -mc));
-      add_exps(acc, v1, make_float2(c, c), make_float2(-mc, -mc));
+#pragma unroll
+      for (int q = 0; q < 4; ++q) add_exps(acc, v[q], make_float2(c, c), make_float2(-mc, -mc));
       // stage the flagged groups (fewer than 32 are staged before each group
       // is added, at most 63 after); turn staged groups into candidates 32 at a
       // time
 #pragma unroll
-      for (uint32_t g = 0; g < 2; ++g) {
-        const bool f = (g ? g1 : g0) >= thr;
+      for (uint32_t q = 0; q < 4; ++q) {
+        const bool f = gq[q] >= thr;
         const unsigned bal = __ballot_sync(0xFFFFFFFFu, f);
         if (bal) {
           if (f) {
             const uint32_t p = sc + __popc(bal & lt);
-            stg[p] = g ? v1 : v0;
-            sgid[p] = uint16_t(gbase + (g ? gi1 : gi0));
+            stg[p] = v[q];
+            sgid[p] = uint16_t(gg[q]);
           }
           sc += __popc(bal);
           if (sc >= 32) {
