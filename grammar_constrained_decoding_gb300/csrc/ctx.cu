@@ -158,8 +158,38 @@ int cg_ctx_create(const cg_grammar* const* g, uint32_t n_g, const cg_vocab* v, v
     delete c;
     return CG_E_NOMEM;
   }
+  // the table in 16 bits when every state number fits (the fused step's
+  // accept reads a window of it from shared memory), padded by 16 bytes for
+  // that window's aligned bulk copy; 32-byte token records (length, bytes)
+  std::vector<uint16_t> table16;
+  std::vector<uint32_t> tok_rec;
+  try {
+    bool fits = true;
+    for (uint32_t i = 0; i < n_g; ++i) fits = fits && gdesc[i].n_states < cgk::kDead16;
+    if (fits) {
+      table16.resize(table.size() + 8);
+      for (size_t i = 0; i < table.size(); ++i)
+        table16[i] = table[i] == CG_DEAD ? cgk::kDead16 : uint16_t(table[i]);
+    }
+    tok_rec.assign(size_t(V) * 8, 0u);
+    for (uint32_t k = 0; k < V; ++k) {
+      const uint32_t b0 = v->off[k], n = v->off[k + 1] - b0;
+      uint8_t* rec = reinterpret_cast<uint8_t*>(tok_rec.data() + size_t(k) * 8);
+      if (n >= 32) {
+        rec[0] = uint8_t(cgk::kLongToken);
+        continue;
+      }
+      rec[0] = uint8_t(n);
+      for (uint32_t i = 0; i < n; ++i) rec[1 + i] = v->bytes[b0 + i];
+    }
+  } catch (const std::bad_alloc&) {
+    delete c;
+    return CG_E_NOMEM;
+  }
   cgk::Tables& t = c->t;
   cudaError_t e = cudaSuccess;
+  uint16_t* d_table16 = nullptr;
+  uint32_t* d_rec = nullptr;
   uint32_t* d_table;
   cgk::DevGrammar* d_gd;
   uint16_t* d_col;
@@ -174,7 +204,8 @@ int cg_ctx_create(const cg_grammar* const* g, uint32_t n_g, const cg_vocab* v, v
       (e = upload(c, v->bytes, &d_bytes)) != cudaSuccess || (e = upload(c, v->sorted_off, &d_soff)) != cudaSuccess ||
       (e = upload(c, v->sorted_bytes, &d_sbytes)) != cudaSuccess || (e = upload(c, v->perm, &d_perm)) != cudaSuccess ||
       (e = upload(c, v->lcp, &d_lcp)) != cudaSuccess || (e = upload(c, class_rep, &d_rep)) != cudaSuccess ||
-      (e = upload(c, class_gid, &d_cgid)) != cudaSuccess) {
+      (e = upload(c, class_gid, &d_cgid)) != cudaSuccess || (e = upload(c, tok_rec, &d_rec)) != cudaSuccess ||
+      (!table16.empty() && (e = upload(c, table16, &d_table16)) != cudaSuccess)) {
     release(c);
     delete c;
     return CG_E_CUDA;
@@ -211,6 +242,8 @@ int cg_ctx_create(const cg_grammar* const* g, uint32_t n_g, const cg_vocab* v, v
   t.perm = d_perm;
   t.lcp = d_lcp;
   t.status = d_status;
+  t.table16 = d_table16;
+  t.tok_rec = reinterpret_cast<const uint4*>(d_rec);
   c->class_rep = d_rep;
   c->class_gid = d_cgid;
   c->grammars = std::move(gdesc);

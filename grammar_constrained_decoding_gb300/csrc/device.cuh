@@ -61,7 +61,13 @@ struct Tables {
   const uint32_t* perm;        // trie position -> token id
   const uint8_t* lcp;          // common prefix with the previous trie position
   uint32_t* status;            // first CG_DEV_* error
+  const uint16_t* table16;     // `table` in 16 bits (kDead16 for CG_DEAD); null when a grammar has too many states
+  const uint4* tok_rec;        // [V][2] 32-byte token records: byte 0 the length, bytes 1..31 the token's bytes;
+                               // length kLongToken: 32 bytes or more, read through tok_off
 };
+
+constexpr uint16_t kDead16 = 0xFFFFu;      // CG_DEAD in table16
+constexpr uint32_t kLongToken = 0xFFu;     // token record length of a token read through tok_off
 
 __device__ __forceinline__ void record_error(uint32_t* status, uint32_t code) {
   atomicCAS(status, 0u, code);

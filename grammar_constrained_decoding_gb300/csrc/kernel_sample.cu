@@ -20,6 +20,7 @@
 // temperature folded into one scale c = log2(e) / temp.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -321,6 +322,8 @@ constexpr float kMarginZ = 9.0f;                                // nats below th
 constexpr float kNoRef = -1e30f;                                // finite reference before any allowed logit
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kMaxCols = 512;                              // symbol columns a grammar can have
+constexpr uint32_t kWinRowsMax = 512;                           // states in the accept's table window
+constexpr uint32_t kWinBytesMax = 16384;                        // shared memory for that window
 constexpr uint32_t kSlots = 16;                                 // list entries per thread after the stream
 constexpr uint32_t kCandPerRow = kThreads * kSlots;             // candidate list entries per row (8192)
 constexpr uint32_t kBatchIds = 4;                               // nucleus id loads in flight per thread
@@ -511,6 +514,7 @@ struct StepArgs {
   DevGrammar pg[kParamGrammars];  // copies of t.grammars[0 .. n_pg): one dependent load fewer
   uint32_t n_pg;
   uint32_t cache_complete;  // every class mask is in the cache (cg_ctx_prefill ran): skip the ready check
+  uint32_t win_bytes;       // shared memory for the accept's table window (0: none)
 };
 
 // Grammar g's descriptor from the kernel parameters when they hold it (an
@@ -531,7 +535,7 @@ __device__ __forceinline__ DevGrammar step_grammar(const StepArgs& sa, uint32_t 
 // parity 0, when *s_copied is set).  scol is 512 bytes of free shared memory
 // for the miss path.
 __device__ void step_row_mask(const StepArgs& sa, uint32_t b, uint32_t W, uint32_t* smask, uint16_t* scol,
-                              uint64_t* mbar_mask, uint32_t& s_copied, uint32_t& s_srow, uint32_t& s_mode,
+                              uint64_t* mbar_mask, uint32_t& s_copied, uint32_t& s_mode,
                               uint32_t& s_cls, uint32_t& s_ready, uint32_t& s_claim, uint32_t& s_g, uint32_t& s_s,
                               int32_t& s_f) {
   const Tables& t = sa.t;
@@ -562,7 +566,6 @@ __device__ void step_row_mask(const StepArgs& sa, uint32_t b, uint32_t W, uint32
       }
     }
     s_copied = copied;
-    s_srow = in_range && gd.n_cols <= kMaxCols;
     s_mode = uint32_t(mode);
     s_cls = cls;
     s_ready = ready;
@@ -603,16 +606,33 @@ __device__ void step_row_mask(const StepArgs& sa, uint32_t b, uint32_t W, uint32
 }
 
 // The accept's tables, staged by the producer warp while the row streams:
-// grammar g's symbol -> column map and row s of its transition table.
-__device__ void stage_accept_tables(const StepArgs& sa, uint32_t g, uint32_t s, bool srow_ok, uint16_t* scols,
-                                    uint32_t* srow, uint32_t lane) {
+// grammar g's symbol -> column map, and (lane 0, one bulk copy completing on
+// *mbar_win) the rows of the states around s in the 16-bit table, with their
+// flags.  *s_wlo / *s_wrows / *s_wdelta describe the window (rows 0: none).
+__device__ void stage_accept_tables(const StepArgs& sa, uint32_t g, uint32_t s, uint16_t* scols, uint16_t* win,
+                                    uint8_t* wflags, uint64_t* mbar_win, uint32_t* s_wlo, uint32_t* s_wrows,
+                                    uint32_t* s_wdelta, uint32_t lane) {
   const Tables& t = sa.t;
   if (g >= t.n_g) return;
   for (uint32_t i = lane; i < 512; i += 32) scols[i] = t.colmap[size_t(g) * 512 + i];
-  if (srow_ok) {
-    const DevGrammar gd = step_grammar(sa, g);
-    for (uint32_t i = lane; i < gd.n_cols; i += 32) srow[i] = t.table[gd.table_off + size_t(s) * gd.n_cols + i];
+  const DevGrammar gd = step_grammar(sa, g);
+  if (!t.table16 || s >= gd.n_states || gd.n_cols == 0 || sa.win_bytes < 32) return;
+  const uint32_t cap = min(kWinRowsMax, (sa.win_bytes - 16) / (2 * gd.n_cols));
+  if (cap == 0) return;
+  const uint32_t hi = min(gd.n_states, max(s, cap / 2) + (cap - cap / 2));
+  const uint32_t lo = hi > cap ? hi - cap : 0u;
+  const uint32_t rows = hi - lo;
+  const uintptr_t src = reinterpret_cast<uintptr_t>(t.table16 + gd.table_off + size_t(lo) * gd.n_cols);
+  const uintptr_t src0 = src & ~uintptr_t(15);
+  const uint32_t bytes = (uint32_t(src - src0) + rows * gd.n_cols * 2 + 15u) & ~15u;  // <= win_bytes
+  if (lane == 0) {
+    mbar_expect_tx(mbar_win, bytes);
+    bulk_g2s(win, reinterpret_cast<const void*>(src0), bytes, mbar_win);
+    *s_wlo = lo;
+    *s_wdelta = uint32_t(src - src0) / 2;
+    *s_wrows = rows;
   }
+  for (uint32_t i = lane; i < rows; i += 32) wflags[i] = t.state_flags[gd.state_off + lo + i];
 }
 
 template <bool STEP>
@@ -628,9 +648,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint16_t* sgid_all = reinterpret_cast<uint16_t*>(stg_all + kConsumerWarps * kStage);
   uint32_t* smask = reinterpret_cast<uint32_t*>(sgid_all + kConsumerWarps * kStage);  // [W]
   uint16_t* scols = reinterpret_cast<uint16_t*>(smask + ((W + 3) & ~3u));          // [512] (fused step)
-  uint32_t* srow = reinterpret_cast<uint32_t*>(scols + 512);                        // [kMaxCols] (fused step)
-  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], mbar_mask;
-  __shared__ uint32_t s_copied, s_srow;
+  uint8_t* wflags = reinterpret_cast<uint8_t*>(scols + 512);                        // [kWinRowsMax] (fused step)
+  uint16_t* win = reinterpret_cast<uint16_t*>(wflags + kWinRowsMax);                // [win_bytes / 2] (fused step)
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], mbar_mask, mbar_win;
+  __shared__ uint32_t s_copied, s_wlo, s_wrows, s_wdelta;
   __shared__ float red_f[33];
   __shared__ unsigned long long red_u64[33];
   __shared__ uint32_t s_maxkey, s_flag, s_count, s_tau;
@@ -650,12 +671,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(empty + i, kConsumerWarps);
     }
     mbar_init(&mbar_mask, 1);
+    mbar_init(&mbar_win, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_maxkey = fkey(-INFINITY);
     s_flag = 0;  // bit 0: a wait ran out
     s_count = 0;
     s_copied = 0;
-    s_srow = 0;
+    s_wrows = 0;
   }
   for (uint32_t i = tid; i < 256; i += kThreads) {
     uint32_t w[4];
@@ -673,8 +695,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     // the logits do not depend on the mask: start the first copies now
     if (warp == kConsumerWarps && lane == 0)
       for (uint32_t k = 0; k < nchunks && k < uint32_t(kStages); ++k) issue_chunk(ring, full, row, V, k);
-    step_row_mask(sa, b, W, smask, reinterpret_cast<uint16_t*>(stg_all), &mbar_mask, s_copied, s_srow, s_mode, s_cls,
-                  s_ready, s_claim, s_g, s_s, s_f);
+    step_row_mask(sa, b, W, smask, reinterpret_cast<uint16_t*>(stg_all), &mbar_mask, s_copied, s_mode, s_cls, s_ready,
+                  s_claim, s_g, s_s, s_f);
   }
   __syncthreads();
 
@@ -688,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (warp == kConsumerWarps) {
     // ---- producer warp --------------------------------------------------------------
-    if (STEP) stage_accept_tables(sa, s_g, s_s, s_srow != 0u, scols, srow, lane);
+    if (STEP) stage_accept_tables(sa, s_g, s_s, scols, win, wflags, &mbar_win, &s_wlo, &s_wrows, &s_wdelta, lane);
     if (lane == 0) {
       bool ok = true;
       for (uint32_t k = STEP ? min(nchunks, uint32_t(kStages)) : 0u; k < nchunks; ++k) {
@@ -817,6 +839,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_wait(full + sl, (issued - 1) & 1u);
     }
     if (STEP && s_copied) mbar_wait(&mbar_mask, 0);
+    if (STEP && s_wrows) mbar_wait(&mbar_win, 0);
   }
   const float M = fkey_inv(s_maxkey);  // -inf when no logit is allowed
   // S: per-thread partial sums, warp sums and the 16 warp sums, all in float
@@ -998,9 +1021,21 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   if (tid == 0) {
     out_tok[b] = tok;
-    if (STEP)
+    if (STEP) {
+      StateWindow w;
+      if (s_wrows) {
+        if (mbar_wait(&mbar_win, 0)) {
+          w.next = win + s_wdelta;
+          w.flags = wflags;
+          w.lo = s_wlo;
+          w.rows = s_wrows;
+        } else {
+          record_error(status, CG_DEV_TIMEOUT);
+        }
+      }
       accept_row(sa.t, b, s_g, s_s, tok, s_f, sa.counts, sa.max_tokens, sa.out_states, sa.out_flags,
-                 s_g < sa.t.n_g ? scols : nullptr, s_srow ? srow : nullptr);
+                 s_g < sa.t.n_g ? scols : nullptr, w);
+    }
   }
   if (STEP && sa.bitmask_out) {
     uint32_t* out = sa.bitmask_out + size_t(b) * W;
@@ -1173,10 +1208,16 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 size_t pick_smem(uint32_t W) { return size_t(kRing) + 4096 + size_t((W + 3) & ~3u) * 4; }
 
-size_t stream_smem(uint32_t W) {
+// Dynamic shared memory of the top-p kernel; the fused step adds win_bytes for
+// the accept's table window.
+size_t stream_smem(uint32_t W, uint32_t win_bytes = 0) {
   return size_t(kRing) + 4096 + size_t(kConsumerWarps) * kStage * 18 + size_t((W + 3) & ~3u) * 4 + 512 * 2 +
-         size_t(kMaxCols) * 4;
+         kWinRowsMax + win_bytes;
 }
+
+// Dynamic shared memory per CTA that still lets two CTAs share an SM: 228 KB
+// per SM, less 1 KB reserved and up to 2 KB of static shared memory per CTA.
+constexpr size_t kTwoCtaSmem = 111 * 1024;
 
 }  // namespace fast
 
@@ -1282,17 +1323,23 @@ cudaError_t launch_step(const Tables& t, const uint32_t* states, const uint16_t*
                         bool cache_complete, cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
   const uint32_t W = t.W;
-  const size_t s1 = fast::stream_smem(W);
+  const size_t base = fast::stream_smem(W);
+  const uint32_t win_bytes =
+      base + 1024 <= fast::kTwoCtaSmem
+          ? uint32_t(std::min<size_t>(fast::kWinBytesMax, fast::kTwoCtaSmem - base) & ~size_t(15))
+          : 0u;
+  const size_t s1 = base + win_bytes;
   cudaError_t e = allow_smem(reinterpret_cast<const void*>(fast::stream_topp_kernel<true>), s1);
   if (e != cudaSuccess) return e;
   uint32_t* cand_id = static_cast<uint32_t*>(scratch);
   uint16_t* cand_key = reinterpret_cast<uint16_t*>(cand_id + size_t(B) * fast::kCandPerRow);
-  fast::StepArgs sa{t, states, gid, forced, counts, max_tokens, out_states, out_flags, bitmask_out, {}, 0u, 0u};
+  fast::StepArgs sa{t, states, gid, forced, counts, max_tokens, out_states, out_flags, bitmask_out, {}, 0u, 0u, 0u};
   if (host_grammars && t.n_g <= fast::kParamGrammars) {
     for (uint32_t i = 0; i < t.n_g; ++i) sa.pg[i] = host_grammars[i];
     sa.n_pg = t.n_g;
   }
   sa.cache_complete = cache_complete ? 1u : 0u;
+  sa.win_bytes = win_bytes;
   return launch_dependent(fast::stream_topp_kernel<true>, dim3(B), dim3(fast::kThreads), s1, stream, logits, V, W,
                           static_cast<const uint32_t*>(nullptr), temp, top_p, uint32_t(seed), uint32_t(seed >> 32),
                           step, out_tok, static_cast<float*>(nullptr), 0, cand_id, cand_key, fast::kCandPerRow,

@@ -91,19 +91,29 @@ __device__ inline void walk_tokens(const Tables& t, const DevGrammar& gd, const 
 
 constexpr uint32_t kPrefetch = 16;  // token bytes whose columns are loaded up front
 
+// Rows [lo, lo + rows) of a grammar's 16-bit transition table and the flags
+// of those states, copied into shared memory: transitions from these states
+// are read there instead of from global memory.
+struct StateWindow {
+  const uint16_t* next = nullptr;  // [rows][n_cols]
+  const uint8_t* flags = nullptr;  // [rows]
+  uint32_t lo = 0, rows = 0;
+};
+
 // Advance one row by its token (labs.miniml.ai "Evaluator aware decoding":
 // after injection the grammar state must be advanced; a forced token's bytes
 // are walked as host-injected symbols).  With token counts, finished or capped
 // rows restart from state 0 (usetacet.com/docs/grammar, "A valid call also has
 // to end").  Writes out_states[b], out_flags[b] and counts[b].
 // cols_g (optional) is a copy of grammar g's 512-entry symbol -> column map
-// and srow (optional) a copy of row s of its transition table, both in shared
-// memory: they only shorten the chain of dependent loads.
+// and win (optional) a window of its transition table, both in shared memory:
+// they only shorten the chain of dependent loads.
 __device__ inline void accept_row(const Tables& t, uint32_t b, uint32_t g, uint32_t s, uint32_t tok, int32_t f,
                                   uint32_t* counts, uint32_t max_tokens, uint32_t* out_states, uint8_t* out_flags,
-                                  const uint16_t* cols_g = nullptr, const uint32_t* srow = nullptr) {
+                                  const uint16_t* cols_g = nullptr, const StateWindow& win = StateWindow()) {
   uint32_t ns = s;
   uint8_t fl = 0;
+  const uint32_t n0 = counts ? counts[b] : 0u;  // independent of the walk: loaded first
   if (g >= t.n_g) {
     record_error(t.status, CG_DEV_BAD_GID);
     ns = CG_DEAD;
@@ -130,31 +140,58 @@ __device__ inline void accept_row(const Tables& t, uint32_t b, uint32_t g, uint3
       const uint32_t shift = f >= 0 ? 256u : 0u;
       const uint16_t* cols = (cols_g ? cols_g : t.colmap + size_t(g) * 512) + shift;
       const uint32_t* table = t.table + gd.table_off;
-      // the token's columns first (independent loads), then the chain of
-      // table lookups
-      const uint32_t i0 = t.tok_off[tok], len = t.tok_off[tok + 1] - i0;
-      uint32_t col[kPrefetch];
-#pragma unroll
-      for (uint32_t k = 0; k < kPrefetch; ++k) col[k] = k < len ? cols[t.tok_bytes[i0 + k]] : 0u;
+      const uint32_t nc = gd.n_cols;
+      auto step_from = [&](uint32_t st, uint32_t col) -> uint32_t {
+        const uint32_t r = st - win.lo;
+        if (r < win.rows) {
+          const uint16_t nx = win.next[r * nc + col];
+          return nx == kDead16 ? CG_DEAD : uint32_t(nx);
+        }
+        return table[size_t(st) * nc + col];
+      };
       uint32_t st = s;
+      uint32_t len = kLongToken;
+      uint4 r0 = make_uint4(0u, 0u, 0u, 0u), r1 = r0;
+      if (t.tok_rec) {
+        // the token's bytes in one 32-byte record
+        r0 = t.tok_rec[size_t(tok) * 2];
+        r1 = t.tok_rec[size_t(tok) * 2 + 1];
+        len = r0.x & 0xFFu;
+      }
+      if (len != kLongToken) {
+        const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
-      for (uint32_t k = 0; k < kPrefetch; ++k)
-        if (k < len && st != CG_DEAD) st = (k == 0 && srow) ? srow[col[0]] : table[size_t(st) * gd.n_cols + col[k]];
-      for (uint32_t i = i0 + kPrefetch; i < i0 + len && st != CG_DEAD; ++i)
-        st = table[size_t(st) * gd.n_cols + cols[t.tok_bytes[i]]];
+        for (uint32_t k = 0; k < 31; ++k) {
+          if (k >= len || st == CG_DEAD) break;
+          const uint32_t byte = (w[(k + 1) >> 2] >> (8 * ((k + 1) & 3))) & 0xFFu;
+          st = step_from(st, cols[byte]);
+        }
+      } else {
+        // the offset table; the token's columns first (independent loads),
+        // then the chain of lookups
+        const uint32_t i0 = t.tok_off[tok], n = t.tok_off[tok + 1] - i0;
+        uint32_t col[kPrefetch];
+#pragma unroll
+        for (uint32_t k = 0; k < kPrefetch; ++k) col[k] = k < n ? cols[t.tok_bytes[i0 + k]] : 0u;
+#pragma unroll
+        for (uint32_t k = 0; k < kPrefetch; ++k)
+          if (k < n && st != CG_DEAD) st = step_from(st, col[k]);
+        for (uint32_t i = i0 + kPrefetch; i < i0 + n && st != CG_DEAD; ++i) st = step_from(st, cols[t.tok_bytes[i]]);
+      }
       ns = st;
       if (st == CG_DEAD) {
         record_error(t.status, CG_DEV_REJECTED);
         fl = CG_FLAG_REJECTED;
       } else {
-        const uint8_t sf = t.state_flags[gd.state_off + st];
+        const uint32_t r = st - win.lo;
+        const uint8_t sf = r < win.rows ? win.flags[r] : t.state_flags[gd.state_off + st];
         if (sf & CG_STATE_SINK) fl |= CG_FLAG_DONE;
         if (sf & CG_STATE_FORCED_ONLY) fl |= CG_FLAG_FORCED_NEXT;
       }
     }
   }
   if (counts) {
-    uint32_t n = counts[b] + (tok != CG_NO_TOKEN ? 1u : 0u);
+    uint32_t n = n0 + (tok != CG_NO_TOKEN ? 1u : 0u);
     if ((fl & CG_FLAG_DONE) || n >= max_tokens) {
       if (!(fl & CG_FLAG_DONE)) fl |= CG_FLAG_CAPPED;
       ns = 0u;
