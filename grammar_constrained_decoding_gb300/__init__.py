@@ -210,6 +210,22 @@ class Ctx:
             _ptr(out_flags)))
 
 
+    def step_host(self, states, h_logits, temp: float, top_p: float, seed: int, step: int, h_out_tok, out_states,
+                  out_flags, gid=None, forced=None, counts=None, max_tokens: int = 2048, out_tok=None) -> None:
+        """cg_step with the logits in (page-locked) host memory and the ids
+        copied back to host memory; asynchronous until sync()."""
+        import torch
+        dtype = {torch.float32: L.CG_F32, torch.bfloat16: L.CG_BF16}[h_logits.dtype]
+        B, V = h_logits.shape
+        L.check("cg_step_host", L.lib().cg_step_host(
+            self._h, _ptr(states), _ptr(gid), _ptr(forced), B, _ptr(h_logits), dtype, V, float(temp), float(top_p),
+            int(seed), int(step), _ptr(counts), max_tokens, _ptr(h_out_tok), _ptr(out_tok), _ptr(out_states),
+            _ptr(out_flags)))
+
+    def sync(self) -> None:
+        L.check("cg_ctx_sync", L.lib().cg_ctx_sync(self._h))
+
+
 class Driver:
     """Host driver of forced tokens (evaluator-aware grammars)."""
 

@@ -64,6 +64,10 @@ SIGNATURES = {
     "cg_mask_and_sample_noalloc": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_uint32, C.c_uint32, C.c_void_p,
                                              C.c_float, C.c_float, C.c_uint64, C.c_uint32, C.c_void_p, C.c_void_p,
                                              C.c_uint32]),
+    "cg_step_host": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_uint32, C.c_void_p, C.c_int,
+                               C.c_uint32, C.c_float, C.c_float, C.c_uint64, C.c_uint32, C.c_void_p, C.c_uint32,
+                               C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
+    "cg_ctx_sync": (C.c_int, [C.c_void_p]),
     "cg_step": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_uint32, C.c_void_p, C.c_int, C.c_uint32,
                           C.c_float, C.c_float, C.c_uint64, C.c_uint32, C.c_void_p, C.c_uint32, C.c_void_p, C.c_void_p,
                           C.c_void_p, C.c_void_p]),

@@ -43,6 +43,15 @@ struct cg_ctx {
   uint32_t* step_bitmask = nullptr;      // bitmask of cg_step's unfused path when the caller gives none
   size_t step_bitmask_bytes = 0;
   std::vector<cgk::DevGrammar> grammars; // host copy of t.grammars
+  // cg_step_host: the copy stream, two logit buffers and their events
+  cudaStream_t copy_stream = nullptr;
+  void* host_in[2] = {nullptr, nullptr};
+  size_t host_in_bytes[2] = {0, 0};
+  cudaEvent_t copied[2] = {nullptr, nullptr};   // logits of buffer k on the device
+  cudaEvent_t consumed[2] = {nullptr, nullptr}; // the step that read buffer k has finished
+  uint32_t next_in = 0;
+  uint32_t* host_tok = nullptr;                 // ids when the caller gives no device buffer
+  size_t host_tok_bytes = 0;
   bool cache_complete = false;           // cg_ctx_prefill has filled every class mask (in stream order)
 };
 
@@ -68,6 +77,19 @@ void release(cg_ctx* c) {
   if (c->step_bitmask) cudaFree(c->step_bitmask);
   c->step_bitmask = nullptr;
   c->step_bitmask_bytes = 0;
+  for (int k = 0; k < 2; ++k) {
+    if (c->host_in[k]) cudaFree(c->host_in[k]);
+    c->host_in[k] = nullptr;
+    c->host_in_bytes[k] = 0;
+    if (c->copied[k]) cudaEventDestroy(c->copied[k]);
+    if (c->consumed[k]) cudaEventDestroy(c->consumed[k]);
+    c->copied[k] = c->consumed[k] = nullptr;
+  }
+  if (c->host_tok) cudaFree(c->host_tok);
+  c->host_tok = nullptr;
+  c->host_tok_bytes = 0;
+  if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
+  c->copy_stream = nullptr;
 }
 
 // Grows a context-owned device buffer to at least `need` bytes (synchronising
@@ -254,6 +276,7 @@ int cg_ctx_create(const cg_grammar* const* g, uint32_t n_g, const cg_vocab* v, v
 void cg_ctx_destroy(cg_ctx* c) {
   if (!c) return;
   cudaStreamSynchronize(c->stream);
+  if (c->copy_stream) cudaStreamSynchronize(c->copy_stream);
   release(c);
   delete c;
 }
@@ -370,3 +393,52 @@ int cg_step(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const in
 }
 
 }  // extern "C"
+
+int cg_ctx_sync(cg_ctx* c) {
+  if (!c) return CG_E_ARG;
+  return cudaStreamSynchronize(c->stream) == cudaSuccess ? CG_OK : CG_E_CUDA;
+}
+
+int cg_step_host(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const int32_t* d_forced, uint32_t B,
+                 const void* h_logits, int dtype, uint32_t V, float temp, float top_p, uint64_t seed, uint32_t step,
+                 uint32_t* d_counts, uint32_t max_tokens, uint32_t* h_out_tok, uint32_t* d_out_tok,
+                 uint32_t* d_out_states, uint8_t* d_out_flags) {
+  if (!c || (B && (!d_states || !h_logits || !h_out_tok || !d_out_states || !d_out_flags))) return CG_E_ARG;
+  if (dtype != CG_F32 && dtype != CG_BF16) return CG_E_ARG;
+  if (V != c->t.V || !(temp >= 0.f) || temp == INFINITY || !(top_p == top_p)) return CG_E_ARG;
+  if (d_counts && max_tokens == 0) return CG_E_ARG;
+  if (B == 0) return CG_OK;
+  if (!c->copy_stream) {
+    if (cudaStreamCreateWithFlags(&c->copy_stream, cudaStreamNonBlocking) != cudaSuccess) return CG_E_CUDA;
+    for (int k = 0; k < 2; ++k)
+      if (cudaEventCreateWithFlags(&c->copied[k], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&c->consumed[k], cudaEventDisableTiming) != cudaSuccess)
+        return CG_E_CUDA;
+  }
+  const size_t bytes = size_t(B) * V * (dtype == CG_BF16 ? 2 : 4);
+  const uint32_t k = c->next_in;
+  if (bytes > c->host_in_bytes[k] && cudaStreamSynchronize(c->copy_stream) != cudaSuccess) return CG_E_CUDA;
+  int rc = grow(c, &c->host_in[k], &c->host_in_bytes[k], bytes);
+  if (rc != CG_OK) return rc;
+  uint32_t* tok = d_out_tok;
+  if (!tok) {
+    rc = grow(c, reinterpret_cast<void**>(&c->host_tok), &c->host_tok_bytes, size_t(B) * 4);
+    if (rc != CG_OK) return rc;
+    tok = c->host_tok;
+  }
+  // buffer k is free once the step that last read it has finished (an event
+  // never recorded is complete)
+  if (cudaStreamWaitEvent(c->copy_stream, c->consumed[k], 0) != cudaSuccess ||
+      cudaMemcpyAsync(c->host_in[k], h_logits, bytes, cudaMemcpyHostToDevice, c->copy_stream) != cudaSuccess ||
+      cudaEventRecord(c->copied[k], c->copy_stream) != cudaSuccess ||
+      cudaStreamWaitEvent(c->stream, c->copied[k], 0) != cudaSuccess)
+    return CG_E_CUDA;
+  c->next_in = k ^ 1u;
+  rc = cg_step(c, d_states, d_gid, d_forced, B, c->host_in[k], dtype, V, temp, top_p, seed, step, d_counts,
+               max_tokens, nullptr, tok, d_out_states, d_out_flags);
+  if (rc != CG_OK) return rc;
+  if (cudaEventRecord(c->consumed[k], c->stream) != cudaSuccess ||
+      cudaMemcpyAsync(h_out_tok, tok, size_t(B) * 4, cudaMemcpyDeviceToHost, c->stream) != cudaSuccess)
+    return CG_E_CUDA;
+  return CG_OK;
+}

@@ -245,6 +245,35 @@ int cg_step(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const in
             uint32_t* d_counts, uint32_t max_tokens, uint32_t* d_bitmask, uint32_t* d_out_tok,
             uint32_t* d_out_states, uint8_t* d_out_flags);
 
+/* cg_step with the logits in HOST memory and the sampled ids returned to host
+ * memory: the end-to-end form of the step for a caller whose logits are not on
+ * the device.  The pages have no counterpart: it only moves the inputs and
+ * outputs of the step (usetacet.com/docs/grammar, "Constrained decoding").
+ *  h_logits  : [B][V] of dtype in host memory, page-locked (cudaHostAlloc or
+ *              cudaHostRegister) for the copy to run asynchronously; pageable
+ *              memory works but the copy then blocks the calling thread
+ *  h_out_tok : u32 [B] host memory (page-locked for an asynchronous copy)
+ *  d_out_tok : u32 [B] device memory that also receives the ids, or NULL
+ *  the rest  : as cg_step (states, forced ids, counts and flags stay on the device)
+ * The logits are copied on a stream of the context's own into one of two
+ * context-owned device buffers (grown like the sampling scratch), the step
+ * waits for that copy on the context stream, and the ids are copied back on
+ * the context stream.  The buffers alternate from call to call, so the copy of
+ * one step's logits overlaps the previous step's kernels.
+ * Asynchronous: the call returns once all of this is queued.  h_logits must
+ * stay unchanged and h_out_tok unread until cg_ctx_sync (or cg_ctx_status)
+ * has returned.  Not for stream capture.
+ * Errors: as cg_step; CG_E_CUDA when a copy, stream or event call fails. */
+int cg_step_host(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const int32_t* d_forced, uint32_t B,
+                 const void* h_logits, int dtype, uint32_t V, float temp, float top_p, uint64_t seed, uint32_t step,
+                 uint32_t* d_counts, uint32_t max_tokens, uint32_t* h_out_tok, uint32_t* d_out_tok,
+                 uint32_t* d_out_states, uint8_t* d_out_flags);
+
+/* Waits until everything queued on the context has finished (the context
+ * stream, and through it the copies of cg_step_host).  CG_E_CUDA on a CUDA
+ * error. */
+int cg_ctx_sync(cg_ctx* c);
+
 /* Variant of cg_mask_and_sample that never allocates device memory.  The pages
  * have no counterpart: it is a deployment variant of step 2, not a step of the
  * method.  Arguments, results and error codes are those of cg_mask_and_sample,

@@ -120,3 +120,39 @@ def test_step_without_bitmask_output():
             outs.append((host(tok), host(ns), host(fl)))
         for a, b in zip(*outs):
             assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("temp,top_p", [(0.7, 0.9), (0.0, 1.0)])
+def test_step_host_matches_step(temp, top_p):
+    """cg_step_host (logits in page-locked host memory, ids copied back, two
+    device buffers alternating) gives cg_step's results; four calls are queued
+    before the first sync, so copies overlap the previous steps' kernels."""
+    import torch
+    names, V, B, steps = ("calc_eval", "booking"), 128256, 40, 4
+    ctx_a, ctx_b = make_ctx(names, "bpe", V), make_ctx(names, "bpe", V)
+    gid = u16(np.arange(B) % len(names))
+    s0 = _start_states(names, B, np.random.default_rng(8))
+    st_a, st_b = u32(s0), u32(s0)
+    cnt_a, cnt_b = u32(np.zeros(B)), u32(np.zeros(B))
+    xs = [_logits(V, B, k, "bf16") for k in range(steps)]
+    hx = [x.cpu().pin_memory() for x in xs]
+    htok = [torch.full((B,), -1, dtype=torch.int32).pin_memory() for _ in range(steps)]
+    ns_b = [empty((B,), torch.int32).view(torch.uint32) for _ in range(steps)]
+    fl_b = [empty((B,), torch.uint8) for _ in range(steps)]
+    want = []
+    for k in range(steps):
+        tok = empty((B,), torch.int32)
+        ns, fl = empty((B,), torch.int32).view(torch.uint32), empty((B,), torch.uint8)
+        ctx_a.step(st_a, xs[k], temp, top_p, 5, k, tok, ns, fl, gid=gid, counts=cnt_a, max_tokens=6)
+        want.append((host(tok), host(ns), host(fl)))
+        st_a = ns
+    for k in range(steps):
+        ctx_b.step_host(st_b, hx[k], temp, top_p, 5, k, htok[k], ns_b[k], fl_b[k], gid=gid, counts=cnt_b,
+                        max_tokens=6)
+        st_b = ns_b[k]
+    ctx_b.sync()
+    assert ctx_a.status() == 0 and ctx_b.status() == 0
+    for k in range(steps):
+        assert np.array_equal(htok[k].numpy(), want[k][0]), k
+        assert np.array_equal(host(ns_b[k]), want[k][1]), k
+        assert np.array_equal(host(fl_b[k]), want[k][2]), k
