@@ -175,3 +175,77 @@ def accept(dfa: OracleDFA, state: int, tok: int, tokens: list[bytes], forced: bo
     if (dfa.next[ns, :256] < 0).all() and (dfa.next[ns, 256:] >= 0).any():
         flags |= FLAG_FORCED_NEXT
     return ns, flags
+
+
+FLAG_CAPPED = 16
+FLAG_DRAFT_CUT = 32
+
+
+@dataclass
+class DraftResult:
+    n: int               # draft tokens accepted (a prefix of the draft)
+    path: list[int]      # state before position 0 .. n (path[j + 1]: after draft token j)
+    state: int           # the row's state afterwards (0 after DONE or CAPPED)
+    flags: int
+    count: int | None    # token count afterwards (when counts are kept)
+
+
+def state_flags(dfa: OracleDFA, s: int) -> int:
+    """DONE / FORCED_NEXT of a live state, as ``accept`` reports them."""
+    flags = 0
+    if dfa.accept[s] and (dfa.next[s] < 0).all():
+        flags |= FLAG_DONE
+    if (dfa.next[s, :256] < 0).all() and (dfa.next[s, 256:] >= 0).any():
+        flags |= FLAG_FORCED_NEXT
+    return flags
+
+
+def accept_many(dfa: OracleDFA, state: int, draft: list[int], tokens: list[bytes],
+                forced: list[int] | None = None, count: int | None = None,
+                max_tokens: int | None = None) -> DraftResult:
+    """Speculative verification of a draft against the grammar
+    (labs.miniml.ai "Evaluator aware decoding", "Where XGrammar-2 could take
+    this": a draft token that closes an evaluated span pins the tokens that
+    follow it, whose check is then exact string matching).
+
+    Token j of the draft is accepted when ``accept`` of it from the state left
+    by tokens 0..j-1 does not reach DEAD; where ``forced[j] >= 0`` the host has
+    pinned position j, so the token must equal that id and is walked as
+    injected bytes.  Verification stops at the first refused token (flag
+    DRAFT_CUT; the state stays that of the accepted prefix), after a token that
+    ends the grammar (DONE), when the token count reaches max_tokens (CAPPED),
+    or after a token whose state continues only with injected bytes when
+    position j+1 is not pinned (the host has to evaluate the span first).
+    The flags also carry DONE / FORCED_NEXT of the final state.  As in
+    ``accept``, a row whose accepted tokens end it (DONE) or reach the cap
+    restarts from state 0 with count 0.  An empty draft reports NO_TOKEN; a
+    DEAD row accepts nothing (REJECTED)."""
+    forced = forced if forced is not None else [-1] * len(draft)
+    path = [state]
+    if not draft:
+        return DraftResult(0, path, state, FLAG_NO_TOKEN, count)
+    if state < 0:
+        return DraftResult(0, path, state, FLAG_REJECTED, count)
+    s, n, cut, capped, c = state, 0, 0, 0, count
+    for j, t in enumerate(draft):
+        f = forced[j]
+        ns = DEAD if (f >= 0 and t != f) else accept(dfa, s, t, tokens, f >= 0)[0]
+        if ns == DEAD:
+            cut = FLAG_DRAFT_CUT
+            break
+        s, n = ns, n + 1
+        path.append(s)
+        if c is not None:
+            c += 1
+        if state_flags(dfa, s) & FLAG_DONE:
+            break
+        if c is not None and c >= max_tokens:
+            capped = FLAG_CAPPED
+            break
+        if state_flags(dfa, s) & FLAG_FORCED_NEXT and not (j + 1 < len(draft) and forced[j + 1] >= 0):
+            break
+    flags = state_flags(dfa, s) | cut | capped
+    if n > 0 and flags & (FLAG_DONE | FLAG_CAPPED):
+        s = 0
+        c = 0 if c is not None else None
+    return DraftResult(n, path, s, flags, c)
