@@ -216,10 +216,11 @@ def accept_many(dfa: OracleDFA, state: int, draft: list[int], tokens: list[bytes
     ends the grammar (DONE), when the token count reaches max_tokens (CAPPED),
     or after a token whose state continues only with injected bytes when
     position j+1 is not pinned (the host has to evaluate the span first).
-    The flags also carry DONE / FORCED_NEXT of the final state.  As in
-    ``accept``, a row whose accepted tokens end it (DONE) or reach the cap
-    restarts from state 0 with count 0.  An empty draft reports NO_TOKEN; a
-    DEAD row accepts nothing (REJECTED)."""
+    The flags also carry DONE / FORCED_NEXT of the final state.  When token
+    counts are kept (``count`` given), a row whose accepted tokens end it
+    (DONE) or reach the cap restarts from state 0 with count 0, as the device
+    accept does with counts.  An empty draft reports NO_TOKEN; a DEAD row
+    accepts nothing (REJECTED)."""
     forced = forced if forced is not None else [-1] * len(draft)
     path = [state]
     if not draft:
@@ -245,7 +246,6 @@ def accept_many(dfa: OracleDFA, state: int, draft: list[int], tokens: list[bytes
         if state_flags(dfa, s) & FLAG_FORCED_NEXT and not (j + 1 < len(draft) and forced[j + 1] >= 0):
             break
     flags = state_flags(dfa, s) | cut | capped
-    if n > 0 and flags & (FLAG_DONE | FLAG_CAPPED):
-        s = 0
-        c = 0 if c is not None else None
+    if c is not None and n > 0 and flags & (FLAG_DONE | FLAG_CAPPED):
+        s, c = 0, 0
     return DraftResult(n, path, s, flags, c)
