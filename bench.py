@@ -247,6 +247,42 @@ def run_ours(args) -> dict | None:
         sampler.stop()
     del graphs, sample_graphs
 
+    # speculative verification (cg_accept_many): drafts of K = 8 tokens taken
+    # from the workload's own next 8 steps, verified from the states before them
+    K = 8
+    s_before = states.clone()
+    c_before = counts.clone()
+    draft = torch.empty((B, K), dtype=torch.int32, device="cuda")
+    for j in range(K):
+        step(2 * 10**6 + j, bufs[j % R])
+        draft[:, j] = tok
+    states.copy_(s_before)
+    counts.copy_(c_before)
+    dlen = torch.full((B,), K, dtype=torch.int32, device="cuda").view(torch.uint32)
+    am_s = torch.empty(B, dtype=torch.int32, device="cuda").view(torch.uint32)
+    am_n = torch.empty(B, dtype=torch.int32, device="cuda").view(torch.uint32)
+    am_f = torch.empty(B, dtype=torch.uint8, device="cuda")
+    am_path = torch.empty((B, K + 1), dtype=torch.int32, device="cuda").view(torch.uint32)
+    draft_u = draft.view(torch.uint32)
+
+    def verify():
+        ctx.accept_many(states, draft_u, dlen, am_s, am_n, am_f, gid=gid, path=am_path)
+
+    for _ in range(3):
+        verify()
+    torch.cuda.synchronize()
+    n_am = 500
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(n_am):
+        verify()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    am_us = a0.elapsed_time(a1) / n_am * 1e3
+    am_accepted = float(am_n.view(torch.int32).float().mean().item())
+    if ctx.status() != 0:
+        raise RuntimeError("device status after accept_many")
+
     # end to end through cg_step_host: each step's logits copied from
     # page-locked host memory (overlapping the previous step's kernel) and its
     # ids copied back to host memory
@@ -304,7 +340,9 @@ def run_ours(args) -> dict | None:
                    "mask_classes": info["n_classes"]},
         "gpu_launches": args.steps,
         "kernel_us": {"step (cg_step, one fused kernel)": round(per_step * 1e3, 3),
-                      "step as three calls (fill_bitmask, mask_and_sample, accept)": round(three_ms * 1e3, 3)},
+                      "step as three calls (fill_bitmask, mask_and_sample, accept)": round(three_ms * 1e3, 3),
+                      "accept_many (B rows, drafts of 8 tokens from the next 8 steps)": round(am_us, 3)},
+        "accept_many_mean_accepted": round(am_accepted, 3),
         "roofline": {"kernel": "stream_topp_kernel<true> (cg_step)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),

@@ -210,6 +210,15 @@ class Ctx:
             _ptr(out_flags)))
 
 
+    def accept_many(self, states, draft, draft_len, out_states, out_n, out_flags, gid=None, forced=None,
+                    counts=None, max_tokens: int = 2048, path=None) -> None:
+        """Speculative verification: the longest grammatical prefix of each row's
+        draft ([B, K] ids, draft_len per row); forced [B, K] pins positions."""
+        B, K = draft.shape
+        L.check("cg_accept_many", L.lib().cg_accept_many(
+            self._h, _ptr(states), _ptr(gid), _ptr(draft), _ptr(draft_len), _ptr(forced), B, K, _ptr(counts),
+            max_tokens, _ptr(out_states), _ptr(out_n), _ptr(out_flags), _ptr(path)))
+
     def step_host(self, states, h_logits, temp: float, top_p: float, seed: int, step: int, h_out_tok, out_states,
                   out_flags, gid=None, forced=None, counts=None, max_tokens: int = 2048, out_tok=None) -> None:
         """cg_step with the logits in (page-locked) host memory and the ids

@@ -16,6 +16,7 @@ CG_GBNF, CG_JSON_SCHEMA = 0, 1
 CG_F32, CG_BF16 = 0, 1
 CG_DEAD = CG_NO_TOKEN = 0xFFFFFFFF
 CG_FLAG_DONE, CG_FLAG_FORCED_NEXT, CG_FLAG_REJECTED, CG_FLAG_NO_TOKEN, CG_FLAG_CAPPED = 1, 2, 4, 8, 16
+CG_FLAG_DRAFT_CUT = 32
 CG_STATE_ACCEPT, CG_STATE_SINK, CG_STATE_FORCED_ONLY = 1, 2, 4
 CG_SAMPLE_INPLACE = 1
 CG_NOALLOC_MAX_ROWS = 64
@@ -64,6 +65,8 @@ SIGNATURES = {
     "cg_mask_and_sample_noalloc": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_uint32, C.c_uint32, C.c_void_p,
                                              C.c_float, C.c_float, C.c_uint64, C.c_uint32, C.c_void_p, C.c_void_p,
                                              C.c_uint32]),
+    "cg_accept_many": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_uint32,
+                                 C.c_uint32, C.c_void_p, C.c_uint32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
     "cg_step_host": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_uint32, C.c_void_p, C.c_int,
                                C.c_uint32, C.c_float, C.c_float, C.c_uint64, C.c_uint32, C.c_void_p, C.c_uint32,
                                C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),

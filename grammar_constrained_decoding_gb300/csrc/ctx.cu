@@ -28,6 +28,10 @@ cudaError_t launch_step(const Tables& t, const uint32_t* states, const uint16_t*
 cudaError_t launch_accept(const Tables& t, const uint32_t* states, const uint16_t* gid, const uint32_t* toks,
                           const int32_t* forced, uint32_t B, uint32_t* counts, uint32_t max_tokens,
                           uint32_t* out_states, uint8_t* out_flags, cudaStream_t stream);
+cudaError_t launch_accept_many(const Tables& t, const uint32_t* states, const uint16_t* gid, const uint32_t* draft,
+                               const uint32_t* draft_len, const int32_t* forced, uint32_t B, uint32_t K,
+                               uint32_t* counts, uint32_t max_tokens, uint32_t* out_states, uint32_t* out_n,
+                               uint8_t* out_flags, uint32_t* path, cudaStream_t stream);
 }  // namespace cgk
 
 struct cg_ctx {
@@ -441,4 +445,17 @@ int cg_step_host(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, con
       cudaMemcpyAsync(h_out_tok, tok, size_t(B) * 4, cudaMemcpyDeviceToHost, c->stream) != cudaSuccess)
     return CG_E_CUDA;
   return CG_OK;
+}
+
+int cg_accept_many(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const uint32_t* d_draft,
+                   const uint32_t* d_draft_len, const int32_t* d_forced, uint32_t B, uint32_t K, uint32_t* d_counts,
+                   uint32_t max_tokens, uint32_t* d_out_states, uint32_t* d_out_n, uint8_t* d_out_flags,
+                   uint32_t* d_out_path) {
+  if (!c || (B && (!d_states || !d_draft || !d_draft_len || !d_out_states || !d_out_n || !d_out_flags))) return CG_E_ARG;
+  if (B && K == 0) return CG_E_ARG;
+  if (d_counts && max_tokens == 0) return CG_E_ARG;
+  return cgk::launch_accept_many(c->t, d_states, d_gid, d_draft, d_draft_len, d_forced, B, K, d_counts, max_tokens,
+                                 d_out_states, d_out_n, d_out_flags, d_out_path, c->stream) == cudaSuccess
+             ? CG_OK
+             : CG_E_CUDA;
 }

@@ -100,6 +100,61 @@ struct StateWindow {
   uint32_t lo = 0, rows = 0;
 };
 
+// Walks token tok's bytes from state st of grammar gd through the columns
+// `cols` (the symbol -> column map, shifted by 256 for injected bytes); returns
+// CG_DEAD when a byte has no transition.  win (optional): a window of the
+// 16-bit table in shared memory, read instead of global memory for its states.
+__device__ inline uint32_t walk_token(const Tables& t, const DevGrammar& gd, const uint16_t* cols, uint32_t st,
+                                      uint32_t tok, const StateWindow& win) {
+  const uint32_t* table = t.table + gd.table_off;
+  const uint32_t nc = gd.n_cols;
+  auto step_from = [&](uint32_t s, uint32_t col) -> uint32_t {
+    const uint32_t r = s - win.lo;
+    if (r < win.rows) {
+      const uint16_t nx = win.next[r * nc + col];
+      return nx == kDead16 ? CG_DEAD : uint32_t(nx);
+    }
+    return table[size_t(s) * nc + col];
+  };
+  uint32_t len = kLongToken;
+  uint4 r0 = make_uint4(0u, 0u, 0u, 0u), r1 = r0;
+  if (t.tok_rec) {
+    // the token's bytes in one 32-byte record
+    r0 = t.tok_rec[size_t(tok) * 2];
+    r1 = t.tok_rec[size_t(tok) * 2 + 1];
+    len = r0.x & 0xFFu;
+  }
+  if (len != kLongToken) {
+    const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+    for (uint32_t k = 0; k < 31; ++k) {
+      if (k >= len || st == CG_DEAD) break;
+      const uint32_t byte = (w[(k + 1) >> 2] >> (8 * ((k + 1) & 3))) & 0xFFu;
+      st = step_from(st, cols[byte]);
+    }
+    return st;
+  }
+  // the offset table; the token's columns first (independent loads), then the
+  // chain of lookups
+  const uint32_t i0 = t.tok_off[tok], n = t.tok_off[tok + 1] - i0;
+  uint32_t col[kPrefetch];
+#pragma unroll
+  for (uint32_t k = 0; k < kPrefetch; ++k) col[k] = k < n ? cols[t.tok_bytes[i0 + k]] : 0u;
+#pragma unroll
+  for (uint32_t k = 0; k < kPrefetch; ++k)
+    if (k < n && st != CG_DEAD) st = step_from(st, col[k]);
+  for (uint32_t i = i0 + kPrefetch; i < i0 + n && st != CG_DEAD; ++i) st = step_from(st, cols[t.tok_bytes[i]]);
+  return st;
+}
+
+// CG_FLAG_DONE / CG_FLAG_FORCED_NEXT of a live state from its CG_STATE_* bits.
+__device__ __forceinline__ uint8_t state_result_flags(uint8_t sf) {
+  uint8_t fl = 0;
+  if (sf & CG_STATE_SINK) fl |= CG_FLAG_DONE;
+  if (sf & CG_STATE_FORCED_ONLY) fl |= CG_FLAG_FORCED_NEXT;
+  return fl;
+}
+
 // Advance one row by its token (labs.miniml.ai "Evaluator aware decoding":
 // after injection the grammar state must be advanced; a forced token's bytes
 // are walked as host-injected symbols).  With token counts, finished or capped
@@ -137,56 +192,15 @@ __device__ inline void accept_row(const Tables& t, uint32_t b, uint32_t g, uint3
       ns = CG_DEAD;
       fl = CG_FLAG_REJECTED;
     } else {
-      const uint32_t shift = f >= 0 ? 256u : 0u;
-      const uint16_t* cols = (cols_g ? cols_g : t.colmap + size_t(g) * 512) + shift;
-      const uint32_t* table = t.table + gd.table_off;
-      const uint32_t nc = gd.n_cols;
-      auto step_from = [&](uint32_t st, uint32_t col) -> uint32_t {
-        const uint32_t r = st - win.lo;
-        if (r < win.rows) {
-          const uint16_t nx = win.next[r * nc + col];
-          return nx == kDead16 ? CG_DEAD : uint32_t(nx);
-        }
-        return table[size_t(st) * nc + col];
-      };
-      uint32_t st = s;
-      uint32_t len = kLongToken;
-      uint4 r0 = make_uint4(0u, 0u, 0u, 0u), r1 = r0;
-      if (t.tok_rec) {
-        // the token's bytes in one 32-byte record
-        r0 = t.tok_rec[size_t(tok) * 2];
-        r1 = t.tok_rec[size_t(tok) * 2 + 1];
-        len = r0.x & 0xFFu;
-      }
-      if (len != kLongToken) {
-        const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-#pragma unroll
-        for (uint32_t k = 0; k < 31; ++k) {
-          if (k >= len || st == CG_DEAD) break;
-          const uint32_t byte = (w[(k + 1) >> 2] >> (8 * ((k + 1) & 3))) & 0xFFu;
-          st = step_from(st, cols[byte]);
-        }
-      } else {
-        // the offset table; the token's columns first (independent loads),
-        // then the chain of lookups
-        const uint32_t i0 = t.tok_off[tok], n = t.tok_off[tok + 1] - i0;
-        uint32_t col[kPrefetch];
-#pragma unroll
-        for (uint32_t k = 0; k < kPrefetch; ++k) col[k] = k < n ? cols[t.tok_bytes[i0 + k]] : 0u;
-#pragma unroll
-        for (uint32_t k = 0; k < kPrefetch; ++k)
-          if (k < n && st != CG_DEAD) st = step_from(st, col[k]);
-        for (uint32_t i = i0 + kPrefetch; i < i0 + n && st != CG_DEAD; ++i) st = step_from(st, cols[t.tok_bytes[i]]);
-      }
+      const uint16_t* cols = (cols_g ? cols_g : t.colmap + size_t(g) * 512) + (f >= 0 ? 256u : 0u);
+      const uint32_t st = walk_token(t, gd, cols, s, tok, win);
       ns = st;
       if (st == CG_DEAD) {
         record_error(t.status, CG_DEV_REJECTED);
         fl = CG_FLAG_REJECTED;
       } else {
         const uint32_t r = st - win.lo;
-        const uint8_t sf = r < win.rows ? win.flags[r] : t.state_flags[gd.state_off + st];
-        if (sf & CG_STATE_SINK) fl |= CG_FLAG_DONE;
-        if (sf & CG_STATE_FORCED_ONLY) fl |= CG_FLAG_FORCED_NEXT;
+        fl = state_result_flags(r < win.rows ? win.flags[r] : t.state_flags[gd.state_off + st]);
       }
     }
   }
@@ -200,6 +214,95 @@ __device__ inline void accept_row(const Tables& t, uint32_t b, uint32_t g, uint3
     counts[b] = n;
   }
   out_states[b] = ns;
+  out_flags[b] = fl;
+}
+
+// Speculative verification of row b's draft toks[0 .. n) (labs.miniml.ai
+// "Evaluator aware decoding", "Where XGrammar-2 could take this": a draft
+// token that closes an evaluated span pins the tokens that follow it, and
+// checking those is exact matching).  Accepts the longest prefix whose tokens
+// the grammar allows one after another; a position with forced[j] >= 0 must
+// carry exactly that id and is walked as injected bytes.  Stops at the first
+// refused token (CG_FLAG_DRAFT_CUT, the state stays that of the prefix), after
+// a token that ends the grammar, when the count reaches max_tokens, or after a
+// token whose state continues only with injected bytes when the next position
+// is not pinned.  With counts, a row ended or capped by its accepted tokens
+// restarts from state 0 with count 0.  Writes out_n[b] (tokens accepted), out_states[b],
+// out_flags[b] (CG_FLAG_DONE / CG_FLAG_FORCED_NEXT of the final state plus
+// CG_FLAG_DRAFT_CUT / CG_FLAG_CAPPED; CG_FLAG_NO_TOKEN for an empty draft,
+// CG_FLAG_REJECTED for a dead row), counts[b], and path[0 .. K] (optional):
+// the state before each position up to out_n, CG_DEAD after.
+__device__ inline void accept_many_row(const Tables& t, uint32_t b, uint32_t g, uint32_t s, const uint32_t* toks,
+                                       uint32_t n, const int32_t* forced, uint32_t K, uint32_t* counts,
+                                       uint32_t max_tokens, uint32_t* out_states, uint32_t* out_n,
+                                       uint8_t* out_flags, uint32_t* path) {
+  uint32_t c = counts ? counts[b] : 0u;
+  uint32_t st = s, acc = 0;
+  uint8_t fl = 0;
+  if (n > K) {
+    record_error(t.status, CG_DEV_BAD_LENGTH);
+    n = K;
+  }
+  if (path) path[0] = s;
+  if (n == 0) {
+    fl = CG_FLAG_NO_TOKEN;
+  } else if (g >= t.n_g) {
+    record_error(t.status, CG_DEV_BAD_GID);
+    st = CG_DEAD;
+    fl = CG_FLAG_REJECTED;
+  } else if (s == CG_DEAD) {
+    fl = CG_FLAG_REJECTED;
+  } else {
+    const DevGrammar gd = t.grammars[g];
+    if (s >= gd.n_states) {
+      record_error(t.status, CG_DEV_BAD_STATE);
+      st = CG_DEAD;
+      fl = CG_FLAG_REJECTED;
+    } else {
+      const uint16_t* cols0 = t.colmap + size_t(g) * 512;
+      uint8_t cut = 0, capped = 0;
+      uint8_t sres = state_result_flags(t.state_flags[gd.state_off + st]);
+      int32_t f = forced ? forced[0] : -1;
+      for (uint32_t j = 0; j < n; ++j) {
+        const uint32_t tok = toks[j];
+        const int32_t f_next = (forced && j + 1 < n) ? forced[j + 1] : -1;
+        if (tok >= t.V) {
+          record_error(t.status, CG_DEV_BAD_TOKEN);
+          cut = CG_FLAG_DRAFT_CUT;
+          break;
+        }
+        const uint32_t ns = (f >= 0 && tok != uint32_t(f))
+                                ? CG_DEAD
+                                : walk_token(t, gd, cols0 + (f >= 0 ? 256u : 0u), st, tok, StateWindow());
+        if (ns == CG_DEAD) {
+          cut = CG_FLAG_DRAFT_CUT;
+          break;
+        }
+        st = ns;
+        ++acc;
+        ++c;
+        if (path) path[acc] = st;
+        sres = state_result_flags(t.state_flags[gd.state_off + st]);
+        if (sres & CG_FLAG_DONE) break;
+        if (counts && c >= max_tokens) {
+          capped = CG_FLAG_CAPPED;
+          break;
+        }
+        if ((sres & CG_FLAG_FORCED_NEXT) && f_next < 0) break;
+        f = f_next;
+      }
+      fl = sres | cut | capped;
+      if (counts && acc > 0 && (fl & (CG_FLAG_DONE | CG_FLAG_CAPPED))) {
+        st = 0u;
+        c = 0u;
+      }
+    }
+  }
+  if (path)
+    for (uint32_t j = acc + 1; j <= K; ++j) path[j] = CG_DEAD;
+  if (counts) counts[b] = c;
+  out_states[b] = st;
+  out_n[b] = acc;
   out_flags[b] = fl;
 }
 

@@ -71,6 +71,7 @@ extern "C" {
 #define CG_FLAG_REJECTED    4u  /* the token was not allowed: state is CG_DEAD */
 #define CG_FLAG_NO_TOKEN    8u  /* the row had no token this step */
 #define CG_FLAG_CAPPED     16u  /* the row hit max_tokens and was reset */
+#define CG_FLAG_DRAFT_CUT  32u  /* accept_many: a draft token was refused; the state is the accepted prefix's */
 
 /* state flags exported by cg_grammar_export */
 #define CG_STATE_ACCEPT      1u
@@ -88,6 +89,7 @@ extern "C" {
 #define CG_DEV_REJECTED        7  /* accept: the token walks the automaton to CG_DEAD */
 #define CG_DEV_TIMEOUT         8  /* sample: a bounded wait for an asynchronous copy ran out;
                                      the row gets CG_NO_TOKEN */
+#define CG_DEV_BAD_LENGTH      9  /* accept_many: a draft length > K (clamped to K) */
 
 /* mask_and_sample flags */
 #define CG_SAMPLE_INPLACE 1u     /* also write -inf into masked logits (the "&mut [f32]" form) */
@@ -312,6 +314,42 @@ int cg_mask_and_sample_noalloc(cg_ctx* c, void* d_logits, int dtype, uint32_t B,
 int cg_accept(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const uint32_t* d_toks,
               const int32_t* d_forced, uint32_t B, uint32_t* d_counts, uint32_t max_tokens,
               uint32_t* d_out_states, uint8_t* d_out_flags);
+
+/* Speculative verification of drafts against the grammar (labs.miniml.ai
+ * "Evaluator aware decoding", "Where XGrammar-2 could take this": a draft token
+ * that closes an evaluated span pins the tokens that must follow it, so their
+ * verification is exact string matching).  Per row, the longest prefix of the
+ * draft whose tokens the grammar allows one after another is accepted, as
+ * cg_accept would accept them one per step.
+ *  d_states, d_gid : as in cg_accept (d_gid may be NULL)
+ *  d_draft         : u32 [B][K] draft token ids, row-major; d_draft_len u32 [B]
+ *                    the number of them per row (at most K; a longer length is
+ *                    clamped to K and recorded as CG_DEV_BAD_LENGTH)
+ *  d_forced        : i32 [B][K] or NULL; forced[b][j] >= 0 pins position j: the
+ *                    draft token there must equal it and is walked as
+ *                    host-injected bytes (the result tokens the host computed)
+ *  d_counts, max_tokens : as in cg_accept; each accepted token counts
+ *  d_out_states    : u32 [B] the state after the accepted prefix (may alias d_states)
+ *  d_out_n         : u32 [B] draft tokens accepted
+ *  d_out_flags     : u8 [B] CG_FLAG_DONE / CG_FLAG_FORCED_NEXT of that state, plus
+ *                    CG_FLAG_DRAFT_CUT (a token was refused: not an error, the
+ *                    state is the accepted prefix's), CG_FLAG_CAPPED,
+ *                    CG_FLAG_NO_TOKEN (empty draft), CG_FLAG_REJECTED (dead row)
+ *  d_out_path      : u32 [B][K + 1] or NULL: the state before each position
+ *                    0..out_n (the caller masks the next position's logits from
+ *                    it), CG_DEAD after out_n
+ * Verification of a row stops at the first refused token, after a token that
+ * ends the grammar, when the count reaches max_tokens, and after a token whose
+ * state continues only with injected bytes when the next position is not
+ * pinned (the host evaluates the span, then pins its result).  With d_counts a
+ * row ended or capped by its accepted tokens restarts from state 0 with count
+ * 0.  Device errors as cg_accept (a refused token is not one).
+ * Errors: CG_E_ARG for a NULL required pointer, K == 0 with B > 0, or d_counts
+ * with max_tokens == 0. */
+int cg_accept_many(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const uint32_t* d_draft,
+                   const uint32_t* d_draft_len, const int32_t* d_forced, uint32_t B, uint32_t K, uint32_t* d_counts,
+                   uint32_t max_tokens, uint32_t* d_out_states, uint32_t* d_out_n, uint8_t* d_out_flags,
+                   uint32_t* d_out_path);
 
 /* ---- evaluator-aware host side --------------------------------------------------- */
 
