@@ -320,7 +320,6 @@ constexpr uint32_t kHistBytes = kHists * kBins * 8;
 constexpr uint32_t kNucCap = (kRing - kHistBytes) / 6;          // packed nucleus entries (u32 id + u16 key)
 constexpr float kMarginZ = 9.0f;                                // nats below the maximum kept as candidates
 constexpr float kNoRef = -1e30f;                                // finite reference before any allowed logit
-constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kMaxCols = 512;                              // symbol columns a grammar can have
 constexpr uint32_t kWinRowsMax = 512;                           // states in the accept's table window
 constexpr uint32_t kWinBytesMax = 16384;                        // shared memory for that window
@@ -328,41 +327,6 @@ constexpr uint32_t kSlots = 16;                                 // list entries 
 constexpr uint32_t kCandPerRow = kThreads * kSlots;             // candidate list entries per row (8192)
 constexpr uint32_t kBatchIds = 4;                               // nucleus id loads in flight per thread
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// bounded wait on a phase; false when the limit ran out
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
 // 2^x with the multi-function unit (relative error about 2^-22; results
 // below 2^-126 flush to zero, far below any mass that matters here)
 __device__ __forceinline__ float ex2(float x) {
@@ -616,22 +580,16 @@ __device__ void stage_accept_tables(const StepArgs& sa, uint32_t g, uint32_t s, 
   if (g >= t.n_g) return;
   for (uint32_t i = lane; i < 512; i += 32) scols[i] = t.colmap[size_t(g) * 512 + i];
   const DevGrammar gd = step_grammar(sa, g);
-  if (!t.table16 || s >= gd.n_states || gd.n_cols == 0 || sa.win_bytes < 32) return;
-  const uint32_t cap = min(kWinRowsMax, (sa.win_bytes - 16) / (2 * gd.n_cols));
-  if (cap == 0) return;
-  const uint32_t hi = min(gd.n_states, max(s, cap / 2) + (cap - cap / 2));
-  const uint32_t lo = hi > cap ? hi - cap : 0u;
-  const uint32_t rows = hi - lo;
-  const uintptr_t src = reinterpret_cast<uintptr_t>(t.table16 + gd.table_off + size_t(lo) * gd.n_cols);
-  const uintptr_t src0 = src & ~uintptr_t(15);
-  const uint32_t bytes = (uint32_t(src - src0) + rows * gd.n_cols * 2 + 15u) & ~15u;  // <= win_bytes
+  const WindowCopy wc = window_copy(t, gd, s, sa.win_bytes, kWinRowsMax);
+  if (wc.rows == 0) return;
   if (lane == 0) {
-    mbar_expect_tx(mbar_win, bytes);
-    bulk_g2s(win, reinterpret_cast<const void*>(src0), bytes, mbar_win);
-    *s_wlo = lo;
-    *s_wdelta = uint32_t(src - src0) / 2;
-    *s_wrows = rows;
+    mbar_expect_tx(mbar_win, wc.bytes);
+    bulk_g2s(win, wc.src, wc.bytes, mbar_win);
+    *s_wlo = wc.lo;
+    *s_wdelta = wc.delta;
+    *s_wrows = wc.rows;
   }
+  const uint32_t lo = wc.lo, rows = wc.rows;
   for (uint32_t i = lane; i < rows; i += 32) wflags[i] = t.state_flags[gd.state_off + lo + i];
 }
 

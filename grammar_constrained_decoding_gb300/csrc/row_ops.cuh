@@ -100,12 +100,38 @@ struct StateWindow {
   uint32_t lo = 0, rows = 0;
 };
 
+// Rows of the 16-bit table to copy for a window around state s: at most
+// max_rows states and cap_bytes of shared memory (an aligned bulk copy may
+// start up to 15 bytes early).  Fills lo/rows, the copy's 16-byte aligned
+// source and size, and delta, the entries to skip at the start of the copy.
+// rows == 0: no window (no 16-bit table, or nothing fits).
+struct WindowCopy {
+  uint32_t lo = 0, rows = 0, delta = 0, bytes = 0;
+  const void* src = nullptr;
+};
+__device__ inline WindowCopy window_copy(const Tables& t, const DevGrammar& gd, uint32_t s, uint32_t cap_bytes,
+                                         uint32_t max_rows) {
+  WindowCopy w;
+  if (!t.table16 || s >= gd.n_states || gd.n_cols == 0 || cap_bytes < 32) return w;
+  const uint32_t cap = min(max_rows, (cap_bytes - 16) / (2 * gd.n_cols));
+  if (cap == 0) return w;
+  const uint32_t hi = min(gd.n_states, max(s, cap / 2) + (cap - cap / 2));
+  w.lo = hi > cap ? hi - cap : 0u;
+  w.rows = hi - w.lo;
+  const uintptr_t src = reinterpret_cast<uintptr_t>(t.table16 + gd.table_off + size_t(w.lo) * gd.n_cols);
+  const uintptr_t src0 = src & ~uintptr_t(15);
+  w.src = reinterpret_cast<const void*>(src0);
+  w.delta = uint32_t(src - src0) / 2;
+  w.bytes = (uint32_t(src - src0) + w.rows * gd.n_cols * 2 + 15u) & ~15u;  // <= cap_bytes
+  return w;
+}
+
 // Walks token tok's bytes from state st of grammar gd through the columns
 // `cols` (the symbol -> column map, shifted by 256 for injected bytes); returns
 // CG_DEAD when a byte has no transition.  win (optional): a window of the
 // 16-bit table in shared memory, read instead of global memory for its states.
 __device__ inline uint32_t walk_token(const Tables& t, const DevGrammar& gd, const uint16_t* cols, uint32_t st,
-                                      uint32_t tok, const StateWindow& win) {
+                                      uint32_t tok, const StateWindow& win, const uint4* rec = nullptr) {
   const uint32_t* table = t.table + gd.table_off;
   const uint32_t nc = gd.n_cols;
   auto step_from = [&](uint32_t s, uint32_t col) -> uint32_t {
@@ -118,10 +144,10 @@ __device__ inline uint32_t walk_token(const Tables& t, const DevGrammar& gd, con
   };
   uint32_t len = kLongToken;
   uint4 r0 = make_uint4(0u, 0u, 0u, 0u), r1 = r0;
-  if (t.tok_rec) {
-    // the token's bytes in one 32-byte record
-    r0 = t.tok_rec[size_t(tok) * 2];
-    r1 = t.tok_rec[size_t(tok) * 2 + 1];
+  if (rec || t.tok_rec) {
+    // the token's bytes in one 32-byte record (rec: a copy already loaded)
+    r0 = rec ? rec[0] : t.tok_rec[size_t(tok) * 2];
+    r1 = rec ? rec[1] : t.tok_rec[size_t(tok) * 2 + 1];
     len = r0.x & 0xFFu;
   }
   if (len != kLongToken) {
@@ -231,11 +257,14 @@ __device__ inline void accept_row(const Tables& t, uint32_t b, uint32_t g, uint3
 // out_flags[b] (CG_FLAG_DONE / CG_FLAG_FORCED_NEXT of the final state plus
 // CG_FLAG_DRAFT_CUT / CG_FLAG_CAPPED; CG_FLAG_NO_TOKEN for an empty draft,
 // CG_FLAG_REJECTED for a dead row), counts[b], and path[0 .. K] (optional):
-// the state before each position up to out_n, CG_DEAD after.
+// the state before each position up to out_n, CG_DEAD after.  recs (optional):
+// the token records of positions 0 .. n_recs already copied into shared
+// memory; win (optional): a window of the 16-bit table (only shorten loads).
 __device__ inline void accept_many_row(const Tables& t, uint32_t b, uint32_t g, uint32_t s, const uint32_t* toks,
                                        uint32_t n, const int32_t* forced, uint32_t K, uint32_t* counts,
                                        uint32_t max_tokens, uint32_t* out_states, uint32_t* out_n,
-                                       uint8_t* out_flags, uint32_t* path) {
+                                       uint8_t* out_flags, uint32_t* path, const uint4* recs = nullptr,
+                                       uint32_t n_recs = 0, const StateWindow& win = StateWindow()) {
   uint32_t c = counts ? counts[b] : 0u;
   uint32_t st = s, acc = 0;
   uint8_t fl = 0;
@@ -261,7 +290,11 @@ __device__ inline void accept_many_row(const Tables& t, uint32_t b, uint32_t g, 
     } else {
       const uint16_t* cols0 = t.colmap + size_t(g) * 512;
       uint8_t cut = 0, capped = 0;
-      uint8_t sres = state_result_flags(t.state_flags[gd.state_off + st]);
+      auto flags_of = [&](uint32_t x) -> uint8_t {
+        const uint32_t r = x - win.lo;
+        return state_result_flags(r < win.rows ? win.flags[r] : t.state_flags[gd.state_off + x]);
+      };
+      uint8_t sres = flags_of(st);
       int32_t f = forced ? forced[0] : -1;
       for (uint32_t j = 0; j < n; ++j) {
         const uint32_t tok = toks[j];
@@ -273,7 +306,8 @@ __device__ inline void accept_many_row(const Tables& t, uint32_t b, uint32_t g, 
         }
         const uint32_t ns = (f >= 0 && tok != uint32_t(f))
                                 ? CG_DEAD
-                                : walk_token(t, gd, cols0 + (f >= 0 ? 256u : 0u), st, tok, StateWindow());
+                                : walk_token(t, gd, cols0 + (f >= 0 ? 256u : 0u), st, tok, win,
+                                             j < n_recs ? recs + 2 * j : nullptr);
         if (ns == CG_DEAD) {
           cut = CG_FLAG_DRAFT_CUT;
           break;
@@ -282,7 +316,7 @@ __device__ inline void accept_many_row(const Tables& t, uint32_t b, uint32_t g, 
         ++acc;
         ++c;
         if (path) path[acc] = st;
-        sres = state_result_flags(t.state_flags[gd.state_off + st]);
+        sres = flags_of(st);
         if (sres & CG_FLAG_DONE) break;
         if (counts && c >= max_tokens) {
           capped = CG_FLAG_CAPPED;
