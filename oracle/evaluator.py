@@ -143,16 +143,22 @@ def evaluate(span: bytes) -> int:
 
 
 def format_result(span: bytes | None, fmt: str) -> bytes:
-    """Bytes the host forces after the span closes (no span found -> parse error)."""
+    """Bytes the host forces after the span closes (no span found -> parse error).
+    ``strop_tag`` evaluates a string operation (oracle.strops) and writes the
+    result as ``calc_tag`` does."""
     try:
         if span is None:
             raise EvalError('parse')
-        value = str(evaluate(span)).encode('ascii')
+        if fmt == 'strop_tag':
+            from .strops import evaluate_strop
+            value = evaluate_strop(span)
+        else:
+            value = str(evaluate(span)).encode('ascii')
         ok = True
     except EvalError as e:
         value = e.code.encode('ascii')
         ok = False
-    if fmt == 'calc_tag':
+    if fmt in ('calc_tag', 'strop_tag'):
         return (b'<result>' + value + b'</result>') if ok else \
                (b'<result_error>' + value + b'</result_error>')
     if fmt == 'json_answer':

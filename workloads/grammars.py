@@ -52,10 +52,10 @@ class GrammarSpec:
     # Evaluator-aware grammars: the host evaluates the text between the last
     # ``span_open`` and the ``span_close`` that ends the generated text when
     # the automaton enters a forced region, and forces the formatted result.
-    evaluator: str | None = None     # "arith" or None
+    evaluator: str | None = None     # "arith", "strop" or None
     span_open: bytes = b""
     span_close: bytes = b""
-    result_format: str = ""         # "calc_tag" | "json_answer"
+    result_format: str = ""         # "calc_tag" | "json_answer" | "strop_tag"
 
 
 CALC_CALL = r'''
@@ -144,6 +144,18 @@ norun ::= ( [^ ] | " "{1,8} [^ ] )* " "{0,8}
 answer ::= ", \"answer\": " ( "-"? [0-9]{1,64} "}" | "null, \"error\": \"" [a-z_]{1,32} "\"}" )
 '''
 
+STROP_EVAL = r'''
+# The answer is <strop>OP("...")</strop><result>V</result> then a short tail.
+root ::= "The answer is <strop>" call "</strop>" @forced( result ) tail
+call ::= "count(" str "," sp str ")" | "len(" str ")" | "reverse(" str ")" | "upper(" str ")"
+       | "substr(" str "," sp int "," sp int ")"
+str ::= "\"" ( [a-zA-Z0-9 .,!?'\-] | "\\\"" | "\\\\" ){0,24} "\""
+int ::= "-"? [0-9]{1,2}
+sp ::= " "?
+result ::= "<result>" [^<]{0,64} "</result>" | "<result_error>" [a-z_]{1,32} "</result_error>"
+tail ::= [a-z ,]{0,24} "."
+'''
+
 
 GRAMMARS: dict[str, GrammarSpec] = {
     "calc_call": GrammarSpec("calc_call", "gbnf", CALC_CALL),
@@ -156,6 +168,8 @@ GRAMMARS: dict[str, GrammarSpec] = {
     "json_eval": GrammarSpec("json_eval", "gbnf", JSON_EVAL, evaluator="arith",
                              span_open=b'{"expression": "', span_close=b'"',
                              result_format="json_answer"),
+    "strop_eval": GrammarSpec("strop_eval", "gbnf", STROP_EVAL, evaluator="strop",
+                              span_open=b"<strop>", span_close=b"</strop>", result_format="strop_tag"),
     "extraction": GrammarSpec("extraction", "json", extraction_schema()),
     "reasoned": GrammarSpec("reasoned", "json", reasoned_schema()),
 }
