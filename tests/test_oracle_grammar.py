@@ -24,7 +24,7 @@ import pytest
 from oracle.dfa import DEAD, build_dfa, compile_grammar, is_acyclic, walk
 from oracle.grammar import GrammarError, gbnf_to_tree, schema_to_tree
 from tests.oracle_cache import oracle_dfa, parse_marked
-from workloads import GRAMMARS, Bounds
+from workloads import CONFIGS, GRAMMARS, Bounds
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "worked_strings.txt")
 
@@ -353,7 +353,8 @@ def test_workload_automata_invariants(name):
     # always offers the model a byte (all single bytes are tokens: mask non-empty)
     assert np.all(sink | fo | model_moves)
     assert int(dfa.accept.sum()) == int(sink.sum())           # accepting states are final
-    assert 500 <= dfa.n_states <= 30000
+    if any(name in c.grammars for c in CONFIGS.values()):
+        assert 500 <= dfa.n_states <= 30000                   # the workloads' automaton sizes
 
 
 def test_fail_closed():
