@@ -283,6 +283,17 @@ def run_ours(args) -> dict | None:
     if ctx.status() != 0:
         raise RuntimeError("device status after accept_many")
 
+    # host evaluators of the forced-token path, per call through the C ABI
+    # (Python's call overhead included) on the pages' examples
+    host_eval = {}
+    for label, fn, span in (("arith 17 * 23 + 91", lambda x: cg.eval_arith(x, "calc_tag"), b"17 * 23 + 91"),
+                            ('strop count("strawberry", "r")', cg.eval_strop, b'count("strawberry", "r")')):
+        fn(span)
+        t_h = time.perf_counter()
+        for _ in range(20000):
+            fn(span)
+        host_eval[label] = round((time.perf_counter() - t_h) / 20000 * 1e6, 3)
+
     # end to end through cg_step_host: each step's logits copied from
     # page-locked host memory (overlapping the previous step's kernel) and its
     # ids copied back to host memory
@@ -343,6 +354,7 @@ def run_ours(args) -> dict | None:
                       "step as three calls (fill_bitmask, mask_and_sample, accept)": round(three_ms * 1e3, 3),
                       "accept_many (B rows, drafts of 8 tokens from the next 8 steps)": round(am_us, 3)},
         "accept_many_mean_accepted": round(am_accepted, 3),
+        "host_eval_us_per_call": host_eval,
         "roofline": {"kernel": "stream_topp_kernel<true> (cg_step)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),

@@ -123,6 +123,14 @@ def eval_arith(span: bytes, fmt: str) -> tuple[bytes, bool]:
     return buf.raw[:n.value], bool(ok.value)
 
 
+def eval_strop(span: bytes) -> tuple[bytes, bool]:
+    """A string operation's forced bytes (<result>V</result> or <result_error>code</result_error>)."""
+    buf = C.create_string_buffer(256)
+    n, ok = C.c_size_t(), C.c_int()
+    L.check("cg_eval_strop", L.lib().cg_eval_strop(span, len(span), buf, len(buf), C.byref(n), C.byref(ok)))
+    return buf.raw[:n.value], bool(ok.value)
+
+
 def _ptr(t) -> int | None:
     if t is None:
         return None

@@ -1,7 +1,8 @@
-// Host side of evaluator-aware decoding: an exact arithmetic evaluator, the
-// result formatting the host injects, and the per-row forced-token driver
-// (labs.miniml.ai "Evaluator aware decoding": "The core idea" steps 1-4,
-// "A concrete prototype on llama.cpp").
+// Host side of evaluator-aware decoding: an exact arithmetic evaluator, a
+// string-operation evaluator, the result formatting the host injects, and the
+// per-row forced-token driver (labs.miniml.ai "Evaluator aware decoding": "The
+// core idea" steps 1-4, "A concrete prototype on llama.cpp", "Not just
+// arithmetic: string operations").
 //
 // Values are exact rationals num/den over arbitrary-precision integers; a
 // span longer than 4096 bytes is refused as overflow (evaluators must stay
@@ -252,6 +253,118 @@ class Evaluator {
   }
 };
 
+// ------------------------------------------------------------- string operations
+// Span: NAME '(' ARG (',' ARG)* ')' with spaces around the pieces; ARG is a
+// string literal "..." (escapes \" and \\ only) or an integer -?[0-9]{1,9}.
+// count(s, sub) non-overlapping occurrences left to right (sub not empty),
+// len(s) bytes, reverse(s), upper(s) (ASCII a-z), substr(s, i, j) the slice
+// [i, j) with negative indices from the end, both clamped to [0, len].  Strings
+// are bytes.  Results over 64 bytes are "overflow"; a result holding '<'
+// (which would end the result tag) is "bad_char".
+struct StrArg {
+  bool is_str = false;
+  std::string s;
+  long long v = 0;
+};
+
+std::string eval_strop(const std::string& span) {
+  if (span.size() > 4096) throw EvalFail{"overflow"};
+  const size_t n = span.size();
+  size_t i = 0;
+  auto at = [&](size_t k) { return static_cast<unsigned char>(span[k]); };
+  auto skip = [&]() { while (i < n && at(i) == ' ') ++i; };
+  skip();
+  const size_t name0 = i;
+  while (i < n && at(i) >= 'a' && at(i) <= 'z') ++i;
+  const std::string name = span.substr(name0, i - name0);
+  if (name.empty()) throw EvalFail{"parse"};
+  skip();
+  if (i >= n || at(i) != '(') throw EvalFail{"parse"};
+  ++i;
+  std::vector<StrArg> args;
+  for (;;) {
+    skip();
+    StrArg a;
+    if (i < n && at(i) == '"') {
+      a.is_str = true;
+      ++i;
+      for (;;) {
+        if (i >= n) throw EvalFail{"parse"};
+        const unsigned char ch = at(i);
+        if (ch == '"') { ++i; break; }
+        if (ch == '\\') {
+          if (i + 1 >= n || (at(i + 1) != '"' && at(i + 1) != '\\')) throw EvalFail{"parse"};
+          a.s.push_back(span[i + 1]);
+          i += 2;
+          continue;
+        }
+        a.s.push_back(span[i]);
+        ++i;
+      }
+    } else {
+      const bool neg = i < n && at(i) == '-';
+      const size_t d0 = neg ? i + 1 : i;
+      size_t d = d0;
+      while (d < n && at(d) >= '0' && at(d) <= '9') ++d;
+      if (d == d0 || d - d0 > 9) throw EvalFail{"parse"};
+      long long v = 0;
+      for (size_t k = d0; k < d; ++k) v = v * 10 + (at(k) - '0');
+      a.v = neg ? -v : v;
+      i = d;
+    }
+    args.push_back(std::move(a));
+    skip();
+    if (i < n && at(i) == ',') { ++i; continue; }
+    if (i < n && at(i) == ')') { ++i; break; }
+    throw EvalFail{"parse"};
+  }
+  skip();
+  if (i != n) throw EvalFail{"parse"};
+  auto kinds = [&](const char* k) {  // 's' string, 'i' integer, one letter per argument
+    const size_t m = std::strlen(k);
+    if (args.size() != m) return false;
+    for (size_t q = 0; q < m; ++q)
+      if (args[q].is_str != (k[q] == 's')) return false;
+    return true;
+  };
+  std::string out;
+  if (name == "count") {
+    if (!kinds("ss")) throw EvalFail{"arity"};
+    const std::string& h = args[0].s;
+    const std::string& nd = args[1].s;
+    if (nd.empty()) throw EvalFail{"empty"};
+    size_t c = 0;
+    for (size_t p = 0; p + nd.size() <= h.size();) {
+      if (h.compare(p, nd.size(), nd) == 0) { ++c; p += nd.size(); } else { ++p; }
+    }
+    out = std::to_string(c);
+  } else if (name == "len") {
+    if (!kinds("s")) throw EvalFail{"arity"};
+    out = std::to_string(args[0].s.size());
+  } else if (name == "reverse") {
+    if (!kinds("s")) throw EvalFail{"arity"};
+    out.assign(args[0].s.rbegin(), args[0].s.rend());
+  } else if (name == "upper") {
+    if (!kinds("s")) throw EvalFail{"arity"};
+    out = args[0].s;
+    for (char& ch : out) {
+      const unsigned char u = static_cast<unsigned char>(ch);
+      if (u >= 'a' && u <= 'z') ch = char(u - 32);
+    }
+  } else if (name == "substr") {
+    if (!kinds("sii")) throw EvalFail{"arity"};
+    const long long L = static_cast<long long>(args[0].s.size());
+    auto clamp = [&](long long x) { if (x < 0) x += L; return std::min(std::max(x, 0LL), L); };
+    const long long a = clamp(args[1].v), b = clamp(args[2].v);
+    if (a < b) out = args[0].s.substr(size_t(a), size_t(b - a));
+  } else {
+    throw EvalFail{"unknown_op"};
+  }
+  if (out.size() > 64) throw EvalFail{"overflow"};
+  if (out.find('<') != std::string::npos) throw EvalFail{"bad_char"};
+  return out;
+}
+
 bool put(uint8_t* out, size_t cap, size_t* out_len, const std::string& s) {
   *out_len = s.size();
   if (!out || s.size() > cap) return false;
@@ -260,7 +373,7 @@ bool put(uint8_t* out, size_t cap, size_t* out_len, const std::string& s) {
 }
 
 std::string format(const std::string& value, bool ok, int fmt) {
-  if (fmt == CG_RESULT_CALC_TAG)
+  if (fmt == CG_RESULT_CALC_TAG || fmt == CG_RESULT_STROP_TAG)
     return ok ? "<result>" + value + "</result>" : "<result_error>" + value + "</result_error>";
   return ok ? ", \"answer\": " + value + "}" : ", \"answer\": null, \"error\": \"" + value + "\"}";
 }
@@ -270,8 +383,12 @@ std::string evaluate_and_format(const std::string& span, bool found, int fmt, bo
   bool ok = false;
   try {
     if (!found) throw EvalFail{"parse"};
-    if (span.size() > 4096) throw EvalFail{"overflow"};
-    value = to_decimal(Evaluator(span).run());
+    if (fmt == CG_RESULT_STROP_TAG) {
+      value = eval_strop(span);
+    } else {
+      if (span.size() > 4096) throw EvalFail{"overflow"};
+      value = to_decimal(Evaluator(span).run());
+    }
     ok = true;
   } catch (const EvalFail& f) {
     value = f.code;
@@ -289,6 +406,15 @@ int cg_eval_arith(const uint8_t* span, size_t n, int fmt, uint8_t* out, size_t c
   if (fmt != CG_RESULT_CALC_TAG && fmt != CG_RESULT_JSON_ANSWER) return CG_E_ARG;
   bool good = false;
   std::string s = evaluate_and_format(std::string(reinterpret_cast<const char*>(span), n), true, fmt, &good);
+  if (ok) *ok = good ? 1 : 0;
+  return put(out, cap, out_len, s) ? CG_OK : CG_E_LIMIT;
+}
+
+int cg_eval_strop(const uint8_t* span, size_t n, uint8_t* out, size_t cap, size_t* out_len, int* ok) {
+  if ((!span && n) || !out_len) return CG_E_ARG;
+  bool good = false;
+  std::string s = evaluate_and_format(std::string(reinterpret_cast<const char*>(span), n), true, CG_RESULT_STROP_TAG,
+                                      &good);
   if (ok) *ok = good ? 1 : 0;
   return put(out, cap, out_len, s) ? CG_OK : CG_E_LIMIT;
 }

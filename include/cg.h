@@ -355,6 +355,7 @@ int cg_accept_many(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, c
 
 #define CG_RESULT_CALC_TAG    0  /* <result>V</result> | <result_error>code</result_error> */
 #define CG_RESULT_JSON_ANSWER 1  /* , "answer": V}     | , "answer": null, "error": "code"} */
+#define CG_RESULT_STROP_TAG   2  /* string operation: <result>V</result> | <result_error>code</result_error> */
 
 /* Evaluate an arithmetic span exactly over the rationals (labs.miniml.ai
  * "Evaluator aware decoding": "17 * 23 + 91 = 482") and format the bytes the
@@ -367,6 +368,20 @@ int cg_accept_many(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, c
 int cg_eval_arith(const uint8_t* span, size_t n, int fmt, uint8_t* out, size_t cap,
                   size_t* out_len, int* ok);
 
+/* Evaluate a string operation (labs.miniml.ai "Evaluator aware decoding", "Not
+ * just arithmetic: string operations": count("strawberry", "r") = 3) and format
+ * the bytes the host forces as CG_RESULT_STROP_TAG.  Span: NAME(ARG, ...) with
+ * spaces around the pieces; ARG a string literal "..." (escapes \" and \\
+ * only) or an integer -?[0-9]{1,9}.  count(s, sub) counts non-overlapping
+ * occurrences left to right; len(s) counts bytes; reverse(s); upper(s) raises
+ * ASCII a-z; substr(s, i, j) is the slice [i, j) with negative indices counted
+ * from the end and both ends clamped.  Strings are bytes.  Failures format an
+ * error code: parse, unknown_op, arity, empty (count of ""), overflow (a result
+ * over 64 bytes or a span over 4096), bad_char (a result holding '<').
+ * Writes up to cap bytes; out_len receives the length (CG_E_LIMIT if cap is
+ * too small).  *ok receives 1 for a result, 0 for an error code. */
+int cg_eval_strop(const uint8_t* span, size_t n, uint8_t* out, size_t cap, size_t* out_len, int* ok);
+
 /* Host driver of forced tokens for B rows (labs.miniml.ai "Evaluator aware
  * decoding", "The core idea" steps 1-4).  Row b uses grammar rules[gid[b]]:
  * when a step leaves the row in a forced-only state with nothing queued, the
@@ -375,7 +390,8 @@ int cg_eval_arith(const uint8_t* span, size_t n, int fmt, uint8_t* out, size_t c
 typedef struct {
     const uint8_t* span_open;  size_t span_open_len;
     const uint8_t* span_close; size_t span_close_len;
-    int result_format;         /* CG_RESULT_*, or -1 for a grammar without evaluator */
+    int result_format;         /* CG_RESULT_* (the evaluator follows from it), or -1 for a grammar
+                                  without evaluator */
 } cg_span_rule;
 
 int cg_driver_create(const cg_vocab* v, uint32_t B, const uint16_t* h_gid,

@@ -21,7 +21,7 @@ from tests.test_oracle_grammar import _gbnf, _lang, _rand_tree
 from workloads import GRAMMARS, Bounds as WBounds
 
 gcd = pytest.importorskip("grammar_constrained_decoding_gb300")
-from grammar_constrained_decoding_gb300 import Bounds, Grammar, Vocab, Driver, eval_arith, _lib  # noqa: E402
+from grammar_constrained_decoding_gb300 import Bounds, Grammar, Vocab, Driver, eval_arith, eval_strop, _lib  # noqa: E402
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "cg.h")
 
@@ -133,6 +133,34 @@ def test_evaluator_matches_oracle():
             assert out == format_result(span, fmt), span
 
 
+def test_string_operations_match_oracle():
+    """cg_eval_strop against the oracle's string-operation evaluator, on the
+    page's example, the error cases and random well- and ill-formed spans."""
+    rng = random.Random(23)
+    spans = [b'count("strawberry", "r")', b'len("")', b'substr("abc", -2, 99)', b'upper("a<b")', b'reverse("b<")',
+             b'count("a", "")', b'lower("a")', b'len(1)', b'len("a"', b' len ( "a\\\"b" ) ', b'substr("a", 1, 2, 3)',
+             b'substr("abc", 1234567890, 1)', b'upper("' + b"x" * 70 + b'")', b'len("' + b"y" * 5000 + b'")', b""]
+    ops = [b"count", b"len", b"reverse", b"upper", b"substr", b"lower"]
+    chars = b'ab rs"\\<,()-0123456789'
+    for _ in range(4000):
+        args = []
+        for _ in range(rng.randint(0, 3)):
+            if rng.random() < 0.6:
+                body = bytes(rng.choice(b"abcrs .!\\\"") for _ in range(rng.randint(0, 12)))
+                args.append(b'"' + body + b'"')
+            else:
+                args.append(str(rng.randint(-30, 30)).encode())
+        span = rng.choice(ops) + b"(" + b", ".join(args) + b")"
+        if rng.random() < 0.2:
+            k = rng.randrange(len(span) + 1)
+            span = span[:k] + bytes([rng.choice(chars)]) + span[k:]
+        spans.append(span)
+    for span in spans:
+        out, ok = eval_strop(span)
+        assert out == format_result(span, "strop_tag"), span
+        assert ok == out.startswith(b"<result>"), span
+
+
 def test_tokenizer_matches_oracle():
     toks = vocab("bpe", 4000)
     v = Vocab(toks)
@@ -173,3 +201,35 @@ def test_driver_matches_oracle_host_rules():
             break
     text = b"".join(toks[t] for t in produced)
     assert text == b"The expression is <calc>17 + 23 * 2</calc><result>63</result>."
+
+
+def test_driver_evaluates_string_operations():
+    """The C++ driver evaluates a <strop> span and queues the result tokens the
+    oracle's host rules queue (the page's count("strawberry", "r") = 3)."""
+    spec = GRAMMARS["strop_eval"]
+    toks = [bytes([b]) for b in range(256)] + [b"<result>", b"</result>", b"straw", b"berry"]
+    v = Vocab(toks)
+    d = Driver(v, 1, None, [(spec.span_open, spec.span_close, _lib.CG_RESULT_STROP_TAG)])
+    run = OracleRun([oracle_dfa("strop_eval")], [spec], toks, 2048)
+    row = Row(0, 0)
+    script = list(b'The answer is <strop>count("') + [258, 259] + list(b'", "r")</strop>')
+    fnext = np.full(1, -1, np.int32)
+    produced = []
+    for step in range(120):
+        x = np.zeros(len(toks))
+        if script and not row.queue:
+            x[script[0]] = 9.0
+        else:
+            x[ord(".")] = 9.0
+        rec = run.step_row(row, x, 0.0, 1.0, 0, step)
+        if rec["forced"] < 0 and script:
+            script.pop(0)
+        used = np.array([rec["forced"]], np.int32)
+        assert used[0] == fnext[0]
+        d.update(np.array([rec["tok"]], np.uint32), np.array([rec["flags"]], np.uint8), used, fnext)
+        assert fnext[0] == (row.queue[0] if row.queue else -1)
+        produced.append(rec["tok"])
+        if rec["flags"] & FLAG_DONE:
+            break
+    text = b"".join(toks[t] for t in produced)
+    assert text == b'The answer is <strop>count("strawberry", "r")</strop><result>3</result>.'

@@ -4,7 +4,8 @@ host) decode the same rows from the same logits, step by step, and must agree
 on every token, every accept flag and every forced token -- including the
 steps where a row closes an arithmetic span, the host evaluates it and the
 result is forced into the row (labs.miniml.ai "Evaluator aware decoding",
-"The core idea").  A sampled token may differ only where the oracle reports a
+"The core idea"; string operations: "Not just arithmetic: string
+operations").  A sampled token may differ only where the oracle reports a
 tolerance case (top-two Gumbel scores or the top-p boundary within 1e-5); such
 a row is not compared further.
 """
@@ -18,13 +19,15 @@ from workloads import GRAMMARS, make_logits
 
 pytestmark = pytest.mark.gpu
 
-FORMATS = {"calc_tag": 0, "json_answer": 1}
+FORMATS = {"calc_tag": 0, "json_answer": 1, "strop_tag": 2}
 
 
 @pytest.mark.parametrize("names,temp,top_p", [
     (("calc_eval", "json_eval"), 0.0, 1.0),
     (("calc_eval", "json_eval"), 0.8, 0.9),
     (("calc_eval", "booking"), 0.7, 1.0),
+    (("strop_eval", "calc_eval"), 0.0, 1.0),
+    (("strop_eval", "json_eval"), 0.7, 0.9),
 ])
 def test_trajectory_matches_oracle(names, temp, top_p):
     import torch
@@ -45,7 +48,7 @@ def test_trajectory_matches_oracle(names, temp, top_p):
     counts = u32(np.zeros(B))
     forced_next = np.full(B, -1, np.int32)
     live = np.ones(B, bool)
-    forced_steps = 0
+    forced_steps = np.zeros(len(names), int)
     for step in range(steps):
         vals, raw = make_logits(V, list(range(B)), step, seed, 2.0, 4.0, 0.05, "bf16")
         x = torch.from_numpy(raw.view(np.int16)).cuda().view(torch.bfloat16)
@@ -67,7 +70,7 @@ def test_trajectory_matches_oracle(names, temp, top_p):
                 live[b] = False
                 continue
             assert int(f_gpu[b]) == rec["flags"], (step, b, int(f_gpu[b]), rec["flags"])
-            forced_steps += rec["forced"] >= 0
+            forced_steps[b % len(names)] += rec["forced"] >= 0
         drv.update(t_gpu, f_gpu, forced_used, forced_next)
         s_gpu = host(states).view(np.uint32)
         for b in range(B):
@@ -75,4 +78,6 @@ def test_trajectory_matches_oracle(names, temp, top_p):
                 assert int(s_gpu[b]) == rows[b].state, (step, b, int(s_gpu[b]), rows[b].state)
     assert live.sum() >= B // 2
     if temp == 0.0:
-        assert forced_steps > 0, "no row reached an evaluated span"
+        for k, spec in enumerate(specs):
+            if spec.result_format:
+                assert forced_steps[k] > 0, f"no {spec.name} row reached an evaluated span"
