@@ -547,4 +547,239 @@ def source_to_tree(kind: str, source: str, bounds) -> tuple:
         return gbnf_to_tree(source, bounds.depth_max)
     if kind == 'json':
         return schema_to_tree(source, bounds.ws_max, bounds.max_len_default, bounds.max_items_default)
+    if kind == 'structtag':
+        return structtag_to_tree(source, bounds.ws_max, bounds.max_len_default, bounds.max_items_default)
     raise GrammarError('syntax', f'unknown grammar kind {kind}')
+
+
+# ----------------------------------------------------------------------------
+# Structural tags
+# ----------------------------------------------------------------------------
+#
+# labs.miniml.ai "Evaluator aware decoding", "Where XGrammar-2 could take
+# this": a Structural Tag is a JSON description whose atomic types (JSON
+# schema, regex, literal strings) nest, and an evaluated tag is a tag
+# (begin, content, end) whose completed content goes to a registered evaluator
+# with the result forced into a sibling span.  The page sketches one element
+# only; the reading taken here:
+#   {"type": "literal", "text": S}
+#   {"type": "regex", "pattern": P}          P in the subset of regex_to_tree, its
+#                                            match at most max_len_default bytes
+#   {"type": "json_schema", "json_schema": J}   the JSON-schema subset above
+#   {"type": "sequence", "elements": [E...]} {"type": "or", "elements": [E...]}
+#   {"type": "tag", "begin": S, "content": E, "end": S}
+#   {"type": "evaluated_tag", "begin": S, "content": E, "end": S,
+#    "evaluator": "arithmetic" | "string",
+#    "result": {"begin": "<result>", "end": "</result>"}}
+# An evaluated tag is followed by a forced region: <result>V</result> (V an
+# optional minus and 1..64 digits for arithmetic, 0..64 bytes other than '<'
+# for string operations) or <result_error>[a-z_]{1,32}</result_error>, the
+# forms the host injects.  Unknown types or keys, other result tags and empty
+# alternatives fail closed.
+
+_RE_SPECIAL = set(b'()[]{}|*+?.\\^$')
+_RE_CLASS_ESC = {ord('d'): b'0123456789',
+                 ord('w'): b'abcdefghijklmnopqrstuvwxyzABCDEFGHIJKLMNOPQRSTUVWXYZ0123456789_',
+                 ord('s'): b' \t\n\r\x0b\x0c'}
+_RE_CHAR_ESC = {ord('n'): 0x0A, ord('t'): 0x09, ord('r'): 0x0D, ord('f'): 0x0C, ord('v'): 0x0B}
+
+
+def regex_to_tree(pattern: str) -> tuple:
+    """Regex subset over model bytes: literals, '.', classes [..] with ranges and
+    '^', escapes (\\d \\w \\s \\n \\t \\r \\f \\v and escaped punctuation), groups,
+    '|', and the postfix operators * + ? {m} {m,} {m,n}.  '.' is any byte but
+    a newline.  Anchors, backreferences, lookarounds and non-ASCII characters
+    inside classes fail closed."""
+    src = pattern.encode('utf-8')
+    pos = [0]
+
+    def peek():
+        return src[pos[0]] if pos[0] < len(src) else None
+
+    def take():
+        c = peek()
+        if c is None:
+            raise GrammarError('syntax', 'regex: unexpected end')
+        pos[0] += 1
+        return c
+
+    def escape_atom():
+        c = take()
+        if c in _RE_CLASS_ESC:
+            return sym_of(_RE_CLASS_ESC[c])
+        if c in _RE_CHAR_ESC:
+            return sym_of([_RE_CHAR_ESC[c]])
+        if c in _RE_SPECIAL or c in b'-/"\'':
+            return sym_of([c])
+        raise GrammarError('unsupported', f'regex escape \\{chr(c)}')
+
+    def class_atom():
+        neg = False
+        if peek() == ord('^'):
+            take()
+            neg = True
+        members = set()
+        first = True
+        while True:
+            c = take()
+            if c == ord(']') and not first:
+                break
+            first = False
+            if c == ord('\\'):
+                e = take()
+                if e in _RE_CLASS_ESC:
+                    members |= set(_RE_CLASS_ESC[e])
+                    continue
+                lo = _RE_CHAR_ESC.get(e, e)
+            else:
+                lo = c
+            if lo >= 0x80:
+                raise GrammarError('unsupported', 'regex: non-ASCII in a class')
+            if peek() == ord('-') and pos[0] + 1 < len(src) and src[pos[0] + 1] != ord(']'):
+                take()
+                h = take()
+                if h == ord('\\'):
+                    h = take()
+                    h = _RE_CHAR_ESC.get(h, h)
+                if h >= 0x80 or h < lo:
+                    raise GrammarError('syntax', 'regex: bad class range')
+                members |= set(range(lo, h + 1))
+            else:
+                members.add(lo)
+        if neg:
+            members = set(range(256)) - members
+        return sym_of(members)
+
+    def atom():
+        c = take()
+        if c == ord('('):
+            if peek() == ord('?'):
+                raise GrammarError('unsupported', 'regex: group flags')
+            x = alternation()
+            if take() != ord(')'):
+                raise GrammarError('syntax', 'regex: unbalanced (')
+            return x
+        if c == ord('['):
+            return class_atom()
+        if c == ord('.'):
+            return sym_of(b for b in range(256) if b != 0x0A)
+        if c == ord('\\'):
+            return escape_atom()
+        if c in b'^$':
+            raise GrammarError('unsupported', 'regex: anchors')
+        if c in b')|*+?{}]':
+            raise GrammarError('syntax', f'regex: unexpected {chr(c)}')
+        return sym_of([c])
+
+    def postfix():
+        x = atom()
+        while True:
+            c = peek()
+            if c == ord('*'):
+                take()
+                x = rep(x, 0, None)
+            elif c == ord('+'):
+                take()
+                x = rep(x, 1, None)
+            elif c == ord('?'):
+                take()
+                x = rep(x, 0, 1)
+            elif c == ord('{'):
+                take()
+                body = bytearray()
+                while peek() is not None and peek() != ord('}'):
+                    body.append(take())
+                take()
+                parts = body.decode('ascii').split(',')
+                try:
+                    m = int(parts[0])
+                    n = m if len(parts) == 1 else (None if parts[1] == '' else int(parts[1]))
+                except ValueError:
+                    raise GrammarError('syntax', 'regex: bad {m,n}') from None
+                if len(parts) > 2 or m < 0 or (n is not None and n < m):
+                    raise GrammarError('syntax', 'regex: bad {m,n}')
+                x = rep(x, m, n)
+            else:
+                return x
+
+    def sequence():
+        items = []
+        while peek() is not None and peek() not in b'|)':
+            items.append(postfix())
+        if not items:
+            return EPS
+        return cat(*items)
+
+    def alternation():
+        xs = [sequence()]
+        while peek() == ord('|'):
+            take()
+            xs.append(sequence())
+        return alt(*xs)
+
+    tree = alternation()
+    if pos[0] != len(src):
+        raise GrammarError('syntax', 'regex: unbalanced )')
+    return tree
+
+
+_ST_KEYS = {'literal': {'text'}, 'regex': {'pattern'}, 'json_schema': {'json_schema'},
+            'sequence': {'elements'}, 'or': {'elements'}, 'tag': {'begin', 'content', 'end'},
+            'evaluated_tag': {'begin', 'content', 'end', 'evaluator', 'result'}}
+
+
+def structtag_to_tree(text: str, ws_max: int, max_len_default: int, max_items_default: int) -> tuple:
+    try:
+        doc = json.loads(text)
+    except ValueError as e:
+        raise GrammarError('syntax', f'structural tag: {e}') from None
+    any_byte = sym_of(range(256))
+
+    def text_of(e, k):
+        v = e.get(k)
+        if not isinstance(v, str):
+            raise GrammarError('unsupported', f'structural tag: {k} must be a string')
+        return v.encode('utf-8')
+
+    def lower(e):
+        if not isinstance(e, dict) or e.get('type') not in _ST_KEYS:
+            raise GrammarError('unsupported', 'structural tag: unknown element')
+        ty = e['type']
+        if set(e) - {'type'} != _ST_KEYS[ty]:
+            raise GrammarError('unsupported', f'structural tag: keys of {ty}')
+        if ty == 'literal':
+            return lit(text_of(e, 'text'))
+        if ty == 'regex':
+            return ('and', (regex_to_tree(e['pattern']) if isinstance(e['pattern'], str) else
+                            _raise_unsupported('pattern'), rep(any_byte, 0, max_len_default)))
+        if ty == 'json_schema':
+            return schema_to_tree(json.dumps(e['json_schema']), ws_max, max_len_default, max_items_default)
+        if ty in ('sequence', 'or'):
+            els = e['elements']
+            if not isinstance(els, list) or (ty == 'or' and not els):
+                raise GrammarError('unsupported', f'structural tag: elements of {ty}')
+            kids = [lower(x) for x in els]
+            if ty == 'sequence':
+                return cat(*kids) if kids else EPS
+            return alt(*kids)
+        body = cat(lit(text_of(e, 'begin')), lower(e['content']), lit(text_of(e, 'end')))
+        if ty == 'tag':
+            return body
+        res = e['result']
+        if res != {'begin': '<result>', 'end': '</result>'}:
+            raise GrammarError('unsupported', 'structural tag: result tags other than <result>')
+        if e['evaluator'] == 'arithmetic':
+            value = cat(rep(lit(b'-'), 0, 1), rep(rng(0x30, 0x39), 1, 64))
+        elif e['evaluator'] == 'string':
+            value = rep(sym_of(b for b in range(256) if b != 0x3C), 0, 64)
+        else:
+            raise GrammarError('unsupported', 'structural tag: unknown evaluator')
+        error = cat(lit(b'<result_error>'), rep(sym_of(b'abcdefghijklmnopqrstuvwxyz_'), 1, 32),
+                    lit(b'</result_error>'))
+        return cat(body, forced(alt(cat(lit(b'<result>'), value, lit(b'</result>')), error)))
+
+    return lower(doc)
+
+
+def _raise_unsupported(what):
+    raise GrammarError('unsupported', f'structural tag: {what}')

@@ -46,7 +46,7 @@ class Bounds:
 @dataclass(frozen=True)
 class GrammarSpec:
     name: str
-    kind: str                   # "gbnf" | "json"
+    kind: str                   # "gbnf" | "json" | "structtag"
     source: str
     bounds: Bounds = field(default_factory=Bounds)
     # Evaluator-aware grammars: the host evaluates the text between the last
@@ -156,6 +156,22 @@ result ::= "<result>" [^<]{0,64} "</result>" | "<result_error>" [a-z_]{1,32} "</
 tail ::= [a-z ,]{0,24} "."
 '''
 
+# The page's evaluated tag (labs.miniml.ai "Evaluator aware decoding", "Where
+# XGrammar-2 could take this") inside a structural tag with the calc_eval
+# framing: the same language as calc_eval's outer shape, written as nested
+# structural-tag elements.
+CALC_STRUCTTAG = json.dumps({
+    "type": "sequence",
+    "elements": [
+        {"type": "literal", "text": "The expression is "},
+        {"type": "evaluated_tag", "begin": "<calc>",
+         "content": {"type": "regex", "pattern": "[0-9+\\-*/(). ]+"},
+         "end": "</calc>", "evaluator": "arithmetic",
+         "result": {"begin": "<result>", "end": "</result>"}},
+        {"type": "regex", "pattern": "[a-z ,]{0,24}\\."},
+    ],
+})
+
 
 GRAMMARS: dict[str, GrammarSpec] = {
     "calc_call": GrammarSpec("calc_call", "gbnf", CALC_CALL),
@@ -170,6 +186,9 @@ GRAMMARS: dict[str, GrammarSpec] = {
                              result_format="json_answer"),
     "strop_eval": GrammarSpec("strop_eval", "gbnf", STROP_EVAL, evaluator="strop",
                               span_open=b"<strop>", span_close=b"</strop>", result_format="strop_tag"),
+    "calc_structtag": GrammarSpec("calc_structtag", "structtag", CALC_STRUCTTAG, Bounds(max_len_default=48),
+                                  evaluator="arith", span_open=b"<calc>", span_close=b"</calc>",
+                                  result_format="calc_tag"),
     "extraction": GrammarSpec("extraction", "json", extraction_schema()),
     "reasoned": GrammarSpec("reasoned", "json", reasoned_schema()),
 }
