@@ -51,7 +51,7 @@ class Grammar:
         data = source.encode("utf-8") if isinstance(source, str) else bytes(source)
         out = C.c_void_p()
         err = C.create_string_buffer(512)
-        k = {"gbnf": L.CG_GBNF, "json": L.CG_JSON_SCHEMA}[kind]
+        k = {"gbnf": L.CG_GBNF, "json": L.CG_JSON_SCHEMA, "structtag": L.CG_STRUCTURAL_TAG}[kind]
         b = bounds.c()
         rc = L.lib().cg_compile(data, len(data), k, C.byref(b), C.byref(out), err, len(err))
         L.check("cg_compile", rc, err.value.decode("utf-8", "replace"))

@@ -12,7 +12,7 @@ LIB_PATH = os.path.join(_PKG, "_build", "libcg.so")
 CG_OK = 0
 CG_E_ARG, CG_E_SYNTAX, CG_E_UNSUPPORTED, CG_E_EMPTY, CG_E_UNDEFINED_RULE = -1, -2, -3, -4, -5
 CG_E_LIMIT, CG_E_CUDA, CG_E_DEVICE, CG_E_NOMEM = -6, -7, -8, -9
-CG_GBNF, CG_JSON_SCHEMA = 0, 1
+CG_GBNF, CG_JSON_SCHEMA, CG_STRUCTURAL_TAG = 0, 1, 2
 CG_F32, CG_BF16 = 0, 1
 CG_DEAD = CG_NO_TOKEN = 0xFFFFFFFF
 CG_FLAG_DONE, CG_FLAG_FORCED_NEXT, CG_FLAG_REJECTED, CG_FLAG_NO_TOKEN, CG_FLAG_CAPPED = 1, 2, 4, 8, 16

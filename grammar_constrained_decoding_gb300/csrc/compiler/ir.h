@@ -87,10 +87,12 @@ struct CompileError {
   std::string msg;
 };
 
-// Front-ends (gbnf.cpp, schema.cpp): return the root node of the language.
+// Front-ends (gbnf.cpp, schema.cpp, structtag.cpp): return the root node of the language.
 int parse_gbnf(IR& ir, const std::string& src, uint32_t depth_max);
 int lower_json_schema(IR& ir, const std::string& src, uint32_t ws_max, uint32_t max_len_default,
                       uint32_t max_items_default);
+int lower_structural_tag(IR& ir, const std::string& src, uint32_t ws_max, uint32_t max_len_default,
+                         uint32_t max_items_default);
 
 // Minimal trimmed DFA over the 512 symbols with canonical breadth-first
 // numbering (automaton.cpp).

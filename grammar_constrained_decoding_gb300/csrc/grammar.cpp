@@ -110,15 +110,16 @@ extern "C" {
 int cg_compile(const char* src, size_t src_len, int kind, const cg_bounds* bounds, cg_grammar** out,
                char* err, size_t errlen) {
   if (!src || !bounds || !out) return CG_E_ARG;
-  if (kind != CG_GBNF && kind != CG_JSON_SCHEMA) return CG_E_ARG;
+  if (kind != CG_GBNF && kind != CG_JSON_SCHEMA && kind != CG_STRUCTURAL_TAG) return CG_E_ARG;
   *out = nullptr;
   try {
     cg::IR ir;
     std::string text(src, src_len);
-    int root = kind == CG_GBNF
-                   ? cg::parse_gbnf(ir, text, bounds->depth_max)
-                   : cg::lower_json_schema(ir, text, bounds->ws_max, bounds->max_len_default,
-                                           bounds->max_items_default);
+    int root = kind == CG_GBNF ? cg::parse_gbnf(ir, text, bounds->depth_max)
+               : kind == CG_JSON_SCHEMA
+                   ? cg::lower_json_schema(ir, text, bounds->ws_max, bounds->max_len_default, bounds->max_items_default)
+                   : cg::lower_structural_tag(ir, text, bounds->ws_max, bounds->max_len_default,
+                                              bounds->max_items_default);
     auto* g = new cg_grammar;
     g->dfa = cg::build_dfa(ir, root);
     finish_grammar(g);

@@ -58,6 +58,9 @@ extern "C" {
 /* ---- enumerations ---------------------------------------------------------- */
 #define CG_GBNF        0        /* GBNF-style rule text, start rule "root" */
 #define CG_JSON_SCHEMA 1        /* JSON-schema subset */
+#define CG_STRUCTURAL_TAG 2     /* structural tag: nested literal / regex / json_schema / sequence / or /
+                                   tag / evaluated_tag elements (labs.miniml.ai "Evaluator aware
+                                   decoding", "Where XGrammar-2 could take this") */
 
 #define CG_F32  0               /* logits as IEEE binary32 */
 #define CG_BF16 1               /* logits as bfloat16 */
@@ -115,8 +118,8 @@ typedef struct {
 /* Compile a grammar to its minimal byte-level automaton (usetacet.com/docs/grammar,
  * "The guarantee": the automaton masks the logits at every step; nesting is
  * bounded so the automaton is finite).
- *  src, src_len : grammar text (GBNF rules or a JSON schema), not NUL-terminated
- *  kind         : CG_GBNF or CG_JSON_SCHEMA
+ *  src, src_len : grammar text (GBNF rules, a JSON schema or a structural tag), not NUL-terminated
+ *  kind         : CG_GBNF, CG_JSON_SCHEMA or CG_STRUCTURAL_TAG
  *  bounds       : termination bounds (not retained)
  *  out          : receives the grammar on CG_OK
  *  err, errlen  : optional buffer for a NUL-terminated message (may be NULL/0)

@@ -14,7 +14,7 @@ import pytest
 from oracle.dfa import build_dfa
 from oracle.driver import OracleRun, Row
 from oracle.evaluator import format_result, tokenize_greedy
-from oracle.grammar import GrammarError, gbnf_to_tree, schema_to_tree
+from oracle.grammar import GrammarError, gbnf_to_tree, schema_to_tree, source_to_tree
 from oracle.step import FLAG_DONE, FLAG_FORCED_NEXT
 from tests.oracle_cache import oracle_dfa, vocab
 from tests.test_oracle_grammar import _gbnf, _lang, _rand_tree
@@ -68,6 +68,62 @@ def test_compiler_matches_oracle_on_random_grammars():
         nxt, _ = Grammar.compile(src, "gbnf").export()
         assert np.array_equal(nxt, o.next), src
         done += 1
+
+
+def _rand_regex(rng, depth):
+    atoms = ["a", "b", "\\.", "[a-c]", "[^ab]", "\\d", ".", "x", "[\\-y]"]
+    if depth == 0 or rng.random() < 0.35:
+        return rng.choice(atoms)
+    kind = rng.randrange(4)
+    if kind == 0:
+        return _rand_regex(rng, depth - 1) + _rand_regex(rng, depth - 1)
+    if kind == 1:
+        return "(" + _rand_regex(rng, depth - 1) + "|" + _rand_regex(rng, depth - 1) + ")"
+    if kind == 2:
+        return "(" + _rand_regex(rng, depth - 1) + ")" + rng.choice(["*", "+", "?", "{2}", "{1,3}", "{2,}"])
+    return _rand_regex(rng, depth - 1)
+
+
+def _rand_structtag(rng, depth):
+    kind = rng.randrange(6) if depth > 0 else rng.randrange(2)
+    if kind == 0:
+        return {"type": "literal", "text": rng.choice(["ab", "x", "<t>", ""])}
+    if kind == 1:
+        return {"type": "regex", "pattern": _rand_regex(rng, 3)}
+    if kind == 2:
+        return {"type": "sequence", "elements": [_rand_structtag(rng, depth - 1) for _ in range(rng.randint(0, 3))]}
+    if kind == 3:
+        return {"type": "or", "elements": [_rand_structtag(rng, depth - 1) for _ in range(rng.randint(1, 3))]}
+    if kind == 4:
+        return {"type": "tag", "begin": "<t>", "content": _rand_structtag(rng, depth - 1), "end": "</t>"}
+    return {"type": "evaluated_tag", "begin": "<c>", "content": _rand_structtag(rng, depth - 1), "end": "</c>",
+            "evaluator": rng.choice(["arithmetic", "string"]), "result": {"begin": "<result>", "end": "</result>"}}
+
+
+def test_structural_tags_match_oracle():
+    """Random structural tags (nested regexes, sequences, alternatives, tags,
+    evaluated tags, a JSON-schema element) compile to the oracle's tables;
+    documents the oracle refuses are refused too."""
+    rng = random.Random(41)
+    wb = WBounds(max_len_default=12)
+    b = _bounds(wb)
+    docs = [_rand_structtag(rng, 3) for _ in range(120)]
+    docs.append({"type": "sequence", "elements": [
+        {"type": "literal", "text": "A:"},
+        {"type": "json_schema", "json_schema": {"type": "object", "properties": {"n": {"type": "integer"}},
+                                                "required": ["n"]}}]})
+    docs += [{"type": "regex", "pattern": "^a"}, {"type": "or", "elements": []}, {"type": "literal", "text": 3},
+             {"type": "tag", "begin": "<t>", "content": {"type": "literal", "text": "a"}, "end": "</t>", "x": 1}]
+    for doc in docs:
+        src = json.dumps(doc)
+        try:
+            o = build_dfa(source_to_tree("structtag", src, wb))
+        except GrammarError:
+            with pytest.raises(_lib.CgError):
+                Grammar.compile(src, "structtag", b)
+            continue
+        nxt, _ = Grammar.compile(src, "structtag", b).export()
+        assert np.array_equal(nxt, o.next), src
 
 
 def test_compiler_unbounded_and_recursive_rules():

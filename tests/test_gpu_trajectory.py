@@ -28,6 +28,7 @@ FORMATS = {"calc_tag": 0, "json_answer": 1, "strop_tag": 2}
     (("calc_eval", "booking"), 0.7, 1.0),
     (("strop_eval", "calc_eval"), 0.0, 1.0),
     (("strop_eval", "json_eval"), 0.7, 0.9),
+    (("calc_structtag", "strop_eval"), 0.0, 1.0),
 ])
 def test_trajectory_matches_oracle(names, temp, top_p):
     import torch
