@@ -123,6 +123,18 @@ def eval_arith(span: bytes, fmt: str) -> tuple[bytes, bool]:
     return buf.raw[:n.value], bool(ok.value)
 
 
+def mask_classes(grammars: list["Grammar"], max_len: int) -> tuple[np.ndarray, int]:
+    """Joint mask classes of grammars used in one context: (class of every
+    state, grammar after grammar; number of classes)."""
+    arr = (C.c_void_p * len(grammars))(*[g._h.value for g in grammars])
+    S, n = C.c_uint32(), C.c_uint32()
+    L.check("cg_mask_classes", L.lib().cg_mask_classes(arr, len(grammars), max_len, None, 0, C.byref(S), C.byref(n)))
+    out = np.zeros(S.value, dtype=np.uint32)
+    L.check("cg_mask_classes", L.lib().cg_mask_classes(arr, len(grammars), max_len, out.ctypes.data, S.value,
+                                                        C.byref(S), C.byref(n)))
+    return out, n.value
+
+
 def eval_strop(span: bytes) -> tuple[bytes, bool]:
     """A string operation's forced bytes (<result>V</result> or <result_error>code</result_error>)."""
     buf = C.create_string_buffer(256)

@@ -43,9 +43,12 @@ struct cg_driver {
 };
 
 namespace cg {
-// Mask classes: states whose allowed-token sets agree for every token of at
-// most max_len bytes share a class.  Returns the class of each state and the
-// number of classes (grammar.cpp).
-uint32_t mask_classes(const cg_grammar& g, uint32_t max_len, std::vector<uint32_t>& class_of,
-                      std::vector<uint32_t>& rep_state);
+// Mask classes over several grammars at once (grammar.cpp): states, of any of
+// the grammars, whose allowed-token sets agree for every token of at most
+// max_len bytes share a class (one cached mask).  States are numbered grammar
+// after grammar; rep_gid / rep_state give each class's representative
+// (grammar, state).
+uint32_t mask_classes_joint(const std::vector<const cg_grammar*>& gs, uint32_t max_len,
+                            std::vector<uint32_t>& class_of, std::vector<uint32_t>& rep_gid,
+                            std::vector<uint32_t>& rep_state);
 }  // namespace cg

@@ -165,18 +165,18 @@ int cg_ctx_create(const cg_grammar* const* g, uint32_t n_g, const cg_vocab* v, v
   uint64_t table_off = 0;
   uint32_t state_off = 0;
   try {
+    // mask classes over all grammars at once: states of different grammars
+    // with equal masks share one class and one cached mask
+    std::vector<const cg_grammar*> gs(g, g + n_g);
+    std::vector<uint32_t> rep_gid;
+    n_classes = cg::mask_classes_joint(gs, v->max_len, class_of, rep_gid, class_rep);
+    class_gid.assign(rep_gid.begin(), rep_gid.end());
     for (uint32_t i = 0; i < n_g; ++i) {
       const cg_grammar& gr = *g[i];
-      std::vector<uint32_t> cls, rep;
-      uint32_t nc = cg::mask_classes(gr, v->max_len, cls, rep);
       gdesc[i] = {table_off, gr.dfa.n_states, gr.n_cols, state_off, 0};
       table.insert(table.end(), gr.table.begin(), gr.table.end());
       std::copy(gr.col_of.begin(), gr.col_of.end(), colmap.begin() + size_t(i) * 512);
       flags.insert(flags.end(), gr.flags.begin(), gr.flags.end());
-      for (uint32_t s = 0; s < gr.dfa.n_states; ++s) class_of.push_back(cls[s] + n_classes);
-      class_rep.insert(class_rep.end(), rep.begin(), rep.end());
-      class_gid.insert(class_gid.end(), nc, uint16_t(i));
-      n_classes += nc;
       table_off += gr.table.size();
       state_off += gr.dfa.n_states;
     }

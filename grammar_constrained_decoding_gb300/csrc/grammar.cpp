@@ -64,48 +64,90 @@ void finish_grammar(cg_grammar* g) {
 
 namespace cg {
 
-uint32_t mask_classes(const cg_grammar& g, uint32_t max_len, std::vector<uint32_t>& class_of,
-                      std::vector<uint32_t>& rep_state) {
-  // Refine {all states} by model-byte successors for max_len rounds: after k
-  // rounds, two states share a class iff every model-byte word of length <= k
-  // either fails from both or from neither.  The mask of a token of <= max_len
-  // bytes therefore depends only on the class.
-  const uint32_t S = g.dfa.n_states;
-  std::vector<uint16_t> mcols;  // distinct model-byte columns
-  for (int a = 0; a < 256; ++a)
-    if (std::find(mcols.begin(), mcols.end(), g.col_of[a]) == mcols.end()) mcols.push_back(g.col_of[a]);
+uint32_t mask_classes_joint(const std::vector<const cg_grammar*>& gs, uint32_t max_len,
+                            std::vector<uint32_t>& class_of, std::vector<uint32_t>& rep_gid,
+                            std::vector<uint32_t>& rep_state) {
+  // Model bytes that every grammar maps to one column each: one representative
+  // byte per combination of columns carries all transitions.
+  std::vector<int> rep_bytes;
+  {
+    std::unordered_map<std::vector<int32_t>, int, ColHash> seen;
+    std::vector<int32_t> key(gs.size());
+    for (int a = 0; a < 256; ++a) {
+      for (size_t i = 0; i < gs.size(); ++i) key[i] = gs[i]->col_of[a];
+      if (seen.emplace(key, a).second) rep_bytes.push_back(a);
+    }
+  }
+  std::vector<uint32_t> off(gs.size() + 1, 0);
+  for (size_t i = 0; i < gs.size(); ++i) off[i + 1] = off[i] + gs[i]->dfa.n_states;
+  const uint32_t S = off.back();
+  // Refine {all states of all grammars} by model-byte successors, as in
+  // mask_classes: after k rounds two states share a class iff every model-byte
+  // word of length <= k fails from both or from neither.
   std::vector<uint32_t> cls(S, 0), next_cls(S);
   uint32_t n = 1;
   std::unordered_map<std::vector<int32_t>, uint32_t, ColHash> ids;
-  std::vector<int32_t> sig(mcols.size() + 1);
+  std::vector<int32_t> sig(rep_bytes.size() + 1);
   for (uint32_t round = 0; round < max_len; ++round) {
     ids.clear();
-    for (uint32_t s = 0; s < S; ++s) {
-      sig[0] = int32_t(cls[s]);
-      for (size_t k = 0; k < mcols.size(); ++k) {
-        uint32_t t = g.table[size_t(s) * g.n_cols + mcols[k]];
-        sig[k + 1] = t == CG_DEAD ? -1 : int32_t(cls[t]);
+    for (size_t i = 0; i < gs.size(); ++i) {
+      const cg_grammar& g = *gs[i];
+      for (uint32_t s = 0; s < g.dfa.n_states; ++s) {
+        sig[0] = int32_t(cls[off[i] + s]);
+        for (size_t k = 0; k < rep_bytes.size(); ++k) {
+          const uint32_t t = g.table[size_t(s) * g.n_cols + g.col_of[rep_bytes[k]]];
+          sig[k + 1] = t == CG_DEAD ? -1 : int32_t(cls[off[i] + t]);
+        }
+        auto it = ids.find(sig);
+        if (it == ids.end()) it = ids.emplace(sig, uint32_t(ids.size())).first;
+        next_cls[off[i] + s] = it->second;
       }
-      auto it = ids.find(sig);
-      if (it == ids.end()) it = ids.emplace(sig, uint32_t(ids.size())).first;
-      next_cls[s] = it->second;
     }
-    uint32_t m = uint32_t(ids.size());
+    const uint32_t m = uint32_t(ids.size());
     cls.swap(next_cls);
     if (m == n) break;
     n = m;
   }
   class_of = cls;
+  rep_gid.assign(n, 0);
   rep_state.assign(n, 0);
   std::vector<char> seen(n, 0);
-  for (uint32_t s = 0; s < S; ++s)
-    if (!seen[cls[s]]) { seen[cls[s]] = 1; rep_state[cls[s]] = s; }
+  for (size_t i = 0; i < gs.size(); ++i)
+    for (uint32_t s = 0; s < gs[i]->dfa.n_states; ++s) {
+      const uint32_t c = cls[off[i] + s];
+      if (!seen[c]) { seen[c] = 1; rep_gid[c] = uint32_t(i); rep_state[c] = s; }
+    }
   return n;
 }
 
 }  // namespace cg
 
 extern "C" {
+
+int cg_mask_classes(const cg_grammar* const* g, uint32_t n_g, uint32_t max_len, uint32_t* class_of, uint32_t cap,
+                    uint32_t* n_states, uint32_t* n_classes) {
+  if (!g || n_g == 0 || !n_states || !n_classes) return CG_E_ARG;
+  std::vector<const cg_grammar*> gs;
+  uint64_t S = 0;
+  for (uint32_t i = 0; i < n_g; ++i) {
+    if (!g[i]) return CG_E_ARG;
+    gs.push_back(g[i]);
+    S += g[i]->dfa.n_states;
+  }
+  try {
+    std::vector<uint32_t> cls, rg, rs;
+    *n_classes = cg::mask_classes_joint(gs, max_len, cls, rg, rs);
+    *n_states = uint32_t(S);
+    if (class_of) {
+      if (cap < S) return CG_E_LIMIT;
+      std::copy(cls.begin(), cls.end(), class_of);
+    }
+  } catch (const std::bad_alloc&) {
+    return CG_E_NOMEM;
+  }
+  return CG_OK;
+}
+
 
 int cg_compile(const char* src, size_t src_len, int kind, const cg_bounds* bounds, cg_grammar** out,
                char* err, size_t errlen) {

@@ -154,6 +154,20 @@ int cg_try_input(const cg_grammar* g, const uint8_t* s, size_t n, const uint8_t*
  * start state is live[r mod n].  out may be NULL to query n. */
 int cg_live_states(const cg_grammar* g, uint32_t* out, uint32_t cap, uint32_t* n);
 
+/* Mask classes of grammars used together in one context: a mask depends on the
+ * automaton state alone, so states with equal masks can share one cached row,
+ * across grammars too (labs.miniml.ai "Evaluator aware decoding", "Where
+ * XGrammar-2 could take this", on caching across grammars).  States
+ * of all n_g grammars, numbered grammar after grammar, share a class when every
+ * model-byte word of at most max_len bytes fails from both or from neither, so
+ * their token masks for tokens of at most max_len bytes agree; a context keeps
+ * one cached mask per class.
+ *  class_of : u32 [sum of the grammars' states] or NULL (cap entries available)
+ *  n_states : receives the total number of states; n_classes the classes
+ * Errors: CG_E_ARG, CG_E_LIMIT (cap too small), CG_E_NOMEM. */
+int cg_mask_classes(const cg_grammar* const* g, uint32_t n_g, uint32_t max_len, uint32_t* class_of, uint32_t cap,
+                    uint32_t* n_states, uint32_t* n_classes);
+
 /* ---- vocabulary --------------------------------------------------------------- */
 
 /* Token t is bytes[off[t] .. off[t+1]); V >= 1, every token 1..64 bytes.

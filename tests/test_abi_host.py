@@ -217,6 +217,37 @@ def test_string_operations_match_oracle():
         assert ok == out.startswith(b"<result>"), span
 
 
+def test_joint_mask_classes_are_sound_and_shared():
+    """Mask classes computed over several grammars at once: every class's
+    member states, from whichever grammar, have the same oracle mask, and
+    classes are shared across grammars (fewer than computed one by one)."""
+    from grammar_constrained_decoding_gb300 import mask_classes
+    from oracle.step import VocabMatrix, token_mask
+    names = ("calc_eval", "json_eval", "booking_200", "strop_eval")
+    toks = vocab("bpe", 2000)
+    max_len = max(len(t) for t in toks)
+    gs = [Grammar.compile(GRAMMARS[n].source, GRAMMARS[n].kind, _bounds(GRAMMARS[n].bounds)) for n in names]
+    cls, n = mask_classes(gs, max_len)
+    n_sep = sum(mask_classes([g], max_len)[1] for g in gs)
+    assert n < n_sep
+    dfas = [oracle_dfa(x) for x in names]
+    off = np.cumsum([0] + [d.n_states for d in dfas])
+    vm = VocabMatrix(toks)
+    members = {}
+    for gi, d in enumerate(dfas):
+        for s in range(d.n_states):
+            members.setdefault(int(cls[off[gi] + s]), []).append((gi, s))
+    shared = 0
+    for c, ms in members.items():
+        grammars = {gi for gi, _ in ms}
+        shared += len(grammars) > 1
+        pick = ms[:2] + [m for m in ms if m[0] != ms[0][0]][:2]
+        want = token_mask(dfas[pick[0][0]], vm, pick[0][1])
+        for gi, s in pick[1:]:
+            assert np.array_equal(token_mask(dfas[gi], vm, s), want), (c, pick)
+    assert shared > 0
+
+
 def test_tokenizer_matches_oracle():
     toks = vocab("bpe", 4000)
     v = Vocab(toks)
