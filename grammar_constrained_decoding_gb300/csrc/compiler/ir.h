@@ -1,8 +1,9 @@
 // Regular-expression IR shared by the grammar front-ends and the automaton
 // builder.  Symbols: 0..255 are bytes written by the model, 256..511 are the
-// same bytes injected by the host (forced tokens), so the evaluator-aware
-// rule "the grammar should not allow the model to write its own <result>
-// block" (labs.miniml.ai "Evaluator aware decoding") is automaton structure.
+// same bytes injected by the host (forced tokens), so the evaluator-aware rule
+// that the model never writes the result block itself (labs.miniml.ai
+// "Evaluator aware decoding", "A concrete prototype on llama.cpp") is
+// automaton structure.
 #pragma once
 
 #include <cstdint>

@@ -15,8 +15,8 @@
 //   anyOf / type lists: union
 // CHAR: a well-formed UTF-8 scalar other than '"', '\\' and controls < 0x20,
 // or one escape (\" \\ \/ \b \f \n \r \t \uXXXX), each counting as one
-// character.  Every other keyword fails closed (dev.to "I found a runner
-// bug...": "Unsupported cases fail closed"; whitespace bounded per
+// character.  Every other keyword fails closed, as the compiler of dev.to "I
+// found a runner bug..." refuses what it does not support; whitespace bounded per
 // usetacet.com/docs/grammar "A valid call also has to end" and the pinned
 // compact separators of the dev.to page).
 #include <algorithm>

@@ -1,9 +1,9 @@
 // Bitmask fill: which vocabulary tokens the grammar allows in each row's state
 // (usetacet.com/docs/grammar, "The guarantee").  Masks are cached per mask
-// class (states that allow the same tokens), "the token mask cache makes the
-// surrounding constraints near-free" (labs.miniml.ai "Evaluator aware
-// decoding", "Where XGrammar-2 could take this"); a class is computed the first
-// time a row needs it.
+// class (states that allow the same tokens), which is what keeps grammar
+// constraints cheap (labs.miniml.ai "Evaluator aware decoding", "Where
+// XGrammar-2 could take this", on the token mask cache); a class is computed
+// the first time a row needs it.
 //
 // One CTA per row.  A cache hit copies one W-word row (L2-resident cache).  A
 // miss walks every token's bytes through the transition table in trie

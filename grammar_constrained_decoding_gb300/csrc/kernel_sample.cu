@@ -1,5 +1,5 @@
 // Mask-apply + temperature + softmax + top-p + sampling, one CTA per row
-// ("Sampling runs after masking, so no sampling strategy can escape it",
+// (the sampler sees only masked logits, whatever the sampling strategy:
 // usetacet.com/docs/grammar, "The guarantee").
 //
 // Per row b, over the tokens t the bitmask allows, with x_t the logit:

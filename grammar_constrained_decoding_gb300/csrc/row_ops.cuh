@@ -182,8 +182,8 @@ __device__ __forceinline__ uint8_t state_result_flags(uint8_t sf) {
 }
 
 // Advance one row by its token (labs.miniml.ai "Evaluator aware decoding":
-// after injection the grammar state must be advanced; a forced token's bytes
-// are walked as host-injected symbols).  With token counts, finished or capped
+// the automaton also moves forward over injected tokens; a forced token's
+// bytes are walked as host-injected symbols).  With token counts, finished or capped
 // rows restart from state 0 (usetacet.com/docs/grammar, "A valid call also has
 // to end").  Writes out_states[b], out_flags[b] and counts[b].
 // cols_g (optional) is a copy of grammar g's 512-entry symbol -> column map
@@ -244,9 +244,9 @@ __device__ inline void accept_row(const Tables& t, uint32_t b, uint32_t g, uint3
 }
 
 // Speculative verification of row b's draft toks[0 .. n) (labs.miniml.ai
-// "Evaluator aware decoding", "Where XGrammar-2 could take this": a draft
-// token that closes an evaluated span pins the tokens that follow it, and
-// checking those is exact matching).  Accepts the longest prefix whose tokens
+// "Evaluator aware decoding", "Where XGrammar-2 could take this": once a
+// draft token ends an evaluated span the evaluator's result fixes the tokens
+// after it, so checking them is a comparison of ids).  Accepts the longest prefix whose tokens
 // the grammar allows one after another; a position with forced[j] >= 0 must
 // carry exactly that id and is walked as injected bytes.  Stops at the first
 // refused token (CG_FLAG_DRAFT_CUT, the state stays that of the prefix), after

@@ -211,8 +211,8 @@ int cg_ctx_status(cg_ctx* c, uint32_t* dev_code);
 int cg_ctx_prefill(cg_ctx* c);
 
 /* Step 1 -- which tokens may follow each row's state (usetacet.com/docs/grammar,
- * "The guarantee"; masks come from pure automaton state ahead of the step,
- * labs.miniml.ai "Why isn't this in production APIs yet?").
+ * "The guarantee"; a mask depends on the automaton state alone and is known
+ * before the step, labs.miniml.ai "Why isn't this in production APIs yet?").
  *  d_states  : u32 [B] automaton state of each row (CG_DEAD -> empty mask)
  *  d_gid     : u16 [B] grammar index of each row, or NULL for grammar 0
  *  d_forced  : i32 [B] token the host forces on the row, -1 for none, or NULL;
@@ -316,8 +316,9 @@ int cg_mask_and_sample_noalloc(cg_ctx* c, void* d_logits, int dtype, uint32_t B,
                                const uint32_t* d_bitmask, float temp, float top_p, uint64_t seed,
                                uint32_t step, uint32_t* d_out_tok, float* d_probs, uint32_t flags);
 
-/* Step 3 -- advance each row's automaton by its token ("after injection the
- * grammar state must be advanced", labs.miniml.ai "Evaluator aware decoding").
+/* Step 3 -- advance each row's automaton by its token (labs.miniml.ai "Evaluator
+ * aware decoding", "A concrete prototype on llama.cpp": the automaton also moves
+ * forward over injected tokens).
  *  d_states, d_gid : as in cg_fill_bitmask (d_gid may be NULL)
  *  d_toks          : u32 [B] tokens from cg_mask_and_sample
  *  d_forced        : i32 [B] or NULL; a row with d_forced >= 0 must carry that
@@ -333,9 +334,9 @@ int cg_accept(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const 
               uint32_t* d_out_states, uint8_t* d_out_flags);
 
 /* Speculative verification of drafts against the grammar (labs.miniml.ai
- * "Evaluator aware decoding", "Where XGrammar-2 could take this": a draft token
- * that closes an evaluated span pins the tokens that must follow it, so their
- * verification is exact string matching).  Per row, the longest prefix of the
+ * "Evaluator aware decoding", "Where XGrammar-2 could take this": once a draft
+ * token ends an evaluated span, the evaluator's result fixes the tokens after
+ * it, so checking them is a comparison of ids).  Per row, the longest prefix of the
  * draft whose tokens the grammar allows one after another is accepted, as
  * cg_accept would accept them one per step.
  *  d_states, d_gid : as in cg_accept (d_gid may be NULL)

@@ -2,12 +2,11 @@ r"""Grammar front-ends of the oracle: source text -> regular-expression tree.
 
 Alphabet: 512 symbols.  Symbol b in 0..255 is byte b written by the model;
 symbol 256 + b is byte b injected by the host (a forced token).  Injected
-bytes are a separate alphabet so that "the grammar should not allow the model
-to write its own <result> block, and after injection the grammar state must be
-advanced so the forced tokens are legal" (labs.miniml.ai "Evaluator aware
-decoding", "A concrete prototype on llama.cpp", item 2) is plain automaton
-structure: a state inside a forced region has transitions on injected symbols
-only.
+bytes are a separate alphabet so that two rules of labs.miniml.ai "Evaluator
+aware decoding" ("A concrete prototype on llama.cpp", item 2) -- the model
+never writes the result block itself, and the automaton moves forward over the
+injected result -- are plain automaton structure: a state inside a forced
+region has transitions on injected symbols only.
 
 Tree nodes are tuples:
   ('empty',)            the empty language

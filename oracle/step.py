@@ -8,7 +8,8 @@ one (the token that closes ``</calc>``) but never pass through one.  A row with
 a host-forced token gets a mask holding exactly that token (labs.miniml.ai
 "Evaluator aware decoding", "A concrete prototype on llama.cpp").
 
-Sampler ("Sampling runs after masking", usetacet.com/docs/grammar), per row,
+Sampler (it sees only masked logits: usetacet.com/docs/grammar, "The
+guarantee"), per row,
 in float64 on the exact logit values x:
   * no allowed token -> NO_TOKEN;
   * temperature 0 -> argmax x over allowed tokens, ties to the lowest id;
@@ -205,8 +206,8 @@ def accept_many(dfa: OracleDFA, state: int, draft: list[int], tokens: list[bytes
                 max_tokens: int | None = None) -> DraftResult:
     """Speculative verification of a draft against the grammar
     (labs.miniml.ai "Evaluator aware decoding", "Where XGrammar-2 could take
-    this": a draft token that closes an evaluated span pins the tokens that
-    follow it, whose check is then exact string matching).
+    this": once a draft token ends an evaluated span, the evaluator's result
+    fixes the tokens after it, so checking them is a comparison of ids).
 
     Token j of the draft is accepted when ``accept`` of it from the state left
     by tokens 0..j-1 does not reach DEAD; where ``forced[j] >= 0`` the host has

@@ -292,8 +292,8 @@ def test_integer_lexicon_property():
 
 
 def test_integer_boundary_keeps_minus_drops_quote():
-    # dev.to "I found a runner bug...": at the answer boundary the integer grammar
-    # removes quote and structural-space continuations while leaving minus legal.
+    # dev.to "I found a runner bug...": where the answer starts, an integer-typed
+    # field allows a minus sign but neither a quote nor a space.
     dfa = oracle_dfa("reasoning_answer_1024")
     s = walk(dfa, 0, list(b'{"reasoning":"x","answer":'))
     assert dfa.next[s, ord("-")] >= 0
