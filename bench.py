@@ -38,9 +38,15 @@ SAMPLE_SOURCES = ["grammar_constrained_decoding_gb300/csrc/kernel_sample.cu",
 
 
 def _kernel_hash() -> str:
+    """Hash of the sampling kernel's code (comments and blank lines removed, so
+    that a comment edit keeps a recorded DRAM-traffic figure valid)."""
+    import re
     h = hashlib.sha256()
     for p in SAMPLE_SOURCES:
-        h.update(open(os.path.join(ROOT, p), "rb").read())
+        src = open(os.path.join(ROOT, p), encoding="utf-8").read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update("\n".join(ln.rstrip() for ln in src.splitlines() if ln.strip()).encode())
     return h.hexdigest()[:16]
 
 
