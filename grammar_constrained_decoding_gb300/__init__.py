@@ -251,6 +251,10 @@ class Ctx:
             int(seed), int(step), _ptr(counts), max_tokens, _ptr(h_out_tok), _ptr(out_tok), _ptr(out_states),
             _ptr(out_flags)))
 
+    def self_test_wait_timeout(self) -> None:
+        """Make one bounded device wait run out (the status then reads CG_DEV_TIMEOUT)."""
+        L.check("cg_self_test_wait_timeout", L.lib().cg_self_test_wait_timeout(self._h))
+
     def sync(self) -> None:
         L.check("cg_ctx_sync", L.lib().cg_ctx_sync(self._h))
 

@@ -67,6 +67,7 @@ SIGNATURES = {
                                              C.c_uint32]),
     "cg_mask_classes": (C.c_int, [C.c_void_p, C.c_uint32, C.c_uint32, C.c_void_p, C.c_uint32,
                                   C.POINTER(C.c_uint32), C.POINTER(C.c_uint32)]),
+    "cg_self_test_wait_timeout": (C.c_int, [C.c_void_p]),
     "cg_accept_many": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_uint32,
                                  C.c_uint32, C.c_void_p, C.c_uint32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
     "cg_step_host": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_uint32, C.c_void_p, C.c_int,

@@ -32,6 +32,7 @@ cudaError_t launch_accept_many(const Tables& t, const uint32_t* states, const ui
                                const uint32_t* draft_len, const int32_t* forced, uint32_t B, uint32_t K,
                                uint32_t* counts, uint32_t max_tokens, uint32_t* out_states, uint32_t* out_n,
                                uint8_t* out_flags, uint32_t* path, cudaStream_t stream);
+cudaError_t launch_wait_timeout_self_test(uint32_t* status, cudaStream_t stream);
 }  // namespace cgk
 
 struct cg_ctx {
@@ -458,4 +459,9 @@ int cg_accept_many(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, c
                                  d_out_states, d_out_n, d_out_flags, d_out_path, c->stream) == cudaSuccess
              ? CG_OK
              : CG_E_CUDA;
+}
+
+int cg_self_test_wait_timeout(cg_ctx* c) {
+  if (!c) return CG_E_ARG;
+  return cgk::launch_wait_timeout_self_test(c->t.status, c->stream) == cudaSuccess ? CG_OK : CG_E_CUDA;
 }

@@ -71,7 +71,8 @@ constexpr uint32_t kLongToken = 0xFFu;     // token record length of a token rea
 
 // ---- mbarrier waits and bulk (TMA) copies into shared memory ----------------------
 
-constexpr uint32_t kWaitLimit = 1u << 22;  // polls of a bounded mbarrier wait
+constexpr uint32_t kWaitLimit = 1u << 18;  // polls of a bounded mbarrier wait (about a second: a poll
+                                           // suspends for a few microseconds when the phase is open)
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -116,4 +116,23 @@ cudaError_t launch_accept_many(const Tables& t, const uint32_t* states, const ui
                           out_n, out_flags, path);
 }
 
+// Self-test of the bounded waits every kernel here uses: one block arms a
+// barrier for bytes no copy will deliver, waits with mbar_wait (the same
+// polling limit as the sampling and accept kernels), and records
+// CG_DEV_TIMEOUT when the limit runs out.  Nothing is in flight, so the block
+// simply returns: the context stays usable.
+__global__ void wait_timeout_self_test_kernel(uint32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  mbar_expect_tx(&bar, 16);  // arrives, but the 16 bytes never come: the phase stays open
+  if (!mbar_wait(&bar, 0)) record_error(status, CG_DEV_TIMEOUT);
+}
+
+cudaError_t launch_wait_timeout_self_test(uint32_t* status, cudaStream_t stream) {
+  wait_timeout_self_test_kernel<<<1, 32, 0, stream>>>(status);
+  return cudaGetLastError();
+}
+
 }  // namespace cgk

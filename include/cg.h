@@ -369,6 +369,16 @@ int cg_accept_many(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, c
                    uint32_t max_tokens, uint32_t* d_out_states, uint32_t* d_out_n, uint8_t* d_out_flags,
                    uint32_t* d_out_path);
 
+/* Self-test of the device's failure detection: every wait of the library's
+ * kernels (bulk copies into shared memory, the mask-cache claim) is bounded
+ * and, when its limit runs out, records CG_DEV_TIMEOUT in the status word
+ * and returns instead of hanging.  This call launches one block whose
+ * bounded wait on a barrier that no copy completes runs out; afterwards
+ * cg_ctx_status reports CG_DEV_TIMEOUT and the context stays usable.
+ * Asynchronous on the context stream; the wait polls for well under a second.
+ * Errors: CG_E_ARG, CG_E_CUDA. */
+int cg_self_test_wait_timeout(cg_ctx* c);
+
 /* ---- evaluator-aware host side --------------------------------------------------- */
 
 #define CG_RESULT_CALC_TAG    0  /* <result>V</result> | <result_error>code</result_error> */
