@@ -18,8 +18,9 @@ Tree nodes are tuples:
   ('rep', a, m, n)      m..n copies of a (n None = unbounded)
 
 GBNF-style rule language (one reading of the pages' GBNF grammar, labs.miniml.ai
-"This is a grammar problem"; pushdown nesting is bounded per spec reading,
-usetacet.com/docs/grammar "The guarantee"):
+"This is a grammar problem"; the pages call the automaton a pushdown automaton,
+read here as bounded nesting so that it stays finite, usetacet.com/docs/grammar
+"The guarantee"):
   rule     NAME ::= alt            (a rule starts at every ``NAME ::=``)
   alt      inter ('|' inter)*
   inter    seq ('&' seq)*
