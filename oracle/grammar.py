@@ -30,7 +30,11 @@ read here as bounded nesting so that it stays finite, usetacet.com/docs/grammar
 Escapes in literals and classes: \\ \" \] \[ \- \^ \n \r \t \xHH.  ``#``
 comments run to end of line.  The start rule is ``root``.  References are
 expanded by inlining; a rule may be active at most ``depth_max`` times on the
-expansion stack, and a reference beyond that denotes the empty language.
+expansion stack, and a reference beyond that denotes the empty language.  The
+pushdown reading (``gbnf_to_tree(..., nesting='stack')``) bounds instead the
+number of frames of recursive rules open at once, the stack of the device's
+pushdown automaton; under either bound the language is regular, so the
+derivative construction of oracle.dfa builds its automaton.
 
 JSON-schema subset: see ``schema_to_tree``.
 """
@@ -321,13 +325,65 @@ class _Parser:
         raise GrammarError('syntax', f'unexpected token {k}')
 
 
-def gbnf_to_tree(src: str | bytes, depth_max: int) -> tuple:
+def gbnf_rules(src: str | bytes) -> dict:
+    """Rule name -> rule body (with ('ref', NAME) nodes), as parsed."""
     if isinstance(src, str):
         src = src.encode('utf-8')
     rules = _Parser(_tokenize(src)).rules()
     if 'root' not in rules:
         raise GrammarError('syntax', 'no root rule')
+    return rules
+
+
+def _refs(node, out: set) -> set:
+    if node[0] == 'ref':
+        out.add(node[1])
+    elif node[0] in ('cat', 'alt', 'and'):
+        for c in node[1]:
+            _refs(c, out)
+    elif node[0] in ('rep', 'forced'):
+        _refs(node[1], out)
+    return out
+
+
+def recursive_rules(rules: dict) -> set:
+    """Rules that can reach themselves through references (a rule on a cycle of
+    the reference graph), by a search from each rule."""
+    succ = {name: _refs(body, set()) for name, body in rules.items()}
+    for name, ss in succ.items():
+        for r in ss:
+            if r not in rules:
+                raise GrammarError('undefined_rule', r)
+    out = set()
+    for name in rules:
+        seen, stack = set(), list(succ[name])
+        while stack:
+            r = stack.pop()
+            if r == name:
+                out.add(name)
+                break
+            if r not in seen:
+                seen.add(r)
+                stack.extend(succ[r])
+    return out
+
+
+def gbnf_to_tree(src: str | bytes, depth_max: int, nesting: str = 'per_rule') -> tuple:
+    """Expand the rules from ``root`` into one tree.
+
+    nesting='per_rule': a rule may be active at most ``depth_max`` times on the
+    expansion stack (the bound of every GBNF grammar in the workloads).
+    nesting='stack': the bound of a pushdown automaton whose stack holds at most
+    ``depth_max`` frames -- every reference to a recursive rule (one on a cycle
+    of the reference graph) opens a frame, references to other rules are plain
+    inlining, and a reference that would open frame depth_max + 1 denotes the
+    empty language.  The start rule is the base and opens no frame."""
+    rules = gbnf_rules(src)
+    if nesting not in ('per_rule', 'stack'):
+        raise ValueError(nesting)
+    rec = recursive_rules(rules) if nesting == 'stack' else set()
     active: dict[str, int] = {}
+    frames = [0]
 
     def expand(node):
         kind = node[0]
@@ -335,6 +391,15 @@ def gbnf_to_tree(src: str | bytes, depth_max: int) -> tuple:
             name = node[1]
             if name not in rules:
                 raise GrammarError('undefined_rule', name)
+            if nesting == 'stack':
+                if name not in rec:
+                    return expand(rules[name])
+                if frames[0] >= depth_max:
+                    return EMPTY
+                frames[0] += 1
+                body = expand(rules[name])
+                frames[0] -= 1
+                return body
             if active.get(name, 0) >= depth_max:
                 return EMPTY
             active[name] = active.get(name, 0) + 1
@@ -349,6 +414,8 @@ def gbnf_to_tree(src: str | bytes, depth_max: int) -> tuple:
             return ('rep', expand(node[1]), node[2], node[3])
         return node
 
+    if nesting == 'stack':
+        return expand(rules['root'])
     return expand(('ref', 'root'))
 
 

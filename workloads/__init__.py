@@ -10,6 +10,6 @@ booking-decision schema runs, GSM8K answers), none of which ships here.
 """
 
 from .configs import CONFIGS, Config, get_config  # noqa: F401
-from .grammars import GRAMMARS, GrammarSpec, Bounds  # noqa: F401
+from .grammars import GRAMMARS, PDA_GRAMMARS, GrammarSpec, Bounds  # noqa: F401
 from .vocab import make_vocab, vocab_csr  # noqa: F401
 from .logits import make_logits, make_start_draws  # noqa: F401

@@ -173,6 +173,27 @@ CALC_STRUCTTAG = json.dumps({
 })
 
 
+# Any JSON value without whitespace: strings of printable ASCII other than '"'
+# and '\\' (no escapes), integers.  value, object, member and array lie on a
+# cycle of references, so each reference to them opens a frame of the
+# pushdown automaton: an array costs two frames per level (value, array), an
+# object three (value, object, member).
+JSON_NESTED = r'''
+root ::= value
+value ::= object | array | string | number | "true" | "false" | "null"
+object ::= "{" ( member ( "," member )* )? "}"
+member ::= string ":" value
+array ::= "[" ( value ( "," value )* )? "]"
+string ::= "\"" [ !#-\[\]-~]* "\""
+number ::= "-"? ( "0" | [1-9] [0-9]* )
+'''
+
+# Recursive grammars for the pushdown path: name -> (GBNF source, stack bound).
+PDA_GRAMMARS: dict[str, tuple[str, int]] = {
+    "json_nested": (JSON_NESTED, 32),
+}
+
+
 GRAMMARS: dict[str, GrammarSpec] = {
     "calc_call": GrammarSpec("calc_call", "gbnf", CALC_CALL),
     "booking": GrammarSpec("booking", "json", booking_schema(700)),
