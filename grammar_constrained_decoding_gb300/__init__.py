@@ -259,6 +259,70 @@ class Ctx:
         L.check("cg_ctx_sync", L.lib().cg_ctx_sync(self._h))
 
 
+class PdaGrammar:
+    """A recursive GBNF grammar compiled to a pushdown automaton with a stack
+    bound of ``depth`` frames (cg_pda_compile)."""
+
+    def __init__(self, source: str | bytes, depth: int):
+        data = source.encode("utf-8") if isinstance(source, str) else bytes(source)
+        out = C.c_void_p()
+        L.check("cg_pda_compile", L.lib().cg_pda_compile(data, len(data), int(depth), C.byref(out)))
+        self._h = out
+
+    def __del__(self):
+        if getattr(self, "_h", None) and self._h.value:
+            L.lib().cg_pda_grammar_destroy(self._h)
+            self._h = C.c_void_p()
+
+    def info(self) -> dict:
+        n, r, cols, d = C.c_uint32(), C.c_uint32(), C.c_uint32(), C.c_uint32()
+        L.check("cg_pda_grammar_info", L.lib().cg_pda_grammar_info(self._h, C.byref(n), C.byref(r), C.byref(cols),
+                                                                    C.byref(d)))
+        return {"n_states": n.value, "n_rules": r.value, "n_cols": cols.value, "depth": d.value}
+
+    def try_input(self, data: bytes, injected: np.ndarray | None = None) -> tuple[int, bool, int]:
+        """(bytes walked before the first refused one, complete, stack level)."""
+        n, acc, lvl = C.c_size_t(), C.c_int(), C.c_uint32()
+        inj = None
+        if injected is not None:
+            injected = np.ascontiguousarray(injected, dtype=np.uint8)
+            inj = injected.ctypes.data
+        L.check("cg_pda_try_input", L.lib().cg_pda_try_input(self._h, data, len(data), inj, C.byref(n),
+                                                              C.byref(acc), C.byref(lvl)))
+        return n.value, bool(acc.value), lvl.value
+
+
+class Pda:
+    """Pushdown rows on a context (cg_pda_create).  Row configurations are a
+    u32 tensor [B, depth + 2]: state, stack level, return states."""
+
+    def __init__(self, ctx: Ctx, vocab: Vocab, grammar: PdaGrammar):
+        h = C.c_void_p()
+        L.check("cg_pda_create", L.lib().cg_pda_create(ctx._h, vocab._h, grammar._h, C.byref(h)))
+        self._h = h
+        self._ctx = ctx  # destroyed before its context
+        self.depth = grammar.info()["depth"]
+        self.row_words = self.depth + 2
+
+    def __del__(self):
+        if getattr(self, "_h", None) and self._h.value:
+            L.lib().cg_pda_destroy(self._h)
+            self._h = C.c_void_p()
+
+    def info(self) -> dict:
+        k, m, cb, nc = C.c_uint32(), C.c_uint32(), C.c_uint64(), C.c_uint32()
+        L.check("cg_pda_info", L.lib().cg_pda_info(self._h, C.byref(k), C.byref(m), C.byref(cb), C.byref(nc)))
+        return {"n_keys": k.value, "n_masks": m.value, "cache_bytes": cb.value, "n_candidates": nc.value}
+
+    def fill_bitmask(self, cfg, bitmask, forced=None) -> None:
+        L.check("cg_pda_fill_bitmask", L.lib().cg_pda_fill_bitmask(self._h, _ptr(cfg), cfg.shape[0], _ptr(forced),
+                                                                    _ptr(bitmask)))
+
+    def accept(self, cfg, toks, out_flags, forced=None, counts=None, max_tokens: int = 0) -> None:
+        L.check("cg_pda_accept", L.lib().cg_pda_accept(self._h, _ptr(cfg), cfg.shape[0], _ptr(toks), _ptr(forced),
+                                                        _ptr(counts), int(max_tokens), _ptr(out_flags)))
+
+
 class Driver:
     """Host driver of forced tokens (evaluator-aware grammars)."""
 

@@ -21,6 +21,7 @@ CG_STATE_ACCEPT, CG_STATE_SINK, CG_STATE_FORCED_ONLY = 1, 2, 4
 CG_SAMPLE_INPLACE = 1
 CG_NOALLOC_MAX_ROWS = 64
 CG_RESULT_CALC_TAG, CG_RESULT_JSON_ANSWER, CG_RESULT_STROP_TAG = 0, 1, 2
+CG_PDA_MAX_DEPTH = 64
 
 ERROR_NAMES = {CG_E_ARG: "CG_E_ARG", CG_E_SYNTAX: "CG_E_SYNTAX", CG_E_UNSUPPORTED: "CG_E_UNSUPPORTED",
                CG_E_EMPTY: "CG_E_EMPTY", CG_E_UNDEFINED_RULE: "CG_E_UNDEFINED_RULE", CG_E_LIMIT: "CG_E_LIMIT",
@@ -83,6 +84,19 @@ SIGNATURES = {
                                 C.POINTER(C.c_int)]),
     "cg_eval_arith": (C.c_int, [C.c_char_p, C.c_size_t, C.c_int, C.c_void_p, C.c_size_t, C.POINTER(C.c_size_t),
                                 C.POINTER(C.c_int)]),
+    "cg_pda_compile": (C.c_int, [C.c_char_p, C.c_size_t, C.c_uint32, C.POINTER(C.c_void_p)]),
+    "cg_pda_grammar_destroy": (None, [C.c_void_p]),
+    "cg_pda_grammar_info": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint32), C.POINTER(C.c_uint32),
+                                      C.POINTER(C.c_uint32), C.POINTER(C.c_uint32)]),
+    "cg_pda_try_input": (C.c_int, [C.c_void_p, C.c_char_p, C.c_size_t, C.c_void_p, C.POINTER(C.c_size_t),
+                                   C.POINTER(C.c_int), C.POINTER(C.c_uint32)]),
+    "cg_pda_create": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.POINTER(C.c_void_p)]),
+    "cg_pda_destroy": (None, [C.c_void_p]),
+    "cg_pda_info": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint32), C.POINTER(C.c_uint32), C.POINTER(C.c_uint64),
+                              C.POINTER(C.c_uint32)]),
+    "cg_pda_fill_bitmask": (C.c_int, [C.c_void_p, C.c_void_p, C.c_uint32, C.c_void_p, C.c_void_p]),
+    "cg_pda_accept": (C.c_int, [C.c_void_p, C.c_void_p, C.c_uint32, C.c_void_p, C.c_void_p, C.c_void_p,
+                                C.c_uint32, C.c_void_p]),
     "cg_driver_create": (C.c_int, [C.c_void_p, C.c_uint32, C.c_void_p, C.POINTER(cg_span_rule), C.c_uint32,
                                    C.POINTER(C.c_void_p)]),
     "cg_driver_destroy": (None, [C.c_void_p]),

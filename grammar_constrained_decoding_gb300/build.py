@@ -21,8 +21,8 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libcg.so")
 
 CXX_SOURCES = ["compiler/gbnf.cpp", "compiler/schema.cpp", "compiler/structtag.cpp", "compiler/automaton.cpp",
-               "grammar.cpp", "evaluator.cpp"]
-CU_SOURCES = ["ctx.cu", "kernel_mask.cu", "kernel_sample.cu", "kernel_accept.cu"]
+               "compiler/pda.cpp", "grammar.cpp", "evaluator.cpp"]
+CU_SOURCES = ["ctx.cu", "kernel_mask.cu", "kernel_sample.cu", "kernel_accept.cu", "pda.cu"]
 HEADERS = ["compiler/ir.h", "compiler/json.h", "cg_internal.h", "device.cuh", "row_ops.cuh"]
 GENCODE = "arch=compute_103a,code=sm_103a"
 

@@ -42,7 +42,45 @@ struct cg_driver {
   std::vector<std::deque<uint32_t>> queue;
 };
 
+// Pushdown automaton of a recursive GBNF grammar (compiler/pda.cpp).  States
+// of all rule automata are numbered together, the start rule's first (state 0
+// is the start).  A row's configuration is its state q and a stack of return
+// states of level <= depth.  act[q * n_cols + col_of[symbol]] is the action of
+// a symbol: kPdaNone (no edge: pop when q ends its rule and the stack is not
+// empty, else refuse), a state (shift; allowed when level + h[target] <=
+// depth), or kPdaCall | offset of a call chain in `chain`: chain[o] = n |
+// req << 8, then the n return states to push (outermost first), then the
+// state that consumes the symbol in the innermost rule; allowed when
+// level + req <= depth.
+constexpr uint32_t kPdaNone = 0xFFFFFFFFu;
+constexpr uint32_t kPdaCall = 0x80000000u;
+constexpr uint8_t kPdaInf = 0xFF;  // no completion / no continuation
+
+struct cg_pda_grammar {
+  uint32_t depth = 0;
+  uint32_t n_states = 0;
+  std::vector<std::string> rule_names;  // "root", then the recursive rules
+  std::vector<uint32_t> rule_start;     // start state of each rule automaton
+  std::vector<uint32_t> rule_of;        // [S] rule automaton of each state
+  std::vector<uint8_t> accept;          // [S] the state may end its rule
+  std::vector<uint8_t> h;               // [S] least extra levels needed to end the rule from here
+  std::vector<uint8_t> need_model;      // [S] least headroom of a continuation by a model byte
+  std::vector<uint8_t> need_inj;        // [S] same for an injected byte
+  uint32_t n_cols = 0;
+  std::vector<uint16_t> col_of;         // [512] symbol -> column
+  std::vector<uint32_t> act;            // [S * n_cols]
+  std::vector<uint32_t> chain;
+};
+
 namespace cg {
+// Result of walking one token from state q with an empty stack below it
+// (compiler/pda.cpp): kPdaTokDead (refused whatever the stack), kPdaTokPop
+// (the walk needs the frame below the start: decided per row), or the least
+// headroom depth - level at which the token is allowed.
+constexpr uint32_t kPdaTokDead = 0xFFFFFFFFu;
+constexpr uint32_t kPdaTokPop = 0xFFFFFFFEu;
+uint32_t pda_token_need(const cg_pda_grammar& g, uint32_t q, const uint8_t* bytes, uint32_t n);
+
 // Mask classes over several grammars at once (grammar.cpp): states, of any of
 // the grammars, whose allowed-token sets agree for every token of at most
 // max_len bytes share a class (one cached mask).  States are numbered grammar

@@ -1,7 +1,8 @@
 // Regular expression -> minimal trimmed DFA with canonical numbering.
 //
-//  1. Alphabet classes: the 512 symbols are partitioned so that every symbol
-//     set of the IR is a union of classes.
+//  1. Alphabet classes: the symbols (512, plus call symbols for the pushdown
+//     compiler) are partitioned so that every symbol set of the IR is a union
+//     of classes.
 //  2. Thompson-style NFA over classes.  Bounded repetition x{m,n} is m copies
 //     followed by n-m optional copies, each of which may exit to the end;
 //     x{m,} loops.  An intersection is built as the product of its operands'
@@ -9,8 +10,8 @@
 //  3. Subset construction (epsilon closures keyed by their sorted member list).
 //  4. Trimming: states that cannot reach acceptance are dropped (DEAD).
 //  5. Hopcroft partition refinement on the completed automaton.
-//  6. Canonical numbering: breadth-first from the start state, symbols 0..511
-//     in order.  The minimal trimmed automaton is unique up to renaming, so
+//  6. Canonical numbering: breadth-first from the start state, symbols in
+//     order.  The minimal trimmed automaton is unique up to renaming, so
 //     this numbering is unique.
 #include <algorithm>
 #include <cstring>
@@ -35,15 +36,15 @@ struct VecHash {
   }
 };
 
-// Partition of the 512 symbols induced by the IR's symbol sets.
+// Partition of the alphabet induced by the IR's symbol sets.
 struct Classes {
   int n = 0;
-  std::vector<int> of_symbol;                       // [512]
+  std::vector<int> of_symbol;                       // [n_sym]
   std::vector<std::vector<uint16_t>> members_of_set;  // per distinct set: its classes
   std::unordered_map<int, int> set_index;           // IR node -> distinct set index
 };
 
-Classes make_classes(const IR& ir, int root) {
+Classes make_classes(const IR& ir, int root, int n_sym) {
   std::vector<int> stack = {root};
   std::vector<char> seen(ir.nodes.size(), 0);
   std::vector<int> sym_nodes;
@@ -57,7 +58,7 @@ Classes make_classes(const IR& ir, int root) {
     for (int k : n.kids) stack.push_back(k);
   }
   Classes c;
-  c.of_symbol.assign(kNumSymbols, 0);
+  c.of_symbol.assign(n_sym, 0);
   c.n = 1;
   std::vector<SymSet> distinct;
   for (int x : sym_nodes) {
@@ -71,8 +72,8 @@ Classes make_classes(const IR& ir, int root) {
     // split every class into (inside s) and (outside s)
     std::vector<int> remap_in(c.n, -1), remap_out(c.n, -1);
     int next_id = 0;
-    std::vector<int> fresh(kNumSymbols);
-    for (int a = 0; a < kNumSymbols; ++a) {
+    std::vector<int> fresh(n_sym);
+    for (int a = 0; a < n_sym; ++a) {
       int old = c.of_symbol[a];
       int& slot = s.test(a) ? remap_in[old] : remap_out[old];
       if (slot < 0) slot = next_id++;
@@ -84,7 +85,7 @@ Classes make_classes(const IR& ir, int root) {
   c.members_of_set.resize(distinct.size());
   for (size_t i = 0; i < distinct.size(); ++i) {
     std::vector<char> has(c.n, 0);
-    for (int a = 0; a < kNumSymbols; ++a) if (distinct[i].test(a)) has[c.of_symbol[a]] = 1;
+    for (int a = 0; a < n_sym; ++a) if (distinct[i].test(a)) has[c.of_symbol[a]] = 1;
     for (int k = 0; k < c.n; ++k) if (has[k]) c.members_of_set[i].push_back(uint16_t(k));
   }
   return c;
@@ -475,33 +476,35 @@ ClassDfa Builder::intersection(const std::vector<int>& kids) {
 
 }  // namespace
 
-Dfa build_dfa(IR& ir, int root) {
-  Classes cls = make_classes(ir, root);
+Dfa build_dfa(IR& ir, int root, int n_sym) {
+  if (n_sym < kNumSymbols || n_sym > kMaxSymbols) fail(CG_E_ARG, "alphabet size");
+  Classes cls = make_classes(ir, root, n_sym);
   Builder b(ir, cls);
   ClassDfa d = minimise(trim(b.dfa_of(root)));
   if (d.size() == 0) fail(CG_E_EMPTY, "the grammar accepts no string");
-  // canonical breadth-first numbering over the 512 symbols
+  // canonical breadth-first numbering over the symbols in order
   int C = d.n_cls;
   std::vector<int> canon(d.size(), -1), order;
   canon[d.start] = 0;
   order.push_back(d.start);
   for (size_t q = 0; q < order.size(); ++q) {
     int s = order[q];
-    for (int a = 0; a < kNumSymbols; ++a) {
+    for (int a = 0; a < n_sym; ++a) {
       int t = d.trans[size_t(s) * C + cls.of_symbol[a]];
       if (t >= 0 && canon[t] < 0) { canon[t] = int(order.size()); order.push_back(t); }
     }
   }
   Dfa out;
   out.n_states = uint32_t(order.size());
-  out.next.assign(size_t(out.n_states) * kNumSymbols, -1);
+  out.n_sym = uint32_t(n_sym);
+  out.next.assign(size_t(out.n_states) * n_sym, -1);
   out.accept.assign(out.n_states, 0);
   for (uint32_t i = 0; i < out.n_states; ++i) {
     int s = order[i];
     out.accept[i] = d.acc[s];
-    for (int a = 0; a < kNumSymbols; ++a) {
+    for (int a = 0; a < n_sym; ++a) {
       int t = d.trans[size_t(s) * C + cls.of_symbol[a]];
-      out.next[size_t(i) * kNumSymbols + a] = t < 0 ? -1 : canon[t];
+      out.next[size_t(i) * n_sym + a] = t < 0 ? -1 : canon[t];
     }
   }
   return out;

@@ -315,7 +315,102 @@ class Expander {
   }
 };
 
+// Rules that reach themselves through references (the rules on a cycle of
+// the reference graph), by a search from each rule.
+void collect_refs(const Ast& a, std::vector<std::string>& out) {
+  if (a.k == Ast::Ref) out.push_back(a.text);
+  for (auto& c : a.kids) collect_refs(*c, out);
+}
+
+std::map<std::string, int> recursive_rule_index(const std::map<std::string, AstP>& rules) {
+  std::map<std::string, std::vector<std::string>> succ;
+  for (auto& [name, body] : rules) {
+    collect_refs(*body, succ[name]);
+    for (auto& r : succ[name]) if (!rules.count(r)) fail(CG_E_UNDEFINED_RULE, r);
+  }
+  std::map<std::string, int> index;
+  for (auto& [name, body] : rules) {
+    std::map<std::string, bool> seen;
+    std::vector<std::string> stack = succ[name];
+    bool cyc = false;
+    while (!stack.empty() && !cyc) {
+      std::string r = stack.back();
+      stack.pop_back();
+      if (r == name) cyc = true;
+      else if (!seen[r]) { seen[r] = true; for (auto& x : succ[r]) stack.push_back(x); }
+    }
+    if (cyc) {
+      const int j = int(index.size());
+      index[name] = j;
+    }
+  }
+  if (index.size() > size_t(kNumCallSymbols)) fail(CG_E_LIMIT, "more than 64 recursive rules");
+  return index;
+}
+
+// Lowers one rule body: other rules inline, recursive rule j becomes call
+// symbol 512 + j.  A call inside @forced( ) or under '&' has no meaning for a
+// deterministic pushdown automaton (its bytes would be injected, or matched
+// against another language as a whole) and is refused.
+class CallLowerer {
+ public:
+  CallLowerer(IR& ir, const std::map<std::string, AstP>& rules, const std::map<std::string, int>& rec)
+      : ir_(ir), rules_(rules), rec_(rec) {}
+
+  int lower(const Ast& a, bool in_forced, bool in_and) {
+    switch (a.k) {
+      case Ast::Eps: return ir_.eps();
+      case Ast::Lit: return ir_.literal(a.text);
+      case Ast::Class: return ir_.sym(a.set);
+      case Ast::Ref: {
+        auto r = rec_.find(a.text);
+        if (r != rec_.end()) {
+          if (in_forced || in_and)
+            fail(CG_E_UNSUPPORTED, "recursive rule " + a.text + " referenced inside @forced( ) or '&'");
+          SymSet s;
+          s.set(kNumSymbols + r->second);
+          return ir_.sym(s);
+        }
+        return lower(*rules_.at(a.text), in_forced, in_and);  // acyclic: terminates
+      }
+      case Ast::Forced: return ir_.injected(lower(*a.kids[0], true, in_and));
+      case Ast::Rep: return ir_.rep(lower(*a.kids[0], in_forced, in_and), a.lo, a.hi);
+      case Ast::Cat: case Ast::Alt: case Ast::And: {
+        std::vector<int> k;
+        for (auto& c : a.kids) k.push_back(lower(*c, in_forced, in_and || a.k == Ast::And));
+        if (a.k == Ast::Cat) return ir_.cat(std::move(k));
+        if (a.k == Ast::Alt) return ir_.alt(std::move(k));
+        return ir_.conj(std::move(k));
+      }
+    }
+    return ir_.empty();
+  }
+
+ private:
+  IR& ir_;
+  const std::map<std::string, AstP>& rules_;
+  const std::map<std::string, int>& rec_;
+};
+
 }  // namespace
+
+RuleSystem lower_gbnf_rules(IR& ir, const std::string& src) {
+  Parser p(lex(src));
+  auto rules = p.rules();
+  if (!rules.count("root")) fail(CG_E_SYNTAX, "no root rule");
+  const auto rec = recursive_rule_index(rules);
+  RuleSystem out;
+  out.names.assign(1 + rec.size(), "");
+  out.automata.assign(1 + rec.size(), -1);
+  CallLowerer low(ir, rules, rec);
+  out.names[0] = "root";
+  out.automata[0] = low.lower(*rules.at("root"), false, false);
+  for (auto& [name, j] : rec) {
+    out.names[1 + j] = name;
+    out.automata[1 + j] = low.lower(*rules.at(name), false, false);
+  }
+  return out;
+}
 
 int parse_gbnf(IR& ir, const std::string& src, uint32_t depth_max) {
   Parser p(lex(src));

@@ -13,9 +13,13 @@
 namespace cg {
 
 constexpr int kNumSymbols = 512;
+// The pushdown compiler (pda.cpp) extends the alphabet: symbol 512 + j stands
+// for a reference to recursive rule j inside a rule body (a call).
+constexpr int kNumCallSymbols = 64;
+constexpr int kMaxSymbols = kNumSymbols + kNumCallSymbols;
 
 struct SymSet {
-  uint64_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  uint64_t w[kMaxSymbols / 64] = {};
   void set(int a) { w[a >> 6] |= uint64_t(1) << (a & 63); }
   bool test(int a) const { return (w[a >> 6] >> (a & 63)) & 1; }
   void set_range(int lo, int hi) { for (int a = lo; a <= hi; ++a) set(a); }
@@ -24,11 +28,12 @@ struct SymSet {
     return true;
   }
   bool operator==(const SymSet& o) const {
-    for (int i = 0; i < 8; ++i) if (w[i] != o.w[i]) return false;
+    for (int i = 0; i < kMaxSymbols / 64; ++i) if (w[i] != o.w[i]) return false;
     return true;
   }
   SymSet shifted_to_injected() const {
-    // model bytes move to the injected half; injected bytes stay
+    // model bytes move to the injected half; injected bytes stay (call
+    // symbols never occur inside a forced region)
     SymSet r;
     for (int i = 0; i < 4; ++i) r.w[i + 4] = w[i] | w[i + 4];
     return r;
@@ -95,13 +100,25 @@ int lower_json_schema(IR& ir, const std::string& src, uint32_t ws_max, uint32_t 
 int lower_structural_tag(IR& ir, const std::string& src, uint32_t ws_max, uint32_t max_len_default,
                          uint32_t max_items_default);
 
-// Minimal trimmed DFA over the 512 symbols with canonical breadth-first
-// numbering (automaton.cpp).
+// Minimal trimmed DFA over the first n_sym symbols (512, or more with call
+// symbols) with canonical breadth-first numbering (automaton.cpp).
 struct Dfa {
   uint32_t n_states = 0;
-  std::vector<int32_t> next;   // [n_states * 512], -1 = DEAD
+  uint32_t n_sym = kNumSymbols;
+  std::vector<int32_t> next;   // [n_states * n_sym], -1 = DEAD
   std::vector<uint8_t> accept; // [n_states]
 };
-Dfa build_dfa(IR& ir, int root);
+Dfa build_dfa(IR& ir, int root, int n_sym = kNumSymbols);
+
+// Recursive GBNF rules for the pushdown compiler (gbnf.cpp).  automata[0] is
+// the start rule's body, automata[1 + j] the body of recursive rule j (a rule
+// on a cycle of the reference graph); in every body, references to other
+// rules are inlined and a reference to recursive rule j is call symbol 512 + j.
+struct RuleSystem {
+  std::vector<std::string> names;  // [1 + n_rec]: "root", then the recursive rules
+  std::vector<int> automata;       // IR roots, same order
+  int n_rec() const { return int(names.size()) - 1; }
+};
+RuleSystem lower_gbnf_rules(IR& ir, const std::string& src);
 
 }  // namespace cg

@@ -60,6 +60,10 @@ struct cg_ctx {
   bool cache_complete = false;           // cg_ctx_prefill has filled every class mask (in stream order)
 };
 
+namespace cgk {
+CtxView ctx_view(const cg_ctx* c) { return {c->stream, c->t}; }
+}  // namespace cgk
+
 namespace {
 
 template <typename T>

@@ -66,6 +66,14 @@ struct Tables {
                                // length kLongToken: 32 bytes or more, read through tok_off
 };
 
+// A context's stream and device tables, for the pushdown rows (pda.cu) that
+// run on a context without being part of it (ctx.cu).
+struct CtxView {
+  cudaStream_t stream;
+  Tables t;
+};
+CtxView ctx_view(const cg_ctx* c);
+
 constexpr uint16_t kDead16 = 0xFFFFu;      // CG_DEAD in table16
 constexpr uint32_t kLongToken = 0xFFu;     // token record length of a token read through tok_off
 

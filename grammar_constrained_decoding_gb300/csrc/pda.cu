@@ -1,0 +1,412 @@
+// Pushdown rows on the device (cg_pda_*): each row carries its state and a
+// stack of return states (usetacet.com/docs/grammar, "The guarantee": the
+// automaton that masks the logits is a pushdown automaton).
+//
+// Mask of a row in state q at level L (headroom depth - L):
+//  * the cached part: tokens whose walk from q never pops below the row's own
+//    frame.  Whether such a token is allowed depends only on q and on the
+//    headroom (calls it opens must fit), so the host walks every token once
+//    per state at creation, records the least headroom each needs, and keeps
+//    one mask per (state, headroom up to the largest need), shared where equal;
+//  * the per-row part: tokens whose walk pops below the row's frame (they end
+//    the rule and continue in the caller).  Their fate depends on the stack,
+//    so the fill kernel walks them against the row's own stack, in parallel
+//    over the block's threads, and ORs the allowed ones into the cached mask.
+// Accept walks the sampled token through the actions one thread per row,
+// updating the row's state and stack in place.
+#include <algorithm>
+#include <cstring>
+#include <new>
+#include <unordered_map>
+#include <vector>
+
+#include "cg_internal.h"
+#include "device.cuh"
+
+namespace cgk {
+
+struct DevPda {
+  const uint32_t* act;       // [S * n_cols] actions (kPdaNone, a state, or kPdaCall | chain offset)
+  const uint16_t* colmap;    // [512] symbol -> column
+  const uint32_t* chain;     // call chains: n | req << 8, n return states, target
+  const uint32_t* sinfo;     // [S] bit 0 may end its rule; bits 8..15 h; 16..23 need_model; 24..31 need_inj
+  const uint32_t* key;       // [S] first key << 8 | largest headroom with its own key
+  const uint32_t* mask_of;   // [n_keys] index of the cached mask
+  const uint32_t* masks;     // [n_masks][W]
+  const uint32_t* cand_off;  // [S + 1] per state, the tokens that pop below the row's frame
+  const uint32_t* cand;
+  uint32_t S, n_cols, depth, stride;
+};
+
+// The row's own stack, read and written in place (accept).
+struct RowStack {
+  uint32_t* s;
+  __device__ __forceinline__ uint32_t pop(uint32_t i) { return s[i]; }
+  __device__ __forceinline__ uint32_t get(uint32_t i) const { return s[i]; }
+  __device__ __forceinline__ void put(uint32_t i, uint32_t v) { s[i] = v; }
+};
+
+// A thread's view of a row's stack (fill): entries below `keep` are the
+// row's, shared read-only in shared memory; entries pushed by this thread's
+// walk live in its own array.  keep only falls (to the lowest level popped to).
+struct OverlayStack {
+  const uint32_t* base;
+  uint32_t keep;
+  uint32_t local[CG_PDA_MAX_DEPTH];
+  __device__ __forceinline__ uint32_t pop(uint32_t i) {
+    const uint32_t v = i < keep ? base[i] : local[i];
+    keep = min(keep, i);
+    return v;
+  }
+  __device__ __forceinline__ uint32_t get(uint32_t i) const { return i < keep ? base[i] : local[i]; }
+  __device__ __forceinline__ void put(uint32_t i, uint32_t v) { local[i] = v; }
+};
+
+__device__ __forceinline__ uint32_t pda_h(uint32_t info) { return (info >> 8) & 0xFFu; }
+
+// One symbol (column col) from (q, lvl): pops while q may end its rule and the
+// symbol has no action here, then shifts or runs the call chain.  false: the
+// symbol is refused (no action, nothing to pop, or the headroom is too small).
+template <class Stack>
+__device__ __forceinline__ bool pda_symbol(const DevPda& p, uint32_t col, uint32_t& q, uint32_t& lvl, Stack& st) {
+  for (;;) {  // every pass returns or pops one level
+    const uint32_t a = p.act[size_t(q) * p.n_cols + col];
+    if (a == kPdaNone) {
+      if (!(p.sinfo[q] & 1u) || lvl == 0) return false;
+      --lvl;
+      q = st.pop(lvl);
+      continue;
+    }
+    if (a & kPdaCall) {
+      const uint32_t o = a & ~kPdaCall, head = p.chain[o], n = head & 0xFFu, req = head >> 8;
+      if (lvl + req > p.depth) return false;
+      for (uint32_t i = 0; i < n; ++i) st.put(lvl + i, p.chain[o + 1 + i]);
+      lvl += n;
+      q = p.chain[o + 1 + n];
+      return true;
+    }
+    if (lvl + pda_h(p.sinfo[a]) > p.depth) return false;
+    q = a;
+    return true;
+  }
+}
+
+// Walks token tok's bytes (as injected bytes when sym_off is 256).
+template <class Stack>
+__device__ bool pda_walk(const DevPda& p, const Tables& t, uint32_t tok, uint32_t sym_off, uint32_t& q,
+                         uint32_t& lvl, Stack& st) {
+  const uint16_t* cols = p.colmap + sym_off;
+  const uint4 r0 = t.tok_rec[size_t(tok) * 2];
+  const uint32_t len = r0.x & 0xFFu;
+  if (len != kLongToken) {
+    const uint4 r1 = t.tok_rec[size_t(tok) * 2 + 1];
+    const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+    for (uint32_t k = 0; k < len; ++k) {
+      const uint32_t byte = (w[(k + 1) >> 2] >> (8 * ((k + 1) & 3))) & 0xFFu;
+      if (!pda_symbol(p, cols[byte], q, lvl, st)) return false;
+    }
+    return true;
+  }
+  for (uint32_t i = t.tok_off[tok]; i < t.tok_off[tok + 1]; ++i)
+    if (!pda_symbol(p, cols[t.tok_bytes[i]], q, lvl, st)) return false;
+  return true;
+}
+
+// CG_FLAG_DONE / CG_FLAG_FORCED_NEXT of a configuration: a continuation exists
+// in a frame when its state has one within the frame's headroom; the frame
+// below is reached only through a state that may end its rule.
+template <class Stack>
+__device__ uint8_t pda_flags(const DevPda& p, uint32_t q, uint32_t lvl, const Stack& st) {
+  bool model = false, inj = false, complete = false;
+  uint32_t s = q, l = lvl;
+  for (;;) {  // at most lvl + 1 frames
+    const uint32_t info = p.sinfo[s], hr = p.depth - l;
+    model = model || ((info >> 16) & 0xFFu) <= hr;
+    inj = inj || (info >> 24) <= hr;
+    if (!(info & 1u)) break;
+    if (l == 0) {
+      complete = true;
+      break;
+    }
+    --l;
+    s = st.get(l);
+  }
+  uint8_t fl = 0;
+  if (complete && !model && !inj) fl |= CG_FLAG_DONE;
+  if (!model && inj) fl |= CG_FLAG_FORCED_NEXT;
+  return fl;
+}
+
+constexpr uint32_t kPdaFillThreads = 256;
+
+__global__ void __launch_bounds__(kPdaFillThreads)
+    pda_fill_kernel(DevPda p, Tables t, const uint32_t* __restrict__ cfg, const int32_t* __restrict__ forced,
+                    uint32_t* __restrict__ bitmask) {
+  extern __shared__ uint32_t sm[];  // [W] bits of the per-row tokens, then the row's stack
+  griddep_launch_dependents();
+  griddep_wait();  // configurations come from the previous accept
+  const uint32_t b = blockIdx.x, W = t.W, tid = threadIdx.x;
+  uint32_t* bits = sm;
+  uint32_t* stk = sm + W;
+  const uint32_t* row = cfg + size_t(b) * p.stride;
+  const uint32_t q = row[0], lvl = row[1];
+  const int32_t f = forced ? forced[b] : -1;
+  uint32_t* out = bitmask + size_t(b) * W;
+  const bool ok = q < p.S && lvl <= p.depth;
+  if (f >= 0 || !ok) {
+    // forced row: exactly that token; failed or malformed row: nothing
+    if (tid == 0) {
+      if (f >= 0 && uint32_t(f) >= t.V) record_error(t.status, CG_DEV_BAD_FORCED);
+      else if (f < 0 && q != CG_DEAD) record_error(t.status, CG_DEV_BAD_STATE);
+    }
+    const bool one = f >= 0 && uint32_t(f) < t.V;
+    for (uint32_t w = tid; w < W; w += blockDim.x)
+      out[w] = (one && w == uint32_t(f) >> 5) ? (1u << (uint32_t(f) & 31u)) : 0u;
+    return;
+  }
+  const uint32_t kinfo = p.key[q], hr = p.depth - lvl;
+  const uint32_t* src = p.masks + size_t(p.mask_of[(kinfo >> 8) + min(hr, kinfo & 0xFFu)]) * W;
+  const uint32_t c0 = p.cand_off[q], c1 = p.cand_off[q + 1];
+  if (c0 == c1) {  // nothing decided per row: the cached mask as is
+    if ((W & 3u) == 0) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(src);
+      uint4* o4 = reinterpret_cast<uint4*>(out);
+      for (uint32_t w = tid; w < W / 4; w += blockDim.x) o4[w] = s4[w];
+    } else {
+      for (uint32_t w = tid; w < W; w += blockDim.x) out[w] = src[w];
+    }
+    return;
+  }
+  for (uint32_t w = tid; w < W; w += blockDim.x) bits[w] = 0u;
+  for (uint32_t i = tid; i < lvl; i += blockDim.x) stk[i] = row[2 + i];
+  __syncthreads();
+  for (uint32_t i = c0 + tid; i < c1; i += blockDim.x) {
+    const uint32_t tok = p.cand[i];
+    uint32_t qq = q, ll = lvl;
+    OverlayStack st;
+    st.base = stk;
+    st.keep = lvl;
+    if (pda_walk(p, t, tok, 0u, qq, ll, st)) atomicOr(&bits[tok >> 5], 1u << (tok & 31u));
+  }
+  __syncthreads();
+  for (uint32_t w = tid; w < W; w += blockDim.x) out[w] = src[w] | bits[w];
+}
+
+constexpr uint32_t kPdaAcceptThreads = 128;
+
+__global__ void __launch_bounds__(kPdaAcceptThreads)
+    pda_accept_kernel(DevPda p, Tables t, uint32_t* __restrict__ cfg, uint32_t B, const uint32_t* __restrict__ toks,
+                      const int32_t* __restrict__ forced, uint32_t* counts, uint32_t max_tokens,
+                      uint8_t* __restrict__ out_flags) {
+  griddep_launch_dependents();
+  griddep_wait();  // the tokens come from the sampling kernel
+  const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  uint32_t* row = cfg + size_t(b) * p.stride;
+  uint32_t q = row[0], lvl = row[1];
+  const uint32_t tok = toks[b];
+  const int32_t f = forced ? forced[b] : -1;
+  const uint32_t n0 = counts ? counts[b] : 0u;
+  uint8_t fl = 0;
+  if (tok == CG_NO_TOKEN) {
+    fl = CG_FLAG_NO_TOKEN;
+  } else if (tok >= t.V) {
+    record_error(t.status, CG_DEV_BAD_TOKEN);
+    q = CG_DEAD;
+    fl = CG_FLAG_REJECTED;
+  } else if (q == CG_DEAD) {
+    fl = CG_FLAG_REJECTED;
+  } else if (q >= p.S || lvl > p.depth) {
+    record_error(t.status, CG_DEV_BAD_STATE);
+    q = CG_DEAD;
+    fl = CG_FLAG_REJECTED;
+  } else if (f >= 0 && tok != uint32_t(f)) {
+    record_error(t.status, CG_DEV_FORCED_MISMATCH);
+    q = CG_DEAD;
+    fl = CG_FLAG_REJECTED;
+  } else {
+    RowStack st{row + 2};
+    if (pda_walk(p, t, tok, f >= 0 ? 256u : 0u, q, lvl, st)) {
+      fl = pda_flags(p, q, lvl, st);
+    } else {
+      record_error(t.status, CG_DEV_REJECTED);
+      q = CG_DEAD;
+      fl = CG_FLAG_REJECTED;
+    }
+  }
+  if (q == CG_DEAD) lvl = 0;
+  if (counts) {
+    uint32_t n = n0 + (tok != CG_NO_TOKEN ? 1u : 0u);
+    if ((fl & CG_FLAG_DONE) || n >= max_tokens) {
+      if (!(fl & CG_FLAG_DONE)) fl |= CG_FLAG_CAPPED;
+      q = 0u;
+      lvl = 0u;
+      n = 0u;
+    }
+    counts[b] = n;
+  }
+  row[0] = q;
+  row[1] = lvl;
+  out_flags[b] = fl;
+}
+
+}  // namespace cgk
+
+struct cg_pda {
+  cudaStream_t stream = nullptr;
+  cgk::Tables t{};
+  cgk::DevPda d{};
+  std::vector<void*> allocations;
+  uint32_t n_keys = 0, n_masks = 0, n_cand = 0;
+  uint64_t cache_bytes = 0;
+};
+
+namespace {
+
+void pda_release(cg_pda* p) {
+  for (void* a : p->allocations) cudaFree(a);
+  p->allocations.clear();
+}
+
+template <typename T>
+cudaError_t pda_upload(cg_pda* p, const std::vector<T>& host, const T** dev) {
+  void* d = nullptr;
+  cudaError_t e = cudaMalloc(&d, std::max<size_t>(host.size() * sizeof(T), 16));
+  if (e != cudaSuccess) return e;
+  p->allocations.push_back(d);
+  *dev = static_cast<const T*>(d);
+  if (host.empty()) return cudaSuccess;
+  return cudaMemcpyAsync(d, host.data(), host.size() * sizeof(T), cudaMemcpyHostToDevice, p->stream);
+}
+
+// Distinct masks of W words, by content.
+struct MaskSet {
+  uint32_t W;
+  std::vector<uint32_t> words;
+  std::unordered_multimap<uint64_t, uint32_t> at;
+  uint32_t intern(const std::vector<uint32_t>& m) {
+    uint64_t hsh = 1469598103934665603ull;
+    for (uint32_t x : m) { hsh ^= x; hsh *= 1099511628211ull; }
+    auto range = at.equal_range(hsh);
+    for (auto it = range.first; it != range.second; ++it)
+      if (std::memcmp(words.data() + size_t(it->second) * W, m.data(), size_t(W) * 4) == 0) return it->second;
+    const uint32_t idx = uint32_t(words.size() / W);
+    words.insert(words.end(), m.begin(), m.end());
+    at.emplace(hsh, idx);
+    return idx;
+  }
+};
+
+}  // namespace
+
+extern "C" {
+
+int cg_pda_create(cg_ctx* c, const cg_vocab* v, const cg_pda_grammar* g, cg_pda** out) {
+  if (!c || !v || !g || !out) return CG_E_ARG;
+  *out = nullptr;
+  const cgk::CtxView view = cgk::ctx_view(c);
+  if (v->V != view.t.V) return CG_E_ARG;
+  const uint32_t V = v->V, W = view.t.W, S = g->n_states, D = g->depth;
+  if ((size_t(W) + D) * 4 > 48 * 1024) return CG_E_LIMIT;
+  cg_pda* p = new (std::nothrow) cg_pda;
+  if (!p) return CG_E_NOMEM;
+  p->stream = view.stream;
+  p->t = view.t;
+  std::vector<uint32_t> sinfo(S), key(S), mask_of, cand_off(S + 1, 0), cand;
+  MaskSet ms{W, {}, {}};
+  try {
+    std::vector<uint32_t> need(V);
+    std::vector<uint32_t> m(W);
+    std::vector<std::vector<uint32_t>> by_need;
+    for (uint32_t q = 0; q < S; ++q) {
+      sinfo[q] = uint32_t(g->accept[q] ? 1u : 0u) | (uint32_t(g->h[q]) << 8) | (uint32_t(g->need_model[q]) << 16) |
+                 (uint32_t(g->need_inj[q]) << 24);
+      uint32_t cap = 0;
+      for (uint32_t tk = 0; tk < V; ++tk) {
+        const uint32_t r = cg::pda_token_need(*g, q, v->bytes.data() + v->off[tk], v->off[tk + 1] - v->off[tk]);
+        need[tk] = r;
+        if (r == cg::kPdaTokPop) cand.push_back(tk);
+        else if (r != cg::kPdaTokDead) cap = std::max(cap, std::min(r, D));
+      }
+      cand_off[q + 1] = uint32_t(cand.size());
+      // one key per headroom 0..cap (a larger headroom reads key cap)
+      by_need.assign(cap + 1, {});
+      for (uint32_t tk = 0; tk < V; ++tk)
+        if (need[tk] <= cap) by_need[need[tk]].push_back(tk);
+      if (mask_of.size() >= (1u << 24)) { delete p; return CG_E_LIMIT; }
+      key[q] = (uint32_t(mask_of.size()) << 8) | cap;
+      std::fill(m.begin(), m.end(), 0u);
+      for (uint32_t hr = 0; hr <= cap; ++hr) {
+        for (uint32_t tk : by_need[hr]) m[tk >> 5] |= 1u << (tk & 31u);
+        mask_of.push_back(ms.intern(m));
+      }
+    }
+  } catch (const std::bad_alloc&) {
+    delete p;
+    return CG_E_NOMEM;
+  }
+  p->n_keys = uint32_t(mask_of.size());
+  p->n_masks = uint32_t(ms.words.size() / W);
+  p->n_cand = uint32_t(cand.size());
+  p->cache_bytes = uint64_t(ms.words.size()) * 4;
+  cgk::DevPda& d = p->d;
+  cudaError_t e;
+  if ((e = pda_upload(p, g->act, &d.act)) != cudaSuccess || (e = pda_upload(p, g->col_of, &d.colmap)) != cudaSuccess ||
+      (e = pda_upload(p, g->chain, &d.chain)) != cudaSuccess || (e = pda_upload(p, sinfo, &d.sinfo)) != cudaSuccess ||
+      (e = pda_upload(p, key, &d.key)) != cudaSuccess || (e = pda_upload(p, mask_of, &d.mask_of)) != cudaSuccess ||
+      (e = pda_upload(p, ms.words, &d.masks)) != cudaSuccess ||
+      (e = pda_upload(p, cand_off, &d.cand_off)) != cudaSuccess || (e = pda_upload(p, cand, &d.cand)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(p->stream)) != cudaSuccess) {
+    pda_release(p);
+    delete p;
+    return CG_E_CUDA;
+  }
+  d.S = S;
+  d.n_cols = g->n_cols;
+  d.depth = D;
+  d.stride = D + 2;
+  *out = p;
+  return CG_OK;
+}
+
+void cg_pda_destroy(cg_pda* p) {
+  if (!p) return;
+  cudaStreamSynchronize(p->stream);
+  pda_release(p);
+  delete p;
+}
+
+int cg_pda_info(const cg_pda* p, uint32_t* n_keys, uint32_t* n_masks, uint64_t* cache_bytes,
+                uint32_t* n_candidates) {
+  if (!p) return CG_E_ARG;
+  if (n_keys) *n_keys = p->n_keys;
+  if (n_masks) *n_masks = p->n_masks;
+  if (cache_bytes) *cache_bytes = p->cache_bytes;
+  if (n_candidates) *n_candidates = p->n_cand;
+  return CG_OK;
+}
+
+int cg_pda_fill_bitmask(cg_pda* p, const uint32_t* d_cfg, uint32_t B, const int32_t* d_forced,
+                        uint32_t* d_bitmask) {
+  if (!p || (B && (!d_cfg || !d_bitmask))) return CG_E_ARG;
+  if (B == 0) return CG_OK;
+  const size_t smem = (size_t(p->t.W) + p->d.depth) * 4;
+  return cgk::launch_dependent(cgk::pda_fill_kernel, dim3(B), dim3(cgk::kPdaFillThreads), smem, p->stream, p->d,
+                               p->t, d_cfg, d_forced, d_bitmask) == cudaSuccess
+             ? CG_OK
+             : CG_E_CUDA;
+}
+
+int cg_pda_accept(cg_pda* p, uint32_t* d_cfg, uint32_t B, const uint32_t* d_toks, const int32_t* d_forced,
+                  uint32_t* d_counts, uint32_t max_tokens, uint8_t* d_out_flags) {
+  if (!p || (B && (!d_cfg || !d_toks || !d_out_flags))) return CG_E_ARG;
+  if (B == 0) return CG_OK;
+  const uint32_t grid = (B + cgk::kPdaAcceptThreads - 1) / cgk::kPdaAcceptThreads;
+  return cgk::launch_dependent(cgk::pda_accept_kernel, dim3(grid), dim3(cgk::kPdaAcceptThreads), 0, p->stream,
+                               p->d, p->t, d_cfg, B, d_toks, d_forced, d_counts, max_tokens, d_out_flags) ==
+                 cudaSuccess
+             ? CG_OK
+             : CG_E_CUDA;
+}
+
+}  // extern "C"

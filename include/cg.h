@@ -379,6 +379,87 @@ int cg_accept_many(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, c
  * Errors: CG_E_ARG, CG_E_CUDA. */
 int cg_self_test_wait_timeout(cg_ctx* c);
 
+/* ---- pushdown automaton for recursive grammars ---------------------------------- */
+
+/* usetacet.com/docs/grammar, "The guarantee": the automaton that masks the
+ * logits is a pushdown automaton.  cg_compile flattens nesting into a DFA
+ * (each rule active at most depth_max times), whose size grows with the
+ * bound; these calls keep one automaton per recursive rule and a stack per
+ * row instead.
+ *
+ * Language: GBNF as in cg_compile.  Every reference to a recursive rule (one
+ * on a cycle of references) opens a frame; other rules are inlined; the start
+ * rule is the base frame and opens none.  At most `depth` frames are open at
+ * once; a reference past that matches nothing.  Prefixes that can no longer
+ * be completed within the bound are refused.
+ *
+ * Grammar class (CG_E_UNSUPPORTED otherwise): deterministic with one symbol
+ * of lookahead -- in every state the bytes that continue the rule and the
+ * first bytes of each rule it may call are disjoint; no recursive rule
+ * matches the empty string or calls itself before its first byte; where a
+ * state may end its rule, none of the bytes it consumes can follow the rule.
+ * Recursive rules may not be referenced inside @forced( ) or under '&'.
+ *
+ * Row configuration, u32 [B][depth + 2] on the device, updated in place by
+ * cg_pda_accept: word 0 the state (CG_DEAD for a failed row), word 1 the stack
+ * level L (0..depth), words 2..2+L-1 the return states bottom to top (words
+ * past L are unused).  A fresh row is {0, 0}. */
+#define CG_PDA_MAX_DEPTH 64
+
+typedef struct cg_pda_grammar cg_pda_grammar;
+typedef struct cg_pda cg_pda;
+
+/* Compile a recursive GBNF grammar with a stack bound depth <= CG_PDA_MAX_DEPTH.
+ * Errors: CG_E_ARG, CG_E_SYNTAX, CG_E_UNDEFINED_RULE, CG_E_UNSUPPORTED (the
+ * grammar class above), CG_E_EMPTY, CG_E_LIMIT (more than 64 recursive rules
+ * or 2^24 states), CG_E_NOMEM. */
+int cg_pda_compile(const char* src, size_t src_len, uint32_t depth, cg_pda_grammar** out);
+void cg_pda_grammar_destroy(cg_pda_grammar* g);
+
+/* Sizes: states of all rule automata, rules (the start rule and the recursive
+ * ones), transition columns, stack bound.  Any output may be NULL. */
+int cg_pda_grammar_info(const cg_pda_grammar* g, uint32_t* n_states, uint32_t* n_rules, uint32_t* n_cols,
+                        uint32_t* depth);
+
+/* Walk bytes s[0..n) from a fresh row (injected[i] != 0: byte i is host-injected;
+ * injected may be NULL).  consumed receives the number of bytes walked before
+ * the first refused one (n when none is refused), accepted 1 when all were
+ * walked and the text may end there, level (optional) the stack level after
+ * the walk.  Host only. */
+int cg_pda_try_input(const cg_pda_grammar* g, const uint8_t* s, size_t n, const uint8_t* injected,
+                     size_t* consumed, int* accepted, uint32_t* level);
+
+/* Device pushdown object on context c, for the vocabulary v the context was
+ * created with (same V).  Precomputes, per state and stack headroom, the mask
+ * of the tokens whose walk never pops below the row's level (one cached mask
+ * per distinct set), and per state the list of tokens that do (decided per row
+ * against its stack).  Uses c's stream and status word; destroy it before c.
+ * Errors: CG_E_ARG, CG_E_CUDA, CG_E_NOMEM. */
+int cg_pda_create(cg_ctx* c, const cg_vocab* v, const cg_pda_grammar* g, cg_pda** out);
+void cg_pda_destroy(cg_pda* p);
+
+/* Sizes of the precomputation: (state, headroom) keys, distinct cached masks,
+ * their bytes, tokens on the per-state lists.  Any output may be NULL. */
+int cg_pda_info(const cg_pda* p, uint32_t* n_keys, uint32_t* n_masks, uint64_t* cache_bytes,
+                uint32_t* n_candidates);
+
+/* Step 1 for pushdown rows: d_cfg u32 [B][depth + 2] as above; d_forced as in
+ * cg_fill_bitmask (NULL for none); d_bitmask u32 [B][W].  A failed row gets an
+ * empty mask; a row whose state or level is out of range records
+ * CG_DEV_BAD_STATE and gets an empty mask.  Sampling is cg_mask_and_sample on
+ * the same context. */
+int cg_pda_fill_bitmask(cg_pda* p, const uint32_t* d_cfg, uint32_t B, const int32_t* d_forced,
+                        uint32_t* d_bitmask);
+
+/* Step 3 for pushdown rows: advance each row's configuration in place by its
+ * token (as injected bytes where d_forced >= 0, which must match the token).
+ * d_counts / max_tokens and the flags as in cg_accept: CG_FLAG_DONE when the
+ * text is complete and nothing may follow, CG_FLAG_FORCED_NEXT when only
+ * injected bytes may follow; a finished or capped row restarts at {0, 0} when
+ * counts are kept. */
+int cg_pda_accept(cg_pda* p, uint32_t* d_cfg, uint32_t B, const uint32_t* d_toks, const int32_t* d_forced,
+                  uint32_t* d_counts, uint32_t max_tokens, uint8_t* d_out_flags);
+
 /* ---- evaluator-aware host side --------------------------------------------------- */
 
 #define CG_RESULT_CALC_TAG    0  /* <result>V</result> | <result_error>code</result_error> */
