@@ -145,7 +145,8 @@ def run_ours(args) -> dict | None:
     toks = make_vocab(cfg.vocab_kind, V, cfg.vocab_seed)
     stream = torch.cuda.Stream()      # graphs are captured on a side stream
     torch.cuda.set_stream(stream)
-    ctx = cg.Ctx(grammars, cg.Vocab(toks), stream)
+    vocab = cg.Vocab(toks)
+    ctx = cg.Ctx(grammars, vocab, stream)
     ctx.prefill()   # every mask class computed once, outside the timed steps
     dtype = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
     esz = 2 if cfg.dtype == "bf16" else 4
@@ -289,6 +290,11 @@ def run_ours(args) -> dict | None:
     if ctx.status() != 0:
         raise RuntimeError("device status after accept_many")
 
+    # pushdown rows (cg_pda_*): the recursive JSON grammar with a stack of 32
+    # frames on the same vocabulary, rows and logits, as the three calls
+    # fill (pushdown) -> mask_and_sample -> accept (pushdown), in graphs
+    pda_out = _bench_pushdown(args, cg, ctx, vocab, stream, bufs, R, B, V, W, cfg, seed)
+
     # host evaluators of the forced-token path, per call through the C ABI
     # (Python's call overhead included) on the pages' examples
     host_eval = {}
@@ -360,6 +366,7 @@ def run_ours(args) -> dict | None:
                       "step as three calls (fill_bitmask, mask_and_sample, accept)": round(three_ms * 1e3, 3),
                       "accept_many (B rows, drafts of 8 tokens from the next 8 steps)": round(am_us, 3)},
         "accept_many_mean_accepted": round(am_accepted, 3),
+        "pushdown": pda_out,
         "host_eval_us_per_call": host_eval,
         "roofline": {"kernel": "stream_topp_kernel<true> (cg_step)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -372,6 +379,93 @@ def run_ours(args) -> dict | None:
         "clocks": clocks,
     }
     return out
+
+
+def _bench_pushdown(args, cg, ctx, vocab, stream, bufs, R, B, V, W, cfg, seed) -> dict:
+    """The pushdown path on json_nested (stack bound 32): per-step time of
+    the three calls, and each kernel launched alone back to back."""
+    import torch
+    from workloads import PDA_GRAMMARS
+
+    source, depth = PDA_GRAMMARS["json_nested"]
+    pg = cg.PdaGrammar(source, depth)
+    pda = cg.Pda(ctx, vocab, pg)
+    cfg_rows = torch.zeros((B, depth + 2), dtype=torch.int32, device="cuda").view(torch.uint32)
+    counts = torch.zeros(B, dtype=torch.int32, device="cuda").view(torch.uint32)
+    bm = torch.empty((B, W), dtype=torch.int32, device="cuda")
+    tok = torch.empty(B, dtype=torch.int32, device="cuda")
+    tok_u = tok.view(torch.uint32)
+    flags = torch.empty(B, dtype=torch.uint8, device="cuda")
+
+    def pstep(i, logits):
+        pda.fill_bitmask(cfg_rows, bm)
+        ctx.mask_and_sample(logits, bm, cfg.temp, cfg.top_p, seed, i, tok)
+        pda.accept(cfg_rows, tok_u, flags, counts=counts, max_tokens=2048)
+
+    base = 3 * 10**6
+    for i in range(max(args.warmup, 3)):
+        pstep(base + i, bufs[i % R])
+    n = min(args.steps, 250)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+        for i in range(n):
+            pstep(base + 100 + i, bufs[i % R])
+    g.replay()   # upload, and rows move past the first steps
+    torch.cuda.synchronize()
+    if ctx.status() != 0:
+        raise RuntimeError("device status after the pushdown warm-up")
+
+    def timed(fn, reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps * 1e3
+
+    step_us = timed(g.replay, 1) / n
+    levels = cfg_rows.view(torch.int32)[:, 1].float()
+    mean_level, max_level = float(levels.mean().item()), int(levels.max().item())
+    fill_us = timed(lambda: pda.fill_bitmask(cfg_rows, bm), 200)
+    sample_us = timed(lambda: ctx.mask_and_sample(bufs[0], bm, cfg.temp, cfg.top_p, seed, 7, tok), 200)
+    # accept alone: the rows are put back before every call (a copy of the
+    # configurations and counts), and the copies alone are timed apart
+    snap, csnap = cfg_rows.clone(), counts.clone()
+
+    def restore():
+        cfg_rows.copy_(snap)
+        counts.copy_(csnap)
+
+    def restore_accept():
+        restore()
+        pda.accept(cfg_rows, tok_u, flags, counts=counts, max_tokens=2048)
+
+    accept_us = timed(restore_accept, 200) - timed(restore, 200)
+    if ctx.status() != 0:
+        raise RuntimeError("device status after the pushdown steps")
+    info, ginfo = pda.info(), pg.info()
+    peaks = _peaks()
+    fill_bytes = B * 8 * W   # the cached mask read and the bitmask written, per row
+    achieved = fill_bytes / (fill_us * 1e-6) / 1e9
+    return {
+        "workload": f"json_nested: recursive JSON grammar, stack bound {depth} frames, V={V}, B={B}, "
+                    f"{cfg.dtype} logits as the main workload, T={cfg.temp}, top_p={cfg.top_p}",
+        "automaton": {"states": ginfo["n_states"], "rules": ginfo["n_rules"], "columns": ginfo["n_cols"],
+                      "cached_masks": info["n_masks"], "keys": info["n_keys"],
+                      "cache_bytes": info["cache_bytes"], "per_row_tokens": info["n_candidates"]},
+        "step_us": round(step_us, 3),
+        "tokens_per_s": round(B / (step_us * 1e-6), 1),
+        "steps": n,
+        "fill_us_alone": round(fill_us, 3),
+        "sample_us_alone": round(sample_us, 3),
+        "accept_us_alone": round(accept_us, 3),
+        "stack_level_after": {"mean": round(mean_level, 2), "max": max_level},
+        "fill_roofline": {"kernel": "pda_fill_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                          "algorithmic_bytes_per_launch": fill_bytes},
+    }
 
 
 class OracleBench:

@@ -70,13 +70,15 @@ struct cg_pda_grammar {
   std::vector<uint16_t> col_of;         // [512] symbol -> column
   std::vector<uint32_t> act;            // [S * n_cols]
   std::vector<uint32_t> chain;
+  std::vector<std::vector<uint32_t>> returns_of;  // per rule: the return states its callers push
 };
 
 namespace cg {
-// Result of walking one token from state q with an empty stack below it
+// Result of walking one token from state q with an unknown stack below it
 // (compiler/pda.cpp): kPdaTokDead (refused whatever the stack), kPdaTokPop
-// (the walk needs the frame below the start: decided per row), or the least
-// headroom depth - level at which the token is allowed.
+// (the walk pops below the start and survives under at least one stack the
+// grammar can build: decided per row), or the least headroom depth - level at
+// which the token is allowed.
 constexpr uint32_t kPdaTokDead = 0xFFFFFFFFu;
 constexpr uint32_t kPdaTokPop = 0xFFFFFFFEu;
 uint32_t pda_token_need(const cg_pda_grammar& g, uint32_t q, const uint8_t* bytes, uint32_t n);

@@ -279,6 +279,13 @@ cg_pda_grammar* compile(const std::string& src, uint32_t depth) {
     g->col_of[c] = it->second;
   }
   g->n_cols = uint32_t(cols.size());
+  g->returns_of.assign(R, {});
+  for (uint32_t q = 0; q < S; ++q)
+    for (int j = 0; j < K; ++j) {
+      const int32_t r = call[size_t(q) * K + j];
+      auto& v = g->returns_of[1 + j];
+      if (r >= 0 && std::find(v.begin(), v.end(), uint32_t(r)) == v.end()) v.push_back(uint32_t(r));
+    }
   g->act.assign(size_t(S) * g->n_cols, kPdaNone);
   for (uint32_t k = 0; k < g->n_cols; ++k)
     for (uint32_t q = 0; q < S; ++q) g->act[size_t(q) * g->n_cols + k] = cols[k][q];
@@ -323,11 +330,43 @@ uint32_t step_symbol(const cg_pda_grammar& g, uint32_t& cur, std::vector<uint32_
 
 }  // namespace
 
+namespace {
+// Can bytes[i..n) be walked from state q, its frame's caller being any of
+// the return states the grammar pushes below q's rule (and so on below),
+// with no bound on the stack?  `hops` counts pops taken at byte i without
+// consuming it: more than the number of states means a cycle of pops.
+bool survives_some_stack(const cg_pda_grammar& g, uint32_t q, const uint8_t* bytes, uint32_t i, uint32_t n,
+                         uint32_t hops) {
+  std::vector<uint32_t> st;
+  uint32_t need = 0;
+  for (; i < n; ++i, hops = 0) {
+    const uint32_t r = step_symbol(g, q, st, bytes[i], -1, need);
+    if (r == kPdaTokDead) return false;
+    if (r == kPdaTokPop) {
+      const uint32_t rule = g.rule_of[q];
+      if (rule == 0 || hops > g.n_states) return false;
+      for (uint32_t ret : g.returns_of[rule])
+        if (survives_some_stack(g, ret, bytes, i, n, hops + 1)) return true;
+      return false;
+    }
+  }
+  return true;
+}
+}  // namespace
+
 uint32_t pda_token_need(const cg_pda_grammar& g, uint32_t q, const uint8_t* bytes, uint32_t n) {
   std::vector<uint32_t> st;
   uint32_t cur = q, need = 0;
   for (uint32_t i = 0; i < n; ++i) {
     const uint32_t r = step_symbol(g, cur, st, bytes[i], -1, need);
+    if (r == kPdaTokPop) {
+      // the start rule is the base frame: nothing lies below it
+      const uint32_t rule = g.rule_of[cur];
+      if (rule == 0) return kPdaTokDead;
+      for (uint32_t ret : g.returns_of[rule])
+        if (survives_some_stack(g, ret, bytes, i, n, 1)) return kPdaTokPop;
+      return kPdaTokDead;
+    }
     if (r) return r;
   }
   return need;
