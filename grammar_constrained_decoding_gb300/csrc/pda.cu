@@ -26,10 +26,15 @@
 namespace cgk {
 
 struct DevPda {
-  const uint32_t* act;       // [S * n_cols] actions (kPdaNone, a state, or kPdaCall | chain offset)
+  // the walk tables, one 16-byte aligned block (`tabs`, tab_n16 uint4s):
+  // colmap at offset 0, then sinfo, act and chain at their byte offsets
   const uint16_t* colmap;    // [512] symbol -> column
-  const uint32_t* chain;     // call chains: n | req << 8, n return states, target
   const uint32_t* sinfo;     // [S] bit 0 may end its rule; bits 8..15 h; 16..23 need_model; 24..31 need_inj
+  const uint32_t* act;       // [S * n_cols] actions (kPdaNone, a state, or kPdaCall | chain offset)
+  const uint32_t* chain;     // call chains: n | req << 8, n return states, target
+  const uint4* tabs;
+  uint32_t tab_n16, off_sinfo, off_act, off_chain;
+  bool tabs_in_smem;         // small enough to copy into each block's shared memory
   const uint32_t* key;       // [S] first key << 8 | largest headroom with its own key
   const uint32_t* mask_of;   // [n_keys] index of the cached mask
   const uint32_t* masks;     // [n_masks][W]
@@ -37,6 +42,21 @@ struct DevPda {
   const uint32_t* cand;
   uint32_t S, n_cols, depth, stride;
 };
+
+constexpr uint32_t kPdaSmemTables = 32 * 1024;  // walk tables up to this size live in shared memory
+
+// Copies the walk tables into shared memory `sm` (all threads of the block
+// take part; the caller synchronises) and returns a view reading them there.
+__device__ __forceinline__ DevPda tables_to_smem(const DevPda& p, uint4* sm, uint32_t tid, uint32_t nthreads) {
+  for (uint32_t i = tid; i < p.tab_n16; i += nthreads) sm[i] = p.tabs[i];
+  DevPda v = p;
+  const unsigned char* base = reinterpret_cast<const unsigned char*>(sm);
+  v.colmap = reinterpret_cast<const uint16_t*>(base);
+  v.sinfo = reinterpret_cast<const uint32_t*>(base + p.off_sinfo);
+  v.act = reinterpret_cast<const uint32_t*>(base + p.off_act);
+  v.chain = reinterpret_cast<const uint32_t*>(base + p.off_chain);
+  return v;
+}
 
 // The row's own stack, read and written in place (accept).
 struct RowStack {
@@ -142,12 +162,13 @@ constexpr uint32_t kPdaFillThreads = 256;
 __global__ void __launch_bounds__(kPdaFillThreads)
     pda_fill_kernel(DevPda p, Tables t, const uint32_t* __restrict__ cfg, const int32_t* __restrict__ forced,
                     uint32_t* __restrict__ bitmask) {
-  extern __shared__ uint32_t sm[];  // [W] bits of the per-row tokens, then the row's stack
+  // [tables (when they fit)] [W bits of the per-row tokens] [the row's stack]
+  extern __shared__ __align__(16) uint4 sm4[];
   griddep_launch_dependents();
   griddep_wait();  // configurations come from the previous accept
   const uint32_t b = blockIdx.x, W = t.W, tid = threadIdx.x;
-  uint32_t* bits = sm;
-  uint32_t* stk = sm + W;
+  uint32_t* bits = reinterpret_cast<uint32_t*>(sm4 + (p.tabs_in_smem ? p.tab_n16 : 0u));
+  uint32_t* stk = bits + W;
   const uint32_t* row = cfg + size_t(b) * p.stride;
   const uint32_t q = row[0], lvl = row[1];
   const int32_t f = forced ? forced[b] : -1;
@@ -177,6 +198,7 @@ __global__ void __launch_bounds__(kPdaFillThreads)
     }
     return;
   }
+  const DevPda pv = p.tabs_in_smem ? tables_to_smem(p, sm4, tid, blockDim.x) : p;
   for (uint32_t w = tid; w < W; w += blockDim.x) bits[w] = 0u;
   for (uint32_t i = tid; i < lvl; i += blockDim.x) stk[i] = row[2 + i];
   __syncthreads();
@@ -186,7 +208,7 @@ __global__ void __launch_bounds__(kPdaFillThreads)
     OverlayStack st;
     st.base = stk;
     st.keep = lvl;
-    if (pda_walk(p, t, tok, 0u, qq, ll, st)) atomicOr(&bits[tok >> 5], 1u << (tok & 31u));
+    if (pda_walk(pv, t, tok, 0u, qq, ll, st)) atomicOr(&bits[tok >> 5], 1u << (tok & 31u));
   }
   __syncthreads();
   for (uint32_t w = tid; w < W; w += blockDim.x) out[w] = src[w] | bits[w];
@@ -198,7 +220,10 @@ __global__ void __launch_bounds__(kPdaAcceptThreads)
     pda_accept_kernel(DevPda p, Tables t, uint32_t* __restrict__ cfg, uint32_t B, const uint32_t* __restrict__ toks,
                       const int32_t* __restrict__ forced, uint32_t* counts, uint32_t max_tokens,
                       uint8_t* __restrict__ out_flags) {
+  extern __shared__ __align__(16) uint4 sm4[];  // the walk tables, when they fit
   griddep_launch_dependents();
+  const DevPda pv = p.tabs_in_smem ? tables_to_smem(p, sm4, threadIdx.x, blockDim.x) : p;
+  if (p.tabs_in_smem) __syncthreads();
   griddep_wait();  // the tokens come from the sampling kernel
   const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
@@ -226,8 +251,8 @@ __global__ void __launch_bounds__(kPdaAcceptThreads)
     fl = CG_FLAG_REJECTED;
   } else {
     RowStack st{row + 2};
-    if (pda_walk(p, t, tok, f >= 0 ? 256u : 0u, q, lvl, st)) {
-      fl = pda_flags(p, q, lvl, st);
+    if (pda_walk(pv, t, tok, f >= 0 ? 256u : 0u, q, lvl, st)) {
+      fl = pda_flags(pv, q, lvl, st);
     } else {
       record_error(t.status, CG_DEV_REJECTED);
       q = CG_DEAD;
@@ -261,7 +286,16 @@ struct cg_pda {
   uint64_t cache_bytes = 0;
 };
 
+namespace cgk {
+cudaError_t allow_smem(const void* kernel, size_t bytes);  // kernel_sample.cu
+}
+
 namespace {
+
+size_t pda_fill_smem(const cgk::DevPda& d, uint32_t W) {
+  return (d.tabs_in_smem ? size_t(d.tab_n16) * 16 : 0) + (size_t(W) + d.depth) * 4;
+}
+size_t pda_accept_smem(const cgk::DevPda& d) { return d.tabs_in_smem ? size_t(d.tab_n16) * 16 : 0; }
 
 void pda_release(cg_pda* p) {
   for (void* a : p->allocations) cudaFree(a);
@@ -307,7 +341,7 @@ int cg_pda_create(cg_ctx* c, const cg_vocab* v, const cg_pda_grammar* g, cg_pda*
   const cgk::CtxView view = cgk::ctx_view(c);
   if (v->V != view.t.V) return CG_E_ARG;
   const uint32_t V = v->V, W = view.t.W, S = g->n_states, D = g->depth;
-  if ((size_t(W) + D) * 4 > 48 * 1024) return CG_E_LIMIT;
+  if ((size_t(W) + D) * 4 + cgk::kPdaSmemTables > 200 * 1024) return CG_E_LIMIT;
   cg_pda* p = new (std::nothrow) cg_pda;
   if (!p) return CG_E_NOMEM;
   p->stream = view.stream;
@@ -350,9 +384,29 @@ int cg_pda_create(cg_ctx* c, const cg_vocab* v, const cg_pda_grammar* g, cg_pda*
   p->n_cand = uint32_t(cand.size());
   p->cache_bytes = uint64_t(ms.words.size()) * 4;
   cgk::DevPda& d = p->d;
+  // the walk tables in one block: colmap, sinfo, act, chain, each 16-byte aligned
+  std::vector<uint4> tabs;
+  uint32_t off_sinfo = 0, off_act = 0, off_chain = 0;
+  try {
+    std::vector<unsigned char> blob;
+    auto put = [&blob](const void* src, size_t bytes) {
+      const uint32_t off = uint32_t(blob.size());
+      blob.insert(blob.end(), static_cast<const unsigned char*>(src), static_cast<const unsigned char*>(src) + bytes);
+      blob.resize((blob.size() + 15) & ~size_t(15), 0);
+      return off;
+    };
+    put(g->col_of.data(), g->col_of.size() * 2);
+    off_sinfo = put(sinfo.data(), sinfo.size() * 4);
+    off_act = put(g->act.data(), g->act.size() * 4);
+    off_chain = put(g->chain.data(), g->chain.size() * 4);
+    tabs.resize(blob.size() / 16);
+    std::memcpy(tabs.data(), blob.data(), blob.size());
+  } catch (const std::bad_alloc&) {
+    delete p;
+    return CG_E_NOMEM;
+  }
   cudaError_t e;
-  if ((e = pda_upload(p, g->act, &d.act)) != cudaSuccess || (e = pda_upload(p, g->col_of, &d.colmap)) != cudaSuccess ||
-      (e = pda_upload(p, g->chain, &d.chain)) != cudaSuccess || (e = pda_upload(p, sinfo, &d.sinfo)) != cudaSuccess ||
+  if ((e = pda_upload(p, tabs, &d.tabs)) != cudaSuccess ||
       (e = pda_upload(p, key, &d.key)) != cudaSuccess || (e = pda_upload(p, mask_of, &d.mask_of)) != cudaSuccess ||
       (e = pda_upload(p, ms.words, &d.masks)) != cudaSuccess ||
       (e = pda_upload(p, cand_off, &d.cand_off)) != cudaSuccess || (e = pda_upload(p, cand, &d.cand)) != cudaSuccess ||
@@ -361,10 +415,26 @@ int cg_pda_create(cg_ctx* c, const cg_vocab* v, const cg_pda_grammar* g, cg_pda*
     delete p;
     return CG_E_CUDA;
   }
+  const unsigned char* tb = reinterpret_cast<const unsigned char*>(d.tabs);
+  d.colmap = reinterpret_cast<const uint16_t*>(tb);
+  d.sinfo = reinterpret_cast<const uint32_t*>(tb + off_sinfo);
+  d.act = reinterpret_cast<const uint32_t*>(tb + off_act);
+  d.chain = reinterpret_cast<const uint32_t*>(tb + off_chain);
+  d.tab_n16 = uint32_t(tabs.size());
+  d.off_sinfo = off_sinfo;
+  d.off_act = off_act;
+  d.off_chain = off_chain;
+  d.tabs_in_smem = size_t(d.tab_n16) * 16 <= cgk::kPdaSmemTables;
   d.S = S;
   d.n_cols = g->n_cols;
   d.depth = D;
   d.stride = D + 2;
+  if (cgk::allow_smem(reinterpret_cast<const void*>(cgk::pda_fill_kernel), pda_fill_smem(d, W)) != cudaSuccess ||
+      cgk::allow_smem(reinterpret_cast<const void*>(cgk::pda_accept_kernel), pda_accept_smem(d)) != cudaSuccess) {
+    pda_release(p);
+    delete p;
+    return CG_E_CUDA;
+  }
   *out = p;
   return CG_OK;
 }
@@ -390,7 +460,7 @@ int cg_pda_fill_bitmask(cg_pda* p, const uint32_t* d_cfg, uint32_t B, const int3
                         uint32_t* d_bitmask) {
   if (!p || (B && (!d_cfg || !d_bitmask))) return CG_E_ARG;
   if (B == 0) return CG_OK;
-  const size_t smem = (size_t(p->t.W) + p->d.depth) * 4;
+  const size_t smem = pda_fill_smem(p->d, p->t.W);
   return cgk::launch_dependent(cgk::pda_fill_kernel, dim3(B), dim3(cgk::kPdaFillThreads), smem, p->stream, p->d,
                                p->t, d_cfg, d_forced, d_bitmask) == cudaSuccess
              ? CG_OK
@@ -402,7 +472,8 @@ int cg_pda_accept(cg_pda* p, uint32_t* d_cfg, uint32_t B, const uint32_t* d_toks
   if (!p || (B && (!d_cfg || !d_toks || !d_out_flags))) return CG_E_ARG;
   if (B == 0) return CG_OK;
   const uint32_t grid = (B + cgk::kPdaAcceptThreads - 1) / cgk::kPdaAcceptThreads;
-  return cgk::launch_dependent(cgk::pda_accept_kernel, dim3(grid), dim3(cgk::kPdaAcceptThreads), 0, p->stream,
+  return cgk::launch_dependent(cgk::pda_accept_kernel, dim3(grid), dim3(cgk::kPdaAcceptThreads),
+                               pda_accept_smem(p->d), p->stream,
                                p->d, p->t, d_cfg, B, d_toks, d_forced, d_counts, max_tokens, d_out_flags) ==
                  cudaSuccess
              ? CG_OK
