@@ -397,20 +397,32 @@ def _bench_pushdown(args, cg, ctx, vocab, stream, bufs, R, B, V, W, cfg, seed) -
     tok_u = tok.view(torch.uint32)
     flags = torch.empty(B, dtype=torch.uint8, device="cuda")
 
-    def pstep(i, logits):
+    def pstep3(i, logits):
+        # the three calls
         pda.fill_bitmask(cfg_rows, bm)
         ctx.mask_and_sample(logits, bm, cfg.temp, cfg.top_p, seed, i, tok)
         pda.accept(cfg_rows, tok_u, flags, counts=counts, max_tokens=2048)
 
+    def pstep(i, logits):
+        # two launches: sampling, then accept of this step with the next step's fill
+        ctx.mask_and_sample(logits, bm, cfg.temp, cfg.top_p, seed, i, tok)
+        pda.accept_fill(cfg_rows, tok_u, flags, bm, counts=counts, max_tokens=2048)
+
     base = 3 * 10**6
     for i in range(max(args.warmup, 3)):
-        pstep(base + i, bufs[i % R])
+        pstep3(base + i, bufs[i % R])
     n = min(args.steps, 250)
+    g3 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g3, stream=stream, capture_error_mode="thread_local"):
+        for i in range(n):
+            pstep3(base + 100 + i, bufs[i % R])
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
         for i in range(n):
-            pstep(base + 100 + i, bufs[i % R])
-    g.replay()   # upload, and rows move past the first steps
+            pstep(base + 100 + n + i, bufs[i % R])
+    g3.replay()   # uploads, and rows move past the first steps
+    pda.fill_bitmask(cfg_rows, bm)
+    g.replay()
     torch.cuda.synchronize()
     if ctx.status() != 0:
         raise RuntimeError("device status after the pushdown warm-up")
@@ -425,6 +437,8 @@ def _bench_pushdown(args, cg, ctx, vocab, stream, bufs, R, B, V, W, cfg, seed) -
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / reps * 1e3
 
+    step3_us = timed(g3.replay, 1) / n
+    pda.fill_bitmask(cfg_rows, bm)
     step_us = timed(g.replay, 1) / n
     levels = cfg_rows.view(torch.int32)[:, 1].float()
     mean_level, max_level = float(levels.mean().item()), int(levels.max().item())
@@ -442,7 +456,13 @@ def _bench_pushdown(args, cg, ctx, vocab, stream, bufs, R, B, V, W, cfg, seed) -
         restore()
         pda.accept(cfg_rows, tok_u, flags, counts=counts, max_tokens=2048)
 
-    accept_us = timed(restore_accept, 200) - timed(restore, 200)
+    def restore_accept_fill():
+        restore()
+        pda.accept_fill(cfg_rows, tok_u, flags, bm, counts=counts, max_tokens=2048)
+
+    t_restore = timed(restore, 200)
+    accept_us = timed(restore_accept, 200) - t_restore
+    accept_fill_us = timed(restore_accept_fill, 200) - t_restore
     if ctx.status() != 0:
         raise RuntimeError("device status after the pushdown steps")
     info, ginfo = pda.info(), pg.info()
@@ -456,11 +476,14 @@ def _bench_pushdown(args, cg, ctx, vocab, stream, bufs, R, B, V, W, cfg, seed) -
                       "cached_masks": info["n_masks"], "keys": info["n_keys"],
                       "cache_bytes": info["cache_bytes"], "per_row_tokens": info["n_candidates"]},
         "step_us": round(step_us, 3),
+        "step": "mask_and_sample, then accept_fill (accept of the step and fill of the next, one launch)",
         "tokens_per_s": round(B / (step_us * 1e-6), 1),
+        "three_call_step_us": round(step3_us, 3),
         "steps": n,
         "fill_us_alone": round(fill_us, 3),
         "sample_us_alone": round(sample_us, 3),
         "accept_us_alone": round(accept_us, 3),
+        "accept_fill_us_alone": round(accept_fill_us, 3),
         "stack_level_after": {"mean": round(mean_level, 2), "max": max_level},
         "fill_roofline": {"kernel": "pda_fill_kernel", "bound": "hbm", "achieved": round(achieved, 1),
                           "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),

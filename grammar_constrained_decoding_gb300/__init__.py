@@ -322,6 +322,13 @@ class Pda:
         L.check("cg_pda_accept", L.lib().cg_pda_accept(self._h, _ptr(cfg), cfg.shape[0], _ptr(toks), _ptr(forced),
                                                         _ptr(counts), int(max_tokens), _ptr(out_flags)))
 
+    def accept_fill(self, cfg, toks, out_flags, bitmask, forced=None, counts=None, max_tokens: int = 0,
+                    forced_next=None) -> None:
+        """accept, then fill_bitmask of the next step, in one launch."""
+        L.check("cg_pda_accept_fill", L.lib().cg_pda_accept_fill(
+            self._h, _ptr(cfg), cfg.shape[0], _ptr(toks), _ptr(forced), _ptr(counts), int(max_tokens),
+            _ptr(out_flags), _ptr(forced_next), _ptr(bitmask)))
+
 
 class Driver:
     """Host driver of forced tokens (evaluator-aware grammars)."""

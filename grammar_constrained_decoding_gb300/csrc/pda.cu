@@ -158,21 +158,16 @@ __device__ uint8_t pda_flags(const DevPda& p, uint32_t q, uint32_t lvl, const St
 }
 
 constexpr uint32_t kPdaFillThreads = 256;
+constexpr uint32_t kPdaVec = 8;  // uint4s of the row's mask a fill thread holds in registers
 
-__global__ void __launch_bounds__(kPdaFillThreads)
-    pda_fill_kernel(DevPda p, Tables t, const uint32_t* __restrict__ cfg, const int32_t* __restrict__ forced,
-                    uint32_t* __restrict__ bitmask) {
-  // [tables (when they fit)] [W bits of the per-row tokens] [the row's stack]
-  extern __shared__ __align__(16) uint4 sm4[];
-  griddep_launch_dependents();
-  griddep_wait();  // configurations come from the previous accept
-  const uint32_t b = blockIdx.x, W = t.W, tid = threadIdx.x;
-  uint32_t* bits = reinterpret_cast<uint32_t*>(sm4 + (p.tabs_in_smem ? p.tab_n16 : 0u));
-  uint32_t* stk = bits + W;
-  const uint32_t* row = cfg + size_t(b) * p.stride;
-  const uint32_t q = row[0], lvl = row[1];
-  const int32_t f = forced ? forced[b] : -1;
-  uint32_t* out = bitmask + size_t(b) * W;
+// Fills row b's mask for configuration (q, lvl) with the stack at row + 2;
+// all threads of the block take part.  pv: the walk tables (in shared memory
+// when tabs_in_smem, copied there by the caller and synchronised);
+// bits / stk: shared scratch of W and depth words.
+__device__ void pda_fill_row(const DevPda& p, const DevPda& pv, const Tables& t, uint32_t q, uint32_t lvl,
+                             const uint32_t* row, int32_t f, uint32_t* __restrict__ out, uint32_t* bits,
+                             uint32_t* stk) {
+  const uint32_t W = t.W, tid = threadIdx.x;
   const bool ok = q < p.S && lvl <= p.depth;
   if (f >= 0 || !ok) {
     // forced row: exactly that token; failed or malformed row: nothing
@@ -186,19 +181,34 @@ __global__ void __launch_bounds__(kPdaFillThreads)
     return;
   }
   const uint32_t kinfo = p.key[q], hr = p.depth - lvl;
-  const uint32_t* src = p.masks + size_t(p.mask_of[(kinfo >> 8) + min(hr, kinfo & 0xFFu)]) * W;
   const uint32_t c0 = p.cand_off[q], c1 = p.cand_off[q + 1];
+  const uint32_t* __restrict__ src = p.masks + size_t(p.mask_of[(kinfo >> 8) + min(hr, kinfo & 0xFFu)]) * W;
+  // the cached mask: every load issued at once (into registers when the row
+  // fits kPdaVec uint4s per thread), before the per-row walks
+  const uint32_t W4 = W / 4;
+  const bool vec = (W & 3u) == 0 && W4 <= kPdaVec * blockDim.x;
+  uint4 v[kPdaVec];
+  if (vec) {
+    const uint4* __restrict__ s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (uint32_t k = 0; k < kPdaVec; ++k) {
+      const uint32_t i = tid + k * blockDim.x;
+      if (i < W4) v[k] = s4[i];
+    }
+  }
+  uint4* o4 = reinterpret_cast<uint4*>(out);
   if (c0 == c1) {  // nothing decided per row: the cached mask as is
-    if ((W & 3u) == 0) {
-      const uint4* s4 = reinterpret_cast<const uint4*>(src);
-      uint4* o4 = reinterpret_cast<uint4*>(out);
-      for (uint32_t w = tid; w < W / 4; w += blockDim.x) o4[w] = s4[w];
+    if (vec) {
+#pragma unroll
+      for (uint32_t k = 0; k < kPdaVec; ++k) {
+        const uint32_t i = tid + k * blockDim.x;
+        if (i < W4) o4[i] = v[k];
+      }
     } else {
       for (uint32_t w = tid; w < W; w += blockDim.x) out[w] = src[w];
     }
     return;
   }
-  const DevPda pv = p.tabs_in_smem ? tables_to_smem(p, sm4, tid, blockDim.x) : p;
   for (uint32_t w = tid; w < W; w += blockDim.x) bits[w] = 0u;
   for (uint32_t i = tid; i < lvl; i += blockDim.x) stk[i] = row[2 + i];
   __syncthreads();
@@ -211,26 +221,26 @@ __global__ void __launch_bounds__(kPdaFillThreads)
     if (pda_walk(pv, t, tok, 0u, qq, ll, st)) atomicOr(&bits[tok >> 5], 1u << (tok & 31u));
   }
   __syncthreads();
-  for (uint32_t w = tid; w < W; w += blockDim.x) out[w] = src[w] | bits[w];
+  if (vec) {
+    const uint4* b4 = reinterpret_cast<const uint4*>(bits);
+#pragma unroll
+    for (uint32_t k = 0; k < kPdaVec; ++k) {
+      const uint32_t i = tid + k * blockDim.x;
+      if (i < W4) {
+        const uint4 x = b4[i];
+        o4[i] = make_uint4(v[k].x | x.x, v[k].y | x.y, v[k].z | x.z, v[k].w | x.w);
+      }
+    }
+  } else {
+    for (uint32_t w = tid; w < W; w += blockDim.x) out[w] = src[w] | bits[w];
+  }
 }
 
-constexpr uint32_t kPdaAcceptThreads = 128;
-
-__global__ void __launch_bounds__(kPdaAcceptThreads)
-    pda_accept_kernel(DevPda p, Tables t, uint32_t* __restrict__ cfg, uint32_t B, const uint32_t* __restrict__ toks,
-                      const int32_t* __restrict__ forced, uint32_t* counts, uint32_t max_tokens,
-                      uint8_t* __restrict__ out_flags) {
-  extern __shared__ __align__(16) uint4 sm4[];  // the walk tables, when they fit
-  griddep_launch_dependents();
-  const DevPda pv = p.tabs_in_smem ? tables_to_smem(p, sm4, threadIdx.x, blockDim.x) : p;
-  if (p.tabs_in_smem) __syncthreads();
-  griddep_wait();  // the tokens come from the sampling kernel
-  const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= B) return;
-  uint32_t* row = cfg + size_t(b) * p.stride;
+// Advances row b (configuration at `row`, updated in place) by token tok;
+// returns the CG_FLAG_* bits and updates counts[b] when counts are kept.
+__device__ uint8_t pda_accept_row(const DevPda& p, const DevPda& pv, const Tables& t, uint32_t* row, uint32_t b,
+                                  uint32_t tok, int32_t f, uint32_t* counts, uint32_t max_tokens) {
   uint32_t q = row[0], lvl = row[1];
-  const uint32_t tok = toks[b];
-  const int32_t f = forced ? forced[b] : -1;
   const uint32_t n0 = counts ? counts[b] : 0u;
   uint8_t fl = 0;
   if (tok == CG_NO_TOKEN) {
@@ -272,7 +282,71 @@ __global__ void __launch_bounds__(kPdaAcceptThreads)
   }
   row[0] = q;
   row[1] = lvl;
-  out_flags[b] = fl;
+  return fl;
+}
+
+// shared memory of a fill block: [tables (when they fit)] [W bits] [the row's stack]
+__device__ __forceinline__ uint32_t* fill_bits(const DevPda& p, uint4* sm4) {
+  return reinterpret_cast<uint32_t*>(sm4 + (p.tabs_in_smem ? p.tab_n16 : 0u));
+}
+
+__global__ void __launch_bounds__(kPdaFillThreads)
+    pda_fill_kernel(DevPda p, Tables t, const uint32_t* __restrict__ cfg, const int32_t* __restrict__ forced,
+                    uint32_t* __restrict__ bitmask) {
+  extern __shared__ __align__(16) uint4 sm4[];
+  griddep_launch_dependents();
+  const DevPda pv = p.tabs_in_smem ? tables_to_smem(p, sm4, threadIdx.x, blockDim.x) : p;
+  griddep_wait();  // configurations come from the previous accept
+  const uint32_t b = blockIdx.x;
+  const uint32_t* row = cfg + size_t(b) * p.stride;
+  uint32_t* bits = fill_bits(p, sm4);
+  pda_fill_row(p, pv, t, row[0], row[1], row, forced ? forced[b] : -1, bitmask + size_t(b) * t.W, bits,
+               bits + t.W);
+}
+
+constexpr uint32_t kPdaAcceptThreads = 128;
+
+__global__ void __launch_bounds__(kPdaAcceptThreads)
+    pda_accept_kernel(DevPda p, Tables t, uint32_t* __restrict__ cfg, uint32_t B, const uint32_t* __restrict__ toks,
+                      const int32_t* __restrict__ forced, uint32_t* counts, uint32_t max_tokens,
+                      uint8_t* __restrict__ out_flags) {
+  extern __shared__ __align__(16) uint4 sm4[];  // the walk tables, when they fit
+  griddep_launch_dependents();
+  const DevPda pv = p.tabs_in_smem ? tables_to_smem(p, sm4, threadIdx.x, blockDim.x) : p;
+  if (p.tabs_in_smem) __syncthreads();
+  griddep_wait();  // the tokens come from the sampling kernel
+  const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  out_flags[b] = pda_accept_row(p, pv, t, cfg + size_t(b) * p.stride, b, toks[b], forced ? forced[b] : -1, counts,
+                                max_tokens);
+}
+
+// Accept of this step and fill of the next in one block per row: thread 0
+// advances the row, the block then fills its next mask from the new
+// configuration (the __syncthreads between them orders the row's global
+// writes before the block's reads).
+__global__ void __launch_bounds__(kPdaFillThreads)
+    pda_accept_fill_kernel(DevPda p, Tables t, uint32_t* __restrict__ cfg, const uint32_t* __restrict__ toks,
+                           const int32_t* __restrict__ forced, uint32_t* counts, uint32_t max_tokens,
+                           uint8_t* __restrict__ out_flags, const int32_t* __restrict__ forced_next,
+                           uint32_t* __restrict__ bitmask) {
+  extern __shared__ __align__(16) uint4 sm4[];
+  __shared__ uint32_t s_cfg[2];
+  griddep_launch_dependents();
+  const DevPda pv = p.tabs_in_smem ? tables_to_smem(p, sm4, threadIdx.x, blockDim.x) : p;
+  if (p.tabs_in_smem) __syncthreads();
+  griddep_wait();  // the tokens come from the sampling kernel
+  const uint32_t b = blockIdx.x;
+  uint32_t* row = cfg + size_t(b) * p.stride;
+  if (threadIdx.x == 0) {
+    out_flags[b] = pda_accept_row(p, pv, t, row, b, toks[b], forced ? forced[b] : -1, counts, max_tokens);
+    s_cfg[0] = row[0];
+    s_cfg[1] = row[1];
+  }
+  __syncthreads();
+  uint32_t* bits = fill_bits(p, sm4);
+  pda_fill_row(p, pv, t, s_cfg[0], s_cfg[1], row, forced_next ? forced_next[b] : -1, bitmask + size_t(b) * t.W,
+               bits, bits + t.W);
 }
 
 }  // namespace cgk
@@ -430,6 +504,8 @@ int cg_pda_create(cg_ctx* c, const cg_vocab* v, const cg_pda_grammar* g, cg_pda*
   d.depth = D;
   d.stride = D + 2;
   if (cgk::allow_smem(reinterpret_cast<const void*>(cgk::pda_fill_kernel), pda_fill_smem(d, W)) != cudaSuccess ||
+      cgk::allow_smem(reinterpret_cast<const void*>(cgk::pda_accept_fill_kernel), pda_fill_smem(d, W)) !=
+          cudaSuccess ||
       cgk::allow_smem(reinterpret_cast<const void*>(cgk::pda_accept_kernel), pda_accept_smem(d)) != cudaSuccess) {
     pda_release(p);
     delete p;
@@ -476,6 +552,18 @@ int cg_pda_accept(cg_pda* p, uint32_t* d_cfg, uint32_t B, const uint32_t* d_toks
                                pda_accept_smem(p->d), p->stream,
                                p->d, p->t, d_cfg, B, d_toks, d_forced, d_counts, max_tokens, d_out_flags) ==
                  cudaSuccess
+             ? CG_OK
+             : CG_E_CUDA;
+}
+
+int cg_pda_accept_fill(cg_pda* p, uint32_t* d_cfg, uint32_t B, const uint32_t* d_toks, const int32_t* d_forced,
+                       uint32_t* d_counts, uint32_t max_tokens, uint8_t* d_out_flags, const int32_t* d_forced_next,
+                       uint32_t* d_bitmask) {
+  if (!p || (B && (!d_cfg || !d_toks || !d_out_flags || !d_bitmask))) return CG_E_ARG;
+  if (B == 0) return CG_OK;
+  return cgk::launch_dependent(cgk::pda_accept_fill_kernel, dim3(B), dim3(cgk::kPdaFillThreads),
+                               pda_fill_smem(p->d, p->t.W), p->stream, p->d, p->t, d_cfg, d_toks, d_forced, d_counts,
+                               max_tokens, d_out_flags, d_forced_next, d_bitmask) == cudaSuccess
              ? CG_OK
              : CG_E_CUDA;
 }

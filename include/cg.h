@@ -460,6 +460,14 @@ int cg_pda_fill_bitmask(cg_pda* p, const uint32_t* d_cfg, uint32_t B, const int3
 int cg_pda_accept(cg_pda* p, uint32_t* d_cfg, uint32_t B, const uint32_t* d_toks, const int32_t* d_forced,
                   uint32_t* d_counts, uint32_t max_tokens, uint8_t* d_out_flags);
 
+/* Step 3 of one step and step 1 of the next in one launch: cg_pda_accept with
+ * these arguments, then cg_pda_fill_bitmask of the updated configurations with
+ * d_forced_next (NULL for none) into d_bitmask.  Results are identical to the
+ * two calls in sequence. */
+int cg_pda_accept_fill(cg_pda* p, uint32_t* d_cfg, uint32_t B, const uint32_t* d_toks, const int32_t* d_forced,
+                       uint32_t* d_counts, uint32_t max_tokens, uint8_t* d_out_flags, const int32_t* d_forced_next,
+                       uint32_t* d_bitmask);
+
 /* ---- evaluator-aware host side --------------------------------------------------- */
 
 #define CG_RESULT_CALC_TAG    0  /* <result>V</result> | <result_error>code</result_error> */

@@ -18,7 +18,8 @@ oracle of the same grammar flattened under the same stack bound.
   frame: 1896 states at 16): rows nest to the bound, where the device refuses
   a further "[", and every finished text parses as JSON within the bound;
 * edge cases: an empty batch, malformed configurations, refused and
-  out-of-range tokens, a forced token that differs from the sampled one.
+  out-of-range tokens, a forced token that differs from the sampled one;
+* cg_pda_accept_fill equals cg_pda_accept followed by cg_pda_fill_bitmask.
 """
 
 import json
@@ -322,3 +323,45 @@ def test_edge_cases():
     g_fl, g_cfg = host(flags), host(cfg).view(np.uint32)
     assert list(g_fl) == [4, 4, 4] and (g_cfg[:, 0] == 0xFFFFFFFF).all()
     assert ctx.status() in (2, 4, 7)
+
+
+def test_accept_fill_equals_the_two_calls():
+    """cg_pda_accept_fill (accept of one step and fill of the next in one
+    launch) gives the configurations, flags, counts and masks of cg_pda_accept
+    followed by cg_pda_fill_bitmask, and the masks are the oracle's."""
+    import torch
+    D, V, B, steps = 8, 32000, 96, 30
+    toks = vocab("bpe", V)
+    orc = OracleRows(JSON_NESTED, D, toks)
+    ctx, pda = _pda(JSON_NESTED, D, V)
+    opens = np.array([t.count(b"[") + t.count(b"{") for t in toks])
+    rng = np.random.default_rng(77)
+    W = (V + 31) // 32
+    cfg_a, cfg_b = _fresh(B, D), _fresh(B, D)
+    bm_a, bm_b = empty((B, W), torch.int32), empty((B, W), torch.int32)
+    fl_a, fl_b = empty((B,), torch.uint8), empty((B,), torch.uint8)
+    cnt_a = torch.zeros((B,), dtype=torch.int32, device="cuda").view(torch.uint32)
+    cnt_b = torch.zeros((B,), dtype=torch.int32, device="cuda").view(torch.uint32)
+    st = [0] * B
+    pda.fill_bitmask(cfg_b, bm_b)
+    for step in range(steps):
+        pda.fill_bitmask(cfg_a, bm_a)
+        g_a = host(bm_a).view(np.uint32)
+        assert np.array_equal(g_a, host(bm_b).view(np.uint32)), step
+        pick = np.empty(B, np.uint32)
+        for b in range(B):
+            want = orc.mask(st[b])
+            assert np.array_equal(g_a[b], want), (step, b)
+            pick[b] = _pick(rng, want, V, opens, 0.3)
+        toks_d = u32(pick)
+        pda.accept(cfg_a, toks_d, fl_a, counts=cnt_a, max_tokens=12)
+        pda.accept_fill(cfg_b, toks_d, fl_b, bm_b, counts=cnt_b, max_tokens=12)
+        assert ctx.status() == 0
+        assert np.array_equal(host(fl_a), host(fl_b)), step
+        assert np.array_equal(host(cfg_a), host(cfg_b)), step
+        assert np.array_equal(host(cnt_a), host(cnt_b)), step
+        g_fl = host(fl_a)
+        for b in range(B):
+            t = int(pick[b])
+            s, f = (st[b], 8) if t == NO_TOKEN else accept(orc.dfa, st[b], t, toks, False)
+            st[b] = 0 if g_fl[b] & (FLAG_DONE | 16) else s
