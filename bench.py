@@ -403,10 +403,14 @@ def _bench_pushdown(args, cg, ctx, vocab, stream, bufs, R, B, V, W, cfg, seed) -
         ctx.mask_and_sample(logits, bm, cfg.temp, cfg.top_p, seed, i, tok)
         pda.accept(cfg_rows, tok_u, flags, counts=counts, max_tokens=2048)
 
-    def pstep(i, logits):
+    def pstep2(i, logits):
         # two launches: sampling, then accept of this step with the next step's fill
         ctx.mask_and_sample(logits, bm, cfg.temp, cfg.top_p, seed, i, tok)
         pda.accept_fill(cfg_rows, tok_u, flags, bm, counts=counts, max_tokens=2048)
+
+    def pstep(i, logits):
+        # one call, one fused kernel per row: mask, sample, accept
+        pda.step(cfg_rows, logits, cfg.temp, cfg.top_p, seed, i, tok_u, flags, counts=counts, max_tokens=2048)
 
     base = 3 * 10**6
     for i in range(max(args.warmup, 3)):
@@ -416,12 +420,17 @@ def _bench_pushdown(args, cg, ctx, vocab, stream, bufs, R, B, V, W, cfg, seed) -
     with torch.cuda.graph(g3, stream=stream, capture_error_mode="thread_local"):
         for i in range(n):
             pstep3(base + 100 + i, bufs[i % R])
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=stream, capture_error_mode="thread_local"):
+        for i in range(n):
+            pstep2(base + 100 + n + i, bufs[i % R])
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
         for i in range(n):
-            pstep(base + 100 + n + i, bufs[i % R])
+            pstep(base + 100 + 2 * n + i, bufs[i % R])
     g3.replay()   # uploads, and rows move past the first steps
     pda.fill_bitmask(cfg_rows, bm)
+    g2.replay()
     g.replay()
     torch.cuda.synchronize()
     if ctx.status() != 0:
@@ -439,6 +448,7 @@ def _bench_pushdown(args, cg, ctx, vocab, stream, bufs, R, B, V, W, cfg, seed) -
 
     step3_us = timed(g3.replay, 1) / n
     pda.fill_bitmask(cfg_rows, bm)
+    step2_us = timed(g2.replay, 1) / n
     step_us = timed(g.replay, 1) / n
     levels = cfg_rows.view(torch.int32)[:, 1].float()
     mean_level, max_level = float(levels.mean().item()), int(levels.max().item())
@@ -469,6 +479,8 @@ def _bench_pushdown(args, cg, ctx, vocab, stream, bufs, R, B, V, W, cfg, seed) -
     peaks = _peaks()
     fill_bytes = B * 8 * W   # the cached mask read and the bitmask written, per row
     achieved = fill_bytes / (fill_us * 1e-6) / 1e9
+    step_bytes = B * (V * (2 if cfg.dtype == "bf16" else 4) + W * 4)   # logits and masks read, as cg_step
+    step_achieved = step_bytes / (step_us * 1e-6) / 1e9
     return {
         "workload": f"json_nested: recursive JSON grammar, stack bound {depth} frames, V={V}, B={B}, "
                     f"{cfg.dtype} logits as the main workload, T={cfg.temp}, top_p={cfg.top_p}",
@@ -476,8 +488,9 @@ def _bench_pushdown(args, cg, ctx, vocab, stream, bufs, R, B, V, W, cfg, seed) -
                       "cached_masks": info["n_masks"], "keys": info["n_keys"],
                       "cache_bytes": info["cache_bytes"], "per_row_tokens": info["n_candidates"]},
         "step_us": round(step_us, 3),
-        "step": "mask_and_sample, then accept_fill (accept of the step and fill of the next, one launch)",
+        "step": "cg_pda_step: mask, sample and accept in one fused kernel per row",
         "tokens_per_s": round(B / (step_us * 1e-6), 1),
+        "sample_then_accept_fill_step_us": round(step2_us, 3),
         "three_call_step_us": round(step3_us, 3),
         "steps": n,
         "fill_us_alone": round(fill_us, 3),
@@ -485,6 +498,9 @@ def _bench_pushdown(args, cg, ctx, vocab, stream, bufs, R, B, V, W, cfg, seed) -
         "accept_us_alone": round(accept_us, 3),
         "accept_fill_us_alone": round(accept_fill_us, 3),
         "stack_level_after": {"mean": round(mean_level, 2), "max": max_level},
+        "step_roofline": {"kernel": "stream_topp_kernel<2> (cg_pda_step)", "bound": "hbm",
+                          "achieved": round(step_achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                          "frac": round(step_achieved / peaks["hbm_gbs"], 4), "algorithmic_bytes_per_launch": step_bytes},
         "fill_roofline": {"kernel": "pda_fill_kernel", "bound": "hbm", "achieved": round(achieved, 1),
                           "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                           "algorithmic_bytes_per_launch": fill_bytes},

@@ -322,6 +322,16 @@ class Pda:
         L.check("cg_pda_accept", L.lib().cg_pda_accept(self._h, _ptr(cfg), cfg.shape[0], _ptr(toks), _ptr(forced),
                                                         _ptr(counts), int(max_tokens), _ptr(out_flags)))
 
+    def step(self, cfg, logits, temp: float, top_p: float, seed: int, step: int, out_tok, out_flags, forced=None,
+             counts=None, max_tokens: int = 0, bitmask=None) -> None:
+        """mask, sample and accept in one call (one kernel on the bf16 top-p path)."""
+        import torch
+        dtype = {torch.float32: L.CG_F32, torch.bfloat16: L.CG_BF16}[logits.dtype]
+        B, V = logits.shape
+        L.check("cg_pda_step", L.lib().cg_pda_step(
+            self._h, _ptr(cfg), B, _ptr(logits), dtype, V, float(temp), float(top_p), int(seed), int(step),
+            _ptr(forced), _ptr(counts), int(max_tokens), _ptr(bitmask), _ptr(out_tok), _ptr(out_flags)))
+
     def accept_fill(self, cfg, toks, out_flags, bitmask, forced=None, counts=None, max_tokens: int = 0,
                     forced_next=None) -> None:
         """accept, then fill_bitmask of the next step, in one launch."""

@@ -116,6 +116,14 @@ int grow(cg_ctx* c, void** buf, size_t* have, size_t need) {
 
 }  // namespace
 
+namespace cgk {
+int ctx_sample_scratch(cg_ctx* c, size_t bytes, void** out) {
+  const int rc = grow(c, &c->sample_scratch, &c->sample_scratch_bytes, bytes);
+  *out = c->sample_scratch;
+  return rc;
+}
+}  // namespace cgk
+
 // Scratch of cg_mask_and_sample_noalloc: the candidate lists of up to
 // CG_NOALLOC_MAX_ROWS rows (u32 ids, then u16 keys), fixed in the module so
 // that the call never allocates.  Its callers are the ones that must not touch

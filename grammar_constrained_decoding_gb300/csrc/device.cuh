@@ -73,6 +73,9 @@ struct CtxView {
   Tables t;
 };
 CtxView ctx_view(const cg_ctx* c);
+// The context's candidate-list scratch of the sampling kernels, grown to at
+// least `bytes` (CG_OK or a CG_E_* code).
+int ctx_sample_scratch(cg_ctx* c, size_t bytes, void** out);
 
 constexpr uint16_t kDead16 = 0xFFFFu;      // CG_DEAD in table16
 constexpr uint32_t kLongToken = 0xFFu;     // token record length of a token read through tok_off

@@ -25,6 +25,7 @@
 #include <mutex>
 #include <utility>
 
+#include "pda.cuh"
 #include "row_ops.cuh"
 
 namespace cgk {
@@ -479,6 +480,8 @@ struct StepArgs {
   uint32_t n_pg;
   uint32_t cache_complete;  // every class mask is in the cache (cg_ctx_prefill ran): skip the ready check
   uint32_t win_bytes;       // shared memory for the accept's table window (0: none)
+  DevPda pda;               // pushdown step: the automaton (its tables read from global memory)
+  uint32_t* pda_cfg;        // pushdown step: row configurations [B][depth + 2], updated in place
 };
 
 // Grammar g's descriptor from the kernel parameters when they hold it (an
@@ -593,7 +596,94 @@ __device__ void stage_accept_tables(const StepArgs& sa, uint32_t g, uint32_t s, 
   for (uint32_t i = lane; i < rows; i += 32) wflags[i] = t.state_flags[gd.state_off + lo + i];
 }
 
-template <bool STEP>
+// The mask of a pushdown row (cg_pda_step), as cg_pda_fill_bitmask defines
+// it.  All threads of the block take part.  Thread 0 reads the row's
+// configuration and forced token and starts the bulk copy of the cached mask
+// of (state, headroom), completing on *mbar_mask (parity 0); meanwhile the
+// threads walk the state's listed tokens against the row's stack (tables read
+// from global memory) and collect the allowed ones in `list` (list_cap words
+// of free shared memory); once the copy has landed they are ORed into the
+// mask.  A longer list than list_cap is ORed in directly after the copy.
+__device__ void pda_row_mask(const StepArgs& sa, uint32_t b, uint32_t W, uint32_t* smask, uint32_t* list,
+                             uint32_t list_cap, uint64_t* mbar_mask, uint32_t& s_copied, uint32_t& s_mode,
+                             uint32_t& s_mi, uint32_t& s_c0, uint32_t& s_c1, uint32_t& s_n, int32_t& s_f,
+                             uint32_t& s_flag) {
+  const Tables& t = sa.t;
+  const DevPda& p = sa.pda;
+  const uint32_t tid = threadIdx.x;
+  const uint32_t* row = sa.pda_cfg + size_t(b) * p.stride;
+  if (tid == 0) {
+    const uint32_t q = row[0], lvl = row[1];
+    const int32_t f = sa.forced ? sa.forced[b] : -1;
+    uint32_t mode = 0, copied = 0, mi = 0, c0 = 0, c1 = 0;
+    if (f >= 0) {
+      mode = uint32_t(f) < t.V ? 2u : 1u;
+      if (mode == 1) record_error(t.status, CG_DEV_BAD_FORCED);
+    } else if (q >= p.S || lvl > p.depth) {
+      mode = 1;
+      if (q != CG_DEAD) record_error(t.status, CG_DEV_BAD_STATE);
+    } else {
+      const uint32_t kinfo = p.key[q];
+      mi = p.mask_of[(kinfo >> 8) + min(p.depth - lvl, kinfo & 0xFFu)];
+      c0 = p.cand_off[q];
+      c1 = p.cand_off[q + 1];
+      if ((W & 3u) == 0) {
+        mbar_expect_tx(mbar_mask, W * 4);
+        bulk_g2s(smask, p.masks + size_t(mi) * W, W * 4, mbar_mask);
+        copied = 1;
+      }
+    }
+    s_mode = mode;
+    s_f = f;
+    s_copied = copied;
+    s_mi = mi;
+    s_c0 = c0;
+    s_c1 = c1;
+    s_n = 0;
+  }
+  __syncthreads();
+  const uint32_t mode = s_mode;
+  if (mode == 1) {
+    for (uint32_t i = tid; i < W; i += blockDim.x) smask[i] = 0u;
+    return;
+  }
+  if (mode == 2) {
+    const uint32_t f = uint32_t(s_f);
+    for (uint32_t i = tid; i < W; i += blockDim.x) smask[i] = (i == (f >> 5)) ? (1u << (f & 31)) : 0u;
+    return;
+  }
+  const bool copied = s_copied != 0;
+  if (!copied) {
+    const uint32_t* crow = p.masks + size_t(s_mi) * W;
+    for (uint32_t i = tid; i < W; i += blockDim.x) smask[i] = crow[i];
+  }
+  const uint32_t c0 = s_c0, c1 = s_c1, q = row[0], lvl = row[1];
+  const bool listed = c1 - c0 <= list_cap;
+  if (!listed) {
+    if (copied && !mbar_wait(mbar_mask, 0)) atomicOr(&s_flag, 1u);
+    __syncthreads();
+  }
+  for (uint32_t i = c0 + tid; i < c1; i += blockDim.x) {
+    const uint32_t tok = p.cand[i];
+    uint32_t qq = q, ll = lvl;
+    OverlayStack st;
+    st.base = row + 2;
+    st.keep = lvl;
+    if (pda_walk(p, t, tok, 0u, qq, ll, st)) {
+      if (listed) list[atomicAdd(&s_n, 1u)] = tok;
+      else atomicOr(&smask[tok >> 5], 1u << (tok & 31u));
+    }
+  }
+  if (listed) {
+    if (copied && !mbar_wait(mbar_mask, 0)) atomicOr(&s_flag, 1u);
+    __syncthreads();
+    for (uint32_t i = tid; i < s_n; i += blockDim.x) atomicOr(&smask[list[i] >> 5], 1u << (list[i] & 31u));
+  }
+}
+
+// STEP: 0 sampling from a bitmask (cg_mask_and_sample); 1 the fused step of
+// automaton rows (cg_step); 2 the fused step of pushdown rows (cg_pda_step).
+template <int STEP>
 __global__ void __launch_bounds__(kThreads, 2)
     stream_topp_kernel(void* logits, uint32_t V, uint32_t W, const uint32_t* __restrict__ bitmask, float temp,
                        float top_p, uint32_t k0, uint32_t k1, uint32_t step, uint32_t* __restrict__ out_tok,
@@ -646,15 +736,19 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncthreads();  // barriers initialised
   griddep_wait();   // the bitmask (or, fused, the states) come from the previous kernel
-  if (!STEP) {
+  if (STEP == 0) {
     const uint32_t* mrow = bitmask + size_t(b) * W;
     for (uint32_t i = tid; i < W; i += kThreads) smask[i] = mrow[i];
   } else {
     // the logits do not depend on the mask: start the first copies now
     if (warp == kConsumerWarps && lane == 0)
       for (uint32_t k = 0; k < nchunks && k < uint32_t(kStages); ++k) issue_chunk(ring, full, row, V, k);
-    step_row_mask(sa, b, W, smask, reinterpret_cast<uint16_t*>(stg_all), &mbar_mask, s_copied, s_mode, s_cls, s_ready,
-                  s_claim, s_g, s_s, s_f);
+    if (STEP == 1)
+      step_row_mask(sa, b, W, smask, reinterpret_cast<uint16_t*>(stg_all), &mbar_mask, s_copied, s_mode, s_cls,
+                    s_ready, s_claim, s_g, s_s, s_f);
+    else
+      pda_row_mask(sa, b, W, smask, reinterpret_cast<uint32_t*>(stg_all), kConsumerWarps * kStage * 4, &mbar_mask,
+                   s_copied, s_mode, s_cls, s_g, s_s, s_ready, s_f, s_flag);
   }
   __syncthreads();
 
@@ -668,10 +762,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (warp == kConsumerWarps) {
     // ---- producer warp --------------------------------------------------------------
-    if (STEP) stage_accept_tables(sa, s_g, s_s, scols, win, wflags, &mbar_win, &s_wlo, &s_wrows, &s_wdelta, lane);
+    if (STEP == 1) stage_accept_tables(sa, s_g, s_s, scols, win, wflags, &mbar_win, &s_wlo, &s_wrows, &s_wdelta, lane);
     if (lane == 0) {
       bool ok = true;
-      for (uint32_t k = STEP ? min(nchunks, uint32_t(kStages)) : 0u; k < nchunks; ++k) {
+      for (uint32_t k = STEP != 0 ? min(nchunks, uint32_t(kStages)) : 0u; k < nchunks; ++k) {
         if (k >= uint32_t(kStages) && !mbar_wait(empty + k % kStages, ((k / kStages) - 1) & 1u)) {
           ok = false;
           break;
@@ -687,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint32_t sc = 0;  // staged groups of this warp (warp-uniform)
     const uint32_t lt = (1u << lane) - 1u;
     // the row's mask (fused step: a bulk copy from the mask cache)
-    if (STEP && s_copied && !mbar_wait(&mbar_mask, 0)) atomicOr(&s_flag, 1u);
+    if (STEP != 0 && s_copied && !mbar_wait(&mbar_mask, 0)) atomicOr(&s_flag, 1u);
     // chunk 0's maximum seeds the reference, so the first chunk does not flag
     // every group
     if (!mbar_wait(full + 0, 0)) atomicOr(&s_flag, 1u);
@@ -796,8 +890,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint32_t issued = (nchunks - sl + kStages - 1) / kStages;
       mbar_wait(full + sl, (issued - 1) & 1u);
     }
-    if (STEP && s_copied) mbar_wait(&mbar_mask, 0);
-    if (STEP && s_wrows) mbar_wait(&mbar_win, 0);
+    if (STEP != 0 && s_copied) mbar_wait(&mbar_mask, 0);
+    if (STEP == 1 && s_wrows) mbar_wait(&mbar_win, 0);
   }
   const float M = fkey_inv(s_maxkey);  // -inf when no logit is allowed
   // S: per-thread partial sums, warp sums and the 16 warp sums, all in float
@@ -979,7 +1073,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   if (tid == 0) {
     out_tok[b] = tok;
-    if (STEP) {
+    if (STEP == 2) {
+      sa.out_flags[b] = pda_accept_row(sa.pda, sa.pda, sa.t, sa.pda_cfg + size_t(b) * sa.pda.stride, b, tok, s_f,
+                                       sa.counts, sa.max_tokens);
+    } else if (STEP == 1) {
       StateWindow w;
       if (s_wrows) {
         if (mbar_wait(&mbar_win, 0)) {
@@ -995,7 +1092,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                  s_g < sa.t.n_g ? scols : nullptr, w);
     }
   }
-  if (STEP && sa.bitmask_out) {
+  if (STEP != 0 && sa.bitmask_out) {
     uint32_t* out = sa.bitmask_out + size_t(b) * W;
     for (uint32_t i = tid; i < W; i += kThreads) out[i] = smask[i];
   }
@@ -1239,11 +1336,11 @@ cudaError_t launch_mask_and_sample(void* logits, int dtype, uint32_t B, uint32_t
   const bool vec = (V % ch == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
   const size_t s1 = fast::stream_smem(W);
   if (bf16 && vec && mode == kTopP && s1 <= 112 * 1024) {
-    cudaError_t e = allow_smem(reinterpret_cast<const void*>(fast::stream_topp_kernel<false>), s1);
+    cudaError_t e = allow_smem(reinterpret_cast<const void*>(fast::stream_topp_kernel<0>), s1);
     if (e != cudaSuccess) return e;
     uint32_t* cand_id = static_cast<uint32_t*>(scratch);
     uint16_t* cand_key = reinterpret_cast<uint16_t*>(cand_id + size_t(B) * fast::kCandPerRow);
-    return launch_dependent(fast::stream_topp_kernel<false>, dim3(B), dim3(fast::kThreads), s1, stream, logits, V,
+    return launch_dependent(fast::stream_topp_kernel<0>, dim3(B), dim3(fast::kThreads), s1, stream, logits, V,
                             W, bitmask, temp, top_p, uint32_t(seed), uint32_t(seed >> 32), step, out_tok, probs,
                             inplace, cand_id, cand_key, fast::kCandPerRow, status, fast::StepArgs{});
   }
@@ -1287,7 +1384,7 @@ cudaError_t launch_step(const Tables& t, const uint32_t* states, const uint16_t*
           ? uint32_t(std::min<size_t>(fast::kWinBytesMax, fast::kTwoCtaSmem - base) & ~size_t(15))
           : 0u;
   const size_t s1 = base + win_bytes;
-  cudaError_t e = allow_smem(reinterpret_cast<const void*>(fast::stream_topp_kernel<true>), s1);
+  cudaError_t e = allow_smem(reinterpret_cast<const void*>(fast::stream_topp_kernel<1>), s1);
   if (e != cudaSuccess) return e;
   uint32_t* cand_id = static_cast<uint32_t*>(scratch);
   uint16_t* cand_key = reinterpret_cast<uint16_t*>(cand_id + size_t(B) * fast::kCandPerRow);
@@ -1298,7 +1395,30 @@ cudaError_t launch_step(const Tables& t, const uint32_t* states, const uint16_t*
   }
   sa.cache_complete = cache_complete ? 1u : 0u;
   sa.win_bytes = win_bytes;
-  return launch_dependent(fast::stream_topp_kernel<true>, dim3(B), dim3(fast::kThreads), s1, stream, logits, V, W,
+  return launch_dependent(fast::stream_topp_kernel<1>, dim3(B), dim3(fast::kThreads), s1, stream, logits, V, W,
+                          static_cast<const uint32_t*>(nullptr), temp, top_p, uint32_t(seed), uint32_t(seed >> 32),
+                          step, out_tok, static_cast<float*>(nullptr), 0, cand_id, cand_key, fast::kCandPerRow,
+                          t.status, sa);
+}
+
+// The fused step of pushdown rows (cg_pda_step): the row's mask from the
+// (state, headroom) cache and its listed tokens, the masked top-p sampling of
+// cg_mask_and_sample, and the accept into the row's configuration, in one
+// kernel per row.
+cudaError_t launch_pda_step(const Tables& t, const DevPda& pda, uint32_t* cfg, const int32_t* forced, uint32_t B,
+                            void* logits, uint32_t V, float temp, float top_p, uint64_t seed, uint32_t step,
+                            uint32_t* counts, uint32_t max_tokens, uint32_t* bitmask_out, uint32_t* out_tok,
+                            uint8_t* out_flags, void* scratch, cudaStream_t stream) {
+  if (B == 0) return cudaSuccess;
+  const uint32_t W = t.W;
+  const size_t s1 = fast::stream_smem(W);
+  cudaError_t e = allow_smem(reinterpret_cast<const void*>(fast::stream_topp_kernel<2>), s1);
+  if (e != cudaSuccess) return e;
+  uint32_t* cand_id = static_cast<uint32_t*>(scratch);
+  uint16_t* cand_key = reinterpret_cast<uint16_t*>(cand_id + size_t(B) * fast::kCandPerRow);
+  fast::StepArgs sa{t,  nullptr, nullptr, forced, counts, max_tokens, nullptr, out_flags, bitmask_out,
+                    {}, 0u,      0u,      0u,     pda,    cfg};
+  return launch_dependent(fast::stream_topp_kernel<2>, dim3(B), dim3(fast::kThreads), s1, stream, logits, V, W,
                           static_cast<const uint32_t*>(nullptr), temp, top_p, uint32_t(seed), uint32_t(seed >> 32),
                           step, out_tok, static_cast<float*>(nullptr), 0, cand_id, cand_key, fast::kCandPerRow,
                           t.status, sa);

@@ -460,6 +460,16 @@ int cg_pda_fill_bitmask(cg_pda* p, const uint32_t* d_cfg, uint32_t B, const int3
 int cg_pda_accept(cg_pda* p, uint32_t* d_cfg, uint32_t B, const uint32_t* d_toks, const int32_t* d_forced,
                   uint32_t* d_counts, uint32_t max_tokens, uint8_t* d_out_flags);
 
+/* The whole step for pushdown rows, as cg_step is for automaton rows: the
+ * mask of each row (as cg_pda_fill_bitmask, into d_bitmask too when it is not
+ * NULL), masked sampling (as cg_mask_and_sample, same arguments) and the
+ * accept into d_cfg (as cg_pda_accept with d_forced, d_counts, max_tokens).
+ * On the bf16 top-p path it is one kernel per row; otherwise the three calls.
+ * Results are identical to the three calls.  Errors: as those calls. */
+int cg_pda_step(cg_pda* p, uint32_t* d_cfg, uint32_t B, void* d_logits, int dtype, uint32_t V, float temp,
+                float top_p, uint64_t seed, uint32_t step, const int32_t* d_forced, uint32_t* d_counts,
+                uint32_t max_tokens, uint32_t* d_bitmask, uint32_t* d_out_tok, uint8_t* d_out_flags);
+
 /* Step 3 of one step and step 1 of the next in one launch: cg_pda_accept with
  * these arguments, then cg_pda_fill_bitmask of the updated configurations with
  * d_forced_next (NULL for none) into d_bitmask.  Results are identical to the

@@ -19,7 +19,8 @@ oracle of the same grammar flattened under the same stack bound.
   a further "[", and every finished text parses as JSON within the bound;
 * edge cases: an empty batch, malformed configurations, refused and
   out-of-range tokens, a forced token that differs from the sampled one;
-* cg_pda_accept_fill equals cg_pda_accept followed by cg_pda_fill_bitmask.
+* cg_pda_accept_fill equals cg_pda_accept followed by cg_pda_fill_bitmask;
+* cg_pda_step (the fused pushdown step) equals the three calls.
 """
 
 import json
@@ -365,3 +366,45 @@ def test_accept_fill_equals_the_two_calls():
             t = int(pick[b])
             s, f = (st[b], 8) if t == NO_TOKEN else accept(orc.dfa, st[b], t, toks, False)
             st[b] = 0 if g_fl[b] & (FLAG_DONE | 16) else s
+
+
+@pytest.mark.parametrize("dtype,V,B,D", [("bf16", 128256, 256, 32), ("f32", 32000, 64, 8), ("bf16", 4013, 32, 8)])
+def test_pda_step_equals_the_three_calls(dtype, V, B, D):
+    """cg_pda_step (one fused kernel per row on the bf16 top-p path, else the
+    three calls inside the library) gives the ids, flags, configurations,
+    counts and masks of cg_pda_fill_bitmask, cg_mask_and_sample and
+    cg_pda_accept, step after step; the masks are the oracle's at D = 8."""
+    import torch
+    temp, top_p, seed, steps = 0.7, 0.9, 5, 12
+    toks = vocab("bpe", V)
+    ctx, pda = _pda(JSON_NESTED, D, V)
+    orc = OracleRows(JSON_NESTED, D, toks) if D <= 8 else None
+    W = (V + 31) // 32
+    cfg_a, cfg_b = _fresh(B, D), _fresh(B, D)
+    bm_a, bm_b = empty((B, W), torch.int32), empty((B, W), torch.int32)
+    tok_a, tok_b = empty((B,), torch.int32), empty((B,), torch.int32)
+    fl_a, fl_b = empty((B,), torch.uint8), empty((B,), torch.uint8)
+    cnt_a = torch.zeros((B,), dtype=torch.int32, device="cuda").view(torch.uint32)
+    cnt_b = torch.zeros((B,), dtype=torch.int32, device="cuda").view(torch.uint32)
+    st = [0] * B
+    for step in range(steps):
+        vals, x = logits_rows(V, range(B), step, 4, 2.0, 4.0, 0.05, dtype)
+        pda.fill_bitmask(cfg_a, bm_a)
+        ctx.mask_and_sample(x, bm_a, temp, top_p, seed, step, tok_a)
+        pda.accept(cfg_a, tok_a.view(torch.uint32), fl_a, counts=cnt_a, max_tokens=20)
+        pda.step(cfg_b, x, temp, top_p, seed, step, tok_b.view(torch.uint32), fl_b, counts=cnt_b, max_tokens=20,
+                 bitmask=bm_b)
+        assert ctx.status() == 0
+        g_bm = host(bm_a).view(np.uint32)
+        assert np.array_equal(g_bm, host(bm_b).view(np.uint32)), step
+        assert np.array_equal(host(tok_a), host(tok_b)), step
+        assert np.array_equal(host(fl_a), host(fl_b)), step
+        assert np.array_equal(host(cfg_a), host(cfg_b)), step
+        assert np.array_equal(host(cnt_a), host(cnt_b)), step
+        if orc is not None:
+            g_tok, g_fl = host(tok_a).view(np.uint32), host(fl_a)
+            for b in range(B):
+                assert np.array_equal(g_bm[b], orc.mask(st[b])), (step, b)
+                t = int(g_tok[b])
+                s, f = (st[b], 8) if t == NO_TOKEN else accept(orc.dfa, st[b], t, toks, False)
+                st[b] = 0 if g_fl[b] & (FLAG_DONE | 16) else s
