@@ -368,7 +368,7 @@ def run_ours(args) -> dict | None:
         "accept_many_mean_accepted": round(am_accepted, 3),
         "pushdown": pda_out,
         "host_eval_us_per_call": host_eval,
-        "roofline": {"kernel": "stream_topp_kernel<true> (cg_step)", "bound": "hbm",
+        "roofline": {"kernel": "stream_topp_kernel<1> (cg_step)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "peak_source": f"{peaks['source']} (copy bandwidth)",
