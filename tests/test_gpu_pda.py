@@ -20,7 +20,8 @@ oracle of the same grammar flattened under the same stack bound.
 * edge cases: an empty batch, malformed configurations, refused and
   out-of-range tokens, a forced token that differs from the sampled one;
 * cg_pda_accept_fill equals cg_pda_accept followed by cg_pda_fill_bitmask;
-* cg_pda_step (the fused pushdown step) equals the three calls.
+* cg_pda_step (the fused pushdown step) equals the three calls, with and
+  without forced rows.
 """
 
 import json
@@ -408,3 +409,57 @@ def test_pda_step_equals_the_three_calls(dtype, V, B, D):
                 t = int(g_tok[b])
                 s, f = (st[b], 8) if t == NO_TOKEN else accept(orc.dfa, st[b], t, toks, False)
                 st[b] = 0 if g_fl[b] & (FLAG_DONE | 16) else s
+
+
+def test_pda_step_with_forced_rows_equals_the_three_calls():
+    """The fused step's forced rows: where the oracle's state continues only
+    with injected bytes the row gets a forced single-byte token; cg_pda_step
+    and the three calls give the same ids, flags, configurations and masks,
+    and the flags are the oracle's."""
+    import torch
+    D, V, B, steps = 4, 4096, 64, 40
+    temp, top_p, seed = 0.7, 0.9, 9
+    toks = vocab("bpe", V)
+    orc = OracleRows(MIXED, D, toks)
+    ctx, pda = _pda(MIXED, D, V)
+    single = {t[0]: i for i, t in enumerate(toks) if len(t) == 1}
+    rng = np.random.default_rng(21)
+    W = (V + 31) // 32
+    cfg_a, cfg_b = _fresh(B, D), _fresh(B, D)
+    bm_a, bm_b = empty((B, W), torch.int32), empty((B, W), torch.int32)
+    tok_a, tok_b = empty((B,), torch.int32), empty((B,), torch.int32)
+    fl_a, fl_b = empty((B,), torch.uint8), empty((B,), torch.uint8)
+    st = [0] * B
+    n_forced = 0
+    for step in range(steps):
+        forced = np.full(B, -1, np.int32)
+        for b in range(B):
+            s = st[b]
+            if s != DEAD and (orc.dfa.next[s, :256] < 0).all() and (orc.dfa.next[s, 256:] >= 0).any():
+                live = np.flatnonzero(orc.dfa.next[s, 256:] >= 0)
+                forced[b] = single[int(live[rng.integers(live.size)])]
+        n_forced += int((forced >= 0).sum())
+        f_d = u32(forced.view(np.uint32)).view(torch.int32)
+        vals, x = logits_rows(V, range(B), step, 6, 2.0, 4.0, 0.05, "bf16")
+        pda.fill_bitmask(cfg_a, bm_a, forced=f_d)
+        ctx.mask_and_sample(x, bm_a, temp, top_p, seed, step, tok_a)
+        pda.accept(cfg_a, tok_a.view(torch.uint32), fl_a, forced=f_d)
+        pda.step(cfg_b, x, temp, top_p, seed, step, tok_b.view(torch.uint32), fl_b, forced=f_d, bitmask=bm_b)
+        assert ctx.status() == 0
+        assert np.array_equal(host(bm_a), host(bm_b)), step
+        assert np.array_equal(host(tok_a), host(tok_b)), step
+        assert np.array_equal(host(fl_a), host(fl_b)), step
+        assert np.array_equal(host(cfg_a), host(cfg_b)), step
+        g_tok, g_fl = host(tok_a).view(np.uint32), host(fl_a)
+        for b in range(B):
+            t = int(g_tok[b])
+            s, f = (st[b], 8) if t == NO_TOKEN else accept(orc.dfa, st[b], t, toks, forced[b] >= 0)
+            assert g_fl[b] == f, (step, b, t)
+            st[b] = s
+        done = [b for b in range(B) if g_fl[b] & FLAG_DONE]
+        if done:
+            cfg_a.view(torch.int32)[done] = 0
+            cfg_b.view(torch.int32)[done] = 0
+            for b in done:
+                st[b] = 0
+    assert n_forced > 20
