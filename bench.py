@@ -473,6 +473,26 @@ def _bench_pushdown(args, cg, ctx, vocab, stream, bufs, R, B, V, W, cfg, seed) -
     t_restore = timed(restore, 200)
     accept_us = timed(restore_accept, 200) - t_restore
     accept_fill_us = timed(restore_accept_fill, 200) - t_restore
+    # speculative verification (cg_pda_accept_many): drafts of K = 8 tokens from
+    # the rows' own next 8 fused steps, verified from the configurations before
+    # them (restored before every call)
+    K = 8
+    draft = torch.empty((B, K), dtype=torch.int32, device="cuda")
+    restore()
+    for j in range(K):
+        pstep(base + 10**5 + j, bufs[j % R])
+        draft[:, j] = tok
+    dlen = torch.full((B,), K, dtype=torch.int32, device="cuda").view(torch.uint32)
+    am_n = torch.empty(B, dtype=torch.int32, device="cuda").view(torch.uint32)
+    am_f = torch.empty(B, dtype=torch.uint8, device="cuda")
+    draft_u = draft.view(torch.uint32)
+
+    def restore_verify():
+        restore()
+        pda.accept_many(cfg_rows, draft_u, dlen, am_n, am_f, counts=counts, max_tokens=2048)
+
+    am_us = timed(restore_verify, 200) - t_restore
+    am_accepted = float(am_n.view(torch.int32).float().mean().item())
     if ctx.status() != 0:
         raise RuntimeError("device status after the pushdown steps")
     info, ginfo = pda.info(), pg.info()
@@ -497,6 +517,8 @@ def _bench_pushdown(args, cg, ctx, vocab, stream, bufs, R, B, V, W, cfg, seed) -
         "sample_us_alone": round(sample_us, 3),
         "accept_us_alone": round(accept_us, 3),
         "accept_fill_us_alone": round(accept_fill_us, 3),
+        "accept_many_us (drafts of 8 tokens from the next 8 steps)": round(am_us, 3),
+        "accept_many_mean_accepted": round(am_accepted, 3),
         "stack_level_after": {"mean": round(mean_level, 2), "max": max_level},
         "step_roofline": {"kernel": "stream_topp_kernel<2> (cg_pda_step)", "bound": "hbm",
                           "achieved": round(step_achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",

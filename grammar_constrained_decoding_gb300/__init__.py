@@ -332,6 +332,14 @@ class Pda:
             self._h, _ptr(cfg), B, _ptr(logits), dtype, V, float(temp), float(top_p), int(seed), int(step),
             _ptr(forced), _ptr(counts), int(max_tokens), _ptr(bitmask), _ptr(out_tok), _ptr(out_flags)))
 
+    def accept_many(self, cfg, draft, draft_len, out_n, out_flags, forced=None, counts=None,
+                    max_tokens: int = 0) -> None:
+        """Speculative verification of drafts [B, K] against the rows' configurations."""
+        B, K = draft.shape
+        L.check("cg_pda_accept_many", L.lib().cg_pda_accept_many(
+            self._h, _ptr(cfg), B, _ptr(draft), _ptr(draft_len), _ptr(forced), K, _ptr(counts), int(max_tokens),
+            _ptr(out_n), _ptr(out_flags)))
+
     def accept_fill(self, cfg, toks, out_flags, bitmask, forced=None, counts=None, max_tokens: int = 0,
                     forced_next=None) -> None:
         """accept, then fill_bitmask of the next step, in one launch."""

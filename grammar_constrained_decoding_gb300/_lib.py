@@ -97,6 +97,8 @@ SIGNATURES = {
     "cg_pda_fill_bitmask": (C.c_int, [C.c_void_p, C.c_void_p, C.c_uint32, C.c_void_p, C.c_void_p]),
     "cg_pda_accept": (C.c_int, [C.c_void_p, C.c_void_p, C.c_uint32, C.c_void_p, C.c_void_p, C.c_void_p,
                                 C.c_uint32, C.c_void_p]),
+    "cg_pda_accept_many": (C.c_int, [C.c_void_p, C.c_void_p, C.c_uint32, C.c_void_p, C.c_void_p, C.c_void_p,
+                                     C.c_uint32, C.c_void_p, C.c_uint32, C.c_void_p, C.c_void_p]),
     "cg_pda_step": (C.c_int, [C.c_void_p, C.c_void_p, C.c_uint32, C.c_void_p, C.c_int, C.c_uint32, C.c_float,
                               C.c_float, C.c_uint64, C.c_uint32, C.c_void_p, C.c_void_p, C.c_uint32, C.c_void_p,
                               C.c_void_p, C.c_void_p]),

@@ -141,6 +141,93 @@ __global__ void __launch_bounds__(kPdaAcceptThreads)
                                 max_tokens);
 }
 
+// Speculative verification of pushdown rows (cg_pda_accept_many), one thread
+// per row: the draft's tokens are walked one after another, each on an
+// overlay of the row's stack that is written back only when the token is
+// accepted, so a refused token leaves the accepted prefix's configuration.
+// The rules are those of cg_accept_many: stop at the first refused token
+// (CG_FLAG_DRAFT_CUT), after a token that ends the grammar, at the token cap,
+// or after a token whose configuration continues only with injected bytes when
+// the next position is not pinned.
+__global__ void __launch_bounds__(kPdaAcceptThreads)
+    pda_accept_many_kernel(DevPda p, Tables t, uint32_t* __restrict__ cfg, uint32_t B,
+                           const uint32_t* __restrict__ draft, const uint32_t* __restrict__ draft_len,
+                           const int32_t* __restrict__ forced, uint32_t K, uint32_t* counts, uint32_t max_tokens,
+                           uint32_t* __restrict__ out_n, uint8_t* __restrict__ out_flags) {
+  extern __shared__ __align__(16) uint4 sm4[];  // the walk tables, when they fit
+  griddep_launch_dependents();
+  const DevPda pv = p.tabs_in_smem ? tables_to_smem(p, sm4, threadIdx.x, blockDim.x) : p;
+  if (p.tabs_in_smem) __syncthreads();
+  griddep_wait();  // drafts and configurations come from earlier work on the stream
+  const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  uint32_t* row = cfg + size_t(b) * p.stride;
+  const uint32_t* toks = draft + size_t(b) * K;
+  const int32_t* fb = forced ? forced + size_t(b) * K : nullptr;
+  uint32_t q = row[0], lvl = row[1], n = draft_len[b];
+  uint32_t c = counts ? counts[b] : 0u, acc = 0;
+  uint8_t fl = 0;
+  if (n > K) {
+    record_error(t.status, CG_DEV_BAD_LENGTH);
+    n = K;
+  }
+  if (n == 0) {
+    fl = CG_FLAG_NO_TOKEN;
+  } else if (q == CG_DEAD) {
+    fl = CG_FLAG_REJECTED;
+  } else if (q >= p.S || lvl > p.depth) {
+    record_error(t.status, CG_DEV_BAD_STATE);
+    q = CG_DEAD;
+    fl = CG_FLAG_REJECTED;
+  } else {
+    RowStack rs{row + 2};
+    uint8_t cut = 0, capped = 0, sres = pda_flags(pv, q, lvl, rs);
+    int32_t f = fb ? fb[0] : -1;
+    for (uint32_t j = 0; j < n; ++j) {
+      const uint32_t tok = toks[j];
+      const int32_t f_next = (fb && j + 1 < n) ? fb[j + 1] : -1;
+      if (tok >= t.V) {
+        record_error(t.status, CG_DEV_BAD_TOKEN);
+        cut = CG_FLAG_DRAFT_CUT;
+        break;
+      }
+      OverlayStack st;
+      st.base = row + 2;
+      st.keep = lvl;
+      uint32_t qq = q, ll = lvl;
+      if ((f >= 0 && tok != uint32_t(f)) || !pda_walk(pv, t, tok, f >= 0 ? 256u : 0u, qq, ll, st)) {
+        cut = CG_FLAG_DRAFT_CUT;
+        break;
+      }
+      for (uint32_t i = st.keep; i < ll; ++i) row[2 + i] = st.local[i];  // the token's pushes
+      q = qq;
+      lvl = ll;
+      ++acc;
+      ++c;
+      sres = pda_flags(pv, q, lvl, rs);
+      if (sres & CG_FLAG_DONE) break;
+      if (counts && c >= max_tokens) {
+        capped = CG_FLAG_CAPPED;
+        break;
+      }
+      if ((sres & CG_FLAG_FORCED_NEXT) && f_next < 0) break;
+      f = f_next;
+    }
+    fl = sres | cut | capped;
+    if (counts && acc > 0 && (fl & (CG_FLAG_DONE | CG_FLAG_CAPPED))) {
+      q = 0u;
+      lvl = 0u;
+      c = 0u;
+    }
+  }
+  if (q == CG_DEAD) lvl = 0;
+  if (counts) counts[b] = c;
+  row[0] = q;
+  row[1] = lvl;
+  out_n[b] = acc;
+  out_flags[b] = fl;
+}
+
 // Accept of this step and fill of the next in one block per row: thread 0
 // advances the row, the block then fills its next mask from the new
 // configuration (the __syncthreads between them orders the row's global
@@ -339,7 +426,9 @@ int cg_pda_create(cg_ctx* c, const cg_vocab* v, const cg_pda_grammar* g, cg_pda*
   if (cgk::allow_smem(reinterpret_cast<const void*>(cgk::pda_fill_kernel), pda_fill_smem(d, W)) != cudaSuccess ||
       cgk::allow_smem(reinterpret_cast<const void*>(cgk::pda_accept_fill_kernel), pda_fill_smem(d, W)) !=
           cudaSuccess ||
-      cgk::allow_smem(reinterpret_cast<const void*>(cgk::pda_accept_kernel), pda_accept_smem(d)) != cudaSuccess) {
+      cgk::allow_smem(reinterpret_cast<const void*>(cgk::pda_accept_kernel), pda_accept_smem(d)) != cudaSuccess ||
+      cgk::allow_smem(reinterpret_cast<const void*>(cgk::pda_accept_many_kernel), pda_accept_smem(d)) !=
+          cudaSuccess) {
     pda_release(p);
     delete p;
     return CG_E_CUDA;
@@ -385,6 +474,20 @@ int cg_pda_accept(cg_pda* p, uint32_t* d_cfg, uint32_t B, const uint32_t* d_toks
                                pda_accept_smem(p->d), p->stream,
                                p->d, p->t, d_cfg, B, d_toks, d_forced, d_counts, max_tokens, d_out_flags) ==
                  cudaSuccess
+             ? CG_OK
+             : CG_E_CUDA;
+}
+
+int cg_pda_accept_many(cg_pda* p, uint32_t* d_cfg, uint32_t B, const uint32_t* d_draft, const uint32_t* d_draft_len,
+                       const int32_t* d_forced, uint32_t K, uint32_t* d_counts, uint32_t max_tokens,
+                       uint32_t* d_out_n, uint8_t* d_out_flags) {
+  if (!p || (B && (!d_cfg || !d_draft || !d_draft_len || !d_out_n || !d_out_flags || K == 0))) return CG_E_ARG;
+  if (d_counts && max_tokens == 0) return CG_E_ARG;
+  if (B == 0) return CG_OK;
+  const uint32_t grid = (B + cgk::kPdaAcceptThreads - 1) / cgk::kPdaAcceptThreads;
+  return cgk::launch_dependent(cgk::pda_accept_many_kernel, dim3(grid), dim3(cgk::kPdaAcceptThreads),
+                               pda_accept_smem(p->d), p->stream, p->d, p->t, d_cfg, B, d_draft, d_draft_len, d_forced,
+                               K, d_counts, max_tokens, d_out_n, d_out_flags) == cudaSuccess
              ? CG_OK
              : CG_E_CUDA;
 }

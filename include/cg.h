@@ -460,6 +460,18 @@ int cg_pda_fill_bitmask(cg_pda* p, const uint32_t* d_cfg, uint32_t B, const int3
 int cg_pda_accept(cg_pda* p, uint32_t* d_cfg, uint32_t B, const uint32_t* d_toks, const int32_t* d_forced,
                   uint32_t* d_counts, uint32_t max_tokens, uint8_t* d_out_flags);
 
+/* Speculative verification for pushdown rows, as cg_accept_many is for
+ * automaton rows (same draft, pin, count and stopping rules and the same
+ * flags): d_cfg u32 [B][depth + 2] is updated in place to the configuration
+ * after the accepted prefix (a refused token leaves it unchanged); d_draft
+ * u32 [B][K], d_draft_len u32 [B], d_forced i32 [B][K] or NULL, d_out_n u32 [B]
+ * tokens accepted, d_out_flags u8 [B].  No path output: a pushdown
+ * configuration is a stack, not one word.  Errors: CG_E_ARG for a NULL required
+ * pointer, K == 0 with B > 0, or d_counts with max_tokens == 0. */
+int cg_pda_accept_many(cg_pda* p, uint32_t* d_cfg, uint32_t B, const uint32_t* d_draft, const uint32_t* d_draft_len,
+                       const int32_t* d_forced, uint32_t K, uint32_t* d_counts, uint32_t max_tokens,
+                       uint32_t* d_out_n, uint8_t* d_out_flags);
+
 /* The whole step for pushdown rows, as cg_step is for automaton rows: the
  * mask of each row (as cg_pda_fill_bitmask, into d_bitmask too when it is not
  * NULL), masked sampling (as cg_mask_and_sample, same arguments) and the
