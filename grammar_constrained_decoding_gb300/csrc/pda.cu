@@ -24,7 +24,6 @@
 
 namespace cgk {
 
-
 constexpr uint32_t kPdaFillThreads = 256;
 constexpr uint32_t kPdaVec = 8;  // uint4s of the row's mask a fill thread holds in registers
 
@@ -103,7 +102,6 @@ __device__ void pda_fill_row(const DevPda& p, const DevPda& pv, const Tables& t,
     for (uint32_t w = tid; w < W; w += blockDim.x) out[w] = src[w] | bits[w];
   }
 }
-
 
 // shared memory of a fill block: [tables (when they fit)] [W bits] [the row's stack]
 __device__ __forceinline__ uint32_t* fill_bits(const DevPda& p, uint4* sm4) {
