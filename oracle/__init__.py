@@ -8,7 +8,7 @@ bug...") and from the published Philox4x32-10 definition (Salmon, Moraes, Dror,
 Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC'11).
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
-leg may import anything under ``oracle/``.  The product path never does, and
+and reference legs may import anything under ``oracle/``.  The product path never does, and
 this package shares no code with it: the grammar front-ends, the automaton
 construction (Brzozowski derivatives + Moore minimisation here, against the
 product's NFA/subset/Hopcroft pipeline), the mask walk, the sampler, the
@@ -25,7 +25,10 @@ Modules
   step       token mask, sampler (temperature, softmax, top-p, Gumbel-max),
              accept.
   evaluator  exact-rational arithmetic evaluator and greedy forced tokeniser.
+  strops     string operations of the <strop> evaluator.
   driver     host rules around the step (reset, forced queue, token cap).
+  pda        recursive grammars under a stack bound: the flattened language
+             whose automaton the pushdown path is checked against.
 
 Parity pins (tests/test_oracle_*.py) tie every function to something other
 than itself; there is no function here whose parity is unpinned.
