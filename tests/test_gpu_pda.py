@@ -241,12 +241,14 @@ def _frames(v):
     return 1
 
 
-def test_deep_stack_texts_are_json_within_the_bound():
+@pytest.mark.parametrize("D,steps", [(32, 120), (64, 220)])
+def test_deep_stack_texts_are_json_within_the_bound(D, steps):
     """Rows open arrays while they may, then close: the stack reaches its
-    bound, where the device refuses "[" outside strings, and every finished
-    text is JSON whose frame count fits the bound."""
+    bound (up to the largest, CG_PDA_MAX_DEPTH = 64), where the device refuses
+    "[" outside strings, and every finished text is JSON whose frame count fits
+    the bound."""
     import torch
-    D, V, B, steps = 32, 32000, 64, 120
+    V, B = 32000, 64
     toks = vocab("bpe", V)
     ctx, pda = _pda(JSON_NESTED, D, V)
     W = (V + 31) // 32
