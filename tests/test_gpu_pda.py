@@ -21,7 +21,9 @@ oracle of the same grammar flattened under the same stack bound.
   out-of-range tokens, a forced token that differs from the sampled one;
 * cg_pda_accept_fill equals cg_pda_accept followed by cg_pda_fill_bitmask;
 * cg_pda_step (the fused pushdown step) equals the three calls, with and
-  without forced rows.
+  without forced rows;
+* random walks on two more grammar shapes: one whose open nodes need headroom
+  to complete, one whose start rule is itself recursive.
 """
 
 import json
@@ -465,3 +467,56 @@ def test_pda_step_with_forced_rows_equals_the_three_calls():
             for b in done:
                 st[b] = 0
     assert n_forced > 20
+
+
+TREE = r'''
+root ::= node "."
+node ::= "(" node "," node ")" | [a-c]+
+'''
+ROOTED = r'''
+root ::= "[" ( root ( ";" root )* )? "]" | "x"
+'''
+
+
+@pytest.mark.parametrize("source,D", [(TREE, 3), (TREE, 6), (ROOTED, 3), (ROOTED, 5)])
+def test_other_grammar_shapes_match_the_oracle(source, D):
+    """Random walks on a grammar whose open nodes need headroom to complete
+    (a node opened deep must still fit its second child) and on one whose
+    start rule is itself recursive (the base frame and called frames share the
+    rule): masks and flags bit for bit against the oracle."""
+    import torch
+    V, B, steps = 4096, 96, 30
+    toks = vocab("bpe", V)
+    orc = OracleRows(source, D, toks)
+    ctx, pda = _pda(source, D, V)
+    rng = np.random.default_rng(D + len(source))
+    W = (V + 31) // 32
+    cfg = _fresh(B, D)
+    bm = empty((B, W), torch.int32)
+    flags = empty((B,), torch.uint8)
+    opens = np.array([t.count(b"(") + t.count(b"[") for t in toks])
+    st = [0] * B
+    max_level = 0
+    for step in range(steps):
+        pda.fill_bitmask(cfg, bm)
+        g_bm = host(bm).view(np.uint32)
+        pick = np.empty(B, np.uint32)
+        for b in range(B):
+            want = orc.mask(st[b])
+            assert np.array_equal(g_bm[b], want), (step, b)
+            pick[b] = _pick(rng, want, V, opens, 0.4)
+        pda.accept(cfg, u32(pick), flags)
+        assert ctx.status() == 0
+        g_fl, g_cfg = host(flags), host(cfg).view(np.uint32)
+        for b in range(B):
+            t = int(pick[b])
+            s, f = (st[b], 8) if t == NO_TOKEN else accept(orc.dfa, st[b], t, toks, False)
+            assert g_fl[b] == f, (step, b, t)
+            st[b] = s
+            max_level = max(max_level, int(g_cfg[b, 1]))
+        done = [b for b in range(B) if g_fl[b] & (FLAG_DONE | 8)]
+        if done:
+            cfg.view(torch.int32)[done] = 0
+            for b in done:
+                st[b] = 0
+    assert max_level >= min(D, 3)
