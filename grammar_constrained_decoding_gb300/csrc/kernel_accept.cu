@@ -14,12 +14,19 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(Tables t, const 
                                                                 const int32_t* __restrict__ forced, uint32_t B,
                                                                 uint32_t* counts, uint32_t max_tokens,
                                                                 uint32_t* out_states, uint8_t* out_flags) {
+  // the column map in shared memory when every row uses one grammar (the
+  // tables are static: copied before the wait for the sampled tokens)
+  __shared__ uint16_t scol[512];
   griddep_launch_dependents();
+  const bool staged = gid == nullptr || t.n_g == 1;
+  if (staged)
+    for (uint32_t i = threadIdx.x; i < 512; i += blockDim.x) scol[i] = t.colmap[i];
+  __syncthreads();
   griddep_wait();  // the tokens come from the sampling kernel
   const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   accept_row(t, b, gid ? gid[b] : 0u, states[b], toks[b], forced ? forced[b] : -1, counts, max_tokens, out_states,
-             out_flags);
+             out_flags, staged ? scol : nullptr);
 }
 
 cudaError_t launch_accept(const Tables& t, const uint32_t* states, const uint16_t* gid, const uint32_t* toks,
