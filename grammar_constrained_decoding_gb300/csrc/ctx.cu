@@ -11,7 +11,7 @@
 
 namespace cgk {
 cudaError_t launch_fill_bitmask(const Tables& t, const uint32_t* states, const uint16_t* gid, const int32_t* forced,
-                                uint32_t B, uint32_t* bitmask, cudaStream_t stream);
+                                uint32_t B, uint32_t* bitmask, bool cache_complete, cudaStream_t stream);
 size_t fill_bitmask_smem(uint32_t W);
 cudaError_t launch_prefill(const Tables& t, const uint32_t* class_rep, const uint16_t* class_gid, cudaStream_t stream);
 cudaError_t launch_mask_and_sample(void* logits, int dtype, uint32_t B, uint32_t V, uint32_t W,
@@ -327,7 +327,8 @@ int cg_ctx_prefill(cg_ctx* c) {
 int cg_fill_bitmask(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const int32_t* d_forced, uint32_t B,
                     uint32_t* d_bitmask) {
   if (!c || (B && (!d_states || !d_bitmask))) return CG_E_ARG;
-  return cgk::launch_fill_bitmask(c->t, d_states, d_gid, d_forced, B, d_bitmask, c->stream) == cudaSuccess
+  return cgk::launch_fill_bitmask(c->t, d_states, d_gid, d_forced, B, d_bitmask, c->cache_complete, c->stream) ==
+                 cudaSuccess
              ? CG_OK
              : CG_E_CUDA;
 }

@@ -20,7 +20,8 @@ constexpr int kFillThreads = 512;
 __global__ void __launch_bounds__(kFillThreads) fill_bitmask_kernel(Tables t, const uint32_t* __restrict__ states,
                                                                       const uint16_t* __restrict__ gid,
                                                                       const int32_t* __restrict__ forced,
-                                                                      uint32_t* __restrict__ bitmask) {
+                                                                      uint32_t* __restrict__ bitmask,
+                                                                      uint32_t cache_complete) {
   extern __shared__ uint32_t smem[];
   uint32_t* smask = smem;                                   // [W]
   uint16_t* scol = reinterpret_cast<uint16_t*>(smem + t.W); // [256] model-byte columns
@@ -46,10 +47,13 @@ __global__ void __launch_bounds__(kFillThreads) fill_bitmask_kernel(Tables t, co
   const DevGrammar gd = t.grammars[g];
   const uint32_t cls = t.class_of[gd.state_off + s];
   const uint32_t* crow = t.cache + size_t(cls) * W;
-  // one thread reads the flag so that the whole block takes the same path
-  if (threadIdx.x == 0) s_ready = load_acquire(t.cache_state + cls) == kStateReady;
-  __syncthreads();
-  if (s_ready) {
+  // one thread reads the flag so that the whole block takes the same path;
+  // after cg_ctx_prefill every class is ready and the flag is not read
+  if (!cache_complete) {
+    if (threadIdx.x == 0) s_ready = load_acquire(t.cache_state + cls) == kStateReady;
+    __syncthreads();
+  }
+  if (cache_complete || s_ready) {
     if ((W & 3u) == 0) {
       const uint4* src = reinterpret_cast<const uint4*>(crow);
       uint4* dst = reinterpret_cast<uint4*>(out);
@@ -111,11 +115,11 @@ cudaError_t launch_prefill(const Tables& t, const uint32_t* class_rep, const uin
 }
 
 cudaError_t launch_fill_bitmask(const Tables& t, const uint32_t* states, const uint16_t* gid, const int32_t* forced,
-                                uint32_t B, uint32_t* bitmask, cudaStream_t stream) {
+                                uint32_t B, uint32_t* bitmask, bool cache_complete, cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
   const size_t smem = size_t(t.W) * 4 + 256 * 2;
   return launch_dependent(fill_bitmask_kernel, dim3(B), dim3(kFillThreads), smem, stream, t, states, gid, forced,
-                          bitmask);
+                          bitmask, cache_complete ? 1u : 0u);
 }
 
 size_t fill_bitmask_smem(uint32_t W) { return size_t(W) * 4 + 256 * 2; }
