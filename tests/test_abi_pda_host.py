@@ -11,6 +11,7 @@ recursive rules matching the empty string, two actions for one byte, a rule
 that may both end and continue on a byte, recursion inside @forced or '&').
 """
 
+import ctypes as C
 import random
 
 import numpy as np
@@ -176,3 +177,23 @@ e ::= "(" e ")"''', 4)
     assert ei.value.code == L.CG_E_EMPTY
     with pytest.raises(GrammarError):
         compile_pda(JSON_NESTED, 0)
+
+
+def test_device_entry_points_refuse_missing_handles_without_a_gpu():
+    """The pushdown device calls check their arguments on the host before any
+    CUDA call: a NULL object or a NULL required buffer is CG_E_ARG."""
+    lib = L.lib()
+    dummy = 16  # a non-null address the calls must not reach
+    assert lib.cg_pda_fill_bitmask(None, dummy, 4, None, dummy) == L.CG_E_ARG
+    assert lib.cg_pda_accept(None, dummy, 4, dummy, None, None, 0, dummy) == L.CG_E_ARG
+    assert lib.cg_pda_accept_fill(None, dummy, 4, dummy, None, None, 0, dummy, None, dummy) == L.CG_E_ARG
+    assert lib.cg_pda_accept_many(None, dummy, 4, dummy, dummy, None, 8, None, 0, dummy, dummy) == L.CG_E_ARG
+    assert lib.cg_pda_step(None, dummy, 4, dummy, L.CG_BF16, 4096, 0.7, 0.9, 1, 0, None, None, 0, None, dummy,
+                           dummy) == L.CG_E_ARG
+    assert lib.cg_pda_create(None, None, None, None) == L.CG_E_ARG
+    assert lib.cg_pda_info(None, None, None, None, None) == L.CG_E_ARG
+    assert lib.cg_pda_grammar_info(None, None, None, None, None) == L.CG_E_ARG
+    n, acc = C.c_size_t(), C.c_int()
+    assert lib.cg_pda_try_input(None, b"x", 1, None, C.byref(n), C.byref(acc), None) == L.CG_E_ARG
+    lib.cg_pda_destroy(None)
+    lib.cg_pda_grammar_destroy(None)
