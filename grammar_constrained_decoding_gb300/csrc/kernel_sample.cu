@@ -319,7 +319,12 @@ static_assert(kBins == kThreads, "one histogram bin per thread in the scans");
 // after the stream the ring holds the histograms, then the packed nucleus
 constexpr uint32_t kHistBytes = kHists * kBins * 8;
 constexpr uint32_t kNucCap = (kRing - kHistBytes) / 6;          // packed nucleus entries (u32 id + u16 key)
-constexpr float kMarginZ = 9.0f;                                // nats below the maximum kept as candidates
+// nats below the maximum kept as candidates: a row whose top-p boundary lies
+// deeper takes the general path (same result, one more pass over the row).
+// Where a few percent of the tokens carry most of the mass the boundary lies
+// within about 7.2 nats of the maximum; flat rows (Gaussian logits over tens
+// of thousands of tokens, no dominant ones) can reach past 9.
+constexpr float kMarginZ = 8.5f;
 constexpr float kNoRef = -1e30f;                                // finite reference before any allowed logit
 constexpr uint32_t kMaxCols = 512;                              // symbol columns a grammar can have
 constexpr uint32_t kWinRowsMax = 512;                           // states in the accept's table window
