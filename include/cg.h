@@ -17,8 +17,8 @@
  *    detected on the host before anything is launched.
  *  - Ownership: pointers named d_* are device pointers owned by the caller;
  *    h_* and plain pointers are host memory owned by the caller.  Opaque
- *    objects (cg_grammar, cg_vocab, cg_ctx, cg_driver) are owned by the
- *    library and released by their *_destroy call.
+ *    objects (cg_grammar, cg_vocab, cg_ctx, cg_driver, cg_pda_grammar, cg_pda)
+ *    are owned by the library and released by their *_destroy call.
  *  - Asynchrony: the three step calls only enqueue kernels on the context's
  *    CUDA stream and return; results are ready after the stream is
  *    synchronised.  Errors that only the device can see (a state or token id
