@@ -185,6 +185,13 @@ class Ctx:
     def prefill(self) -> None:
         L.check("cg_ctx_prefill", L.lib().cg_ctx_prefill(self._h))
 
+    def cache_stats(self) -> dict:
+        """Mask-class lookups and class masks computed by the fused step's miss
+        path since the context was created (synchronises the stream)."""
+        lk, cm = C.c_uint64(), C.c_uint64()
+        L.check("cg_ctx_cache_stats", L.lib().cg_ctx_cache_stats(self._h, C.byref(lk), C.byref(cm)))
+        return {"lookups": lk.value, "computed": cm.value}
+
     def fill_bitmask(self, states, bitmask, gid=None, forced=None) -> None:
         B = states.shape[0]
         L.check("cg_fill_bitmask", L.lib().cg_fill_bitmask(self._h, _ptr(states), _ptr(gid), _ptr(forced), B,
@@ -219,8 +226,8 @@ class Ctx:
 
     def step(self, states, logits, temp: float, top_p: float, seed: int, step: int, out_tok, out_states, out_flags,
              gid=None, forced=None, counts=None, max_tokens: int = 2048, bitmask=None) -> None:
-        """fill_bitmask + mask_and_sample + accept in one call (one kernel on the
-        top-p bf16 path); bitmask, when given, receives the row masks."""
+        """fill_bitmask + mask_and_sample + accept in one call (one segmented
+        kernel for bf16 logits); bitmask, when given, receives the row masks."""
         import torch
         dtype = {torch.float32: L.CG_F32, torch.bfloat16: L.CG_BF16}[logits.dtype]
         B, V = logits.shape

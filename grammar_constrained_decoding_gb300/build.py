@@ -22,8 +22,8 @@ LIB = os.path.join(OUT_DIR, "libcg.so")
 
 CXX_SOURCES = ["compiler/gbnf.cpp", "compiler/schema.cpp", "compiler/structtag.cpp", "compiler/automaton.cpp",
                "compiler/pda.cpp", "grammar.cpp", "evaluator.cpp"]
-CU_SOURCES = ["ctx.cu", "kernel_mask.cu", "kernel_sample.cu", "kernel_accept.cu", "pda.cu"]
-HEADERS = ["compiler/ir.h", "compiler/json.h", "cg_internal.h", "device.cuh", "row_ops.cuh", "pda.cuh"]
+CU_SOURCES = ["ctx.cu", "kernel_mask.cu", "kernel_sample.cu", "kernel_seg.cu", "kernel_accept.cu", "pda.cu"]
+HEADERS = ["compiler/ir.h", "compiler/json.h", "cg_internal.h", "device.cuh", "row_ops.cuh", "pda.cuh", "bf16_ops.cuh"]
 GENCODE = "arch=compute_103a,code=sm_103a"
 
 

@@ -19,12 +19,6 @@ cudaError_t launch_mask_and_sample(void* logits, int dtype, uint32_t B, uint32_t
                                    uint32_t* out_tok, float* probs, int inplace, void* scratch, uint32_t* status,
                                    cudaStream_t stream);
 size_t sample_scratch_bytes(uint32_t B, uint32_t V);
-bool step_fusable(int dtype, uint32_t V, uint32_t W, float temp, float top_p, const void* logits);
-cudaError_t launch_step(const Tables& t, const uint32_t* states, const uint16_t* gid, const int32_t* forced,
-                        uint32_t B, void* logits, uint32_t V, float temp, float top_p, uint64_t seed, uint32_t step,
-                        uint32_t* counts, uint32_t max_tokens, uint32_t* bitmask_out, uint32_t* out_tok,
-                        uint32_t* out_states, uint8_t* out_flags, void* scratch, const DevGrammar* host_grammars,
-                        bool cache_complete, cudaStream_t stream);
 cudaError_t launch_accept(const Tables& t, const uint32_t* states, const uint16_t* gid, const uint32_t* toks,
                           const int32_t* forced, uint32_t B, uint32_t* counts, uint32_t max_tokens,
                           uint32_t* out_states, uint8_t* out_flags, cudaStream_t stream);
@@ -33,6 +27,19 @@ cudaError_t launch_accept_many(const Tables& t, const uint32_t* states, const ui
                                uint32_t* counts, uint32_t max_tokens, uint32_t* out_states, uint32_t* out_n,
                                uint8_t* out_flags, uint32_t* path, cudaStream_t stream);
 cudaError_t launch_wait_timeout_self_test(uint32_t* status, cudaStream_t stream);
+cudaError_t launch_cache_fill(const Tables& t, const uint32_t* states, const uint16_t* gid, const int32_t* forced,
+                              uint32_t B, unsigned long long* stats, cudaStream_t stream);
+size_t seg_scratch_bytes(uint32_t B);
+bool seg_usable(int dtype, uint32_t V, const void* logits, float* probs, int inplace);
+bool seg_bitmask_ok(uint32_t W, const void* bitmask);
+cudaError_t launch_seg_sample(const void* logits, uint32_t B, uint32_t V, uint32_t W, const uint32_t* bitmask,
+                              float temp, float top_p, uint64_t seed, uint32_t step, uint32_t* out_tok,
+                              void* scratch, uint32_t* status, cudaStream_t stream);
+cudaError_t launch_seg_step(const Tables& t, const uint32_t* states, const uint16_t* gid, const int32_t* forced,
+                            uint32_t B, const void* logits, uint32_t V, float temp, float top_p, uint64_t seed,
+                            uint32_t step, uint32_t* counts, uint32_t max_tokens, uint32_t* bitmask_out,
+                            uint32_t* out_tok, uint32_t* out_states, uint8_t* out_flags, void* scratch,
+                            const DevGrammar* host_grammars, cudaStream_t stream);
 }  // namespace cgk
 
 struct cg_ctx {
@@ -43,8 +50,11 @@ struct cg_ctx {
   uint64_t cache_bytes = 0;
   const uint32_t* class_rep = nullptr;   // representative state of each mask class
   const uint16_t* class_gid = nullptr;   // grammar of each mask class
-  void* sample_scratch = nullptr;        // candidate lists of the sampling kernel
+  void* sample_scratch = nullptr;        // candidate lists of the per-row sampling kernels
   size_t sample_scratch_bytes = 0;
+  void* seg_scratch = nullptr;           // the segmented sampler's counters, row accumulators and histograms
+  size_t seg_scratch_bytes = 0;          // (zero when allocated; every launch leaves it at zero)
+  unsigned long long* cache_stats = nullptr;  // [0] class lookups, [1] classes computed, by the fused step's miss path
   uint32_t* step_bitmask = nullptr;      // bitmask of cg_step's unfused path when the caller gives none
   size_t step_bitmask_bytes = 0;
   std::vector<cgk::DevGrammar> grammars; // host copy of t.grammars
@@ -83,6 +93,9 @@ void release(cg_ctx* c) {
   if (c->sample_scratch) cudaFree(c->sample_scratch);
   c->sample_scratch = nullptr;
   c->sample_scratch_bytes = 0;
+  if (c->seg_scratch) cudaFree(c->seg_scratch);
+  c->seg_scratch = nullptr;
+  c->seg_scratch_bytes = 0;
   if (c->step_bitmask) cudaFree(c->step_bitmask);
   c->step_bitmask = nullptr;
   c->step_bitmask_bytes = 0;
@@ -114,9 +127,18 @@ int grow(cg_ctx* c, void** buf, size_t* have, size_t need) {
   return CG_OK;
 }
 
+// grow() for the segmented sampler's scratch, which must start at zero
+int grow_zeroed(cg_ctx* c, void** buf, size_t* have, size_t need) {
+  if (need <= *have) return CG_OK;
+  const int rc = grow(c, buf, have, need);
+  if (rc != CG_OK) return rc;
+  return cudaMemsetAsync(*buf, 0, need, c->stream) == cudaSuccess ? CG_OK : CG_E_CUDA;
+}
+
 }  // namespace
 
 namespace cgk {
+int ctx_device(const cg_ctx* c) { return c->device; }
 int ctx_sample_scratch(cg_ctx* c, size_t bytes, void** out) {
   const int rc = grow(c, &c->sample_scratch, &c->sample_scratch_bytes, bytes);
   *out = c->sample_scratch;
@@ -124,17 +146,22 @@ int ctx_sample_scratch(cg_ctx* c, size_t bytes, void** out) {
 }
 }  // namespace cgk
 
-// Scratch of cg_mask_and_sample_noalloc: the candidate lists of up to
-// CG_NOALLOC_MAX_ROWS rows (u32 ids, then u16 keys), fixed in the module so
-// that the call never allocates.  Its callers are the ones that must not touch
-// the allocator while decoding: cudaMalloc/cudaFree synchronise the device and
-// can fail once a server has planned all of its memory at start-up.  Shared by
-// every call on a device (calls that may overlap race on it).
-constexpr size_t kNoAllocScratchBytes = size_t(CG_NOALLOC_MAX_ROWS) * 8192 * 6;
+// Scratch of cg_mask_and_sample_noalloc, fixed in the module so that the
+// call never allocates: the per-row sampler's candidate lists of up to
+// CG_NOALLOC_MAX_ROWS rows (u32 ids, then u16 keys), then the segmented
+// sampler's counters and row blocks for as many rows.  Its callers are the
+// ones that must not touch the allocator while decoding: cudaMalloc/cudaFree
+// synchronise the device and can fail once a server has planned all of its
+// memory at start-up.  Shared by every call on a device (calls that may
+// overlap race on it).
+constexpr size_t kNoAllocListBytes = size_t(CG_NOALLOC_MAX_ROWS) * 8192 * 6;
+constexpr size_t kNoAllocSegBytes = size_t(3) << 20;  // 3 MiB
+constexpr size_t kNoAllocScratchBytes = kNoAllocListBytes + kNoAllocSegBytes;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace {
-// device address of g_noalloc_scratch, looked up once per device
+// device address of g_noalloc_scratch on the current device, looked up once
+// per device (the caller makes the context's device current first)
 void* noalloc_scratch(cudaError_t* err) {
   static std::mutex mu;
   static void* addr[64] = {};
@@ -154,6 +181,27 @@ void* noalloc_scratch(cudaError_t* err) {
   }
   return addr[dev];
 }
+
+bool sample_args_ok(const cg_ctx* c, void* d_logits, int dtype, uint32_t B, uint32_t V, const uint32_t* d_bitmask,
+                    float temp, float top_p, uint32_t* d_out_tok, uint32_t flags) {
+  if (!c || (B && (!d_logits || !d_bitmask || !d_out_tok))) return false;
+  if (dtype != CG_F32 && dtype != CG_BF16) return false;
+  if (V != c->t.V || !(temp >= 0.f) || temp == INFINITY || !(top_p == top_p)) return false;
+  return (flags & ~CG_SAMPLE_INPLACE) == 0;
+}
+
+// cg_mask_and_sample on the given scratch: the segmented sampler (needs
+// `seg` zero) or the per-row kernels (`lists`)
+int sample_on(cg_ctx* c, void* d_logits, int dtype, uint32_t B, uint32_t V, const uint32_t* d_bitmask, float temp,
+              float top_p, uint64_t seed, uint32_t step, uint32_t* d_out_tok, float* d_probs, int inplace,
+              bool seg_path, void* lists, void* seg) {
+  const cudaError_t e =
+      seg_path ? cgk::launch_seg_sample(d_logits, B, V, c->t.W, d_bitmask, temp, top_p, seed, step, d_out_tok, seg,
+                                        c->t.status, c->stream)
+               : cgk::launch_mask_and_sample(d_logits, dtype, B, V, c->t.W, d_bitmask, temp, top_p, seed, step,
+                                             d_out_tok, d_probs, inplace, lists, c->t.status, c->stream);
+  return e == cudaSuccess ? CG_OK : CG_E_CUDA;
+}
 }  // namespace
 
 extern "C" {
@@ -166,7 +214,7 @@ int cg_ctx_create(const cg_grammar* const* g, uint32_t n_g, const cg_vocab* v, v
   if (!c) return CG_E_NOMEM;
   c->stream = static_cast<cudaStream_t>(cuda_stream);
   cudaGetDevice(&c->device);
-  const uint32_t V = v->V, W = (V + 31) / 32;
+  const uint32_t V = v->V, W = (V + 31) / 32, Wc = (W + 3) & ~3u;
 
   std::vector<cgk::DevGrammar> gdesc(n_g);
   std::vector<uint32_t> table;
@@ -250,15 +298,20 @@ int cg_ctx_create(const cg_grammar* const* g, uint32_t n_g, const cg_vocab* v, v
     return CG_E_CUDA;
   }
   uint32_t *d_cache = nullptr, *d_cstate = nullptr, *d_status = nullptr;
-  c->cache_bytes = uint64_t(n_classes) * W * 4;
+  c->cache_bytes = uint64_t(n_classes) * Wc * 4;
   if ((e = cudaMalloc(&d_cache, std::max<uint64_t>(c->cache_bytes, 16))) != cudaSuccess) { release(c); delete c; return CG_E_CUDA; }
   c->allocations.push_back(d_cache);
   if ((e = cudaMalloc(&d_cstate, size_t(n_classes) * 4 + 16)) != cudaSuccess) { release(c); delete c; return CG_E_CUDA; }
   c->allocations.push_back(d_cstate);
   if ((e = cudaMalloc(&d_status, 16)) != cudaSuccess) { release(c); delete c; return CG_E_CUDA; }
   c->allocations.push_back(d_status);
+  unsigned long long* d_stats = nullptr;
+  if ((e = cudaMalloc(&d_stats, 16)) != cudaSuccess) { release(c); delete c; return CG_E_CUDA; }
+  c->allocations.push_back(d_stats);
+  c->cache_stats = d_stats;
   e = cudaMemsetAsync(d_cstate, 0, size_t(n_classes) * 4 + 16, c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(d_status, 0, 16, c->stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(d_stats, 0, 16, c->stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
   if (e == cudaSuccess && cgk::fill_bitmask_smem(W) > 48 * 1024) e = cudaErrorInvalidValue;
   if (e != cudaSuccess) { release(c); delete c; return e == cudaErrorInvalidValue ? CG_E_LIMIT : CG_E_CUDA; }
@@ -273,6 +326,7 @@ int cg_ctx_create(const cg_grammar* const* g, uint32_t n_g, const cg_vocab* v, v
   t.n_classes = n_classes;
   t.V = V;
   t.W = W;
+  t.Wc = Wc;
   t.max_len = v->max_len;
   t.tok_off = d_off;
   t.tok_bytes = d_bytes;
@@ -292,9 +346,12 @@ int cg_ctx_create(const cg_grammar* const* g, uint32_t n_g, const cg_vocab* v, v
 
 void cg_ctx_destroy(cg_ctx* c) {
   if (!c) return;
-  cudaStreamSynchronize(c->stream);
-  if (c->copy_stream) cudaStreamSynchronize(c->copy_stream);
-  release(c);
+  {
+    cgk::DeviceGuard dg(c->device);
+    cudaStreamSynchronize(c->stream);
+    if (c->copy_stream) cudaStreamSynchronize(c->copy_stream);
+    release(c);
+  }
   delete c;
 }
 
@@ -309,16 +366,36 @@ int cg_ctx_info(const cg_ctx* c, uint32_t* n_classes, uint64_t* cache_bytes, uin
 
 int cg_ctx_status(cg_ctx* c, uint32_t* dev_code) {
   if (!c) return CG_E_ARG;
+  cgk::DeviceGuard dg(c->device);
+  if (!dg.ok) return CG_E_CUDA;
   uint32_t code = 0;
   if (cudaStreamSynchronize(c->stream) != cudaSuccess) return CG_E_CUDA;
   if (cudaMemcpy(&code, c->t.status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return CG_E_CUDA;
   if (code && cudaMemset(c->t.status, 0, 4) != cudaSuccess) return CG_E_CUDA;
+  // a kernel that gave up on a bounded wait may have left the segmented
+  // sampler's scratch (which every complete launch leaves at zero) dirty
+  if (code == CG_DEV_TIMEOUT && c->seg_scratch && cudaMemset(c->seg_scratch, 0, c->seg_scratch_bytes) != cudaSuccess)
+    return CG_E_CUDA;
   if (dev_code) *dev_code = code;
   return code ? CG_E_DEVICE : CG_OK;
 }
 
+int cg_ctx_cache_stats(cg_ctx* c, uint64_t* lookups, uint64_t* computed) {
+  if (!c) return CG_E_ARG;
+  cgk::DeviceGuard dg(c->device);
+  if (!dg.ok) return CG_E_CUDA;
+  unsigned long long v[2] = {0ull, 0ull};
+  if (cudaStreamSynchronize(c->stream) != cudaSuccess) return CG_E_CUDA;
+  if (cudaMemcpy(v, c->cache_stats, 16, cudaMemcpyDeviceToHost) != cudaSuccess) return CG_E_CUDA;
+  if (lookups) *lookups = v[0];
+  if (computed) *computed = v[1];
+  return CG_OK;
+}
+
 int cg_ctx_prefill(cg_ctx* c) {
   if (!c) return CG_E_ARG;
+  cgk::DeviceGuard dg(c->device);
+  if (!dg.ok) return CG_E_CUDA;
   if (cgk::launch_prefill(c->t, c->class_rep, c->class_gid, c->stream) != cudaSuccess) return CG_E_CUDA;
   c->cache_complete = true;  // later kernels on the stream see every class ready
   return CG_OK;
@@ -327,6 +404,8 @@ int cg_ctx_prefill(cg_ctx* c) {
 int cg_fill_bitmask(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const int32_t* d_forced, uint32_t B,
                     uint32_t* d_bitmask) {
   if (!c || (B && (!d_states || !d_bitmask))) return CG_E_ARG;
+  cgk::DeviceGuard dg(c->device);
+  if (!dg.ok) return CG_E_CUDA;
   return cgk::launch_fill_bitmask(c->t, d_states, d_gid, d_forced, B, d_bitmask, c->cache_complete, c->stream) ==
                  cudaSuccess
              ? CG_OK
@@ -336,36 +415,41 @@ int cg_fill_bitmask(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, 
 int cg_mask_and_sample(cg_ctx* c, void* d_logits, int dtype, uint32_t B, uint32_t V, const uint32_t* d_bitmask,
                        float temp, float top_p, uint64_t seed, uint32_t step, uint32_t* d_out_tok, float* d_probs,
                        uint32_t flags) {
-  if (!c || (B && (!d_logits || !d_bitmask || !d_out_tok))) return CG_E_ARG;
-  if (dtype != CG_F32 && dtype != CG_BF16) return CG_E_ARG;
-  if (V != c->t.V || !(temp >= 0.f) || temp == INFINITY || !(top_p == top_p)) return CG_E_ARG;
-  if (flags & ~CG_SAMPLE_INPLACE) return CG_E_ARG;
+  if (!sample_args_ok(c, d_logits, dtype, B, V, d_bitmask, temp, top_p, d_out_tok, flags)) return CG_E_ARG;
+  if (B == 0) return CG_OK;
+  cgk::DeviceGuard dg(c->device);
+  if (!dg.ok) return CG_E_CUDA;
+  const int inplace = (flags & CG_SAMPLE_INPLACE) ? 1 : 0;
+  const bool seg_path = cgk::seg_usable(dtype, V, d_logits, d_probs, inplace) && cgk::seg_bitmask_ok(c->t.W, d_bitmask);
   // grown once per larger batch (outside any stream capture)
-  const int rc = grow(c, &c->sample_scratch, &c->sample_scratch_bytes, cgk::sample_scratch_bytes(B, V));
+  const int rc = seg_path ? grow_zeroed(c, &c->seg_scratch, &c->seg_scratch_bytes, cgk::seg_scratch_bytes(B))
+                          : grow(c, &c->sample_scratch, &c->sample_scratch_bytes, cgk::sample_scratch_bytes(B, V));
   if (rc != CG_OK) return rc;
-  return cgk::launch_mask_and_sample(d_logits, dtype, B, V, c->t.W, d_bitmask, temp, top_p, seed, step, d_out_tok,
-                                     d_probs, (flags & CG_SAMPLE_INPLACE) ? 1 : 0, c->sample_scratch, c->t.status,
-                                     c->stream) == cudaSuccess
-             ? CG_OK
-             : CG_E_CUDA;
+  return sample_on(c, d_logits, dtype, B, V, d_bitmask, temp, top_p, seed, step, d_out_tok, d_probs, inplace,
+                   seg_path, c->sample_scratch, c->seg_scratch);
 }
 
 int cg_mask_and_sample_noalloc(cg_ctx* c, void* d_logits, int dtype, uint32_t B, uint32_t V,
                                const uint32_t* d_bitmask, float temp, float top_p, uint64_t seed, uint32_t step,
                                uint32_t* d_out_tok, float* d_probs, uint32_t flags) {
-  if (!c || (B && (!d_logits || !d_bitmask || !d_out_tok))) return CG_E_ARG;
-  if (dtype != CG_F32 && dtype != CG_BF16) return CG_E_ARG;
-  if (V != c->t.V || !(temp >= 0.f) || temp == INFINITY || !(top_p == top_p)) return CG_E_ARG;
-  if (flags & ~CG_SAMPLE_INPLACE) return CG_E_ARG;
-  if (B > CG_NOALLOC_MAX_ROWS || cgk::sample_scratch_bytes(B, V) > kNoAllocScratchBytes) return CG_E_LIMIT;
+  if (!sample_args_ok(c, d_logits, dtype, B, V, d_bitmask, temp, top_p, d_out_tok, flags)) return CG_E_ARG;
+  if (B > CG_NOALLOC_MAX_ROWS || cgk::sample_scratch_bytes(B, V) > kNoAllocListBytes ||
+      cgk::seg_scratch_bytes(B) > kNoAllocSegBytes)
+    return CG_E_LIMIT;
+  if (B == 0) return CG_OK;
+  cgk::DeviceGuard dg(c->device);
+  if (!dg.ok) return CG_E_CUDA;
   cudaError_t e = cudaSuccess;
-  void* scratch = noalloc_scratch(&e);
+  unsigned char* scratch = static_cast<unsigned char*>(noalloc_scratch(&e));
   if (!scratch) return CG_E_CUDA;
-  return cgk::launch_mask_and_sample(d_logits, dtype, B, V, c->t.W, d_bitmask, temp, top_p, seed, step, d_out_tok,
-                                     d_probs, (flags & CG_SAMPLE_INPLACE) ? 1 : 0, scratch, c->t.status,
-                                     c->stream) == cudaSuccess
-             ? CG_OK
-             : CG_E_CUDA;
+  const int inplace = (flags & CG_SAMPLE_INPLACE) ? 1 : 0;
+  const bool seg_path = cgk::seg_usable(dtype, V, d_logits, d_probs, inplace) && cgk::seg_bitmask_ok(c->t.W, d_bitmask);
+  unsigned char* seg = scratch + kNoAllocListBytes;
+  // the segmented sampler's part starts at zero: cleared here, whatever an
+  // earlier call (or one that ran out of a bounded wait) left in it
+  if (seg_path && cudaMemsetAsync(seg, 0, cgk::seg_scratch_bytes(B), c->stream) != cudaSuccess) return CG_E_CUDA;
+  return sample_on(c, d_logits, dtype, B, V, d_bitmask, temp, top_p, seed, step, d_out_tok, d_probs, inplace,
+                   seg_path, scratch, seg);
 }
 
 int cg_accept(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const uint32_t* d_toks,
@@ -373,6 +457,8 @@ int cg_accept(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const 
               uint8_t* d_out_flags) {
   if (!c || (B && (!d_states || !d_toks || !d_out_states || !d_out_flags))) return CG_E_ARG;
   if (d_counts && max_tokens == 0) return CG_E_ARG;
+  cgk::DeviceGuard dg(c->device);
+  if (!dg.ok) return CG_E_CUDA;
   return cgk::launch_accept(c->t, d_states, d_gid, d_toks, d_forced, B, d_counts, max_tokens, d_out_states,
                             d_out_flags, c->stream) == cudaSuccess
              ? CG_OK
@@ -388,14 +474,22 @@ int cg_step(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const in
   if (V != c->t.V || !(temp >= 0.f) || temp == INFINITY || !(top_p == top_p)) return CG_E_ARG;
   if (d_counts && max_tokens == 0) return CG_E_ARG;
   if (B == 0) return CG_OK;
-  int rc = grow(c, &c->sample_scratch, &c->sample_scratch_bytes, cgk::sample_scratch_bytes(B, V));
-  if (rc != CG_OK) return rc;
-  if (cgk::step_fusable(dtype, V, c->t.W, temp, top_p, d_logits))
-    return cgk::launch_step(c->t, d_states, d_gid, d_forced, B, d_logits, V, temp, top_p, seed, step, d_counts,
-                            max_tokens, d_bitmask, d_out_tok, d_out_states, d_out_flags, c->sample_scratch,
-                            c->grammars.data(), c->cache_complete, c->stream) == cudaSuccess
+  cgk::DeviceGuard dg(c->device);
+  if (!dg.ok) return CG_E_CUDA;
+  int rc;
+  if (cgk::seg_usable(dtype, V, d_logits, nullptr, 0)) {
+    // one segmented kernel (after the class masks the rows miss, when the
+    // cache is not complete)
+    if ((rc = grow_zeroed(c, &c->seg_scratch, &c->seg_scratch_bytes, cgk::seg_scratch_bytes(B))) != CG_OK) return rc;
+    if (!c->cache_complete &&
+        cgk::launch_cache_fill(c->t, d_states, d_gid, d_forced, B, c->cache_stats, c->stream) != cudaSuccess)
+      return CG_E_CUDA;
+    return cgk::launch_seg_step(c->t, d_states, d_gid, d_forced, B, d_logits, V, temp, top_p, seed, step, d_counts,
+                                max_tokens, d_bitmask, d_out_tok, d_out_states, d_out_flags, c->seg_scratch,
+                                c->grammars.data(), c->stream) == cudaSuccess
                ? CG_OK
                : CG_E_CUDA;
+  }
   // otherwise the three calls, through a context bitmask when the caller gives none
   uint32_t* bm = d_bitmask;
   if (!bm) {
@@ -414,6 +508,8 @@ int cg_step(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const in
 
 int cg_ctx_sync(cg_ctx* c) {
   if (!c) return CG_E_ARG;
+  cgk::DeviceGuard dg(c->device);
+  if (!dg.ok) return CG_E_CUDA;
   return cudaStreamSynchronize(c->stream) == cudaSuccess ? CG_OK : CG_E_CUDA;
 }
 
@@ -426,6 +522,8 @@ int cg_step_host(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, con
   if (V != c->t.V || !(temp >= 0.f) || temp == INFINITY || !(top_p == top_p)) return CG_E_ARG;
   if (d_counts && max_tokens == 0) return CG_E_ARG;
   if (B == 0) return CG_OK;
+  cgk::DeviceGuard dg(c->device);
+  if (!dg.ok) return CG_E_CUDA;
   if (!c->copy_stream) {
     if (cudaStreamCreateWithFlags(&c->copy_stream, cudaStreamNonBlocking) != cudaSuccess) return CG_E_CUDA;
     for (int k = 0; k < 2; ++k)
@@ -468,6 +566,8 @@ int cg_accept_many(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, c
   if (!c || (B && (!d_states || !d_draft || !d_draft_len || !d_out_states || !d_out_n || !d_out_flags))) return CG_E_ARG;
   if (B && K == 0) return CG_E_ARG;
   if (d_counts && max_tokens == 0) return CG_E_ARG;
+  cgk::DeviceGuard dg(c->device);
+  if (!dg.ok) return CG_E_CUDA;
   return cgk::launch_accept_many(c->t, d_states, d_gid, d_draft, d_draft_len, d_forced, B, K, d_counts, max_tokens,
                                  d_out_states, d_out_n, d_out_flags, d_out_path, c->stream) == cudaSuccess
              ? CG_OK
@@ -476,5 +576,7 @@ int cg_accept_many(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, c
 
 int cg_self_test_wait_timeout(cg_ctx* c) {
   if (!c) return CG_E_ARG;
+  cgk::DeviceGuard dg(c->device);
+  if (!dg.ok) return CG_E_CUDA;
   return cgk::launch_wait_timeout_self_test(c->t.status, c->stream) == cudaSuccess ? CG_OK : CG_E_CUDA;
 }

@@ -50,10 +50,11 @@ struct Tables {
   const uint16_t* colmap;      // [n_g][512] symbol -> column
   const uint8_t* state_flags;  // CG_STATE_* per state (all grammars)
   const uint32_t* class_of;    // mask class per state (all grammars, global ids)
-  uint32_t* cache;             // [n_classes][W] allowed-token bitmask per class
+  uint32_t* cache;             // [n_classes][Wc] allowed-token bitmask per class (words W..Wc unused)
   uint32_t* cache_state;       // per class: 0 empty, 1 being filled, 2 ready
   uint32_t n_classes;
   uint32_t V, W, max_len;
+  uint32_t Wc;                 // row stride of the mask cache: W rounded up to 4 words (16-byte aligned rows)
   const uint32_t* tok_off;     // [V+1] token bytes in id order
   const uint8_t* tok_bytes;
   const uint32_t* sorted_off;  // [V+1] token bytes in trie (lexicographic) order
@@ -76,6 +77,35 @@ CtxView ctx_view(const cg_ctx* c);
 // The context's candidate-list scratch of the sampling kernels, grown to at
 // least `bytes` (CG_OK or a CG_E_* code).
 int ctx_sample_scratch(cg_ctx* c, size_t bytes, void** out);
+// The device a context was created on.
+int ctx_device(const cg_ctx* c);
+
+// Makes a device current for the duration of a call and puts the caller's
+// back: every launch, allocation and symbol lookup of a library call then
+// happens on the device its context's tables live on.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    int cur = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess) {
+      ok = false;
+      return;
+    }
+    if (cur != dev) {
+      if (cudaSetDevice(dev) != cudaSuccess) {
+        ok = false;
+        return;
+      }
+      prev = cur;
+    }
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+  DeviceGuard(const DeviceGuard&) = delete;
+  DeviceGuard& operator=(const DeviceGuard&) = delete;
+};
 
 constexpr uint16_t kDead16 = 0xFFFFu;      // CG_DEAD in table16
 constexpr uint32_t kLongToken = 0xFFu;     // token record length of a token read through tok_off

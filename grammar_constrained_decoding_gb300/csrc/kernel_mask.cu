@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(kFillThreads) fill_bitmask_kernel(Tables t, co
 
   const DevGrammar gd = t.grammars[g];
   const uint32_t cls = t.class_of[gd.state_off + s];
-  const uint32_t* crow = t.cache + size_t(cls) * W;
+  const uint32_t* crow = t.cache + size_t(cls) * t.Wc;
   // one thread reads the flag so that the whole block takes the same path;
   // after cg_ctx_prefill every class is ready and the flag is not read
   if (!cache_complete) {
@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(kFillThreads) fill_bitmask_kernel(Tables t, co
   walk_tokens(t, gd, scol, s, smask, threadIdx.x, blockDim.x);
   __syncthreads();
   const bool claimed = s_claim != 0u;
-  uint32_t* cw = t.cache + size_t(cls) * W;
+  uint32_t* cw = t.cache + size_t(cls) * t.Wc;
   for (uint32_t i = threadIdx.x; i < W; i += blockDim.x) {
     const uint32_t w = smask[i];
     out[i] = w;
@@ -82,6 +82,52 @@ __global__ void __launch_bounds__(kFillThreads) fill_bitmask_kernel(Tables t, co
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) store_release(t.cache_state + cls, kStateReady);
+  }
+}
+
+// The fused step's miss path: one CTA per row computes the mask of the row's
+// class when it is not in the cache yet (claiming it first, so that one row
+// computes each class); rows whose class is ready, or claimed by another row
+// of the same launch, do nothing.  After this grid every class the rows need
+// is ready.  stats[0] counts the rows that looked a class up, stats[1] the
+// classes computed.
+__global__ void __launch_bounds__(kFillThreads) cache_fill_kernel(Tables t, const uint32_t* __restrict__ states,
+                                                                    const uint16_t* __restrict__ gid,
+                                                                    const int32_t* __restrict__ forced,
+                                                                    unsigned long long* stats) {
+  extern __shared__ uint32_t smem[];
+  uint32_t* smask = smem;
+  uint16_t* scol = reinterpret_cast<uint16_t*>(smem + t.W);
+  __shared__ uint32_t s_claim;
+  griddep_launch_dependents();
+  griddep_wait();  // states (and forced tokens) come from the previous step
+  const uint32_t b = blockIdx.x, W = t.W;
+  const uint32_t g = gid ? gid[b] : 0u;
+  const int32_t f = forced ? forced[b] : -1;
+  const uint32_t s = states[b];
+  uint32_t err = 0;
+  if (row_mask_mode(t, g, f, s, &err) != 0) return;  // errors are the step kernel's to record
+  const DevGrammar gd = t.grammars[g];
+  const uint32_t cls = t.class_of[gd.state_off + s];
+  if (threadIdx.x == 0) {
+    atomicAdd(stats, 1ull);
+    s_claim = load_acquire(t.cache_state + cls) != kStateReady &&
+              atomicCAS(t.cache_state + cls, kStateEmpty, kStateBusy) == kStateEmpty;
+  }
+  __syncthreads();
+  if (!s_claim) return;
+  for (uint32_t i = threadIdx.x; i < W; i += blockDim.x) smask[i] = 0u;
+  for (uint32_t i = threadIdx.x; i < 256; i += blockDim.x) scol[i] = t.colmap[size_t(g) * 512 + i];
+  __syncthreads();
+  walk_tokens(t, gd, scol, s, smask, threadIdx.x, blockDim.x);
+  __syncthreads();
+  uint32_t* cw = t.cache + size_t(cls) * t.Wc;
+  for (uint32_t i = threadIdx.x; i < W; i += blockDim.x) cw[i] = smask[i];
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    store_release(t.cache_state + cls, kStateReady);
+    atomicAdd(stats + 1, 1ull);
   }
 }
 
@@ -99,7 +145,7 @@ __global__ void __launch_bounds__(kFillThreads) prefill_kernel(Tables t, const u
   __syncthreads();
   walk_tokens(t, t.grammars[g], scol, class_rep[cls], smask, threadIdx.x, blockDim.x);
   __syncthreads();
-  uint32_t* cw = t.cache + size_t(cls) * W;
+  uint32_t* cw = t.cache + size_t(cls) * t.Wc;
   for (uint32_t i = threadIdx.x; i < W; i += blockDim.x) cw[i] = smask[i];
   __threadfence();
   __syncthreads();
@@ -123,5 +169,13 @@ cudaError_t launch_fill_bitmask(const Tables& t, const uint32_t* states, const u
 }
 
 size_t fill_bitmask_smem(uint32_t W) { return size_t(W) * 4 + 256 * 2; }
+
+cudaError_t launch_cache_fill(const Tables& t, const uint32_t* states, const uint16_t* gid, const int32_t* forced,
+                              uint32_t B, unsigned long long* stats, cudaStream_t stream) {
+  if (B == 0) return cudaSuccess;
+  const size_t smem = size_t(t.W) * 4 + 256 * 2;
+  return launch_dependent(cache_fill_kernel, dim3(B), dim3(kFillThreads), smem, stream, t, states, gid, forced,
+                          stats);
+}
 
 }  // namespace cgk

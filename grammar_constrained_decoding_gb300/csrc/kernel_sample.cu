@@ -25,6 +25,7 @@
 #include <mutex>
 #include <utility>
 
+#include "bf16_ops.cuh"
 #include "pda.cuh"
 #include "row_ops.cuh"
 
@@ -36,14 +37,6 @@ constexpr int kAcc = 8;           // independent partial sums per thread
 constexpr uint32_t kNotFound = 0xFFFFFFFFu;
 
 enum SampleMode { kGreedy = 0, kTopP = 1, kFull = 2 };
-
-__device__ __forceinline__ float bf16_bits_to_float(uint32_t h) { return __uint_as_float(h << 16); }
-
-// inverse of the 16-bit monotone bf16 key (fkey(x) >> 16)
-__device__ __forceinline__ float bf16key_to_float(uint32_t k16) {
-  const uint32_t h = (k16 & 0x8000u) ? (k16 & 0x7FFFu) : (~k16 & 0xFFFFu);
-  return bf16_bits_to_float(h);
-}
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   uint4 v;
@@ -333,63 +326,6 @@ constexpr uint32_t kSlots = 16;                                 // list entries 
 constexpr uint32_t kCandPerRow = kThreads * kSlots;             // candidate list entries per row (8192)
 constexpr uint32_t kBatchIds = 4;                               // nucleus id loads in flight per thread
 
-// 2^x with the multi-function unit (relative error about 2^-22; results
-// below 2^-126 flush to zero, far below any mass that matters here)
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
-  __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a), y = *reinterpret_cast<__nv_bfloat162*>(&b);
-  __nv_bfloat162 r = __hmax2(x, y);
-  return *reinterpret_cast<uint32_t*>(&r);
-}
-// masked logits become -inf (bf16 0xFF80)
-__device__ __forceinline__ uint4 apply_mask(uint4 v, uint4 pm) {
-  v.x = (v.x & pm.x) | (~pm.x & 0xFF80FF80u);
-  v.y = (v.y & pm.y) | (~pm.y & 0xFF80FF80u);
-  v.z = (v.z & pm.z) | (~pm.z & 0xFF80FF80u);
-  v.w = (v.w & pm.w) | (~pm.w & 0xFF80FF80u);
-  return v;
-}
-__device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-__device__ __forceinline__ float group_max(const uint4& v) {
-  const uint32_t mx = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
-  return fmaxf(lo_f(mx), hi_f(mx));
-}
-// acc[j] += exp2(x_j c - mc) for the group's logits, sums j and j + 1 paired in
-// one float2 (the packed fp32 multiply-add and add round each lane as the
-// scalar instructions do, so the sums are those of scalar code)
-__device__ __forceinline__ float2 ex2_pair(float2 z) { return make_float2(ex2(z.x), ex2(z.y)); }
-__device__ __forceinline__ void add_exps(float2* acc, const uint4& v, float2 c2, float2 nmc2) {
-  acc[0] = __fadd2_rn(acc[0], ex2_pair(__ffma2_rn(make_float2(lo_f(v.x), hi_f(v.x)), c2, nmc2)));
-  acc[1] = __fadd2_rn(acc[1], ex2_pair(__ffma2_rn(make_float2(lo_f(v.y), hi_f(v.y)), c2, nmc2)));
-  acc[2] = __fadd2_rn(acc[2], ex2_pair(__ffma2_rn(make_float2(lo_f(v.z), hi_f(v.z)), c2, nmc2)));
-  acc[3] = __fadd2_rn(acc[3], ex2_pair(__ffma2_rn(make_float2(lo_f(v.w), hi_f(v.w)), c2, nmc2)));
-}
-// logit e (0..7) of an 8-logit group
-__device__ __forceinline__ float group_at(const uint4& v, uint32_t e) {
-  const uint32_t wd = e < 4 ? (e < 2 ? v.x : v.y) : (e < 6 ? v.z : v.w);
-  return (e & 1u) ? hi_f(wd) : lo_f(wd);
-}
-// bf16 bits of logit e (0..7) of an 8-logit group
-__device__ __forceinline__ uint32_t group_bits(const uint4& v, uint32_t e) {
-  const uint32_t wd = e < 4 ? (e < 2 ? v.x : v.y) : (e < 6 ? v.z : v.w);
-  return (e & 1u) ? (wd >> 16) : (wd & 0xFFFFu);
-}
-// monotone 16-bit key of a bf16 (the high half of fkey of its float)
-__device__ __forceinline__ uint16_t bf16_key(uint32_t h) {
-  if (h == 0x8000u) h = 0u;
-  return uint16_t((h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u));
-}
-// mass of logit x in 2^-40 units of exp2((M - M) c) = 1: fixed point, so that
-// sums do not depend on their order
-__device__ __forceinline__ unsigned long long mass_q(float x, float M, float c) {
-  return static_cast<unsigned long long>(ex2((x - M) * c) * 1099511627776.0f);
-}
-
 // Prefix sums over bins 0..kBins-1 (bin = thread; q = this thread's bin mass),
 // starting from `base`: returns the first bin whose inclusive sum reaches
 // target (or kNotFound) and, through `above`, the sum before that bin.
@@ -533,7 +469,7 @@ __device__ void step_row_mask(const StepArgs& sa, uint32_t b, uint32_t W, uint32
       ready = sa.cache_complete ? 1u : (load_acquire(t.cache_state + cls) == kStateReady);
       if (ready && (W & 3u) == 0) {
         mbar_expect_tx(mbar_mask, W * 4);
-        bulk_g2s(smask, t.cache + size_t(cls) * W, W * 4, mbar_mask);
+        bulk_g2s(smask, t.cache + size_t(cls) * t.Wc, W * 4, mbar_mask);
         copied = 1;
       }
     }
@@ -554,7 +490,7 @@ __device__ void step_row_mask(const StepArgs& sa, uint32_t b, uint32_t W, uint32
     for (uint32_t i = tid; i < W; i += blockDim.x) smask[i] = (i == (f >> 5)) ? (1u << (f & 31)) : 0u;
   } else if (s_ready) {
     if (!s_copied) {
-      const uint32_t* crow = t.cache + size_t(s_cls) * W;
+      const uint32_t* crow = t.cache + size_t(s_cls) * t.Wc;
       for (uint32_t i = tid; i < W; i += blockDim.x) smask[i] = crow[i];
     }
   } else {
@@ -568,7 +504,7 @@ __device__ void step_row_mask(const StepArgs& sa, uint32_t b, uint32_t W, uint32
     walk_tokens(t, t.grammars[g], scol, s_s, smask, tid, blockDim.x);
     __syncthreads();
     if (s_claim) {
-      uint32_t* cw = t.cache + size_t(cls) * W;
+      uint32_t* cw = t.cache + size_t(cls) * t.Wc;
       for (uint32_t i = tid; i < W; i += blockDim.x) cw[i] = smask[i];
       __threadfence();
       __syncthreads();
@@ -732,13 +668,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     s_copied = 0;
     s_wrows = 0;
   }
-  for (uint32_t i = tid; i < 256; i += kThreads) {
-    uint32_t w[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      w[q] = (((i >> (2 * q)) & 1u) ? 0x0000FFFFu : 0u) | (((i >> (2 * q + 1)) & 1u) ? 0xFFFF0000u : 0u);
-    lut[i] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
+  for (uint32_t i = tid; i < 256; i += kThreads) lut[i] = pair_mask_entry(i);
   __syncthreads();  // barriers initialised
   griddep_wait();   // the bitmask (or, fused, the states) come from the previous kernel
   if (STEP == 0) {
@@ -1139,13 +1069,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_flag = 0;
   }
-  for (uint32_t i = tid; i < 256; i += kThreads) {
-    uint32_t w[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      w[q] = (((i >> (2 * q)) & 1u) ? 0x0000FFFFu : 0u) | (((i >> (2 * q + 1)) & 1u) ? 0xFFFF0000u : 0u);
-    lut[i] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
+  for (uint32_t i = tid; i < 256; i += kThreads) lut[i] = pair_mask_entry(i);
   __syncthreads();
   griddep_wait();  // the bitmask comes from fill_bitmask
   const uint32_t* mrow = bitmask + size_t(b) * W;

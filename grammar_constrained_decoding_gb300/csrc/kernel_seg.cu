@@ -1,0 +1,1619 @@
+// Segmented streaming sampler: mask-apply + temperature + softmax + top-p +
+// Gumbel-max (or greedy, or Gumbel-max over every allowed token) with every SM
+// carrying the same share of the logits (the sampler sees only masked logits:
+// usetacet.com/docs/grammar, "The guarantee").
+//
+// What is computed per row b is what kernel_sample.cu's header states: with
+// z_t = x_t / temp over the allowed tokens, m = max z, S = sum exp(z - m), the
+// nucleus {t : z_t >= tau} with tau the largest value whose upper set carries
+// at least top_p of the mass, and the token argmax over the nucleus of
+// z_t + g_t, g_t = -log(-log u_t), u_t from Philox4x32-10 word t&3 of counter
+// (t>>2, b, step, 0).
+//
+// Work decomposition.  Each row is cut into segments of up to four 4096-logit
+// chunks; a persistent grid (two CTAs per SM) takes segments (row-major) from
+// a work counter, so the bytes each SM streams differ by at most a segment.
+// A CTA has three roles.  The producer warp resolves each segment's mask
+// source (the caller's bitmask, or in the fused step the row's mask class in
+// the mask cache) one segment ahead and streams the segment's logits and mask
+// words into an 8-slot shared-memory ring with bulk asynchronous copies.
+// Eight consumer warps take each chunk 16 logits per thread.  The service
+// warp does the cross-CTA bookkeeping off the consumers' path: per finished
+// segment it counts the row's done segments (a fence and an atomic), and the
+// CTA that completes a row finishes it there (the token, and in the fused step
+// the accept) while the consumers stream on.
+//
+// Top-p, per segment.  Pass 1 (as the chunks land): masked logits, packed
+// bf16 group maxima kept in registers, and exp2((x - m) c) summed against the
+// thread's running maximum m (so that the sum does not depend on timing);
+// each warp publishes its chunk maximum to the row's running maximum in
+// global memory.  Segment end: the segment maximum m_s and S_s = sum over the
+// segment of exp2((x - m_s) c) are stored for the row; the candidate
+// threshold is max(m_s, the row's running maximum) minus a margin of kMarginZ
+// nats -- never above M - margin, M the row maximum, so every allowed logit
+// within the margin of M becomes a candidate.  Pass 2: the groups whose packed
+// maximum reaches the threshold are re-read from the ring (still held) and
+// their candidates pooled in shared memory; each candidate's Gumbel score is
+// drawn and recorded twice: in the row's key histogram in global memory (bin
+// = 16-bit bf16 key mod kNB: the count of the candidates with that key and
+// their best packed (score, id)) and in the segment's slice of the row's
+// candidate list.  The row's finisher takes M and S from the segments'
+// (m_s, S_s); tau is the largest key whose upper set carries top_p * S (masses
+// count x exp2((x - M) c) in 2^-40 fixed point, so sums do not depend on
+// order): from the histogram when the candidates' keys span fewer than kNB
+// keys, else from the list (masses per high key byte, then per key); the token
+// is the best packed score at or above tau.  A row whose list overflowed, or
+// whose nucleus reaches below the margin, is handed back to the consumers for
+// the exact multi-pass path over the row (same result).
+//
+// Greedy keeps each thread's best (x, lowest id).  Gumbel-max over every
+// allowed token (top_p >= 1) draws the Philox block of each group of four
+// tokens with an allowed one and tests a cheap upper bound of each token's
+// score (the noise g(u) = -ln(-ln u) is at most -ln(1 - u)) against the best
+// score found so far; the few tokens that pass are queued per warp and scored
+// exactly 32 at a time.  Both publish a packed (value, id) maximum per row.
+//
+// The fused step (cg_step) also builds each row's mask from the mask-class
+// cache (rows with a forced token or without allowed tokens stream nothing:
+// the token is the forced one, or none), writes the bitmask when asked, and
+// accepts the token when the row finishes.
+//
+// Device scratch (the context's, zero before the first launch): a work counter
+// pair and, per row, accumulators, the segments' partial sums, the key
+// histogram and the candidate list.  Every launch leaves the counters, the
+// accumulators and the histogram at zero again: the last CTA to stop taking
+// work resets the counters and each row's finisher clears its accumulators and
+// the histogram bins its candidates touched.
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "bf16_ops.cuh"
+#include "row_ops.cuh"
+
+namespace cgk {
+
+cudaError_t allow_smem(const void* kernel, size_t bytes);  // kernel_sample.cu
+
+namespace seg {
+
+constexpr uint32_t kConsWarps = 8;
+constexpr uint32_t kCons = kConsWarps * 32;                // 256 consumer threads
+constexpr uint32_t kProdWarp = kConsWarps;                 // the producer warp
+constexpr uint32_t kSvcWarp = kConsWarps + 1;              // the service warp
+constexpr uint32_t kThreads = kCons + 64;
+constexpr uint32_t kChunk = 4096;                          // logits per ring slot
+constexpr uint32_t kChunkBytes = kChunk * 2;               // 8 KiB
+constexpr uint32_t kChunkWords = kChunk / 32;              // mask words per slot
+constexpr uint32_t kGroups = kChunk / 8;                   // 8-logit groups per slot
+constexpr uint32_t kMaxSegChunks = 4;
+constexpr uint32_t kSlots = 8;                             // two segments of four chunks in flight
+constexpr uint32_t kNB = 1024;                             // key-histogram bins per row
+constexpr uint32_t kWarpCand = 256;                        // candidates a consumer warp holds per segment
+constexpr uint32_t kMaxNS = 64;                            // segments per row
+constexpr uint32_t kSlices = kMaxNS * kConsWarps;          // (segment, consumer warp) partials per row
+constexpr uint32_t kWindow = 4096;                         // per-key counters of the exact path
+constexpr uint32_t kListCap = 2048;                        // candidate-list entries per row
+constexpr uint32_t kSQ = 16;                               // records queued for the service warp (> kSlots)
+constexpr uint32_t kQ = 160;                               // queued exact scores per consumer warp (full)
+constexpr float kMarginZ = 8.5f;                           // nats below the maximum kept as candidates
+constexpr float kNoRef = -1e30f;                           // "no allowed logit yet"
+constexpr uint32_t kNotFound = 0xFFFFFFFFu;
+constexpr uint32_t kM0 = 0xD2511F53u, kM1 = 0xCD9E8D57u;   // Philox4x32 multipliers
+static_assert(kGroups == 2 * kCons, "two groups per consumer thread and slot");
+
+// dynamic shared memory
+constexpr uint32_t kOffRing = 0;
+constexpr uint32_t kOffMask = kOffRing + kSlots * kChunkBytes;
+constexpr uint32_t kOffLut = kOffMask + kSlots * kChunkWords * 4;
+constexpr uint32_t kOffPool = kOffLut + 256 * 16;
+constexpr uint32_t kPoolBytes = kWindow * 4;               // candidate buffers, exact-score queues, exact path's counters
+constexpr uint32_t kOffDesc = kOffPool + kPoolBytes;
+constexpr uint32_t kOffSvc = kOffDesc + kSlots * 16;       // the service warp's list keys, histogram, offsets
+constexpr uint32_t kSvcBytes = kListCap * 2 + (kSlices + 4) * 4;
+constexpr uint32_t kSmem = kOffSvc + kSvcBytes;
+static_assert(kConsWarps * kWarpCand * 6 <= kPoolBytes, "candidate buffers fit the pool region");
+static_assert(kConsWarps * kQ * 10 <= kPoolBytes, "exact-score queues fit the pool region");
+
+enum Mode { kModeGreedy = 0, kModeTopP = 1, kModeFull = 2 };
+// kinds of ring descriptors and service records
+constexpr uint32_t kStream = 0, kEmptyRow = 1, kForcedRow = 2, kNone = 3, kEnd = 4, kSkipPending = 5;
+
+struct RowAcc {
+  uint32_t maxkey;            // fkey of the running maximum logit published by the row's segments
+  uint32_t done;              // segments finished
+  uint32_t lowinv;            // max over segments of 0x10000 - (lowest candidate key)
+  uint32_t flags;             // bit 0: a segment's candidates overflowed the pool, or a non-finite range
+  unsigned long long best;    // greedy / full: packed (value, id) maximum
+  unsigned long long pad;
+};
+
+// Per-row block of the scratch, at the same place whatever the batch size or
+// segment count of a launch (so that what one launch leaves at zero is zero
+// for the next): accumulators, each (segment, consumer warp) slice's partial
+// maximum and sum and its candidate count, the key histogram, and the
+// candidate list (slice i writes its candidates, as packed (score, id) and
+// 16-bit key, into entries [i c, i c + c), c = kListCap / (NS kConsWarps)).
+constexpr uint32_t kRowPart = 32;                                   // after RowAcc
+constexpr uint32_t kRowNSeg = kRowPart + kSlices * 8;
+constexpr uint32_t kRowCnt = kRowNSeg + kSlices * 4;
+constexpr uint32_t kRowBest = kRowCnt + kNB * 4;
+constexpr uint32_t kRowLBest = kRowBest + kNB * 8;
+constexpr uint32_t kRowLKey = kRowLBest + kListCap * 8;
+constexpr uint32_t kRowStride = (kRowLKey + kListCap * 2 + 127) & ~127u;
+constexpr uint32_t kCtlBytes = 256;
+
+struct Scratch {
+  unsigned char* base;        // [kCtlBytes] counters, then [B] row blocks of kRowStride bytes
+  __device__ uint32_t* ctl() const { return reinterpret_cast<uint32_t*>(base); }  // [0] next segment, [1] CTAs done
+  __device__ unsigned char* blk(uint32_t b) const { return base + kCtlBytes + size_t(b) * kRowStride; }
+  __device__ RowAcc* row(uint32_t b) const { return reinterpret_cast<RowAcc*>(blk(b)); }
+  __device__ float2* part(uint32_t b) const { return reinterpret_cast<float2*>(blk(b) + kRowPart); }
+  __device__ uint32_t* nseg(uint32_t b) const { return reinterpret_cast<uint32_t*>(blk(b) + kRowNSeg); }
+  __device__ uint32_t* cnt(uint32_t b) const { return reinterpret_cast<uint32_t*>(blk(b) + kRowCnt); }
+  __device__ unsigned long long* hbest(uint32_t b) const {
+    return reinterpret_cast<unsigned long long*>(blk(b) + kRowBest);
+  }
+  __device__ unsigned long long* lbest(uint32_t b) const {
+    return reinterpret_cast<unsigned long long*>(blk(b) + kRowLBest);
+  }
+  __device__ uint16_t* lkey(uint32_t b) const { return reinterpret_cast<uint16_t*>(blk(b) + kRowLKey); }
+};
+
+struct Fused {
+  Tables t;
+  const uint32_t* states;
+  const uint16_t* gid;        // may be null
+  const int32_t* forced;      // may be null
+  uint32_t* counts;           // may be null
+  uint32_t max_tokens;
+  uint32_t* out_states;
+  uint8_t* out_flags;
+  uint32_t* bitmask_out;      // may be null
+  DevGrammar pg[8];           // grammar descriptors by value (one dependent load fewer)
+  uint32_t n_pg;
+};
+
+struct Params {
+  const uint16_t* logits;     // [B][V] bf16 bits, 16-byte aligned rows (V % 8 == 0)
+  uint32_t V, W, B, NS, segc, nchunks, N;
+  const uint32_t* bitmask;    // sampling from a bitmask: [B][W], W % 4 == 0, 16-byte aligned
+  float temp, top_p;
+  uint32_t step;
+  uint32_t rk[20];            // Philox round keys: rk[2r] = seed lo + r W0, rk[2r + 1] = seed hi + r W1
+  uint32_t ph_lo1, ph_hi1;    // M1 x step, the step's term of the first Philox round
+  uint32_t* out_tok;
+  uint32_t* status;
+  Scratch sc;
+  Fused f;
+};
+
+struct Src {
+  uint32_t b, s, kind, aux;
+  const uint32_t* mask;
+};
+
+// shared memory views and scalars
+struct Smem {
+  uint4* ring4;
+  uint32_t* mask32;
+  uint4* lut;
+  uint32_t* pool;              // per consumer warp: candidate ids and bits, or exact-score queues
+  uint4* desc;
+  uint16_t* svc_keys;          // [kListCap] the finishing row's candidate keys
+  uint32_t* svc_off;           // [kSlices + 1] their slices' offsets
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* sq_full;           // [kSQ] consumers -> service: a record is ready (kCons arrivals)
+  uint64_t* sq_empty;          // [kSQ] service -> consumers: the record slot is free again
+  uint4* sq_rec;               // [kSQ]
+  unsigned long long* red64;   // [kConsWarps + 1]
+  float* redf;                 // [kConsWarps + 1]
+  double* redd;                // [kConsWarps + 1]
+  uint32_t* words;             // [32] scalars
+  uint32_t* xq;                // [kXQ] rows the service warp hands back for the exact path
+};
+enum {
+  kWJ = 0,      // scan result of the exact path
+  kWAbort,      // a bounded wait ran out
+  kWIssued,     // ring slots the producer used
+  kWXTail,      // rows queued in xq by the service warp
+  kWXHead,      // rows of xq the consumers took
+  kWSvcDone,    // the service warp has finished
+  kWSnap,       // the consumers' uniform copy of kWXTail (and kWSnap + 16: the other parity's)
+};
+constexpr uint32_t kXQ = 64;
+
+__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(kCons) : "memory"); }
+// consumer barrier that also returns whether any consumer thread passed true
+// (bounded waits can run out in some threads only; what follows must be uniform)
+__device__ __forceinline__ bool cbar_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(uint32_t(v)), "n"(kCons)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void red_add_u32(uint32_t* p, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_max_u32(uint32_t* p, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_max_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_volatile_s(const uint32_t* p) { return *reinterpret_cast<const volatile uint32_t*>(p); }
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// bulk copy with an L2 eviction hint: the logits are read once per step and
+// should not push the mask cache and the scratch out of L2
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long y = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    v = y > v ? y : v;
+  }
+  return v;
+}
+
+// consumer-wide reductions (all 256 consumer threads call them; the result is
+// returned to every one of them)
+__device__ __forceinline__ unsigned long long cons_max_u64(unsigned long long v, unsigned long long* red) {
+  v = warp_max_u64(v);
+  cbar();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  cbar();
+  unsigned long long r = red[0];
+#pragma unroll
+  for (uint32_t w = 1; w < kConsWarps; ++w) r = red[w] > r ? red[w] : r;
+  return r;
+}
+__device__ __forceinline__ float cons_max_f(float v, float* red) {
+  v = warp_reduce(v, MaxOp());
+  cbar();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  cbar();
+  float r = red[0];
+#pragma unroll
+  for (uint32_t w = 1; w < kConsWarps; ++w) r = fmaxf(r, red[w]);
+  return r;
+}
+__device__ __forceinline__ double cons_sum_d(double v, double* red) {
+  v = warp_reduce(v, SumOp());
+  cbar();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  cbar();
+  double r = 0.0;
+#pragma unroll
+  for (uint32_t w = 0; w < kConsWarps; ++w) r += red[w];
+  return r;
+}
+
+__device__ __forceinline__ DevGrammar grammar_of(const Fused& f, uint32_t g) {
+  if (g >= f.n_pg) return f.t.grammars[g];
+  DevGrammar gd = f.pg[0];
+#pragma unroll
+  for (uint32_t i = 1; i < 8; ++i)
+    if (g == i) gd = f.pg[i];
+  return gd;
+}
+
+// ---- Philox4x32-10 with the row's constant terms hoisted ---------------------------
+// The counter of token t is (t >> 2, b, step, 0): in round one the product
+// M1 x step is the same for every block of the launch, and the first word
+// after round one depends on the row only, so round two's M0 product is the
+// row's too.  philox_q(row, q) equals philox4x32_10((q, b, step, 0), seed).
+__device__ __forceinline__ void mul_wide(uint32_t a, uint32_t b, uint32_t& lo, uint32_t& hi) {
+  unsigned long long r;
+  asm("mul.wide.u32 %0, %1, %2;" : "=l"(r) : "r"(a), "r"(b));
+  lo = static_cast<uint32_t>(r);
+  hi = static_cast<uint32_t>(r >> 32);
+}
+struct PhRow {
+  uint32_t a1, l2, h2;  // word 0 after round one; M0 x a1 (lo, hi)
+};
+__device__ __forceinline__ PhRow philox_row(const Params& p, uint32_t b) {
+  PhRow r;
+  r.a1 = p.ph_hi1 ^ b ^ p.rk[0];
+  mul_wide(kM0, r.a1, r.l2, r.h2);
+  return r;
+}
+__device__ __forceinline__ uint4 philox_q(const Params& p, const PhRow& r, uint32_t q) {
+  uint32_t lo0, hi0, lo1, hi1;
+  mul_wide(kM0, q, lo0, hi0);
+  // after round one: (a1, lo(M1 step), hi0 ^ k1, lo0); round two
+  const uint32_t c2 = hi0 ^ p.rk[1];
+  mul_wide(kM1, c2, lo1, hi1);
+  uint32_t c0 = hi1 ^ p.ph_lo1 ^ p.rk[2], c1 = lo1, c3 = r.l2;
+  uint32_t cz = r.h2 ^ lo0 ^ p.rk[3];
+#pragma unroll
+  for (int rr = 2; rr < 10; ++rr) {
+    uint32_t l0, h0, l1, h1;
+    mul_wide(kM0, c0, l0, h0);
+    mul_wide(kM1, cz, l1, h1);
+    const uint32_t n0 = h1 ^ c1 ^ p.rk[2 * rr], n2 = h0 ^ c3 ^ p.rk[2 * rr + 1];
+    c0 = n0;
+    c1 = l1;
+    cz = n2;
+    c3 = l0;
+  }
+  return make_uint4(c0, c1, cz, c3);
+}
+
+// Gumbel score of token id with logit bits xb: z + g, g = -log(-log u)
+__device__ __forceinline__ float gumbel_score(float x, float temp, uint32_t w) {
+  return __fdiv_rn(x, temp) + gumbel_from_word(w);
+}
+
+// Where segment idx's mask comes from, in two stages so that the producer can
+// have the loads of both in flight while it streams: stage1 loads the row's
+// grammar, forced token and state; stage2 the state's flags and mask class.
+// Fused: the row's mask class in the cache, or -- for a row with a forced
+// token or without allowed tokens -- no stream at all (kSkipPending: the
+// producer counts the row's segments and the row's owner finishes it once all
+// have been counted, so that nothing writes the row's state before every
+// segment has read it).
+struct Stage1 {
+  uint32_t idx, g, st;
+  int32_t fo;
+};
+template <int FUSED>
+__device__ __forceinline__ Stage1 stage1(const Params& p, uint32_t idx) {
+  Stage1 r{idx, 0u, 0u, -1};
+  if (!FUSED || idx >= p.N) return r;
+  const Fused& f = p.f;
+  const uint32_t b = idx / p.NS;
+  r.g = f.gid ? f.gid[b] : 0u;
+  r.fo = f.forced ? f.forced[b] : -1;
+  r.st = f.states[b];
+  return r;
+}
+template <int FUSED>
+__device__ __forceinline__ Src stage2(const Params& p, const Stage1& a, bool record = true) {
+  Src r;
+  r.b = a.idx / p.NS;
+  r.s = a.idx - r.b * p.NS;
+  r.kind = kStream;
+  r.aux = 0;
+  r.mask = nullptr;
+  if (!FUSED) {
+    r.mask = p.bitmask + size_t(r.b) * p.W;
+    return r;
+  }
+  const Fused& f = p.f;
+  const Tables& t = f.t;
+  DevGrammar gd{};
+  if (a.g < t.n_g) gd = grammar_of(f, a.g);
+  uint8_t sflags = 0;
+  uint32_t cls = 0;
+  if (a.g < t.n_g && a.fo < 0 && a.st != CG_DEAD && a.st < gd.n_states) {
+    sflags = t.state_flags[gd.state_off + a.st];
+    cls = t.class_of[gd.state_off + a.st];
+  }
+  uint32_t err = 0;
+  const int mode = row_mask_mode_of(t.n_g, t.V, a.g, a.fo, a.st, gd.n_states, sflags, &err);
+  if (mode == 0) {
+    r.mask = t.cache + size_t(cls) * t.Wc;
+    return r;
+  }
+  if (record && err && r.s == 0) record_error(t.status, err);
+  r.kind = kSkipPending;
+  r.aux = (mode == 2) ? (uint32_t(a.fo) | 0x80000000u) : 0u;
+  return r;
+}
+
+// The producer warp's lane 0: takes segments from the work counter and
+// streams their chunks (logits with an evict-first L2 hint, then the chunk's
+// mask words) into the ring.  The next item's mask source and the row of the
+// one after are loaded while the current item's chunks are issued.  Returns
+// the slots used.
+template <int FUSED>
+__device__ uint32_t produce(const Params& p, unsigned char* dsm, uint64_t* full, uint64_t* empty, uint4* desc,
+                            uint32_t* s_abort) {
+  const uint32_t N = p.N;
+  const uint64_t pol = evict_first_policy();
+  uint32_t q = 0;
+  bool ok = true;
+  uint32_t i0 = atomicAdd(p.sc.ctl(), 1u);
+  uint32_t i1 = i0 < N ? atomicAdd(p.sc.ctl(), 1u) : N;
+  uint32_t i2 = i1 < N ? atomicAdd(p.sc.ctl(), 1u) : N;
+  Src cur{};
+  if (i0 < N) cur = stage2<FUSED>(p, stage1<FUSED>(p, i0));
+  Stage1 s1 = stage1<FUSED>(p, i1);
+  auto take_slot = [&](uint32_t& sl) -> bool {
+    sl = q % kSlots;
+    return q < kSlots || mbar_wait(empty + sl, ((q / kSlots) - 1u) & 1u);
+  };
+  while (i0 < N) {
+    // loads for the items ahead, in flight while this one streams
+    Src nxt{};
+    if (i1 < N) nxt = stage2<FUSED>(p, s1);
+    const Stage1 s2 = stage1<FUSED>(p, i2);
+    const uint32_t i3 = i2 < N ? atomicAdd(p.sc.ctl(), 1u) : N;
+    uint32_t kind = cur.kind;
+    if (FUSED && kind == kSkipPending) {
+      // a row without a stream: its segments only count, and the row's owner
+      // finishes it once every segment has read the row's state
+      red_release_add(&p.sc.row(cur.b)->done, 1u);
+      kind = kNone;
+    }
+    if (kind != kNone) {
+      const uint32_t nch = kind == kStream ? min(p.segc, p.nchunks - cur.s * p.segc) : 1u;
+      for (uint32_t k = 0; k < nch; ++k, ++q) {
+        uint32_t sl;
+        if (!take_slot(sl)) {
+          ok = false;
+          break;
+        }
+        desc[sl] = make_uint4(cur.b, cur.s, kind | (nch << 8), cur.aux & 0x7FFFFFFFu);
+        if (kind == kStream) {
+          const uint32_t ck = cur.s * p.segc + k;
+          const uint32_t n = min(kChunk, p.V - ck * kChunk);
+          const uint32_t mw = (((n + 31u) >> 5) + 3u) & ~3u;
+          mbar_expect_tx(full + sl, n * 2 + mw * 4);
+          bulk_g2s_hint(dsm + kOffRing + sl * kChunkBytes, p.logits + size_t(cur.b) * p.V + size_t(ck) * kChunk,
+                        n * 2, full + sl, pol);
+          bulk_g2s(dsm + kOffMask + sl * (kChunkWords * 4), cur.mask + size_t(ck) * kChunkWords, mw * 4, full + sl);
+        } else {
+          mbar_arrive(full + sl);  // the descriptor is the whole message
+        }
+      }
+      if (!ok) break;
+    }
+    cur = nxt;
+    s1 = s2;
+    i0 = i1;
+    i1 = i2;
+    i2 = i3;
+  }
+  if (ok) {
+    uint32_t sl;
+    if (take_slot(sl)) {
+      desc[sl] = make_uint4(0u, 0u, kEnd, 0u);
+      mbar_arrive(full + sl);
+      ++q;
+    } else {
+      ok = false;
+    }
+  }
+  if (!ok) {
+    record_error(p.status, CG_DEV_TIMEOUT);
+    atomicExch(s_abort, 1u);
+  }
+  // this CTA takes no more segments: the last one to stop resets the counters
+  // for the next launch
+  __threadfence();
+  if (atomicAdd(p.sc.ctl() + 1, 1u) == gridDim.x - 1) {
+    p.sc.ctl()[0] = 0u;
+    p.sc.ctl()[1] = 0u;
+  }
+  return q;
+}
+
+// Mask row of b in global memory (the exact path reads it).
+template <int FUSED>
+__device__ const uint32_t* row_mask_ptr(const Params& p, uint32_t b) {
+  if (!FUSED) return p.bitmask + size_t(b) * p.W;
+  return stage2<1>(p, stage1<1>(p, b * p.NS)).mask;
+}
+
+// Exact top-p over the row in global memory (consumer threads only): pass A
+// for M and S (compensated sums), the per-key counts of the kWindow keys below
+// the maximum (bisection over the key space when the nucleus reaches deeper),
+// then Gumbel-max over the nucleus.  The same definition as the streaming
+// path; it reads the row three times or more.
+__device__ __noinline__ uint32_t exact_topp(const Params& p, uint32_t b, const uint32_t* gmask, uint32_t* cnt,
+                               unsigned long long* red64, float* redf, double* redd, uint32_t* s_word) {
+  const uint32_t V = p.V, tid = threadIdx.x;
+  const float temp = p.temp, c = 1.4426950408889634f / temp;
+  const uint4* row4 = reinterpret_cast<const uint4*>(p.logits + size_t(b) * V);
+  // f(t, bf16 bits of x_t) for every allowed token, four groups per thread
+  // and pass with their loads in flight together
+  auto for_allowed = [&](auto&& f) {
+    const uint32_t ng = V / 8;
+    for (uint32_t i0 = tid; i0 < ng; i0 += 4 * kCons) {
+      uint4 v[4];
+      uint32_t bits[4];
+#pragma unroll
+      for (uint32_t u = 0; u < 4; ++u) {
+        const uint32_t i = i0 + u * kCons;
+        bits[u] = i < ng ? (__ldg(gmask + (i >> 2)) >> ((i & 3u) * 8u)) & 0xFFu : 0u;
+        v[u] = i < ng ? __ldg(row4 + i) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (uint32_t u = 0; u < 4; ++u) {
+        if (!bits[u]) continue;
+        const uint32_t i = i0 + u * kCons;
+#pragma unroll
+        for (uint32_t e = 0; e < 8; ++e)
+          if ((bits[u] >> e) & 1u) f(i * 8 + e, group_bits(v[u], e));
+      }
+    }
+  };
+  float m = -INFINITY, sum = 0.f, comp = 0.f;
+  for_allowed([&](uint32_t, uint32_t h) {
+    const float x = bf16_bits_to_float(h);
+    if (x > m) {
+      const float r = exp2f((m - x) * c);
+      sum *= r;
+      comp *= r;
+      m = x;
+    }
+    const float y = exp2f((x - m) * c) - comp;
+    const float nt = sum + y;
+    comp = (nt - sum) - y;
+    sum = nt;
+  });
+  const float M = cons_max_f(m, redf);
+  if (!(M > -INFINITY)) return CG_NO_TOKEN;
+  double part = 0.0;
+  if (m > -INFINITY) part = (double(sum) - double(comp)) * double(exp2f((m - M) * c));
+  const double S = cons_sum_d(part, redd);
+  const double target = double(p.top_p) * S;
+  const uint32_t km = fkey(M) >> 16;
+  const uint32_t lo = km >= kWindow - 1 ? km - (kWindow - 1) : 0u;
+  for (uint32_t i = tid; i < kWindow; i += kCons) cnt[i] = 0u;
+  cbar();
+  for_allowed([&](uint32_t, uint32_t h) {
+    const uint32_t k = fkey(bf16_bits_to_float(h)) >> 16;
+    if (k >= lo) atomicAdd(cnt + (km - k), 1u);
+  });
+  cbar();
+  if (tid < 32) {
+    const uint32_t lane = tid;
+    double cum = 0.0;
+    uint32_t found = kNotFound;
+    for (uint32_t base = 0; base <= km - lo && found == kNotFound; base += 32) {
+      const uint32_t j = base + lane;
+      double mass = 0.0;
+      if (j <= km - lo && cnt[j]) mass = double(cnt[j]) * double(exp2f((bf16key_to_float(km - j) - M) * c));
+      double incl = mass;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= uint32_t(o)) incl += y;
+      }
+      const unsigned hit = __ballot_sync(0xFFFFFFFFu, cum + incl >= target);
+      if (hit) found = base + uint32_t(__ffs(hit) - 1);
+      cum += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (lane == 0) *s_word = (found == kNotFound) ? kNotFound : km - found;
+  }
+  cbar();
+  uint32_t tau = *s_word;
+  if (tau == kNotFound) {
+    // largest key whose upper set carries the target, by bisection
+    uint32_t klo = 0, khi = km;
+    while (klo < khi) {
+      const uint32_t mid = klo + (khi - klo + 1) / 2;
+      float ps = 0.f;
+      for_allowed([&](uint32_t, uint32_t h) {
+        const float x = bf16_bits_to_float(h);
+        if ((fkey(x) >> 16) >= mid) ps += exp2f((x - M) * c);
+      });
+      const double mass = cons_sum_d(double(ps), redd);
+      if (mass >= target) klo = mid; else khi = mid - 1;
+    }
+    tau = klo;
+  }
+  unsigned long long best = 0ull;
+  uint32_t cached = 0xFFFFFFFFu;
+  uint4 blk = make_uint4(0u, 0u, 0u, 0u);
+  for_allowed([&](uint32_t t, uint32_t h) {
+    const float x = bf16_bits_to_float(h);
+    if ((fkey(x) >> 16) < tau) return;
+    if ((t >> 2) != cached) {
+      blk = philox4x32_10(make_uint4(t >> 2, b, p.step, 0u), p.rk[0], p.rk[1]);
+      cached = t >> 2;
+    }
+    best = max(best, pack_best(__fdiv_rn(x, temp) + gumbel_from_word(philox_word(blk, t & 3u)), t));
+  });
+  best = cons_max_u64(best, red64);
+  return best ? best_id(best) : CG_NO_TOKEN;
+}
+
+// Outputs of a finished row: the token, and in the fused step the accept.
+template <int FUSED>
+__device__ __noinline__ void emit(const Params& p, uint32_t b, uint32_t tok) {
+  p.out_tok[b] = tok;
+  if (FUSED) {
+    const Fused& f = p.f;
+    const uint32_t g = f.gid ? f.gid[b] : 0u;
+    const int32_t fo = f.forced ? f.forced[b] : -1;
+    accept_row(f.t, b, g, f.states[b], tok, fo, f.counts, f.max_tokens, f.out_states, f.out_flags);
+  }
+}
+
+// ---- the service warp ------------------------------------------------------------------
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// The nucleus key of row b from its candidate list (rows whose candidate keys
+// span more than the histogram): the largest key kappa in [kthr, km] whose
+// upper set of entries carries target, by bisection over the key (masses in
+// 2^-40 fixed point, so every sum is exact).  kNotFound when a slice
+// overflowed or the mass does not reach the target.  Leaves the keys in
+// sm.svc_keys and the slices' offsets in sm.svc_off; *n_out the list length.
+__device__ __noinline__ uint32_t list_tau(const Params& p, uint32_t b, float M, float c, uint32_t kthr, uint32_t km,
+                             unsigned long long target, const Smem& sm, uint32_t* n_out) {
+  const uint32_t lane = threadIdx.x & 31, NSW = p.NS * kConsWarps, capW = kListCap / NSW;
+  const uint32_t* ns = p.sc.nseg(b);
+  // offsets of the slices' entries in flat order
+  uint32_t* off = sm.svc_off;
+  uint32_t base = 0;
+  bool over = false;
+  for (uint32_t i0 = 0; i0 < NSW; i0 += 32) {
+    const uint32_t n = i0 + lane < NSW ? __ldcg(ns + i0 + lane) : 0u;
+    over = over || n > capW;
+    uint32_t inc = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+      if (lane >= uint32_t(o)) inc += y;
+    }
+    if (i0 + lane < NSW) off[i0 + lane] = base + inc - n;
+    base += __shfl_sync(0xFFFFFFFFu, inc, 31);
+  }
+  if (__any_sync(0xFFFFFFFFu, over)) return kNotFound;
+  const uint32_t L = base;
+  if (lane == 0) off[NSW] = L;
+  *n_out = L;
+  __syncwarp();
+  const uint16_t* lk = p.sc.lkey(b);
+  for (uint32_t j0 = lane; j0 < L; j0 += 32 * 8) {
+    uint16_t k[8];  // eight loads in flight together
+#pragma unroll
+    for (uint32_t u = 0; u < 8; ++u) {
+      const uint32_t j = j0 + 32 * u;
+      k[u] = 0;
+      if (j < L) {
+        uint32_t lo = 0, hi = NSW;  // the slice of flat entry j: off[lo] <= j < off[lo + 1]
+        while (hi - lo > 1) {
+          const uint32_t mid = (lo + hi) / 2;
+          if (off[mid] <= j) lo = mid; else hi = mid;
+        }
+        k[u] = __ldcg(lk + lo * capW + (j - off[lo]));
+      }
+    }
+#pragma unroll
+    for (uint32_t u = 0; u < 8; ++u)
+      if (j0 + 32 * u < L) sm.svc_keys[j0 + 32 * u] = k[u];
+  }
+  __syncwarp();
+  auto mass_above = [&](uint32_t kappa) {
+    unsigned long long m = 0ull;
+    for (uint32_t j = lane; j < L; j += 32) {
+      const uint32_t k = sm.svc_keys[j];
+      if (k >= kappa) m += mass_q(bf16key_to_float(k), M, c);
+    }
+    return warp_sum_u64(m);
+  };
+  if (mass_above(kthr) < target) return kNotFound;
+  uint32_t lo = kthr, hi = km;
+  while (lo < hi) {
+    const uint32_t mid = lo + (hi - lo + 1) / 2;
+    if (mass_above(mid) >= target) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Finishes row b (top-p) on the service warp.  Returns false when the row is
+// to take the exact path.
+template <int FUSED>
+__device__ __noinline__ bool finish_topp(const Params& p, uint32_t b, const Smem& sm) {
+  const uint32_t lane = threadIdx.x & 31, NSW = p.NS * kConsWarps;
+  RowAcc* ra = p.sc.row(b);
+  const float c = 1.4426950408889634f / p.temp, margin = kMarginZ * p.temp;
+  // one round of loads: the row's accumulators and every slice's (maximum, sum);
+  // S merges the slices online (lane by lane in slice order, then across lanes)
+  uint32_t mk = 0, flags = 0, lowinv = 0;
+  if (lane == 0) {
+    mk = __ldcg(&ra->maxkey);
+    flags = __ldcg(&ra->flags);
+    lowinv = __ldcg(&ra->lowinv);
+  }
+  const float2* part = p.sc.part(b);
+  float lm = kNoRef, ls = 0.f;
+  for (uint32_t i = lane; i < NSW; i += 32) {
+    const float2 v = __ldcg(part + i);
+    if (v.x > kNoRef && v.y > 0.f) {
+      if (v.x > lm) {
+        ls = ls * ex2((lm - v.x) * c) + v.y;
+        lm = v.x;
+      } else {
+        ls += v.y * ex2((v.x - lm) * c);
+      }
+    }
+  }
+  const float M = warp_reduce(lm, MaxOp());
+  const float S = warp_reduce(lm > kNoRef ? ls * ex2((lm - M) * c) : 0.f, SumOp());
+  mk = __shfl_sync(0xFFFFFFFFu, mk, 0);
+  flags = __shfl_sync(0xFFFFFFFFu, flags, 0);
+  lowinv = __shfl_sync(0xFFFFFFFFu, lowinv, 0);
+  uint32_t tok = CG_NO_TOKEN;
+  bool exact = false, clear_all = true;
+  uint32_t km = 0, lowkey = 0x10000u;
+  if (M > kNoRef) {
+    exact = !(M < 1e29f && M > -1e29f) || (flags & 1u);
+    if (!exact) {
+      const float thrF = M - margin;
+      km = fkey(M) >> 16;
+      uint32_t kthr = fkey(thrF) >> 16;
+      if (bf16key_to_float(kthr) < thrF) ++kthr;
+      lowkey = lowinv ? 0x10000u - lowinv : 0x10000u;
+      const bool hist_ok = lowkey <= km && km - lowkey < kNB;
+      clear_all = !hist_ok;
+      const unsigned long long target =
+          static_cast<unsigned long long>(p.top_p * S * 1099511627776.0f);  // top_p of the mass, 2^-40 units
+      unsigned long long best = 0ull;
+      if (kthr > km) {
+        exact = true;
+      } else if (hist_ok) {
+        // bins from the top, 128 a round: counts and bests loaded together
+        const uint32_t span = km - kthr;
+        const uint32_t* cnt = p.sc.cnt(b);
+        const unsigned long long* hbp = p.sc.hbest(b);
+        unsigned long long base = 0ull;
+        bool found = false;
+        for (uint32_t r0 = 0; r0 <= span && !found; r0 += 128) {
+          uint32_t n[4];
+          unsigned long long hv[4];
+#pragma unroll
+          for (uint32_t u = 0; u < 4; ++u) {
+            const uint32_t j = r0 + 32 * u + lane;
+            n[u] = 0u;
+            hv[u] = 0ull;
+            if (j <= span) {
+              n[u] = __ldcg(cnt + ((km - j) & (kNB - 1)));
+              hv[u] = __ldcg(hbp + ((km - j) & (kNB - 1)));
+            }
+          }
+#pragma unroll
+          for (uint32_t u = 0; u < 4; ++u) {
+            if (found) break;
+            const uint32_t j = r0 + 32 * u + lane;
+            const unsigned long long q =
+                n[u] ? (unsigned long long)n[u] * mass_q(bf16key_to_float(km - j), M, c) : 0ull;
+            unsigned long long incl = q;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+              if (lane >= uint32_t(o)) incl += y;
+            }
+            const unsigned hit = __ballot_sync(0xFFFFFFFFu, q != 0ull && base + incl >= target);
+            // bins at or above the nucleus key: this round's lanes up to the hit
+            const uint32_t last = hit ? uint32_t(__ffs(hit) - 1) : 31u;
+            if (lane <= last) best = hv[u] > best ? hv[u] : best;
+            found = hit != 0u;
+            base += __shfl_sync(0xFFFFFFFFu, incl, 31);
+          }
+        }
+        exact = !found;
+      } else {
+        uint32_t L = 0;
+        const uint32_t tau = list_tau(p, b, M, c, kthr, km, target, sm, &L);
+        if (tau == kNotFound) {
+          exact = true;
+        } else {
+          // the best packed score among the entries at or above tau
+          const uint32_t capW = kListCap / NSW;
+          const unsigned long long* lb = p.sc.lbest(b);
+          for (uint32_t j = lane; j < L; j += 32) {
+            if (sm.svc_keys[j] < tau) continue;
+            uint32_t lo = 0, hi = NSW;
+            while (hi - lo > 1) {
+              const uint32_t mid = (lo + hi) / 2;
+              if (sm.svc_off[mid] <= j) lo = mid; else hi = mid;
+            }
+            const unsigned long long v = __ldcg(lb + lo * capW + (j - sm.svc_off[lo]));
+            best = v > best ? v : best;
+          }
+        }
+      }
+      if (!exact) {
+        best = warp_max_u64(best);
+        tok = best ? best_id(best) : CG_NO_TOKEN;
+      }
+    }
+  } else {
+    clear_all = false;  // no slice had an allowed logit: no candidate was recorded
+  }
+  (void)mk;
+  __syncwarp();
+  // clear what this row's candidates touched: keys lowkey..km, or every bin
+  uint32_t* cnt = p.sc.cnt(b);
+  unsigned long long* hb = p.sc.hbest(b);
+  const uint32_t nz = clear_all ? kNB : (lowkey <= km ? km - lowkey + 1 : 0u);
+  for (uint32_t j = lane; j < nz; j += 32) {
+    const uint32_t bin = (km - j) & (kNB - 1);
+    cnt[bin] = 0u;
+    hb[bin] = 0ull;
+  }
+  if (lane == 0) {
+    ra->maxkey = 0u;
+    ra->done = 0u;
+    ra->lowinv = 0u;
+    ra->flags = 0u;
+    if (!exact) emit<FUSED>(p, b, tok);
+  }
+  return !exact;
+}
+
+// Finishes a row without a stream (fused step): a forced token (that token)
+// or none; the bitmask when asked.
+template <int FUSED>
+__device__ __noinline__ void finish_skip(const Params& p, uint32_t b, uint32_t kind, uint32_t f) {
+  const uint32_t lane = threadIdx.x & 31;
+  if (FUSED && p.f.bitmask_out) {
+    uint32_t* out = p.f.bitmask_out + size_t(b) * p.W;
+    for (uint32_t i = lane; i < p.W; i += 32) out[i] = (kind == kForcedRow && i == (f >> 5)) ? (1u << (f & 31u)) : 0u;
+  }
+  if (lane == 0) {
+    p.sc.row(b)->done = 0u;
+    emit<FUSED>(p, b, kind == kForcedRow ? f : CG_NO_TOKEN);
+  }
+}
+
+// The service warp.  Counts the rows' finished segments: every record the
+// consumers complete is taken in a batch, one fence for the batch and one
+// reduction per record (nothing waits for a returned value).  Finishes the
+// rows this CTA owns (b = blockIdx.x + k gridDim.x, in order) once all their
+// segments are counted; rows for the exact path are queued (xq) for the
+// consumers.  Returns when the consumers' end record has arrived and every
+// owned row is finished.
+template <int MODE, int FUSED>
+__device__ void service(const Params& p, const Smem& sm) {
+  const uint32_t lane = threadIdx.x & 31;
+  uint32_t k = 0;          // next record
+  bool end = false;        // the consumers' end record arrived
+  uint32_t own = blockIdx.x;  // next owned row
+  uint32_t idle = 0;
+  while (!end || own < p.B) {
+    bool busy = false;
+    if (!end) {
+      // every record already complete, from k on
+      bool ready = false;
+      if (lane < kSQ) ready = mbar_try_wait(sm.sq_full + (k + lane) % kSQ, ((k + lane) / kSQ) & 1u);
+      const unsigned notready = __ballot_sync(0xFFFFFFFFu, !ready);
+      const uint32_t n = notready ? uint32_t(__ffs(notready) - 1) : 32u;
+      if (n) {
+        busy = true;
+        uint4 r = make_uint4(0u, 0u, kNone, 0u);
+        if (lane < n) r = sm.sq_rec[(k + lane) % kSQ];
+        __syncwarp();
+        if (lane < n) mbar_arrive(sm.sq_empty + (k + lane) % kSQ);
+        k += n;
+        end = __any_sync(0xFFFFFFFFu, lane < n && r.z == kEnd);
+        // every consumer thread's writes for a record precede its arrival on
+        // the record's barrier, and this fence orders them before the counts
+        __threadfence();
+        if (lane < n && r.z == kStream) red_add_u32(&p.sc.row(r.x)->done, 1u);
+      }
+    }
+    if (own < p.B) {
+      uint32_t d = 0;
+      if (lane == 0) d = ld_acquire_gpu(&p.sc.row(own)->done);
+      d = __shfl_sync(0xFFFFFFFFu, d, 0);
+      if (d >= p.NS) {
+        busy = true;
+        __threadfence();
+        // the row's kind: a stream, or (fused) a forced token / no allowed token
+        uint32_t kind = kStream, f = 0;
+        if (FUSED) {
+          const Src r = stage2<FUSED>(p, stage1<FUSED>(p, own * p.NS), false);
+          if (r.kind == kSkipPending) {
+            kind = (r.aux & 0x80000000u) ? kForcedRow : kEmptyRow;
+            f = r.aux & 0x7FFFFFFFu;
+          }
+        }
+        if (kind != kStream) {
+          finish_skip<FUSED>(p, own, kind, f);
+        } else if (MODE == kModeTopP) {
+          if (!finish_topp<FUSED>(p, own, sm) && lane == 0) {
+            // the exact path: queued for the consumers, who take it after their stream
+            const uint32_t t = sm.words[kWXTail];
+            if (t - ld_volatile_s(&sm.words[kWXHead]) >= kXQ) {
+              record_error(p.status, CG_DEV_TIMEOUT);  // more exact rows in one CTA than the queue holds
+            } else {
+              sm.xq[t % kXQ] = own;
+              __threadfence_block();
+              *reinterpret_cast<volatile uint32_t*>(&sm.words[kWXTail]) = t + 1;
+            }
+          }
+        } else if (lane == 0) {
+          RowAcc* ra = p.sc.row(own);
+          const unsigned long long v = __ldcg(&ra->best);
+          ra->best = 0ull;
+          ra->done = 0u;
+          emit<FUSED>(p, own, v ? best_id(v) : CG_NO_TOKEN);
+        }
+        __syncwarp();
+        own += gridDim.x;
+      }
+    }
+    if (busy) {
+      idle = 0;
+    } else if (++idle > kWaitLimit) {
+      if (lane == 0) {
+        record_error(p.status, CG_DEV_TIMEOUT);
+        atomicExch(&sm.words[kWAbort], 1u);
+      }
+      break;
+    } else {
+      __nanosleep(128);
+    }
+  }
+  if (lane == 0) {
+    __threadfence_block();
+    *reinterpret_cast<volatile uint32_t*>(&sm.words[kWSvcDone]) = 1u;
+  }
+}
+
+// ---- the consumer warps ------------------------------------------------------------------
+
+// Full mode: score the warp's queued tokens [base, base + n) exactly, one per
+// lane, and raise the lanes' bests and the warp's bound reference.
+__device__ __noinline__ void drain_queue(const uint32_t* qid, const uint32_t* qw, const uint16_t* qx,
+                                            uint32_t base, uint32_t n, float temp, unsigned long long& best,
+                                            float& bestv, float& offB) {
+  const uint32_t lane = threadIdx.x & 31;
+  if (lane < n) {
+    const uint32_t i = base + lane;
+    const float sc = gumbel_score(bf16_bits_to_float(qx[i]), temp, qw[i]);
+    const unsigned long long pk = pack_best(sc, qid[i]);
+    if (pk > best) best = pk;
+  }
+  // the warp's best score is the bound reference of all its lanes
+  const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, best ? static_cast<uint32_t>(best >> 32) : 0u);
+  if (wk) {
+    const float wb = fkey_inv(wk);
+    if (wb > bestv) {
+      bestv = wb;
+      offB = 23.f - wb * 1.4426950408889634f;
+    }
+  }
+}
+
+// Keeps the first n buffered candidates whose 16-bit key is at least k16, in
+// order, at the front of the warp's buffer; returns how many (all lanes).
+__device__ __forceinline__ uint32_t compact_cands(uint32_t* cid, uint16_t* cx, uint32_t n, uint32_t k16) {
+  const uint32_t lane = threadIdx.x & 31, lt = (1u << lane) - 1u;
+  uint32_t kept = 0;
+  for (uint32_t i0 = 0; i0 < n; i0 += 32) {
+    const uint32_t i = i0 + lane;
+    uint32_t id = 0;
+    uint16_t xb = 0;
+    bool keep = false;
+    if (i < n) {
+      id = cid[i];
+      xb = cx[i];
+      keep = bf16_key(xb) >= k16;
+    }
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep);
+    __syncwarp();
+    if (keep) {  // never past the entries still to be read
+      cid[kept + __popc(bal & lt)] = id;
+      cx[kept + __popc(bal & lt)] = xb;
+    }
+    kept += __popc(bal);
+    __syncwarp();
+  }
+  return kept;
+}
+
+// Each consumer warp works on its own share of every chunk (64 groups of 8
+// logits) and ends each segment on its own: no consumer-wide barrier on the
+// stream's path.  Per segment a warp publishes its slice's (maximum, sum),
+// extracts its candidates against max(its maximum, the row's running
+// maximum) - margin, scores them, releases the ring slots and arrives on the
+// service record.
+template <int MODE, int FUSED>
+__device__ void consume(const Params& p, const Smem& sm) {
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float temp = p.temp;
+  const float c = (MODE == kModeGreedy) ? 0.f : 1.4426950408889634f / temp;
+  const float margin = kMarginZ * temp;
+  const uint32_t g0 = warp * 64 + lane, g1 = g0 + 32;
+  const uint32_t lt = (1u << lane) - 1u;
+  const uint4 kNeg4 = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+  uint32_t q = 0;     // ring slots taken
+  uint32_t nrec = 0;  // records sent to the service warp
+  bool ok = true;
+  // One record for the service warp: thread 0 writes it once its slot is
+  // free; every consumer thread arrives once its own writes for it are done.
+  auto post = [&](uint32_t b, uint32_t s, uint32_t kind, uint32_t aux) {
+    const uint32_t k = nrec % kSQ;
+    if (tid == 0) {
+      if (nrec >= kSQ && !mbar_wait(sm.sq_empty + k, ((nrec / kSQ) - 1u) & 1u)) {
+        record_error(p.status, CG_DEV_TIMEOUT);
+        atomicExch(&sm.words[kWAbort], 1u);
+      }
+      sm.sq_rec[k] = make_uint4(b, s, kind, aux);
+    }
+    mbar_arrive(sm.sq_full + k);
+    ++nrec;
+  };
+  // per warp: candidate ids and bits (top-p), or the exact-score queue (full)
+  uint32_t* cid = sm.pool + warp * kWarpCand;
+  uint16_t* cx = reinterpret_cast<uint16_t*>(sm.pool + kConsWarps * kWarpCand) + warp * kWarpCand;
+  uint32_t* qid = sm.pool + warp * kQ;
+  uint32_t* qw = sm.pool + kConsWarps * kQ + warp * kQ;
+  uint16_t* qx = reinterpret_cast<uint16_t*>(sm.pool + 2 * kConsWarps * kQ) + warp * kQ;
+  for (;;) {
+    const uint32_t sl0 = q % kSlots;
+    if (!mbar_wait(sm.full + sl0, (q / kSlots) & 1u)) {
+      ok = false;
+      break;
+    }
+    const uint4 d = sm.desc[sl0];
+    const uint32_t kind = d.z & 0xFFu;
+    if (kind == kEnd) break;
+    const uint32_t b = d.x, s = d.y, nch = (d.z >> 8) & 0xFFu;
+    RowAcc* ra = p.sc.row(b);
+    if (kind != kStream) {
+      // fused step: a row with a forced token or without allowed tokens, for the service warp
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.empty + sl0);
+      post(b, s, kind, d.w);
+      ++q;
+      continue;
+    }
+
+    // ---- pass 1 over the segment's chunks -------------------------------------------
+    float2 acc[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j] = make_float2(0.f, 0.f);
+    float mt = kNoRef;                 // top-p: this thread's running maximum (its sums' reference)
+    uint32_t wmk = 0;                  // top-p: fkey of the warp's running maximum
+    uint32_t gk = 0;                   // top-p: the row's running maximum as last read
+    uint32_t wn = 0;                   // top-p: candidates this warp buffered in the segment
+    bool lost = false;                 // top-p: a chunk's candidates did not fit the buffer
+    unsigned long long best = 0ull;    // greedy / full: packed (value, id)
+    float bestv = -INFINITY;           // greedy: value of best; full: the bound's reference score
+    float offB = INFINITY;             // full: 23 - bestv log2(e)
+    uint32_t qn = 0;                   // full: this warp's queued exact scores
+    PhRow phr{};
+    unsigned long long seed_best = 0ull;
+    if (MODE == kModeFull) {
+      phr = philox_row(p, b);
+      if (lane == 0) seed_best = ld_relaxed64(&ra->best);  // the row's best so far (other segments)
+    }
+    uint32_t gk_next = 0;              // top-p: a read of the row's running maximum in flight
+    if (MODE == kModeTopP && lane == 0) gk_next = ld_relaxed(&ra->maxkey);
+#pragma unroll 1
+    for (uint32_t k = 0; k < nch; ++k) {
+      const uint32_t qk = q + k, sl = qk % kSlots;
+      if (k > 0 && !mbar_wait(sm.full + sl, (qk / kSlots) & 1u)) {
+        ok = false;
+        break;
+      }
+      if (MODE == kModeTopP) gk = max(gk, gk_next);  // the read issued one chunk earlier
+      const uint32_t ck = s * p.segc + k;
+      const uint32_t ng = min(kGroups, (p.V - ck * kChunk) >> 3);
+      const uint4* r4 = sm.ring4 + sl * kGroups;
+      const uint8_t* m8 = reinterpret_cast<const uint8_t*>(sm.mask32 + sl * kChunkWords);
+      uint4 v0 = kNeg4, v1 = kNeg4;
+      uint32_t mb0 = 0, mb1 = 0;
+      if (g0 < ng) {
+        mb0 = m8[g0];
+        v0 = apply_mask(r4[g0], sm.lut[mb0]);
+      }
+      if (g1 < ng) {
+        mb1 = m8[g1];
+        v1 = apply_mask(r4[g1], sm.lut[mb1]);
+      }
+      if (MODE == kModeTopP) {
+        if (FUSED && p.f.bitmask_out && lane < 16) {
+          const uint32_t wi = ck * kChunkWords + warp * 16 + lane;
+          if (wi < p.W) p.f.bitmask_out[size_t(b) * p.W + wi] = sm.mask32[sl * kChunkWords + warp * 16 + lane];
+        }
+        // the data are in registers: the slot goes back to the producer now
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.empty + sl);
+        const uint32_t a0 = group_pmax(v0), a1 = group_pmax(v1);
+        const float gm = pmax_f(bmax2(a0, a1));
+        // the warp's running maximum, published to the row's (shared with its other segments)
+        const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, fkey(gm));
+        if (lane == 0) {
+          if (wk > 0x007FFFFFu) red_max_u32(&ra->maxkey, wk);
+          gk_next = ld_relaxed(&ra->maxkey);  // for the next chunk's threshold, used then
+        }
+        wmk = max(wmk, wk);
+        // candidates buffered against max(warp maximum, row maximum) - margin: a
+        // superset of the final candidates, filtered at the segment end
+        const uint32_t rk = max(wmk, __shfl_sync(0xFFFFFFFFu, gk, 0));
+        if (rk > 0x007FFFFFu) {
+          const float thr = fkey_inv(rk) - margin;
+          if (thr > -1e29f && thr < 1e29f) {
+            uint32_t k16 = fkey(thr) >> 16;
+            if (bf16key_to_float(k16) < thr) ++k16;
+            const uint32_t t16 = __float_as_uint(bf16key_to_float(k16)) >> 16;
+            const uint32_t t2 = t16 | (t16 << 16);
+            const __nv_bfloat162 tb = *reinterpret_cast<const __nv_bfloat162*>(&t2);
+            const bool f0 = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&a0), tb) != 0u;
+            const bool f1 = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&a1), tb) != 0u;
+            if (wn > kWarpCand / 2 && __any_sync(0xFFFFFFFFu, f0 || f1)) {
+              // thresholds only rise: drop the buffered entries below this one
+              wn = compact_cands(cid, cx, min(wn, kWarpCand), k16);
+            }
+            if (__any_sync(0xFFFFFFFFu, f0 || f1)) {
+              const uint32_t b0 = f0 ? group_ge_bits(v0, t2) : 0u, b1 = f1 ? group_ge_bits(v1, t2) : 0u;
+              const uint32_t n = __popc(b0) + __popc(b1);
+              uint32_t inc = n;
+#pragma unroll
+              for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+                if (lane >= uint32_t(o)) inc += y;
+              }
+              uint32_t pos = wn + inc - n;
+#pragma unroll
+              for (uint32_t h = 0; h < 2; ++h) {
+                uint32_t bits = h ? b1 : b0;
+                const uint4& v = h ? v1 : v0;
+                const uint32_t t0 = ck * kChunk + (h ? g1 : g0) * 8;
+                while (bits) {
+                  const uint32_t e = __ffs(bits) - 1;
+                  bits &= bits - 1;
+                  if (pos < kWarpCand) {
+                    cid[pos] = t0 + e;
+                    cx[pos] = uint16_t(group_bits(v, e));
+                  }
+                  ++pos;
+                }
+              }
+              wn += __shfl_sync(0xFFFFFFFFu, inc, 31);
+              lost = lost || wn > kWarpCand;
+            }
+          } else if (lane == 0) {
+            atomicOr(&ra->flags, 1u);  // non-finite range: the exact path decides
+          }
+        }
+        if (gm > mt) {
+          const float r = ex2((mt - gm) * c);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[j] = __fmul2_rn(acc[j], make_float2(r, r));
+          mt = gm;
+        }
+        const float2 c2 = make_float2(c, c), nmc2 = make_float2(-mt * c, -mt * c);
+        add_exps(acc, v0, c2, nmc2);
+        add_exps(acc, v1, c2, nmc2);
+      } else {
+        if (FUSED && p.f.bitmask_out && lane < 16) {
+          const uint32_t wi = ck * kChunkWords + warp * 16 + lane;
+          if (wi < p.W) p.f.bitmask_out[size_t(b) * p.W + wi] = sm.mask32[sl * kChunkWords + warp * 16 + lane];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.empty + sl);
+        if (MODE == kModeGreedy) {
+          const uint32_t a0 = group_pmax(v0), a1 = group_pmax(v1);
+#pragma unroll
+          for (uint32_t h = 0; h < 2; ++h) {
+            const uint4& v = h ? v1 : v0;
+            const float gm = pmax_f(h ? a1 : a0);
+            if (gm > bestv) {  // strictly: this thread sees ids in increasing order
+              uint32_t e = 0;
+              while (e < 7 && group_at(v, e) != gm) ++e;
+              best = pack_best(gm, ck * kChunk + (h ? g1 : g0) * 8 + e);
+              bestv = gm;
+            }
+          }
+        } else {
+          if (k == 1) {
+            // the bound's first outside reference: the row's best score from its other segments
+            const unsigned long long sb = __shfl_sync(0xFFFFFFFFu, seed_best, 0);
+            if (sb) {
+              const float v = fkey_inv(static_cast<uint32_t>(sb >> 32));
+              if (v > bestv) {
+                bestv = v;
+                offB = 23.f - v * 1.4426950408889634f;
+              }
+            }
+          }
+#pragma unroll 1
+          for (uint32_t h = 0; h < 2; ++h) {
+            const uint4 v = h ? v1 : v0;
+            const uint32_t mb = h ? mb1 : mb0;
+            const uint32_t t0 = ck * kChunk + (h ? g1 : g0) * 8;
+#pragma unroll 1
+            for (uint32_t half = 0; half < 2; ++half) {
+              const uint32_t nib = (mb >> (4 * half)) & 15u;
+              uint4 blk = make_uint4(0u, 0u, 0u, 0u);
+              if (nib) blk = philox_q(p, phr, (t0 >> 2) + half);
+              const uint32_t wa = half ? v.z : v.x, wb = half ? v.w : v.y;
+#pragma unroll
+              for (uint32_t e = 0; e < 4; ++e) {
+                const uint32_t wd = e < 2 ? wa : wb;
+                const float x = (e & 1u) ? hi_f(wd) : lo_f(wd);
+                const uint32_t w = e == 0 ? blk.x : e == 1 ? blk.y : e == 2 ? blk.z : blk.w;
+                // the token's score can beat bestv only if 2^23 exp(z - bestv)
+                // (slightly enlarged) exceeds 2^23 - 1 - (w >> 9), i.e. the
+                // bound -ln(1 - u) of its noise reaches bestv - z
+                const float tq = ex2(fmaf(x, c, offB)) * 1.0001f;
+                const float vv = __uint_as_float((w >> 9) ^ 0x4B7FFFFFu) - 8388608.0f;
+                const bool pass = ((nib >> e) & 1u) && vv < tq;
+                const unsigned bal = __ballot_sync(0xFFFFFFFFu, pass);
+                if (bal) {
+                  const uint32_t pos = qn + __popc(bal & lt);
+                  if (pass) {
+                    qid[pos] = t0 + 4 * half + e;
+                    qw[pos] = w;
+                    qx[pos] = uint16_t((e & 1u) ? (wd >> 16) : (wd & 0xFFFFu));
+                  }
+                  qn += __popc(bal);
+                }
+              }
+              while (qn >= 32) {
+                __syncwarp();
+                drain_queue(qid, qw, qx, qn - 32, 32, temp, best, bestv, offB);
+                qn -= 32;
+                __syncwarp();
+              }
+            }
+          }
+        }
+      }
+    }
+    if (!__all_sync(0xFFFFFFFFu, ok)) {
+      ok = false;
+      break;
+    }
+
+    // ---- segment end (this warp's slice) ------------------------------------------------
+    const uint32_t slice = s * kConsWarps + warp;
+    if (MODE == kModeTopP) {
+      // the slice's maximum and its threads' sums rescaled to it
+      const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, fkey(mt));
+      const float wm = fkey_inv(wk);  // kNoRef: nothing allowed in the slice
+      const float a = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+      float part = (wm > kNoRef && a > 0.f) ? a * ex2((mt - wm) * c) : 0.f;
+      part = warp_reduce(part, SumOp());
+      // final candidates: buffered ones >= max(slice maximum, the row's running maximum) - margin
+      uint32_t k16 = kNotFound;
+      if (lane == 0) {
+        p.sc.part(b)[slice] = make_float2(wm, part);
+        if (wm > kNoRef) {
+          const uint32_t g2 = max(gk, ld_relaxed(&ra->maxkey));
+          const float G = g2 > 0x007FFFFFu ? fkey_inv(g2) : -INFINITY;
+          const float thr = fmaxf(wm, G) - margin;
+          if (thr > -1e29f && thr < 1e29f) {
+            k16 = fkey(thr) >> 16;
+            if (bf16key_to_float(k16) < thr) ++k16;
+            red_max_u32(&ra->lowinv, 0x10000u - k16);
+          } else {
+            atomicOr(&ra->flags, 1u);  // non-finite range: the exact path decides
+          }
+        }
+        if (lost) atomicOr(&ra->flags, 1u);  // the buffer overflowed: the exact path decides
+      }
+      k16 = __shfl_sync(0xFFFFFFFFu, k16, 0);
+      // keep the buffered candidates at or above the final threshold (in place, in order)
+      const uint32_t nc = k16 != kNotFound ? compact_cands(cid, cx, min(wn, kWarpCand), k16) : 0u;
+      if (lane == 0) p.sc.nseg(b)[slice] = nc;
+      // Gumbel scores of the candidates into the row's key histogram and
+      // into this slice of the row's candidate list
+      if (nc) {
+        uint32_t* cnt = p.sc.cnt(b);
+        unsigned long long* hbr = p.sc.hbest(b);
+        const uint32_t capW = kListCap / (p.NS * kConsWarps);
+        unsigned long long* lb = p.sc.lbest(b) + slice * capW;
+        uint16_t* lk = p.sc.lkey(b) + slice * capW;
+        const PhRow pr = philox_row(p, b);
+        for (uint32_t i = lane; i < nc; i += 32) {
+          const uint32_t id = cid[i], xb = cx[i];
+          const uint4 blk = philox_q(p, pr, id >> 2);
+          const float score = gumbel_score(bf16_bits_to_float(xb), temp, philox_word(blk, id & 3u));
+          const uint32_t key = bf16_key(xb);
+          const unsigned long long pk = pack_best(score, id);
+          red_add_u32(cnt + (key & (kNB - 1)), 1u);
+          red_max_u64(hbr + (key & (kNB - 1)), pk);
+          if (i < capW) {
+            lb[i] = pk;
+            lk[i] = uint16_t(key);
+          }
+        }
+      }
+      __syncwarp();
+    } else {
+      // greedy / full: the slice's packed maximum into the row's
+      if (MODE == kModeFull && qn) {
+        __syncwarp();
+        drain_queue(qid, qw, qx, 0, qn, temp, best, bestv, offB);
+      }
+      const unsigned long long v = warp_max_u64(best);
+      if (lane == 0 && v) red_max_u64(&ra->best, v);
+    }
+    post(b, s, kStream, 0u);
+    q += nch;
+  }
+  if (!ok) {
+    record_error(p.status, CG_DEV_TIMEOUT);
+    atomicExch(&sm.words[kWAbort], 1u);
+  }
+  post(0u, 0u, kEnd, 0u);
+  if (MODE != kModeTopP) return;
+  // together now: the rows the service warp queued for the exact path, until it is done
+  cbar();
+  uint32_t xhead = 0, it = 0;
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    uint32_t* snap = &sm.words[kWSnap] + 16 * (it & 1u);  // the parity's copy: no copy is rewritten while read
+    if (tid == 0) {
+      // done flag first: a tail read after it holds every row the service queued
+      const uint32_t done = ld_volatile_s(&sm.words[kWSvcDone]) | ld_volatile_s(&sm.words[kWAbort]);
+      __threadfence_block();
+      *snap = ld_volatile_s(&sm.words[kWXTail]) | (done ? 0x80000000u : 0u);
+    }
+    cbar();
+    ++it;
+    const uint32_t v = *snap;
+    while (xhead < (v & 0x7FFFFFFFu)) {
+      const uint32_t b = sm.xq[xhead % kXQ];
+      const uint32_t tok = exact_topp(p, b, row_mask_ptr<FUSED>(p, b), sm.pool, sm.red64, sm.redf, sm.redd,
+                                      &sm.words[kWJ]);
+      cbar();
+      ++xhead;
+      if (tid == 0) {
+        emit<FUSED>(p, b, tok);
+        *reinterpret_cast<volatile uint32_t*>(&sm.words[kWXHead]) = xhead;
+      }
+    }
+    if (v & 0x80000000u) break;
+    if (tid == 0) __nanosleep(200);
+  }
+}
+
+template <int MODE, int FUSED>
+__global__ void __launch_bounds__(kThreads, 2) seg_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(128) unsigned char dsm[];
+  __shared__ __align__(8) uint64_t full[kSlots], empty[kSlots], sq_full[kSQ], sq_empty[kSQ];
+  __shared__ uint4 sq_rec[kSQ];
+  __shared__ unsigned long long red64[kConsWarps + 1];
+  __shared__ float redf[kConsWarps + 1];
+  __shared__ double redd[kConsWarps + 1];
+  __shared__ uint32_t words[32];
+  __shared__ uint32_t xq[kXQ];
+  Smem sm;
+  sm.ring4 = reinterpret_cast<uint4*>(dsm + kOffRing);
+  sm.mask32 = reinterpret_cast<uint32_t*>(dsm + kOffMask);
+  sm.lut = reinterpret_cast<uint4*>(dsm + kOffLut);
+  sm.pool = reinterpret_cast<uint32_t*>(dsm + kOffPool);
+  sm.desc = reinterpret_cast<uint4*>(dsm + kOffDesc);
+  sm.svc_keys = reinterpret_cast<uint16_t*>(dsm + kOffSvc);
+  sm.svc_off = reinterpret_cast<uint32_t*>(dsm + kOffSvc + kListCap * 2);
+  sm.full = full;
+  sm.empty = empty;
+  sm.sq_full = sq_full;
+  sm.sq_empty = sq_empty;
+  sm.sq_rec = sq_rec;
+  sm.red64 = red64;
+  sm.redf = redf;
+  sm.redd = redd;
+  sm.words = words;
+  sm.xq = xq;
+
+  griddep_launch_dependents();
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    for (uint32_t i = 0; i < kSlots; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, kConsWarps);
+    }
+    for (uint32_t i = 0; i < kSQ; ++i) {
+      mbar_init(sq_full + i, kCons);
+      mbar_init(sq_empty + i, 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (uint32_t i = 0; i < 32; ++i) words[i] = 0u;
+  }
+  for (uint32_t i = tid; i < 256; i += kThreads) sm.lut[i] = pair_mask_entry(i);
+  __syncthreads();
+  griddep_wait();  // the logits, the bitmask or the rows' states come from earlier work on the stream
+
+  if (warp == kProdWarp) {
+    if (lane == 0) words[kWIssued] = produce<FUSED>(p, dsm, full, empty, sm.desc, &words[kWAbort]);
+  } else if (warp == kSvcWarp) {
+    service<MODE, FUSED>(p, sm);
+  } else {
+    consume<MODE, FUSED>(p, sm);
+  }
+  __syncthreads();
+  if (tid == 0 && words[kWAbort]) {
+    // a wait ran out: let the copies still in flight land before the shared
+    // memory is released (again with bounded waits)
+    const uint32_t used = words[kWIssued];
+    for (uint32_t sl = 0; sl < kSlots && sl < used; ++sl) {
+      const uint32_t last = used - 1 - ((used - 1 - sl) % kSlots);  // last sequence index of slot sl
+      mbar_wait(full + sl, (last / kSlots) & 1u);
+    }
+  }
+}
+
+// ---- host side ---------------------------------------------------------------------------
+
+// Chunks per segment: the largest of 4, 2, 1 that still gives the grid a few
+// segments per CTA, among those that keep a row within kMaxNS segments.
+uint32_t segs_for(uint32_t B, uint32_t nchunks, uint32_t grid) {
+  uint32_t pick = 0;
+  for (uint32_t sc = 1; sc <= kMaxSegChunks; sc *= 2) {
+    const uint32_t ns = (nchunks + sc - 1) / sc;
+    if (ns > kMaxNS) continue;
+    if (pick == 0 || uint64_t(B) * ns >= uint64_t(4) * grid) pick = sc;
+  }
+  return pick;  // seg_usable() guarantees that sc = kMaxSegChunks fits
+}
+
+struct Occ {
+  int sms = 0, per_sm = 0;
+};
+template <int MODE, int FUSED>
+cudaError_t occupancy(Occ* o) {
+  static std::mutex mu;
+  static std::map<int, Occ> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = done.find(dev);
+  if (it != done.end()) {
+    *o = it->second;
+    return cudaSuccess;
+  }
+  auto* k = seg_kernel<MODE, FUSED>;
+  if ((e = allow_smem(reinterpret_cast<const void*>(k), kSmem)) != cudaSuccess) return e;
+  Occ r;
+  if ((e = cudaDeviceGetAttribute(&r.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r.per_sm, k, kThreads, kSmem)) != cudaSuccess) return e;
+  if (r.per_sm < 1) return cudaErrorInvalidConfiguration;
+  done[dev] = r;
+  *o = r;
+  return cudaSuccess;
+}
+
+template <int MODE, int FUSED>
+cudaError_t launch(Params& p, void* scratch, uint32_t B, uint32_t V, cudaStream_t stream) {
+  Occ o;
+  cudaError_t e = occupancy<MODE, FUSED>(&o);
+  if (e != cudaSuccess) return e;
+  const uint32_t grid_max = uint32_t(o.sms) * uint32_t(o.per_sm);
+  p.nchunks = (V + kChunk - 1) / kChunk;
+  p.segc = segs_for(B, p.nchunks, grid_max);
+  p.NS = (p.nchunks + p.segc - 1) / p.segc;
+  p.N = B * p.NS;
+  p.sc.base = static_cast<unsigned char*>(scratch);
+  const uint32_t grid = std::min<uint32_t>(grid_max, p.N);
+  return launch_dependent(seg_kernel<MODE, FUSED>, dim3(grid), dim3(kThreads), size_t(kSmem), stream, p);
+}
+
+// Philox round keys of the seed and the step's first-round product.
+void set_philox(Params& p, uint64_t seed, uint32_t step) {
+  uint32_t k0 = uint32_t(seed), k1 = uint32_t(seed >> 32);
+  for (int r = 0; r < 10; ++r) {
+    p.rk[2 * r] = k0;
+    p.rk[2 * r + 1] = k1;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  const uint64_t m = uint64_t(kM1) * step;
+  p.ph_lo1 = uint32_t(m);
+  p.ph_hi1 = uint32_t(m >> 32);
+  p.step = step;
+}
+
+template <int FUSED>
+cudaError_t launch_mode(Params& p, void* scratch, uint32_t B, uint32_t V, cudaStream_t stream) {
+  if (p.temp == 0.f) return launch<kModeGreedy, FUSED>(p, scratch, B, V, stream);
+  if (p.top_p >= 1.f) return launch<kModeFull, FUSED>(p, scratch, B, V, stream);
+  return launch<kModeTopP, FUSED>(p, scratch, B, V, stream);
+}
+
+}  // namespace seg
+
+// Scratch bytes of the segmented sampler for B rows (zero before the first
+// launch; every launch leaves it at zero).
+size_t seg_scratch_bytes(uint32_t B) { return seg::kCtlBytes + size_t(B) * seg::kRowStride; }
+
+// The segmented sampler takes bf16 rows of V % 8 == 0 logits at 16-byte
+// aligned addresses, up to kMaxNS x 4 chunks, without the optional outputs.
+bool seg_usable(int dtype, uint32_t V, const void* logits, float* probs, int inplace) {
+  const uint32_t nchunks = (V + seg::kChunk - 1) / seg::kChunk;
+  return dtype == CG_BF16 && V % 8 == 0 && V > 0 && nchunks <= seg::kMaxNS * seg::kMaxSegChunks &&
+         (reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && probs == nullptr && inplace == 0;
+}
+
+// cg_mask_and_sample through the segmented sampler (the bitmask must have
+// W % 4 == 0 words per row at a 16-byte aligned address).
+bool seg_bitmask_ok(uint32_t W, const void* bitmask) {
+  return W % 4 == 0 && (reinterpret_cast<uintptr_t>(bitmask) & 15u) == 0;
+}
+
+cudaError_t launch_seg_sample(const void* logits, uint32_t B, uint32_t V, uint32_t W, const uint32_t* bitmask,
+                              float temp, float top_p, uint64_t seed, uint32_t step, uint32_t* out_tok,
+                              void* scratch, uint32_t* status, cudaStream_t stream) {
+  if (B == 0) return cudaSuccess;
+  seg::Params p{};
+  p.logits = static_cast<const uint16_t*>(logits);
+  p.V = V;
+  p.W = W;
+  p.B = B;
+  p.bitmask = bitmask;
+  p.temp = temp;
+  p.top_p = top_p;
+  seg::set_philox(p, seed, step);
+  p.out_tok = out_tok;
+  p.status = status;
+  return seg::launch_mode<0>(p, scratch, B, V, stream);
+}
+
+cudaError_t launch_seg_step(const Tables& t, const uint32_t* states, const uint16_t* gid, const int32_t* forced,
+                            uint32_t B, const void* logits, uint32_t V, float temp, float top_p, uint64_t seed,
+                            uint32_t step, uint32_t* counts, uint32_t max_tokens, uint32_t* bitmask_out,
+                            uint32_t* out_tok, uint32_t* out_states, uint8_t* out_flags, void* scratch,
+                            const DevGrammar* host_grammars, cudaStream_t stream) {
+  if (B == 0) return cudaSuccess;
+  seg::Params p{};
+  p.logits = static_cast<const uint16_t*>(logits);
+  p.V = V;
+  p.W = t.W;
+  p.B = B;
+  p.temp = temp;
+  p.top_p = top_p;
+  seg::set_philox(p, seed, step);
+  p.out_tok = out_tok;
+  p.status = t.status;
+  seg::Fused& f = p.f;
+  f.t = t;
+  f.states = states;
+  f.gid = gid;
+  f.forced = forced;
+  f.counts = counts;
+  f.max_tokens = max_tokens;
+  f.out_states = out_states;
+  f.out_flags = out_flags;
+  f.bitmask_out = bitmask_out;
+  f.n_pg = 0;
+  if (host_grammars && t.n_g <= 8) {
+    for (uint32_t i = 0; i < t.n_g; ++i) f.pg[i] = host_grammars[i];
+    f.n_pg = t.n_g;
+  }
+  return seg::launch_mode<1>(p, scratch, B, V, stream);
+}
+
+}  // namespace cgk

@@ -329,6 +329,8 @@ extern "C" {
 int cg_pda_create(cg_ctx* c, const cg_vocab* v, const cg_pda_grammar* g, cg_pda** out) {
   if (!c || !v || !g || !out) return CG_E_ARG;
   *out = nullptr;
+  cgk::DeviceGuard dg(cgk::ctx_device(c));
+  if (!dg.ok) return CG_E_CUDA;
   const cgk::CtxView view = cgk::ctx_view(c);
   if (v->V != view.t.V) return CG_E_ARG;
   const uint32_t V = v->V, W = view.t.W, S = g->n_states, D = g->depth;
@@ -437,8 +439,11 @@ int cg_pda_create(cg_ctx* c, const cg_vocab* v, const cg_pda_grammar* g, cg_pda*
 
 void cg_pda_destroy(cg_pda* p) {
   if (!p) return;
-  cudaStreamSynchronize(p->stream);
-  pda_release(p);
+  {
+    cgk::DeviceGuard dg(cgk::ctx_device(p->ctx));
+    cudaStreamSynchronize(p->stream);
+    pda_release(p);
+  }
   delete p;
 }
 
@@ -456,6 +461,8 @@ int cg_pda_fill_bitmask(cg_pda* p, const uint32_t* d_cfg, uint32_t B, const int3
                         uint32_t* d_bitmask) {
   if (!p || (B && (!d_cfg || !d_bitmask))) return CG_E_ARG;
   if (B == 0) return CG_OK;
+  cgk::DeviceGuard dg(cgk::ctx_device(p->ctx));
+  if (!dg.ok) return CG_E_CUDA;
   const size_t smem = pda_fill_smem(p->d, p->t.W);
   return cgk::launch_dependent(cgk::pda_fill_kernel, dim3(B), dim3(cgk::kPdaFillThreads), smem, p->stream, p->d,
                                p->t, d_cfg, d_forced, d_bitmask) == cudaSuccess
@@ -467,6 +474,8 @@ int cg_pda_accept(cg_pda* p, uint32_t* d_cfg, uint32_t B, const uint32_t* d_toks
                   uint32_t* d_counts, uint32_t max_tokens, uint8_t* d_out_flags) {
   if (!p || (B && (!d_cfg || !d_toks || !d_out_flags))) return CG_E_ARG;
   if (B == 0) return CG_OK;
+  cgk::DeviceGuard dg(cgk::ctx_device(p->ctx));
+  if (!dg.ok) return CG_E_CUDA;
   const uint32_t grid = (B + cgk::kPdaAcceptThreads - 1) / cgk::kPdaAcceptThreads;
   return cgk::launch_dependent(cgk::pda_accept_kernel, dim3(grid), dim3(cgk::kPdaAcceptThreads),
                                pda_accept_smem(p->d), p->stream,
@@ -482,6 +491,8 @@ int cg_pda_accept_many(cg_pda* p, uint32_t* d_cfg, uint32_t B, const uint32_t* d
   if (!p || (B && (!d_cfg || !d_draft || !d_draft_len || !d_out_n || !d_out_flags || K == 0))) return CG_E_ARG;
   if (d_counts && max_tokens == 0) return CG_E_ARG;
   if (B == 0) return CG_OK;
+  cgk::DeviceGuard dg(cgk::ctx_device(p->ctx));
+  if (!dg.ok) return CG_E_CUDA;
   const uint32_t grid = (B + cgk::kPdaAcceptThreads - 1) / cgk::kPdaAcceptThreads;
   return cgk::launch_dependent(cgk::pda_accept_many_kernel, dim3(grid), dim3(cgk::kPdaAcceptThreads),
                                pda_accept_smem(p->d), p->stream, p->d, p->t, d_cfg, B, d_draft, d_draft_len, d_forced,
@@ -498,6 +509,8 @@ int cg_pda_step(cg_pda* p, uint32_t* d_cfg, uint32_t B, void* d_logits, int dtyp
   if (V != p->t.V || !(temp >= 0.f) || temp == INFINITY || !(top_p == top_p)) return CG_E_ARG;
   if (d_counts && max_tokens == 0) return CG_E_ARG;
   if (B == 0) return CG_OK;
+  cgk::DeviceGuard dg(cgk::ctx_device(p->ctx));
+  if (!dg.ok) return CG_E_CUDA;
   void* scratch = nullptr;
   int rc = cgk::ctx_sample_scratch(p->ctx, cgk::sample_scratch_bytes(B, V), &scratch);
   if (rc != CG_OK) return rc;
@@ -532,6 +545,8 @@ int cg_pda_accept_fill(cg_pda* p, uint32_t* d_cfg, uint32_t B, const uint32_t* d
                        uint32_t* d_bitmask) {
   if (!p || (B && (!d_cfg || !d_toks || !d_out_flags || !d_bitmask))) return CG_E_ARG;
   if (B == 0) return CG_OK;
+  cgk::DeviceGuard dg(cgk::ctx_device(p->ctx));
+  if (!dg.ok) return CG_E_CUDA;
   return cgk::launch_dependent(cgk::pda_accept_fill_kernel, dim3(B), dim3(cgk::kPdaFillThreads),
                                pda_fill_smem(p->d, p->t.W), p->stream, p->d, p->t, d_cfg, d_toks, d_forced, d_counts,
                                max_tokens, d_out_flags, d_forced_next, d_bitmask) == cudaSuccess

@@ -210,6 +210,16 @@ int cg_ctx_status(cg_ctx* c, uint32_t* dev_code);
  * Errors: CG_E_ARG, CG_E_CUDA. */
 int cg_ctx_prefill(cg_ctx* c);
 
+/* Mask-cache behaviour of the fused step (cg_step) on a context without
+ * cg_ctx_prefill: before each step a pass over the rows computes the class
+ * masks not yet in the cache (labs.miniml.ai "Evaluator aware decoding",
+ * "Where XGrammar-2 could take this", on the token mask cache).
+ *  lookups  : rows of automaton states that looked their class up (hits + misses)
+ *  computed : class masks computed because a row missed them
+ * Counted since the context was created; synchronises the context's stream.
+ * Either output may be NULL.  Errors: CG_E_ARG, CG_E_CUDA. */
+int cg_ctx_cache_stats(cg_ctx* c, uint64_t* lookups, uint64_t* computed);
+
 /* Step 1 -- which tokens may follow each row's state (usetacet.com/docs/grammar,
  * "The guarantee"; a mask depends on the automaton state alone and is known
  * before the step, labs.miniml.ai "Why isn't this in production APIs yet?").

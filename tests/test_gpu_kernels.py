@@ -85,19 +85,23 @@ def _sampler_case(V, dtype, temp, top_p, B=13, seed=3, boost=4.0, frac=0.05, den
         # ties: a block of equal logits
         x[4, :40] = x[4, 0]
         xt[4, :40] = xt[4, 0]
-    out = empty((B,), torch.int32)
-    probs = empty((B, V), torch.float32)
-    ctx.mask_and_sample(xt, u32(bm), temp, top_p, 0xABCDEF0123, 5, out, probs=probs)
-    assert ctx.status() == 0
-    got = host(out).view(np.uint32)
-    gp = host(probs)
-    for b in range(B):
-        res = sample_row(x[b], masks[b], temp, top_p, 0xABCDEF0123, b, 5)
-        if temp == 0.0:
-            assert got[b] == res.tok, (b, got[b], res.tok)
-        else:
-            assert same_token(int(got[b]), res), (b, got[b], res.tok, res.gap, res.margin)
-        assert np.max(np.abs(gp[b] - res.probs)) <= 1e-5, b
+    # with probabilities requested (the per-row kernels), then without (the
+    # segmented sampler for bf16 rows)
+    for want_probs in (True, False):
+        out = empty((B,), torch.int32)
+        probs = empty((B, V), torch.float32) if want_probs else None
+        ctx.mask_and_sample(xt, u32(bm), temp, top_p, 0xABCDEF0123, 5, out, probs=probs)
+        assert ctx.status() == 0
+        got = host(out).view(np.uint32)
+        gp = host(probs) if want_probs else None
+        for b in range(B):
+            res = sample_row(x[b], masks[b], temp, top_p, 0xABCDEF0123, b, 5)
+            if temp == 0.0:
+                assert got[b] == res.tok, (want_probs, b, got[b], res.tok)
+            else:
+                assert same_token(int(got[b]), res), (want_probs, b, got[b], res.tok, res.gap, res.margin)
+            if want_probs:
+                assert np.max(np.abs(gp[b] - res.probs)) <= 1e-5, b
 
 
 @pytest.mark.parametrize("V", [512, 4013, 32000])
@@ -237,13 +241,15 @@ def test_single_pass_topp_branches(case, temp, top_p):
     x, xt, masks = _topp_rows(V, B, case, rng)
     from oracle.step import pack_bitmask
     bm = u32(np.stack([pack_bitmask(m) for m in masks]))
-    out = empty((B,), torch.int32)
-    probs = empty((B, V), torch.float32)
-    ctx.mask_and_sample(xt, bm, temp, top_p, 99, 3, out, probs=probs)
-    assert ctx.status() == 0
-    got = host(out).view(np.uint32)
-    gp = host(probs)
-    for b in range(B):
-        res = sample_row(x[b], masks[b], temp, top_p, 99, b, 3)
-        assert same_token(int(got[b]), res), (case, b, got[b], res.tok, res.gap, res.margin, res.nucleus_size)
-        assert np.max(np.abs(gp[b] - res.probs)) <= 1e-5, (case, b)
+    for want_probs in (True, False):
+        out = empty((B,), torch.int32)
+        probs = empty((B, V), torch.float32) if want_probs else None
+        ctx.mask_and_sample(xt, bm, temp, top_p, 99, 3, out, probs=probs)
+        assert ctx.status() == 0
+        got = host(out).view(np.uint32)
+        for b in range(B):
+            res = sample_row(x[b], masks[b], temp, top_p, 99, b, 3)
+            assert same_token(int(got[b]), res), (case, want_probs, b, got[b], res.tok, res.gap, res.margin,
+                                                  res.nucleus_size)
+            if want_probs:
+                assert np.max(np.abs(host(probs)[b] - res.probs)) <= 1e-5, (case, b)
