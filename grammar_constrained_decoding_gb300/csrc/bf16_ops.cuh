@@ -55,6 +55,21 @@ __device__ __forceinline__ uint4 pair_mask_entry(uint32_t i) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// The same four pair masks computed from the byte itself: multiplying its low
+// (high) nibble by 0x10204080 (0x01020408) puts mask bit i of the nibble on
+// the top bit of byte i of the product (the sixteen shifted copies land on
+// distinct bits, so nothing carries), and prmt's sign mode (selector nibble
+// 8 + byte) spreads each top bit over a byte.
+__device__ __forceinline__ uint32_t prmt_sign(uint32_t x, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(x), "r"(sel));
+  return r;
+}
+__device__ __forceinline__ uint4 pair_mask_of(uint32_t mb) {
+  const uint32_t r0 = (mb & 0x0Fu) * 0x10204080u, r1 = (mb & 0xF0u) * 0x01020408u;
+  return make_uint4(prmt_sign(r0, 0x9988u), prmt_sign(r0, 0xBBAAu), prmt_sign(r1, 0x9988u), prmt_sign(r1, 0xBBAAu));
+}
+
 __device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

@@ -154,9 +154,7 @@ int ctx_sample_scratch(cg_ctx* c, size_t bytes, void** out) {
 // synchronise the device and can fail once a server has planned all of its
 // memory at start-up.  Shared by every call on a device (calls that may
 // overlap race on it).
-constexpr size_t kNoAllocListBytes = size_t(CG_NOALLOC_MAX_ROWS) * 8192 * 6;
-constexpr size_t kNoAllocSegBytes = size_t(3) << 20;  // 3 MiB
-constexpr size_t kNoAllocScratchBytes = kNoAllocListBytes + kNoAllocSegBytes;
+constexpr size_t kNoAllocScratchBytes = cgk::kNoAllocListBytes + cgk::kNoAllocSegBytes;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace {
@@ -433,8 +431,8 @@ int cg_mask_and_sample_noalloc(cg_ctx* c, void* d_logits, int dtype, uint32_t B,
                                const uint32_t* d_bitmask, float temp, float top_p, uint64_t seed, uint32_t step,
                                uint32_t* d_out_tok, float* d_probs, uint32_t flags) {
   if (!sample_args_ok(c, d_logits, dtype, B, V, d_bitmask, temp, top_p, d_out_tok, flags)) return CG_E_ARG;
-  if (B > CG_NOALLOC_MAX_ROWS || cgk::sample_scratch_bytes(B, V) > kNoAllocListBytes ||
-      cgk::seg_scratch_bytes(B) > kNoAllocSegBytes)
+  if (B > CG_NOALLOC_MAX_ROWS || cgk::sample_scratch_bytes(B, V) > cgk::kNoAllocListBytes ||
+      cgk::seg_scratch_bytes(B) > cgk::kNoAllocSegBytes)
     return CG_E_LIMIT;
   if (B == 0) return CG_OK;
   cgk::DeviceGuard dg(c->device);
@@ -444,7 +442,7 @@ int cg_mask_and_sample_noalloc(cg_ctx* c, void* d_logits, int dtype, uint32_t B,
   if (!scratch) return CG_E_CUDA;
   const int inplace = (flags & CG_SAMPLE_INPLACE) ? 1 : 0;
   const bool seg_path = cgk::seg_usable(dtype, V, d_logits, d_probs, inplace) && cgk::seg_bitmask_ok(c->t.W, d_bitmask);
-  unsigned char* seg = scratch + kNoAllocListBytes;
+  unsigned char* seg = scratch + cgk::kNoAllocListBytes;
   // the segmented sampler's part starts at zero: cleared here, whatever an
   // earlier call (or one that ran out of a bounded wait) left in it
   if (seg_path && cudaMemsetAsync(seg, 0, cgk::seg_scratch_bytes(B), c->stream) != cudaSuccess) return CG_E_CUDA;

@@ -80,6 +80,15 @@ int ctx_sample_scratch(cg_ctx* c, size_t bytes, void** out);
 // The device a context was created on.
 int ctx_device(const cg_ctx* c);
 
+// The fixed scratch of cg_mask_and_sample_noalloc (ctx.cu): the per-row
+// sampler's candidate lists (kSampleListEntries u32 ids and u16 keys a row),
+// then the segmented sampler's counters and row blocks, for
+// CG_NOALLOC_MAX_ROWS rows.  Each sampler static_asserts that its layout for
+// that many rows fits.
+constexpr uint32_t kSampleListEntries = 8192;
+constexpr size_t kNoAllocListBytes = size_t(CG_NOALLOC_MAX_ROWS) * kSampleListEntries * 6;
+constexpr size_t kNoAllocSegBytes = size_t(7) << 20;
+
 // Makes a device current for the duration of a call and puts the caller's
 // back: every launch, allocation and symbol lookup of a library call then
 // happens on the device its context's tables live on.

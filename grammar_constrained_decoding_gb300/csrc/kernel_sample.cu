@@ -324,6 +324,7 @@ constexpr uint32_t kWinRowsMax = 512;                           // states in the
 constexpr uint32_t kWinBytesMax = 16384;                        // shared memory for that window
 constexpr uint32_t kSlots = 16;                                 // list entries per thread after the stream
 constexpr uint32_t kCandPerRow = kThreads * kSlots;             // candidate list entries per row (8192)
+static_assert(kCandPerRow == kSampleListEntries, "the no-allocation scratch holds the rows' lists");
 constexpr uint32_t kBatchIds = 4;                               // nucleus id loads in flight per thread
 
 // Prefix sums over bins 0..kBins-1 (bin = thread; q = this thread's bin mass),

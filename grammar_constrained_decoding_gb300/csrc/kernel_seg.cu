@@ -11,40 +11,37 @@
 // (t>>2, b, step, 0).
 //
 // Work decomposition.  Each row is cut into segments of up to four 4096-logit
-// chunks; a persistent grid (two CTAs per SM) takes segments (row-major) from
-// a work counter, so the bytes each SM streams differ by at most a segment.
-// A CTA has three roles.  The producer warp resolves each segment's mask
-// source (the caller's bitmask, or in the fused step the row's mask class in
-// the mask cache) one segment ahead and streams the segment's logits and mask
-// words into an 8-slot shared-memory ring with bulk asynchronous copies.
-// Eight consumer warps take each chunk 16 logits per thread.  The service
-// warp does the cross-CTA bookkeeping off the consumers' path: per finished
-// segment it counts the row's done segments (a fence and an atomic), and the
-// CTA that completes a row finishes it there (the token, and in the fused step
-// the accept) while the consumers stream on.
+// chunks; a persistent grid (two CTAs per SM) takes segments from a work
+// counter in segment-major order (segment s of every row before segment s + 1,
+// so that a row's running maximum is mostly known before its later segments
+// are read), and the bytes each SM streams differ by at most a segment.  A CTA
+// has three roles.  The producer warp resolves each segment's mask source (the
+// caller's bitmask, or in the fused step the row's mask class in the mask
+// cache) ahead of time and streams the segment's logits and mask words into an
+// 8-slot shared-memory ring with bulk asynchronous copies.  Eight consumer
+// warps take each segment together, 64 logits per thread (two 8-logit groups
+// of each chunk).  The service warp counts each row's finished segments (a
+// fence and an atomic per segment, off the consumers' path).  Once the stream
+// is done, the consumers finish the rows their CTA owns (b = blockIdx.x +
+// k gridDim.x), each as soon as every segment of it is counted.
 //
-// Top-p, per segment.  Pass 1 (as the chunks land): masked logits, packed
-// bf16 group maxima kept in registers, and exp2((x - m) c) summed against the
-// thread's running maximum m (so that the sum does not depend on timing);
-// each warp publishes its chunk maximum to the row's running maximum in
-// global memory.  Segment end: the segment maximum m_s and S_s = sum over the
-// segment of exp2((x - m_s) c) are stored for the row; the candidate
-// threshold is max(m_s, the row's running maximum) minus a margin of kMarginZ
-// nats -- never above M - margin, M the row maximum, so every allowed logit
-// within the margin of M becomes a candidate.  Pass 2: the groups whose packed
-// maximum reaches the threshold are re-read from the ring (still held) and
-// their candidates pooled in shared memory; each candidate's Gumbel score is
-// drawn and recorded twice: in the row's key histogram in global memory (bin
-// = 16-bit bf16 key mod kNB: the count of the candidates with that key and
-// their best packed (score, id)) and in the segment's slice of the row's
-// candidate list.  The row's finisher takes M and S from the segments'
-// (m_s, S_s); tau is the largest key whose upper set carries top_p * S (masses
-// count x exp2((x - M) c) in 2^-40 fixed point, so sums do not depend on
-// order): from the histogram when the candidates' keys span fewer than kNB
-// keys, else from the list (masses per high key byte, then per key); the token
-// is the best packed score at or above tau.  A row whose list overflowed, or
-// whose nucleus reaches below the margin, is handed back to the consumers for
-// the exact multi-pass path over the row (same result).
+// Top-p, per segment and consumer warp (a "slice").  The thread's groups of
+// every chunk are loaded and masked at once and the ring slots released; the
+// slice maximum m_s goes to the row's running maximum in global memory, and
+// S_s = sum over the slice of exp2((x - m_s) c) (each thread against its own
+// maximum, rescaled once) is stored with m_s.  Candidates are the slice's
+// allowed logits at or above max(m_s, the row's running maximum) - margin
+// (kMarginZ nats), never above M - margin with M the row maximum, so every
+// allowed logit within the margin of M is one; the warp writes them (token
+// id, bf16 bits) into its region of the row's candidate list.  The row's
+// finisher merges M and S from the slices, gathers the candidates at or above
+// M - margin into shared memory and finds tau, the largest key whose upper
+// set carries top_p S (masses count exp2((x - M) c) in 2^-40 fixed point, so
+// sums do not depend on order), from 32-key mass bins and then the keys of
+// the bin where the target is reached; the token is the best Gumbel score
+// among the candidates at or above tau.  A row whose list region overflowed,
+// with more candidates than the finisher holds, or whose nucleus reaches below
+// the margin takes the exact multi-pass path over the row (same result).
 //
 // Greedy keeps each thread's best (x, lowest id).  Gumbel-max over every
 // allowed token (top_p >= 1) draws the Philox block of each group of four
@@ -59,11 +56,11 @@
 // accepts the token when the row finishes.
 //
 // Device scratch (the context's, zero before the first launch): a work counter
-// pair and, per row, accumulators, the segments' partial sums, the key
-// histogram and the candidate list.  Every launch leaves the counters, the
-// accumulators and the histogram at zero again: the last CTA to stop taking
-// work resets the counters and each row's finisher clears its accumulators and
-// the histogram bins its candidates touched.
+// pair and, per row, accumulators, the slices' partial sums and candidate
+// counts, and the candidate list.  Every launch leaves the counters and the
+// accumulators at zero again (the last CTA to stop taking work resets the
+// counters; each row's finisher its accumulators); slices, counts and lists are
+// written in full before they are read.
 #include <algorithm>
 #include <map>
 #include <mutex>
@@ -89,12 +86,12 @@ constexpr uint32_t kChunkWords = kChunk / 32;              // mask words per slo
 constexpr uint32_t kGroups = kChunk / 8;                   // 8-logit groups per slot
 constexpr uint32_t kMaxSegChunks = 4;
 constexpr uint32_t kSlots = 8;                             // two segments of four chunks in flight
-constexpr uint32_t kNB = 1024;                             // key-histogram bins per row
-constexpr uint32_t kWarpCand = 256;                        // candidates a consumer warp holds per segment
 constexpr uint32_t kMaxNS = 64;                            // segments per row
 constexpr uint32_t kSlices = kMaxNS * kConsWarps;          // (segment, consumer warp) partials per row
 constexpr uint32_t kWindow = 4096;                         // per-key counters of the exact path
-constexpr uint32_t kListCap = 2048;                        // candidate-list entries per row
+constexpr uint32_t kListCap = 16384;                       // candidate-list entries per row (split among its slices)
+constexpr uint32_t kFinCap = 8192;                         // candidates a row's finisher holds (in the idle ring)
+constexpr uint32_t kCoarse = 2048;                         // finisher: mass bins of 32 keys below the maximum key
 constexpr uint32_t kSQ = 16;                               // records queued for the service warp (> kSlots)
 constexpr uint32_t kQ = 160;                               // queued exact scores per consumer warp (full)
 constexpr float kMarginZ = 8.5f;                           // nats below the maximum kept as candidates
@@ -106,15 +103,18 @@ static_assert(kGroups == 2 * kCons, "two groups per consumer thread and slot");
 // dynamic shared memory
 constexpr uint32_t kOffRing = 0;
 constexpr uint32_t kOffMask = kOffRing + kSlots * kChunkBytes;
-constexpr uint32_t kOffLut = kOffMask + kSlots * kChunkWords * 4;
-constexpr uint32_t kOffPool = kOffLut + 256 * 16;
-constexpr uint32_t kPoolBytes = kWindow * 4;               // candidate buffers, exact-score queues, exact path's counters
+constexpr uint32_t kOffPool = kOffMask + kSlots * kChunkWords * 4;
+constexpr uint32_t kPoolBytes = (kCoarse + 32) * 8 + kConsWarps * (kMaxNS + 2) * 4;  // exact-score queues, the exact
+                                                           // path's counters, the finisher's mass bins and offsets
 constexpr uint32_t kOffDesc = kOffPool + kPoolBytes;
-constexpr uint32_t kOffSvc = kOffDesc + kSlots * 16;       // the service warp's list keys, histogram, offsets
-constexpr uint32_t kSvcBytes = kListCap * 2 + (kSlices + 4) * 4;
-constexpr uint32_t kSmem = kOffSvc + kSvcBytes;
-static_assert(kConsWarps * kWarpCand * 6 <= kPoolBytes, "candidate buffers fit the pool region");
+constexpr uint32_t kSmem = kOffDesc + kSlots * 16;
+// Once a CTA's stream is over (no copy in flight) its finisher keeps the
+// candidates of the row it finishes in the ring: ids, then bf16 bits.
+constexpr uint32_t kOffFin = kOffRing;
+static_assert(kFinCap * 6 <= kSlots * kChunkBytes, "the finisher's candidates fit the ring");
+static_assert(kWindow * 4 <= kPoolBytes, "the exact path's counters fit the pool region");
 static_assert(kConsWarps * kQ * 10 <= kPoolBytes, "exact-score queues fit the pool region");
+static_assert(kSmem <= 111 * 1024, "two CTAs a multiprocessor");
 
 enum Mode { kModeGreedy = 0, kModeTopP = 1, kModeFull = 2 };
 // kinds of ring descriptors and service records
@@ -122,27 +122,29 @@ constexpr uint32_t kStream = 0, kEmptyRow = 1, kForcedRow = 2, kNone = 3, kEnd =
 
 struct RowAcc {
   uint32_t maxkey;            // fkey of the running maximum logit published by the row's segments
-  uint32_t done;              // segments finished
-  uint32_t lowinv;            // max over segments of 0x10000 - (lowest candidate key)
-  uint32_t flags;             // bit 0: a segment's candidates overflowed the pool, or a non-finite range
+  uint32_t done;              // segments counted
+  uint32_t flags;             // bit 0: a slice's candidates overflowed its list region, or a non-finite range
+  uint32_t pad;
   unsigned long long best;    // greedy / full: packed (value, id) maximum
-  unsigned long long pad;
+  unsigned long long pad2;
 };
 
 // Per-row block of the scratch, at the same place whatever the batch size or
 // segment count of a launch (so that what one launch leaves at zero is zero
 // for the next): accumulators, each (segment, consumer warp) slice's partial
-// maximum and sum and its candidate count, the key histogram, and the
-// candidate list (slice i writes its candidates, as packed (score, id) and
-// 16-bit key, into entries [i c, i c + c), c = kListCap / (NS kConsWarps)).
+// maximum and sum and its candidate count, and the candidate list: slice i
+// writes its candidates (token id, bf16 bits) into entries [i c, i c + c),
+// c = kListCap / (NS kConsWarps).  Slices and counts are written in full by
+// every launch; only the accumulators must start at zero.
 constexpr uint32_t kRowPart = 32;                                   // after RowAcc
 constexpr uint32_t kRowNSeg = kRowPart + kSlices * 8;
-constexpr uint32_t kRowCnt = kRowNSeg + kSlices * 4;
-constexpr uint32_t kRowBest = kRowCnt + kNB * 4;
-constexpr uint32_t kRowLBest = kRowBest + kNB * 8;
-constexpr uint32_t kRowLKey = kRowLBest + kListCap * 8;
-constexpr uint32_t kRowStride = (kRowLKey + kListCap * 2 + 127) & ~127u;
+constexpr uint32_t kRowLId = kRowNSeg + kSlices * 4;
+constexpr uint32_t kRowLBits = kRowLId + kListCap * 4;
+constexpr uint32_t kRowStride = (kRowLBits + kListCap * 2 + 127) & ~127u;
 constexpr uint32_t kCtlBytes = 256;
+static_assert(sizeof(RowAcc) <= kRowPart, "the row's accumulators precede its slices");
+static_assert(kCtlBytes + size_t(CG_NOALLOC_MAX_ROWS) * kRowStride <= kNoAllocSegBytes,
+              "the no-allocation scratch holds the segmented sampler's rows");
 
 struct Scratch {
   unsigned char* base;        // [kCtlBytes] counters, then [B] row blocks of kRowStride bytes
@@ -151,14 +153,8 @@ struct Scratch {
   __device__ RowAcc* row(uint32_t b) const { return reinterpret_cast<RowAcc*>(blk(b)); }
   __device__ float2* part(uint32_t b) const { return reinterpret_cast<float2*>(blk(b) + kRowPart); }
   __device__ uint32_t* nseg(uint32_t b) const { return reinterpret_cast<uint32_t*>(blk(b) + kRowNSeg); }
-  __device__ uint32_t* cnt(uint32_t b) const { return reinterpret_cast<uint32_t*>(blk(b) + kRowCnt); }
-  __device__ unsigned long long* hbest(uint32_t b) const {
-    return reinterpret_cast<unsigned long long*>(blk(b) + kRowBest);
-  }
-  __device__ unsigned long long* lbest(uint32_t b) const {
-    return reinterpret_cast<unsigned long long*>(blk(b) + kRowLBest);
-  }
-  __device__ uint16_t* lkey(uint32_t b) const { return reinterpret_cast<uint16_t*>(blk(b) + kRowLKey); }
+  __device__ uint32_t* lid(uint32_t b) const { return reinterpret_cast<uint32_t*>(blk(b) + kRowLId); }
+  __device__ uint16_t* lbits(uint32_t b) const { return reinterpret_cast<uint16_t*>(blk(b) + kRowLBits); }
 };
 
 struct Fused {
@@ -198,11 +194,11 @@ struct Src {
 struct Smem {
   uint4* ring4;
   uint32_t* mask32;
-  uint4* lut;
   uint32_t* pool;              // per consumer warp: candidate ids and bits, or exact-score queues
   uint4* desc;
-  uint16_t* svc_keys;          // [kListCap] the finishing row's candidate keys
-  uint32_t* svc_off;           // [kSlices + 1] their slices' offsets
+  uint32_t* segk;              // [2][kConsWarps] the slices' maximum keys of a segment, by parity
+  uint32_t* fin_id;            // [kFinCap] the finishing row's candidates: token ids
+  uint16_t* fin_bits;          // [kFinCap] and bf16 bits
   uint64_t* full;
   uint64_t* empty;
   uint64_t* sq_full;           // [kSQ] consumers -> service: a record is ready (kCons arrivals)
@@ -212,18 +208,18 @@ struct Smem {
   float* redf;                 // [kConsWarps + 1]
   double* redd;                // [kConsWarps + 1]
   uint32_t* words;             // [32] scalars
-  uint32_t* xq;                // [kXQ] rows the service warp hands back for the exact path
 };
 enum {
   kWJ = 0,      // scan result of the exact path
   kWAbort,      // a bounded wait ran out
   kWIssued,     // ring slots the producer used
-  kWXTail,      // rows queued in xq by the service warp
-  kWXHead,      // rows of xq the consumers took
-  kWSvcDone,    // the service warp has finished
-  kWSnap,       // the consumers' uniform copy of kWXTail (and kWSnap + 16: the other parity's)
+  kWRowOk,      // the finishing row's segments are all counted
+  kWKind,       // the finishing row's kind and forced token
+  kWAux,
+  kWFinN,       // candidates the finisher gathered
+  kWBin,        // the finisher's crossing bin
+  kWTau,        // and nucleus key
 };
-constexpr uint32_t kXQ = 64;
 
 __device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(kCons) : "memory"); }
 // consumer barrier that also returns whether any consumer thread passed true
@@ -397,7 +393,7 @@ __device__ __forceinline__ Stage1 stage1(const Params& p, uint32_t idx) {
   Stage1 r{idx, 0u, 0u, -1};
   if (!FUSED || idx >= p.N) return r;
   const Fused& f = p.f;
-  const uint32_t b = idx / p.NS;
+  const uint32_t b = idx % p.B;
   r.g = f.gid ? f.gid[b] : 0u;
   r.fo = f.forced ? f.forced[b] : -1;
   r.st = f.states[b];
@@ -406,8 +402,8 @@ __device__ __forceinline__ Stage1 stage1(const Params& p, uint32_t idx) {
 template <int FUSED>
 __device__ __forceinline__ Src stage2(const Params& p, const Stage1& a, bool record = true) {
   Src r;
-  r.b = a.idx / p.NS;
-  r.s = a.idx - r.b * p.NS;
+  r.s = a.idx / p.B;  // segment-major: segment s of every row before segment s + 1
+  r.b = a.idx - r.s * p.B;
   r.kind = kStream;
   r.aux = 0;
   r.mask = nullptr;
@@ -529,7 +525,7 @@ __device__ uint32_t produce(const Params& p, unsigned char* dsm, uint64_t* full,
 template <int FUSED>
 __device__ const uint32_t* row_mask_ptr(const Params& p, uint32_t b) {
   if (!FUSED) return p.bitmask + size_t(b) * p.W;
-  return stage2<1>(p, stage1<1>(p, b * p.NS)).mask;
+  return stage2<1>(p, stage1<1>(p, b)).mask;
 }
 
 // Exact top-p over the row in global memory (consumer threads only): pass A
@@ -661,100 +657,83 @@ __device__ __noinline__ void emit(const Params& p, uint32_t b, uint32_t tok) {
 
 // ---- the service warp ------------------------------------------------------------------
 
-__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  return v;
-}
-
-// The nucleus key of row b from its candidate list (rows whose candidate keys
-// span more than the histogram): the largest key kappa in [kthr, km] whose
-// upper set of entries carries target, by bisection over the key (masses in
-// 2^-40 fixed point, so every sum is exact).  kNotFound when a slice
-// overflowed or the mass does not reach the target.  Leaves the keys in
-// sm.svc_keys and the slices' offsets in sm.svc_off; *n_out the list length.
-__device__ __noinline__ uint32_t list_tau(const Params& p, uint32_t b, float M, float c, uint32_t kthr, uint32_t km,
-                             unsigned long long target, const Smem& sm, uint32_t* n_out) {
-  const uint32_t lane = threadIdx.x & 31, NSW = p.NS * kConsWarps, capW = kListCap / NSW;
-  const uint32_t* ns = p.sc.nseg(b);
-  // offsets of the slices' entries in flat order
-  uint32_t* off = sm.svc_off;
-  uint32_t base = 0;
-  bool over = false;
-  for (uint32_t i0 = 0; i0 < NSW; i0 += 32) {
-    const uint32_t n = i0 + lane < NSW ? __ldcg(ns + i0 + lane) : 0u;
-    over = over || n > capW;
-    uint32_t inc = n;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-      if (lane >= uint32_t(o)) inc += y;
+// Counts the rows' finished segments: takes the consumers' records in order
+// (one per segment, then the end record) and, per stream record, fences and
+// adds one to the row's count.  The consumers go on streaming meanwhile: the
+// fence is off their path.
+__device__ void service(const Params& p, const Smem& sm) {
+  const uint32_t lane = threadIdx.x & 31;
+  for (uint32_t k = 0;; ++k) {
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait(sm.sq_full + k % kSQ, (k / kSQ) & 1u);
+    if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+      if (lane == 0) {
+        record_error(p.status, CG_DEV_TIMEOUT);
+        atomicExch(&sm.words[kWAbort], 1u);
+      }
+      return;
     }
-    if (i0 + lane < NSW) off[i0 + lane] = base + inc - n;
-    base += __shfl_sync(0xFFFFFFFFu, inc, 31);
-  }
-  if (__any_sync(0xFFFFFFFFu, over)) return kNotFound;
-  const uint32_t L = base;
-  if (lane == 0) off[NSW] = L;
-  *n_out = L;
-  __syncwarp();
-  const uint16_t* lk = p.sc.lkey(b);
-  for (uint32_t j0 = lane; j0 < L; j0 += 32 * 8) {
-    uint16_t k[8];  // eight loads in flight together
-#pragma unroll
-    for (uint32_t u = 0; u < 8; ++u) {
-      const uint32_t j = j0 + 32 * u;
-      k[u] = 0;
-      if (j < L) {
-        uint32_t lo = 0, hi = NSW;  // the slice of flat entry j: off[lo] <= j < off[lo + 1]
-        while (hi - lo > 1) {
-          const uint32_t mid = (lo + hi) / 2;
-          if (off[mid] <= j) lo = mid; else hi = mid;
-        }
-        k[u] = __ldcg(lk + lo * capW + (j - off[lo]));
+    const uint4 r = sm.sq_rec[k % kSQ];
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(sm.sq_empty + k % kSQ);
+      if (r.z == kStream) {
+        // every consumer thread's writes for the segment precede its arrival
+        // on the record's barrier; the fence orders them before the count
+        __threadfence();
+        red_add_u32(&p.sc.row(r.x)->done, 1u);
       }
     }
-#pragma unroll
-    for (uint32_t u = 0; u < 8; ++u)
-      if (j0 + 32 * u < L) sm.svc_keys[j0 + 32 * u] = k[u];
+    if (r.z == kEnd) return;
   }
-  __syncwarp();
-  auto mass_above = [&](uint32_t kappa) {
-    unsigned long long m = 0ull;
-    for (uint32_t j = lane; j < L; j += 32) {
-      const uint32_t k = sm.svc_keys[j];
-      if (k >= kappa) m += mass_q(bf16key_to_float(k), M, c);
-    }
-    return warp_sum_u64(m);
-  };
-  if (mass_above(kthr) < target) return kNotFound;
-  uint32_t lo = kthr, hi = km;
-  while (lo < hi) {
-    const uint32_t mid = lo + (hi - lo + 1) / 2;
-    if (mass_above(mid) >= target) lo = mid; else hi = mid - 1;
-  }
-  return lo;
 }
 
-// Finishes row b (top-p) on the service warp.  Returns false when the row is
-// to take the exact path.
+// ---- finishing a row (the consumer threads of the row's CTA, together) ------------------
+
+// A row without a stream (fused step): a forced token or no allowed token.
 template <int FUSED>
-__device__ __noinline__ bool finish_topp(const Params& p, uint32_t b, const Smem& sm) {
-  const uint32_t lane = threadIdx.x & 31, NSW = p.NS * kConsWarps;
-  RowAcc* ra = p.sc.row(b);
-  const float c = 1.4426950408889634f / p.temp, margin = kMarginZ * p.temp;
-  // one round of loads: the row's accumulators and every slice's (maximum, sum);
-  // S merges the slices online (lane by lane in slice order, then across lanes)
-  uint32_t mk = 0, flags = 0, lowinv = 0;
-  if (lane == 0) {
-    mk = __ldcg(&ra->maxkey);
-    flags = __ldcg(&ra->flags);
-    lowinv = __ldcg(&ra->lowinv);
+__device__ void finish_skip(const Params& p, uint32_t b, uint32_t kind, uint32_t f) {
+  if (FUSED && p.f.bitmask_out) {
+    uint32_t* out = p.f.bitmask_out + size_t(b) * p.W;
+    for (uint32_t i = threadIdx.x; i < p.W; i += kCons)
+      out[i] = (kind == kForcedRow && i == (f >> 5)) ? (1u << (f & 31u)) : 0u;
   }
+  if (threadIdx.x == 0) {
+    p.sc.row(b)->done = 0u;
+    emit<FUSED>(p, b, kind == kForcedRow ? f : CG_NO_TOKEN);
+  }
+}
+
+// Top-p token of row b from its slices and candidate list, or kNotFound when
+// the exact path must decide (a slice's list region overflowed, a non-finite
+// range, more candidates than the finisher holds, or a nucleus that reaches
+// below the candidates' margin).  M and S merge the slices' (m_s, S_s); the
+// candidates at or above M - margin are gathered into shared memory; tau,
+// the largest key whose upper set carries top_p S (masses count
+// exp2((x - M) c) in 2^-40 fixed point, so that no sum depends on order),
+// comes from two passes of mass bins: 32-key bins below the maximum key,
+// then the keys of the bin where the upper mass reaches the target; the
+// token is the best Gumbel score among the candidates at or above tau.
+template <int FUSED>
+__device__ __noinline__ uint32_t finish_topp(const Params& p, uint32_t b, const Smem& sm) {
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t NS = p.NS, NSW = NS * kConsWarps, capW = kListCap / NSW;
+  const float temp = p.temp, c = 1.4426950408889634f / temp, margin = kMarginZ * temp;
+  const RowAcc* ra = p.sc.row(b);
+  // one round of loads: the flags, every slice's (m_s, S_s), and each warp's
+  // slices' candidate counts (warp w takes slices w, w + 8, ..., one per segment)
+  const uint32_t flags = __ldcg(&ra->flags);
   const float2* part = p.sc.part(b);
+  const float2 pa = tid < NSW ? __ldcg(part + tid) : make_float2(kNoRef, 0.f);
+  const float2 pb = tid + kCons < NSW ? __ldcg(part + tid + kCons) : make_float2(kNoRef, 0.f);
+  const uint32_t* nseg = p.sc.nseg(b);
+  const uint32_t na = lane < NS ? __ldcg(nseg + warp + kConsWarps * lane) : 0u;
+  const uint32_t nb = lane + 32 < NS ? __ldcg(nseg + warp + kConsWarps * (lane + 32)) : 0u;
+  // M and S: the thread's two slices merged, then across the threads
   float lm = kNoRef, ls = 0.f;
-  for (uint32_t i = lane; i < NSW; i += 32) {
-    const float2 v = __ldcg(part + i);
+#pragma unroll
+  for (uint32_t h = 0; h < 2; ++h) {
+    const float2 v = h ? pb : pa;
     if (v.x > kNoRef && v.y > 0.f) {
       if (v.x > lm) {
         ls = ls * ex2((lm - v.x) * c) + v.y;
@@ -764,227 +743,195 @@ __device__ __noinline__ bool finish_topp(const Params& p, uint32_t b, const Smem
       }
     }
   }
-  const float M = warp_reduce(lm, MaxOp());
-  const float S = warp_reduce(lm > kNoRef ? ls * ex2((lm - M) * c) : 0.f, SumOp());
-  mk = __shfl_sync(0xFFFFFFFFu, mk, 0);
-  flags = __shfl_sync(0xFFFFFFFFu, flags, 0);
-  lowinv = __shfl_sync(0xFFFFFFFFu, lowinv, 0);
-  uint32_t tok = CG_NO_TOKEN;
-  bool exact = false, clear_all = true;
-  uint32_t km = 0, lowkey = 0x10000u;
-  if (M > kNoRef) {
-    exact = !(M < 1e29f && M > -1e29f) || (flags & 1u);
-    if (!exact) {
-      const float thrF = M - margin;
-      km = fkey(M) >> 16;
-      uint32_t kthr = fkey(thrF) >> 16;
-      if (bf16key_to_float(kthr) < thrF) ++kthr;
-      lowkey = lowinv ? 0x10000u - lowinv : 0x10000u;
-      const bool hist_ok = lowkey <= km && km - lowkey < kNB;
-      clear_all = !hist_ok;
-      const unsigned long long target =
-          static_cast<unsigned long long>(p.top_p * S * 1099511627776.0f);  // top_p of the mass, 2^-40 units
-      unsigned long long best = 0ull;
-      if (kthr > km) {
-        exact = true;
-      } else if (hist_ok) {
-        // bins from the top, 128 a round: counts and bests loaded together
-        const uint32_t span = km - kthr;
-        const uint32_t* cnt = p.sc.cnt(b);
-        const unsigned long long* hbp = p.sc.hbest(b);
-        unsigned long long base = 0ull;
-        bool found = false;
-        for (uint32_t r0 = 0; r0 <= span && !found; r0 += 128) {
-          uint32_t n[4];
-          unsigned long long hv[4];
+  const float M = cons_max_f(lm, sm.redf);
+  const double S = cons_sum_d(lm > kNoRef ? double(ls * ex2((lm - M) * c)) : 0.0, sm.redd);
+  if (!(M > kNoRef)) return CG_NO_TOKEN;  // no allowed token in the row
+  if (!(M < 1e29f) || (flags & 1u)) return kNotFound;
+  const float thrF = M - margin;
+  const uint32_t km = fkey(M) >> 16;
+  uint32_t kthr = fkey(thrF) >> 16;
+  if (bf16key_to_float(kthr) < thrF) ++kthr;
+  const unsigned long long target =
+      max(1ull, static_cast<unsigned long long>(double(p.top_p) * S * 1099511627776.0));  // top_p of the mass
+  // gather the candidates at or above kthr into shared memory: the warp's
+  // slices' offsets by a scan, then every entry's loads in flight together
+  unsigned long long* hist = reinterpret_cast<unsigned long long*>(sm.pool);  // [kCoarse + 32]
+  uint32_t* woff = reinterpret_cast<uint32_t*>(sm.pool + (kCoarse + 32) * 2) + warp * (kMaxNS + 2);
+  const uint32_t nws = NS;
+  for (uint32_t i = tid; i < kCoarse + 32; i += kCons) hist[i] = 0ull;
+  if (tid == 0) sm.words[kWFinN] = 0u;
+  uint32_t ia = na, ib = nb;
 #pragma unroll
-          for (uint32_t u = 0; u < 4; ++u) {
-            const uint32_t j = r0 + 32 * u + lane;
-            n[u] = 0u;
-            hv[u] = 0ull;
-            if (j <= span) {
-              n[u] = __ldcg(cnt + ((km - j) & (kNB - 1)));
-              hv[u] = __ldcg(hbp + ((km - j) & (kNB - 1)));
-            }
-          }
-#pragma unroll
-          for (uint32_t u = 0; u < 4; ++u) {
-            if (found) break;
-            const uint32_t j = r0 + 32 * u + lane;
-            const unsigned long long q =
-                n[u] ? (unsigned long long)n[u] * mass_q(bf16key_to_float(km - j), M, c) : 0ull;
-            unsigned long long incl = q;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-              if (lane >= uint32_t(o)) incl += y;
-            }
-            const unsigned hit = __ballot_sync(0xFFFFFFFFu, q != 0ull && base + incl >= target);
-            // bins at or above the nucleus key: this round's lanes up to the hit
-            const uint32_t last = hit ? uint32_t(__ffs(hit) - 1) : 31u;
-            if (lane <= last) best = hv[u] > best ? hv[u] : best;
-            found = hit != 0u;
-            base += __shfl_sync(0xFFFFFFFFu, incl, 31);
-          }
-        }
-        exact = !found;
-      } else {
-        uint32_t L = 0;
-        const uint32_t tau = list_tau(p, b, M, c, kthr, km, target, sm, &L);
-        if (tau == kNotFound) {
-          exact = true;
-        } else {
-          // the best packed score among the entries at or above tau
-          const uint32_t capW = kListCap / NSW;
-          const unsigned long long* lb = p.sc.lbest(b);
-          for (uint32_t j = lane; j < L; j += 32) {
-            if (sm.svc_keys[j] < tau) continue;
-            uint32_t lo = 0, hi = NSW;
-            while (hi - lo > 1) {
-              const uint32_t mid = (lo + hi) / 2;
-              if (sm.svc_off[mid] <= j) lo = mid; else hi = mid;
-            }
-            const unsigned long long v = __ldcg(lb + lo * capW + (j - sm.svc_off[lo]));
-            best = v > best ? v : best;
-          }
-        }
-      }
-      if (!exact) {
-        best = warp_max_u64(best);
-        tok = best ? best_id(best) : CG_NO_TOKEN;
-      }
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t ya = __shfl_up_sync(0xFFFFFFFFu, ia, o), yb = __shfl_up_sync(0xFFFFFFFFu, ib, o);
+    if (lane >= uint32_t(o)) {
+      ia += ya;
+      ib += yb;
     }
+  }
+  const uint32_t ta = __shfl_sync(0xFFFFFFFFu, ia, 31);
+  woff[lane] = ia - na;                 // start of slice warp + 8 lane in the warp's flat order
+  woff[lane + 32] = ta + ib - nb;
+  const uint32_t T = ta + __shfl_sync(0xFFFFFFFFu, ib, 31);
+  woff[64] = T;
+  cbar();
+  const uint32_t* lid = p.sc.lid(b);
+  const uint16_t* lbits = p.sc.lbits(b);
+  // f(valid, id, bits) for every entry of the warp's slices, 4 x 32 at a time
+  // (warp-uniform trip count: f may use warp collectives)
+  auto walk = [&](auto&& f) {
+    for (uint32_t e0 = 0; e0 < T; e0 += 32 * 4) {
+      uint32_t id[4], xb[4];
+#pragma unroll
+      for (uint32_t u = 0; u < 4; ++u) {
+        const uint32_t e = e0 + 32 * u + lane;
+        id[u] = 0u;
+        xb[u] = 0u;
+        if (e < T) {
+          uint32_t lo = 0, hi = nws;  // the slice of flat entry e: woff[lo] <= e < woff[lo + 1]
+          while (hi - lo > 1) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if (woff[mid] <= e) lo = mid; else hi = mid;
+          }
+          const size_t at = size_t(warp + kConsWarps * lo) * capW + (e - woff[lo]);
+          id[u] = __ldcg(lid + at);
+          xb[u] = __ldcg(lbits + at);
+        }
+      }
+#pragma unroll
+      for (uint32_t u = 0; u < 4; ++u) f(e0 + 32 * u + lane < T && bf16_key(xb[u]) >= kthr, id[u], xb[u]);
+    }
+  };
+  walk([&](bool keep, uint32_t id, uint32_t xb) {
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep);
+    uint32_t base = 0;
+    if (lane == 0 && bal) base = atomicAdd(&sm.words[kWFinN], uint32_t(__popc(bal)));
+    base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(bal & ((1u << lane) - 1u));
+    if (keep && base < kFinCap) {
+      sm.fin_id[base] = id;
+      sm.fin_bits[base] = uint16_t(xb);
+    }
+  });
+  cbar();
+  const uint32_t nf = sm.words[kWFinN];
+  // f(id, bits) for every candidate at or above kthr: from shared memory, or
+  // (more than it holds) from the list again
+  auto for_cands = [&](auto&& f) {
+    if (nf <= kFinCap) {
+      for (uint32_t i = tid; i < nf; i += kCons) f(sm.fin_id[i], uint32_t(sm.fin_bits[i]));
+    } else {
+      walk([&](bool keep, uint32_t id, uint32_t xb) {
+        if (keep) f(id, xb);
+      });
+    }
+  };
+  // pass 1: masses per 32-key bin, bin 0 the maximum key's
+  for_cands([&](uint32_t, uint32_t h) {
+    atomicAdd(hist + ((km - bf16_key(h)) >> 5), mass_q(bf16_bits_to_float(h), M, c));
+  });
+  cbar();
+  // the bin where the upper mass reaches the target: thread t sums bins 8t .. 8t + 7
+  unsigned long long loc = 0ull;
+#pragma unroll
+  for (uint32_t i = 0; i < 8; ++i) loc += hist[8 * tid + i];
+  unsigned long long sc64 = loc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, sc64, o);
+    if (lane >= uint32_t(o)) sc64 += y;
+  }
+  if (lane == 31) sm.red64[warp] = sc64;
+  cbar();
+  unsigned long long before = 0ull, total = 0ull;
+#pragma unroll
+  for (uint32_t w = 0; w < kConsWarps; ++w) {
+    before += w < warp ? sm.red64[w] : 0ull;
+    total += sm.red64[w];
+  }
+  before += sc64 - loc;  // the mass of the bins above this thread's
+  if (total < target) return kNotFound;  // the nucleus reaches below the candidates (uniform)
+  cbar();
+  if (before < target && before + loc >= target) {
+    unsigned long long run = before;
+    for (uint32_t i = 0; i < 8; ++i) {
+      const unsigned long long h = hist[8 * tid + i];
+      if (run + h >= target) {
+        sm.words[kWBin] = 8 * tid + i;
+        sm.red64[kConsWarps] = run;  // the mass above the bin
+        break;
+      }
+      run += h;
+    }
+  }
+  cbar();
+  const uint32_t bin = sm.words[kWBin];
+  // pass 2: masses per key of that bin; tau where the upper mass reaches the target
+  unsigned long long* fine = hist + kCoarse;
+  for_cands([&](uint32_t, uint32_t h) {
+    const uint32_t d = km - bf16_key(h);
+    if ((d >> 5) == bin) atomicAdd(fine + (d & 31u), mass_q(bf16_bits_to_float(h), M, c));
+  });
+  cbar();
+  if (warp == 0) {
+    unsigned long long run = fine[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, run, o);
+      if (lane >= uint32_t(o)) run += y;
+    }
+    const unsigned hit = __ballot_sync(0xFFFFFFFFu, sm.red64[kConsWarps] + run >= target);
+    if (lane == 0) sm.words[kWTau] = km - (32 * bin + (hit ? uint32_t(__ffs(hit) - 1) : 31u));
+  }
+  cbar();
+  const uint32_t tau = sm.words[kWTau];
+  // pass 3: the best Gumbel score among the candidates at or above tau
+  const PhRow pr = philox_row(p, b);
+  unsigned long long best = 0ull;
+  for_cands([&](uint32_t id, uint32_t h) {
+    if (bf16_key(h) < tau) return;
+    const uint4 blk = philox_q(p, pr, id >> 2);
+    best = max(best, pack_best(gumbel_score(bf16_bits_to_float(h), temp, philox_word(blk, id & 3u)), id));
+  });
+  best = cons_max_u64(best, sm.red64);
+  return best ? best_id(best) : CG_NO_TOKEN;
+}
+
+// Finishes row b once every segment of it is counted: its token (and the
+// accept in the fused step), then its accumulators back to zero.
+template <int MODE, int FUSED>
+__device__ void finish_row(const Params& p, uint32_t b, const Smem& sm) {
+  const uint32_t tid = threadIdx.x;
+  RowAcc* ra = p.sc.row(b);
+  if (FUSED) {
+    if (tid == 0) {
+      const Src r = stage2<FUSED>(p, stage1<FUSED>(p, b), false);
+      sm.words[kWKind] = r.kind == kSkipPending ? ((r.aux & 0x80000000u) ? kForcedRow : kEmptyRow) : kStream;
+      sm.words[kWAux] = r.aux & 0x7FFFFFFFu;
+    }
+    cbar();
+    const uint32_t kind = sm.words[kWKind], aux = sm.words[kWAux];
+    cbar();
+    if (kind != kStream) {
+      finish_skip<FUSED>(p, b, kind, aux);
+      return;
+    }
+  }
+  uint32_t tok;
+  if (MODE == kModeTopP) {
+    tok = finish_topp<FUSED>(p, b, sm);
+    cbar();
+    if (tok == kNotFound)
+      tok = exact_topp(p, b, row_mask_ptr<FUSED>(p, b), sm.pool, sm.red64, sm.redf, sm.redd, &sm.words[kWJ]);
   } else {
-    clear_all = false;  // no slice had an allowed logit: no candidate was recorded
+    const unsigned long long v = __ldcg(&ra->best);
+    tok = v ? best_id(v) : CG_NO_TOKEN;
   }
-  (void)mk;
-  __syncwarp();
-  // clear what this row's candidates touched: keys lowkey..km, or every bin
-  uint32_t* cnt = p.sc.cnt(b);
-  unsigned long long* hb = p.sc.hbest(b);
-  const uint32_t nz = clear_all ? kNB : (lowkey <= km ? km - lowkey + 1 : 0u);
-  for (uint32_t j = lane; j < nz; j += 32) {
-    const uint32_t bin = (km - j) & (kNB - 1);
-    cnt[bin] = 0u;
-    hb[bin] = 0ull;
-  }
-  if (lane == 0) {
+  if (tid == 0) {
     ra->maxkey = 0u;
     ra->done = 0u;
-    ra->lowinv = 0u;
     ra->flags = 0u;
-    if (!exact) emit<FUSED>(p, b, tok);
-  }
-  return !exact;
-}
-
-// Finishes a row without a stream (fused step): a forced token (that token)
-// or none; the bitmask when asked.
-template <int FUSED>
-__device__ __noinline__ void finish_skip(const Params& p, uint32_t b, uint32_t kind, uint32_t f) {
-  const uint32_t lane = threadIdx.x & 31;
-  if (FUSED && p.f.bitmask_out) {
-    uint32_t* out = p.f.bitmask_out + size_t(b) * p.W;
-    for (uint32_t i = lane; i < p.W; i += 32) out[i] = (kind == kForcedRow && i == (f >> 5)) ? (1u << (f & 31u)) : 0u;
-  }
-  if (lane == 0) {
-    p.sc.row(b)->done = 0u;
-    emit<FUSED>(p, b, kind == kForcedRow ? f : CG_NO_TOKEN);
-  }
-}
-
-// The service warp.  Counts the rows' finished segments: every record the
-// consumers complete is taken in a batch, one fence for the batch and one
-// reduction per record (nothing waits for a returned value).  Finishes the
-// rows this CTA owns (b = blockIdx.x + k gridDim.x, in order) once all their
-// segments are counted; rows for the exact path are queued (xq) for the
-// consumers.  Returns when the consumers' end record has arrived and every
-// owned row is finished.
-template <int MODE, int FUSED>
-__device__ void service(const Params& p, const Smem& sm) {
-  const uint32_t lane = threadIdx.x & 31;
-  uint32_t k = 0;          // next record
-  bool end = false;        // the consumers' end record arrived
-  uint32_t own = blockIdx.x;  // next owned row
-  uint32_t idle = 0;
-  while (!end || own < p.B) {
-    bool busy = false;
-    if (!end) {
-      // every record already complete, from k on
-      bool ready = false;
-      if (lane < kSQ) ready = mbar_try_wait(sm.sq_full + (k + lane) % kSQ, ((k + lane) / kSQ) & 1u);
-      const unsigned notready = __ballot_sync(0xFFFFFFFFu, !ready);
-      const uint32_t n = notready ? uint32_t(__ffs(notready) - 1) : 32u;
-      if (n) {
-        busy = true;
-        uint4 r = make_uint4(0u, 0u, kNone, 0u);
-        if (lane < n) r = sm.sq_rec[(k + lane) % kSQ];
-        __syncwarp();
-        if (lane < n) mbar_arrive(sm.sq_empty + (k + lane) % kSQ);
-        k += n;
-        end = __any_sync(0xFFFFFFFFu, lane < n && r.z == kEnd);
-        // every consumer thread's writes for a record precede its arrival on
-        // the record's barrier, and this fence orders them before the counts
-        __threadfence();
-        if (lane < n && r.z == kStream) red_add_u32(&p.sc.row(r.x)->done, 1u);
-      }
-    }
-    if (own < p.B) {
-      uint32_t d = 0;
-      if (lane == 0) d = ld_acquire_gpu(&p.sc.row(own)->done);
-      d = __shfl_sync(0xFFFFFFFFu, d, 0);
-      if (d >= p.NS) {
-        busy = true;
-        __threadfence();
-        // the row's kind: a stream, or (fused) a forced token / no allowed token
-        uint32_t kind = kStream, f = 0;
-        if (FUSED) {
-          const Src r = stage2<FUSED>(p, stage1<FUSED>(p, own * p.NS), false);
-          if (r.kind == kSkipPending) {
-            kind = (r.aux & 0x80000000u) ? kForcedRow : kEmptyRow;
-            f = r.aux & 0x7FFFFFFFu;
-          }
-        }
-        if (kind != kStream) {
-          finish_skip<FUSED>(p, own, kind, f);
-        } else if (MODE == kModeTopP) {
-          if (!finish_topp<FUSED>(p, own, sm) && lane == 0) {
-            // the exact path: queued for the consumers, who take it after their stream
-            const uint32_t t = sm.words[kWXTail];
-            if (t - ld_volatile_s(&sm.words[kWXHead]) >= kXQ) {
-              record_error(p.status, CG_DEV_TIMEOUT);  // more exact rows in one CTA than the queue holds
-            } else {
-              sm.xq[t % kXQ] = own;
-              __threadfence_block();
-              *reinterpret_cast<volatile uint32_t*>(&sm.words[kWXTail]) = t + 1;
-            }
-          }
-        } else if (lane == 0) {
-          RowAcc* ra = p.sc.row(own);
-          const unsigned long long v = __ldcg(&ra->best);
-          ra->best = 0ull;
-          ra->done = 0u;
-          emit<FUSED>(p, own, v ? best_id(v) : CG_NO_TOKEN);
-        }
-        __syncwarp();
-        own += gridDim.x;
-      }
-    }
-    if (busy) {
-      idle = 0;
-    } else if (++idle > kWaitLimit) {
-      if (lane == 0) {
-        record_error(p.status, CG_DEV_TIMEOUT);
-        atomicExch(&sm.words[kWAbort], 1u);
-      }
-      break;
-    } else {
-      __nanosleep(128);
-    }
-  }
-  if (lane == 0) {
-    __threadfence_block();
-    *reinterpret_cast<volatile uint32_t*>(&sm.words[kWSvcDone]) = 1u;
+    ra->best = 0ull;
+    emit<FUSED>(p, b, tok);
   }
 }
 
@@ -1013,31 +960,144 @@ __device__ __noinline__ void drain_queue(const uint32_t* qid, const uint32_t* qw
   }
 }
 
-// Keeps the first n buffered candidates whose 16-bit key is at least k16, in
-// order, at the front of the warp's buffer; returns how many (all lanes).
-__device__ __forceinline__ uint32_t compact_cands(uint32_t* cid, uint16_t* cx, uint32_t n, uint32_t k16) {
-  const uint32_t lane = threadIdx.x & 31, lt = (1u << lane) - 1u;
-  uint32_t kept = 0;
-  for (uint32_t i0 = 0; i0 < n; i0 += 32) {
-    const uint32_t i = i0 + lane;
-    uint32_t id = 0;
-    uint16_t xb = 0;
-    bool keep = false;
-    if (i < n) {
-      id = cid[i];
-      xb = cx[i];
-      keep = bf16_key(xb) >= k16;
+// Top-p: one segment of a row in one step of a consumer warp.  The thread's
+// groups of every chunk of the segment are loaded and masked together (the
+// slots go back to the producer as soon as the loads are done); then the
+// warp's maximum (published to the row's), the thread's exponential sums
+// against its own maximum (no rescaling inside a segment), and the candidates
+// at or above max(warp maximum, the row's maximum as read at the segment's
+// start) - margin, extracted with one warp scan, scored with their Gumbel
+// noise and added to the row's key histogram and candidate list.  Returns
+// false (all lanes) when a wait for a chunk ran out.
+template <int FUSED>
+__device__ __forceinline__ bool topp_segment(const Params& p, const Smem& sm, uint32_t b, uint32_t s, uint32_t nch,
+                                             uint32_t q, uint32_t par) {
+  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float c = 1.4426950408889634f / p.temp, margin = kMarginZ * p.temp;
+  const uint32_t g0 = warp * 64 + lane;
+  RowAcc* ra = p.sc.row(b);
+  uint32_t G = 0;  // the row's maximum so far, read while the segment's chunks arrive
+  if (lane == 0) G = ld_relaxed(&ra->maxkey);
+  bool ok = true;
+  for (uint32_t k = 1; k < nch; ++k) ok = ok && mbar_wait(sm.full + (q + k) % kSlots, ((q + k) / kSlots) & 1u);
+
+  // the thread's 2 nch groups, masked, and their packed maxima
+  uint4 v[2 * kMaxSegChunks];
+  uint32_t a[2 * kMaxSegChunks];
+  uint32_t am = 0xFF80FF80u;
+#pragma unroll
+  for (uint32_t j = 0; j < 2 * kMaxSegChunks; ++j) {
+    const uint32_t k = j >> 1, g = g0 + (j & 1u) * 32u;
+    v[j] = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+    if (k < nch) {
+      const uint32_t ck = s * p.segc + k, sl = (q + k) % kSlots;
+      if (g < min(kGroups, (p.V - ck * kChunk) >> 3)) {
+        const uint32_t mb = reinterpret_cast<const uint8_t*>(sm.mask32 + sl * kChunkWords)[g];
+        v[j] = apply_mask(sm.ring4[sl * kGroups + g], pair_mask_of(mb));
+      }
     }
-    const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep);
-    __syncwarp();
-    if (keep) {  // never past the entries still to be read
-      cid[kept + __popc(bal & lt)] = id;
-      cx[kept + __popc(bal & lt)] = xb;
-    }
-    kept += __popc(bal);
-    __syncwarp();
+    a[j] = group_pmax(v[j]);
+    am = bmax2(am, a[j]);
   }
-  return kept;
+  if (FUSED && p.f.bitmask_out && lane < 16) {
+    for (uint32_t k = 0; k < nch; ++k) {
+      const uint32_t wi = (s * p.segc + k) * kChunkWords + warp * 16 + lane;
+      if (wi < p.W) p.f.bitmask_out[size_t(b) * p.W + wi] = sm.mask32[((q + k) % kSlots) * kChunkWords + warp * 16 + lane];
+    }
+  }
+  const bool wok = __all_sync(0xFFFFFFFFu, ok);
+  __syncwarp();  // the warp's reads of the slots before their release
+  if (lane == 0 && wok)
+    for (uint32_t k = 0; k < nch; ++k) mbar_arrive(sm.empty + (q + k) % kSlots);
+
+  // the slice's maximum, and the segment's (the eight slices' through shared
+  // memory, double-buffered by segment parity), published to the row's
+  const float tm = pmax_f(am);
+  const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, fkey(tm));
+  const bool any = wk > 0x007FFFFFu;  // an allowed logit in the slice
+  const float wm = any ? fkey_inv(wk) : kNoRef;
+  uint32_t* segk = sm.segk + (par & 1u) * kConsWarps;
+  if (lane == 0) segk[warp] = wk;
+  if (cbar_or(!ok)) return false;  // every consumer thread arrives here once per segment
+  uint32_t sk = segk[0];
+#pragma unroll
+  for (uint32_t w = 1; w < kConsWarps; ++w) sk = max(sk, segk[w]);
+  if (threadIdx.x == 0 && sk > 0x007FFFFFu) red_max_u32(&ra->maxkey, sk);
+
+  // the thread's sums against its own maximum (masked logits add exp2(-inf) = 0)
+  const float mt = fmaxf(tm, kNoRef);
+  float2 acc[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] = make_float2(0.f, 0.f);
+  const float2 c2 = make_float2(c, c), nmc2 = make_float2(-mt * c, -mt * c);
+#pragma unroll
+  for (uint32_t j = 0; j < 2 * kMaxSegChunks; ++j)  // groups masked out for the whole warp add nothing
+    if ((j >> 1) < nch && __any_sync(0xFFFFFFFFu, a[j] != 0xFF80FF80u)) add_exps(acc, v[j], c2, nmc2);
+  const float asum = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+  float part = (any && asum > 0.f) ? asum * ex2((mt - wm) * c) : 0.f;
+  part = warp_reduce(part, SumOp());
+
+  // the candidate threshold: its bf16 key k16 (and bits t2 in both halves)
+  G = max(sk, __shfl_sync(0xFFFFFFFFu, G, 0));
+  uint32_t k16 = kNotFound, t2 = 0;
+  bool bad = false;  // a non-finite range or an overflowing buffer: the exact path decides
+  if (any) {
+    const float thr = fkey_inv(G) - margin;
+    if (thr > -1e29f && thr < 1e29f) {
+      k16 = fkey(thr) >> 16;
+      if (bf16key_to_float(k16) < thr) ++k16;
+      const uint32_t t16 = __float_as_uint(bf16key_to_float(k16)) >> 16;
+      t2 = t16 | (t16 << 16);
+    } else {
+      bad = true;
+    }
+  }
+  // candidates: per group the bits of its logits >= threshold, one scan for the positions
+  unsigned long long cb = 0ull;
+  uint32_t n = 0;
+  const __nv_bfloat162 tb = *reinterpret_cast<const __nv_bfloat162*>(&t2);
+  if (k16 != kNotFound && __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&am), tb) != 0u) {
+#pragma unroll
+    for (uint32_t j = 0; j < 2 * kMaxSegChunks; ++j) {
+      if (__hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&a[j]), tb) != 0u) {
+        const uint32_t bits = group_ge_bits(v[j], t2);
+        cb |= static_cast<unsigned long long>(bits) << (8 * j);
+        n += __popc(bits);
+      }
+    }
+  }
+  uint32_t inc = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+    if (lane >= uint32_t(o)) inc += y;
+  }
+  const uint32_t total = __shfl_sync(0xFFFFFFFFu, inc, 31);
+  // into the slice's region of the row's candidate list
+  const uint32_t slice = s * kConsWarps + warp, capW = kListCap / (p.NS * kConsWarps);
+  uint32_t* lid = p.sc.lid(b) + size_t(slice) * capW;
+  uint16_t* lbits = p.sc.lbits(b) + size_t(slice) * capW;
+  uint32_t pos = inc - n;
+#pragma unroll
+  for (uint32_t j = 0; j < 2 * kMaxSegChunks; ++j) {
+    uint32_t bits = static_cast<uint32_t>(cb >> (8 * j)) & 0xFFu;
+    const uint32_t t0 = (s * p.segc + (j >> 1)) * kChunk + (g0 + (j & 1u) * 32u) * 8u;
+    while (bits) {
+      const uint32_t e = __ffs(bits) - 1;
+      bits &= bits - 1;
+      if (pos < capW) {
+        lid[pos] = t0 + e;
+        lbits[pos] = uint16_t(group_bits(v[j], e));
+      }
+      ++pos;
+    }
+  }
+  if (lane == 0) {
+    p.sc.part(b)[slice] = make_float2(wm, part);
+    p.sc.nseg(b)[slice] = min(total, capW);
+    if (bad || total > capW) atomicOr(&ra->flags, 1u);
+  }
+  return true;
 }
 
 // Each consumer warp works on its own share of every chunk (64 groups of 8
@@ -1051,12 +1111,12 @@ __device__ void consume(const Params& p, const Smem& sm) {
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float temp = p.temp;
   const float c = (MODE == kModeGreedy) ? 0.f : 1.4426950408889634f / temp;
-  const float margin = kMarginZ * temp;
   const uint32_t g0 = warp * 64 + lane, g1 = g0 + 32;
   const uint32_t lt = (1u << lane) - 1u;
   const uint4 kNeg4 = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
   uint32_t q = 0;     // ring slots taken
   uint32_t nrec = 0;  // records sent to the service warp
+  uint32_t nts = 0;   // top-p segments taken
   bool ok = true;
   // One record for the service warp: thread 0 writes it once its slot is
   // free; every consumer thread arrives once its own writes for it are done.
@@ -1072,9 +1132,7 @@ __device__ void consume(const Params& p, const Smem& sm) {
     mbar_arrive(sm.sq_full + k);
     ++nrec;
   };
-  // per warp: candidate ids and bits (top-p), or the exact-score queue (full)
-  uint32_t* cid = sm.pool + warp * kWarpCand;
-  uint16_t* cx = reinterpret_cast<uint16_t*>(sm.pool + kConsWarps * kWarpCand) + warp * kWarpCand;
+  // per warp: the exact-score queue (full)
   uint32_t* qid = sm.pool + warp * kQ;
   uint32_t* qw = sm.pool + kConsWarps * kQ + warp * kQ;
   uint16_t* qx = reinterpret_cast<uint16_t*>(sm.pool + 2 * kConsWarps * kQ) + warp * kQ;
@@ -1097,16 +1155,17 @@ __device__ void consume(const Params& p, const Smem& sm) {
       ++q;
       continue;
     }
+    if (MODE == kModeTopP) {
+      if (!topp_segment<FUSED>(p, sm, b, s, nch, q, nts++)) {
+        ok = false;
+        break;
+      }
+      post(b, s, kStream, 0u);
+      q += nch;
+      continue;
+    }
 
-    // ---- pass 1 over the segment's chunks -------------------------------------------
-    float2 acc[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[j] = make_float2(0.f, 0.f);
-    float mt = kNoRef;                 // top-p: this thread's running maximum (its sums' reference)
-    uint32_t wmk = 0;                  // top-p: fkey of the warp's running maximum
-    uint32_t gk = 0;                   // top-p: the row's running maximum as last read
-    uint32_t wn = 0;                   // top-p: candidates this warp buffered in the segment
-    bool lost = false;                 // top-p: a chunk's candidates did not fit the buffer
+    // ---- greedy / full: the segment's chunks one by one ------------------------------
     unsigned long long best = 0ull;    // greedy / full: packed (value, id)
     float bestv = -INFINITY;           // greedy: value of best; full: the bound's reference score
     float offB = INFINITY;             // full: 23 - bestv log2(e)
@@ -1117,8 +1176,6 @@ __device__ void consume(const Params& p, const Smem& sm) {
       phr = philox_row(p, b);
       if (lane == 0) seed_best = ld_relaxed64(&ra->best);  // the row's best so far (other segments)
     }
-    uint32_t gk_next = 0;              // top-p: a read of the row's running maximum in flight
-    if (MODE == kModeTopP && lane == 0) gk_next = ld_relaxed(&ra->maxkey);
 #pragma unroll 1
     for (uint32_t k = 0; k < nch; ++k) {
       const uint32_t qk = q + k, sl = qk % kSlots;
@@ -1126,7 +1183,6 @@ __device__ void consume(const Params& p, const Smem& sm) {
         ok = false;
         break;
       }
-      if (MODE == kModeTopP) gk = max(gk, gk_next);  // the read issued one chunk earlier
       const uint32_t ck = s * p.segc + k;
       const uint32_t ng = min(kGroups, (p.V - ck * kChunk) >> 3);
       const uint4* r4 = sm.ring4 + sl * kGroups;
@@ -1135,88 +1191,13 @@ __device__ void consume(const Params& p, const Smem& sm) {
       uint32_t mb0 = 0, mb1 = 0;
       if (g0 < ng) {
         mb0 = m8[g0];
-        v0 = apply_mask(r4[g0], sm.lut[mb0]);
+        v0 = apply_mask(r4[g0], pair_mask_of(mb0));
       }
       if (g1 < ng) {
         mb1 = m8[g1];
-        v1 = apply_mask(r4[g1], sm.lut[mb1]);
+        v1 = apply_mask(r4[g1], pair_mask_of(mb1));
       }
-      if (MODE == kModeTopP) {
-        if (FUSED && p.f.bitmask_out && lane < 16) {
-          const uint32_t wi = ck * kChunkWords + warp * 16 + lane;
-          if (wi < p.W) p.f.bitmask_out[size_t(b) * p.W + wi] = sm.mask32[sl * kChunkWords + warp * 16 + lane];
-        }
-        // the data are in registers: the slot goes back to the producer now
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sm.empty + sl);
-        const uint32_t a0 = group_pmax(v0), a1 = group_pmax(v1);
-        const float gm = pmax_f(bmax2(a0, a1));
-        // the warp's running maximum, published to the row's (shared with its other segments)
-        const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, fkey(gm));
-        if (lane == 0) {
-          if (wk > 0x007FFFFFu) red_max_u32(&ra->maxkey, wk);
-          gk_next = ld_relaxed(&ra->maxkey);  // for the next chunk's threshold, used then
-        }
-        wmk = max(wmk, wk);
-        // candidates buffered against max(warp maximum, row maximum) - margin: a
-        // superset of the final candidates, filtered at the segment end
-        const uint32_t rk = max(wmk, __shfl_sync(0xFFFFFFFFu, gk, 0));
-        if (rk > 0x007FFFFFu) {
-          const float thr = fkey_inv(rk) - margin;
-          if (thr > -1e29f && thr < 1e29f) {
-            uint32_t k16 = fkey(thr) >> 16;
-            if (bf16key_to_float(k16) < thr) ++k16;
-            const uint32_t t16 = __float_as_uint(bf16key_to_float(k16)) >> 16;
-            const uint32_t t2 = t16 | (t16 << 16);
-            const __nv_bfloat162 tb = *reinterpret_cast<const __nv_bfloat162*>(&t2);
-            const bool f0 = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&a0), tb) != 0u;
-            const bool f1 = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&a1), tb) != 0u;
-            if (wn > kWarpCand / 2 && __any_sync(0xFFFFFFFFu, f0 || f1)) {
-              // thresholds only rise: drop the buffered entries below this one
-              wn = compact_cands(cid, cx, min(wn, kWarpCand), k16);
-            }
-            if (__any_sync(0xFFFFFFFFu, f0 || f1)) {
-              const uint32_t b0 = f0 ? group_ge_bits(v0, t2) : 0u, b1 = f1 ? group_ge_bits(v1, t2) : 0u;
-              const uint32_t n = __popc(b0) + __popc(b1);
-              uint32_t inc = n;
-#pragma unroll
-              for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-                if (lane >= uint32_t(o)) inc += y;
-              }
-              uint32_t pos = wn + inc - n;
-#pragma unroll
-              for (uint32_t h = 0; h < 2; ++h) {
-                uint32_t bits = h ? b1 : b0;
-                const uint4& v = h ? v1 : v0;
-                const uint32_t t0 = ck * kChunk + (h ? g1 : g0) * 8;
-                while (bits) {
-                  const uint32_t e = __ffs(bits) - 1;
-                  bits &= bits - 1;
-                  if (pos < kWarpCand) {
-                    cid[pos] = t0 + e;
-                    cx[pos] = uint16_t(group_bits(v, e));
-                  }
-                  ++pos;
-                }
-              }
-              wn += __shfl_sync(0xFFFFFFFFu, inc, 31);
-              lost = lost || wn > kWarpCand;
-            }
-          } else if (lane == 0) {
-            atomicOr(&ra->flags, 1u);  // non-finite range: the exact path decides
-          }
-        }
-        if (gm > mt) {
-          const float r = ex2((mt - gm) * c);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[j] = __fmul2_rn(acc[j], make_float2(r, r));
-          mt = gm;
-        }
-        const float2 c2 = make_float2(c, c), nmc2 = make_float2(-mt * c, -mt * c);
-        add_exps(acc, v0, c2, nmc2);
-        add_exps(acc, v1, c2, nmc2);
-      } else {
+      {
         if (FUSED && p.f.bitmask_out && lane < 16) {
           const uint32_t wi = ck * kChunkWords + warp * 16 + lane;
           if (wi < p.W) p.f.bitmask_out[size_t(b) * p.W + wi] = sm.mask32[sl * kChunkWords + warp * 16 + lane];
@@ -1298,61 +1279,7 @@ __device__ void consume(const Params& p, const Smem& sm) {
     }
 
     // ---- segment end (this warp's slice) ------------------------------------------------
-    const uint32_t slice = s * kConsWarps + warp;
-    if (MODE == kModeTopP) {
-      // the slice's maximum and its threads' sums rescaled to it
-      const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, fkey(mt));
-      const float wm = fkey_inv(wk);  // kNoRef: nothing allowed in the slice
-      const float a = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
-      float part = (wm > kNoRef && a > 0.f) ? a * ex2((mt - wm) * c) : 0.f;
-      part = warp_reduce(part, SumOp());
-      // final candidates: buffered ones >= max(slice maximum, the row's running maximum) - margin
-      uint32_t k16 = kNotFound;
-      if (lane == 0) {
-        p.sc.part(b)[slice] = make_float2(wm, part);
-        if (wm > kNoRef) {
-          const uint32_t g2 = max(gk, ld_relaxed(&ra->maxkey));
-          const float G = g2 > 0x007FFFFFu ? fkey_inv(g2) : -INFINITY;
-          const float thr = fmaxf(wm, G) - margin;
-          if (thr > -1e29f && thr < 1e29f) {
-            k16 = fkey(thr) >> 16;
-            if (bf16key_to_float(k16) < thr) ++k16;
-            red_max_u32(&ra->lowinv, 0x10000u - k16);
-          } else {
-            atomicOr(&ra->flags, 1u);  // non-finite range: the exact path decides
-          }
-        }
-        if (lost) atomicOr(&ra->flags, 1u);  // the buffer overflowed: the exact path decides
-      }
-      k16 = __shfl_sync(0xFFFFFFFFu, k16, 0);
-      // keep the buffered candidates at or above the final threshold (in place, in order)
-      const uint32_t nc = k16 != kNotFound ? compact_cands(cid, cx, min(wn, kWarpCand), k16) : 0u;
-      if (lane == 0) p.sc.nseg(b)[slice] = nc;
-      // Gumbel scores of the candidates into the row's key histogram and
-      // into this slice of the row's candidate list
-      if (nc) {
-        uint32_t* cnt = p.sc.cnt(b);
-        unsigned long long* hbr = p.sc.hbest(b);
-        const uint32_t capW = kListCap / (p.NS * kConsWarps);
-        unsigned long long* lb = p.sc.lbest(b) + slice * capW;
-        uint16_t* lk = p.sc.lkey(b) + slice * capW;
-        const PhRow pr = philox_row(p, b);
-        for (uint32_t i = lane; i < nc; i += 32) {
-          const uint32_t id = cid[i], xb = cx[i];
-          const uint4 blk = philox_q(p, pr, id >> 2);
-          const float score = gumbel_score(bf16_bits_to_float(xb), temp, philox_word(blk, id & 3u));
-          const uint32_t key = bf16_key(xb);
-          const unsigned long long pk = pack_best(score, id);
-          red_add_u32(cnt + (key & (kNB - 1)), 1u);
-          red_max_u64(hbr + (key & (kNB - 1)), pk);
-          if (i < capW) {
-            lb[i] = pk;
-            lk[i] = uint16_t(key);
-          }
-        }
-      }
-      __syncwarp();
-    } else {
+    {
       // greedy / full: the slice's packed maximum into the row's
       if (MODE == kModeFull && qn) {
         __syncwarp();
@@ -1369,34 +1296,30 @@ __device__ void consume(const Params& p, const Smem& sm) {
     atomicExch(&sm.words[kWAbort], 1u);
   }
   post(0u, 0u, kEnd, 0u);
-  if (MODE != kModeTopP) return;
-  // together now: the rows the service warp queued for the exact path, until it is done
-  cbar();
-  uint32_t xhead = 0, it = 0;
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
-    uint32_t* snap = &sm.words[kWSnap] + 16 * (it & 1u);  // the parity's copy: no copy is rewritten while read
+  // together now: the rows this CTA owns (b = blockIdx.x + k gridDim.x), each
+  // once the service warps have counted all its segments
+  for (uint32_t own = blockIdx.x; own < p.B; own += gridDim.x) {
     if (tid == 0) {
-      // done flag first: a tail read after it holds every row the service queued
-      const uint32_t done = ld_volatile_s(&sm.words[kWSvcDone]) | ld_volatile_s(&sm.words[kWAbort]);
-      __threadfence_block();
-      *snap = ld_volatile_s(&sm.words[kWXTail]) | (done ? 0x80000000u : 0u);
+      bool ready = false;
+      for (uint32_t i = 0; i < kWaitLimit && !ready; ++i) {
+        if (ld_acquire_gpu(&p.sc.row(own)->done) >= p.NS) {
+          ready = true;
+        } else {
+          if (ld_volatile_s(&sm.words[kWAbort])) break;
+          __nanosleep(64);
+        }
+      }
+      if (!ready) {
+        record_error(p.status, CG_DEV_TIMEOUT);
+        atomicExch(&sm.words[kWAbort], 1u);
+      }
+      // (after an abort copies may still be in flight into the ring: no finishing)
+      sm.words[kWRowOk] = (ready && !ld_volatile_s(&sm.words[kWAbort])) ? 1u : 0u;
     }
     cbar();
-    ++it;
-    const uint32_t v = *snap;
-    while (xhead < (v & 0x7FFFFFFFu)) {
-      const uint32_t b = sm.xq[xhead % kXQ];
-      const uint32_t tok = exact_topp(p, b, row_mask_ptr<FUSED>(p, b), sm.pool, sm.red64, sm.redf, sm.redd,
-                                      &sm.words[kWJ]);
-      cbar();
-      ++xhead;
-      if (tid == 0) {
-        emit<FUSED>(p, b, tok);
-        *reinterpret_cast<volatile uint32_t*>(&sm.words[kWXHead]) = xhead;
-      }
-    }
-    if (v & 0x80000000u) break;
-    if (tid == 0) __nanosleep(200);
+    if (!sm.words[kWRowOk]) break;
+    finish_row<MODE, FUSED>(p, own, sm);
+    cbar();  // before the next row reuses the shared memory
   }
 }
 
@@ -1409,15 +1332,14 @@ __global__ void __launch_bounds__(kThreads, 2) seg_kernel(const __grid_constant_
   __shared__ float redf[kConsWarps + 1];
   __shared__ double redd[kConsWarps + 1];
   __shared__ uint32_t words[32];
-  __shared__ uint32_t xq[kXQ];
+  __shared__ uint32_t segk[2 * kConsWarps];
   Smem sm;
   sm.ring4 = reinterpret_cast<uint4*>(dsm + kOffRing);
   sm.mask32 = reinterpret_cast<uint32_t*>(dsm + kOffMask);
-  sm.lut = reinterpret_cast<uint4*>(dsm + kOffLut);
   sm.pool = reinterpret_cast<uint32_t*>(dsm + kOffPool);
   sm.desc = reinterpret_cast<uint4*>(dsm + kOffDesc);
-  sm.svc_keys = reinterpret_cast<uint16_t*>(dsm + kOffSvc);
-  sm.svc_off = reinterpret_cast<uint32_t*>(dsm + kOffSvc + kListCap * 2);
+  sm.fin_id = reinterpret_cast<uint32_t*>(dsm + kOffFin);
+  sm.fin_bits = reinterpret_cast<uint16_t*>(dsm + kOffFin + kFinCap * 4);
   sm.full = full;
   sm.empty = empty;
   sm.sq_full = sq_full;
@@ -1427,7 +1349,7 @@ __global__ void __launch_bounds__(kThreads, 2) seg_kernel(const __grid_constant_
   sm.redf = redf;
   sm.redd = redd;
   sm.words = words;
-  sm.xq = xq;
+  sm.segk = segk;
 
   griddep_launch_dependents();
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1443,14 +1365,13 @@ __global__ void __launch_bounds__(kThreads, 2) seg_kernel(const __grid_constant_
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     for (uint32_t i = 0; i < 32; ++i) words[i] = 0u;
   }
-  for (uint32_t i = tid; i < 256; i += kThreads) sm.lut[i] = pair_mask_entry(i);
   __syncthreads();
   griddep_wait();  // the logits, the bitmask or the rows' states come from earlier work on the stream
 
   if (warp == kProdWarp) {
     if (lane == 0) words[kWIssued] = produce<FUSED>(p, dsm, full, empty, sm.desc, &words[kWAbort]);
   } else if (warp == kSvcWarp) {
-    service<MODE, FUSED>(p, sm);
+    service(p, sm);
   } else {
     consume<MODE, FUSED>(p, sm);
   }
