@@ -29,8 +29,14 @@ cudaError_t launch_accept_many(const Tables& t, const uint32_t* states, const ui
 cudaError_t launch_wait_timeout_self_test(uint32_t* status, cudaStream_t stream);
 cudaError_t launch_cache_fill(const Tables& t, const uint32_t* states, const uint16_t* gid, const int32_t* forced,
                               uint32_t B, unsigned long long* stats, cudaStream_t stream);
+bool step_fusable(int dtype, uint32_t V, uint32_t W, float temp, float top_p, const void* logits);
+cudaError_t launch_step(const Tables& t, const uint32_t* states, const uint16_t* gid, const int32_t* forced,
+                        uint32_t B, void* logits, uint32_t V, float temp, float top_p, uint64_t seed, uint32_t step,
+                        uint32_t* counts, uint32_t max_tokens, uint32_t* bitmask_out, uint32_t* out_tok,
+                        uint32_t* out_states, uint8_t* out_flags, void* scratch, const DevGrammar* host_grammars,
+                        bool cache_complete, cudaStream_t stream);
 size_t seg_scratch_bytes(uint32_t B);
-bool seg_usable(int dtype, uint32_t V, const void* logits, float* probs, int inplace);
+bool seg_usable(int dtype, uint32_t V, const void* logits, float* probs, int inplace, float temp, float top_p);
 bool seg_bitmask_ok(uint32_t W, const void* bitmask);
 cudaError_t launch_seg_sample(const void* logits, uint32_t B, uint32_t V, uint32_t W, const uint32_t* bitmask,
                               float temp, float top_p, uint64_t seed, uint32_t step, uint32_t* out_tok,
@@ -418,7 +424,8 @@ int cg_mask_and_sample(cg_ctx* c, void* d_logits, int dtype, uint32_t B, uint32_
   cgk::DeviceGuard dg(c->device);
   if (!dg.ok) return CG_E_CUDA;
   const int inplace = (flags & CG_SAMPLE_INPLACE) ? 1 : 0;
-  const bool seg_path = cgk::seg_usable(dtype, V, d_logits, d_probs, inplace) && cgk::seg_bitmask_ok(c->t.W, d_bitmask);
+  const bool seg_path =
+      cgk::seg_usable(dtype, V, d_logits, d_probs, inplace, temp, top_p) && cgk::seg_bitmask_ok(c->t.W, d_bitmask);
   // grown once per larger batch (outside any stream capture)
   const int rc = seg_path ? grow_zeroed(c, &c->seg_scratch, &c->seg_scratch_bytes, cgk::seg_scratch_bytes(B))
                           : grow(c, &c->sample_scratch, &c->sample_scratch_bytes, cgk::sample_scratch_bytes(B, V));
@@ -441,7 +448,8 @@ int cg_mask_and_sample_noalloc(cg_ctx* c, void* d_logits, int dtype, uint32_t B,
   unsigned char* scratch = static_cast<unsigned char*>(noalloc_scratch(&e));
   if (!scratch) return CG_E_CUDA;
   const int inplace = (flags & CG_SAMPLE_INPLACE) ? 1 : 0;
-  const bool seg_path = cgk::seg_usable(dtype, V, d_logits, d_probs, inplace) && cgk::seg_bitmask_ok(c->t.W, d_bitmask);
+  const bool seg_path =
+      cgk::seg_usable(dtype, V, d_logits, d_probs, inplace, temp, top_p) && cgk::seg_bitmask_ok(c->t.W, d_bitmask);
   unsigned char* seg = scratch + cgk::kNoAllocListBytes;
   // the segmented sampler's part starts at zero: cleared here, whatever an
   // earlier call (or one that ran out of a bounded wait) left in it
@@ -475,9 +483,19 @@ int cg_step(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const in
   cgk::DeviceGuard dg(c->device);
   if (!dg.ok) return CG_E_CUDA;
   int rc;
-  if (cgk::seg_usable(dtype, V, d_logits, nullptr, 0)) {
-    // one segmented kernel (after the class masks the rows miss, when the
-    // cache is not complete)
+  if (cgk::step_fusable(dtype, V, c->t.W, temp, top_p, d_logits)) {
+    // top-p: one per-row kernel (mask, sample and accept in one launch)
+    if ((rc = grow(c, &c->sample_scratch, &c->sample_scratch_bytes, cgk::sample_scratch_bytes(B, V))) != CG_OK)
+      return rc;
+    return cgk::launch_step(c->t, d_states, d_gid, d_forced, B, d_logits, V, temp, top_p, seed, step, d_counts,
+                            max_tokens, d_bitmask, d_out_tok, d_out_states, d_out_flags, c->sample_scratch,
+                            c->grammars.data(), c->cache_complete, c->stream) == cudaSuccess
+               ? CG_OK
+               : CG_E_CUDA;
+  }
+  if (cgk::seg_usable(dtype, V, d_logits, nullptr, 0, temp, top_p)) {
+    // greedy / every allowed token: one segmented kernel (after the class
+    // masks the rows miss, when the cache is not complete)
     if ((rc = grow_zeroed(c, &c->seg_scratch, &c->seg_scratch_bytes, cgk::seg_scratch_bytes(B))) != CG_OK) return rc;
     if (!c->cache_complete &&
         cgk::launch_cache_fill(c->t, d_states, d_gid, d_forced, B, c->cache_stats, c->stream) != cudaSuccess)

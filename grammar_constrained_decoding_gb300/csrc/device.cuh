@@ -87,7 +87,7 @@ int ctx_device(const cg_ctx* c);
 // that many rows fits.
 constexpr uint32_t kSampleListEntries = 8192;
 constexpr size_t kNoAllocListBytes = size_t(CG_NOALLOC_MAX_ROWS) * kSampleListEntries * 6;
-constexpr size_t kNoAllocSegBytes = size_t(7) << 20;
+constexpr size_t kNoAllocSegBytes = size_t(64) << 10;
 
 // Makes a device current for the duration of a call and puts the caller's
 // back: every launch, allocation and symbol lookup of a library call then

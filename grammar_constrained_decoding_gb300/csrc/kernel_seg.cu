@@ -1,54 +1,37 @@
-// Segmented streaming sampler: mask-apply + temperature + softmax + top-p +
-// Gumbel-max (or greedy, or Gumbel-max over every allowed token) with every SM
-// carrying the same share of the logits (the sampler sees only masked logits:
-// usetacet.com/docs/grammar, "The guarantee").
+// Segmented streaming sampler for greedy rows and for Gumbel-max over every
+// allowed token (top_p >= 1), with every SM carrying the same share of the
+// logits whatever the batch size (the sampler sees only masked logits:
+// usetacet.com/docs/grammar, "The guarantee").  Top-p rows take the per-row
+// kernels of kernel_sample.cu.
 //
 // What is computed per row b is what kernel_sample.cu's header states: with
-// z_t = x_t / temp over the allowed tokens, m = max z, S = sum exp(z - m), the
-// nucleus {t : z_t >= tau} with tau the largest value whose upper set carries
-// at least top_p of the mass, and the token argmax over the nucleus of
-// z_t + g_t, g_t = -log(-log u_t), u_t from Philox4x32-10 word t&3 of counter
-// (t>>2, b, step, 0).
+// z_t = x_t / temp over the allowed tokens, the token argmax of z_t + g_t,
+// g_t = -log(-log u_t), u_t from Philox4x32-10 word t&3 of counter
+// (t>>2, b, step, 0); greedy (temp = 0) the allowed token of largest logit,
+// lowest id on ties.
 //
 // Work decomposition.  Each row is cut into segments of up to four 4096-logit
 // chunks; a persistent grid (two CTAs per SM) takes segments from a work
-// counter in segment-major order (segment s of every row before segment s + 1,
-// so that a row's running maximum is mostly known before its later segments
-// are read), and the bytes each SM streams differ by at most a segment.  A CTA
-// has three roles.  The producer warp resolves each segment's mask source (the
-// caller's bitmask, or in the fused step the row's mask class in the mask
-// cache) ahead of time and streams the segment's logits and mask words into an
-// 8-slot shared-memory ring with bulk asynchronous copies.  Eight consumer
-// warps take each segment together, 64 logits per thread (two 8-logit groups
-// of each chunk).  The service warp counts each row's finished segments (a
-// fence and an atomic per segment, off the consumers' path).  Once the stream
-// is done, the consumers finish the rows their CTA owns (b = blockIdx.x +
-// k gridDim.x), each as soon as every segment of it is counted.
-//
-// Top-p, per segment and consumer warp (a "slice").  The thread's groups of
-// every chunk are loaded and masked at once and the ring slots released; the
-// slice maximum m_s goes to the row's running maximum in global memory, and
-// S_s = sum over the slice of exp2((x - m_s) c) (each thread against its own
-// maximum, rescaled once) is stored with m_s.  Candidates are the slice's
-// allowed logits at or above max(m_s, the row's running maximum) - margin
-// (kMarginZ nats), never above M - margin with M the row maximum, so every
-// allowed logit within the margin of M is one; the warp writes them (token
-// id, bf16 bits) into its region of the row's candidate list.  The row's
-// finisher merges M and S from the slices, gathers the candidates at or above
-// M - margin into shared memory and finds tau, the largest key whose upper
-// set carries top_p S (masses count exp2((x - M) c) in 2^-40 fixed point, so
-// sums do not depend on order), from 32-key mass bins and then the keys of
-// the bin where the target is reached; the token is the best Gumbel score
-// among the candidates at or above tau.  A row whose list region overflowed,
-// with more candidates than the finisher holds, or whose nucleus reaches below
-// the margin takes the exact multi-pass path over the row (same result).
+// counter in segment-major order (segment s of every row before segment
+// s + 1, so that a row's best score so far is mostly known before its later
+// segments are read), and the bytes each SM streams differ by at most a
+// segment.  A CTA has three roles.  The producer warp resolves each segment's
+// mask source (the caller's bitmask, or in the fused step the row's mask class
+// in the mask cache) ahead of time and streams the segment's logits and mask
+// words into an 8-slot shared-memory ring with bulk asynchronous copies.
+// Eight consumer warps take each chunk 16 logits per thread (two 8-logit
+// groups).  The service warp counts each row's finished segments (a fence and
+// an atomic per segment, off the consumers' path).  Once the stream is done,
+// the consumers finish the rows their CTA owns (b = blockIdx.x + k gridDim.x),
+// each as soon as every segment of it is counted.
 //
 // Greedy keeps each thread's best (x, lowest id).  Gumbel-max over every
-// allowed token (top_p >= 1) draws the Philox block of each group of four
-// tokens with an allowed one and tests a cheap upper bound of each token's
-// score (the noise g(u) = -ln(-ln u) is at most -ln(1 - u)) against the best
-// score found so far; the few tokens that pass are queued per warp and scored
-// exactly 32 at a time.  Both publish a packed (value, id) maximum per row.
+// allowed token draws the Philox block of each group of four tokens with an
+// allowed one and tests a cheap upper bound of each token's score (the noise
+// g(u) = -ln(-ln u) is at most -ln(1 - u)) against the best score found so
+// far (the row's best from its earlier segments included); the few tokens
+// that pass are queued per warp and scored exactly 32 at a time.  Both publish
+// a packed (value, id) maximum per row; the finisher takes the row's.
 //
 // The fused step (cg_step) also builds each row's mask from the mask-class
 // cache (rows with a forced token or without allowed tokens stream nothing:
@@ -56,11 +39,9 @@
 // accepts the token when the row finishes.
 //
 // Device scratch (the context's, zero before the first launch): a work counter
-// pair and, per row, accumulators, the slices' partial sums and candidate
-// counts, and the candidate list.  Every launch leaves the counters and the
-// accumulators at zero again (the last CTA to stop taking work resets the
-// counters; each row's finisher its accumulators); slices, counts and lists are
-// written in full before they are read.
+// pair and a (segments counted, best) pair per row.  Every launch leaves them
+// at zero again (the last CTA to stop taking work resets the counters; each
+// row's finisher its pair).
 #include <algorithm>
 #include <map>
 #include <mutex>
@@ -87,16 +68,8 @@ constexpr uint32_t kGroups = kChunk / 8;                   // 8-logit groups per
 constexpr uint32_t kMaxSegChunks = 4;
 constexpr uint32_t kSlots = 8;                             // two segments of four chunks in flight
 constexpr uint32_t kMaxNS = 64;                            // segments per row
-constexpr uint32_t kSlices = kMaxNS * kConsWarps;          // (segment, consumer warp) partials per row
-constexpr uint32_t kWindow = 4096;                         // per-key counters of the exact path
-constexpr uint32_t kListCap = 16384;                       // candidate-list entries per row (split among its slices)
-constexpr uint32_t kFinCap = 8192;                         // candidates a row's finisher holds (in the idle ring)
-constexpr uint32_t kCoarse = 2048;                         // finisher: mass bins of 32 keys below the maximum key
 constexpr uint32_t kSQ = 16;                               // records queued for the service warp (> kSlots)
 constexpr uint32_t kQ = 160;                               // queued exact scores per consumer warp (full)
-constexpr float kMarginZ = 8.5f;                           // nats below the maximum kept as candidates
-constexpr float kNoRef = -1e30f;                           // "no allowed logit yet"
-constexpr uint32_t kNotFound = 0xFFFFFFFFu;
 constexpr uint32_t kM0 = 0xD2511F53u, kM1 = 0xCD9E8D57u;   // Philox4x32 multipliers
 static_assert(kGroups == 2 * kCons, "two groups per consumer thread and slot");
 
@@ -104,57 +77,36 @@ static_assert(kGroups == 2 * kCons, "two groups per consumer thread and slot");
 constexpr uint32_t kOffRing = 0;
 constexpr uint32_t kOffMask = kOffRing + kSlots * kChunkBytes;
 constexpr uint32_t kOffPool = kOffMask + kSlots * kChunkWords * 4;
-constexpr uint32_t kPoolBytes = (kCoarse + 32) * 8 + kConsWarps * (kMaxNS + 2) * 4;  // exact-score queues, the exact
-                                                           // path's counters, the finisher's mass bins and offsets
+constexpr uint32_t kPoolBytes = kConsWarps * kQ * 10;      // exact-score queues (full)
 constexpr uint32_t kOffDesc = kOffPool + kPoolBytes;
 constexpr uint32_t kSmem = kOffDesc + kSlots * 16;
-// Once a CTA's stream is over (no copy in flight) its finisher keeps the
-// candidates of the row it finishes in the ring: ids, then bf16 bits.
-constexpr uint32_t kOffFin = kOffRing;
-static_assert(kFinCap * 6 <= kSlots * kChunkBytes, "the finisher's candidates fit the ring");
-static_assert(kWindow * 4 <= kPoolBytes, "the exact path's counters fit the pool region");
-static_assert(kConsWarps * kQ * 10 <= kPoolBytes, "exact-score queues fit the pool region");
 static_assert(kSmem <= 111 * 1024, "two CTAs a multiprocessor");
 
-enum Mode { kModeGreedy = 0, kModeTopP = 1, kModeFull = 2 };
+enum Mode { kModeGreedy = 0, kModeFull = 2 };
 // kinds of ring descriptors and service records
 constexpr uint32_t kStream = 0, kEmptyRow = 1, kForcedRow = 2, kNone = 3, kEnd = 4, kSkipPending = 5;
 
 struct RowAcc {
-  uint32_t maxkey;            // fkey of the running maximum logit published by the row's segments
   uint32_t done;              // segments counted
-  uint32_t flags;             // bit 0: a slice's candidates overflowed its list region, or a non-finite range
   uint32_t pad;
-  unsigned long long best;    // greedy / full: packed (value, id) maximum
-  unsigned long long pad2;
+  unsigned long long best;    // packed (value, id) maximum over the row's segments
 };
 
-// Per-row block of the scratch, at the same place whatever the batch size or
-// segment count of a launch (so that what one launch leaves at zero is zero
-// for the next): accumulators, each (segment, consumer warp) slice's partial
-// maximum and sum and its candidate count, and the candidate list: slice i
-// writes its candidates (token id, bf16 bits) into entries [i c, i c + c),
-// c = kListCap / (NS kConsWarps).  Slices and counts are written in full by
-// every launch; only the accumulators must start at zero.
-constexpr uint32_t kRowPart = 32;                                   // after RowAcc
-constexpr uint32_t kRowNSeg = kRowPart + kSlices * 8;
-constexpr uint32_t kRowLId = kRowNSeg + kSlices * 4;
-constexpr uint32_t kRowLBits = kRowLId + kListCap * 4;
-constexpr uint32_t kRowStride = (kRowLBits + kListCap * 2 + 127) & ~127u;
+// Per-row accumulators in the scratch, after a work-counter pair.  Every
+// launch leaves them at zero (the last CTA to stop taking work resets the
+// counters, each row's finisher its accumulators).
+constexpr uint32_t kRowStride = 16;
 constexpr uint32_t kCtlBytes = 256;
-static_assert(sizeof(RowAcc) <= kRowPart, "the row's accumulators precede its slices");
+static_assert(sizeof(RowAcc) == kRowStride, "one accumulator block a row");
 static_assert(kCtlBytes + size_t(CG_NOALLOC_MAX_ROWS) * kRowStride <= kNoAllocSegBytes,
               "the no-allocation scratch holds the segmented sampler's rows");
 
 struct Scratch {
   unsigned char* base;        // [kCtlBytes] counters, then [B] row blocks of kRowStride bytes
   __device__ uint32_t* ctl() const { return reinterpret_cast<uint32_t*>(base); }  // [0] next segment, [1] CTAs done
-  __device__ unsigned char* blk(uint32_t b) const { return base + kCtlBytes + size_t(b) * kRowStride; }
-  __device__ RowAcc* row(uint32_t b) const { return reinterpret_cast<RowAcc*>(blk(b)); }
-  __device__ float2* part(uint32_t b) const { return reinterpret_cast<float2*>(blk(b) + kRowPart); }
-  __device__ uint32_t* nseg(uint32_t b) const { return reinterpret_cast<uint32_t*>(blk(b) + kRowNSeg); }
-  __device__ uint32_t* lid(uint32_t b) const { return reinterpret_cast<uint32_t*>(blk(b) + kRowLId); }
-  __device__ uint16_t* lbits(uint32_t b) const { return reinterpret_cast<uint16_t*>(blk(b) + kRowLBits); }
+  __device__ RowAcc* row(uint32_t b) const {
+    return reinterpret_cast<RowAcc*>(base + kCtlBytes + size_t(b) * kRowStride);
+  }
 };
 
 struct Fused {
@@ -194,46 +146,26 @@ struct Src {
 struct Smem {
   uint4* ring4;
   uint32_t* mask32;
-  uint32_t* pool;              // per consumer warp: candidate ids and bits, or exact-score queues
+  uint32_t* pool;              // per consumer warp: the exact-score queue (full)
   uint4* desc;
-  uint32_t* segk;              // [2][kConsWarps] the slices' maximum keys of a segment, by parity
-  uint32_t* fin_id;            // [kFinCap] the finishing row's candidates: token ids
-  uint16_t* fin_bits;          // [kFinCap] and bf16 bits
   uint64_t* full;
   uint64_t* empty;
   uint64_t* sq_full;           // [kSQ] consumers -> service: a record is ready (kCons arrivals)
   uint64_t* sq_empty;          // [kSQ] service -> consumers: the record slot is free again
   uint4* sq_rec;               // [kSQ]
-  unsigned long long* red64;   // [kConsWarps + 1]
-  float* redf;                 // [kConsWarps + 1]
-  double* redd;                // [kConsWarps + 1]
   uint32_t* words;             // [32] scalars
 };
 enum {
-  kWJ = 0,      // scan result of the exact path
-  kWAbort,      // a bounded wait ran out
+  kWAbort = 0,  // a bounded wait ran out
   kWIssued,     // ring slots the producer used
   kWRowOk,      // the finishing row's segments are all counted
   kWKind,       // the finishing row's kind and forced token
   kWAux,
-  kWFinN,       // candidates the finisher gathered
-  kWBin,        // the finisher's crossing bin
-  kWTau,        // and nucleus key
 };
 
 __device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(kCons) : "memory"); }
 // consumer barrier that also returns whether any consumer thread passed true
 // (bounded waits can run out in some threads only; what follows must be uniform)
-__device__ __forceinline__ bool cbar_or(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}"
-      : "=r"(r)
-      : "r"(uint32_t(v)), "n"(kCons)
-      : "memory");
-  return r != 0;
-}
-
 __device__ __forceinline__ void red_add_u32(uint32_t* p, uint32_t v) {
   asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -285,39 +217,6 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
     v = y > v ? y : v;
   }
   return v;
-}
-
-// consumer-wide reductions (all 256 consumer threads call them; the result is
-// returned to every one of them)
-__device__ __forceinline__ unsigned long long cons_max_u64(unsigned long long v, unsigned long long* red) {
-  v = warp_max_u64(v);
-  cbar();
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  cbar();
-  unsigned long long r = red[0];
-#pragma unroll
-  for (uint32_t w = 1; w < kConsWarps; ++w) r = red[w] > r ? red[w] : r;
-  return r;
-}
-__device__ __forceinline__ float cons_max_f(float v, float* red) {
-  v = warp_reduce(v, MaxOp());
-  cbar();
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  cbar();
-  float r = red[0];
-#pragma unroll
-  for (uint32_t w = 1; w < kConsWarps; ++w) r = fmaxf(r, red[w]);
-  return r;
-}
-__device__ __forceinline__ double cons_sum_d(double v, double* red) {
-  v = warp_reduce(v, SumOp());
-  cbar();
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  cbar();
-  double r = 0.0;
-#pragma unroll
-  for (uint32_t w = 0; w < kConsWarps; ++w) r += red[w];
-  return r;
 }
 
 __device__ __forceinline__ DevGrammar grammar_of(const Fused& f, uint32_t g) {
@@ -521,128 +420,6 @@ __device__ uint32_t produce(const Params& p, unsigned char* dsm, uint64_t* full,
   return q;
 }
 
-// Mask row of b in global memory (the exact path reads it).
-template <int FUSED>
-__device__ const uint32_t* row_mask_ptr(const Params& p, uint32_t b) {
-  if (!FUSED) return p.bitmask + size_t(b) * p.W;
-  return stage2<1>(p, stage1<1>(p, b)).mask;
-}
-
-// Exact top-p over the row in global memory (consumer threads only): pass A
-// for M and S (compensated sums), the per-key counts of the kWindow keys below
-// the maximum (bisection over the key space when the nucleus reaches deeper),
-// then Gumbel-max over the nucleus.  The same definition as the streaming
-// path; it reads the row three times or more.
-__device__ __noinline__ uint32_t exact_topp(const Params& p, uint32_t b, const uint32_t* gmask, uint32_t* cnt,
-                               unsigned long long* red64, float* redf, double* redd, uint32_t* s_word) {
-  const uint32_t V = p.V, tid = threadIdx.x;
-  const float temp = p.temp, c = 1.4426950408889634f / temp;
-  const uint4* row4 = reinterpret_cast<const uint4*>(p.logits + size_t(b) * V);
-  // f(t, bf16 bits of x_t) for every allowed token, four groups per thread
-  // and pass with their loads in flight together
-  auto for_allowed = [&](auto&& f) {
-    const uint32_t ng = V / 8;
-    for (uint32_t i0 = tid; i0 < ng; i0 += 4 * kCons) {
-      uint4 v[4];
-      uint32_t bits[4];
-#pragma unroll
-      for (uint32_t u = 0; u < 4; ++u) {
-        const uint32_t i = i0 + u * kCons;
-        bits[u] = i < ng ? (__ldg(gmask + (i >> 2)) >> ((i & 3u) * 8u)) & 0xFFu : 0u;
-        v[u] = i < ng ? __ldg(row4 + i) : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (uint32_t u = 0; u < 4; ++u) {
-        if (!bits[u]) continue;
-        const uint32_t i = i0 + u * kCons;
-#pragma unroll
-        for (uint32_t e = 0; e < 8; ++e)
-          if ((bits[u] >> e) & 1u) f(i * 8 + e, group_bits(v[u], e));
-      }
-    }
-  };
-  float m = -INFINITY, sum = 0.f, comp = 0.f;
-  for_allowed([&](uint32_t, uint32_t h) {
-    const float x = bf16_bits_to_float(h);
-    if (x > m) {
-      const float r = exp2f((m - x) * c);
-      sum *= r;
-      comp *= r;
-      m = x;
-    }
-    const float y = exp2f((x - m) * c) - comp;
-    const float nt = sum + y;
-    comp = (nt - sum) - y;
-    sum = nt;
-  });
-  const float M = cons_max_f(m, redf);
-  if (!(M > -INFINITY)) return CG_NO_TOKEN;
-  double part = 0.0;
-  if (m > -INFINITY) part = (double(sum) - double(comp)) * double(exp2f((m - M) * c));
-  const double S = cons_sum_d(part, redd);
-  const double target = double(p.top_p) * S;
-  const uint32_t km = fkey(M) >> 16;
-  const uint32_t lo = km >= kWindow - 1 ? km - (kWindow - 1) : 0u;
-  for (uint32_t i = tid; i < kWindow; i += kCons) cnt[i] = 0u;
-  cbar();
-  for_allowed([&](uint32_t, uint32_t h) {
-    const uint32_t k = fkey(bf16_bits_to_float(h)) >> 16;
-    if (k >= lo) atomicAdd(cnt + (km - k), 1u);
-  });
-  cbar();
-  if (tid < 32) {
-    const uint32_t lane = tid;
-    double cum = 0.0;
-    uint32_t found = kNotFound;
-    for (uint32_t base = 0; base <= km - lo && found == kNotFound; base += 32) {
-      const uint32_t j = base + lane;
-      double mass = 0.0;
-      if (j <= km - lo && cnt[j]) mass = double(cnt[j]) * double(exp2f((bf16key_to_float(km - j) - M) * c));
-      double incl = mass;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= uint32_t(o)) incl += y;
-      }
-      const unsigned hit = __ballot_sync(0xFFFFFFFFu, cum + incl >= target);
-      if (hit) found = base + uint32_t(__ffs(hit) - 1);
-      cum += __shfl_sync(0xFFFFFFFFu, incl, 31);
-    }
-    if (lane == 0) *s_word = (found == kNotFound) ? kNotFound : km - found;
-  }
-  cbar();
-  uint32_t tau = *s_word;
-  if (tau == kNotFound) {
-    // largest key whose upper set carries the target, by bisection
-    uint32_t klo = 0, khi = km;
-    while (klo < khi) {
-      const uint32_t mid = klo + (khi - klo + 1) / 2;
-      float ps = 0.f;
-      for_allowed([&](uint32_t, uint32_t h) {
-        const float x = bf16_bits_to_float(h);
-        if ((fkey(x) >> 16) >= mid) ps += exp2f((x - M) * c);
-      });
-      const double mass = cons_sum_d(double(ps), redd);
-      if (mass >= target) klo = mid; else khi = mid - 1;
-    }
-    tau = klo;
-  }
-  unsigned long long best = 0ull;
-  uint32_t cached = 0xFFFFFFFFu;
-  uint4 blk = make_uint4(0u, 0u, 0u, 0u);
-  for_allowed([&](uint32_t t, uint32_t h) {
-    const float x = bf16_bits_to_float(h);
-    if ((fkey(x) >> 16) < tau) return;
-    if ((t >> 2) != cached) {
-      blk = philox4x32_10(make_uint4(t >> 2, b, p.step, 0u), p.rk[0], p.rk[1]);
-      cached = t >> 2;
-    }
-    best = max(best, pack_best(__fdiv_rn(x, temp) + gumbel_from_word(philox_word(blk, t & 3u)), t));
-  });
-  best = cons_max_u64(best, red64);
-  return best ? best_id(best) : CG_NO_TOKEN;
-}
-
 // Outputs of a finished row: the token, and in the fused step the accept.
 template <int FUSED>
 __device__ __noinline__ void emit(const Params& p, uint32_t b, uint32_t tok) {
@@ -704,198 +481,6 @@ __device__ void finish_skip(const Params& p, uint32_t b, uint32_t kind, uint32_t
   }
 }
 
-// Top-p token of row b from its slices and candidate list, or kNotFound when
-// the exact path must decide (a slice's list region overflowed, a non-finite
-// range, more candidates than the finisher holds, or a nucleus that reaches
-// below the candidates' margin).  M and S merge the slices' (m_s, S_s); the
-// candidates at or above M - margin are gathered into shared memory; tau,
-// the largest key whose upper set carries top_p S (masses count
-// exp2((x - M) c) in 2^-40 fixed point, so that no sum depends on order),
-// comes from two passes of mass bins: 32-key bins below the maximum key,
-// then the keys of the bin where the upper mass reaches the target; the
-// token is the best Gumbel score among the candidates at or above tau.
-template <int FUSED>
-__device__ __noinline__ uint32_t finish_topp(const Params& p, uint32_t b, const Smem& sm) {
-  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t NS = p.NS, NSW = NS * kConsWarps, capW = kListCap / NSW;
-  const float temp = p.temp, c = 1.4426950408889634f / temp, margin = kMarginZ * temp;
-  const RowAcc* ra = p.sc.row(b);
-  // one round of loads: the flags, every slice's (m_s, S_s), and each warp's
-  // slices' candidate counts (warp w takes slices w, w + 8, ..., one per segment)
-  const uint32_t flags = __ldcg(&ra->flags);
-  const float2* part = p.sc.part(b);
-  const float2 pa = tid < NSW ? __ldcg(part + tid) : make_float2(kNoRef, 0.f);
-  const float2 pb = tid + kCons < NSW ? __ldcg(part + tid + kCons) : make_float2(kNoRef, 0.f);
-  const uint32_t* nseg = p.sc.nseg(b);
-  const uint32_t na = lane < NS ? __ldcg(nseg + warp + kConsWarps * lane) : 0u;
-  const uint32_t nb = lane + 32 < NS ? __ldcg(nseg + warp + kConsWarps * (lane + 32)) : 0u;
-  // M and S: the thread's two slices merged, then across the threads
-  float lm = kNoRef, ls = 0.f;
-#pragma unroll
-  for (uint32_t h = 0; h < 2; ++h) {
-    const float2 v = h ? pb : pa;
-    if (v.x > kNoRef && v.y > 0.f) {
-      if (v.x > lm) {
-        ls = ls * ex2((lm - v.x) * c) + v.y;
-        lm = v.x;
-      } else {
-        ls += v.y * ex2((v.x - lm) * c);
-      }
-    }
-  }
-  const float M = cons_max_f(lm, sm.redf);
-  const double S = cons_sum_d(lm > kNoRef ? double(ls * ex2((lm - M) * c)) : 0.0, sm.redd);
-  if (!(M > kNoRef)) return CG_NO_TOKEN;  // no allowed token in the row
-  if (!(M < 1e29f) || (flags & 1u)) return kNotFound;
-  const float thrF = M - margin;
-  const uint32_t km = fkey(M) >> 16;
-  uint32_t kthr = fkey(thrF) >> 16;
-  if (bf16key_to_float(kthr) < thrF) ++kthr;
-  const unsigned long long target =
-      max(1ull, static_cast<unsigned long long>(double(p.top_p) * S * 1099511627776.0));  // top_p of the mass
-  // gather the candidates at or above kthr into shared memory: the warp's
-  // slices' offsets by a scan, then every entry's loads in flight together
-  unsigned long long* hist = reinterpret_cast<unsigned long long*>(sm.pool);  // [kCoarse + 32]
-  uint32_t* woff = reinterpret_cast<uint32_t*>(sm.pool + (kCoarse + 32) * 2) + warp * (kMaxNS + 2);
-  const uint32_t nws = NS;
-  for (uint32_t i = tid; i < kCoarse + 32; i += kCons) hist[i] = 0ull;
-  if (tid == 0) sm.words[kWFinN] = 0u;
-  uint32_t ia = na, ib = nb;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t ya = __shfl_up_sync(0xFFFFFFFFu, ia, o), yb = __shfl_up_sync(0xFFFFFFFFu, ib, o);
-    if (lane >= uint32_t(o)) {
-      ia += ya;
-      ib += yb;
-    }
-  }
-  const uint32_t ta = __shfl_sync(0xFFFFFFFFu, ia, 31);
-  woff[lane] = ia - na;                 // start of slice warp + 8 lane in the warp's flat order
-  woff[lane + 32] = ta + ib - nb;
-  const uint32_t T = ta + __shfl_sync(0xFFFFFFFFu, ib, 31);
-  woff[64] = T;
-  cbar();
-  const uint32_t* lid = p.sc.lid(b);
-  const uint16_t* lbits = p.sc.lbits(b);
-  // f(valid, id, bits) for every entry of the warp's slices, 4 x 32 at a time
-  // (warp-uniform trip count: f may use warp collectives)
-  auto walk = [&](auto&& f) {
-    for (uint32_t e0 = 0; e0 < T; e0 += 32 * 4) {
-      uint32_t id[4], xb[4];
-#pragma unroll
-      for (uint32_t u = 0; u < 4; ++u) {
-        const uint32_t e = e0 + 32 * u + lane;
-        id[u] = 0u;
-        xb[u] = 0u;
-        if (e < T) {
-          uint32_t lo = 0, hi = nws;  // the slice of flat entry e: woff[lo] <= e < woff[lo + 1]
-          while (hi - lo > 1) {
-            const uint32_t mid = (lo + hi) >> 1;
-            if (woff[mid] <= e) lo = mid; else hi = mid;
-          }
-          const size_t at = size_t(warp + kConsWarps * lo) * capW + (e - woff[lo]);
-          id[u] = __ldcg(lid + at);
-          xb[u] = __ldcg(lbits + at);
-        }
-      }
-#pragma unroll
-      for (uint32_t u = 0; u < 4; ++u) f(e0 + 32 * u + lane < T && bf16_key(xb[u]) >= kthr, id[u], xb[u]);
-    }
-  };
-  walk([&](bool keep, uint32_t id, uint32_t xb) {
-    const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep);
-    uint32_t base = 0;
-    if (lane == 0 && bal) base = atomicAdd(&sm.words[kWFinN], uint32_t(__popc(bal)));
-    base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(bal & ((1u << lane) - 1u));
-    if (keep && base < kFinCap) {
-      sm.fin_id[base] = id;
-      sm.fin_bits[base] = uint16_t(xb);
-    }
-  });
-  cbar();
-  const uint32_t nf = sm.words[kWFinN];
-  // f(id, bits) for every candidate at or above kthr: from shared memory, or
-  // (more than it holds) from the list again
-  auto for_cands = [&](auto&& f) {
-    if (nf <= kFinCap) {
-      for (uint32_t i = tid; i < nf; i += kCons) f(sm.fin_id[i], uint32_t(sm.fin_bits[i]));
-    } else {
-      walk([&](bool keep, uint32_t id, uint32_t xb) {
-        if (keep) f(id, xb);
-      });
-    }
-  };
-  // pass 1: masses per 32-key bin, bin 0 the maximum key's
-  for_cands([&](uint32_t, uint32_t h) {
-    atomicAdd(hist + ((km - bf16_key(h)) >> 5), mass_q(bf16_bits_to_float(h), M, c));
-  });
-  cbar();
-  // the bin where the upper mass reaches the target: thread t sums bins 8t .. 8t + 7
-  unsigned long long loc = 0ull;
-#pragma unroll
-  for (uint32_t i = 0; i < 8; ++i) loc += hist[8 * tid + i];
-  unsigned long long sc64 = loc;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, sc64, o);
-    if (lane >= uint32_t(o)) sc64 += y;
-  }
-  if (lane == 31) sm.red64[warp] = sc64;
-  cbar();
-  unsigned long long before = 0ull, total = 0ull;
-#pragma unroll
-  for (uint32_t w = 0; w < kConsWarps; ++w) {
-    before += w < warp ? sm.red64[w] : 0ull;
-    total += sm.red64[w];
-  }
-  before += sc64 - loc;  // the mass of the bins above this thread's
-  if (total < target) return kNotFound;  // the nucleus reaches below the candidates (uniform)
-  cbar();
-  if (before < target && before + loc >= target) {
-    unsigned long long run = before;
-    for (uint32_t i = 0; i < 8; ++i) {
-      const unsigned long long h = hist[8 * tid + i];
-      if (run + h >= target) {
-        sm.words[kWBin] = 8 * tid + i;
-        sm.red64[kConsWarps] = run;  // the mass above the bin
-        break;
-      }
-      run += h;
-    }
-  }
-  cbar();
-  const uint32_t bin = sm.words[kWBin];
-  // pass 2: masses per key of that bin; tau where the upper mass reaches the target
-  unsigned long long* fine = hist + kCoarse;
-  for_cands([&](uint32_t, uint32_t h) {
-    const uint32_t d = km - bf16_key(h);
-    if ((d >> 5) == bin) atomicAdd(fine + (d & 31u), mass_q(bf16_bits_to_float(h), M, c));
-  });
-  cbar();
-  if (warp == 0) {
-    unsigned long long run = fine[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, run, o);
-      if (lane >= uint32_t(o)) run += y;
-    }
-    const unsigned hit = __ballot_sync(0xFFFFFFFFu, sm.red64[kConsWarps] + run >= target);
-    if (lane == 0) sm.words[kWTau] = km - (32 * bin + (hit ? uint32_t(__ffs(hit) - 1) : 31u));
-  }
-  cbar();
-  const uint32_t tau = sm.words[kWTau];
-  // pass 3: the best Gumbel score among the candidates at or above tau
-  const PhRow pr = philox_row(p, b);
-  unsigned long long best = 0ull;
-  for_cands([&](uint32_t id, uint32_t h) {
-    if (bf16_key(h) < tau) return;
-    const uint4 blk = philox_q(p, pr, id >> 2);
-    best = max(best, pack_best(gumbel_score(bf16_bits_to_float(h), temp, philox_word(blk, id & 3u)), id));
-  });
-  best = cons_max_u64(best, sm.red64);
-  return best ? best_id(best) : CG_NO_TOKEN;
-}
-
 // Finishes row b once every segment of it is counted: its token (and the
 // accept in the fused step), then its accumulators back to zero.
 template <int MODE, int FUSED>
@@ -916,20 +501,10 @@ __device__ void finish_row(const Params& p, uint32_t b, const Smem& sm) {
       return;
     }
   }
-  uint32_t tok;
-  if (MODE == kModeTopP) {
-    tok = finish_topp<FUSED>(p, b, sm);
-    cbar();
-    if (tok == kNotFound)
-      tok = exact_topp(p, b, row_mask_ptr<FUSED>(p, b), sm.pool, sm.red64, sm.redf, sm.redd, &sm.words[kWJ]);
-  } else {
-    const unsigned long long v = __ldcg(&ra->best);
-    tok = v ? best_id(v) : CG_NO_TOKEN;
-  }
+  const unsigned long long v = __ldcg(&ra->best);
+  const uint32_t tok = v ? best_id(v) : CG_NO_TOKEN;
   if (tid == 0) {
-    ra->maxkey = 0u;
     ra->done = 0u;
-    ra->flags = 0u;
     ra->best = 0ull;
     emit<FUSED>(p, b, tok);
   }
@@ -960,152 +535,10 @@ __device__ __noinline__ void drain_queue(const uint32_t* qid, const uint32_t* qw
   }
 }
 
-// Top-p: one segment of a row in one step of a consumer warp.  The thread's
-// groups of every chunk of the segment are loaded and masked together (the
-// slots go back to the producer as soon as the loads are done); then the
-// warp's maximum (published to the row's), the thread's exponential sums
-// against its own maximum (no rescaling inside a segment), and the candidates
-// at or above max(warp maximum, the row's maximum as read at the segment's
-// start) - margin, extracted with one warp scan, scored with their Gumbel
-// noise and added to the row's key histogram and candidate list.  Returns
-// false (all lanes) when a wait for a chunk ran out.
-template <int FUSED>
-__device__ __forceinline__ bool topp_segment(const Params& p, const Smem& sm, uint32_t b, uint32_t s, uint32_t nch,
-                                             uint32_t q, uint32_t par) {
-  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const float c = 1.4426950408889634f / p.temp, margin = kMarginZ * p.temp;
-  const uint32_t g0 = warp * 64 + lane;
-  RowAcc* ra = p.sc.row(b);
-  uint32_t G = 0;  // the row's maximum so far, read while the segment's chunks arrive
-  if (lane == 0) G = ld_relaxed(&ra->maxkey);
-  bool ok = true;
-  for (uint32_t k = 1; k < nch; ++k) ok = ok && mbar_wait(sm.full + (q + k) % kSlots, ((q + k) / kSlots) & 1u);
-
-  // the thread's 2 nch groups, masked, and their packed maxima
-  uint4 v[2 * kMaxSegChunks];
-  uint32_t a[2 * kMaxSegChunks];
-  uint32_t am = 0xFF80FF80u;
-#pragma unroll
-  for (uint32_t j = 0; j < 2 * kMaxSegChunks; ++j) {
-    const uint32_t k = j >> 1, g = g0 + (j & 1u) * 32u;
-    v[j] = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
-    if (k < nch) {
-      const uint32_t ck = s * p.segc + k, sl = (q + k) % kSlots;
-      if (g < min(kGroups, (p.V - ck * kChunk) >> 3)) {
-        const uint32_t mb = reinterpret_cast<const uint8_t*>(sm.mask32 + sl * kChunkWords)[g];
-        v[j] = apply_mask(sm.ring4[sl * kGroups + g], pair_mask_of(mb));
-      }
-    }
-    a[j] = group_pmax(v[j]);
-    am = bmax2(am, a[j]);
-  }
-  if (FUSED && p.f.bitmask_out && lane < 16) {
-    for (uint32_t k = 0; k < nch; ++k) {
-      const uint32_t wi = (s * p.segc + k) * kChunkWords + warp * 16 + lane;
-      if (wi < p.W) p.f.bitmask_out[size_t(b) * p.W + wi] = sm.mask32[((q + k) % kSlots) * kChunkWords + warp * 16 + lane];
-    }
-  }
-  const bool wok = __all_sync(0xFFFFFFFFu, ok);
-  __syncwarp();  // the warp's reads of the slots before their release
-  if (lane == 0 && wok)
-    for (uint32_t k = 0; k < nch; ++k) mbar_arrive(sm.empty + (q + k) % kSlots);
-
-  // the slice's maximum, and the segment's (the eight slices' through shared
-  // memory, double-buffered by segment parity), published to the row's
-  const float tm = pmax_f(am);
-  const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, fkey(tm));
-  const bool any = wk > 0x007FFFFFu;  // an allowed logit in the slice
-  const float wm = any ? fkey_inv(wk) : kNoRef;
-  uint32_t* segk = sm.segk + (par & 1u) * kConsWarps;
-  if (lane == 0) segk[warp] = wk;
-  if (cbar_or(!ok)) return false;  // every consumer thread arrives here once per segment
-  uint32_t sk = segk[0];
-#pragma unroll
-  for (uint32_t w = 1; w < kConsWarps; ++w) sk = max(sk, segk[w]);
-  if (threadIdx.x == 0 && sk > 0x007FFFFFu) red_max_u32(&ra->maxkey, sk);
-
-  // the thread's sums against its own maximum (masked logits add exp2(-inf) = 0)
-  const float mt = fmaxf(tm, kNoRef);
-  float2 acc[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) acc[j] = make_float2(0.f, 0.f);
-  const float2 c2 = make_float2(c, c), nmc2 = make_float2(-mt * c, -mt * c);
-#pragma unroll
-  for (uint32_t j = 0; j < 2 * kMaxSegChunks; ++j)  // groups masked out for the whole warp add nothing
-    if ((j >> 1) < nch && __any_sync(0xFFFFFFFFu, a[j] != 0xFF80FF80u)) add_exps(acc, v[j], c2, nmc2);
-  const float asum = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
-  float part = (any && asum > 0.f) ? asum * ex2((mt - wm) * c) : 0.f;
-  part = warp_reduce(part, SumOp());
-
-  // the candidate threshold: its bf16 key k16 (and bits t2 in both halves)
-  G = max(sk, __shfl_sync(0xFFFFFFFFu, G, 0));
-  uint32_t k16 = kNotFound, t2 = 0;
-  bool bad = false;  // a non-finite range or an overflowing buffer: the exact path decides
-  if (any) {
-    const float thr = fkey_inv(G) - margin;
-    if (thr > -1e29f && thr < 1e29f) {
-      k16 = fkey(thr) >> 16;
-      if (bf16key_to_float(k16) < thr) ++k16;
-      const uint32_t t16 = __float_as_uint(bf16key_to_float(k16)) >> 16;
-      t2 = t16 | (t16 << 16);
-    } else {
-      bad = true;
-    }
-  }
-  // candidates: per group the bits of its logits >= threshold, one scan for the positions
-  unsigned long long cb = 0ull;
-  uint32_t n = 0;
-  const __nv_bfloat162 tb = *reinterpret_cast<const __nv_bfloat162*>(&t2);
-  if (k16 != kNotFound && __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&am), tb) != 0u) {
-#pragma unroll
-    for (uint32_t j = 0; j < 2 * kMaxSegChunks; ++j) {
-      if (__hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&a[j]), tb) != 0u) {
-        const uint32_t bits = group_ge_bits(v[j], t2);
-        cb |= static_cast<unsigned long long>(bits) << (8 * j);
-        n += __popc(bits);
-      }
-    }
-  }
-  uint32_t inc = n;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-    if (lane >= uint32_t(o)) inc += y;
-  }
-  const uint32_t total = __shfl_sync(0xFFFFFFFFu, inc, 31);
-  // into the slice's region of the row's candidate list
-  const uint32_t slice = s * kConsWarps + warp, capW = kListCap / (p.NS * kConsWarps);
-  uint32_t* lid = p.sc.lid(b) + size_t(slice) * capW;
-  uint16_t* lbits = p.sc.lbits(b) + size_t(slice) * capW;
-  uint32_t pos = inc - n;
-#pragma unroll
-  for (uint32_t j = 0; j < 2 * kMaxSegChunks; ++j) {
-    uint32_t bits = static_cast<uint32_t>(cb >> (8 * j)) & 0xFFu;
-    const uint32_t t0 = (s * p.segc + (j >> 1)) * kChunk + (g0 + (j & 1u) * 32u) * 8u;
-    while (bits) {
-      const uint32_t e = __ffs(bits) - 1;
-      bits &= bits - 1;
-      if (pos < capW) {
-        lid[pos] = t0 + e;
-        lbits[pos] = uint16_t(group_bits(v[j], e));
-      }
-      ++pos;
-    }
-  }
-  if (lane == 0) {
-    p.sc.part(b)[slice] = make_float2(wm, part);
-    p.sc.nseg(b)[slice] = min(total, capW);
-    if (bad || total > capW) atomicOr(&ra->flags, 1u);
-  }
-  return true;
-}
-
 // Each consumer warp works on its own share of every chunk (64 groups of 8
 // logits) and ends each segment on its own: no consumer-wide barrier on the
-// stream's path.  Per segment a warp publishes its slice's (maximum, sum),
-// extracts its candidates against max(its maximum, the row's running
-// maximum) - margin, scores them, releases the ring slots and arrives on the
-// service record.
+// stream's path.  Per segment a warp raises the row's packed best with its
+// own and arrives on the service record.
 template <int MODE, int FUSED>
 __device__ void consume(const Params& p, const Smem& sm) {
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1116,7 +549,6 @@ __device__ void consume(const Params& p, const Smem& sm) {
   const uint4 kNeg4 = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
   uint32_t q = 0;     // ring slots taken
   uint32_t nrec = 0;  // records sent to the service warp
-  uint32_t nts = 0;   // top-p segments taken
   bool ok = true;
   // One record for the service warp: thread 0 writes it once its slot is
   // free; every consumer thread arrives once its own writes for it are done.
@@ -1155,16 +587,6 @@ __device__ void consume(const Params& p, const Smem& sm) {
       ++q;
       continue;
     }
-    if (MODE == kModeTopP) {
-      if (!topp_segment<FUSED>(p, sm, b, s, nch, q, nts++)) {
-        ok = false;
-        break;
-      }
-      post(b, s, kStream, 0u);
-      q += nch;
-      continue;
-    }
-
     // ---- greedy / full: the segment's chunks one by one ------------------------------
     unsigned long long best = 0ull;    // greedy / full: packed (value, id)
     float bestv = -INFINITY;           // greedy: value of best; full: the bound's reference score
@@ -1197,77 +619,75 @@ __device__ void consume(const Params& p, const Smem& sm) {
         mb1 = m8[g1];
         v1 = apply_mask(r4[g1], pair_mask_of(mb1));
       }
-      {
-        if (FUSED && p.f.bitmask_out && lane < 16) {
-          const uint32_t wi = ck * kChunkWords + warp * 16 + lane;
-          if (wi < p.W) p.f.bitmask_out[size_t(b) * p.W + wi] = sm.mask32[sl * kChunkWords + warp * 16 + lane];
+      if (FUSED && p.f.bitmask_out && lane < 16) {
+        const uint32_t wi = ck * kChunkWords + warp * 16 + lane;
+        if (wi < p.W) p.f.bitmask_out[size_t(b) * p.W + wi] = sm.mask32[sl * kChunkWords + warp * 16 + lane];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.empty + sl);
+      if (MODE == kModeGreedy) {
+        const uint32_t a0 = group_pmax(v0), a1 = group_pmax(v1);
+#pragma unroll
+        for (uint32_t h = 0; h < 2; ++h) {
+          const uint4& v = h ? v1 : v0;
+          const float gm = pmax_f(h ? a1 : a0);
+          if (gm > bestv) {  // strictly: this thread sees ids in increasing order
+            uint32_t e = 0;
+            while (e < 7 && group_at(v, e) != gm) ++e;
+            best = pack_best(gm, ck * kChunk + (h ? g1 : g0) * 8 + e);
+            bestv = gm;
+          }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sm.empty + sl);
-        if (MODE == kModeGreedy) {
-          const uint32_t a0 = group_pmax(v0), a1 = group_pmax(v1);
-#pragma unroll
-          for (uint32_t h = 0; h < 2; ++h) {
-            const uint4& v = h ? v1 : v0;
-            const float gm = pmax_f(h ? a1 : a0);
-            if (gm > bestv) {  // strictly: this thread sees ids in increasing order
-              uint32_t e = 0;
-              while (e < 7 && group_at(v, e) != gm) ++e;
-              best = pack_best(gm, ck * kChunk + (h ? g1 : g0) * 8 + e);
-              bestv = gm;
+      } else {
+        if (k == 1) {
+          // the bound's first outside reference: the row's best score from its other segments
+          const unsigned long long sb = __shfl_sync(0xFFFFFFFFu, seed_best, 0);
+          if (sb) {
+            const float v = fkey_inv(static_cast<uint32_t>(sb >> 32));
+            if (v > bestv) {
+              bestv = v;
+              offB = 23.f - v * 1.4426950408889634f;
             }
           }
-        } else {
-          if (k == 1) {
-            // the bound's first outside reference: the row's best score from its other segments
-            const unsigned long long sb = __shfl_sync(0xFFFFFFFFu, seed_best, 0);
-            if (sb) {
-              const float v = fkey_inv(static_cast<uint32_t>(sb >> 32));
-              if (v > bestv) {
-                bestv = v;
-                offB = 23.f - v * 1.4426950408889634f;
-              }
-            }
-          }
+        }
 #pragma unroll 1
-          for (uint32_t h = 0; h < 2; ++h) {
-            const uint4 v = h ? v1 : v0;
-            const uint32_t mb = h ? mb1 : mb0;
-            const uint32_t t0 = ck * kChunk + (h ? g1 : g0) * 8;
+        for (uint32_t h = 0; h < 2; ++h) {
+          const uint4 v = h ? v1 : v0;
+          const uint32_t mb = h ? mb1 : mb0;
+          const uint32_t t0 = ck * kChunk + (h ? g1 : g0) * 8;
 #pragma unroll 1
-            for (uint32_t half = 0; half < 2; ++half) {
-              const uint32_t nib = (mb >> (4 * half)) & 15u;
-              uint4 blk = make_uint4(0u, 0u, 0u, 0u);
-              if (nib) blk = philox_q(p, phr, (t0 >> 2) + half);
-              const uint32_t wa = half ? v.z : v.x, wb = half ? v.w : v.y;
+          for (uint32_t half = 0; half < 2; ++half) {
+            const uint32_t nib = (mb >> (4 * half)) & 15u;
+            uint4 blk = make_uint4(0u, 0u, 0u, 0u);
+            if (nib) blk = philox_q(p, phr, (t0 >> 2) + half);
+            const uint32_t wa = half ? v.z : v.x, wb = half ? v.w : v.y;
 #pragma unroll
-              for (uint32_t e = 0; e < 4; ++e) {
-                const uint32_t wd = e < 2 ? wa : wb;
-                const float x = (e & 1u) ? hi_f(wd) : lo_f(wd);
-                const uint32_t w = e == 0 ? blk.x : e == 1 ? blk.y : e == 2 ? blk.z : blk.w;
-                // the token's score can beat bestv only if 2^23 exp(z - bestv)
-                // (slightly enlarged) exceeds 2^23 - 1 - (w >> 9), i.e. the
-                // bound -ln(1 - u) of its noise reaches bestv - z
-                const float tq = ex2(fmaf(x, c, offB)) * 1.0001f;
-                const float vv = __uint_as_float((w >> 9) ^ 0x4B7FFFFFu) - 8388608.0f;
-                const bool pass = ((nib >> e) & 1u) && vv < tq;
-                const unsigned bal = __ballot_sync(0xFFFFFFFFu, pass);
-                if (bal) {
-                  const uint32_t pos = qn + __popc(bal & lt);
-                  if (pass) {
-                    qid[pos] = t0 + 4 * half + e;
-                    qw[pos] = w;
-                    qx[pos] = uint16_t((e & 1u) ? (wd >> 16) : (wd & 0xFFFFu));
-                  }
-                  qn += __popc(bal);
+            for (uint32_t e = 0; e < 4; ++e) {
+              const uint32_t wd = e < 2 ? wa : wb;
+              const float x = (e & 1u) ? hi_f(wd) : lo_f(wd);
+              const uint32_t w = e == 0 ? blk.x : e == 1 ? blk.y : e == 2 ? blk.z : blk.w;
+              // the token's score can beat bestv only if 2^23 exp(z - bestv)
+              // (slightly enlarged) exceeds 2^23 - 1 - (w >> 9), i.e. the
+              // bound -ln(1 - u) of its noise reaches bestv - z
+              const float tq = ex2(fmaf(x, c, offB)) * 1.0001f;
+              const float vv = __uint_as_float((w >> 9) ^ 0x4B7FFFFFu) - 8388608.0f;
+              const bool pass = ((nib >> e) & 1u) && vv < tq;
+              const unsigned bal = __ballot_sync(0xFFFFFFFFu, pass);
+              if (bal) {
+                const uint32_t pos = qn + __popc(bal & lt);
+                if (pass) {
+                  qid[pos] = t0 + 4 * half + e;
+                  qw[pos] = w;
+                  qx[pos] = uint16_t((e & 1u) ? (wd >> 16) : (wd & 0xFFFFu));
                 }
+                qn += __popc(bal);
               }
-              while (qn >= 32) {
-                __syncwarp();
-                drain_queue(qid, qw, qx, qn - 32, 32, temp, best, bestv, offB);
-                qn -= 32;
-                __syncwarp();
-              }
+            }
+            while (qn >= 32) {
+              __syncwarp();
+              drain_queue(qid, qw, qx, qn - 32, 32, temp, best, bestv, offB);
+              qn -= 32;
+              __syncwarp();
             }
           }
         }
@@ -1328,28 +748,18 @@ __global__ void __launch_bounds__(kThreads, 2) seg_kernel(const __grid_constant_
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ __align__(8) uint64_t full[kSlots], empty[kSlots], sq_full[kSQ], sq_empty[kSQ];
   __shared__ uint4 sq_rec[kSQ];
-  __shared__ unsigned long long red64[kConsWarps + 1];
-  __shared__ float redf[kConsWarps + 1];
-  __shared__ double redd[kConsWarps + 1];
   __shared__ uint32_t words[32];
-  __shared__ uint32_t segk[2 * kConsWarps];
   Smem sm;
   sm.ring4 = reinterpret_cast<uint4*>(dsm + kOffRing);
   sm.mask32 = reinterpret_cast<uint32_t*>(dsm + kOffMask);
   sm.pool = reinterpret_cast<uint32_t*>(dsm + kOffPool);
   sm.desc = reinterpret_cast<uint4*>(dsm + kOffDesc);
-  sm.fin_id = reinterpret_cast<uint32_t*>(dsm + kOffFin);
-  sm.fin_bits = reinterpret_cast<uint16_t*>(dsm + kOffFin + kFinCap * 4);
   sm.full = full;
   sm.empty = empty;
   sm.sq_full = sq_full;
   sm.sq_empty = sq_empty;
   sm.sq_rec = sq_rec;
-  sm.red64 = red64;
-  sm.redf = redf;
-  sm.redd = redd;
   sm.words = words;
-  sm.segk = segk;
 
   griddep_launch_dependents();
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1462,7 +872,7 @@ template <int FUSED>
 cudaError_t launch_mode(Params& p, void* scratch, uint32_t B, uint32_t V, cudaStream_t stream) {
   if (p.temp == 0.f) return launch<kModeGreedy, FUSED>(p, scratch, B, V, stream);
   if (p.top_p >= 1.f) return launch<kModeFull, FUSED>(p, scratch, B, V, stream);
-  return launch<kModeTopP, FUSED>(p, scratch, B, V, stream);
+  return cudaErrorInvalidValue;  // top-p rows take the per-row kernels (seg_usable)
 }
 
 }  // namespace seg
@@ -1471,12 +881,16 @@ cudaError_t launch_mode(Params& p, void* scratch, uint32_t B, uint32_t V, cudaSt
 // launch; every launch leaves it at zero).
 size_t seg_scratch_bytes(uint32_t B) { return seg::kCtlBytes + size_t(B) * seg::kRowStride; }
 
-// The segmented sampler takes bf16 rows of V % 8 == 0 logits at 16-byte
-// aligned addresses, up to kMaxNS x 4 chunks, without the optional outputs.
-bool seg_usable(int dtype, uint32_t V, const void* logits, float* probs, int inplace) {
+// The segmented sampler takes greedy rows and Gumbel-max over every allowed
+// token (top_p >= 1): bf16 rows of V % 8 == 0 logits at 16-byte aligned
+// addresses, up to kMaxNS x 4 chunks, without the optional outputs.  Top-p
+// rows (0 < top_p < 1) take the per-row kernels of kernel_sample.cu, measured
+// faster at every batch size tried (16 to 512 rows of 32000 to 151936 logits).
+bool seg_usable(int dtype, uint32_t V, const void* logits, float* probs, int inplace, float temp, float top_p) {
   const uint32_t nchunks = (V + seg::kChunk - 1) / seg::kChunk;
   return dtype == CG_BF16 && V % 8 == 0 && V > 0 && nchunks <= seg::kMaxNS * seg::kMaxSegChunks &&
-         (reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && probs == nullptr && inplace == 0;
+         (reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && probs == nullptr && inplace == 0 &&
+         (temp == 0.f || top_p >= 1.f);
 }
 
 // cg_mask_and_sample through the segmented sampler (the bitmask must have
