@@ -5,16 +5,25 @@ V = 128256 synthetic tokens, B = 256 rows, bf16 logits N(0, 2) with +4 on 5% of
 tokens, temperature 0.7, top-p 0.9.  Rows start in the start state; rows that
 finish or reach 2048 tokens are reset by accept.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--prefix P] [--impl ours|reference]
 
 Prints one JSON line.  ``value`` is constrained tokens/s with the step's inputs
-already resident in HBM: R pre-generated logit buffers whose total exceeds 4x
-the L2 size are used in rotation, so every step reads its logits from HBM.
+already resident in HBM, over a steady-state window: the timed steps come after
+an untimed prefix of P steps (default 300) and are named in ``config.window``;
+the first steps after the warm-up are timed apart (``fresh_start``).  R
+pre-generated logit buffers whose total exceeds 4x the L2 size are used in
+rotation, so every step reads its logits from HBM.  Beside the headline:
+``workloads`` (the four other synthetic workloads, each with its roofline
+fraction; mixed_eval_152k also as a decode loop through the host forced-token
+driver), ``bench_gap`` (the step against the same sampling with an all-ones
+mask), ``mask_cache_without_prefill`` (misses per step and step times on a
+context without prefill), the pushdown rows and speculative verification.
 ``e2e`` repeats the measurement through cg_step_host: every step's logits are
 copied from page-locked host memory (the copy of one step overlapping the
 previous step's kernel) and its sampled tokens copied back to host memory.
 ``--impl reference`` times the CPU oracle (the plain restatement the kernels
-are checked against) on a bounded sample of the same workload.
+are checked against) on a bounded sample of the same workload, on every host
+core; ``cpu_baseline`` gives that sample on one thread and on every core.
 """
 
 from __future__ import annotations
@@ -33,6 +42,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "constrained tokens/s and µs/step (mask+apply+sample) at V=128256, B=256"
 SAMPLE_SOURCES = ["grammar_constrained_decoding_gb300/csrc/kernel_sample.cu",
+                  "grammar_constrained_decoding_gb300/csrc/bf16_ops.cuh",
                   "grammar_constrained_decoding_gb300/csrc/device.cuh",
                   "grammar_constrained_decoding_gb300/csrc/row_ops.cuh"]
 
@@ -117,6 +127,44 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside)}
 
 
+def _parse_cpulist(txt: str) -> set:
+    cpus = set()
+    for part in txt.strip().split(","):
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        elif part:
+            cpus.add(int(part))
+    return cpus
+
+
+def _numa_bind(index: int) -> dict:
+    """Binds this process to the CPUs of the GPU's NUMA node when the system
+    reports one, so that the page-locked buffers allocated next are local to
+    the GPU's host link, and says what it found."""
+    info = {"gpu_numa_node": None, "bound_cpus": None}
+    try:
+        bus = subprocess.run(["nvidia-smi", f"--id={index}", "--query-gpu=pci.bus_id", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=30).stdout.strip()
+        dom, rest = bus.split(":", 1)
+        node = int(open(f"/sys/bus/pci/devices/{(dom[-4:] + ':' + rest).lower()}/numa_node").read())
+        info["gpu_numa_node"] = node
+        if node >= 0:
+            cpus = _parse_cpulist(open(f"/sys/devices/system/node/node{node}/cpulist").read())
+            if cpus:
+                os.sched_setaffinity(0, cpus)
+                info["bound_cpus"] = f"{min(cpus)}-{max(cpus)} ({len(cpus)} cpus)"
+    except Exception as e:  # no nvidia-smi, no sysfs entry: report and go on unbound
+        info["error"] = f"{type(e).__name__}: {e}"[:160]
+    try:
+        info["nodes_with_cpus"] = sorted(int(d[4:]) for d in os.listdir("/sys/devices/system/node")
+                                         if d.startswith("node") and d[4:].isdigit()
+                                         and open(f"/sys/devices/system/node/{d}/cpulist").read().strip())
+    except OSError:
+        pass
+    return info
+
+
 def _dist():
     from grammar_constrained_decoding_gb300.replicas import rank_info
     return rank_info()
@@ -184,6 +232,29 @@ def run_ours(args) -> dict | None:
     torch.cuda.synchronize()
     if ctx.status() != 0:
         raise RuntimeError("device status after warm-up")
+    applied = args.warmup   # steps applied to the rows' states so far
+
+    # fresh-start figure: the next F steps of trajectories that began in the
+    # start state, where most rows sit in cheap JSON-structure states
+    F = 20
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for i in range(applied, applied + F):
+        step(i, bufs[i % R])
+    f1.record(stream)
+    torch.cuda.synchronize()
+    fresh_us = f0.elapsed_time(f1) / F * 1e3
+    fresh_window = f"steps {applied}..{applied + F - 1}"
+    applied += F
+    # steady state: an untimed prefix before the timed window, so that the
+    # window sees the workload's own mix of row states (rows restart in the
+    # start state when they finish or reach the token cap)
+    for i in range(applied, applied + args.prefix):
+        step(i, bufs[i % R])
+    applied += args.prefix
+    torch.cuda.synchronize()
+    if ctx.status() != 0:
+        raise RuntimeError("device status after the prefix")
 
     # The timed steps run as CUDA graphs of G steps each (launch-bound host
     # code out of the way); each step of a graph keeps its own step index and
@@ -199,23 +270,29 @@ def run_ours(args) -> dict | None:
                 fn(i, bufs[i % R])
         return g
 
-    for i in range(args.warmup):       # the three-call path's buffers and scratch, before capture
+    for i in range(applied, applied + args.warmup):   # the three-call path's buffers and scratch, before capture
         three_calls(i, bufs[i % R])
+    applied += args.warmup
 
-    graphs, first = [], args.warmup
+    graphs, first = [], applied
     for n in plan:
         graphs.append(capture(first, n, step))
         first += n
-    sample_graphs, first = [], args.warmup
+    sample_graphs, first = [], applied
     for n in plan:
         sample_graphs.append(capture(first, n, three_calls))
         first += n
-    # one untimed replay of each graph set (first replays upload the graphs)
-    for g in graphs + sample_graphs:
+    # one untimed replay of the step graphs (first replays upload the graphs)
+    for g in graphs:
         g.replay()
     torch.cuda.synchronize()
     if ctx.status() != 0:
         raise RuntimeError("device status after graph warm-up")
+    applied += args.steps
+    window = (f"steps {applied}..{applied + args.steps - 1} of every row's trajectory from the start state "
+              f"(untimed before them: {args.warmup} warm-up, {F} fresh-start, {args.prefix} prefix, "
+              f"{args.warmup} three-call warm-up steps and one replay of the step graphs); rows restart in the "
+              f"start state when they finish or reach {b.max_tokens} tokens")
 
     sampler = ClockSampler(local) if rank == 0 else None
     time.sleep(0.25)
@@ -237,6 +314,8 @@ def run_ours(args) -> dict | None:
     if status != 0:
         raise RuntimeError(f"device status {status} in the timed region")
     # the same steps as three separate calls
+    for g in sample_graphs:
+        g.replay()
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     s0.record(stream)
@@ -294,6 +373,8 @@ def run_ours(args) -> dict | None:
     # frames on the same vocabulary, rows and logits, as the three calls
     # fill (pushdown) -> mask_and_sample -> accept (pushdown), in graphs
     pda_out = _bench_pushdown(args, cg, ctx, vocab, stream, bufs, R, B, V, W, cfg, seed)
+    gap = _bench_gap(ctx, stream, bufs, R, B, V, W, cfg, seed, G, ms / args.steps * 1e3)
+    cache = _bench_cache(cg, grammars, vocab, stream, bufs, R, B, cfg, seed, b, fresh_us)
 
     # host evaluators of the forced-token path, per call through the C ABI
     # (Python's call overhead included) on the pages' examples
@@ -311,6 +392,8 @@ def run_ours(args) -> dict | None:
     # ids copied back to host memory
     e2e_steps = min(args.steps, args.e2e_steps)
     nh = 2
+    cpus0 = os.sched_getaffinity(0)
+    numa = _numa_bind(local)   # page-locked buffers on the GPU's NUMA node, when it has one
     host_bufs = [bufs[i].cpu().pin_memory() for i in range(nh)]
     tok_host = torch.empty(B, dtype=torch.int32, pin_memory=True)
     ctx.step_host(states, host_bufs[0], cfg.temp, cfg.top_p, seed, 10**6, tok_host, states, flags, gid=gid,
@@ -328,6 +411,8 @@ def run_ours(args) -> dict | None:
     ctx.sync()
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    os.sched_setaffinity(0, cpus0)
+    workloads = None if args.no_workloads else _bench_workloads(cg, local, _peaks(), args.quick)
 
     if rank != 0:
         return None
@@ -360,12 +445,17 @@ def run_ours(args) -> dict | None:
                    "B": B, "V": V, "l2_policy": f"{R} rotated logit buffers, {R * step_bytes / 2**20:.0f} MiB "
                                                  f">= 4x L2 ({l2 / 2**20:.0f} MiB): every step reads HBM",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "mask_classes": info["n_classes"]},
+                   "mask_classes": info["n_classes"], "window": window},
         "gpu_launches": args.steps,
         "kernel_us": {"step (cg_step, one fused kernel)": round(per_step * 1e3, 3),
                       "step as three calls (fill_bitmask, mask_and_sample, accept)": round(three_ms * 1e3, 3),
                       "accept_many (B rows, drafts of 8 tokens from the next 8 steps)": round(am_us, 3)},
         "accept_many_mean_accepted": round(am_accepted, 3),
+        "fresh_start": {"us_per_step": round(fresh_us, 3), "window": fresh_window,
+                        "tokens_per_s": round(B / (fresh_us * 1e-6), 1)},
+        "bench_gap": gap,
+        "mask_cache_without_prefill": cache,
+        "workloads": workloads,
         "pushdown": pda_out,
         "host_eval_us_per_call": host_eval,
         "roofline": {"kernel": "stream_topp_kernel<1> (cg_step)", "bound": "hbm",
@@ -375,10 +465,235 @@ def run_ours(args) -> dict | None:
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "traffic": traffic["dram_bytes_per_launch"] if traffic else None},
         "e2e": {"value": round(B / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": step_bytes, "d2h_bytes_per_step": B * 4, "steps": e2e_steps},
+                "h2d_bytes_per_step": step_bytes, "d2h_bytes_per_step": B * 4, "steps": e2e_steps,
+                "h2d_gbs": round(step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "numa": numa},
         "clocks": clocks,
     }
     return out
+
+
+FORMATS = {"calc_tag": 0, "json_answer": 1, "strop_tag": 2}   # CG_RESULT_* of include/cg.h
+
+
+def _alg_bytes(B: int, V: int, esz: int) -> int:
+    """Algorithmic bytes of one step: every row's logits read once and its
+    bitmask words once (the per-unit figure 2V + 4W for bf16)."""
+    return B * (V * esz + ((V + 31) // 32) * 4)
+
+
+def _graph_us(stream, fn, first: int, n: int, reps: int = 1) -> float:
+    """Device time per step of n steps fn(i) captured in one CUDA graph (one
+    untimed replay first; the steps keep their own indices)."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+        for i in range(first, first + n):
+            fn(i)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    del g
+    return e0.elapsed_time(e1) / (n * reps) * 1e3
+
+
+def _bench_gap(ctx, stream, bufs, R, B, V, W, cfg, seed, n, step_us) -> dict:
+    """Enforcement overhead (usetacet.com/docs/grammar, "What it is worth": the
+    same calls with the automaton on and off): the constrained step against
+    the same sampling with the automaton off (an all-ones mask, no bitmask
+    fill, no accept)."""
+    import torch
+    ones = torch.full((B, W), -1, dtype=torch.int32, device="cuda")
+    if V % 32:
+        ones[:, W - 1] = (1 << (V % 32)) - 1
+    tok = torch.empty(B, dtype=torch.int32, device="cuda")
+
+    def f(i):
+        ctx.mask_and_sample(bufs[i % R], ones, cfg.temp, cfg.top_p, seed, i, tok)
+
+    for i in range(3):
+        f(i)
+    un_us = _graph_us(stream, f, 3, n)
+    return {"unconstrained_us_per_step": round(un_us, 3), "constrained_us_per_step": round(step_us, 3),
+            "overhead": round(step_us / un_us - 1.0, 4),
+            "unconstrained": "cg_mask_and_sample with an all-ones bitmask (no fill, no accept)",
+            "constrained": "cg_step (mask fill, masked sampling and accept), steady-state window"}
+
+
+def _bench_cache(cg, grammars, vocab, stream, bufs, R, B, cfg, seed, b, fresh_us, n=40) -> dict:
+    """The fused step on a context without prefill: every class mask is
+    computed by the first row that misses it (labs.miniml.ai "Evaluator aware
+    decoding", "Where XGrammar-2 could take this", on the token mask cache)."""
+    import torch
+    ctx = cg.Ctx(grammars, vocab, stream)
+    n_cls = ctx.info()["n_classes"]
+    states = torch.zeros(B, dtype=torch.int32, device="cuda").view(torch.uint32)
+    counts = torch.zeros(B, dtype=torch.int32, device="cuda").view(torch.uint32)
+    tok = torch.empty(B, dtype=torch.int32, device="cuda")
+    flags = torch.empty(B, dtype=torch.uint8, device="cuda")
+    us, misses, ready = [], [], ctx.cache_stats()["ready"]
+    for i in range(n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ctx.step(states, bufs[i % R], cfg.temp, cfg.top_p, seed, i, tok, states, flags, counts=counts,
+                 max_tokens=b.max_tokens)
+        e1.record(stream)
+        r = ctx.cache_stats()["ready"]   # synchronises the stream
+        us.append(e0.elapsed_time(e1) * 1e3)
+        misses.append(r - ready)
+        ready = r
+    if ctx.status() != 0:
+        raise RuntimeError("device status in the cache leg")
+    return {"n_classes": n_cls, "steps": n, "lookups_per_step": B,
+            "misses_per_step_first10": misses[:10], "misses_total": sum(misses), "classes_ready_after": ready,
+            "us_step0": round(us[0], 2), "us_per_step_1_9": round(sum(us[1:10]) / 9, 2),
+            "us_per_step_10_39": round(sum(us[10:40]) / 30, 2),
+            "with_prefill_us_per_step_fresh_start": round(fresh_us, 2),
+            "note": "steps from the start state on a fresh context (no cg_ctx_prefill), one CUDA-event pair "
+                    "per step; a miss is a class mask computed during that step"}
+
+
+def _mixed_loop(cg, ctx, vocab, stream, bufs, R, B, cfg, gid_np, gid, specs, max_tokens, prefix, n) -> dict:
+    """mixed_eval_152k as a decode loop with the host forced-token driver
+    (labs.miniml.ai "Evaluator aware decoding", "The core idea"): every step
+    the tokens and flags come back to the host, the driver evaluates the rows
+    that closed a span and the next step's forced tokens go back to the device
+    (the host round trip the pages' "Why isn't this in production APIs yet?"
+    names)."""
+    import numpy as np
+    import torch
+    rules = [(s.span_open, s.span_close, FORMATS[s.result_format]) if s.result_format else (b"", b"", -1)
+             for s in specs]
+    drv = cg.Driver(vocab, B, gid_np, rules)
+    states = torch.zeros(B, dtype=torch.int32, device="cuda").view(torch.uint32)
+    counts = torch.zeros(B, dtype=torch.int32, device="cuda").view(torch.uint32)
+    tok = torch.empty(B, dtype=torch.int32, device="cuda")
+    flags = torch.empty(B, dtype=torch.uint8, device="cuda")
+    forced_d = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+    tok_h = torch.empty(B, dtype=torch.int32, pin_memory=True)
+    flags_h = torch.empty(B, dtype=torch.uint8, pin_memory=True)
+    fnext_h = torch.full((B,), -1, dtype=torch.int32, pin_memory=True)
+    forced_used = np.full(B, -1, np.int32)
+    forced_next = np.full(B, -1, np.int32)
+    dev_us, host_us, wall_us, forced_rows, evals = [], [], [], [], []
+    for i in range(prefix + n):
+        forced_used[:] = forced_next
+        t0 = time.perf_counter()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ctx.step(states, bufs[i % R], cfg.temp, cfg.top_p, cfg.sample_seed, i, tok, states, flags, gid=gid,
+                 forced=forced_d, counts=counts, max_tokens=max_tokens)
+        e1.record(stream)
+        tok_h.copy_(tok, non_blocking=True)
+        flags_h.copy_(flags, non_blocking=True)
+        stream.synchronize()
+        t1 = time.perf_counter()
+        ne = drv.update(tok_h.numpy().view(np.uint32), flags_h.numpy(), forced_used, forced_next)
+        fnext_h.numpy()[:] = forced_next
+        forced_d.copy_(fnext_h, non_blocking=True)
+        t2 = time.perf_counter()
+        if i >= prefix:
+            dev_us.append(e0.elapsed_time(e1) * 1e3)
+            host_us.append((t2 - t1) * 1e6)
+            wall_us.append((t2 - t0) * 1e6)
+            forced_rows.append(int((forced_used >= 0).sum()))
+            evals.append(ne)
+    torch.cuda.synchronize()
+    if ctx.status() != 0:
+        raise RuntimeError("device status in the mixed decode loop")
+    m = lambda v: round(sum(v) / len(v), 3)
+    return {"steps": n, "after_prefix": prefix, "wall_us_per_step": m(wall_us), "device_step_us": m(dev_us),
+            "host_us_per_step (driver update + forced-token upload)": m(host_us),
+            "forced_rows_per_step": m(forced_rows), "injected_tokens_per_step": m(forced_rows),
+            "evaluations_per_step": m(evals), "tokens_per_s_wall": round(B / (m(wall_us) * 1e-6), 1),
+            "readback_bytes_per_step": B * 5, "upload_bytes_per_step": B * 4}
+
+
+def _bench_workloads(cg, local, peaks, quick: bool) -> dict:
+    """Per-workload steady-state step time, throughput and HBM roofline
+    fraction of the four workloads beside the headline one."""
+    import numpy as np
+    import torch
+    from workloads import CONFIGS, GRAMMARS, make_vocab
+    from workloads.logits import make_logits_device
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    out = {}
+    for name in ("tiny", "booking_32k", "reasoning_152k", "mixed_eval_152k"):
+        cfg = CONFIGS[name]
+        B, V = cfg.B, cfg.V
+        esz = 2 if cfg.dtype == "bf16" else 4
+        specs = [GRAMMARS[n] for n in cfg.grammars]
+        grammars = [cg.Grammar.compile(s.source, s.kind, cg.Bounds(s.bounds.ws_max, s.bounds.max_len_default,
+                                                                    s.bounds.depth_max, s.bounds.max_items_default,
+                                                                    s.bounds.max_tokens)) for s in specs]
+        vocab = cg.Vocab(make_vocab(cfg.vocab_kind, V, cfg.vocab_seed))
+        stream = torch.cuda.current_stream()
+        ctx = cg.Ctx(grammars, vocab, stream)
+        ctx.prefill()
+        R = max(2, -(-4 * l2 // (B * V * esz)))
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(cfg.logit_seed)
+        bufs = [make_logits_device(B, V, 0, cfg.sigma, cfg.boost, cfg.boost_frac, cfg.dtype, "cuda", gen)
+                for _ in range(R)]
+        gid_np = (np.arange(B) % len(specs)).astype(np.uint16)
+        gid = torch.as_tensor(gid_np.astype(np.int16)).cuda().view(torch.uint16) if len(specs) > 1 else None
+        if cfg.random_start:
+            live = grammars[0].live_states()
+            st = live[np.random.default_rng([cfg.logit_seed, 0x5747]).integers(0, len(live), B)].astype(np.uint32)
+        else:
+            st = np.zeros(B, np.uint32)
+        states = torch.from_numpy(st.view(np.int32)).cuda().view(torch.uint32)
+        counts = torch.zeros(B, dtype=torch.int32, device="cuda").view(torch.uint32)
+        tok = torch.empty(B, dtype=torch.int32, device="cuda")
+        flags = torch.empty(B, dtype=torch.uint8, device="cuda")
+        mt = specs[0].bounds.max_tokens
+
+        def step(i):
+            ctx.step(states, bufs[i % R], cfg.temp, cfg.top_p, cfg.sample_seed, i, tok, states, flags, gid=gid,
+                     counts=counts, max_tokens=mt)
+
+        prefix = 20 if quick else (50 if B * V > 10**8 else 100)
+        n = 20 if quick else 100
+        loop = None
+        if any(s.result_format for s in specs):
+            # evaluator grammars need the host driver's forced tokens every
+            # step: the step is timed inside that decode loop (CUDA events
+            # around each cg_step)
+            loop = _mixed_loop(cg, ctx, vocab, stream, bufs, R, B, cfg, gid_np, gid, specs, mt, prefix, n)
+            us = loop["device_step_us"]
+            window = f"steps {prefix}..{prefix + n - 1} of the decode loop (CUDA events around each cg_step)"
+        else:
+            for i in range(prefix):
+                step(i)
+            torch.cuda.synchronize()
+            us = _graph_us(stream, step, prefix, n)
+            window = (f"steps {prefix + n}..{prefix + 2 * n - 1} (after a {prefix}-step prefix and one untimed "
+                      f"graph replay)")
+        if ctx.status() != 0:
+            raise RuntimeError(f"device status in workload {name}")
+        ab = _alg_bytes(B, V, esz)
+        ach = ab / (us * 1e-6) / 1e9
+        if cfg.dtype != "bf16":
+            path = "three calls (fill_bitmask, per-row f32 sampler, accept)"
+        elif cfg.temp > 0 and cfg.top_p < 1:
+            path = "stream_topp_kernel<1> (cg_step, per-row fused top-p)"
+        else:
+            path = "seg_kernel (cg_step, segmented fused " + ("greedy" if cfg.temp == 0 else "Gumbel-max") + ")"
+        res = {"B": B, "V": V, "dtype": cfg.dtype, "temp": cfg.temp, "top_p": cfg.top_p, "path": path,
+               "us_per_step": round(us, 3), "tokens_per_s": round(B / (us * 1e-6), 1), "window": window,
+               "roofline": {"bound": "hbm", "algorithmic_bytes_per_step": ab, "achieved": round(ach, 1),
+                            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4)}}
+        if loop:
+            res["decode_loop_with_host_driver"] = loop
+        out[name] = res
+        del ctx, bufs
+        torch.cuda.empty_cache()
+    return out
+
 
 
 def _bench_pushdown(args, cg, ctx, vocab, stream, bufs, R, B, V, W, cfg, seed) -> dict:
@@ -536,8 +851,7 @@ class OracleBench:
     """The oracle stepping rows of the workload, each on its own trajectory from
     the start state (the logits of a row-step are generated outside the timing)."""
 
-    def __init__(self, cfg_name: str, rows: int):
-        import numpy as np  # noqa: F401
+    def __init__(self, cfg_name: str, row_ids):
         from oracle.dfa import compile_grammar
         from oracle.driver import OracleRun, Row
         from workloads import CONFIGS, GRAMMARS, make_vocab
@@ -546,8 +860,8 @@ class OracleBench:
         dfas = [compile_grammar(s.kind, s.source, s.bounds) for s in specs]
         toks = make_vocab(self.cfg.vocab_kind, self.cfg.V, self.cfg.vocab_seed)
         self.run = OracleRun(dfas, specs, toks, specs[0].bounds.max_tokens)
-        self.rows = [Row(b, b % len(specs)) for b in range(rows)]
-        self.step_of = [0] * rows
+        self.rows = [Row(b, b % len(specs)) for b in row_ids]
+        self.step_of = [0] * len(self.rows)
         self.spent = 0.0
         self.done = 0
 
@@ -565,39 +879,76 @@ class OracleBench:
         self.done += 1
 
 
-def cpu_baseline(cfg_name: str, budget_s: float = 15.0) -> dict:
-    ob = OracleBench(cfg_name, 4)
-    k = 0
-    while ob.spent < budget_s:
-        ob.row_step(k % 4)
+ORACLE_ROWS = 4   # rows a worker steps round robin
+
+
+def _oracle_worker(job):
+    """One worker of the CPU sample: rows [first, first + ORACLE_ROWS) of the
+    batch, stepped round robin for budget_s seconds of oracle work (or exactly
+    n_steps row-steps), after `warm` untimed row-steps."""
+    cfg_name, first, budget_s, n_steps, warm = job
+    ob = OracleBench(cfg_name, range(first, first + ORACLE_ROWS))
+    for k in range(warm):
+        ob.row_step(k % ORACLE_ROWS)
+    ob.spent, ob.done = 0.0, 0
+    t0 = time.perf_counter()
+    k = warm
+    while (ob.spent < budget_s) if n_steps is None else (ob.done < n_steps):
+        ob.row_step(k % ORACLE_ROWS)
         k += 1
-    return {"value": round(ob.done / ob.spent, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{ob.done} row-steps of {cfg_name} (4 rows from the start state, round robin), "
-                      f"float64 numpy, one thread, {ob.spent:.1f} s of CPU work (logit generation excluded)"}
+    return ob.done, ob.spent, time.perf_counter() - t0
+
+
+def _oracle_pool(cfg_name: str, workers: int, budget_s, n_steps, warm):
+    """The CPU sample on `workers` processes (spawned: no fork after CUDA), each
+    on its own rows; returns [(row-steps, oracle seconds, wall seconds)]."""
+    import multiprocessing as mp
+    jobs = [(cfg_name, ORACLE_ROWS * w, budget_s, n_steps, warm) for w in range(workers)]
+    if workers == 1:
+        return [_oracle_worker(jobs[0])]
+    with mp.get_context("spawn").Pool(workers) as pool:
+        return pool.map(_oracle_worker, jobs)
+
+
+def cpu_baseline(cfg_name: str, budget_s: float = 10.0) -> dict:
+    """The oracle as it stands on the host cores: one thread, and one process
+    per core the process may use (os.sched_getaffinity), each on 4 rows of its
+    own from the start state."""
+    cores = len(os.sched_getaffinity(0))
+    one = _oracle_pool(cfg_name, 1, budget_s, None, 1)[0]
+    allc = _oracle_pool(cfg_name, cores, budget_s, None, 1)
+    v1 = one[0] / one[1]
+    va = sum(d / w for d, _, w in allc)
+    return {"value": round(va, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "nproc": os.cpu_count(),
+            "sample": f"{cfg_name}: {cores} processes x {ORACLE_ROWS} rows from the start state, round robin, "
+                      f"{budget_s:.0f} s of oracle work each ({sum(d for d, _, _ in allc)} row-steps), float64 "
+                      f"numpy; logit generation excluded",
+            "single_thread": {"value": round(v1, 2), "cores": 1,
+                              "sample": f"{one[0]} row-steps of rows 0..{ORACLE_ROWS - 1}, {one[1]:.1f} s"}}
 
 
 def run_reference(args) -> dict | None:
     world, rank, _ = _dist()
     if rank != 0:
         return None
-    ob = OracleBench(args.config, 4)
-    for i in range(args.warmup):
-        ob.row_step(i % 4)
-    ob.spent, ob.done = 0.0, 0
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        ob.row_step(i % 4)
-    wall = time.perf_counter() - t0
-    value = round(ob.done / ob.spent, 2)
-    cfg = ob.cfg
+    from workloads import CONFIGS
+    cfg = CONFIGS[args.config]
+    cores = len(os.sched_getaffinity(0))
+    # one step = one row-step on each of `cores` processes (the cpu_baseline sample)
+    res = _oracle_pool(args.config, cores, None, args.steps, args.warmup)
+    done = sum(d for d, _, _ in res)
+    wall = max(w for _, _, w in res)
+    value = round(done / wall, 2)
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ob.spent / max(1, args.steps) * 1e3, 3),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall / max(1, args.steps) * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded vocabulary, logits and grammar; no model)",
-            "config": {"workload": f"{cfg.name}: V={cfg.V}, B={cfg.B}; each step is a bounded sample: "
-                                   f"one row of the batch (4 rows round robin)", "B": cfg.B, "V": cfg.V},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{ob.done} row-steps, one row per step, {wall:.1f} s wall"},
+            "config": {"workload": f"{cfg.name}: V={cfg.V}, B={cfg.B}; each step is a bounded sample: one row-step "
+                                   f"on each of {cores} processes ({ORACLE_ROWS} rows each, round robin)",
+                       "B": cfg.B, "V": cfg.V},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{done} row-steps on {cores} processes, {wall:.1f} s wall"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -610,6 +961,9 @@ def main():
     ap.add_argument("--config", default="booking_128k")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefix", type=int, default=300, help="untimed steps before the timed window")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the other four workloads")
+    ap.add_argument("--quick", action="store_true", help="short legs (smoke runs)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")

@@ -186,11 +186,12 @@ class Ctx:
         L.check("cg_ctx_prefill", L.lib().cg_ctx_prefill(self._h))
 
     def cache_stats(self) -> dict:
-        """Mask-class lookups and class masks computed by the fused step's miss
-        path since the context was created (synchronises the stream)."""
-        lk, cm = C.c_uint64(), C.c_uint64()
-        L.check("cg_ctx_cache_stats", L.lib().cg_ctx_cache_stats(self._h, C.byref(lk), C.byref(cm)))
-        return {"lookups": lk.value, "computed": cm.value}
+        """Mask-cache counters (synchronises the stream): lookups and class masks
+        computed by the segmented fused step's pre-pass, and the class masks in
+        the cache now by any path ("ready", of info()["n_classes"])."""
+        lk, cm, rd = C.c_uint64(), C.c_uint64(), C.c_uint32()
+        L.check("cg_ctx_cache_stats", L.lib().cg_ctx_cache_stats(self._h, C.byref(lk), C.byref(cm), C.byref(rd)))
+        return {"lookups": lk.value, "computed": cm.value, "ready": rd.value}
 
     def fill_bitmask(self, states, bitmask, gid=None, forced=None) -> None:
         B = states.shape[0]

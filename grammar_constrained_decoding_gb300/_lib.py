@@ -59,7 +59,8 @@ SIGNATURES = {
                               C.POINTER(C.c_uint32)]),
     "cg_ctx_status": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint32)]),
     "cg_ctx_prefill": (C.c_int, [C.c_void_p]),
-    "cg_ctx_cache_stats": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64)]),
+    "cg_ctx_cache_stats": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64),
+                                     C.POINTER(C.c_uint32)]),
     "cg_fill_bitmask": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_uint32, C.c_void_p]),
     "cg_mask_and_sample": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_uint32, C.c_uint32, C.c_void_p,
                                      C.c_float, C.c_float, C.c_uint64, C.c_uint32, C.c_void_p, C.c_void_p,

@@ -351,7 +351,7 @@ int cg_ctx_create(const cg_grammar* const* g, uint32_t n_g, const cg_vocab* v, v
 void cg_ctx_destroy(cg_ctx* c) {
   if (!c) return;
   {
-    cgk::DeviceGuard dg(c->device);
+    cgk::DeviceGuard dg(c->device, "cg_ctx_destroy");
     cudaStreamSynchronize(c->stream);
     if (c->copy_stream) cudaStreamSynchronize(c->copy_stream);
     release(c);
@@ -370,7 +370,7 @@ int cg_ctx_info(const cg_ctx* c, uint32_t* n_classes, uint64_t* cache_bytes, uin
 
 int cg_ctx_status(cg_ctx* c, uint32_t* dev_code) {
   if (!c) return CG_E_ARG;
-  cgk::DeviceGuard dg(c->device);
+  cgk::DeviceGuard dg(c->device, "cg_ctx_status");
   if (!dg.ok) return CG_E_CUDA;
   uint32_t code = 0;
   if (cudaStreamSynchronize(c->stream) != cudaSuccess) return CG_E_CUDA;
@@ -384,21 +384,28 @@ int cg_ctx_status(cg_ctx* c, uint32_t* dev_code) {
   return code ? CG_E_DEVICE : CG_OK;
 }
 
-int cg_ctx_cache_stats(cg_ctx* c, uint64_t* lookups, uint64_t* computed) {
+int cg_ctx_cache_stats(cg_ctx* c, uint64_t* lookups, uint64_t* computed, uint32_t* ready) {
   if (!c) return CG_E_ARG;
-  cgk::DeviceGuard dg(c->device);
+  cgk::DeviceGuard dg(c->device, "cg_ctx_cache_stats");
   if (!dg.ok) return CG_E_CUDA;
   unsigned long long v[2] = {0ull, 0ull};
   if (cudaStreamSynchronize(c->stream) != cudaSuccess) return CG_E_CUDA;
   if (cudaMemcpy(v, c->cache_stats, 16, cudaMemcpyDeviceToHost) != cudaSuccess) return CG_E_CUDA;
   if (lookups) *lookups = v[0];
   if (computed) *computed = v[1];
+  if (ready) {
+    std::vector<uint32_t> st(c->t.n_classes);
+    if (!st.empty() &&
+        cudaMemcpy(st.data(), c->t.cache_state, st.size() * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+      return CG_E_CUDA;
+    *ready = uint32_t(std::count(st.begin(), st.end(), 2u));  // kStateReady
+  }
   return CG_OK;
 }
 
 int cg_ctx_prefill(cg_ctx* c) {
   if (!c) return CG_E_ARG;
-  cgk::DeviceGuard dg(c->device);
+  cgk::DeviceGuard dg(c->device, "cg_ctx_prefill");
   if (!dg.ok) return CG_E_CUDA;
   if (cgk::launch_prefill(c->t, c->class_rep, c->class_gid, c->stream) != cudaSuccess) return CG_E_CUDA;
   c->cache_complete = true;  // later kernels on the stream see every class ready
@@ -408,7 +415,7 @@ int cg_ctx_prefill(cg_ctx* c) {
 int cg_fill_bitmask(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const int32_t* d_forced, uint32_t B,
                     uint32_t* d_bitmask) {
   if (!c || (B && (!d_states || !d_bitmask))) return CG_E_ARG;
-  cgk::DeviceGuard dg(c->device);
+  cgk::DeviceGuard dg(c->device, "cg_fill_bitmask");
   if (!dg.ok) return CG_E_CUDA;
   return cgk::launch_fill_bitmask(c->t, d_states, d_gid, d_forced, B, d_bitmask, c->cache_complete, c->stream) ==
                  cudaSuccess
@@ -421,7 +428,7 @@ int cg_mask_and_sample(cg_ctx* c, void* d_logits, int dtype, uint32_t B, uint32_
                        uint32_t flags) {
   if (!sample_args_ok(c, d_logits, dtype, B, V, d_bitmask, temp, top_p, d_out_tok, flags)) return CG_E_ARG;
   if (B == 0) return CG_OK;
-  cgk::DeviceGuard dg(c->device);
+  cgk::DeviceGuard dg(c->device, "cg_mask_and_sample");
   if (!dg.ok) return CG_E_CUDA;
   const int inplace = (flags & CG_SAMPLE_INPLACE) ? 1 : 0;
   const bool seg_path =
@@ -442,7 +449,7 @@ int cg_mask_and_sample_noalloc(cg_ctx* c, void* d_logits, int dtype, uint32_t B,
       cgk::seg_scratch_bytes(B) > cgk::kNoAllocSegBytes)
     return CG_E_LIMIT;
   if (B == 0) return CG_OK;
-  cgk::DeviceGuard dg(c->device);
+  cgk::DeviceGuard dg(c->device, "cg_mask_and_sample_noalloc");
   if (!dg.ok) return CG_E_CUDA;
   cudaError_t e = cudaSuccess;
   unsigned char* scratch = static_cast<unsigned char*>(noalloc_scratch(&e));
@@ -463,7 +470,7 @@ int cg_accept(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const 
               uint8_t* d_out_flags) {
   if (!c || (B && (!d_states || !d_toks || !d_out_states || !d_out_flags))) return CG_E_ARG;
   if (d_counts && max_tokens == 0) return CG_E_ARG;
-  cgk::DeviceGuard dg(c->device);
+  cgk::DeviceGuard dg(c->device, "cg_accept");
   if (!dg.ok) return CG_E_CUDA;
   return cgk::launch_accept(c->t, d_states, d_gid, d_toks, d_forced, B, d_counts, max_tokens, d_out_states,
                             d_out_flags, c->stream) == cudaSuccess
@@ -480,7 +487,7 @@ int cg_step(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const in
   if (V != c->t.V || !(temp >= 0.f) || temp == INFINITY || !(top_p == top_p)) return CG_E_ARG;
   if (d_counts && max_tokens == 0) return CG_E_ARG;
   if (B == 0) return CG_OK;
-  cgk::DeviceGuard dg(c->device);
+  cgk::DeviceGuard dg(c->device, "cg_step");
   if (!dg.ok) return CG_E_CUDA;
   int rc;
   if (cgk::step_fusable(dtype, V, c->t.W, temp, top_p, d_logits)) {
@@ -524,7 +531,7 @@ int cg_step(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const in
 
 int cg_ctx_sync(cg_ctx* c) {
   if (!c) return CG_E_ARG;
-  cgk::DeviceGuard dg(c->device);
+  cgk::DeviceGuard dg(c->device, "cg_ctx_sync");
   if (!dg.ok) return CG_E_CUDA;
   return cudaStreamSynchronize(c->stream) == cudaSuccess ? CG_OK : CG_E_CUDA;
 }
@@ -538,7 +545,7 @@ int cg_step_host(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, con
   if (V != c->t.V || !(temp >= 0.f) || temp == INFINITY || !(top_p == top_p)) return CG_E_ARG;
   if (d_counts && max_tokens == 0) return CG_E_ARG;
   if (B == 0) return CG_OK;
-  cgk::DeviceGuard dg(c->device);
+  cgk::DeviceGuard dg(c->device, "cg_step_host");
   if (!dg.ok) return CG_E_CUDA;
   if (!c->copy_stream) {
     if (cudaStreamCreateWithFlags(&c->copy_stream, cudaStreamNonBlocking) != cudaSuccess) return CG_E_CUDA;
@@ -582,7 +589,7 @@ int cg_accept_many(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, c
   if (!c || (B && (!d_states || !d_draft || !d_draft_len || !d_out_states || !d_out_n || !d_out_flags))) return CG_E_ARG;
   if (B && K == 0) return CG_E_ARG;
   if (d_counts && max_tokens == 0) return CG_E_ARG;
-  cgk::DeviceGuard dg(c->device);
+  cgk::DeviceGuard dg(c->device, "cg_accept_many");
   if (!dg.ok) return CG_E_CUDA;
   return cgk::launch_accept_many(c->t, d_states, d_gid, d_draft, d_draft_len, d_forced, B, K, d_counts, max_tokens,
                                  d_out_states, d_out_n, d_out_flags, d_out_path, c->stream) == cudaSuccess
@@ -592,7 +599,7 @@ int cg_accept_many(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, c
 
 int cg_self_test_wait_timeout(cg_ctx* c) {
   if (!c) return CG_E_ARG;
-  cgk::DeviceGuard dg(c->device);
+  cgk::DeviceGuard dg(c->device, "cg_self_test_wait_timeout");
   if (!dg.ok) return CG_E_CUDA;
   return cgk::launch_wait_timeout_self_test(c->t.status, c->stream) == cudaSuccess ? CG_OK : CG_E_CUDA;
 }

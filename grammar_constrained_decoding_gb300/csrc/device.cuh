@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <utility>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/cg.h"
 
@@ -91,11 +92,14 @@ constexpr size_t kNoAllocSegBytes = size_t(64) << 10;
 
 // Makes a device current for the duration of a call and puts the caller's
 // back: every launch, allocation and symbol lookup of a library call then
-// happens on the device its context's tables live on.
+// happens on the device its context's tables live on.  The call is also an
+// NVTX range named after the entry point (free unless a profiler is
+// attached), so that a timeline attributes host time to library calls.
 struct DeviceGuard {
   int prev = -1;
   bool ok = true;
-  explicit DeviceGuard(int dev) {
+  explicit DeviceGuard(int dev, const char* call) {
+    nvtxRangePushA(call);
     int cur = 0;
     if (cudaGetDevice(&cur) != cudaSuccess) {
       ok = false;
@@ -111,6 +115,7 @@ struct DeviceGuard {
   }
   ~DeviceGuard() {
     if (prev >= 0) cudaSetDevice(prev);
+    nvtxRangePop();
   }
   DeviceGuard(const DeviceGuard&) = delete;
   DeviceGuard& operator=(const DeviceGuard&) = delete;

@@ -329,7 +329,7 @@ extern "C" {
 int cg_pda_create(cg_ctx* c, const cg_vocab* v, const cg_pda_grammar* g, cg_pda** out) {
   if (!c || !v || !g || !out) return CG_E_ARG;
   *out = nullptr;
-  cgk::DeviceGuard dg(cgk::ctx_device(c));
+  cgk::DeviceGuard dg(cgk::ctx_device(c), "cg_pda_create");
   if (!dg.ok) return CG_E_CUDA;
   const cgk::CtxView view = cgk::ctx_view(c);
   if (v->V != view.t.V) return CG_E_ARG;
@@ -440,7 +440,7 @@ int cg_pda_create(cg_ctx* c, const cg_vocab* v, const cg_pda_grammar* g, cg_pda*
 void cg_pda_destroy(cg_pda* p) {
   if (!p) return;
   {
-    cgk::DeviceGuard dg(cgk::ctx_device(p->ctx));
+    cgk::DeviceGuard dg(cgk::ctx_device(p->ctx), "cg_pda_destroy");
     cudaStreamSynchronize(p->stream);
     pda_release(p);
   }
@@ -461,7 +461,7 @@ int cg_pda_fill_bitmask(cg_pda* p, const uint32_t* d_cfg, uint32_t B, const int3
                         uint32_t* d_bitmask) {
   if (!p || (B && (!d_cfg || !d_bitmask))) return CG_E_ARG;
   if (B == 0) return CG_OK;
-  cgk::DeviceGuard dg(cgk::ctx_device(p->ctx));
+  cgk::DeviceGuard dg(cgk::ctx_device(p->ctx), "cg_pda_fill_bitmask");
   if (!dg.ok) return CG_E_CUDA;
   const size_t smem = pda_fill_smem(p->d, p->t.W);
   return cgk::launch_dependent(cgk::pda_fill_kernel, dim3(B), dim3(cgk::kPdaFillThreads), smem, p->stream, p->d,
@@ -474,7 +474,7 @@ int cg_pda_accept(cg_pda* p, uint32_t* d_cfg, uint32_t B, const uint32_t* d_toks
                   uint32_t* d_counts, uint32_t max_tokens, uint8_t* d_out_flags) {
   if (!p || (B && (!d_cfg || !d_toks || !d_out_flags))) return CG_E_ARG;
   if (B == 0) return CG_OK;
-  cgk::DeviceGuard dg(cgk::ctx_device(p->ctx));
+  cgk::DeviceGuard dg(cgk::ctx_device(p->ctx), "cg_pda_accept");
   if (!dg.ok) return CG_E_CUDA;
   const uint32_t grid = (B + cgk::kPdaAcceptThreads - 1) / cgk::kPdaAcceptThreads;
   return cgk::launch_dependent(cgk::pda_accept_kernel, dim3(grid), dim3(cgk::kPdaAcceptThreads),
@@ -491,7 +491,7 @@ int cg_pda_accept_many(cg_pda* p, uint32_t* d_cfg, uint32_t B, const uint32_t* d
   if (!p || (B && (!d_cfg || !d_draft || !d_draft_len || !d_out_n || !d_out_flags || K == 0))) return CG_E_ARG;
   if (d_counts && max_tokens == 0) return CG_E_ARG;
   if (B == 0) return CG_OK;
-  cgk::DeviceGuard dg(cgk::ctx_device(p->ctx));
+  cgk::DeviceGuard dg(cgk::ctx_device(p->ctx), "cg_pda_accept_many");
   if (!dg.ok) return CG_E_CUDA;
   const uint32_t grid = (B + cgk::kPdaAcceptThreads - 1) / cgk::kPdaAcceptThreads;
   return cgk::launch_dependent(cgk::pda_accept_many_kernel, dim3(grid), dim3(cgk::kPdaAcceptThreads),
@@ -509,7 +509,7 @@ int cg_pda_step(cg_pda* p, uint32_t* d_cfg, uint32_t B, void* d_logits, int dtyp
   if (V != p->t.V || !(temp >= 0.f) || temp == INFINITY || !(top_p == top_p)) return CG_E_ARG;
   if (d_counts && max_tokens == 0) return CG_E_ARG;
   if (B == 0) return CG_OK;
-  cgk::DeviceGuard dg(cgk::ctx_device(p->ctx));
+  cgk::DeviceGuard dg(cgk::ctx_device(p->ctx), "cg_pda_step");
   if (!dg.ok) return CG_E_CUDA;
   void* scratch = nullptr;
   int rc = cgk::ctx_sample_scratch(p->ctx, cgk::sample_scratch_bytes(B, V), &scratch);
@@ -545,7 +545,7 @@ int cg_pda_accept_fill(cg_pda* p, uint32_t* d_cfg, uint32_t B, const uint32_t* d
                        uint32_t* d_bitmask) {
   if (!p || (B && (!d_cfg || !d_toks || !d_out_flags || !d_bitmask))) return CG_E_ARG;
   if (B == 0) return CG_OK;
-  cgk::DeviceGuard dg(cgk::ctx_device(p->ctx));
+  cgk::DeviceGuard dg(cgk::ctx_device(p->ctx), "cg_pda_accept_fill");
   if (!dg.ok) return CG_E_CUDA;
   return cgk::launch_dependent(cgk::pda_accept_fill_kernel, dim3(B), dim3(cgk::kPdaFillThreads),
                                pda_fill_smem(p->d, p->t.W), p->stream, p->d, p->t, d_cfg, d_toks, d_forced, d_counts,

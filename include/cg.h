@@ -210,15 +210,18 @@ int cg_ctx_status(cg_ctx* c, uint32_t* dev_code);
  * Errors: CG_E_ARG, CG_E_CUDA. */
 int cg_ctx_prefill(cg_ctx* c);
 
-/* Mask-cache behaviour of the fused step (cg_step) on a context without
- * cg_ctx_prefill: before each step a pass over the rows computes the class
- * masks not yet in the cache (labs.miniml.ai "Evaluator aware decoding",
- * "Where XGrammar-2 could take this", on the token mask cache).
- *  lookups  : rows of automaton states that looked their class up (hits + misses)
- *  computed : class masks computed because a row missed them
+/* Mask-cache behaviour on a context without cg_ctx_prefill (labs.miniml.ai
+ * "Evaluator aware decoding", "Where XGrammar-2 could take this", on the token
+ * mask cache).  A class mask is computed by the first row that misses it, on
+ * whichever path the row takes (fill_bitmask, the fused steps, or the
+ * pre-pass of the segmented fused step).
+ *  lookups  : class lookups counted by the segmented fused step's pre-pass
+ *             (greedy and top_p >= 1 steps; hits + misses)
+ *  computed : class masks the pre-pass computed because a row missed them
+ *  ready    : class masks in the cache now, by any path (of n_classes)
  * Counted since the context was created; synchronises the context's stream.
- * Either output may be NULL.  Errors: CG_E_ARG, CG_E_CUDA. */
-int cg_ctx_cache_stats(cg_ctx* c, uint64_t* lookups, uint64_t* computed);
+ * Any output may be NULL.  Errors: CG_E_ARG, CG_E_CUDA. */
+int cg_ctx_cache_stats(cg_ctx* c, uint64_t* lookups, uint64_t* computed, uint32_t* ready);
 
 /* Step 1 -- which tokens may follow each row's state (usetacet.com/docs/grammar,
  * "The guarantee"; a mask depends on the automaton state alone and is known
