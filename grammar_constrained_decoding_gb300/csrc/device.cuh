@@ -142,7 +142,14 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
+// A bulk copy wants both addresses 16-byte aligned and a size that is a
+// multiple of 16: one that breaks the rule is not issued (the waiter's bounded
+// wait then runs out and records CG_DEV_TIMEOUT) instead of faulting the GPU.
+__device__ __forceinline__ bool bulk_ok(const void* dst, const void* src, uint32_t bytes) {
+  return ((smem_addr(dst) | static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src)) | bytes) & 15u) == 0;
+}
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  if (!bulk_ok(dst, src, bytes)) return;
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_addr(dst)),

@@ -319,7 +319,6 @@ constexpr uint32_t kNucCap = (kRing - kHistBytes) / 6;          // packed nucleu
 // of thousands of tokens, no dominant ones) can reach past 9.
 constexpr float kMarginZ = 8.5f;
 constexpr float kNoRef = -1e30f;                                // finite reference before any allowed logit
-constexpr uint32_t kMaxCols = 512;                              // symbol columns a grammar can have
 constexpr uint32_t kWinRowsMax = 512;                           // states in the accept's table window
 constexpr uint32_t kWinBytesMax = 16384;                        // shared memory for that window
 constexpr uint32_t kSlots = 16;                                 // list entries per thread after the stream

@@ -203,6 +203,7 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
 // should not push the mask cache and the scratch out of L2
 __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
                                               uint64_t pol) {
+  if (!bulk_ok(dst, src, bytes)) return;  // (as bulk_g2s)
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
           "r"(smem_addr(dst)),

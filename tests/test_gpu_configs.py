@@ -119,3 +119,53 @@ def test_config_full_size(name):
         states = g_ns.copy()
     if name == "mixed_eval_152k":
         assert forced_rows > 0, "no forced-only state was drawn"
+
+
+@pytest.mark.parametrize("name", ["booking_128k", "reasoning_152k"])
+def test_config_every_row(name):
+    """One cg_step at full size with every row checked against the oracle:
+    its bitmask bit for bit (the oracle's scalar mask, computed once per
+    distinct state), its id against the oracle's sampler on the same logits,
+    and its next state and flags against the oracle's accept."""
+    import torch
+    from grammar_constrained_decoding_gb300 import Ctx, Vocab
+    cfg = CONFIGS[name]
+    V, B, n_g = cfg.V, cfg.B, len(cfg.grammars)
+    W = (V + 31) // 32
+    toks = vocab(cfg.vocab_kind, V, cfg.vocab_seed)
+    vm = VocabMatrix(toks)
+    dfas = [oracle_dfa(n) for n in cfg.grammars]
+    ctx = Ctx([product_grammar(n) for n in cfg.grammars], Vocab(toks))
+    rng = np.random.default_rng(zlib.crc32(name.encode()) ^ 0x5A5A)
+    states = _start(cfg, dfas, rng)
+    step = 1
+    vals, raw = make_logits(V, range(B), step, cfg.logit_seed, cfg.sigma, cfg.boost, cfg.boost_frac, cfg.dtype)
+    x = torch.from_numpy(raw.view(np.int16)).cuda().view(torch.bfloat16)
+    forced = _forced(cfg, dfas, states)
+    bm = empty((B, W), torch.int32)
+    tok = empty((B,), torch.int32)
+    ns, fl = empty((B,), torch.int32).view(torch.uint32), empty((B,), torch.uint8)
+    ctx.step(u32(states), x, cfg.temp, cfg.top_p, cfg.sample_seed, step, tok, ns, fl,
+             forced=torch.from_numpy(forced).cuda(), bitmask=bm)
+    assert ctx.status() == 0
+    g_bm, g_tok = host(bm).view(np.uint32), host(tok).view(np.uint32)
+    g_ns, g_fl = host(ns).view(np.uint32), host(fl)
+    masks = {}
+    for b in range(B):
+        d, s, t = dfas[b % n_g], int(states[b]), int(g_tok[b])
+        if forced[b] >= 0:
+            allowed = onehot_mask(V, int(forced[b]))
+        elif s == 0xFFFFFFFF:
+            allowed = np.zeros(V, bool)
+        else:
+            if (b % n_g, s) not in masks:
+                masks[(b % n_g, s)] = token_mask(d, vm, s)
+            allowed = masks[(b % n_g, s)]
+        bits = np.zeros(W * 32, bool)
+        bits[:V] = allowed
+        want_bm = (bits.reshape(W, 32).astype(np.uint64) << np.arange(32, dtype=np.uint64)).sum(1)
+        assert np.array_equal(g_bm[b], want_bm.astype(np.uint32)), (b, s)
+        res = sample_row(vals[b].astype(np.float64), allowed, cfg.temp, cfg.top_p, cfg.sample_seed, b, step)
+        assert same_token(t, res), (b, t, res.tok, res.gap, res.margin)
+        want_s, want_f = accept(d, -1 if s == 0xFFFFFFFF else s, t, toks, forced[b] >= 0)
+        assert g_ns[b] == (0xFFFFFFFF if want_s == DEAD else want_s) and g_fl[b] == want_f, (b, s, t)

@@ -520,3 +520,40 @@ def test_other_grammar_shapes_match_the_oracle(source, D):
             for b in done:
                 st[b] = 0
     assert max_level >= min(D, 3)
+
+
+def test_fused_pda_step_matches_the_oracle():
+    """cg_pda_step (mask, sample and accept in one fused kernel per row)
+    checked against the oracle directly, row by row and step by step: the
+    bitmask it writes, the sampled id and the accept flags."""
+    import torch
+    D, V, B, steps = 8, 32000, 64, 16
+    temp, top_p, seed = 0.7, 0.9, 13
+    toks = vocab("bpe", V)
+    orc = OracleRows(JSON_NESTED, D, toks)
+    ctx, pda = _pda(JSON_NESTED, D, V)
+    W = (V + 31) // 32
+    cfg = _fresh(B, D)
+    bm = empty((B, W), torch.int32)
+    tok = empty((B,), torch.int32)
+    flags = empty((B,), torch.uint8)
+    st = [0] * B
+    for step in range(steps):
+        vals, x = logits_rows(V, range(B), step, 5, 2.0, 4.0, 0.05, "bf16")
+        pda.step(cfg, x, temp, top_p, seed, step, tok, flags, bitmask=bm)
+        assert ctx.status() == 0
+        g_tok, g_bm, g_fl = host(tok).view(np.uint32), host(bm).view(np.uint32), host(flags)
+        for b in range(B):
+            want = orc.mask(st[b])
+            assert np.array_equal(g_bm[b], want), (step, b)
+            allowed = np.unpackbits(want.view(np.uint8), bitorder="little")[:V].astype(bool)
+            res = sample_row(vals[b], allowed, temp, top_p, seed, b, step)
+            assert same_token(int(g_tok[b]), res), (step, b)
+            s, f = accept(orc.dfa, st[b], int(g_tok[b]), toks, False) if g_tok[b] != NO_TOKEN else (st[b], 8)
+            assert g_fl[b] == f, (step, b)
+            st[b] = s
+        done = [b for b in range(B) if g_fl[b] & FLAG_DONE]
+        if done:  # finished rows start again
+            cfg.view(torch.int32)[done] = 0
+            for b in done:
+                st[b] = 0

@@ -156,3 +156,40 @@ def test_step_host_matches_step(temp, top_p):
         assert np.array_equal(htok[k].numpy(), want[k][0]), k
         assert np.array_equal(host(ns_b[k]), want[k][1]), k
         assert np.array_equal(host(fl_b[k]), want[k][2]), k
+
+
+@pytest.mark.parametrize("temp,top_p", [(0.7, 0.9), (0.7, 1.0)])
+def test_step_host_matches_the_oracle(temp, top_p):
+    """cg_step_host checked against the oracle directly: every row's id (on
+    the same logits and the oracle's mask of its state), next state and flags,
+    over three steps from random live states."""
+    import torch
+    from oracle.dfa import DEAD
+    from oracle.step import VocabMatrix, accept, sample_row, token_mask
+    from tests.gpu_helpers import same_token
+    from tests.oracle_cache import oracle_dfa, vocab
+    name, V, B, steps = "booking", 32000, 32, 3
+    toks = vocab("bpe", V)
+    vm = VocabMatrix(toks)
+    d = oracle_dfa(name)
+    ctx = make_ctx((name,), "bpe", V)
+    states = _start_states((name,), B, np.random.default_rng(21))
+    st = u32(states)
+    for k in range(steps):
+        vals, raw = make_logits(V, list(range(B)), k, 1234, 2.0, 4.0, 0.05, "bf16")
+        hx = torch.from_numpy(raw.view(np.int16)).view(torch.bfloat16).pin_memory()
+        htok = torch.full((B,), -1, dtype=torch.int32).pin_memory()
+        ns, fl = empty((B,), torch.int32).view(torch.uint32), empty((B,), torch.uint8)
+        ctx.step_host(st, hx, temp, top_p, 5, k, htok, ns, fl)
+        ctx.sync()
+        assert ctx.status() == 0
+        g_tok, g_ns, g_fl = htok.numpy().view(np.uint32), host(ns).view(np.uint32), host(fl)
+        for b in range(B):
+            s, t = int(states[b]), int(g_tok[b])
+            allowed = token_mask(d, vm, s) if s != 0xFFFFFFFF else np.zeros(V, bool)
+            res = sample_row(vals[b].astype(np.float64), allowed, temp, top_p, 5, b, k)
+            assert same_token(t, res), (k, b, t, res.tok, res.gap, res.margin)
+            want_s, want_f = accept(d, -1 if s == 0xFFFFFFFF else s, t, toks, False)
+            assert g_ns[b] == (0xFFFFFFFF if want_s == DEAD else want_s) and g_fl[b] == want_f, (k, b)
+        states = g_ns.copy()
+        st = ns

@@ -58,3 +58,36 @@ def test_noalloc_rejects_oversized_batch():
     torch.cuda.synchronize()
     assert (host(tok) == -7).all()        # nothing was launched
     assert ctx.status() == 0
+
+
+@pytest.mark.parametrize("temp,top_p", [(0.7, 0.9), (2.0, 0.999), (0.7, 1.0), (0.0, 1.0)])
+def test_noalloc_full_batch_matches_oracle(temp, top_p):
+    """CG_NOALLOC_MAX_ROWS rows on the fixed array, without the optional
+    outputs: greedy and top_p >= 1 rows take the segmented sampler (its part of
+    the fixed array), top-p rows the per-row kernels; at temperature 2 and
+    top_p 0.999 the nucleus of the dense rows reaches past the candidate margin,
+    so those rows take the general path.  Every row's id agrees with the
+    oracle's (within the pages' tolerance for sampled ids) and with the
+    allocating entry point, over two consecutive calls."""
+    import torch
+    from grammar_constrained_decoding_gb300._lib import CG_NOALLOC_MAX_ROWS
+    from oracle.step import sample_row, unpack_bitmask
+    from tests.gpu_helpers import same_token
+    V, B = 128256, CG_NOALLOC_MAX_ROWS
+    ctx = make_ctx(("calc_call",), "bpe", V)
+    xt, bm = _inputs(V, B, 13)
+    x = xt.float().cpu().numpy().astype(np.float64)
+    masks = [unpack_bitmask(row, V) for row in host(bm).view(np.uint32)]
+    for step in (5, 6):
+        tok_a, tok_b = empty((B,), torch.int32), empty((B,), torch.int32)
+        ctx.mask_and_sample(xt, bm, temp, top_p, 7, step, tok_a)
+        ctx.mask_and_sample_noalloc(xt, bm, temp, top_p, 7, step, tok_b)
+        assert ctx.status() == 0
+        got = host(tok_b).view(np.uint32)
+        assert np.array_equal(host(tok_a).view(np.uint32), got), step
+        for b in range(B):
+            res = sample_row(x[b], masks[b], temp, top_p, 7, b, step)
+            if temp == 0.0:
+                assert int(got[b]) == res.tok, (step, b, int(got[b]), res.tok)
+            else:
+                assert same_token(int(got[b]), res), (step, b, int(got[b]), res.tok, res.gap, res.margin)
