@@ -333,6 +333,16 @@ def run_ours(args) -> dict | None:
         sampler.stop()
     del graphs, sample_graphs
 
+    if args.step_only:   # a profiling run: the timed steps only
+        if rank != 0:
+            return None
+        per_step = ms / args.steps
+        return {"metric": METRIC, "value": round(replicas.job_throughput(B * args.steps, world, ms), 1),
+                "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(per_step, 5), "us_per_step": round(per_step * 1e3, 3),
+                "higher_is_better": True, "dtype": cfg.dtype, "config": {"workload": cfg.name, "window": window},
+                "note": "--step-only: the timed cg_step graphs and the three-call graphs; no other leg ran"}
+
     # speculative verification (cg_accept_many): drafts of K = 8 tokens taken
     # from the workload's own next 8 steps, verified from the states before them
     K = 8
@@ -964,6 +974,7 @@ def main():
     ap.add_argument("--prefix", type=int, default=300, help="untimed steps before the timed window")
     ap.add_argument("--no-workloads", action="store_true", help="skip the other four workloads")
     ap.add_argument("--quick", action="store_true", help="short legs (smoke runs)")
+    ap.add_argument("--step-only", action="store_true", help="profiling runs: the timed steps, no other leg")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
@@ -971,7 +982,7 @@ def main():
         out = run_reference(args)
     else:
         out = run_ours(args)
-        if out is not None:
+        if out is not None and not args.step_only:
             out["cpu_baseline"] = None if args.no_cpu_baseline else cpu_baseline(args.config)
     if out is not None:
         print(json.dumps(out), flush=True)
