@@ -30,6 +30,13 @@
  *    row whose automaton has failed.
  *  - Bitmask layout: row-major u32 [B][W], W = ceil(V / 32); token t is bit
  *    (t & 31) of word (t >> 5); pad bits beyond V are zero.
+ *  - Device: a context belongs to the device current at cg_ctx_create.  Every
+ *    call on a context (or on a cg_pda built on it) makes that device current
+ *    for its duration and puts the caller's back, so its allocations, launches
+ *    and symbol lookups happen there whatever device the calling thread has
+ *    current; device pointers passed in must live on that device.  Each such
+ *    call is also an NVTX range named after the call (nothing is recorded
+ *    unless a profiler is attached).
  */
 #ifndef CG_H
 #define CG_H
@@ -313,17 +320,23 @@ int cg_ctx_sync(cg_ctx* c);
  *  - It is for callers that must not allocate device memory while decoding:
  *    cudaMalloc/cudaFree synchronise the device and can fail once a server has
  *    planned all of HBM (e.g. for its KV cache) at start-up.
- *  - Scratch: a fixed array inside the library, CG_NOALLOC_MAX_ROWS x 8192 x 6
- *    bytes (3 MiB), one per device, holding the per-row candidate lists.
+ *  - Scratch: a fixed array inside the library, one per device: the per-row
+ *    kernels' candidate lists (CG_NOALLOC_MAX_ROWS x 8192 x 6 bytes, 3 MiB),
+ *    then the segmented kernel's counters and per-row pairs (64 KiB; the
+ *    greedy and top_p >= 1 calls without probabilities take that kernel).
  *    B > CG_NOALLOC_MAX_ROWS returns CG_E_LIMIT without launching anything.
- *  - Nothing in the scratch has to start at zero: the kernel writes every list
- *    entry before it reads it.
+ *  - The list part need not start at zero (every entry is written before it is
+ *    read); the segmented part is cleared on the context's stream before each
+ *    launch that uses it.
  *  - Every call on a device uses the same array, so calls that may overlap on
  *    the device (other streams, other contexts, other host threads) race on it;
  *    the caller must serialise them (one stream at a time).
- *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress; CG_E_CUDA if that fails); make that first call
- *    before capturing any stream. */
+ *  - The context's device is made current for the call (as for every entry
+ *    point), so the array is the one on the context's device.  The first call
+ *    on a device looks up its address (cudaGetSymbolAddress; CG_E_CUDA if that
+ *    fails) and keeps it; make that first call before capturing any stream, and
+ *    do not call it again on a device after cudaDeviceReset (the kept address
+ *    is then stale). */
 #define CG_NOALLOC_MAX_ROWS 64u
 int cg_mask_and_sample_noalloc(cg_ctx* c, void* d_logits, int dtype, uint32_t B, uint32_t V,
                                const uint32_t* d_bitmask, float temp, float top_p, uint64_t seed,

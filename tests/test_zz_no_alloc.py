@@ -64,11 +64,11 @@ def test_noalloc_rejects_oversized_batch():
 def test_noalloc_full_batch_matches_oracle(temp, top_p):
     """CG_NOALLOC_MAX_ROWS rows on the fixed array, without the optional
     outputs: greedy and top_p >= 1 rows take the segmented sampler (its part of
-    the fixed array), top-p rows the per-row kernels; at temperature 2 and
-    top_p 0.999 the nucleus of the dense rows reaches past the candidate margin,
-    so those rows take the general path.  Every row's id agrees with the
-    oracle's (within the pages' tolerance for sampled ids) and with the
-    allocating entry point, over two consecutive calls."""
+    the fixed array), top-p rows the per-row kernels (temperature 2 with
+    top_p 0.999 flattens the dense rows: their nuclei reach deep, towards or
+    past the candidate margin).  Every row's id agrees with the oracle's
+    (within the pages' tolerance for sampled ids) and with the allocating
+    entry point, over two consecutive calls."""
     import torch
     from grammar_constrained_decoding_gb300._lib import CG_NOALLOC_MAX_ROWS
     from oracle.step import sample_row, unpack_bitmask
