@@ -11,14 +11,14 @@
 // lowest id on ties.
 //
 // Work decomposition.  Each row is cut into segments of up to four 4096-logit
-// chunks; a persistent grid (two CTAs per SM) takes segments from a work
+// chunks; a persistent grid (three CTAs per SM) takes segments from a work
 // counter in segment-major order (segment s of every row before segment
 // s + 1, so that a row's best score so far is mostly known before its later
 // segments are read), and the bytes each SM streams differ by at most a
 // segment.  A CTA has three roles.  The producer warp resolves each segment's
 // mask source (the caller's bitmask, or in the fused step the row's mask class
 // in the mask cache) ahead of time and streams the segment's logits and mask
-// words into an 8-slot shared-memory ring with bulk asynchronous copies.
+// words into a 6-slot shared-memory ring with bulk asynchronous copies.
 // Eight consumer warps take each chunk 16 logits per thread (two 8-logit
 // groups).  The service warp counts each row's finished segments (a fence and
 // an atomic per segment, off the consumers' path).  Once the stream is done,
@@ -66,7 +66,7 @@ constexpr uint32_t kChunkBytes = kChunk * 2;               // 8 KiB
 constexpr uint32_t kChunkWords = kChunk / 32;              // mask words per slot
 constexpr uint32_t kGroups = kChunk / 8;                   // 8-logit groups per slot
 constexpr uint32_t kMaxSegChunks = 4;
-constexpr uint32_t kSlots = 8;                             // two segments of four chunks in flight
+constexpr uint32_t kSlots = 6;                             // a segment and a half of four chunks in flight
 constexpr uint32_t kMaxNS = 64;                            // segments per row
 constexpr uint32_t kSQ = 16;                               // records queued for the service warp (> kSlots)
 constexpr uint32_t kQ = 160;                               // queued exact scores per consumer warp (full)
@@ -80,7 +80,7 @@ constexpr uint32_t kOffPool = kOffMask + kSlots * kChunkWords * 4;
 constexpr uint32_t kPoolBytes = kConsWarps * kQ * 10;      // exact-score queues (full)
 constexpr uint32_t kOffDesc = kOffPool + kPoolBytes;
 constexpr uint32_t kSmem = kOffDesc + kSlots * 16;
-static_assert(kSmem <= 111 * 1024, "two CTAs a multiprocessor");
+static_assert(kSmem <= 74 * 1024, "three CTAs a multiprocessor");
 
 enum Mode { kModeGreedy = 0, kModeFull = 2 };
 // kinds of ring descriptors and service records
@@ -546,7 +546,6 @@ __device__ void consume(const Params& p, const Smem& sm) {
   const float temp = p.temp;
   const float c = (MODE == kModeGreedy) ? 0.f : 1.4426950408889634f / temp;
   const uint32_t g0 = warp * 64 + lane, g1 = g0 + 32;
-  const uint32_t lt = (1u << lane) - 1u;
   const uint4 kNeg4 = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
   uint32_t q = 0;     // ring slots taken
   uint32_t nrec = 0;  // records sent to the service warp
@@ -651,44 +650,57 @@ __device__ void consume(const Params& p, const Smem& sm) {
             }
           }
         }
-#pragma unroll 1
+#pragma unroll
         for (uint32_t h = 0; h < 2; ++h) {
           const uint4 v = h ? v1 : v0;
           const uint32_t mb = h ? mb1 : mb0;
           const uint32_t t0 = ck * kChunk + (h ? g1 : g0) * 8;
-#pragma unroll 1
+#pragma unroll
           for (uint32_t half = 0; half < 2; ++half) {
             const uint32_t nib = (mb >> (4 * half)) & 15u;
-            uint4 blk = make_uint4(0u, 0u, 0u, 0u);
-            if (nib) blk = philox_q(p, phr, (t0 >> 2) + half);
+            if (!__any_sync(0xFFFFFFFFu, nib != 0u)) continue;  // four tokens a lane, masked out for the whole warp
+            const uint4 blk = philox_q(p, phr, (t0 >> 2) + half);
             const uint32_t wa = half ? v.z : v.x, wb = half ? v.w : v.y;
+            // the token's score can beat bestv only if 2^23 exp(z - bestv)
+            // (slightly enlarged) exceeds 2^23 - 1 - (w >> 9), i.e. the bound
+            // -ln(1 - u) of its noise reaches bestv - z: one bit a token
+            uint32_t pm = 0;
 #pragma unroll
             for (uint32_t e = 0; e < 4; ++e) {
               const uint32_t wd = e < 2 ? wa : wb;
               const float x = (e & 1u) ? hi_f(wd) : lo_f(wd);
               const uint32_t w = e == 0 ? blk.x : e == 1 ? blk.y : e == 2 ? blk.z : blk.w;
-              // the token's score can beat bestv only if 2^23 exp(z - bestv)
-              // (slightly enlarged) exceeds 2^23 - 1 - (w >> 9), i.e. the
-              // bound -ln(1 - u) of its noise reaches bestv - z
               const float tq = ex2(fmaf(x, c, offB)) * 1.0001f;
               const float vv = __uint_as_float((w >> 9) ^ 0x4B7FFFFFu) - 8388608.0f;
-              const bool pass = ((nib >> e) & 1u) && vv < tq;
-              const unsigned bal = __ballot_sync(0xFFFFFFFFu, pass);
-              if (bal) {
-                const uint32_t pos = qn + __popc(bal & lt);
-                if (pass) {
-                  qid[pos] = t0 + 4 * half + e;
-                  qw[pos] = w;
-                  qx[pos] = uint16_t((e & 1u) ? (wd >> 16) : (wd & 0xFFFFu));
-                }
-                qn += __popc(bal);
-              }
+              if (((nib >> e) & 1u) && vv < tq) pm |= 1u << e;
             }
-            while (qn >= 32) {
-              __syncwarp();
-              drain_queue(qid, qw, qx, qn - 32, 32, temp, best, bestv, offB);
-              qn -= 32;
-              __syncwarp();
+            if (__any_sync(0xFFFFFFFFu, pm != 0u)) {
+              // queue the passing tokens (at most 4 a lane: qn stays below kQ)
+              const uint32_t n = __popc(pm);
+              uint32_t inc = n;
+#pragma unroll
+              for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+                if (lane >= uint32_t(o)) inc += y;
+              }
+              uint32_t pos = qn + inc - n;
+#pragma unroll
+              for (uint32_t e = 0; e < 4; ++e) {
+                if ((pm >> e) & 1u) {
+                  const uint32_t wd = e < 2 ? wa : wb;
+                  qid[pos] = t0 + 4 * half + e;
+                  qw[pos] = e == 0 ? blk.x : e == 1 ? blk.y : e == 2 ? blk.z : blk.w;
+                  qx[pos] = uint16_t((e & 1u) ? (wd >> 16) : (wd & 0xFFFFu));
+                  ++pos;
+                }
+              }
+              qn += __shfl_sync(0xFFFFFFFFu, inc, 31);
+              while (qn >= 32) {
+                __syncwarp();
+                drain_queue(qid, qw, qx, qn - 32, 32, temp, best, bestv, offB);
+                qn -= 32;
+                __syncwarp();
+              }
             }
           }
         }
@@ -745,7 +757,7 @@ __device__ void consume(const Params& p, const Smem& sm) {
 }
 
 template <int MODE, int FUSED>
-__global__ void __launch_bounds__(kThreads, 2) seg_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kThreads, 3) seg_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ __align__(8) uint64_t full[kSlots], empty[kSlots], sq_full[kSQ], sq_empty[kSQ];
   __shared__ uint4 sq_rec[kSQ];
