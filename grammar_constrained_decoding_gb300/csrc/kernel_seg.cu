@@ -650,7 +650,7 @@ __device__ void consume(const Params& p, const Smem& sm) {
             }
           }
         }
-#pragma unroll
+#pragma unroll 1
         for (uint32_t h = 0; h < 2; ++h) {
           const uint4 v = h ? v1 : v0;
           const uint32_t mb = h ? mb1 : mb0;
