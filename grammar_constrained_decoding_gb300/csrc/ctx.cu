@@ -305,7 +305,9 @@ int cg_ctx_create(const cg_grammar* const* g, uint32_t n_g, const cg_vocab* v, v
   c->cache_bytes = uint64_t(n_classes) * Wc * 4;
   if ((e = cudaMalloc(&d_cache, std::max<uint64_t>(c->cache_bytes, 16))) != cudaSuccess) { release(c); delete c; return CG_E_CUDA; }
   c->allocations.push_back(d_cache);
-  if ((e = cudaMalloc(&d_cstate, size_t(n_classes) * 4 + 16)) != cudaSuccess) { release(c); delete c; return CG_E_CUDA; }
+  // per class: state, then the miss pre-pass's claimed and finished splits
+  const size_t cls_words = size_t(n_classes) + 4;
+  if ((e = cudaMalloc(&d_cstate, cls_words * 3 * 4)) != cudaSuccess) { release(c); delete c; return CG_E_CUDA; }
   c->allocations.push_back(d_cstate);
   if ((e = cudaMalloc(&d_status, 16)) != cudaSuccess) { release(c); delete c; return CG_E_CUDA; }
   c->allocations.push_back(d_status);
@@ -313,7 +315,9 @@ int cg_ctx_create(const cg_grammar* const* g, uint32_t n_g, const cg_vocab* v, v
   if ((e = cudaMalloc(&d_stats, 16)) != cudaSuccess) { release(c); delete c; return CG_E_CUDA; }
   c->allocations.push_back(d_stats);
   c->cache_stats = d_stats;
-  e = cudaMemsetAsync(d_cstate, 0, size_t(n_classes) * 4 + 16, c->stream);
+  e = cudaMemsetAsync(d_cstate, 0, cls_words * 3 * 4, c->stream);
+  // the miss pre-pass ORs its splits' bits into class rows: they start at zero
+  if (e == cudaSuccess) e = cudaMemsetAsync(d_cache, 0, std::max<uint64_t>(c->cache_bytes, 16), c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(d_status, 0, 16, c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(d_stats, 0, 16, c->stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
@@ -327,6 +331,8 @@ int cg_ctx_create(const cg_grammar* const* g, uint32_t n_g, const cg_vocab* v, v
   t.class_of = d_class;
   t.cache = d_cache;
   t.cache_state = d_cstate;
+  t.cache_claim = d_cstate + cls_words;
+  t.cache_done = d_cstate + 2 * cls_words;
   t.n_classes = n_classes;
   t.V = V;
   t.W = W;
@@ -417,6 +423,10 @@ int cg_fill_bitmask(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, 
   if (!c || (B && (!d_states || !d_bitmask))) return CG_E_ARG;
   cgk::DeviceGuard dg(c->device, "cg_fill_bitmask");
   if (!dg.ok) return CG_E_CUDA;
+  // without prefill, the classes the rows miss first (each split over many blocks)
+  if (!c->cache_complete &&
+      cgk::launch_cache_fill(c->t, d_states, d_gid, d_forced, B, c->cache_stats, c->stream) != cudaSuccess)
+    return CG_E_CUDA;
   return cgk::launch_fill_bitmask(c->t, d_states, d_gid, d_forced, B, d_bitmask, c->cache_complete, c->stream) ==
                  cudaSuccess
              ? CG_OK
@@ -491,9 +501,13 @@ int cg_step(cg_ctx* c, const uint32_t* d_states, const uint16_t* d_gid, const in
   if (!dg.ok) return CG_E_CUDA;
   int rc;
   if (cgk::step_fusable(dtype, V, c->t.W, temp, top_p, d_logits)) {
-    // top-p: one per-row kernel (mask, sample and accept in one launch)
+    // top-p: one per-row kernel (mask, sample and accept in one launch), after
+    // the classes the rows miss when the cache is not complete
     if ((rc = grow(c, &c->sample_scratch, &c->sample_scratch_bytes, cgk::sample_scratch_bytes(B, V))) != CG_OK)
       return rc;
+    if (!c->cache_complete &&
+        cgk::launch_cache_fill(c->t, d_states, d_gid, d_forced, B, c->cache_stats, c->stream) != cudaSuccess)
+      return CG_E_CUDA;
     return cgk::launch_step(c->t, d_states, d_gid, d_forced, B, d_logits, V, temp, top_p, seed, step, d_counts,
                             max_tokens, d_bitmask, d_out_tok, d_out_states, d_out_flags, c->sample_scratch,
                             c->grammars.data(), c->cache_complete, c->stream) == cudaSuccess

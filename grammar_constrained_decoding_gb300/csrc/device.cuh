@@ -53,6 +53,8 @@ struct Tables {
   const uint32_t* class_of;    // mask class per state (all grammars, global ids)
   uint32_t* cache;             // [n_classes][Wc] allowed-token bitmask per class (words W..Wc unused)
   uint32_t* cache_state;       // per class: 0 empty, 1 being filled, 2 ready
+  uint32_t* cache_claim;       // per class: the miss pre-pass's splits claimed (bit per split)
+  uint32_t* cache_done;        // per class: the miss pre-pass's splits finished
   uint32_t n_classes;
   uint32_t V, W, max_len;
   uint32_t Wc;                 // row stride of the mask cache: W rounded up to 4 words (16-byte aligned rows)

@@ -50,17 +50,18 @@ __device__ __forceinline__ int row_mask_mode(const Tables& t, uint32_t g, int32_
   return row_mask_mode_of(t.n_g, t.V, g, f, s, n_states, sflags, err);
 }
 
-// Walk all tokens from state s of grammar g with threads tid = 0..nthreads-1;
-// sets allowed bits in smask[W] (zeroed by the caller).  Each thread takes a
-// contiguous run of the vocabulary in trie (lexicographic) order and resumes
-// each token's walk from the state reached after the prefix it shares with the
-// previous token, so shared prefixes are walked once.
-__device__ inline void walk_tokens(const Tables& t, const DevGrammar& gd, const uint16_t* scol, uint32_t s,
-                                   uint32_t* smask, uint32_t tid, uint32_t nthreads) {
-  const uint32_t V = t.V;
-  const uint32_t per = (V + nthreads - 1) / nthreads;
-  const uint32_t i0 = tid * per;
-  const uint32_t i1 = min(V, i0 + per);
+// Walk the tokens at positions [lo, hi) of the trie (lexicographic) order from
+// state s of grammar g with threads tid = 0..nthreads-1; sets allowed bits in
+// smask[W] (zeroed by the caller).  Each thread takes a contiguous run of
+// positions and resumes each token's walk from the state reached after the
+// prefix it shares with the previous token, so shared prefixes are walked
+// once.  walk_tokens: the whole vocabulary.
+__device__ inline void walk_tokens_range(const Tables& t, const DevGrammar& gd, const uint16_t* scol, uint32_t s,
+                                         uint32_t* smask, uint32_t lo, uint32_t hi, uint32_t tid,
+                                         uint32_t nthreads) {
+  const uint32_t per = (hi - lo + nthreads - 1) / nthreads;
+  const uint32_t i0 = lo + tid * per;
+  const uint32_t i1 = min(hi, i0 + per);
   const uint32_t* table = t.table + gd.table_off;
   const uint32_t ncols = gd.n_cols;
   uint32_t stack[65];
@@ -87,6 +88,11 @@ __device__ inline void walk_tokens(const Tables& t, const DevGrammar& gd, const 
       atomicOr(smask + (id >> 5), 1u << (id & 31));
     }
   }
+}
+
+__device__ inline void walk_tokens(const Tables& t, const DevGrammar& gd, const uint16_t* scol, uint32_t s,
+                                   uint32_t* smask, uint32_t tid, uint32_t nthreads) {
+  walk_tokens_range(t, gd, scol, s, smask, 0u, t.V, tid, nthreads);
 }
 
 constexpr uint32_t kPrefetch = 16;  // token bytes whose columns are loaded up front

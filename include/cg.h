@@ -219,11 +219,10 @@ int cg_ctx_prefill(cg_ctx* c);
 
 /* Mask-cache behaviour on a context without cg_ctx_prefill (labs.miniml.ai
  * "Evaluator aware decoding", "Where XGrammar-2 could take this", on the token
- * mask cache).  A class mask is computed by the first row that misses it, on
- * whichever path the row takes (fill_bitmask, the fused steps, or the
- * pre-pass of the segmented fused step).
- *  lookups  : class lookups counted by the segmented fused step's pre-pass
- *             (greedy and top_p >= 1 steps; hits + misses)
+ * mask cache).  On such a context cg_fill_bitmask and cg_step first run a
+ * miss pre-pass: every class mask a row needs and the cache lacks is computed
+ * by 32 blocks sharing its walk, so the step that follows finds it ready.
+ *  lookups  : rows that looked their class up in the pre-pass (hits + misses)
  *  computed : class masks the pre-pass computed because a row missed them
  *  ready    : class masks in the cache now, by any path (of n_classes)
  * Counted since the context was created; synchronises the context's stream.
