@@ -458,7 +458,9 @@ int cg_driver_update(cg_driver* d, const uint32_t* h_toks, const uint8_t* h_flag
     if (h_forced_used && h_forced_used[b] >= 0 && tok == uint32_t(h_forced_used[b]) && !q.empty()) q.pop_front();
     if (tok != CG_NO_TOKEN) {
       if (tok >= v->V) return CG_E_ARG;
-      text.append(reinterpret_cast<const char*>(v->bytes.data() + v->off[tok]), v->off[tok + 1] - v->off[tok]);
+      // only a row whose grammar evaluates spans needs its text
+      if (d->rules[d->gid[b]].fmt >= 0)
+        text.append(reinterpret_cast<const char*>(v->bytes.data() + v->off[tok]), v->off[tok + 1] - v->off[tok]);
     }
     if (fl & (CG_FLAG_DONE | CG_FLAG_CAPPED)) {
       text.clear();
