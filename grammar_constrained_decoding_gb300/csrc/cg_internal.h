@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <deque>
 #include <string>
+#include <string_view>
 #include <unordered_map>
 #include <vector>
 
@@ -29,7 +30,9 @@ struct cg_vocab {
   std::vector<uint8_t> lcp;
   std::vector<uint8_t> sorted_bytes;
   std::vector<uint32_t> sorted_off;
-  std::unordered_map<std::string, uint32_t> lowest_id;  // token string -> lowest id
+  // token string (a view into `bytes`) -> lowest id with that string
+  std::unordered_map<std::string_view, uint32_t> lowest_id;
+  uint64_t len_mask[256] = {};      // bit L-1: some token of L bytes starts with this byte
 };
 
 struct cg_driver {

@@ -266,9 +266,11 @@ int cg_vocab_create(const uint8_t* bytes, const uint32_t* off, uint32_t V, cg_vo
         v->lcp[i] = uint8_t(k);
       }
     }
+    v->lowest_id.reserve(V);
     for (uint32_t t = 0; t < V; ++t) {
-      std::string key(reinterpret_cast<const char*>(base + off[t]), off[t + 1] - off[t]);
-      v->lowest_id.emplace(key, t);  // first insertion = lowest id
+      const uint32_t len = off[t + 1] - off[t];
+      v->lowest_id.emplace(std::string_view(reinterpret_cast<const char*>(base + off[t]), len), t);  // first = lowest id
+      v->len_mask[base[off[t]]] |= uint64_t(1) << (len - 1);
     }
     *out = v;
     return CG_OK;
@@ -284,10 +286,14 @@ int cg_tokenize_greedy(const cg_vocab* v, const uint8_t* text, size_t n, uint32_
   if (!v || (!text && n) || !n_out) return CG_E_ARG;
   size_t i = 0, k = 0;
   while (i < n) {
-    size_t L = std::min<size_t>(v->max_len, n - i);
+    // candidate lengths: those of the tokens that start with this byte, longest first
+    uint64_t lens = v->len_mask[text[i]];
+    if (n - i < 64) lens &= (uint64_t(1) << (n - i)) - 1u;
     bool found = false;
-    for (; L > 0; --L) {
-      auto it = v->lowest_id.find(std::string(reinterpret_cast<const char*>(text + i), L));
+    while (lens) {
+      const size_t L = 64 - size_t(__builtin_clzll(lens));
+      lens &= ~(uint64_t(1) << (L - 1));
+      auto it = v->lowest_id.find(std::string_view(reinterpret_cast<const char*>(text + i), L));
       if (it != v->lowest_id.end()) {
         if (out && k < cap) out[k] = it->second;
         ++k;
