@@ -206,7 +206,13 @@ void cg_ctx_destroy(cg_ctx* c);
 int cg_ctx_info(const cg_ctx* c, uint32_t* n_classes, uint64_t* cache_bytes, uint32_t* V, uint32_t* W);
 
 /* Synchronise the context's stream, return CG_OK or CG_E_DEVICE, and move the
- * first recorded CG_DEV_* code into *dev_code (may be NULL), clearing it. */
+ * first recorded CG_DEV_* code into *dev_code (may be NULL), clearing it.
+ * CG_DEV_TIMEOUT from a sampling or step call (not from
+ * cg_self_test_wait_timeout, which has no copy in flight) means a block gave
+ * up on a bounded wait; its own last wait for the copies it had issued is
+ * bounded too, so a copy may still have landed in shared memory after the
+ * block exited.  The rows it served got CG_NO_TOKEN; destroy the context and
+ * create a new one before trusting further results. */
 int cg_ctx_status(cg_ctx* c, uint32_t* dev_code);
 
 /* Compute the bitmask of every mask class now (one CTA per class) instead of
