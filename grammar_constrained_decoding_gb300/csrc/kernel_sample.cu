@@ -357,7 +357,9 @@ __device__ __forceinline__ void issue_chunk(unsigned char* ring, uint64_t* full,
   const uint32_t slot = k % kStages;
   const uint32_t bytes = min(kChunkElems, V - k * kChunkElems) * 2;
   mbar_expect_tx(full + slot, bytes);
-  bulk_g2s(ring + size_t(slot) * kChunkBytes, row + size_t(k) * kChunkBytes, bytes, full + slot);
+  // the logits are read once: evict them first, keep the mask cache in L2
+  bulk_g2s_hint(ring + size_t(slot) * kChunkBytes, row + size_t(k) * kChunkBytes, bytes, full + slot,
+                evict_first_policy());
 }
 
 // One warp turns staged groups [top - n, top) into candidates: lane l takes

@@ -194,22 +194,6 @@ __device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long l
   return v;
 }
 __device__ __forceinline__ uint32_t ld_volatile_s(const uint32_t* p) { return *reinterpret_cast<const volatile uint32_t*>(p); }
-__device__ __forceinline__ uint64_t evict_first_policy() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-// bulk copy with an L2 eviction hint: the logits are read once per step and
-// should not push the mask cache and the scratch out of L2
-__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                              uint64_t pol) {
-  if (!bulk_ok(dst, src, bytes)) return;  // (as bulk_g2s)
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
-          "r"(smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
-      : "memory");
-}
 
 __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
 #pragma unroll
